@@ -1,0 +1,355 @@
+/*
+ * CPU oracle for the routed MoE expert-layer forward.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or
+ * call this file; only the tests, the smoke check and the benchmark's CPU
+ * baseline leg do.  It shares no code, header, table or helper with the CUDA
+ * library: every step below is written out plainly, in the order the
+ * documentation pages state it, with no blocking, fusion or reordering.
+ *
+ * Sources (page title, section):
+ *   [P4] "flashinfer.fused_moe.cute_dsl_fused_moe_bf16", summary formula:
+ *        out[t] = sum_k scale[t,k] * ffn(x[t]; e[t,k]),
+ *        ffn(x; e) = (silu(x . W1_gate[e]^T) * (x . W1_up[e]^T)) . W2[e]^T
+ *   [P4] same page, "Supported configuration": bf16 operands, fp32
+ *        accumulation; EP via num_local_experts / local_expert_offset with
+ *        routes outside the local shard contributing zero.
+ *   [P4] same page, "Parameters", use_fused_finalize=False: GEMM2 leaves
+ *        unscaled rows per (token, slot); the combine applies the scales and
+ *        sums in fp32 in a fixed order with one final rounding.
+ *   [P1] "flashinfer.experimental.cake_stepfun_moe", opening paragraphs:
+ *        routing is "Renormalize top-k" (softmax, top-k, renormalise).
+ *   [P2] "flashinfer.fused_moe.cake / cake_cute (MXFP4 SiTU routed MoE)",
+ *        "Host plan": the canonical W1 bank holds the up rows, then the gate
+ *        rows ([up | gate]).
+ *   [P3] "Cake ragged BF16 grouped GEMM (experimental)", operation table:
+ *        Y[offs[e-1]:offs[e]] = X[offs[e-1]:offs[e]] . W[e]^T, offs holding
+ *        cumulative group end offsets, groups may be empty.
+ *
+ * Precision: the pages fix fp32 accumulation with bf16 inputs and outputs, so
+ * the oracle computes in fp32.  The only roundings to bf16 are the SwiGLU
+ * intermediate h and the final output (and the grouped GEMM output Y).  Every
+ * sum runs sequentially in index order.  Build with -ffp-contract=off so that
+ * a*b+c is never fused into one rounding on any host.
+ *
+ * Readings where the pages are silent (each also listed in the design notes):
+ *   - top-k is chosen on the logits (softmax is strictly increasing, so the
+ *     chosen set is the same), ordered by value descending, ties to the lower
+ *     expert id;
+ *   - the renormalised weight of slot j is exp(l_j - l_0) / sum_i exp(l_i - l_0)
+ *     over the chosen k only (the full softmax denominator cancels);
+ *   - silu(g) = g / (1 + exp(-g)) in fp32; u and g are not rounded, h is;
+ *   - the unscaled GEMM2 rows y stay fp32;
+ *   - the pre-routed mode takes ids and weights as given (the caller
+ *     normalised them); ids outside [0, E) are dropped and flagged.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_BAD_EXPERT 1
+
+/* ---- bf16 <-> fp32 from the IEEE-754 binary32 layout -------------------- */
+
+/* bf16 is the upper 16 bits of a binary32, so widening is exact. */
+static float bf16_to_float(uint16_t b) {
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* Round a binary32 to the nearest bf16, ties to even.  The dropped low half
+ * is compared against one half of the bf16 ulp (0x8000); at exactly one half
+ * the kept part is rounded to even.  NaN maps to a quiet NaN. */
+static uint16_t float_to_bf16(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu) != 0)
+        return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t hi = u >> 16;
+    uint32_t lo = u & 0xffffu;
+    if (lo > 0x8000u || (lo == 0x8000u && (hi & 1u)))
+        hi += 1u;
+    return (uint16_t)hi;
+}
+
+uint16_t oracle_float_to_bf16(float f) { return float_to_bf16(f); }
+float oracle_bf16_to_float(uint16_t b) { return bf16_to_float(b); }
+
+static void set_threads(int nthreads) {
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+}
+
+/* ---- routing: softmax -> top-k -> renormalise  [P1 opening; P4 params] -- */
+
+/* logits [T, E] fp32 row-major -> ids [T, k] int32, w [T, k] fp32. */
+void oracle_route(const float *logits, int T, int E, int k, int32_t *ids,
+                  float *w, int nthreads) {
+    set_threads(nthreads);
+#pragma omp parallel for schedule(static)
+    for (int t = 0; t < T; ++t) {
+        const float *l = logits + (size_t)t * E;
+        char *taken = (char *)calloc((size_t)E, 1);
+        int32_t *sel = ids + (size_t)t * k;
+        /* k rounds of "largest remaining logit"; scanning ids upwards with a
+         * strict '>' keeps the lowest id among equal values. */
+        for (int j = 0; j < k; ++j) {
+            int best = -1;
+            for (int e = 0; e < E; ++e) {
+                if (taken[e]) continue;
+                if (best < 0 || l[e] > l[best]) best = e;
+            }
+            taken[best] = 1;
+            sel[j] = best;
+        }
+        free(taken);
+        /* softmax over the chosen k: exp(l_j - max) / sum */
+        float m = l[sel[0]];
+        float ex[64];
+        float s = 0.0f;
+        for (int j = 0; j < k; ++j) {
+            ex[j] = expf(l[sel[j]] - m);
+            s = s + ex[j];
+        }
+        for (int j = 0; j < k; ++j) w[(size_t)t * k + j] = ex[j] / s;
+    }
+}
+
+/* ---- sort / permute by expert  [P3 operation table; P1 prepared launches] -
+ *
+ * Routes are indexed by the expanded index r = t*k + j.  Local experts are the
+ * ids in [off, off+L).  m_indptr[L+1] has a leading zero; group i (global
+ * expert off+i) is permuted rows [m_indptr[i], m_indptr[i+1]).  Inside a group
+ * rows keep ascending r (a stable counting sort).  perm_to_exp[p] = r for
+ * p < M = m_indptr[L]; exp_to_perm[r] = p, or -1 for a route that is not local
+ * (or whose id is outside [0, E)).  Returns ORACLE_BAD_EXPERT when any id is
+ * outside [0, E). */
+int oracle_sort(const int32_t *ids, int T, int k, int E, int off, int L,
+                int32_t *m_indptr, int32_t *perm_to_exp, int32_t *exp_to_perm) {
+    int status = 0;
+    long R = (long)T * k;
+    int32_t *cnt = (int32_t *)calloc((size_t)L + 1, sizeof(int32_t));
+    for (long r = 0; r < R; ++r) {
+        int e = ids[r];
+        if (e < 0 || e >= E) { status |= ORACLE_BAD_EXPERT; continue; }
+        if (e >= off && e < off + L) cnt[e - off] += 1;
+    }
+    m_indptr[0] = 0;
+    for (int i = 0; i < L; ++i) m_indptr[i + 1] = m_indptr[i] + cnt[i];
+    int32_t *next = (int32_t *)malloc(sizeof(int32_t) * ((size_t)L + 1));
+    for (int i = 0; i < L; ++i) next[i] = m_indptr[i];
+    for (long r = 0; r < R; ++r) {
+        int e = ids[r];
+        if (e < 0 || e >= E || e < off || e >= off + L) {
+            exp_to_perm[r] = -1;
+            continue;
+        }
+        int p = next[e - off]++;
+        perm_to_exp[p] = (int32_t)r;
+        exp_to_perm[r] = p;
+    }
+    free(next);
+    free(cnt);
+    return status;
+}
+
+/* ---- one expert's FFN on one row  [P4 formula; P2 host plan for W1 rows] --
+ *
+ * x_row [H] bf16; w1e [2I, H] bf16 with rows 0..I-1 = up, I..2I-1 = gate;
+ * w2e [H, I] bf16.  Writes h [I] bf16 and y [H] fp32 (unscaled, unrounded). */
+static void expert_ffn_row(const uint16_t *x_row, const uint16_t *w1e,
+                           const uint16_t *w2e, int H, int I, uint16_t *h,
+                           float *y) {
+    for (int n = 0; n < I; ++n) {
+        const uint16_t *up_row = w1e + (size_t)n * H;
+        const uint16_t *gate_row = w1e + (size_t)(I + n) * H;
+        float u = 0.0f, g = 0.0f;
+        for (int c = 0; c < H; ++c) {
+            float xv = bf16_to_float(x_row[c]);
+            u = u + xv * bf16_to_float(up_row[c]);
+            g = g + xv * bf16_to_float(gate_row[c]);
+        }
+        float silu_g = g / (1.0f + expf(-g));
+        h[n] = float_to_bf16(silu_g * u);
+    }
+    for (int c = 0; c < H; ++c) {
+        const uint16_t *w2_row = w2e + (size_t)c * I;
+        float acc = 0.0f;
+        for (int n = 0; n < I; ++n)
+            acc = acc + bf16_to_float(h[n]) * bf16_to_float(w2_row[n]);
+        y[c] = acc;
+    }
+}
+
+/* ---- whole layer for a list of tokens  [P4 formula, EP rule, combine] -----
+ *
+ * x [T, H] bf16; ids, w [T, k]; w1 [L, 2I, H]; w2 [L, H, I] (local experts,
+ * local index = global id - off).  tokens[n_tok] selects which tokens to
+ * evaluate; out [n_tok, H] bf16 row i belongs to token tokens[i].
+ * Optional h_out [n_tok*k, I] bf16 and y_out [n_tok*k, H] fp32 receive the
+ * per-route intermediates in (token, slot) order; rows of routes that are not
+ * local are left untouched.  Returns ORACLE_BAD_EXPERT if any selected route
+ * has an id outside [0, E). */
+int oracle_moe_tokens(const uint16_t *x, const int32_t *ids, const float *w,
+                      const uint16_t *w1, const uint16_t *w2, int T, int H,
+                      int I, int E, int k, int off, int L,
+                      const int32_t *tokens, int n_tok, uint16_t *out,
+                      uint16_t *h_out, float *y_out, int nthreads) {
+    (void)T;
+    int status = 0;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : status)
+    for (int i = 0; i < n_tok; ++i) {
+        int t = tokens[i];
+        uint16_t *h = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)I);
+        float *y = (float *)malloc(sizeof(float) * (size_t)H * (size_t)k);
+        char *local = (char *)calloc((size_t)k, 1);
+        for (int j = 0; j < k; ++j) {
+            int e = ids[(size_t)t * k + j];
+            if (e < 0 || e >= E) { status |= ORACLE_BAD_EXPERT; continue; }
+            if (e < off || e >= off + L) continue; /* contributes zero */
+            local[j] = 1;
+            const uint16_t *w1e = w1 + (size_t)(e - off) * 2 * I * H;
+            const uint16_t *w2e = w2 + (size_t)(e - off) * H * I;
+            expert_ffn_row(x + (size_t)t * H, w1e, w2e, H, I, h,
+                           y + (size_t)j * H);
+            if (h_out)
+                memcpy(h_out + ((size_t)i * k + j) * I, h, sizeof(uint16_t) * I);
+            if (y_out)
+                memcpy(y_out + ((size_t)i * k + j) * H, y + (size_t)j * H,
+                       sizeof(float) * H);
+        }
+        for (int c = 0; c < H; ++c) {
+            float acc = 0.0f;
+            for (int j = 0; j < k; ++j)
+                if (local[j])
+                    acc = acc + w[(size_t)t * k + j] * y[(size_t)j * H + c];
+            out[(size_t)i * H + c] = float_to_bf16(acc);
+        }
+        free(local);
+        free(y);
+        free(h);
+    }
+    return status;
+}
+
+/* ---- stages on permuted rows (for stage-by-stage comparisons) ------------
+ *
+ * The permuted layout: group i of the L local experts is rows
+ * [group_end[i-1], group_end[i]) (group_end[-1] = 0)  [P3 operation table]. */
+static int group_of_row(const int32_t *group_end, int L, int p) {
+    for (int i = 0; i < L; ++i)
+        if (p < group_end[i]) return i;
+    return -1;
+}
+
+/* FC1 + SwiGLU on selected permuted rows: xp [*, H] bf16, w1 [L, 2I, H],
+ * rows[n_rows] -> h_rows [n_rows, I] bf16. */
+void oracle_fc1_swiglu_rows(const uint16_t *xp, const uint16_t *w1,
+                            const int32_t *group_end, int L, int H, int I,
+                            const int32_t *rows, int n_rows, uint16_t *h_rows,
+                            int nthreads) {
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int q = 0; q < n_rows; ++q) {
+        int p = rows[q];
+        int g = group_of_row(group_end, L, p);
+        const uint16_t *xr = xp + (size_t)p * H;
+        const uint16_t *w1e = w1 + (size_t)g * 2 * I * H;
+        for (int n = 0; n < I; ++n) {
+            float u = 0.0f, gt = 0.0f;
+            for (int c = 0; c < H; ++c) {
+                float xv = bf16_to_float(xr[c]);
+                u = u + xv * bf16_to_float(w1e[(size_t)n * H + c]);
+                gt = gt + xv * bf16_to_float(w1e[(size_t)(I + n) * H + c]);
+            }
+            float silu_g = gt / (1.0f + expf(-gt));
+            h_rows[(size_t)q * I + n] = float_to_bf16(silu_g * u);
+        }
+    }
+}
+
+/* FC2 on selected permuted rows: h [*, I] bf16, w2 [L, H, I] ->
+ * y_rows [n_rows, H] fp32 (unrounded). */
+void oracle_fc2_rows(const uint16_t *h, const uint16_t *w2,
+                     const int32_t *group_end, int L, int H, int I,
+                     const int32_t *rows, int n_rows, float *y_rows,
+                     int nthreads) {
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int q = 0; q < n_rows; ++q) {
+        int p = rows[q];
+        int g = group_of_row(group_end, L, p);
+        const uint16_t *hr = h + (size_t)p * I;
+        const uint16_t *w2e = w2 + (size_t)g * H * I;
+        for (int c = 0; c < H; ++c) {
+            float acc = 0.0f;
+            for (int n = 0; n < I; ++n)
+                acc = acc + bf16_to_float(hr[n]) *
+                                bf16_to_float(w2e[(size_t)c * I + n]);
+            y_rows[(size_t)q * H + c] = acc;
+        }
+    }
+}
+
+/* Combine: out[t] = bf16( sum_j w[t,j] * y[exp_to_perm[t*k+j]] ), j ascending,
+ * skipping slots with exp_to_perm == -1  [P4 params, deterministic path]. */
+void oracle_finalize(const float *y, const int32_t *exp_to_perm,
+                     const float *w, int T, int k, int H, uint16_t *out,
+                     int nthreads) {
+    set_threads(nthreads);
+#pragma omp parallel for schedule(static)
+    for (int t = 0; t < T; ++t) {
+        for (int c = 0; c < H; ++c) {
+            float acc = 0.0f;
+            for (int j = 0; j < k; ++j) {
+                int p = exp_to_perm[(size_t)t * k + j];
+                if (p < 0) continue;
+                acc = acc + w[(size_t)t * k + j] * y[(size_t)p * H + c];
+            }
+            out[(size_t)t * H + c] = float_to_bf16(acc);
+        }
+    }
+}
+
+/* Ragged grouped GEMM forward on selected rows  [P3 operation table, fwd]:
+ * X [sum_m, K] bf16, W [E, N, K] bf16, offs[E] cumulative ends.  Row p of
+ * group e: Y[p, n] = bf16( sum_c X[p,c] * W[e,n,c] ). */
+void oracle_grouped_gemm_rows(const uint16_t *X, const uint16_t *W,
+                              const int32_t *offs, int E, int N, int K,
+                              const int32_t *rows, int n_rows,
+                              uint16_t *Y_rows, int nthreads) {
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int q = 0; q < n_rows; ++q) {
+        int p = rows[q];
+        int e = group_of_row(offs, E, p);
+        const uint16_t *xr = X + (size_t)p * K;
+        const uint16_t *we = W + (size_t)e * N * K;
+        for (int n = 0; n < N; ++n) {
+            float acc = 0.0f;
+            for (int c = 0; c < K; ++c)
+                acc = acc + bf16_to_float(xr[c]) *
+                                bf16_to_float(we[(size_t)n * K + c]);
+            Y_rows[(size_t)q * N + n] = float_to_bf16(acc);
+        }
+    }
+}
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

@@ -1,0 +1,369 @@
+"""Pins for the CPU oracle against facts fixed outside the oracle itself.
+
+Each test checks the oracle against something it does not compute the same
+way: hand-worked cases, brute force over all subsets, an fp64 evaluation of
+the layer written as a dense masked sum over every (token, expert) pair, a
+library routine (numpy stable argsort, torch fp32 matmul, torch's bf16
+rounding), or an invariant of the mathematics (sum of weights, identical
+experts, token permutation, expert-range partition).
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mixture_experts_expert_router_gb300 import workloads as W
+from tests.tolerances import bf16_to_f64, check_bf16_close, ulp_distance
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_worked.json")
+
+
+def torch_bf16_bits(a64: np.ndarray) -> np.ndarray:
+    """Round fp32 values to bf16 with torch (a library rounding, RNE)."""
+    t = torch.from_numpy(np.ascontiguousarray(a64, np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+# ---------------------------------------------------------------- rounding --
+
+def test_bf16_rounding_matches_torch():
+    lib = oracle.load()
+    rng = np.random.default_rng(1)
+    vals = list(rng.standard_normal(4000).astype(np.float32) * 10.0 ** rng.integers(-40, 38, 4000))
+    # exact ties, values just around them, extremes
+    for hi in (0x3F80, 0x3F81, 0xBF80, 0x0001, 0x7F7F, 0x0080):
+        for lo in (0x7FFF, 0x8000, 0x8001):
+            vals.append(np.array([(hi << 16) | lo], np.uint32).view(np.float32)[0])
+    vals += [0.0, -0.0, np.float32(np.inf), np.float32(-np.inf), np.float32(3.4e38), np.float32(1e-45)]
+    vals = np.array(vals, np.float32)
+    got = np.array([lib.oracle_float_to_bf16(float(v)) for v in vals], np.uint16)
+    want = torch_bf16_bits(vals)
+    assert np.array_equal(got, want)
+
+
+# ----------------------------------------------------------------- routing --
+
+def test_route_hand_worked():
+    cases = json.load(open(GOLDEN))["route"]
+    for c in cases:
+        lg = np.array([c["logits"]], np.float32)
+        ids, w = oracle.route(lg, c["top_k"])
+        assert ids[0].tolist() == c["ids"], c
+        want = [eval(s, {"exp": math.exp}) for s in c["weights_closed_form"]]
+        assert np.allclose(w[0], want, atol=1e-6, rtol=0), (w[0], want)
+
+
+def _total_order_first_k(row, k):
+    """Brute force: the k-subset S such that every member precedes every
+    non-member under (logit desc, id asc); found by trying all subsets."""
+    E = len(row)
+    before = lambda a, b: row[a] > row[b] or (row[a] == row[b] and a < b)
+    hits = []
+    for S in itertools.combinations(range(E), k):
+        rest = [e for e in range(E) if e not in S]
+        if all(before(a, b) for a in S for b in rest):
+            hits.append(S)
+    assert len(hits) == 1
+    S = list(hits[0])
+    # order inside S by the same total order (insertion, no sort call)
+    ordered = []
+    for a in S:
+        pos = 0
+        while pos < len(ordered) and before(ordered[pos], a):
+            pos += 1
+        ordered.insert(pos, a)
+    return ordered
+
+
+@pytest.mark.parametrize("E", [1, 2, 3, 5, 8])
+def test_route_bruteforce_with_ties(E):
+    rng = np.random.default_rng(E)
+    T = 60
+    lg = rng.integers(-2, 3, size=(T, E)).astype(np.float32) * np.float32(0.75)  # many ties
+    for k in range(1, E + 1):
+        ids, _ = oracle.route(lg, k)
+        for t in range(T):
+            assert ids[t].tolist() == _total_order_first_k(lg[t], k)
+
+
+@pytest.mark.parametrize("E,k", [(4, 2), (8, 2), (128, 8), (256, 8), (64, 16)])
+def test_route_weights_vs_fp64_softmax_topk_renorm(E, k):
+    rng = np.random.default_rng(E * 100 + k)
+    lg = (rng.standard_normal((200, E)) * 3).astype(np.float32)
+    ids, w = oracle.route(lg, k)
+    # an independent formulation: full softmax over all E in fp64, pick the
+    # chosen ids, renormalise
+    l64 = lg.astype(np.float64)
+    p = np.exp(l64 - l64.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    sel = np.take_along_axis(p, ids.astype(np.int64), axis=1)
+    ref = sel / sel.sum(axis=1, keepdims=True)
+    assert np.max(np.abs(w - ref)) <= 1e-6
+    assert np.max(np.abs(w.astype(np.float64).sum(axis=1) - 1.0)) <= 1e-6
+    assert np.all(np.diff(w, axis=1) <= 0)  # descending weight order
+
+
+def test_route_zipf_config_histogram():
+    """The Zipf-biased configuration must contain empty and one-row groups."""
+    wl = W.make_moe("prefill_many_fine", H=64, I=64)
+    ids, _ = oracle.route(wl.logits.numpy(), wl.top_k)
+    cnt = np.bincount(ids.ravel(), minlength=wl.E)
+    assert (cnt == 0).sum() >= 1 and (cnt == 1).sum() >= 1
+    assert cnt.sum() == wl.T * wl.top_k
+
+
+# ----------------------------------------------------------------- sorting --
+
+def test_sort_hand_worked():
+    for c in json.load(open(GOLDEN))["sort"]:
+        ids = np.array(c["ids"], np.int32)
+        m, p2e, e2p, st = oracle.sort(ids, c["num_experts"], c["local_offset"], c["num_local"])
+        assert m.tolist() == c["m_indptr"]
+        assert p2e.tolist() == c["perm_to_exp"]
+        assert e2p.tolist() == c["exp_to_perm"]
+        assert st == c["status"]
+
+
+@pytest.mark.parametrize("T,k,E,off,L,bad", [
+    (1, 1, 1, 0, 1, False), (37, 2, 8, 0, 8, False), (100, 8, 256, 0, 256, False),
+    (64, 8, 128, 32, 40, False), (50, 4, 16, 15, 1, True), (513, 3, 7, 2, 3, True),
+    (300, 6, 64, 0, 64, True)])
+def test_sort_vs_stable_argsort(T, k, E, off, L, bad):
+    rng = np.random.default_rng(T * 7 + k)
+    ids = rng.integers(0, E, size=(T, k)).astype(np.int32)
+    if bad:
+        ids.flat[rng.integers(0, T * k, 5)] = rng.choice([-3, -1, E, E + 5], 5)
+    m, p2e, e2p, st = oracle.sort(ids, E, off, L)
+    flat = ids.ravel()
+    local = (flat >= off) & (flat < off + L)
+    # histogram and offsets
+    hist = np.bincount(flat[local] - off, minlength=L)
+    assert m.tolist() == [0] + np.cumsum(hist).tolist()
+    # stable sort (a library routine) of the local routes by expert
+    r_local = np.nonzero(local)[0]
+    order = r_local[np.argsort(flat[r_local], kind="stable")]
+    assert p2e.tolist() == order.tolist()
+    # bijection and inverse
+    assert len(set(p2e.tolist())) == len(p2e)
+    assert np.array_equal(e2p[p2e], np.arange(len(p2e)))
+    assert np.all(e2p[~local] == -1)
+    assert st == (1 if bad else 0)
+
+
+def test_sort_all_on_one_expert_and_empty():
+    ids = np.full((33, 2), 3, np.int32)
+    m, p2e, e2p, st = oracle.sort(ids, 5)
+    assert m.tolist() == [0, 0, 0, 0, 66, 66]
+    assert p2e.tolist() == list(range(66))
+    ids0 = np.zeros((0, 2), np.int32)
+    m, p2e, e2p, st = oracle.sort(ids0, 5)
+    assert m.tolist() == [0] * 6 and p2e.size == 0
+
+
+# --------------------------------------------------------- expert layer -----
+
+def _dense_masked_fp64(x, ids, w, w1, w2, E):
+    """Reference written as a dense sum over all (token, expert) pairs with a
+    gate matrix G[t, e] (zero for experts a token did not choose), in fp64.
+    Returns u, g (fp64) for every (t, e)."""
+    x64 = bf16_to_f64(x)
+    w1_64 = bf16_to_f64(w1)
+    I = w1.shape[1] // 2
+    G = np.zeros((x.shape[0], E))
+    for t in range(ids.shape[0]):
+        for j in range(ids.shape[1]):
+            G[t, ids[t, j]] += w[t, j]
+    u = np.einsum("th,enh->ten", x64, w1_64[:, :I, :])
+    g = np.einsum("th,enh->ten", x64, w1_64[:, I:, :])
+    return G, u, g
+
+
+def test_layer_bruteforce_fp64_tiny():
+    wl = W.make_moe("tiny")
+    x = W.bf16_bits(wl.x)
+    w1 = W.bf16_bits(wl.w1)
+    w2 = W.bf16_bits(wl.w2)
+    ids, w = oracle.route(wl.logits.numpy(), wl.top_k)
+    out, h, y, st = oracle.moe_tokens(x, ids, w, w1, w2, wl.E, want_intermediates=True)
+    assert st == 0
+    G, u, g = _dense_masked_fp64(x, ids, w, w1, w2, wl.E)
+    T, k, I, H = wl.T, wl.top_k, wl.I, wl.H
+    x64, w1_64, w2_64 = bf16_to_f64(x), bf16_to_f64(w1), bf16_to_f64(w2)
+    # step 1: h = bf16(silu(g) * u), each (token, slot).  The fp32 sums can
+    # move a value that sits next to a bf16 rounding boundary across it, so
+    # one ulp is allowed, and nearly all elements must agree exactly.
+    n_exact = 0
+    for t in range(T):
+        for j in range(k):
+            e = ids[t, j]
+            h64 = (g[t, e] / (1.0 + np.exp(-g[t, e]))) * u[t, e]
+            ulp = ulp_distance(h[t * k + j], torch_bf16_bits(h64))
+            assert np.all(ulp <= 1)
+            n_exact += int(np.sum(ulp == 0))
+    assert n_exact >= 0.99 * T * k * I
+    # step 2: y = h . W2^T from the oracle's own h, fp64 with an fp32 bound
+    for t in range(T):
+        for j in range(k):
+            e = ids[t, j]
+            hv = bf16_to_f64(h[t * k + j])
+            y64 = w2_64[e] @ hv
+            bound = I * 2.0 ** -23 * (np.abs(w2_64[e]) @ np.abs(hv)) + 1e-30
+            assert np.all(np.abs(y[t * k + j] - y64) <= bound)
+    # step 3: out = bf16(sum_j w * y) against the dense masked combine in fp64
+    Y = np.zeros((T, wl.E, H))
+    for t in range(T):
+        for j in range(k):
+            Y[t, ids[t, j]] = y[t * k + j]
+    out64 = np.einsum("te,teh->th", G, Y)
+    want = torch_bf16_bits(out64)
+    assert np.all(ulp_distance(out, want) <= 1)
+    assert np.mean(ulp_distance(out, want) == 0) >= 0.99
+
+
+def _dense_swiglu_mlp_torch(x_bits, w1_bits, w2_bits):
+    """Dense SwiGLU MLP with torch fp32 matmuls and a bf16 round of h."""
+    xt = torch.from_numpy(bf16_to_f64(x_bits).astype(np.float32))
+    w1t = torch.from_numpy(bf16_to_f64(w1_bits).astype(np.float32))
+    w2t = torch.from_numpy(bf16_to_f64(w2_bits).astype(np.float32))
+    I = w1t.shape[0] // 2
+    u = xt @ w1t[:I].T
+    g = xt @ w1t[I:].T
+    h = (torch.nn.functional.silu(g) * u).to(torch.bfloat16).float()
+    y = h @ w2t.T
+    return y.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("T,H,I", [(9, 64, 64), (33, 128, 192), (4, 256, 64)])
+def test_e1_k1_equals_dense_swiglu_mlp(T, H, I):
+    wl = W.make_moe(T=T, H=H, I=I, E=1, top_k=1, mode="logits", seed=3)
+    x, w1, w2 = W.bf16_bits(wl.x), W.bf16_bits(wl.w1), W.bf16_bits(wl.w2)
+    ids, w = oracle.route(wl.logits.numpy(), 1)
+    assert np.all(ids == 0) and np.all(w == 1.0)  # e/e == 1 exactly in IEEE
+    out, st = oracle.moe_tokens(x, ids, w, w1, w2, 1)
+    want = _dense_swiglu_mlp_torch(x, w1[0], w2[0])
+    check_bf16_close(out, want, "E=1,k=1 vs dense MLP")
+
+
+def test_identical_experts_independent_of_routing():
+    T, H, I, E, k = 24, 64, 64, 6, 3
+    base = W.make_moe(T=T, H=H, I=I, E=1, top_k=1, mode="logits", seed=5)
+    x = W.bf16_bits(base.x)
+    w1 = np.repeat(W.bf16_bits(base.w1), E, axis=0)
+    w2 = np.repeat(W.bf16_bits(base.w2), E, axis=0)
+    ref, _ = oracle.moe_tokens(x, np.zeros((T, 1), np.int32), np.ones((T, 1), np.float32),
+                               W.bf16_bits(base.w1), W.bf16_bits(base.w2), 1)
+    for seed in range(3):
+        lg = np.random.default_rng(seed).standard_normal((T, E)).astype(np.float32)
+        ids, w = oracle.route(lg, k)
+        out, _ = oracle.moe_tokens(x, ids, w, w1, w2, E)
+        # sum_j w_j * y = (sum_j w_j) * y with sum w = 1 up to fp32 rounding
+        assert np.all(ulp_distance(out, ref) <= 1)
+
+
+def test_token_permutation_equivariance():
+    wl = W.make_moe(T=20, H=64, I=64, E=5, top_k=2, mode="logits", seed=9)
+    x, w1, w2 = W.bf16_bits(wl.x), W.bf16_bits(wl.w1), W.bf16_bits(wl.w2)
+    lg = wl.logits.numpy()
+    ids, w = oracle.route(lg, 2)
+    out, _ = oracle.moe_tokens(x, ids, w, w1, w2, 5)
+    perm = np.random.default_rng(0).permutation(20)
+    ids_p, w_p = oracle.route(lg[perm], 2)
+    out_p, _ = oracle.moe_tokens(x[perm], ids_p, w_p, w1, w2, 5)
+    assert np.array_equal(out_p, out[perm])
+
+
+def test_expert_parallel_partition_sums_to_full():
+    """Routes outside the shard contribute zero: the fp32 partial combines of
+    disjoint expert ranges add up to the full layer."""
+    wl = W.make_moe(T=16, H=64, I=64, E=8, top_k=3, mode="logits", seed=11)
+    x, w1, w2 = W.bf16_bits(wl.x), W.bf16_bits(wl.w1), W.bf16_bits(wl.w2)
+    ids, w = oracle.route(wl.logits.numpy(), 3)
+    full, st = oracle.moe_tokens(x, ids, w, w1, w2, 8)
+    parts = np.zeros((16, 64))
+    bound = np.zeros((16, 64))
+    for off, L in ((0, 3), (3, 4), (7, 1)):
+        part, st = oracle.moe_tokens(x, ids, w, w1[off:off + L], w2[off:off + L], 8,
+                                     local_offset=off, num_local=L)
+        assert st == 0
+        pv = bf16_to_f64(part)
+        parts += pv
+        bound += np.abs(pv) * 2.0 ** -8 + 1e-6   # half a bf16 ulp per rounded partial
+    fv = bf16_to_f64(full)
+    bound += np.abs(fv) * 2.0 ** -8 + 1e-6
+    assert np.all(np.abs(parts - fv) <= bound)
+    # a shard holding none of the chosen experts gives exact zeros
+    none_ids = np.zeros_like(ids)
+    zero, _ = oracle.moe_tokens(x, none_ids, w, w1[4:6], w2[4:6], 8, local_offset=4, num_local=2)
+    assert np.all(bf16_to_f64(zero) == 0)
+
+
+def test_bad_expert_ids_are_dropped_and_flagged():
+    wl = W.make_moe(T=4, H=64, I=64, E=4, top_k=2, mode="prerouted", seed=2)
+    x, w1, w2 = W.bf16_bits(wl.x), W.bf16_bits(wl.w1), W.bf16_bits(wl.w2)
+    ids = wl.topk_ids.numpy().copy()
+    w = wl.topk_w.numpy()
+    ref_ids = ids.copy()
+    ids[1, 1] = 9
+    out, st = oracle.moe_tokens(x, ids, w, w1, w2, 4)
+    assert st == oracle.BAD_EXPERT
+    ok, _ = oracle.moe_tokens(x, ref_ids, w, w1, w2, 4)
+    assert np.array_equal(out[[0, 2, 3]], ok[[0, 2, 3]])
+    # token 1 keeps only its first route
+    one_ids = ref_ids.copy()
+    w_one = w.copy()
+    w_one[1, 1] = 0.0
+    alt, _ = oracle.moe_tokens(x, one_ids, w_one, w1, w2, 4)
+    assert np.array_equal(out[1], alt[1])
+
+
+def test_stage_functions_compose_to_layer():
+    """The stage-by-stage oracle (route, sort, gather, FC1, FC2, combine)
+    equals the per-token layer bitwise."""
+    wl = W.make_moe(T=30, H=128, I=64, E=6, top_k=2, mode="logits", seed=4)
+    x, w1, w2 = W.bf16_bits(wl.x), W.bf16_bits(wl.w1), W.bf16_bits(wl.w2)
+    ids, w = oracle.route(wl.logits.numpy(), 2)
+    m, p2e, e2p, st = oracle.sort(ids, 6)
+    xp = x[p2e // 2]
+    rows = np.arange(len(p2e), dtype=np.int32)
+    h = oracle.fc1_swiglu_rows(xp, w1, m[1:], rows)
+    y = oracle.fc2_rows(h, w2, m[1:], rows)
+    out = oracle.finalize(y, e2p, w)
+    ref, _ = oracle.moe_tokens(x, ids, w, w1, w2, 6)
+    assert np.array_equal(out, ref)
+
+
+# ------------------------------------------------------------ grouped GEMM --
+
+def test_grouped_gemm_vs_torch_per_group():
+    d = W.make_grouped_gemm(seed=1, sum_m=300, E=7, K=128, N=64, alpha=0.3)
+    X, Wt, offs = W.bf16_bits(d["X"]), W.bf16_bits(d["W"]), d["offs"].numpy()
+    assert (d["sizes"] == 0).any()
+    Y = oracle.grouped_gemm_rows(X, Wt, offs)
+    start = 0
+    for e in range(d["E"]):
+        end = int(offs[e])
+        if end > start:
+            xs = torch.from_numpy(bf16_to_f64(X[start:end]).astype(np.float32))
+            ws = torch.from_numpy(bf16_to_f64(Wt[e]).astype(np.float32))
+            ref = (xs @ ws.T).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+            check_bf16_close(Y[start:end], ref, f"group {e}")
+        start = end
+
+
+def test_workload_generator_is_seeded():
+    a = W.make_moe("tiny", seed=0)
+    b = W.make_moe("tiny", seed=0)
+    c = W.make_moe("tiny", seed=1)
+    assert torch.equal(a.x, b.x) and torch.equal(a.w1, b.w1) and torch.equal(a.logits, b.logits)
+    assert not torch.equal(a.x, c.x)
+    d = W.make_moe("decode_t8")
+    assert torch.allclose(d.topk_w.double().sum(1), torch.ones(8, dtype=torch.float64), atol=1e-6)
+    ids = d.topk_ids.numpy()
+    assert all(len(set(r)) == 8 for r in ids)
+    s = W.grouped_sizes(16384, 64, 0.3, 0)
+    assert s.sum() == 16384 and (s == 0).any() and ((s % 128) != 0).any()

@@ -1,0 +1,62 @@
+"""Acceptance rules shared by the parity tests.
+
+Outputs: max|a - b| <= 1e-2 * rms(b) (rms over the whole tensor, fp64) and at
+least 99.9% of elements within 2 bf16 ulp, the ulp distance being the gap on
+the monotone integer order of the bf16 bit patterns (+0 and -0 equal).
+Routing weights: within 1e-6 absolute.
+"""
+import numpy as np
+
+RMS_FRAC = 1e-2
+ULP_MAX = 2
+ULP_FRACTION = 0.999
+WEIGHT_ATOL = 1e-6
+
+
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    b = np.ascontiguousarray(bits, np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def bf16_order(bits: np.ndarray) -> np.ndarray:
+    b = np.ascontiguousarray(bits, np.uint16).astype(np.int64)
+    mag = b & 0x7FFF
+    return np.where(b & 0x8000, -mag, mag)
+
+
+def ulp_distance(a_bits: np.ndarray, b_bits: np.ndarray) -> np.ndarray:
+    return np.abs(bf16_order(a_bits) - bf16_order(b_bits))
+
+
+def check_bf16_close(got_bits: np.ndarray, want_bits: np.ndarray, what: str = "output"):
+    """Assert the output acceptance rule; returns (max_abs/rms, frac within 2 ulp)."""
+    got = bf16_to_f64(got_bits)
+    want = bf16_to_f64(want_bits)
+    assert got.shape == want.shape, (got.shape, want.shape)
+    if want.size == 0:
+        return 0.0, 1.0
+    assert np.all(np.isfinite(got)), f"{what}: non-finite values"
+    rms = float(np.sqrt(np.mean(want * want)))
+    err = float(np.max(np.abs(got - want)))
+    ulp = ulp_distance(got_bits, want_bits)
+    frac = float(np.mean(ulp <= ULP_MAX))
+    ratio = err / rms if rms > 0 else err
+    assert err <= RMS_FRAC * rms or (rms == 0 and err == 0), f"{what}: max err {err} > 1e-2*rms {rms}"
+    assert frac >= ULP_FRACTION, f"{what}: only {frac:.5f} within {ULP_MAX} ulp"
+    return ratio, frac
+
+
+def check_f32_close(got: np.ndarray, want: np.ndarray, what: str = "output"):
+    """fp32 intermediates: max|a-b| <= 1e-2 * rms(b) and 99.9% within a
+    relative 2^-7 (two bf16 ulp) of |b| + 1e-3 * rms."""
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    assert got.shape == want.shape
+    if want.size == 0:
+        return
+    assert np.all(np.isfinite(got)), f"{what}: non-finite values"
+    rms = float(np.sqrt(np.mean(want * want)))
+    diff = np.abs(got - want)
+    assert diff.max() <= RMS_FRAC * rms, f"{what}: max err {diff.max()} > 1e-2*rms {rms}"
+    frac = float(np.mean(diff <= 2.0 ** -7 * np.abs(want) + 1e-3 * rms))
+    assert frac >= ULP_FRACTION, f"{what}: only {frac:.5f} close"
