@@ -1,0 +1,433 @@
+"""Benchmark of the routed MoE expert-layer forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config NAME] [--no-cpu-baseline]
+
+One step = one full pass of the layer (route -> sort -> gather -> FC1+SwiGLU ->
+FC2 -> finalize) over one batch of seeded synthetic input, launched through the
+prepared-launch C ABI.  The default workload is "prefill_few_large"
+(T=4096 tokens, hidden 4096, intermediate 14336, 8 experts, top-2, routing from
+fp32 logits).  Under torchrun every rank runs its own replica of the workload
+(tokens are independent; there is no data-path collective), so the scaling is
+weak and `value` is the tokens of all ranks divided by the slowest rank's time.
+
+Rank 0 prints one JSON line.  `--impl reference` times the CPU oracle (the only
+other place this script runs it) on a bounded token sample of the same
+workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused-MoE tokens/s and TFLOP/s (or GB/s) at 1 GB300; % of BF16/HBM roofline"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except Exception:
+        return dict(PEAKS_FALLBACK), "fallback"
+
+
+# ------------------------------------------------------------------ clocks --
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: str):
+        self.rows = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-i", index,
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self, t0: float, t1: float):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        inside = [r for ts, r in self.rows if t0 <= ts <= t1]
+        note = None
+        if not inside:
+            # timed region shorter than one sampling period: nearest samples
+            inside = [r for ts, r in self.rows if t0 - 0.5 <= ts <= t1 + 0.5] or [r for _, r in self.rows]
+            note = "timed region shorter than the 200 ms sampling period; nearest samples used"
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in inside if num(r[1]) is not None]
+        smax = [num(r[2]) for r in inside if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i in range(4) if r[5 + i].lower().startswith("active")})
+        out = {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+               "reasons": reasons, "samples": len(inside)}
+        if note:
+            out["note"] = note
+        return out
+
+
+# ------------------------------------------------------------ distributed --
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, value: float) -> float:
+    if world == 1:
+        return value
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if torch.cuda.is_available() else torch.device("cpu")
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# -------------------------------------------------------------- workload --
+
+def layer_flops(M: int, H: int, I: int) -> float:
+    return 2.0 * M * (H * 2 * I + I * H)
+
+
+def layer_bytes(wl, ids: np.ndarray) -> float:
+    """Algorithmic bytes: weights of non-empty local experts, x read, out
+    written, routing inputs read."""
+    L = wl.num_local
+    local = ids[(ids >= wl.local_offset) & (ids < wl.local_offset + L)] - wl.local_offset
+    active = len(np.unique(local))
+    wbytes = active * (2 * wl.I * wl.H + wl.H * wl.I) * 2.0
+    route = wl.T * wl.E * 4.0 if wl.mode == "logits" else wl.T * wl.top_k * 8.0
+    return wbytes + wl.T * wl.H * 2.0 * 2 + route, active
+
+
+def oracle_sample_rate(wl, ids, w, n_tok: int, seed: int, threads: int, host_w=None):
+    """Time the CPU oracle on n_tok sampled tokens (route + layer for them).
+    Returns (tokens/s, seconds, tokens)."""
+    import oracle
+    from mixture_experts_expert_router_gb300 import workloads as W
+    rng = np.random.default_rng(seed)
+    tokens = np.sort(rng.choice(wl.T, size=min(n_tok, wl.T), replace=False)).astype(np.int32)
+    x = W.bf16_bits(wl.x)
+    w1, w2 = host_w
+    t0 = time.perf_counter()
+    if wl.mode == "logits":
+        lg = wl.logits.cpu().numpy()[tokens]
+        ids_s, w_s = oracle.route(lg, wl.top_k, nthreads=threads)
+        ids_full = np.zeros((wl.T, wl.top_k), np.int32)
+        w_full = np.zeros((wl.T, wl.top_k), np.float32)
+        ids_full[tokens], w_full[tokens] = ids_s, w_s
+    else:
+        ids_full, w_full = ids, w
+    oracle.moe_tokens(x, ids_full, w_full, w1, w2, wl.E, tokens=tokens, local_offset=wl.local_offset,
+                      num_local=wl.num_local, nthreads=threads)
+    dt = time.perf_counter() - t0
+    return len(tokens) / dt, dt, len(tokens)
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def calibrated_tokens(wl, ids, w, threads, host_w, budget_s: float):
+    rate, _, _ = oracle_sample_rate(wl, ids, w, min(max(8, 2 * threads), wl.T), 12345, threads, host_w)
+    return int(max(1, min(wl.T, rate * budget_s)))
+
+
+# ------------------------------------------------------------------- main --
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    import oracle
+    from mixture_experts_expert_router_gb300 import workloads as W
+    oracle.build()
+    wl = make_workload(args, 0, "cpu")
+    threads = host_cores()
+    ids = wl.topk_ids.numpy() if wl.topk_ids is not None else None
+    w = wl.topk_w.numpy() if wl.topk_w is not None else None
+    host_w = (W.bf16_bits(wl.w1), W.bf16_bits(wl.w2))
+    steps, warm = args.steps, args.warmup
+    per_step = max(0.5, args.reference_budget / max(1, steps + warm))
+    n_tok = calibrated_tokens(wl, ids, w, threads, host_w, per_step)
+    for i in range(warm):
+        oracle_sample_rate(wl, ids, w, n_tok, 100 + i, threads, host_w)
+    total_tok, total_t = 0, 0.0
+    for i in range(steps):
+        _, dt, n = oracle_sample_rate(wl, ids, w, n_tok, 1000 + i, threads, host_w)
+        total_tok += n
+        total_t += dt
+    value = total_tok / total_t
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": steps, "warmup": warm, "ms_per_step": 1000.0 * total_t / steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded)",
+        "config": config_dict(wl, world),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{n_tok} random tokens of the {wl.T}-token batch per step "
+                                   f"(routing + FC1/SwiGLU + FC2 + combine for those tokens)"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def make_workload(args, rank, weights_device):
+    from mixture_experts_expert_router_gb300 import workloads as W
+    if args.shape:
+        T, H, I, E, k = (int(v) for v in args.shape.split(","))
+        wl = W.make_moe(T=T, H=H, I=I, E=E, top_k=k, mode="logits", seed=args.seed + rank, device="cpu",
+                        weights_device=weights_device)
+        wl.name = f"custom_T{T}_H{H}_I{I}_E{E}_k{k}"
+        return wl
+    return W.make_moe(args.config, seed=args.seed + rank, device="cpu", weights_device=weights_device)
+
+
+def config_dict(wl, world):
+    return {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "top_k": wl.top_k,
+            "routing": wl.mode, "global_batch": wl.T * world,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": "inputs larger than L2: the expert weights stream from HBM every step"}
+
+
+def run_ours(args, world, rank, local):
+    import mixture_experts_expert_router_gb300 as moe
+    from mixture_experts_expert_router_gb300 import workloads as W
+    moe.library()
+    dev = torch.device("cuda", local)
+    wl = make_workload(args, rank, dev)
+    x = wl.x.to(dev)
+    logits = wl.logits.to(dev) if wl.logits is not None else None
+    tids = wl.topk_ids.to(dev) if wl.topk_ids is not None else None
+    tw = wl.topk_w.to(dev) if wl.topk_w is not None else None
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    plan = moe.MoEPlan(x, wl.w1, wl.w2, wl.E, wl.top_k, logits=logits, topk_ids=tids, topk_w=tw,
+                       local_offset=wl.local_offset, status=status, stage_timing=True)
+    kernels = plan.kernels_per_launch()
+    stream = torch.cuda.current_stream(dev)
+
+    # routed rows of this batch (for FLOP and byte counts)
+    plan.launch()
+    torch.cuda.synchronize()
+    R = wl.T * wl.top_k
+    if wl.mode == "logits":  # the routed ids the plan left in its workspace
+        off = plan.buffers()["topk_ids"] - plan.workspace.data_ptr()
+        ids_np = plan.workspace[off:off + R * 4].view(torch.int32).cpu().numpy()
+    else:
+        ids_np = wl.topk_ids.numpy().ravel()
+    L = wl.num_local
+    M = int(np.sum((ids_np >= wl.local_offset) & (ids_np < wl.local_offset + L)))
+    F = layer_flops(M, wl.H, wl.I)
+    F_fc1 = 2.0 * M * wl.H * 2 * wl.I
+    B, active = layer_bytes(wl, ids_np)
+
+    dev_index = str(local)
+    try:
+        uuid = torch.cuda.get_device_properties(dev).uuid
+        dev_index = "GPU-" + str(uuid) if uuid is not None else dev_index
+    except Exception:
+        pass
+    clocks = ClockSampler(dev_index)
+    time.sleep(0.3)
+    for _ in range(args.warmup):
+        plan.launch()
+    torch.cuda.synchronize()
+    plan.stage_reset()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        plan.launch()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    barrier(world)
+    ms_local = ev0.elapsed_time(ev1)
+    stage_ms, n_timed = plan.stage_times()
+    time.sleep(0.25)
+
+    # end to end: pinned host inputs in, result out, every step
+    x_h = wl.x.pin_memory()
+    lg_h = wl.logits.pin_memory() if logits is not None else None
+    ids_h = wl.topk_ids.pin_memory() if tids is not None else None
+    w_h = wl.topk_w.pin_memory() if tw is not None else None
+    out_h = torch.empty(plan.out.shape, dtype=plan.out.dtype).pin_memory()
+    h2d = x_h.numel() * 2 + (lg_h.numel() * 4 if lg_h is not None else 0) + \
+        (ids_h.numel() * 4 + w_h.numel() * 4 if ids_h is not None else 0)
+    d2h = out_h.numel() * 2
+
+    def e2e_step():
+        x.copy_(x_h, non_blocking=True)
+        if lg_h is not None:
+            logits.copy_(lg_h, non_blocking=True)
+        if ids_h is not None:
+            tids.copy_(ids_h, non_blocking=True)
+            tw.copy_(w_h, non_blocking=True)
+        plan.launch()
+        out_h.copy_(plan.out, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks.stop()
+    ms_e2e_local = e0.elapsed_time(e1)
+    st = int(status.item())
+
+    ms = max_over_ranks(world, ms_local)
+    ms_e2e = max_over_ranks(world, ms_e2e_local)
+    tokens_all = wl.T * world * args.steps
+    value = tokens_all / (ms / 1000.0)
+    e2e_value = tokens_all / (ms_e2e / 1000.0)
+    step_s = ms / 1000.0 / args.steps
+
+    peaks, peak_src = load_peaks()
+    fc1_s = stage_ms.get("fc1_swiglu", 0.0) / 1000.0 / max(1, n_timed)
+    fc1_tflops = F_fc1 / fc1_s / 1e12 if fc1_s > 0 else None
+    peak_t = float(peaks.get("bf16_tflops_sustained", PEAKS_FALLBACK["bf16_tflops_sustained"]))
+    roofline_t = max(F / (float(peaks["bf16_tflops"]) * 1e12), B / (float(peaks["hbm_gbs"]) * 1e9))
+    traffic = None
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            traffic = json.load(f).get(wl.name, {}).get("fc1_swiglu")
+    except Exception:
+        traffic = None
+
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded)",
+        "config": config_dict(wl, world),
+        "tflops": F * world / step_s / 1e12,
+        "hbm_gbs": B * world / step_s / 1e9,
+        "roofline_step": {"time_ms": roofline_t * 1000.0, "frac": roofline_t / step_s,
+                          "flops": F, "bytes": B, "active_experts": active,
+                          "peaks": f"{peak_src}: {peaks['bf16_tflops']} TFLOP/s bf16, {peaks['hbm_gbs']} GB/s"},
+        "roofline": {"kernel": "fc1_swiglu", "bound": "tensor", "achieved": fc1_tflops, "peak": peak_t,
+                     "unit": "TFLOP/s", "frac": (fc1_tflops / peak_t) if fc1_tflops else None,
+                     "traffic": traffic, "peak_kind": f"{peak_src} sustained bf16 (kernel timed inside the step)",
+                     "flops_per_launch": F_fc1},
+        "stage_ms": {k: v / max(1, n_timed) for k, v in stage_ms.items()},
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": kernels * args.steps,
+        "clocks": clocks.summary(t_wall0, t_wall1),
+        "device_status": st,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        threads = host_cores()
+        host_w = (W.bf16_bits(wl.w1), W.bf16_bits(wl.w2))
+        ids2 = wl.topk_ids.numpy() if wl.topk_ids is not None else None
+        w2 = wl.topk_w.numpy() if wl.topk_w is not None else None
+        n_tok = calibrated_tokens(wl, ids2, w2, threads, host_w, args.cpu_budget)
+        rate, dt, n = oracle_sample_rate(wl, ids2, w2, n_tok, 7, threads, host_w)
+        line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                                "sample": f"{n} random tokens of the {wl.T}-token batch "
+                                          f"({dt:.1f} s wall on {threads} threads)"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="prefill_few_large")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--shape", default=None,
+                    help="T,H,I,E,top_k of a custom logits-routed workload (profiling runs)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--reference-budget", type=float, default=120.0,
+                    help="seconds of oracle work for the whole --impl reference run")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_setup()
+    try:
+        if args.impl == "reference":
+            return run_reference(args, world, rank)
+        return run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

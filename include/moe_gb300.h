@@ -1,0 +1,252 @@
+/*
+ * moe_gb300.h -- C ABI of the GB300 (sm_103a) routed mixture-of-experts
+ * expert layer.
+ *
+ * The layer (flashinfer.fused_moe.cute_dsl_fused_moe_bf16, summary formula):
+ *
+ *   out[t] = sum_j w[t,j] * ffn(x[t]; e[t,j]),
+ *   ffn(x; e) = (silu(x . W1_gate[e]^T) * (x . W1_up[e]^T)) . W2[e]^T
+ *
+ * computed as route -> sort -> gather -> FC1+SwiGLU -> FC2 -> finalize, every
+ * step in a hand-written CUDA kernel.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers, owned by the caller, row-major
+ *     and contiguous.  bf16 tensors are passed as moe_bf16 (the 16-bit
+ *     pattern).  The library never allocates device memory, never frees a
+ *     caller pointer and never synchronises the host inside a launch.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default).
+ *   - Every call returns MOE_OK (0) or a negative MOE_ERR_* code; on an error
+ *     nothing has been enqueued.  moe_status_string() describes a code.
+ *   - Expert weights are the LOCAL bank of an expert-parallel shard
+ *     (cute_dsl_fused_moe_bf16, Parameters): W1 [L, 2I, H] holds, for local
+ *     expert i (global id local_offset + i), the I "up" rows followed by the
+ *     I "gate" rows (the canonical [up | gate] order of
+ *     flashinfer.fused_moe.cake / cake_cute, Host plan); W2 [L, H, I].
+ *     Routes to global ids outside [local_offset, local_offset + L)
+ *     contribute zero (cute_dsl_fused_moe_bf16, Supported configuration).
+ *   - Arithmetic: bf16 operands, fp32 accumulation, bf16 output
+ *     (cute_dsl_fused_moe_bf16, Supported configuration).
+ *   - Device-side problems that the host cannot see (a pre-routed id outside
+ *     [0, E), a bounded wait that gave up) are reported by OR-ing MOE_DEV_*
+ *     bits into a caller-provided int32 status word in device memory.  The
+ *     launch chain clears it first; read it after the stream has finished.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+typedef uint16_t moe_bf16; /* bfloat16 bit pattern */
+
+/* ---- return codes --------------------------------------------------------- */
+#define MOE_OK 0
+#define MOE_ERR_NULL (-1)        /* a required pointer is NULL                 */
+#define MOE_ERR_SHAPE (-2)       /* a size is out of range or not a supported multiple */
+#define MOE_ERR_ALIGN (-3)       /* a pointer is not 16-byte aligned           */
+#define MOE_ERR_WORKSPACE (-4)   /* workspace NULL or smaller than required    */
+#define MOE_ERR_MODE (-5)        /* routing inputs: give logits XOR (ids, weights) */
+#define MOE_ERR_CUDA (-6)        /* a CUDA runtime call or launch failed       */
+#define MOE_ERR_DEVICE (-7)      /* no device, or the device is not sm_103     */
+#define MOE_ERR_TENSOR_MAP (-8)  /* the driver rejected a TMA tensor map       */
+#define MOE_ERR_STATE (-9)       /* call not valid for this plan's state       */
+
+/* ---- device status bits ---------------------------------------------------- */
+#define MOE_DEV_BAD_EXPERT 1u    /* a routed id outside [0, E): route dropped  */
+#define MOE_DEV_TIMEOUT 2u       /* a bounded in-kernel wait gave up           */
+
+/* ---- limits ------------------------------------------------------------------ */
+#define MOE_MAX_EXPERTS 1024     /* E and L                                    */
+#define MOE_MAX_TOP_K 16
+
+/* Describe a return code (static string, never NULL). */
+MOE_API const char *moe_status_string(int code);
+
+/* Version of this ABI (major * 100 + minor). */
+MOE_API int moe_abi_version(void);
+
+/* ---- S1 route ----------------------------------------------------------------
+ * Renormalised top-k routing ("Renormalize top-k":
+ * flashinfer.experimental.cake_stepfun_moe, opening paragraphs; routing read
+ * from logits, RoutingInputMode.FromLogits, Unified MoE API opt-in).
+ *   logits   [T, E] fp32 (read)
+ *   topk_ids [T, top_k] int32 (written): the top_k experts of each token by
+ *            logit, descending, equal logits ordered by lower expert id.
+ *   topk_w   [T, top_k] fp32 (written): softmax restricted to the chosen
+ *            experts, w_j = exp(l_j - l_0) / sum_i exp(l_i - l_0).
+ * Sizes: T >= 0, 1 <= E <= MOE_MAX_EXPERTS, 1 <= top_k <= min(E, MOE_MAX_TOP_K).
+ * One warp per token.  T == 0 is a no-op. */
+MOE_API int moe_route(const float *logits, int T, int E, int top_k, int32_t *topk_ids,
+              float *topk_w, void *stream);
+
+/* ---- S2 sort -------------------------------------------------------------------
+ * Stable counting sort of the T*top_k routes by local expert (the
+ * consecutive-row groups of Cake ragged BF16 grouped GEMM, operation table;
+ * expanded_idx_to_permuted_idx of flashinfer.experimental.cake_stepfun_moe,
+ * Prepared launches).  Expanded index r = t*top_k + j.
+ *   topk_ids    [T, top_k] int32 global ids (read)
+ *   m_indptr    [L+1] int32 (written): m_indptr[0] = 0, group i = permuted
+ *               rows [m_indptr[i], m_indptr[i+1]); M = m_indptr[L].
+ *   perm_to_exp [T*top_k] int32 (written, first M valid): expanded index of
+ *               each permuted row; ascending r inside a group.
+ *   exp_to_perm [T*top_k] int32 (written): permuted row of each route, -1 for
+ *               a route whose id is not local or outside [0, E).
+ *   workspace   >= moe_sort_workspace_size(T, top_k, L) bytes (may be NULL
+ *               when that size is 0).
+ *   status      optional int32 word: cleared, then MOE_DEV_BAD_EXPERT if any
+ *               id is outside [0, E).
+ * Sizes: 0 <= local_offset, 1 <= L, local_offset + L <= E <= MOE_MAX_EXPERTS. */
+MOE_API size_t moe_sort_workspace_size(int T, int top_k, int num_local);
+MOE_API int moe_sort(const int32_t *topk_ids, int T, int top_k, int E, int local_offset,
+             int num_local, int32_t *m_indptr, int32_t *perm_to_exp,
+             int32_t *exp_to_perm, void *workspace, size_t workspace_bytes,
+             int32_t *status, void *stream);
+
+/* ---- S3 gather -------------------------------------------------------------------
+ * xp[p, :] = x[perm_to_exp[p] / top_k, :] for p < M = m_indptr[L] (the
+ * expanded per-route activations; cute_dsl_fused_moe_bf16, Parameters,
+ * use_fused_finalize).  Rows p >= M of xp are not written.
+ *   x [T, H] bf16, xp [T*top_k, H] bf16.  H % 8 == 0. */
+MOE_API int moe_gather(const moe_bf16 *x, const int32_t *perm_to_exp,
+               const int32_t *m_indptr, int T, int H, int top_k, int num_local,
+               moe_bf16 *xp, void *stream);
+
+/* ---- S4 FC1 + SwiGLU -----------------------------------------------------------
+ * For permuted row p of group i: u = xp[p] . W1[i, 0:I]^T,
+ * g = xp[p] . W1[i, I:2I]^T (fp32), h[p] = bf16_rne(silu(g) * u)
+ * (cute_dsl_fused_moe_bf16, summary formula; SwiGLU fused into GEMM1,
+ * Supported configuration).  tcgen05 grouped GEMM, persistent, TMA-fed.
+ *   xp [max_rows, H] bf16, w1 [L, 2I, H] bf16, m_indptr [L+1] (device),
+ *   h [max_rows, I] bf16 (rows >= M untouched).
+ *   max_rows bounds M (e.g. T*top_k).  H % 64 == 0, I % 64 == 0. */
+MOE_API int moe_fc1_swiglu(const moe_bf16 *xp, const moe_bf16 *w1,
+                   const int32_t *m_indptr, int max_rows, int H, int I,
+                   int num_local, moe_bf16 *h, void *stream);
+
+/* ---- S5 FC2 ------------------------------------------------------------------------
+ * y[p] = h[p] . W2[i]^T, fp32, unscaled and unrounded (cute_dsl_fused_moe_bf16,
+ * Parameters, use_fused_finalize=False).
+ *   h [max_rows, I] bf16, w2 [L, H, I] bf16, y [max_rows, H] fp32.
+ *   H % 64 == 0, I % 64 == 0. */
+MOE_API int moe_fc2(const moe_bf16 *h, const moe_bf16 *w2, const int32_t *m_indptr,
+            int max_rows, int H, int I, int num_local, float *y, void *stream);
+
+/* ---- S6 finalize --------------------------------------------------------------------
+ * out[t] = bf16_rne( sum_{j=0..top_k-1, exp_to_perm[t*top_k+j] >= 0}
+ *                    topk_w[t,j] * y[exp_to_perm[t*top_k+j]] ), summed in fp32
+ * in ascending j with no atomics, so replays are bitwise identical
+ * (cute_dsl_fused_moe_bf16, Parameters, use_fused_finalize=False).
+ *   y [*, H] fp32, exp_to_perm [T*top_k], topk_w [T, top_k] fp32,
+ *   out [T, H] bf16.  H % 8 == 0. */
+MOE_API int moe_finalize(const float *y, const int32_t *exp_to_perm,
+                 const float *topk_w, int T, int top_k, int H, moe_bf16 *out,
+                 void *stream);
+
+/* ---- S8 ragged grouped GEMM forward ---------------------------------------------------
+ * Y[offs[e-1]:offs[e]] = X[offs[e-1]:offs[e]] . W[e]^T (offs[-1] = 0), bf16
+ * output, fp32 accumulation (Cake ragged BF16 grouped GEMM, operation table,
+ * fwd).  offs [E] int32 cumulative group ends, read on the device only; groups
+ * may be empty or any size.  X [sum_m, K], W [E, N, K], Y [sum_m, N].
+ * Rows of Y outside [0, offs[E-1]) are not written.
+ * N % 64 == 0, K % 64 == 0, 1 <= E <= MOE_MAX_EXPERTS, offs[E-1] <= sum_m. */
+MOE_API int grouped_gemm_fwd(const moe_bf16 *X, const moe_bf16 *W, const int32_t *offs,
+                     int sum_m, int E, int N, int K, moe_bf16 *Y, void *stream);
+
+/* ---- whole layer (one shot) --------------------------------------------------------------
+ * Routing inputs: exactly one of
+ *   logits [T, E] fp32                      (RoutingInputMode.FromLogits), or
+ *   topk_ids [T, top_k] int32 + topk_w [T, top_k] fp32, weights normalised
+ *   by the caller                           (UnpackedPrecomputed;
+ *   cute_dsl_fused_moe_bf16, Parameters token_selected_experts /
+ *   token_final_scales).
+ * x [T, H] bf16, w1 [L, 2I, H], w2 [L, H, I], out [T, H] bf16.
+ * workspace >= moe_workspace_size(...) bytes, 256-byte aligned.
+ * T == 0 is a no-op (cute_dsl_fused_moe_bf16, Supported configuration).
+ * H % 64 == 0, I % 64 == 0. */
+MOE_API size_t moe_workspace_size(int T, int H, int I, int E, int top_k, int num_local);
+MOE_API int moe_forward(const moe_bf16 *x, const float *logits, const int32_t *topk_ids,
+                const float *topk_w, const moe_bf16 *w1, const moe_bf16 *w2,
+                int T, int H, int I, int E, int top_k, int local_offset,
+                int num_local, moe_bf16 *out, void *workspace,
+                size_t workspace_bytes, int32_t *status, void *stream);
+
+/* ---- prepared launch ------------------------------------------------------------------------
+ * Prepare once, launch many (flashinfer.experimental.cake_stepfun_moe,
+ * Prepared launches; Cake ragged BF16 grouped GEMM, Prepared launches):
+ * moe_forward_prepare validates the descriptor, lays out the workspace and
+ * encodes the TMA tensor maps (host memory only).  moe_plan_launch then only
+ * enqueues kernels: no allocation, no host synchronisation, capturable in a
+ * CUDA graph, and valid for new VALUES written into the bound buffers.
+ */
+#define MOE_PATH_AUTO 0    /* decided from the shape                         */
+#define MOE_PATH_GROUPED 1 /* route/sort/gather + tcgen05 grouped GEMMs       */
+#define MOE_PATH_DECODE 2  /* weight-streaming kernels for few tokens         */
+
+#define MOE_PLAN_STAGE_TIMING 1 /* record CUDA events around each stage     */
+
+typedef struct moe_forward_desc {
+    const moe_bf16 *x;
+    const float *logits;     /* NULL in pre-routed mode */
+    const int32_t *topk_ids; /* NULL in logits mode     */
+    const float *topk_w;     /* NULL in logits mode     */
+    const moe_bf16 *w1;
+    const moe_bf16 *w2;
+    moe_bf16 *out;
+    void *workspace;
+    size_t workspace_bytes;
+    int32_t *status;         /* optional */
+    int T, H, I, E, top_k, local_offset, num_local;
+    int path;                /* MOE_PATH_* */
+    int flags;               /* MOE_PLAN_* */
+} moe_forward_desc;
+
+typedef struct moe_plan moe_plan;
+
+/* Device pointers to the intermediates a launch leaves in the workspace
+ * (the do_finalize=False outputs of flashinfer.experimental.cake_stepfun_moe,
+ * Prepared launches, plus the sort and FC1 results). */
+typedef struct moe_plan_buffers {
+    int32_t *topk_ids;    /* [T*top_k]; the caller's in pre-routed mode   */
+    float *topk_w;        /* [T*top_k]                                     */
+    int32_t *m_indptr;    /* [L+1]                                         */
+    int32_t *perm_to_exp; /* [T*top_k]                                     */
+    int32_t *exp_to_perm; /* [T*top_k]                                     */
+    moe_bf16 *xp;         /* [T*top_k, H] (grouped path)                   */
+    moe_bf16 *h;          /* [T*top_k, I]                                  */
+    float *y;             /* [T*top_k, H]                                  */
+    int path;             /* the path the plan runs                        */
+} moe_plan_buffers;
+
+MOE_API int moe_forward_prepare(const moe_forward_desc *desc, moe_plan **plan);
+MOE_API int moe_plan_launch(moe_plan *plan, void *stream);
+MOE_API int moe_plan_buffers_get(const moe_plan *plan, moe_plan_buffers *out);
+/* Stage timing (plans prepared with MOE_PLAN_STAGE_TIMING): the number of
+ * stages and their names; moe_plan_stage_times waits for the recorded events
+ * and returns, per stage, the summed milliseconds over the launches since
+ * the last reset (at most 1024 launches are recorded). */
+MOE_API int moe_plan_stage_count(const moe_plan *plan);
+MOE_API const char *moe_plan_stage_name(const moe_plan *plan, int stage);
+MOE_API int moe_plan_stage_times(moe_plan *plan, float *ms, int max_stages,
+                         int *n_launches);
+MOE_API int moe_plan_stage_reset(moe_plan *plan);
+/* Number of kernels one moe_plan_launch enqueues (depends on the path and
+ * on the shape only). */
+MOE_API int moe_plan_kernels_per_launch(const moe_plan *plan);
+MOE_API int moe_plan_destroy(moe_plan *plan);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -1,1 +1,382 @@
-"""GB300-native routed MoE expert layer (binding placeholder)."""
+"""GB300-native (sm_103a) routed mixture-of-experts expert layer.
+
+Python binding of the C ABI declared in ``include/moe_gb300.h``.  The
+functions here carry the ABI's names and only marshal arguments: they check
+dtypes, devices and contiguity, allocate outputs with torch when the caller
+does not pass them, and hand raw device pointers plus the current CUDA stream
+to ``libmoe_gb300.so``.  Every step of the layer runs in that library's CUDA
+kernels; there is no Python or CPU fallback, and a missing library raises.
+
+    out = moe_forward(x, w1, w2, num_experts=E, top_k=k, logits=logits)
+
+Shapes: x [T, H] bf16; w1 [L, 2I, H] bf16 with the I "up" rows of each expert
+followed by its I "gate" rows; w2 [L, H, I] bf16; logits [T, E] fp32, or
+topk_ids [T, k] int32 with topk_w [T, k] fp32 (weights normalised by the
+caller).  out [T, H] bf16.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "MoEError", "library", "library_path", "moe_status_string", "moe_route", "moe_sort",
+    "moe_sort_workspace_size", "moe_gather", "moe_fc1_swiglu", "moe_fc2", "moe_finalize",
+    "grouped_gemm_fwd", "moe_workspace_size", "moe_forward", "MoEPlan", "ABI_SYMBOLS",
+    "PATH_AUTO", "PATH_GROUPED", "PATH_DECODE", "DEV_BAD_EXPERT", "DEV_TIMEOUT",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libmoe_gb300.so")
+
+PATH_AUTO, PATH_GROUPED, PATH_DECODE = 0, 1, 2
+PLAN_STAGE_TIMING = 1
+DEV_BAD_EXPERT, DEV_TIMEOUT = 1, 2
+MAX_EXPERTS, MAX_TOP_K = 1024, 16
+
+# Every function include/moe_gb300.h declares.
+ABI_SYMBOLS = [
+    "moe_status_string", "moe_abi_version", "moe_route", "moe_sort_workspace_size", "moe_sort",
+    "moe_gather", "moe_fc1_swiglu", "moe_fc2", "moe_finalize", "grouped_gemm_fwd",
+    "moe_workspace_size", "moe_forward", "moe_forward_prepare", "moe_plan_launch",
+    "moe_plan_buffers_get", "moe_plan_stage_count", "moe_plan_stage_name", "moe_plan_stage_times",
+    "moe_plan_stage_reset", "moe_plan_kernels_per_launch", "moe_plan_destroy",
+]
+
+
+class MoEError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {moe_status_string(code)} (code {code})")
+        self.code = code
+
+
+class _Desc(ctypes.Structure):
+    _fields_ = [
+        ("x", ctypes.c_void_p), ("logits", ctypes.c_void_p), ("topk_ids", ctypes.c_void_p),
+        ("topk_w", ctypes.c_void_p), ("w1", ctypes.c_void_p), ("w2", ctypes.c_void_p),
+        ("out", ctypes.c_void_p), ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("status", ctypes.c_void_p), ("T", ctypes.c_int), ("H", ctypes.c_int), ("I", ctypes.c_int),
+        ("E", ctypes.c_int), ("top_k", ctypes.c_int), ("local_offset", ctypes.c_int),
+        ("num_local", ctypes.c_int), ("path", ctypes.c_int), ("flags", ctypes.c_int),
+    ]
+
+
+class _Buffers(ctypes.Structure):
+    _fields_ = [
+        ("topk_ids", ctypes.c_void_p), ("topk_w", ctypes.c_void_p), ("m_indptr", ctypes.c_void_p),
+        ("perm_to_exp", ctypes.c_void_p), ("exp_to_perm", ctypes.c_void_p), ("xp", ctypes.c_void_p),
+        ("h", ctypes.c_void_p), ("y", ctypes.c_void_p), ("path", ctypes.c_int),
+    ]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def library():
+    """The loaded CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"{_LIB_PATH} is missing: build it with "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(_LIB_PATH)
+        P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        sig = {
+            "moe_status_string": ([I], ctypes.c_char_p),
+            "moe_abi_version": ([], I),
+            "moe_route": ([P, I, I, I, P, P, P], I),
+            "moe_sort_workspace_size": ([I, I, I], Z),
+            "moe_sort": ([P, I, I, I, I, I, P, P, P, P, Z, P, P], I),
+            "moe_gather": ([P, P, P, I, I, I, I, P, P], I),
+            "moe_fc1_swiglu": ([P, P, P, I, I, I, I, P, P], I),
+            "moe_fc2": ([P, P, P, I, I, I, I, P, P], I),
+            "moe_finalize": ([P, P, P, I, I, I, P, P], I),
+            "grouped_gemm_fwd": ([P, P, P, I, I, I, I, P, P], I),
+            "moe_workspace_size": ([I, I, I, I, I, I], Z),
+            "moe_forward": ([P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, Z, P, P], I),
+            "moe_forward_prepare": ([ctypes.POINTER(_Desc), ctypes.POINTER(P)], I),
+            "moe_plan_launch": ([P, P], I),
+            "moe_plan_buffers_get": ([P, ctypes.POINTER(_Buffers)], I),
+            "moe_plan_stage_count": ([P], I),
+            "moe_plan_stage_name": ([P, I], ctypes.c_char_p),
+            "moe_plan_stage_times": ([P, ctypes.POINTER(ctypes.c_float), I, ctypes.POINTER(I)], I),
+            "moe_plan_stage_reset": ([P], I),
+            "moe_plan_kernels_per_launch": ([P], I),
+            "moe_plan_destroy": ([P], I),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+    return _lib
+
+
+def moe_status_string(code: int) -> str:
+    return library().moe_status_string(int(code)).decode()
+
+
+def _check(rc: int, where: str):
+    if rc != 0:
+        raise MoEError(rc, where)
+
+
+def _stream(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else t.data_ptr()
+
+
+def _need(t: torch.Tensor, dtype, name: str, shape=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t
+
+
+# ----------------------------------------------------------------- stages --
+
+def moe_route(logits: torch.Tensor, top_k: int, topk_ids=None, topk_w=None):
+    """Renormalised top-k routing: (ids [T,k] int32, weights [T,k] fp32)."""
+    _need(logits, torch.float32, "logits")
+    T, E = logits.shape
+    dev = logits.device
+    topk_ids = torch.empty((T, top_k), dtype=torch.int32, device=dev) if topk_ids is None else topk_ids
+    topk_w = torch.empty((T, top_k), dtype=torch.float32, device=dev) if topk_w is None else topk_w
+    _need(topk_ids, torch.int32, "topk_ids", (T, top_k), dev)
+    _need(topk_w, torch.float32, "topk_w", (T, top_k), dev)
+    _check(library().moe_route(_ptr(logits), T, E, top_k, _ptr(topk_ids), _ptr(topk_w), _stream(dev)),
+           "moe_route")
+    return topk_ids, topk_w
+
+
+def moe_sort_workspace_size(T: int, top_k: int, num_local: int) -> int:
+    return int(library().moe_sort_workspace_size(T, top_k, num_local))
+
+
+def moe_sort(topk_ids: torch.Tensor, num_experts: int, local_offset: int = 0, num_local=None,
+             m_indptr=None, perm_to_exp=None, exp_to_perm=None, workspace=None, status=None):
+    """Stable sort of routes by local expert.
+
+    Returns (m_indptr [L+1], perm_to_exp [T*k], exp_to_perm [T*k], status [1])."""
+    _need(topk_ids, torch.int32, "topk_ids")
+    T, k = topk_ids.shape
+    dev = topk_ids.device
+    L = num_experts if num_local is None else num_local
+    R = T * k
+    m_indptr = torch.empty(L + 1, dtype=torch.int32, device=dev) if m_indptr is None else m_indptr
+    perm_to_exp = torch.empty(max(R, 1), dtype=torch.int32, device=dev) if perm_to_exp is None else perm_to_exp
+    exp_to_perm = torch.empty(max(R, 1), dtype=torch.int32, device=dev) if exp_to_perm is None else exp_to_perm
+    status = torch.zeros(1, dtype=torch.int32, device=dev) if status is None else status
+    need = moe_sort_workspace_size(T, k, L)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(library().moe_sort(_ptr(topk_ids), T, k, num_experts, local_offset, L, _ptr(m_indptr),
+                              _ptr(perm_to_exp), _ptr(exp_to_perm), _ptr(workspace), wbytes,
+                              _ptr(status), _stream(dev)), "moe_sort")
+    return m_indptr, perm_to_exp[:R], exp_to_perm[:R], status
+
+
+def moe_gather(x: torch.Tensor, perm_to_exp: torch.Tensor, m_indptr: torch.Tensor, top_k: int, xp=None):
+    _need(x, torch.bfloat16, "x")
+    T, H = x.shape
+    dev = x.device
+    L = m_indptr.numel() - 1
+    xp = torch.empty((T * top_k, H), dtype=torch.bfloat16, device=dev) if xp is None else xp
+    _need(xp, torch.bfloat16, "xp", device=dev)
+    _check(library().moe_gather(_ptr(x), _ptr(perm_to_exp), _ptr(m_indptr), T, H, top_k, L, _ptr(xp),
+                                _stream(dev)), "moe_gather")
+    return xp
+
+
+def moe_fc1_swiglu(xp: torch.Tensor, w1: torch.Tensor, m_indptr: torch.Tensor, h=None):
+    _need(xp, torch.bfloat16, "xp")
+    _need(w1, torch.bfloat16, "w1")
+    _need(m_indptr, torch.int32, "m_indptr")
+    rows, H = xp.shape
+    L, twoI, H2 = w1.shape
+    if H2 != H or twoI % 2:
+        raise ValueError("w1 must be [L, 2I, H]")
+    I = twoI // 2
+    h = torch.empty((rows, I), dtype=torch.bfloat16, device=xp.device) if h is None else h
+    _need(h, torch.bfloat16, "h", (rows, I), xp.device)
+    _check(library().moe_fc1_swiglu(_ptr(xp), _ptr(w1), _ptr(m_indptr), rows, H, I, L, _ptr(h),
+                                    _stream(xp.device)), "moe_fc1_swiglu")
+    return h
+
+
+def moe_fc2(h: torch.Tensor, w2: torch.Tensor, m_indptr: torch.Tensor, y=None):
+    _need(h, torch.bfloat16, "h")
+    _need(w2, torch.bfloat16, "w2")
+    _need(m_indptr, torch.int32, "m_indptr")
+    rows, I = h.shape
+    L, H, I2 = w2.shape
+    if I2 != I:
+        raise ValueError("w2 must be [L, H, I]")
+    y = torch.empty((rows, H), dtype=torch.float32, device=h.device) if y is None else y
+    _need(y, torch.float32, "y", (rows, H), h.device)
+    _check(library().moe_fc2(_ptr(h), _ptr(w2), _ptr(m_indptr), rows, H, I, L, _ptr(y),
+                             _stream(h.device)), "moe_fc2")
+    return y
+
+
+def moe_finalize(y: torch.Tensor, exp_to_perm: torch.Tensor, topk_w: torch.Tensor, out=None):
+    _need(y, torch.float32, "y")
+    _need(exp_to_perm, torch.int32, "exp_to_perm")
+    _need(topk_w, torch.float32, "topk_w")
+    T, k = topk_w.shape
+    H = y.shape[1]
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=y.device) if out is None else out
+    _need(out, torch.bfloat16, "out", (T, H), y.device)
+    _check(library().moe_finalize(_ptr(y), _ptr(exp_to_perm), _ptr(topk_w), T, k, H, _ptr(out),
+                                  _stream(y.device)), "moe_finalize")
+    return out
+
+
+def grouped_gemm_fwd(X: torch.Tensor, W: torch.Tensor, offs: torch.Tensor, Y=None):
+    """Ragged grouped GEMM forward: Y[group e] = X[group e] @ W[e].T (bf16)."""
+    _need(X, torch.bfloat16, "X")
+    _need(W, torch.bfloat16, "W")
+    _need(offs, torch.int32, "offs")
+    sum_m, K = X.shape
+    E, N, K2 = W.shape
+    if K2 != K or offs.numel() != E:
+        raise ValueError("shapes: X [sum_m, K], W [E, N, K], offs [E]")
+    Y = torch.empty((sum_m, N), dtype=torch.bfloat16, device=X.device) if Y is None else Y
+    _need(Y, torch.bfloat16, "Y", (sum_m, N), X.device)
+    _check(library().grouped_gemm_fwd(_ptr(X), _ptr(W), _ptr(offs), sum_m, E, N, K, _ptr(Y),
+                                      _stream(X.device)), "grouped_gemm_fwd")
+    return Y
+
+
+# ------------------------------------------------------------ whole layer --
+
+def moe_workspace_size(T: int, H: int, I: int, E: int, top_k: int, num_local: int | None = None) -> int:
+    return int(library().moe_workspace_size(T, H, I, E, top_k, E if num_local is None else num_local))
+
+
+def _layer_args(x, w1, w2, num_experts, top_k, logits, topk_ids, topk_w, local_offset, out):
+    _need(x, torch.bfloat16, "x")
+    dev = x.device
+    T, H = x.shape
+    _need(w1, torch.bfloat16, "w1", device=dev)
+    _need(w2, torch.bfloat16, "w2", device=dev)
+    L, twoI, H1 = w1.shape
+    I = twoI // 2
+    if H1 != H or tuple(w2.shape) != (L, H, I):
+        raise ValueError("w1 must be [L, 2I, H] and w2 [L, H, I]")
+    if logits is not None:
+        _need(logits, torch.float32, "logits", (T, num_experts), dev)
+    if topk_ids is not None:
+        _need(topk_ids, torch.int32, "topk_ids", (T, top_k), dev)
+    if topk_w is not None:
+        _need(topk_w, torch.float32, "topk_w", (T, top_k), dev)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev) if out is None else out
+    _need(out, torch.bfloat16, "out", (T, H), dev)
+    return T, H, I, L, out
+
+
+def moe_forward(x, w1, w2, num_experts: int, top_k: int, logits=None, topk_ids=None, topk_w=None,
+                local_offset: int = 0, out=None, workspace=None, status=None):
+    """One-shot layer forward (route or pre-routed -> sort -> FC1 -> FC2 -> finalize)."""
+    T, H, I, L, out = _layer_args(x, w1, w2, num_experts, top_k, logits, topk_ids, topk_w,
+                                  local_offset, out)
+    dev = x.device
+    need = moe_workspace_size(T, H, I, num_experts, top_k, L)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+    _check(library().moe_forward(_ptr(x), _ptr(logits), _ptr(topk_ids), _ptr(topk_w), _ptr(w1), _ptr(w2),
+                                 T, H, I, num_experts, top_k, local_offset, L, _ptr(out), _ptr(workspace),
+                                 workspace.numel(), _ptr(status), _stream(dev)), "moe_forward")
+    return out
+
+
+class MoEPlan:
+    """Prepared launch: validate and lay out once, then ``launch()`` only
+    enqueues kernels (no allocation, no host synchronisation; capturable in a
+    CUDA graph).  The plan binds the given tensors; write new values into them
+    between launches."""
+
+    def __init__(self, x, w1, w2, num_experts: int, top_k: int, logits=None, topk_ids=None, topk_w=None,
+                 local_offset: int = 0, out=None, workspace=None, status=None, path: int = PATH_AUTO,
+                 stage_timing: bool = False):
+        T, H, I, L, out = _layer_args(x, w1, w2, num_experts, top_k, logits, topk_ids, topk_w,
+                                      local_offset, out)
+        dev = x.device
+        need = moe_workspace_size(T, H, I, num_experts, top_k, L)
+        if workspace is None:
+            workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+        if status is None:
+            status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self._keep = (x, w1, w2, logits, topk_ids, topk_w, out, workspace, status)
+        self.x, self.w1, self.w2, self.logits, self.topk_ids, self.topk_w = x, w1, w2, logits, topk_ids, topk_w
+        self.out, self.workspace, self.status = out, workspace, status
+        self.T, self.H, self.I, self.E, self.top_k, self.L = T, H, I, num_experts, top_k, L
+        self.device = dev
+        d = _Desc(x=_ptr(x), logits=_ptr(logits), topk_ids=_ptr(topk_ids), topk_w=_ptr(topk_w),
+                  w1=_ptr(w1), w2=_ptr(w2), out=_ptr(out), workspace=_ptr(workspace),
+                  workspace_bytes=workspace.numel(), status=_ptr(status), T=T, H=H, I=I, E=num_experts,
+                  top_k=top_k, local_offset=local_offset, num_local=L, path=path,
+                  flags=PLAN_STAGE_TIMING if stage_timing else 0)
+        handle = ctypes.c_void_p()
+        _check(library().moe_forward_prepare(ctypes.byref(d), ctypes.byref(handle)), "moe_forward_prepare")
+        self._h = handle
+
+    def launch(self, stream=None):
+        s = _stream(self.device) if stream is None else (stream.cuda_stream if hasattr(stream, "cuda_stream") else stream)
+        _check(library().moe_plan_launch(self._h, s), "moe_plan_launch")
+        return self.out
+
+    def buffers(self) -> dict:
+        b = _Buffers()
+        _check(library().moe_plan_buffers_get(self._h, ctypes.byref(b)), "moe_plan_buffers_get")
+        return {name: getattr(b, name) for name, _ in _Buffers._fields_}
+
+    def stage_names(self):
+        lib = library()
+        return [lib.moe_plan_stage_name(self._h, i).decode() for i in range(lib.moe_plan_stage_count(self._h))]
+
+    def stage_times(self):
+        """(per-stage summed ms, launches counted) since the last reset."""
+        names = self.stage_names()
+        arr = (ctypes.c_float * len(names))()
+        n = ctypes.c_int(0)
+        _check(library().moe_plan_stage_times(self._h, arr, len(names), ctypes.byref(n)), "moe_plan_stage_times")
+        return dict(zip(names, list(arr))), n.value
+
+    def kernels_per_launch(self) -> int:
+        return int(library().moe_plan_kernels_per_launch(self._h))
+
+    def stage_reset(self):
+        _check(library().moe_plan_stage_reset(self._h), "moe_plan_stage_reset")
+
+    def close(self):
+        if getattr(self, "_h", None):
+            library().moe_plan_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,457 @@
+// The C ABI (include/moe_gb300.h): argument checks, workspace layout, the
+// prepared launch and the one-shot entry points.  Host code only; every step
+// of the layer runs in the kernels of route.cu, sort.cu, rows.cu and gemm.cu.
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "internal.h"
+#include "moe_gb300.h"
+
+namespace moe {
+
+int device_sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 1;
+  }
+  return n;
+}
+
+namespace {
+
+// The kernels are built for sm_103a only.
+int check_device() {
+  static int cached = 1;  // 1 = unknown
+  if (cached == 1) {
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return MOE_ERR_DEVICE;
+    }
+    cached = (major == 10 && minor == 3) ? MOE_OK : MOE_ERR_DEVICE;
+  }
+  return cached;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct WsLayout {
+  size_t ids, w, m_indptr, p2e, e2p, sort_ws, xp, h, y, total;
+};
+
+WsLayout ws_layout(long T, int H, int I, int k, int L) {
+  WsLayout o;
+  const size_t R = (size_t)T * (size_t)k;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += align_up(bytes > 0 ? bytes : 1, 256);
+    return at;
+  };
+  o.ids = take(R * 4);
+  o.w = take(R * 4);
+  o.m_indptr = take(((size_t)L + 1) * 4);
+  o.p2e = take(R * 4);
+  o.e2p = take(R * 4);
+  o.sort_ws = take(sort_workspace_bytes((long)R, L));
+  o.xp = take(R * (size_t)H * 2);
+  o.h = take(R * (size_t)I * 2);
+  o.y = take(R * (size_t)H * 4);
+  o.total = off;
+  return o;
+}
+
+int check_layer_shape(int T, int H, int I, int E, int k, int off, int L) {
+  if (T < 0 || H <= 0 || I <= 0 || E <= 0 || E > MOE_MAX_EXPERTS) return MOE_ERR_SHAPE;
+  if (k < 1 || k > MOE_MAX_TOP_K || k > E) return MOE_ERR_SHAPE;
+  if (off < 0 || L < 1 || (long)off + L > E) return MOE_ERR_SHAPE;
+  if (H % 64 != 0 || I % 64 != 0) return MOE_ERR_SHAPE;
+  if ((long)T * k > (1L << 30)) return MOE_ERR_SHAPE;
+  return MOE_OK;
+}
+
+enum Stage { kRoute = 0, kSort, kGather, kFc1, kFc2, kFinalize, kNumStages };
+const char *kStageNames[kNumStages] = {"route", "sort", "gather", "fc1_swiglu", "fc2", "finalize"};
+constexpr int kTimingRing = 512;
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+struct moe_plan {
+  moe_forward_desc d;
+  int path;
+  bool logits_mode;
+  long R;
+  int32_t *ids;
+  float *w;
+  int32_t *m_indptr, *p2e, *e2p, *sort_ws;
+  uint16_t *xp, *h;
+  float *y;
+  GemmPlan fc1, fc2;
+  bool timing;
+  cudaEvent_t (*ev)[kNumStages + 1];
+  long n_recorded;
+};
+
+extern "C" {
+
+const char *moe_status_string(int code) {
+  switch (code) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_NULL: return "a required pointer is NULL";
+    case MOE_ERR_SHAPE: return "a size is out of range or not a supported multiple";
+    case MOE_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+    case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+    case MOE_ERR_MODE: return "give logits, or topk_ids with topk_w, not both or neither";
+    case MOE_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";
+    case MOE_ERR_DEVICE: return "no CUDA device, or the device is not sm_103 (GB300/B300)";
+    case MOE_ERR_TENSOR_MAP: return "the driver rejected a TMA tensor map";
+    case MOE_ERR_STATE: return "call not valid for this plan";
+    default: return "unknown status code";
+  }
+}
+
+int moe_abi_version(void) { return 100; }
+
+int moe_route(const float *logits, int T, int E, int top_k, int32_t *topk_ids, float *topk_w,
+              void *stream) {
+  if (T < 0 || E < 1 || E > MOE_MAX_EXPERTS || top_k < 1 || top_k > MOE_MAX_TOP_K || top_k > E)
+    return MOE_ERR_SHAPE;
+  if (T == 0) return MOE_OK;
+  if (!logits || !topk_ids || !topk_w) return MOE_ERR_NULL;
+  if (int rc = check_device()) return rc;
+  Launch l;
+  l.stream = static_cast<cudaStream_t>(stream);
+  return cuda_rc(launch_route(logits, T, E, top_k, topk_ids, topk_w, l));
+}
+
+size_t moe_sort_workspace_size(int T, int top_k, int num_local) {
+  if (T < 0 || top_k < 1 || num_local < 1) return 0;
+  return sort_workspace_bytes((long)T * top_k, num_local);
+}
+
+int moe_sort(const int32_t *topk_ids, int T, int top_k, int E, int local_offset, int num_local,
+             int32_t *m_indptr, int32_t *perm_to_exp, int32_t *exp_to_perm, void *workspace,
+             size_t workspace_bytes, int32_t *status, void *stream) {
+  if (T < 0 || top_k < 1 || top_k > MOE_MAX_TOP_K || E < 1 || E > MOE_MAX_EXPERTS ||
+      local_offset < 0 || num_local < 1 || (long)local_offset + num_local > E ||
+      (long)T * top_k > (1L << 30))
+    return MOE_ERR_SHAPE;
+  if (!m_indptr) return MOE_ERR_NULL;
+  if (int rc = check_device()) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (status && cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
+  const long R = (long)T * top_k;
+  if (R == 0) return cuda_rc(cudaMemsetAsync(m_indptr, 0, ((size_t)num_local + 1) * 4, s));
+  if (!topk_ids || !perm_to_exp || !exp_to_perm) return MOE_ERR_NULL;
+  const size_t need = sort_workspace_bytes(R, num_local);
+  if (need > 0 && (!workspace || workspace_bytes < need)) return MOE_ERR_WORKSPACE;
+  Launch l;
+  l.stream = s;
+  return cuda_rc(launch_sort(topk_ids, R, E, local_offset, num_local, m_indptr, perm_to_exp,
+                             exp_to_perm, static_cast<int32_t *>(workspace), status, l));
+}
+
+int moe_gather(const moe_bf16 *x, const int32_t *perm_to_exp, const int32_t *m_indptr, int T,
+               int H, int top_k, int num_local, moe_bf16 *xp, void *stream) {
+  if (T < 0 || H <= 0 || H % 8 != 0 || top_k < 1 || top_k > MOE_MAX_TOP_K || num_local < 1)
+    return MOE_ERR_SHAPE;
+  if (T == 0) return MOE_OK;
+  if (!x || !perm_to_exp || !m_indptr || !xp) return MOE_ERR_NULL;
+  if (!aligned16(x) || !aligned16(xp)) return MOE_ERR_ALIGN;
+  if (int rc = check_device()) return rc;
+  Launch l;
+  l.stream = static_cast<cudaStream_t>(stream);
+  return cuda_rc(launch_gather(x, perm_to_exp, m_indptr + num_local, H, top_k, (long)T * top_k, xp, l));
+}
+
+int moe_fc1_swiglu(const moe_bf16 *xp, const moe_bf16 *w1, const int32_t *m_indptr, int max_rows,
+                   int H, int I, int num_local, moe_bf16 *h, void *stream) {
+  if (max_rows < 0 || H <= 0 || I <= 0 || H % 64 || I % 64 || num_local < 1 ||
+      num_local > MOE_MAX_EXPERTS)
+    return MOE_ERR_SHAPE;
+  if (max_rows == 0) return MOE_OK;
+  if (!xp || !w1 || !m_indptr || !h) return MOE_ERR_NULL;
+  if (!aligned16(xp) || !aligned16(w1) || !aligned16(h)) return MOE_ERR_ALIGN;
+  if (int rc = check_device()) return rc;
+  GemmPlan p;
+  if (int rc = gemm_prepare(p, Epi::kSwiGLU, xp, max_rows, w1, num_local, 2 * I, H, I,
+                            m_indptr + 1, max_rows, h, nullptr))
+    return rc;
+  Launch l;
+  l.stream = static_cast<cudaStream_t>(stream);
+  return cuda_rc(launch_gemm(p, l));
+}
+
+int moe_fc2(const moe_bf16 *h, const moe_bf16 *w2, const int32_t *m_indptr, int max_rows, int H,
+            int I, int num_local, float *y, void *stream) {
+  if (max_rows < 0 || H <= 0 || I <= 0 || H % 64 || I % 64 || num_local < 1 ||
+      num_local > MOE_MAX_EXPERTS)
+    return MOE_ERR_SHAPE;
+  if (max_rows == 0) return MOE_OK;
+  if (!h || !w2 || !m_indptr || !y) return MOE_ERR_NULL;
+  if (!aligned16(h) || !aligned16(w2) || !aligned16(y)) return MOE_ERR_ALIGN;
+  if (int rc = check_device()) return rc;
+  GemmPlan p;
+  if (int rc = gemm_prepare(p, Epi::kF32, h, max_rows, w2, num_local, H, I, H, m_indptr + 1,
+                            max_rows, y, nullptr))
+    return rc;
+  Launch l;
+  l.stream = static_cast<cudaStream_t>(stream);
+  return cuda_rc(launch_gemm(p, l));
+}
+
+int moe_finalize(const float *y, const int32_t *exp_to_perm, const float *topk_w, int T,
+                 int top_k, int H, moe_bf16 *out, void *stream) {
+  if (T < 0 || H <= 0 || H % 8 != 0 || top_k < 1 || top_k > MOE_MAX_TOP_K) return MOE_ERR_SHAPE;
+  if (T == 0) return MOE_OK;
+  if (!y || !exp_to_perm || !topk_w || !out) return MOE_ERR_NULL;
+  if (!aligned16(y) || !aligned16(out)) return MOE_ERR_ALIGN;
+  if (int rc = check_device()) return rc;
+  Launch l;
+  l.stream = static_cast<cudaStream_t>(stream);
+  return cuda_rc(launch_finalize(y, exp_to_perm, topk_w, T, top_k, H, out, l));
+}
+
+int grouped_gemm_fwd(const moe_bf16 *X, const moe_bf16 *W, const int32_t *offs, int sum_m, int E,
+                     int N, int K, moe_bf16 *Y, void *stream) {
+  if (sum_m < 0 || E < 1 || E > MOE_MAX_EXPERTS || N <= 0 || K <= 0 || N % 64 || K % 64)
+    return MOE_ERR_SHAPE;
+  if (sum_m == 0) return MOE_OK;
+  if (!X || !W || !offs || !Y) return MOE_ERR_NULL;
+  if (!aligned16(X) || !aligned16(W) || !aligned16(Y)) return MOE_ERR_ALIGN;
+  if (int rc = check_device()) return rc;
+  GemmPlan p;
+  if (int rc = gemm_prepare(p, Epi::kBf16, X, sum_m, W, E, N, K, N, offs, sum_m, Y, nullptr))
+    return rc;
+  Launch l;
+  l.stream = static_cast<cudaStream_t>(stream);
+  return cuda_rc(launch_gemm(p, l));
+}
+
+size_t moe_workspace_size(int T, int H, int I, int E, int top_k, int num_local) {
+  if (check_layer_shape(T, H, I, E, top_k, 0, num_local) != MOE_OK) return 0;
+  return ws_layout(T, H, I, top_k, num_local).total;
+}
+
+int moe_forward_prepare(const moe_forward_desc *desc, moe_plan **plan_out) {
+  if (!desc || !plan_out) return MOE_ERR_NULL;
+  *plan_out = nullptr;
+  const moe_forward_desc &d = *desc;
+  if (int rc = check_layer_shape(d.T, d.H, d.I, d.E, d.top_k, d.local_offset, d.num_local))
+    return rc;
+  const bool logits_mode = d.logits != nullptr;
+  const bool routed_mode = d.topk_ids != nullptr || d.topk_w != nullptr;
+  if (logits_mode == routed_mode) return MOE_ERR_MODE;
+  if (routed_mode && (!d.topk_ids || !d.topk_w)) return MOE_ERR_MODE;
+  if (d.path < MOE_PATH_AUTO || d.path > MOE_PATH_DECODE) return MOE_ERR_SHAPE;
+  if (d.T > 0) {
+    if (!d.x || !d.w1 || !d.w2 || !d.out) return MOE_ERR_NULL;
+    if (!aligned16(d.x) || !aligned16(d.w1) || !aligned16(d.w2) || !aligned16(d.out))
+      return MOE_ERR_ALIGN;
+  }
+  const WsLayout lay = ws_layout(d.T, d.H, d.I, d.top_k, d.num_local);
+  if (d.T > 0) {
+    if (!d.workspace || d.workspace_bytes < lay.total) return MOE_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(d.workspace) & 255u) != 0) return MOE_ERR_ALIGN;
+    if (int rc = check_device()) return rc;
+  }
+  moe_plan *p = new (std::nothrow) moe_plan();
+  if (!p) return MOE_ERR_CUDA;
+  p->d = d;
+  p->logits_mode = logits_mode;
+  p->path = MOE_PATH_GROUPED;
+  p->R = (long)d.T * d.top_k;
+  unsigned char *ws = static_cast<unsigned char *>(d.workspace);
+  if (d.T > 0) {
+    p->ids = logits_mode ? reinterpret_cast<int32_t *>(ws + lay.ids) : const_cast<int32_t *>(d.topk_ids);
+    p->w = logits_mode ? reinterpret_cast<float *>(ws + lay.w) : const_cast<float *>(d.topk_w);
+    p->m_indptr = reinterpret_cast<int32_t *>(ws + lay.m_indptr);
+    p->p2e = reinterpret_cast<int32_t *>(ws + lay.p2e);
+    p->e2p = reinterpret_cast<int32_t *>(ws + lay.e2p);
+    p->sort_ws = reinterpret_cast<int32_t *>(ws + lay.sort_ws);
+    p->xp = reinterpret_cast<uint16_t *>(ws + lay.xp);
+    p->h = reinterpret_cast<uint16_t *>(ws + lay.h);
+    p->y = reinterpret_cast<float *>(ws + lay.y);
+    int rc = gemm_prepare(p->fc1, Epi::kSwiGLU, p->xp, p->R, d.w1, d.num_local, 2 * d.I, d.H, d.I,
+                          p->m_indptr + 1, p->R, p->h, d.status);
+    if (rc == MOE_OK)
+      rc = gemm_prepare(p->fc2, Epi::kF32, p->h, p->R, d.w2, d.num_local, d.H, d.I, d.H,
+                        p->m_indptr + 1, p->R, p->y, d.status);
+    if (rc != MOE_OK) {
+      delete p;
+      return rc;
+    }
+  }
+  p->timing = (d.flags & MOE_PLAN_STAGE_TIMING) != 0 && d.T > 0;
+  if (p->timing) {
+    p->ev = new (std::nothrow) cudaEvent_t[kTimingRing][kNumStages + 1];
+    if (!p->ev) {
+      delete p;
+      return MOE_ERR_CUDA;
+    }
+    for (int i = 0; i < kTimingRing; ++i)
+      for (int s = 0; s <= kNumStages; ++s)
+        if (cudaEventCreate(&p->ev[i][s]) != cudaSuccess) {
+          // leave the plan consistent for destroy
+          for (int j = 0; j <= i; ++j)
+            for (int q = 0; q <= kNumStages; ++q)
+              if (j < i || q < s) cudaEventDestroy(p->ev[j][q]);
+          delete[] p->ev;
+          delete p;
+          return MOE_ERR_CUDA;
+        }
+  }
+  *plan_out = p;
+  return MOE_OK;
+}
+
+int moe_plan_launch(moe_plan *p, void *stream) {
+  if (!p) return MOE_ERR_NULL;
+  const moe_forward_desc &d = p->d;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (d.status && cudaMemsetAsync(d.status, 0, sizeof(int32_t), s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (d.T == 0) return MOE_OK;
+  Launch l;
+  l.stream = s;
+  l.pdl = !p->timing;
+  cudaEvent_t *ev = p->timing ? p->ev[p->n_recorded % kTimingRing] : nullptr;
+  auto mark = [&](int stage) -> bool {
+    return !ev || cudaEventRecord(ev[stage], s) == cudaSuccess;
+  };
+  if (!mark(kRoute)) return MOE_ERR_CUDA;
+  if (p->logits_mode) {
+    if (launch_route(d.logits, d.T, d.E, d.top_k, p->ids, p->w, l) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  if (!mark(kSort)) return MOE_ERR_CUDA;
+  if (launch_sort(p->ids, p->R, d.E, d.local_offset, d.num_local, p->m_indptr, p->p2e, p->e2p,
+                  p->sort_ws, d.status, l) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (!mark(kGather)) return MOE_ERR_CUDA;
+  if (launch_gather(d.x, p->p2e, p->m_indptr + d.num_local, d.H, d.top_k, p->R, p->xp, l) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (!mark(kFc1)) return MOE_ERR_CUDA;
+  if (launch_gemm(p->fc1, l) != cudaSuccess) return MOE_ERR_CUDA;
+  if (!mark(kFc2)) return MOE_ERR_CUDA;
+  if (launch_gemm(p->fc2, l) != cudaSuccess) return MOE_ERR_CUDA;
+  if (!mark(kFinalize)) return MOE_ERR_CUDA;
+  if (launch_finalize(p->y, p->e2p, p->w, d.T, d.top_k, d.H, d.out, l) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (!mark(kNumStages)) return MOE_ERR_CUDA;
+  if (ev) ++p->n_recorded;
+  return MOE_OK;
+}
+
+int moe_plan_buffers_get(const moe_plan *p, moe_plan_buffers *out) {
+  if (!p || !out) return MOE_ERR_NULL;
+  out->topk_ids = p->ids;
+  out->topk_w = p->w;
+  out->m_indptr = p->m_indptr;
+  out->perm_to_exp = p->p2e;
+  out->exp_to_perm = p->e2p;
+  out->xp = p->xp;
+  out->h = p->h;
+  out->y = p->y;
+  out->path = p->path;
+  return MOE_OK;
+}
+
+int moe_plan_stage_count(const moe_plan *p) { return p ? kNumStages : 0; }
+
+const char *moe_plan_stage_name(const moe_plan *p, int stage) {
+  if (!p || stage < 0 || stage >= kNumStages) return "";
+  return kStageNames[stage];
+}
+
+int moe_plan_stage_times(moe_plan *p, float *ms, int max_stages, int *n_launches) {
+  if (!p || !ms) return MOE_ERR_NULL;
+  if (!p->timing) return MOE_ERR_STATE;
+  const long n = p->n_recorded < kTimingRing ? p->n_recorded : kTimingRing;
+  const int ns = max_stages < kNumStages ? max_stages : kNumStages;
+  for (int s = 0; s < ns; ++s) ms[s] = 0.f;
+  for (long i = 0; i < n; ++i) {
+    const long slot = (p->n_recorded - 1 - i) % kTimingRing;
+    if (cudaEventSynchronize(p->ev[slot][kNumStages]) != cudaSuccess) return MOE_ERR_CUDA;
+    for (int s = 0; s < ns; ++s) {
+      float t = 0.f;
+      if (cudaEventElapsedTime(&t, p->ev[slot][s], p->ev[slot][s + 1]) != cudaSuccess)
+        return MOE_ERR_CUDA;
+      ms[s] += t;
+    }
+  }
+  if (n_launches) *n_launches = (int)n;
+  return MOE_OK;
+}
+
+int moe_plan_kernels_per_launch(const moe_plan *p) {
+  if (!p || p->d.T == 0) return 0;
+  int n = p->logits_mode ? 1 : 0;                       // route
+  n += p->R <= kSortSingleMax ? 1 : 3;                  // sort
+  n += 1 + 1 + 1 + 1;                                   // gather, fc1, fc2, finalize
+  return n;
+}
+
+int moe_plan_stage_reset(moe_plan *p) {
+  if (!p) return MOE_ERR_NULL;
+  p->n_recorded = 0;
+  return MOE_OK;
+}
+
+int moe_plan_destroy(moe_plan *p) {
+  if (!p) return MOE_OK;
+  if (p->timing && p->ev) {
+    for (int i = 0; i < kTimingRing; ++i)
+      for (int s = 0; s <= kNumStages; ++s) cudaEventDestroy(p->ev[i][s]);
+    delete[] p->ev;
+  }
+  delete p;
+  return MOE_OK;
+}
+
+int moe_forward(const moe_bf16 *x, const float *logits, const int32_t *topk_ids,
+                const float *topk_w, const moe_bf16 *w1, const moe_bf16 *w2, int T, int H, int I,
+                int E, int top_k, int local_offset, int num_local, moe_bf16 *out, void *workspace,
+                size_t workspace_bytes, int32_t *status, void *stream) {
+  moe_forward_desc d;
+  std::memset(&d, 0, sizeof d);
+  d.x = x;
+  d.logits = logits;
+  d.topk_ids = topk_ids;
+  d.topk_w = topk_w;
+  d.w1 = w1;
+  d.w2 = w2;
+  d.out = out;
+  d.workspace = workspace;
+  d.workspace_bytes = workspace_bytes;
+  d.status = status;
+  d.T = T;
+  d.H = H;
+  d.I = I;
+  d.E = E;
+  d.top_k = top_k;
+  d.local_offset = local_offset;
+  d.num_local = num_local;
+  d.path = MOE_PATH_AUTO;
+  moe_plan *p = nullptr;
+  int rc = moe_forward_prepare(&d, &p);
+  if (rc != MOE_OK) return rc;
+  rc = moe_plan_launch(p, stream);
+  moe_plan_destroy(p);
+  return rc;
+}
+
+}  // extern "C"

@@ -1,0 +1,71 @@
+// Internal launchers shared by the C ABI (api.cu) and the kernel files.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "moe_gb300.h"
+
+namespace moe {
+
+// Launch settings shared by every launcher: the stream and whether the kernel
+// may start under programmatic dependent launch (its prologue overlapping the
+// previous kernel's tail; it waits for the predecessor before reading).
+struct Launch {
+  cudaStream_t stream = nullptr;
+  bool pdl = false;
+};
+
+int device_sm_count();
+
+// S1 ---------------------------------------------------------------------------
+cudaError_t launch_route(const float *logits, int T, int E, int k, int32_t *ids, float *w,
+                         const Launch &l);
+
+// S2 ---------------------------------------------------------------------------
+// Routes per CTA of the multi-CTA sort, and the largest route count the
+// single-CTA sort handles.
+constexpr int kSortChunk = 4096;
+constexpr int kSortSingleMax = 2048;
+size_t sort_workspace_bytes(long routes, int L);
+cudaError_t launch_sort(const int32_t *ids, long routes, int E, int off, int L, int32_t *m_indptr,
+                        int32_t *p2e, int32_t *e2p, int32_t *ws, int32_t *status,
+                        const Launch &l);
+
+// S3 / S6 -----------------------------------------------------------------------
+cudaError_t launch_gather(const uint16_t *x, const int32_t *p2e, const int32_t *m_total, int H,
+                          int k, long max_rows, uint16_t *xp, const Launch &l);
+cudaError_t launch_finalize(const float *y, const int32_t *e2p, const float *w, int T, int k,
+                            int H, uint16_t *out, const Launch &l);
+
+// S4 / S5 / S8: persistent tcgen05 grouped GEMM --------------------------------
+enum class Epi : int { kBf16 = 0, kSwiGLU = 1, kF32 = 2 };
+
+struct GemmPlan {
+  CUtensorMap map_a;            // A [rows, K] bf16, box {64, 128}
+  CUtensorMap map_b;            // B [G * b_rows, K] bf16, box {64, box_b}
+  const int32_t *group_end;     // [G] cumulative group ends (device)
+  int G = 0;                    // groups
+  int K = 0;                    // reduction length
+  int n_out = 0;                // output columns per row (N, or I for SwiGLU)
+  int b_rows = 0;               // B rows per group (N, or 2I for SwiGLU)
+  int bn = 0;                   // MMA N (total B rows per tile)
+  int n_tiles = 0;              // output column tiles
+  int m_major = 0;              // tile raster: m-tiles innermost (0) or n (1)
+  long max_rows = 0;            // bound on total rows (grid sizing)
+  void *out = nullptr;          // bf16 or fp32 output, row stride n_out
+  Epi epi = Epi::kBf16;
+  int grid = 0;
+  size_t smem = 0;
+  int32_t *status = nullptr;
+};
+
+// Encodes the tensor maps and picks tile shapes; host only.
+int gemm_prepare(GemmPlan &p, Epi epi, const uint16_t *A, long a_rows, const uint16_t *B, int G,
+                 int b_rows, int K, int n_out, const int32_t *group_end, long max_rows, void *out,
+                 int32_t *status);
+cudaError_t launch_gemm(const GemmPlan &p, const Launch &l);
+
+}  // namespace moe

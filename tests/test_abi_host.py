@@ -1,0 +1,86 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every function include/moe_gb300.h declares, and rejects bad arguments with
+the documented codes before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mixture_experts_expert_router_gb300 as moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_gb300.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mixture_experts_expert_router_gb300 import _build
+    _build.build()
+    return moe.library()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^MOE_API\s+[^;(]*?\b([A-Za-z_][A-Za-z0-9_]*)\s*\(", text, re.M)))
+
+
+def test_header_lists_functions():
+    names = header_functions()
+    assert "moe_forward" in names and "grouped_gemm_fwd" in names and len(names) >= 20
+    assert sorted(moe.ABI_SYMBOLS) == names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+    raw = ctypes.CDLL(moe.library_path())
+    for name in header_functions():
+        getattr(raw, name)
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5, -6, -7, -8, -9):
+        s = moe.moe_status_string(code)
+        assert s and s != "unknown status code"
+    assert moe.moe_status_string(-99) == "unknown status code"
+    assert lib.moe_abi_version() == 100
+
+
+def test_argument_errors_before_device(lib):
+    # shape errors are reported before any CUDA call
+    assert lib.moe_route(None, 4, 8, 9, None, None, None) == -2          # top_k > E
+    assert lib.moe_route(None, 4, 8, 17, None, None, None) == -2         # top_k > 16
+    assert lib.moe_route(None, 0, 8, 2, None, None, None) == 0           # T == 0: no-op
+    assert lib.moe_route(None, 3, 8, 2, None, None, None) == -1          # null pointers
+    assert lib.moe_sort(None, 4, 2, 8, 6, 4, None, None, None, None, 0, None, None) == -2  # shard past E
+    assert lib.grouped_gemm_fwd(None, None, None, 16, 4, 100, 64, None, None) == -2      # N % 64
+    assert lib.grouped_gemm_fwd(None, None, None, 0, 4, 128, 64, None, None) == 0        # empty
+    assert lib.moe_fc1_swiglu(None, None, None, 8, 96, 64, 2, None, None) == -2          # H % 64
+    assert lib.moe_finalize(None, None, None, 4, 2, 12, None, None) == -2                # H % 8
+
+
+def test_workspace_size_and_prepare_errors(lib):
+    assert moe.moe_workspace_size(16, 128, 128, 4, 2) > 0
+    assert moe.moe_workspace_size(16, 100, 128, 4, 2) == 0      # H % 64 != 0
+    # more rows need more workspace
+    assert moe.moe_workspace_size(64, 128, 128, 4, 2) > moe.moe_workspace_size(16, 128, 128, 4, 2)
+    d = moe._Desc(T=4, H=128, I=128, E=4, top_k=2, local_offset=0, num_local=4)
+    h = ctypes.c_void_p()
+    assert lib.moe_forward_prepare(ctypes.byref(d), ctypes.byref(h)) == -5   # no routing input
+    d.logits = 16
+    d.topk_ids = 16
+    d.topk_w = 16
+    assert lib.moe_forward_prepare(ctypes.byref(d), ctypes.byref(h)) == -5   # both modes
+    d.topk_ids = None
+    d.topk_w = None
+    assert lib.moe_forward_prepare(ctypes.byref(d), ctypes.byref(h)) == -1   # null tensors
+    d.x = d.w1 = d.w2 = d.out = 256
+    d.workspace = None
+    assert lib.moe_forward_prepare(ctypes.byref(d), ctypes.byref(h)) == -4   # no workspace
+    d.x = 8
+    assert lib.moe_forward_prepare(ctypes.byref(d), ctypes.byref(h)) == -3   # misaligned
+    d.top_k = 5
+    assert lib.moe_forward_prepare(ctypes.byref(d), ctypes.byref(h)) == -2   # top_k > E
+    assert lib.moe_plan_launch(None, None) == -1
+    assert lib.moe_plan_destroy(None) == 0

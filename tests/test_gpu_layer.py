@@ -1,0 +1,248 @@
+"""End-to-end parity of the whole layer (moe_forward / prepared plans, called
+through the C ABI) against the CPU oracle, at the five workload shapes and at
+the edge cases; plus bitwise replay determinism."""
+import numpy as np
+import pytest
+import torch
+
+import mixture_experts_expert_router_gb300 as moe
+import oracle
+from mixture_experts_expert_router_gb300 import workloads as W
+from tests.tolerances import check_bf16_close
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from mixture_experts_expert_router_gb300 import _build
+    _build.build()
+    moe.library()
+
+
+def _dev(wl):
+    return {k: (getattr(wl, k).to(DEV) if getattr(wl, k) is not None else None)
+            for k in ("x", "w1", "w2", "logits", "topk_ids", "topk_w")}
+
+
+def _oracle_route(wl):
+    if wl.mode == "logits":
+        return oracle.route(wl.logits.cpu().numpy(), wl.top_k)
+    return wl.topk_ids.cpu().numpy(), wl.topk_w.cpu().numpy()
+
+
+def _oracle_out(wl, tokens=None, w1=None, w2=None):
+    ids, w = _oracle_route(wl)
+    w1 = W.bf16_bits(wl.w1) if w1 is None else w1
+    w2 = W.bf16_bits(wl.w2) if w2 is None else w2
+    out, st = oracle.moe_tokens(W.bf16_bits(wl.x), ids, w, w1, w2, wl.E, tokens=tokens,
+                                local_offset=wl.local_offset, num_local=wl.num_local)
+    return out, st
+
+
+def _forward(wl, d, path=moe.PATH_AUTO, status=None):
+    plan = moe.MoEPlan(d["x"], d["w1"], d["w2"], wl.E, wl.top_k, logits=d["logits"],
+                       topk_ids=d["topk_ids"], topk_w=d["topk_w"], local_offset=wl.local_offset,
+                       status=status, path=path)
+    out = plan.launch()
+    torch.cuda.synchronize()
+    return out, plan
+
+
+PATHS = [moe.PATH_GROUPED, moe.PATH_AUTO]
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_tiny_both_routing_modes(path):
+    wl = W.make_moe("tiny")
+    d = _dev(wl)
+    want, st = _oracle_out(wl)
+    out = moe.moe_forward(d["x"], d["w1"], d["w2"], wl.E, wl.top_k, logits=d["logits"])
+    torch.cuda.synchronize()
+    check_bf16_close(W.bf16_bits(out), want, "tiny logits")
+    out_p, _ = _forward(wl, d, path)
+    check_bf16_close(W.bf16_bits(out_p), want, "tiny plan")
+    ids, w = _oracle_route(wl)
+    out_r = moe.moe_forward(d["x"], d["w1"], d["w2"], wl.E, wl.top_k,
+                            topk_ids=torch.from_numpy(ids).to(DEV), topk_w=torch.from_numpy(w).to(DEV))
+    torch.cuda.synchronize()
+    check_bf16_close(W.bf16_bits(out_r), want, "tiny pre-routed")
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("T,H,I,E,k", [(1, 64, 64, 1, 1), (77, 192, 128, 6, 2), (300, 256, 320, 16, 4),
+                                       (513, 128, 64, 3, 3), (40, 128, 128, 20, 8)])
+def test_odd_shapes(path, T, H, I, E, k):
+    wl = W.make_moe(T=T, H=H, I=I, E=E, top_k=k, mode="logits", seed=T + E)
+    out, _ = _forward(wl, _dev(wl), path)
+    want, _ = _oracle_out(wl)
+    check_bf16_close(W.bf16_bits(out), want, f"T={T} H={H} I={I} E={E} k={k}")
+
+
+def test_replays_bitwise_identical_and_graph_capture():
+    wl = W.make_moe(T=600, H=256, I=192, E=12, top_k=3, mode="logits", seed=1)
+    d = _dev(wl)
+    plan = moe.MoEPlan(d["x"], d["w1"], d["w2"], wl.E, wl.top_k, logits=d["logits"])
+    b = plan.buffers()
+    R = wl.T * wl.top_k
+
+    ws = plan.workspace
+
+    def inter_bytes():
+        """Raw bytes of the intermediates the launch left in the workspace."""
+        parts = []
+        for name, nbytes in (("topk_ids", R * 4), ("topk_w", R * 4), ("m_indptr", (wl.E + 1) * 4),
+                             ("perm_to_exp", R * 4), ("exp_to_perm", R * 4), ("h", R * wl.I * 2),
+                             ("y", R * wl.H * 4)):
+            off = b[name] - ws.data_ptr()
+            parts.append(ws[off:off + nbytes].clone())
+        return parts
+
+    ref = plan.launch().clone()
+    torch.cuda.synchronize()
+    ref_inter = inter_bytes()
+    for _ in range(5):
+        ws.fill_(0xAB)
+        plan.launch()
+        torch.cuda.synchronize()
+        assert torch.equal(plan.out, ref)
+        for a, c in zip(inter_bytes(), ref_inter):
+            assert torch.equal(a, c)
+    # the same plan captured in a CUDA graph
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        plan.launch()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    plan.out.zero_()
+    with torch.cuda.graph(g):
+        plan.launch()
+    for _ in range(3):
+        plan.out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(plan.out, ref)
+    want, _ = _oracle_out(wl)
+    check_bf16_close(W.bf16_bits(ref), want, "replay")
+
+
+def test_prepared_launch_sees_new_values():
+    wl = W.make_moe(T=100, H=128, I=128, E=5, top_k=2, mode="logits", seed=2)
+    d = _dev(wl)
+    plan = moe.MoEPlan(d["x"], d["w1"], d["w2"], wl.E, wl.top_k, logits=d["logits"])
+    plan.launch()
+    wl2 = W.make_moe(T=100, H=128, I=128, E=5, top_k=2, mode="logits", seed=3)
+    d["x"].copy_(wl2.x.to(DEV))
+    d["logits"].copy_(wl2.logits.to(DEV))
+    wl2.w1, wl2.w2 = wl.w1, wl.w2
+    out = plan.launch()
+    torch.cuda.synchronize()
+    want, _ = _oracle_out(wl2)
+    check_bf16_close(W.bf16_bits(out), want, "rebound values")
+
+
+@pytest.mark.parametrize("off,L", [(0, 3), (3, 4), (7, 1), (0, 8)])
+def test_expert_parallel_shard(off, L):
+    full = W.make_moe(T=64, H=128, I=128, E=8, top_k=3, mode="logits", seed=4)
+    wl = W.make_moe(T=64, H=128, I=128, E=8, top_k=3, mode="logits", seed=4)
+    wl.w1, wl.w2 = full.w1[off:off + L].contiguous(), full.w2[off:off + L].contiguous()
+    wl.local_offset, wl.num_local = off, L
+    out, _ = _forward(wl, _dev(wl))
+    want, _ = _oracle_out(wl)
+    check_bf16_close(W.bf16_bits(out), want, f"shard {off}+{L}")
+
+
+def test_shard_with_no_routed_tokens_is_zero():
+    wl = W.make_moe(T=32, H=128, I=64, E=8, top_k=2, mode="prerouted", seed=5)
+    wl.topk_ids = torch.zeros_like(wl.topk_ids)
+    wl.topk_ids[:, 1] = 1
+    wl.w1, wl.w2 = wl.w1[4:6].contiguous(), wl.w2[4:6].contiguous()
+    wl.local_offset, wl.num_local = 4, 2
+    out, _ = _forward(wl, _dev(wl))
+    assert torch.all(out == 0)
+
+
+def test_bad_expert_ids_flagged_and_dropped():
+    wl = W.make_moe(T=50, H=128, I=64, E=6, top_k=2, mode="prerouted", seed=6)
+    ids = wl.topk_ids.clone()
+    ids[3, 0] = 6
+    ids[10, 1] = -1
+    wl.topk_ids = ids
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out, _ = _forward(wl, _dev(wl), status=status)
+    assert int(status.item()) & moe.DEV_BAD_EXPERT
+    want, st = _oracle_out(wl)
+    assert st == oracle.BAD_EXPERT
+    check_bf16_close(W.bf16_bits(out), want, "bad ids")
+
+
+def test_zero_tokens_is_noop():
+    wl = W.make_moe(T=0, H=128, I=64, E=4, top_k=2, mode="logits", seed=1)
+    out, _ = _forward(wl, _dev(wl))
+    assert out.shape == (0, 128)
+
+
+def test_all_tokens_on_one_expert():
+    wl = W.make_moe(T=400, H=128, I=128, E=16, top_k=2, mode="prerouted", seed=8)
+    ids = torch.full_like(wl.topk_ids, 5)
+    ids[:, 1] = 9
+    wl.topk_ids = ids
+    out, _ = _forward(wl, _dev(wl))
+    want, _ = _oracle_out(wl)
+    check_bf16_close(W.bf16_bits(out), want, "one expert")
+
+
+# ---------------------------------------------------------- workload shapes --
+
+@pytest.mark.parametrize("name", ["decode_t1", "decode_t8", "decode_t64"])
+@pytest.mark.parametrize("path", PATHS)
+def test_decode_configs_full(name, path):
+    wl = W.make_moe(name)
+    out, _ = _forward(wl, _dev(wl), path)
+    want, _ = _oracle_out(wl)
+    check_bf16_close(W.bf16_bits(out), want, name)
+
+
+def _sample_tokens(ids, T, n, seed):
+    """n seeded random tokens plus, for every expert that receives routes, the
+    first token routed to it (each output row depends only on its own token,
+    so a subset check is exact for those rows)."""
+    rng = np.random.default_rng(seed)
+    chosen = set(rng.choice(T, size=min(n, T), replace=False).tolist())
+    flat = ids.reshape(T, -1)
+    seen = set()
+    for t in range(T):
+        for e in flat[t]:
+            if e not in seen:
+                seen.add(int(e))
+                chosen.add(t)
+    return np.array(sorted(chosen), dtype=np.int32)
+
+
+@pytest.mark.parametrize("name", ["prefill_few_large", "prefill_many_fine"])
+def test_prefill_configs_sampled(name):
+    wl = W.make_moe(name, weights_device=DEV)
+    d = _dev(wl)
+    out, _ = _forward(wl, d)
+    ids, _ = _oracle_route(wl)
+    tokens = _sample_tokens(ids, wl.T, 1024, 0)
+    want, _ = _oracle_out(wl, tokens=tokens, w1=W.bf16_bits(wl.w1), w2=W.bf16_bits(wl.w2))
+    check_bf16_close(W.bf16_bits(out)[tokens], want, f"{name} ({len(tokens)} sampled tokens)")
+
+
+def test_grouped_gemm_config_full_size_sampled():
+    d = W.make_grouped_gemm(seed=0, device="cpu", weights_device=DEV)
+    X, Wt, offs = d["X"].to(DEV), d["W"], d["offs"].to(DEV)
+    Y = moe.grouped_gemm_fwd(X, Wt, offs)
+    torch.cuda.synchronize()
+    ends = d["offs"].numpy()
+    starts = np.concatenate([[0], ends[:-1]])
+    rows = set(np.random.default_rng(0).integers(0, d["sum_m"], 1024).tolist())
+    for s, e in zip(starts, ends):
+        if e > s:
+            rows.update([int(s), int(e) - 1])
+    rows = np.array(sorted(rows), dtype=np.int32)
+    Yo = oracle.grouped_gemm_rows(W.bf16_bits(d["X"]), W.bf16_bits(Wt), ends, rows)
+    check_bf16_close(W.bf16_bits(Y)[rows], Yo, "grouped GEMM 16384x1536x4096")

@@ -1,9 +1,16 @@
 """Acceptance rules shared by the parity tests.
 
-Outputs: max|a - b| <= 1e-2 * rms(b) (rms over the whole tensor, fp64) and at
-least 99.9% of elements within 2 bf16 ulp, the ulp distance being the gap on
-the monotone integer order of the bf16 bit patterns (+0 and -0 equal).
-Routing weights: within 1e-6 absolute.
+Outputs: every element within 1e-2 * rms(b) plus one bf16 ulp of b's element
+(rms over the whole tensor, fp64), and at least 99.9% of elements within 2
+bf16 ulp, the ulp distance being the gap on the monotone integer order of the
+bf16 bit patterns (+0 and -0 equal).  Routing weights: within 1e-6 absolute.
+
+Why the extra ulp: both sides round their own fp32 result to bf16 once, and
+fp32 sums taken in a different order straddle a bf16 rounding boundary now
+and then.  One such flip on an element above 2.56 * rms is already larger than
+1e-2 * rms, so a bare max-error bound of 1e-2 * rms would reject a correct
+kernel; 1e-2 * rms bounds the difference before the final rounding and the
+ulp term is the rounding quantum itself.
 """
 import numpy as np
 
@@ -28,6 +35,13 @@ def ulp_distance(a_bits: np.ndarray, b_bits: np.ndarray) -> np.ndarray:
     return np.abs(bf16_order(a_bits) - bf16_order(b_bits))
 
 
+def bf16_ulp_of(bits: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 values at each element's magnitude (2^(e-7))."""
+    v = np.abs(bf16_to_f64(bits))
+    e = np.floor(np.log2(np.maximum(v, 2.0 ** -133)))
+    return np.exp2(np.maximum(e, -133.0) - 7.0)
+
+
 def check_bf16_close(got_bits: np.ndarray, want_bits: np.ndarray, what: str = "output"):
     """Assert the output acceptance rule; returns (max_abs/rms, frac within 2 ulp)."""
     got = bf16_to_f64(got_bits)
@@ -41,7 +55,10 @@ def check_bf16_close(got_bits: np.ndarray, want_bits: np.ndarray, what: str = "o
     ulp = ulp_distance(got_bits, want_bits)
     frac = float(np.mean(ulp <= ULP_MAX))
     ratio = err / rms if rms > 0 else err
-    assert err <= RMS_FRAC * rms or (rms == 0 and err == 0), f"{what}: max err {err} > 1e-2*rms {rms}"
+    excess = np.abs(got - want) - bf16_ulp_of(want_bits) - RMS_FRAC * rms
+    worst = int(np.argmax(excess))
+    assert excess.flat[worst] <= 0, (f"{what}: |diff| {abs(got.flat[worst] - want.flat[worst])} at "
+                                     f"{want.flat[worst]} exceeds 1e-2*rms ({RMS_FRAC * rms}) + 1 ulp")
     assert frac >= ULP_FRACTION, f"{what}: only {frac:.5f} within {ULP_MAX} ulp"
     return ratio, frac
 
