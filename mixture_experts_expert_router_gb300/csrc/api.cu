@@ -254,8 +254,11 @@ int moe_forward_prepare(const moe_forward_desc *desc, moe_plan **plan_out) {
     return rc;
   const bool logits_mode = d.logits != nullptr;
   const bool routed_mode = d.topk_ids != nullptr || d.topk_w != nullptr;
-  if (logits_mode == routed_mode) return MOE_ERR_MODE;
-  if (routed_mode && (!d.topk_ids || !d.topk_w)) return MOE_ERR_MODE;
+  // With no tokens there is nothing to route (empty tensors may carry NULL).
+  if (d.T > 0) {
+    if (logits_mode == routed_mode) return MOE_ERR_MODE;
+    if (routed_mode && (!d.topk_ids || !d.topk_w)) return MOE_ERR_MODE;
+  }
   if (d.path < MOE_PATH_AUTO || d.path > MOE_PATH_DECODE) return MOE_ERR_SHAPE;
   if (d.T > 0) {
     if (!d.x || !d.w1 || !d.w2 || !d.out) return MOE_ERR_NULL;

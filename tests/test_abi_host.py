@@ -65,8 +65,12 @@ def test_workspace_size_and_prepare_errors(lib):
     assert moe.moe_workspace_size(16, 100, 128, 4, 2) == 0      # H % 64 != 0
     # more rows need more workspace
     assert moe.moe_workspace_size(64, 128, 128, 4, 2) > moe.moe_workspace_size(16, 128, 128, 4, 2)
-    d = moe._Desc(T=4, H=128, I=128, E=4, top_k=2, local_offset=0, num_local=4)
     h = ctypes.c_void_p()
+    d0 = moe._Desc(T=0, H=128, I=128, E=4, top_k=2, local_offset=0, num_local=4)
+    assert lib.moe_forward_prepare(ctypes.byref(d0), ctypes.byref(h)) == 0   # T == 0: empty plan
+    assert lib.moe_plan_kernels_per_launch(h) == 0
+    assert lib.moe_plan_destroy(h) == 0
+    d = moe._Desc(T=4, H=128, I=128, E=4, top_k=2, local_offset=0, num_local=4)
     assert lib.moe_forward_prepare(ctypes.byref(d), ctypes.byref(h)) == -5   # no routing input
     d.logits = 16
     d.topk_ids = 16
