@@ -113,6 +113,29 @@ MOE_API int moe_sort(const int32_t *topk_ids, int T, int top_k, int E, int local
              int32_t *exp_to_perm, void *workspace, size_t workspace_bytes,
              int32_t *status, void *stream);
 
+/* ---- S2 sort without a workspace ----------------------------------------------
+ * The pages have no counterpart of this entry point.  It is moe_sort for
+ * callers that cannot allocate device memory: a plugin whose host framework
+ * hands it only its input and output buffers, or a runtime that plans all
+ * device memory up front and forbids allocating afterwards.  The same kernels
+ * run; the per-chunk table that moe_sort keeps in the caller's workspace lives
+ * instead in a fixed 1 MiB array inside the library's device memory, held on
+ * every device that loads the library until the process exits.  Nothing is
+ * allocated and no workspace is passed; arguments and outputs are those of
+ * moe_sort.
+ *   Limit: ceil(T*top_k / 4096) * num_local <= 262144 table entries (T*top_k
+ *   <= 2048 uses no table at all); larger problems return MOE_ERR_WORKSPACE
+ *   before anything is enqueued.
+ *   The array's device address is looked up on the first call on each device,
+ *   with that device current; make that first call before any stream capture.
+ *   All calls share the array: calls whose kernels overlap on the GPU (for
+ *   example on two streams) race on it and must be serialised by the caller.
+ *   The kernels write every entry they read, so no clearing is needed. */
+MOE_API int moe_sort_no_alloc(const int32_t *topk_ids, int T, int top_k, int E,
+                              int local_offset, int num_local, int32_t *m_indptr,
+                              int32_t *perm_to_exp, int32_t *exp_to_perm,
+                              int32_t *status, void *stream);
+
 /* ---- S3 gather -------------------------------------------------------------------
  * xp[p, :] = x[perm_to_exp[p] / top_k, :] for p < M = m_indptr[L] (the
  * expanded per-route activations; cute_dsl_fused_moe_bf16, Parameters,

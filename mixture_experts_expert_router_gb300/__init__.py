@@ -22,7 +22,7 @@ import os
 import torch
 
 __all__ = [
-    "MoEError", "library", "library_path", "moe_status_string", "moe_route", "moe_sort",
+    "MoEError", "library", "library_path", "moe_status_string", "moe_route", "moe_sort", "moe_sort_no_alloc",
     "moe_sort_workspace_size", "moe_gather", "moe_fc1_swiglu", "moe_fc2", "moe_finalize",
     "grouped_gemm_fwd", "moe_workspace_size", "moe_forward", "MoEPlan", "ABI_SYMBOLS",
     "PATH_AUTO", "PATH_GROUPED", "PATH_DECODE", "DEV_BAD_EXPERT", "DEV_TIMEOUT",
@@ -42,7 +42,7 @@ ABI_SYMBOLS = [
     "moe_gather", "moe_fc1_swiglu", "moe_fc2", "moe_finalize", "grouped_gemm_fwd",
     "moe_workspace_size", "moe_forward", "moe_forward_prepare", "moe_plan_launch",
     "moe_plan_buffers_get", "moe_plan_stage_count", "moe_plan_stage_name", "moe_plan_stage_times",
-    "moe_plan_stage_reset", "moe_plan_kernels_per_launch", "moe_plan_destroy",
+    "moe_plan_stage_reset", "moe_plan_kernels_per_launch", "moe_plan_destroy", "moe_sort_no_alloc",
 ]
 
 
@@ -93,6 +93,7 @@ def library():
             "moe_route": ([P, I, I, I, P, P, P], I),
             "moe_sort_workspace_size": ([I, I, I], Z),
             "moe_sort": ([P, I, I, I, I, I, P, P, P, P, Z, P, P], I),
+            "moe_sort_no_alloc": ([P, I, I, I, I, I, P, P, P, P, P], I),
             "moe_gather": ([P, P, P, I, I, I, I, P, P], I),
             "moe_fc1_swiglu": ([P, P, P, I, I, I, I, P, P], I),
             "moe_fc2": ([P, P, P, I, I, I, I, P, P], I),
@@ -192,6 +193,30 @@ def moe_sort(topk_ids: torch.Tensor, num_experts: int, local_offset: int = 0, nu
     _check(library().moe_sort(_ptr(topk_ids), T, k, num_experts, local_offset, L, _ptr(m_indptr),
                               _ptr(perm_to_exp), _ptr(exp_to_perm), _ptr(workspace), wbytes,
                               _ptr(status), _stream(dev)), "moe_sort")
+    return m_indptr, perm_to_exp[:R], exp_to_perm[:R], status
+
+
+def moe_sort_no_alloc(topk_ids: torch.Tensor, num_experts: int, local_offset: int = 0, num_local=None,
+                      m_indptr=None, perm_to_exp=None, exp_to_perm=None, status=None):
+    """moe_sort without a workspace, for callers that cannot allocate device
+    memory (a plugin that only receives its input and output buffers, or a
+    runtime that forbids allocating after start-up): the library keeps the
+    sort's scratch table in its own fixed device array (see the C header for
+    the size limit and for why overlapping calls race).  This wrapper still
+    creates missing output tensors with torch for convenience; pass them in
+    to allocate nothing."""
+    _need(topk_ids, torch.int32, "topk_ids")
+    T, k = topk_ids.shape
+    dev = topk_ids.device
+    L = num_experts if num_local is None else num_local
+    R = T * k
+    m_indptr = torch.empty(L + 1, dtype=torch.int32, device=dev) if m_indptr is None else m_indptr
+    perm_to_exp = torch.empty(max(R, 1), dtype=torch.int32, device=dev) if perm_to_exp is None else perm_to_exp
+    exp_to_perm = torch.empty(max(R, 1), dtype=torch.int32, device=dev) if exp_to_perm is None else exp_to_perm
+    status = torch.zeros(1, dtype=torch.int32, device=dev) if status is None else status
+    _check(library().moe_sort_no_alloc(_ptr(topk_ids), T, k, num_experts, local_offset, L, _ptr(m_indptr),
+                                       _ptr(perm_to_exp), _ptr(exp_to_perm), _ptr(status), _stream(dev)),
+           "moe_sort_no_alloc")
     return m_indptr, perm_to_exp[:R], exp_to_perm[:R], status
 
 

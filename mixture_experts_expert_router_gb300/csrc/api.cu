@@ -164,6 +164,25 @@ int moe_sort(const int32_t *topk_ids, int T, int top_k, int E, int local_offset,
                              exp_to_perm, static_cast<int32_t *>(workspace), status, l));
 }
 
+int moe_sort_no_alloc(const int32_t *topk_ids, int T, int top_k, int E, int local_offset,
+                      int num_local, int32_t *m_indptr, int32_t *perm_to_exp,
+                      int32_t *exp_to_perm, int32_t *status, void *stream) {
+  if (T < 0 || top_k < 1 || top_k > MOE_MAX_TOP_K || E < 1 || E > MOE_MAX_EXPERTS ||
+      local_offset < 0 || num_local < 1 || (long)local_offset + num_local > E ||
+      (long)T * top_k > (1L << 30))
+    return MOE_ERR_SHAPE;
+  const long R = (long)T * top_k;
+  const size_t need = sort_workspace_bytes(R, num_local) / sizeof(int32_t);
+  if ((long)need > static_sort_scratch_ints()) return MOE_ERR_WORKSPACE;
+  if (!m_indptr) return MOE_ERR_NULL;
+  if (R > 0 && (!topk_ids || !perm_to_exp || !exp_to_perm)) return MOE_ERR_NULL;
+  if (int rc = check_device()) return rc;
+  int32_t *scratch = nullptr;
+  if (need > 0 && static_sort_scratch(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
+  return moe_sort(topk_ids, T, top_k, E, local_offset, num_local, m_indptr, perm_to_exp,
+                  exp_to_perm, scratch, need * sizeof(int32_t), status, stream);
+}
+
 int moe_gather(const moe_bf16 *x, const int32_t *perm_to_exp, const int32_t *m_indptr, int T,
                int H, int top_k, int num_local, moe_bf16 *xp, void *stream) {
   if (T < 0 || H <= 0 || H % 8 != 0 || top_k < 1 || top_k > MOE_MAX_TOP_K || num_local < 1)

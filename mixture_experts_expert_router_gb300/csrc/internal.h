@@ -34,6 +34,10 @@ cudaError_t launch_sort(const int32_t *ids, long routes, int E, int off, int L, 
                         int32_t *p2e, int32_t *e2p, int32_t *ws, int32_t *status,
                         const Launch &l);
 
+// Library-owned scratch for the allocation-free sort (sort.cu).
+long static_sort_scratch_ints();
+cudaError_t static_sort_scratch(int32_t **out);
+
 // S3 / S6 -----------------------------------------------------------------------
 cudaError_t launch_gather(const uint16_t *x, const int32_t *p2e, const int32_t *m_total, int H,
                           int k, long max_rows, uint16_t *xp, const Launch &l);

@@ -247,3 +247,49 @@ cudaError_t launch_sort(const int32_t *ids, long routes, int E, int off, int L, 
 }
 
 }  // namespace moe
+
+// ---------------------------------------------------------------------------
+// Allocation-free sort for callers that cannot allocate device memory.
+//
+// The multi-CTA sort needs a per-(chunk, expert) table in device memory.
+// moe_sort takes it from the caller's workspace; this variant keeps it in a
+// fixed array in the library's own device memory instead, so the caller passes
+// only inputs and outputs.  The array is kStaticSortScratchInts int32 (1 MiB)
+// and exists on every device that loads the library until the process exits.
+// Its address is looked up once per device (the first call on that device,
+// with the device current).  Every call shares the array; the kernels write
+// every entry they later read, so nothing has to be cleared between calls,
+// but two calls whose kernels overlap on the GPU race on it.
+#include <mutex>
+
+namespace moe {
+namespace {
+constexpr long kStaticSortScratchInts = 1L << 18;
+__device__ __align__(256) int32_t g_sort_scratch[kStaticSortScratchInts];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+int32_t *g_scratch_addr[kMaxDevices] = {};
+}  // namespace
+
+long static_sort_scratch_ints() { return kStaticSortScratchInts; }
+
+// Device address of the scratch array on the current device (host code must
+// not pass the symbol itself: on the host it is only a stand-in).
+cudaError_t static_sort_scratch(int32_t **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_sort_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = static_cast<int32_t *>(p);
+  }
+  *out = g_scratch_addr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace moe
