@@ -8,7 +8,7 @@ import torch
 import mixture_experts_expert_router_gb300 as moe
 import oracle
 from mixture_experts_expert_router_gb300 import workloads as W
-from tests.tolerances import check_bf16_close
+from tests.tolerances import check_bf16_close, check_bf16_end_to_end
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -77,7 +77,7 @@ def test_odd_shapes(path, T, H, I, E, k):
     wl = W.make_moe(T=T, H=H, I=I, E=E, top_k=k, mode="logits", seed=T + E)
     out, _ = _forward(wl, _dev(wl), path)
     want, _ = _oracle_out(wl)
-    check_bf16_close(W.bf16_bits(out), want, f"T={T} H={H} I={I} E={E} k={k}")
+    check_bf16_end_to_end(W.bf16_bits(out), want, f"T={T} H={H} I={I} E={E} k={k}")
 
 
 def test_replays_bitwise_identical_and_graph_capture():
@@ -125,7 +125,7 @@ def test_replays_bitwise_identical_and_graph_capture():
         torch.cuda.synchronize()
         assert torch.equal(plan.out, ref)
     want, _ = _oracle_out(wl)
-    check_bf16_close(W.bf16_bits(ref), want, "replay")
+    check_bf16_end_to_end(W.bf16_bits(ref), want, "replay")
 
 
 def test_prepared_launch_sees_new_values():
@@ -140,7 +140,7 @@ def test_prepared_launch_sees_new_values():
     out = plan.launch()
     torch.cuda.synchronize()
     want, _ = _oracle_out(wl2)
-    check_bf16_close(W.bf16_bits(out), want, "rebound values")
+    check_bf16_end_to_end(W.bf16_bits(out), want, "rebound values")
 
 
 @pytest.mark.parametrize("off,L", [(0, 3), (3, 4), (7, 1), (0, 8)])
@@ -151,7 +151,7 @@ def test_expert_parallel_shard(off, L):
     wl.local_offset, wl.num_local = off, L
     out, _ = _forward(wl, _dev(wl))
     want, _ = _oracle_out(wl)
-    check_bf16_close(W.bf16_bits(out), want, f"shard {off}+{L}")
+    check_bf16_end_to_end(W.bf16_bits(out), want, f"shard {off}+{L}")
 
 
 def test_shard_with_no_routed_tokens_is_zero():
@@ -175,7 +175,7 @@ def test_bad_expert_ids_flagged_and_dropped():
     assert int(status.item()) & moe.DEV_BAD_EXPERT
     want, st = _oracle_out(wl)
     assert st == oracle.BAD_EXPERT
-    check_bf16_close(W.bf16_bits(out), want, "bad ids")
+    check_bf16_end_to_end(W.bf16_bits(out), want, "bad ids")
 
 
 def test_zero_tokens_is_noop():
@@ -191,7 +191,7 @@ def test_all_tokens_on_one_expert():
     wl.topk_ids = ids
     out, _ = _forward(wl, _dev(wl))
     want, _ = _oracle_out(wl)
-    check_bf16_close(W.bf16_bits(out), want, "one expert")
+    check_bf16_end_to_end(W.bf16_bits(out), want, "one expert")
 
 
 # ---------------------------------------------------------- workload shapes --
@@ -202,7 +202,7 @@ def test_decode_configs_full(name, path):
     wl = W.make_moe(name)
     out, _ = _forward(wl, _dev(wl), path)
     want, _ = _oracle_out(wl)
-    check_bf16_close(W.bf16_bits(out), want, name)
+    check_bf16_end_to_end(W.bf16_bits(out), want, name)
 
 
 def _sample_tokens(ids, T, n, seed):
@@ -229,7 +229,7 @@ def test_prefill_configs_sampled(name):
     ids, _ = _oracle_route(wl)
     tokens = _sample_tokens(ids, wl.T, 1024, 0)
     want, _ = _oracle_out(wl, tokens=tokens, w1=W.bf16_bits(wl.w1), w2=W.bf16_bits(wl.w2))
-    check_bf16_close(W.bf16_bits(out)[tokens], want, f"{name} ({len(tokens)} sampled tokens)")
+    check_bf16_end_to_end(W.bf16_bits(out)[tokens], want, f"{name} ({len(tokens)} sampled tokens)")
 
 
 def test_grouped_gemm_config_full_size_sampled():
@@ -246,3 +246,47 @@ def test_grouped_gemm_config_full_size_sampled():
     rows = np.array(sorted(rows), dtype=np.int32)
     Yo = oracle.grouped_gemm_rows(W.bf16_bits(d["X"]), W.bf16_bits(Wt), ends, rows)
     check_bf16_close(W.bf16_bits(Y)[rows], Yo, "grouped GEMM 16384x1536x4096")
+
+
+# ----------------------------------------- stage chain at the workload shapes --
+
+def _stage_chain(wl, tokens):
+    """Full-size stage parity with the oracle's intermediates as inputs:
+    GPU FC1+SwiGLU on the oracle's gathered rows against the oracle's h, and
+    GPU FC2 + finalize on the oracle's h against the oracle's output; both
+    under the strict rule (errors do not compound)."""
+    ids, w = _oracle_route(wl)
+    T, k, E = wl.T, wl.top_k, wl.E
+    R = T * k
+    want, h_o, _, st = oracle.moe_tokens(W.bf16_bits(wl.x), ids, w, W.bf16_bits(wl.w1), W.bf16_bits(wl.w2), E,
+                                         tokens=tokens, want_intermediates=True)
+    m_o, p2e_o, e2p_o, _ = oracle.sort(ids, E)
+    w1, w2 = wl.w1.to(DEV), wl.w2.to(DEV)
+    m_d = torch.from_numpy(m_o).to(DEV)
+    # FC1: rows of the sampled routes only need to be right
+    xp = np.zeros((R, wl.H), np.uint16)
+    xp[:len(p2e_o)] = W.bf16_bits(wl.x)[p2e_o // k]
+    h_g = moe.moe_fc1_swiglu(W.from_bf16_bits(xp).to(DEV), w1, m_d)
+    slots = (tokens[:, None] * k + np.arange(k)[None, :]).ravel()
+    rows = e2p_o[slots]
+    check_bf16_close(W.bf16_bits(h_g)[rows], h_o, f"{wl.name}: h (FC1 on the oracle's rows)")
+    # FC2 + finalize on the oracle's h
+    h_in = np.zeros((R, wl.I), np.uint16)
+    h_in[rows] = h_o
+    y = moe.moe_fc2(W.from_bf16_bits(h_in).to(DEV), w2, m_d)
+    out = moe.moe_finalize(y, torch.from_numpy(e2p_o).to(DEV), torch.from_numpy(w).to(DEV))
+    torch.cuda.synchronize()
+    check_bf16_close(W.bf16_bits(out)[tokens], want, f"{wl.name}: out (FC2 + finalize on the oracle's h)")
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode_t1", "decode_t8", "decode_t64"])
+def test_stage_chain_small_configs(name):
+    wl = W.make_moe(name)
+    _stage_chain(wl, np.arange(wl.T, dtype=np.int32))
+
+
+@pytest.mark.parametrize("name", ["prefill_few_large", "prefill_many_fine"])
+def test_stage_chain_prefill_configs(name):
+    wl = W.make_moe(name, weights_device=DEV)
+    ids, _ = _oracle_route(wl)
+    _stage_chain(wl, _sample_tokens(ids, wl.T, 512, 1))
