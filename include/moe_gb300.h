@@ -165,6 +165,23 @@ MOE_API int moe_fc1_swiglu(const moe_bf16 *xp, const moe_bf16 *w1,
 MOE_API int moe_fc2(const moe_bf16 *h, const moe_bf16 *w2, const int32_t *m_indptr,
             int max_rows, int H, int I, int num_local, float *y, void *stream);
 
+/* ---- S7 decode-form FC1 / FC2 ------------------------------------------------------
+ * The same products as moe_fc1_swiglu / moe_fc2, computed with the operands
+ * swapped for few rows per expert (the swap-AB small-token forms of
+ * flashinfer.fused_moe.cake / cake_cute, Generated kernels): 128 weight rows
+ * take the MMA's M side and the expert's rows its N side (16/32/64), so each
+ * weight byte is streamed from HBM once.  max_group_rows is the expected
+ * largest group (it picks the N tile; larger groups are still correct, in
+ * several N tiles).  Arguments and layouts otherwise as moe_fc1_swiglu /
+ * moe_fc2.  moe_forward uses these for T <= 64 tokens (MOE_PATH_AUTO). */
+MOE_API int moe_fc1_swiglu_swapab(const moe_bf16 *xp, const moe_bf16 *w1,
+                                  const int32_t *m_indptr, int max_rows,
+                                  int max_group_rows, int H, int I, int num_local,
+                                  moe_bf16 *h, void *stream);
+MOE_API int moe_fc2_swapab(const moe_bf16 *h, const moe_bf16 *w2, const int32_t *m_indptr,
+                           int max_rows, int max_group_rows, int H, int I,
+                           int num_local, float *y, void *stream);
+
 /* ---- S6 finalize --------------------------------------------------------------------
  * out[t] = bf16_rne( sum_{j=0..top_k-1, exp_to_perm[t*top_k+j] >= 0}
  *                    topk_w[t,j] * y[exp_to_perm[t*top_k+j]] ), summed in fp32

@@ -24,6 +24,7 @@ import torch
 __all__ = [
     "MoEError", "library", "library_path", "moe_status_string", "moe_route", "moe_sort", "moe_sort_no_alloc",
     "moe_sort_workspace_size", "moe_gather", "moe_fc1_swiglu", "moe_fc2", "moe_finalize",
+    "moe_fc1_swiglu_swapab", "moe_fc2_swapab",
     "grouped_gemm_fwd", "moe_workspace_size", "moe_forward", "MoEPlan", "ABI_SYMBOLS",
     "PATH_AUTO", "PATH_GROUPED", "PATH_DECODE", "DEV_BAD_EXPERT", "DEV_TIMEOUT",
 ]
@@ -43,6 +44,7 @@ ABI_SYMBOLS = [
     "moe_workspace_size", "moe_forward", "moe_forward_prepare", "moe_plan_launch",
     "moe_plan_buffers_get", "moe_plan_stage_count", "moe_plan_stage_name", "moe_plan_stage_times",
     "moe_plan_stage_reset", "moe_plan_kernels_per_launch", "moe_plan_destroy", "moe_sort_no_alloc",
+    "moe_fc1_swiglu_swapab", "moe_fc2_swapab",
 ]
 
 
@@ -97,6 +99,8 @@ def library():
             "moe_gather": ([P, P, P, I, I, I, I, P, P], I),
             "moe_fc1_swiglu": ([P, P, P, I, I, I, I, P, P], I),
             "moe_fc2": ([P, P, P, I, I, I, I, P, P], I),
+            "moe_fc1_swiglu_swapab": ([P, P, P, I, I, I, I, I, P, P], I),
+            "moe_fc2_swapab": ([P, P, P, I, I, I, I, I, P, P], I),
             "moe_finalize": ([P, P, P, I, I, I, P, P], I),
             "grouped_gemm_fwd": ([P, P, P, I, I, I, I, P, P], I),
             "moe_workspace_size": ([I, I, I, I, I, I], Z),
@@ -260,6 +264,40 @@ def moe_fc2(h: torch.Tensor, w2: torch.Tensor, m_indptr: torch.Tensor, y=None):
     _need(y, torch.float32, "y", (rows, H), h.device)
     _check(library().moe_fc2(_ptr(h), _ptr(w2), _ptr(m_indptr), rows, H, I, L, _ptr(y),
                              _stream(h.device)), "moe_fc2")
+    return y
+
+
+def moe_fc1_swiglu_swapab(xp: torch.Tensor, w1: torch.Tensor, m_indptr: torch.Tensor, max_group_rows: int,
+                          h=None):
+    """Decode-form FC1 + SwiGLU (weights on the MMA's M side)."""
+    _need(xp, torch.bfloat16, "xp")
+    _need(w1, torch.bfloat16, "w1")
+    _need(m_indptr, torch.int32, "m_indptr")
+    rows, H = xp.shape
+    L, twoI, H2 = w1.shape
+    if H2 != H or twoI % 2:
+        raise ValueError("w1 must be [L, 2I, H]")
+    I = twoI // 2
+    h = torch.empty((rows, I), dtype=torch.bfloat16, device=xp.device) if h is None else h
+    _need(h, torch.bfloat16, "h", (rows, I), xp.device)
+    _check(library().moe_fc1_swiglu_swapab(_ptr(xp), _ptr(w1), _ptr(m_indptr), rows, max_group_rows, H, I, L,
+                                           _ptr(h), _stream(xp.device)), "moe_fc1_swiglu_swapab")
+    return h
+
+
+def moe_fc2_swapab(h: torch.Tensor, w2: torch.Tensor, m_indptr: torch.Tensor, max_group_rows: int, y=None):
+    """Decode-form FC2 (weights on the MMA's M side), fp32 out."""
+    _need(h, torch.bfloat16, "h")
+    _need(w2, torch.bfloat16, "w2")
+    _need(m_indptr, torch.int32, "m_indptr")
+    rows, I = h.shape
+    L, H, I2 = w2.shape
+    if I2 != I:
+        raise ValueError("w2 must be [L, H, I]")
+    y = torch.empty((rows, H), dtype=torch.float32, device=h.device) if y is None else y
+    _need(y, torch.float32, "y", (rows, H), h.device)
+    _check(library().moe_fc2_swapab(_ptr(h), _ptr(w2), _ptr(m_indptr), rows, max_group_rows, H, I, L, _ptr(y),
+                                    _stream(h.device)), "moe_fc2_swapab")
     return y
 
 

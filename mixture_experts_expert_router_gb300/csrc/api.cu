@@ -83,6 +83,8 @@ int check_layer_shape(int T, int H, int I, int E, int k, int off, int L) {
 enum Stage { kRoute = 0, kSort, kGather, kFc1, kFc2, kFinalize, kNumStages };
 const char *kStageNames[kNumStages] = {"route", "sort", "gather", "fc1_swiglu", "fc2", "finalize"};
 constexpr int kTimingRing = 512;
+// Token count up to which MOE_PATH_AUTO picks the weight-streaming decode path.
+constexpr int kDecodeMaxTokens = 64;
 
 }  // namespace
 }  // namespace moe
@@ -100,6 +102,7 @@ struct moe_plan {
   uint16_t *xp, *h;
   float *y;
   GemmPlan fc1, fc2;
+  SwapPlan fc1d, fc2d;  // decode path
   bool timing;
   cudaEvent_t (*ev)[kNumStages + 1];
   long n_recorded;
@@ -232,6 +235,43 @@ int moe_fc2(const moe_bf16 *h, const moe_bf16 *w2, const int32_t *m_indptr, int 
   return cuda_rc(launch_gemm(p, l));
 }
 
+int moe_fc1_swiglu_swapab(const moe_bf16 *xp, const moe_bf16 *w1, const int32_t *m_indptr,
+                          int max_rows, int max_group_rows, int H, int I, int num_local,
+                          moe_bf16 *h, void *stream) {
+  if (max_rows < 0 || max_group_rows < 1 || H <= 0 || I <= 0 || H % 64 || I % 64 ||
+      num_local < 1 || num_local > MOE_MAX_EXPERTS)
+    return MOE_ERR_SHAPE;
+  if (max_rows == 0) return MOE_OK;
+  if (!xp || !w1 || !m_indptr || !h) return MOE_ERR_NULL;
+  if (!aligned16(xp) || !aligned16(w1) || !aligned16(h)) return MOE_ERR_ALIGN;
+  if (int rc = check_device()) return rc;
+  SwapPlan p;
+  if (int rc = swap_prepare(p, true, w1, num_local, 2 * I, H, xp, max_rows, I, m_indptr + 1,
+                            max_group_rows, h, nullptr, false))
+    return rc;
+  Launch l;
+  l.stream = static_cast<cudaStream_t>(stream);
+  return cuda_rc(launch_swap(p, l));
+}
+
+int moe_fc2_swapab(const moe_bf16 *h, const moe_bf16 *w2, const int32_t *m_indptr, int max_rows,
+                   int max_group_rows, int H, int I, int num_local, float *y, void *stream) {
+  if (max_rows < 0 || max_group_rows < 1 || H <= 0 || I <= 0 || H % 64 || I % 64 ||
+      num_local < 1 || num_local > MOE_MAX_EXPERTS)
+    return MOE_ERR_SHAPE;
+  if (max_rows == 0) return MOE_OK;
+  if (!h || !w2 || !m_indptr || !y) return MOE_ERR_NULL;
+  if (!aligned16(h) || !aligned16(w2) || !aligned16(y)) return MOE_ERR_ALIGN;
+  if (int rc = check_device()) return rc;
+  SwapPlan p;
+  if (int rc = swap_prepare(p, false, w2, num_local, H, I, h, max_rows, H, m_indptr + 1,
+                            max_group_rows, y, nullptr, false))
+    return rc;
+  Launch l;
+  l.stream = static_cast<cudaStream_t>(stream);
+  return cuda_rc(launch_swap(p, l));
+}
+
 int moe_finalize(const float *y, const int32_t *exp_to_perm, const float *topk_w, int T,
                  int top_k, int H, moe_bf16 *out, void *stream) {
   if (T < 0 || H <= 0 || H % 8 != 0 || top_k < 1 || top_k > MOE_MAX_TOP_K) return MOE_ERR_SHAPE;
@@ -294,7 +334,8 @@ int moe_forward_prepare(const moe_forward_desc *desc, moe_plan **plan_out) {
   if (!p) return MOE_ERR_CUDA;
   p->d = d;
   p->logits_mode = logits_mode;
-  p->path = MOE_PATH_GROUPED;
+  // Few tokens: each expert gets at most a few rows, the layer streams weights.
+  p->path = d.path != MOE_PATH_AUTO ? d.path : (d.T <= kDecodeMaxTokens ? MOE_PATH_DECODE : MOE_PATH_GROUPED);
   p->R = (long)d.T * d.top_k;
   unsigned char *ws = static_cast<unsigned char *>(d.workspace);
   if (d.T > 0) {
@@ -307,11 +348,20 @@ int moe_forward_prepare(const moe_forward_desc *desc, moe_plan **plan_out) {
     p->xp = reinterpret_cast<uint16_t *>(ws + lay.xp);
     p->h = reinterpret_cast<uint16_t *>(ws + lay.h);
     p->y = reinterpret_cast<float *>(ws + lay.y);
-    int rc = gemm_prepare(p->fc1, Epi::kSwiGLU, p->xp, p->R, d.w1, d.num_local, 2 * d.I, d.H, d.I,
-                          p->m_indptr + 1, p->R, p->h, d.status);
-    if (rc == MOE_OK)
-      rc = gemm_prepare(p->fc2, Epi::kF32, p->h, p->R, d.w2, d.num_local, d.H, d.I, d.H,
-                        p->m_indptr + 1, p->R, p->y, d.status);
+    int rc;
+    if (p->path == MOE_PATH_DECODE) {
+      rc = swap_prepare(p->fc1d, true, d.w1, d.num_local, 2 * d.I, d.H, p->xp, p->R, d.I,
+                        p->m_indptr + 1, d.T, p->h, d.status, true);
+      if (rc == MOE_OK)
+        rc = swap_prepare(p->fc2d, false, d.w2, d.num_local, d.H, d.I, p->h, p->R, d.H,
+                          p->m_indptr + 1, d.T, p->y, d.status, true);
+    } else {
+      rc = gemm_prepare(p->fc1, Epi::kSwiGLU, p->xp, p->R, d.w1, d.num_local, 2 * d.I, d.H, d.I,
+                        p->m_indptr + 1, p->R, p->h, d.status);
+      if (rc == MOE_OK)
+        rc = gemm_prepare(p->fc2, Epi::kF32, p->h, p->R, d.w2, d.num_local, d.H, d.I, d.H,
+                          p->m_indptr + 1, p->R, p->y, d.status);
+    }
     if (rc != MOE_OK) {
       delete p;
       return rc;
@@ -366,10 +416,11 @@ int moe_plan_launch(moe_plan *p, void *stream) {
   if (launch_gather(d.x, p->p2e, p->m_indptr + d.num_local, d.H, d.top_k, p->R, p->xp, l) !=
       cudaSuccess)
     return MOE_ERR_CUDA;
+  const bool dec = p->path == MOE_PATH_DECODE;
   if (!mark(kFc1)) return MOE_ERR_CUDA;
-  if (launch_gemm(p->fc1, l) != cudaSuccess) return MOE_ERR_CUDA;
+  if ((dec ? launch_swap(p->fc1d, l) : launch_gemm(p->fc1, l)) != cudaSuccess) return MOE_ERR_CUDA;
   if (!mark(kFc2)) return MOE_ERR_CUDA;
-  if (launch_gemm(p->fc2, l) != cudaSuccess) return MOE_ERR_CUDA;
+  if ((dec ? launch_swap(p->fc2d, l) : launch_gemm(p->fc2, l)) != cudaSuccess) return MOE_ERR_CUDA;
   if (!mark(kFinalize)) return MOE_ERR_CUDA;
   if (launch_finalize(p->y, p->e2p, p->w, d.T, d.top_k, d.H, d.out, l) != cudaSuccess)
     return MOE_ERR_CUDA;

@@ -81,6 +81,21 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[N]) {
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
+// Barrier over the four epilogue warps that also ORs a flag across them, so
+// that all of them take the same branch after it.
+__device__ __forceinline__ bool epi_bar_any(bool flag) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, 1, 128, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)flag)
+      : "memory");
+  return r != 0;
+}
+
 struct Tile {
   int g, m, n;
 };
@@ -180,6 +195,12 @@ __global__ void __launch_bounds__(kThreads, 1) swapab_kernel(const __grid_consta
   __syncthreads();
   tc_fence_after();
 
+  // The next kernel of a prepared chain only needs this kernel's tile table
+  // inputs to be final (they are: they were written two kernels back), so it
+  // may start streaming its own weights now; it waits for this kernel to
+  // finish before it reads what this kernel writes.
+  pdl_launch_dependents();
+
   const uint32_t tmem_base = *tmem_holder;
   const int total = tile_start[G];
   const int num_kb = args.K / BK;
@@ -196,26 +217,28 @@ __global__ void __launch_bounds__(kThreads, 1) swapab_kernel(const __grid_consta
       // follow it.
       int pending_x = 0;
       bool waited = !args.early;
+      // Activation boxes of the early k-blocks (all of the first tile, k-block
+      // j in ring stage j) go out once the predecessor has finished.
+      auto finish_wait = [&]() {
+        pdl_wait();
+        waited = true;
+        if (pending_x == 0) return;
+        const Tile c0 = decode_swap_tile(blockIdx.x, tile_start, gend, G, args.m_tiles);
+        const int xr0 = (c0.g == 0 ? 0 : gend[c0.g - 1]) + c0.n * BNT;
+        for (int j = 0; j < pending_x; ++j)
+          tma_load_2d(smem_base + j * C::STAGE_BYTES + C::A_BYTES, &args.map_x, full_bar(j), j * BK,
+                      xr0, pol_x);
+        pending_x = 0;
+      };
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        if (!waited && t != (int)blockIdx.x) finish_wait();
         const Tile c = decode_swap_tile(t, tile_start, gend, G, args.m_tiles);
         const int wrow = c.g * args.w_rows + c.m * rows_per_tile;
         const int xrow = (c.g == 0 ? 0 : gend[c.g - 1]) + c.n * BNT;
         for (int kb = 0; kb < num_kb; ++kb, ++it) {
           const int s = it % C::STAGES;
           const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
-          if (!waited && it >= C::STAGES) {
-            // the ring is full of early weight loads: wait, then add their activations
-            pdl_wait();
-            waited = true;
-            for (int j = 0; j < pending_x; ++j) {
-              const int t0 = blockIdx.x;  // early loads all belong to the first tile
-              const Tile c0 = decode_swap_tile(t0, tile_start, gend, G, args.m_tiles);
-              const int xr0 = (c0.g == 0 ? 0 : gend[c0.g - 1]) + c0.n * BNT;
-              tma_load_2d(smem_base + j * C::STAGE_BYTES + C::A_BYTES, &args.map_x, full_bar(j),
-                          j * BK, xr0, pol_x);
-            }
-            pending_x = 0;
-          }
+          if (!waited && it >= C::STAGES) finish_wait();  // the ring is full of early loads
           if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, args.status)) {
             ok = false;
             break;
@@ -236,14 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1) swapab_kernel(const __grid_consta
           }
         }
       }
-      if (!waited) {  // fewer k-blocks in total than ring stages
-        pdl_wait();
-        const Tile c0 = decode_swap_tile(blockIdx.x, tile_start, gend, G, args.m_tiles);
-        const int xr0 = (c0.g == 0 ? 0 : gend[c0.g - 1]) + c0.n * BNT;
-        for (int j = 0; j < pending_x; ++j)
-          tma_load_2d(smem_base + j * C::STAGE_BYTES + C::A_BYTES, &args.map_x, full_bar(j), j * BK,
-                      xr0, pol_x);
-      }
+      if (!waited) finish_wait();  // fewer k-blocks in total than ring stages
       for (int j = it > C::STAGES ? it - C::STAGES : 0; j < it; ++j)
         mbar_wait(full_bar(j % C::STAGES), (uint32_t)(j / C::STAGES) & 1u, nullptr, args.status);
     }
@@ -292,22 +308,21 @@ __global__ void __launch_bounds__(kThreads, 1) swapab_kernel(const __grid_consta
       const int acc = tc & 1;
       const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
       const bool got = mbar_wait(tfull_bar(acc), aph, abort_flag, args.status);
+      if (epi_bar_any(!got)) break;  // a wait gave up somewhere: all four warps stop together
       float v[BNT];
-      if (got) {
-        tc_fence_after();
-        tmem_ld_cols<BNT>(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BNT), v);
-        tmem_ld_wait();
-        tc_fence_before();
-        mbar_arrive(tempty_bar(acc));
-      }
+      tc_fence_after();
+      tmem_ld_cols<BNT>(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BNT), v);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(tempty_bar(acc));
       if (SWIGLU) {
         // the gate half (rows 64..127) hands its values to the up half
-        if (got && r >= 64) {
+        if (r >= 64) {
 #pragma unroll
           for (int j = 0; j < BNT; ++j) sg[j * 64 + (r - 64)] = v[j];
         }
         epi_bar();
-        if (got && r < 64) {
+        if (r < 64) {
           __nv_bfloat16 *h = reinterpret_cast<__nv_bfloat16 *>(args.out);
           const long col = (long)c.m * 64 + r;
 #pragma unroll
@@ -320,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1) swapab_kernel(const __grid_consta
           }
         }
         epi_bar();
-      } else if (got) {
+      } else {
         float *y = reinterpret_cast<float *>(args.out);
         const long col = (long)c.m * 128 + r;
         if (col < args.n_out) {
@@ -329,7 +344,6 @@ __global__ void __launch_bounds__(kThreads, 1) swapab_kernel(const __grid_consta
             if (j < valid) y[(long)(xrow + j) * args.n_out + col] = v[j];
         }
       }
-      if (!got) break;
     }
   }
 

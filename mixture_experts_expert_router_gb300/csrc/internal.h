@@ -72,4 +72,23 @@ int gemm_prepare(GemmPlan &p, Epi epi, const uint16_t *A, long a_rows, const uin
                  int32_t *status);
 cudaError_t launch_gemm(const GemmPlan &p, const Launch &l);
 
+// S7: swap-AB weight-streaming GEMMs for few tokens per expert (decode.cu) ----
+struct SwapPlan {
+  CUtensorMap map_w;            // weights [G * w_rows, K], box {64, 64 | 128}
+  CUtensorMap map_x;            // activations [max_rows, K], box {64, bnt}
+  const int32_t *group_end = nullptr;
+  void *out = nullptr;          // h (bf16) for FC1, y (fp32) for FC2
+  int32_t *status = nullptr;
+  long max_rows = 0;
+  int G = 0, K = 0, n_out = 0, w_rows = 0, m_tiles = 0, bnt = 0, grid = 0;
+  size_t smem = 0;
+  bool swiglu = false;
+  bool early = false;           // may read group_end and stream weights before the PDL wait
+};
+
+int swap_prepare(SwapPlan &p, bool swiglu, const uint16_t *W, int G, int w_rows, int K,
+                 const uint16_t *X, long max_rows, int n_out, const int32_t *group_end,
+                 long max_group_rows, void *out, int32_t *status, bool early);
+cudaError_t launch_swap(const SwapPlan &p, const Launch &l);
+
 }  // namespace moe

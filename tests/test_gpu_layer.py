@@ -50,7 +50,7 @@ def _forward(wl, d, path=moe.PATH_AUTO, status=None):
     return out, plan
 
 
-PATHS = [moe.PATH_GROUPED, moe.PATH_AUTO]
+PATHS = [moe.PATH_GROUPED, moe.PATH_DECODE, moe.PATH_AUTO]
 
 
 @pytest.mark.parametrize("path", PATHS)
@@ -250,7 +250,7 @@ def test_grouped_gemm_config_full_size_sampled():
 
 # ----------------------------------------- stage chain at the workload shapes --
 
-def _stage_chain(wl, tokens):
+def _stage_chain(wl, tokens, swapab=False):
     """Full-size stage parity with the oracle's intermediates as inputs:
     GPU FC1+SwiGLU on the oracle's gathered rows against the oracle's h, and
     GPU FC2 + finalize on the oracle's h against the oracle's output; both
@@ -266,23 +266,30 @@ def _stage_chain(wl, tokens):
     # FC1: rows of the sampled routes only need to be right
     xp = np.zeros((R, wl.H), np.uint16)
     xp[:len(p2e_o)] = W.bf16_bits(wl.x)[p2e_o // k]
-    h_g = moe.moe_fc1_swiglu(W.from_bf16_bits(xp).to(DEV), w1, m_d)
+    if swapab:
+        h_g = moe.moe_fc1_swiglu_swapab(W.from_bf16_bits(xp).to(DEV), w1, m_d, max(1, wl.T))
+    else:
+        h_g = moe.moe_fc1_swiglu(W.from_bf16_bits(xp).to(DEV), w1, m_d)
     slots = (tokens[:, None] * k + np.arange(k)[None, :]).ravel()
     rows = e2p_o[slots]
     check_bf16_close(W.bf16_bits(h_g)[rows], h_o, f"{wl.name}: h (FC1 on the oracle's rows)")
     # FC2 + finalize on the oracle's h
     h_in = np.zeros((R, wl.I), np.uint16)
     h_in[rows] = h_o
-    y = moe.moe_fc2(W.from_bf16_bits(h_in).to(DEV), w2, m_d)
+    if swapab:
+        y = moe.moe_fc2_swapab(W.from_bf16_bits(h_in).to(DEV), w2, m_d, max(1, wl.T))
+    else:
+        y = moe.moe_fc2(W.from_bf16_bits(h_in).to(DEV), w2, m_d)
     out = moe.moe_finalize(y, torch.from_numpy(e2p_o).to(DEV), torch.from_numpy(w).to(DEV))
     torch.cuda.synchronize()
     check_bf16_close(W.bf16_bits(out)[tokens], want, f"{wl.name}: out (FC2 + finalize on the oracle's h)")
 
 
+@pytest.mark.parametrize("swapab", [False, True])
 @pytest.mark.parametrize("name", ["tiny", "decode_t1", "decode_t8", "decode_t64"])
-def test_stage_chain_small_configs(name):
+def test_stage_chain_small_configs(name, swapab):
     wl = W.make_moe(name)
-    _stage_chain(wl, np.arange(wl.T, dtype=np.int32))
+    _stage_chain(wl, np.arange(wl.T, dtype=np.int32), swapab)
 
 
 @pytest.mark.parametrize("name", ["prefill_few_large", "prefill_many_fine"])

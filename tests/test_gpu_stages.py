@@ -171,3 +171,31 @@ def test_grouped_gemm_rows_beyond_offsets_untouched():
     moe.grouped_gemm_fwd(X, d["W"].to(DEV), d["offs"].to(DEV), Y)
     torch.cuda.synchronize()
     assert torch.all(Y[130:] == 3.0)
+
+
+@pytest.mark.parametrize("T,H,I,E,k,max_group", [(1, 2048, 768, 128, 8, 1), (8, 256, 128, 16, 4, 8),
+                                                 (64, 192, 320, 32, 8, 64), (40, 128, 64, 3, 2, 16),
+                                                 (300, 128, 128, 5, 2, 32)])
+def test_swapab_fc1_fc2_stage_parity(T, H, I, E, k, max_group):
+    """Decode-form kernels (weights on the MMA's M side) on the oracle's own
+    intermediates; groups larger than the N tile run in several N tiles."""
+    wl = W.make_moe(T=T, H=H, I=I, E=E, top_k=k, mode="logits", seed=T + 11)
+    x, w1, w2 = W.bf16_bits(wl.x), W.bf16_bits(wl.w1), W.bf16_bits(wl.w2)
+    ids, w = oracle.route(wl.logits.numpy(), k)
+    m, p2e, e2p, _ = oracle.sort(ids, E)
+    R = T * k
+    xp = np.zeros((R, H), np.uint16)
+    xp[:len(p2e)] = x[p2e // k]
+    m_d = torch.from_numpy(m).to(DEV)
+    rows = np.arange(len(p2e), dtype=np.int32)
+    h_g = moe.moe_fc1_swiglu_swapab(W.from_bf16_bits(xp).to(DEV), wl.w1.to(DEV), m_d, max_group)
+    h_o = oracle.fc1_swiglu_rows(xp, w1, m[1:], rows)
+    check_bf16_close(W.bf16_bits(h_g)[rows], h_o, "h (swap-AB)")
+    h_full = np.zeros((R, I), np.uint16)
+    h_full[:len(p2e)] = h_o
+    y_g = moe.moe_fc2_swapab(W.from_bf16_bits(h_full).to(DEV), wl.w2.to(DEV), m_d, max_group)
+    y_o = oracle.fc2_rows(h_full, w2, m[1:], rows)
+    check_f32_close(y_g.cpu().numpy()[rows], y_o, "y (swap-AB)")
+    # the decode-form and grouped FC2 read the same h: compare the two kernels too
+    y_grouped = moe.moe_fc2(W.from_bf16_bits(h_full).to(DEV), wl.w2.to(DEV), m_d)
+    check_f32_close(y_g.cpu().numpy()[rows], y_grouped.cpu().numpy()[rows], "y swap-AB vs grouped")
