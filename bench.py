@@ -245,6 +245,22 @@ def make_workload(args, rank, weights_device):
     return W.make_moe(args.config, seed=args.seed + rank, device="cpu", weights_device=weights_device)
 
 
+def roofline_entry(decode_path, fc1_s, F_fc1, B_fc1, peak_t, peak_b, peak_src, traffic):
+    """Dominant kernel (FC1 + SwiGLU): tensor-bound on the grouped path,
+    HBM-bound (weight streaming) on the decode path."""
+    if fc1_s <= 0:
+        return None
+    if decode_path:
+        gbs = B_fc1 / fc1_s / 1e9
+        return {"kernel": "fc1_swiglu (decode form)", "bound": "hbm", "achieved": gbs, "peak": peak_b,
+                "unit": "GB/s", "frac": gbs / peak_b, "traffic": traffic,
+                "peak_kind": f"{peak_src} HBM copy bandwidth", "bytes_per_launch": B_fc1}
+    tf = F_fc1 / fc1_s / 1e12
+    return {"kernel": "fc1_swiglu", "bound": "tensor", "achieved": tf, "peak": peak_t, "unit": "TFLOP/s",
+            "frac": tf / peak_t, "traffic": traffic,
+            "peak_kind": f"{peak_src} sustained bf16 (kernel timed inside the step)", "flops_per_launch": F_fc1}
+
+
 def config_dict(wl, world):
     return {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "top_k": wl.top_k,
             "routing": wl.mode, "global_batch": wl.T * world,
@@ -264,7 +280,11 @@ def run_ours(args, world, rank, local):
     tw = wl.topk_w.to(dev) if wl.topk_w is not None else None
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     plan = moe.MoEPlan(x, wl.w1, wl.w2, wl.E, wl.top_k, logits=logits, topk_ids=tids, topk_w=tw,
-                       local_offset=wl.local_offset, status=status, stage_timing=True)
+                       local_offset=wl.local_offset, status=status)
+    # a second plan on the same buffers records CUDA events around every stage
+    plan_t = moe.MoEPlan(x, wl.w1, wl.w2, wl.E, wl.top_k, logits=logits, topk_ids=tids, topk_w=tw,
+                         local_offset=wl.local_offset, status=status, out=plan.out,
+                         workspace=plan.workspace, stage_timing=True)
     kernels = plan.kernels_per_launch()
     stream = torch.cuda.current_stream(dev)
 
@@ -283,6 +303,21 @@ def run_ours(args, world, rank, local):
     F_fc1 = 2.0 * M * wl.H * 2 * wl.I
     B, active = layer_bytes(wl, ids_np)
 
+    # one step = one replay of the prepared launch captured in a CUDA graph
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            plan.launch()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            plan.launch()
+    step = graph.replay if graph is not None else plan.launch
+
     dev_index = str(local)
     try:
         uuid = torch.cuda.get_device_properties(dev).uuid
@@ -292,22 +327,36 @@ def run_ours(args, world, rank, local):
     clocks = ClockSampler(dev_index)
     time.sleep(0.3)
     for _ in range(args.warmup):
-        plan.launch()
+        step()
     torch.cuda.synchronize()
-    plan.stage_reset()
     barrier(world)
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t_wall0 = time.time()
     ev0.record(stream)
     for _ in range(args.steps):
-        plan.launch()
+        step()
     ev1.record(stream)
     torch.cuda.synchronize()
     t_wall1 = time.time()
     barrier(world)
     ms_local = ev0.elapsed_time(ev1)
-    stage_ms, n_timed = plan.stage_times()
+
+    # stage pass: the same steps with CUDA events between the stages (no PDL
+    # overlap between them); gives each kernel's mean duration
+    for _ in range(3):
+        plan_t.launch()
+    torch.cuda.synchronize()
+    plan_t.stage_reset()
+    n_stage_steps = min(args.steps, 200)
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for _ in range(n_stage_steps):
+        plan_t.launch()
+    s1.record(stream)
+    torch.cuda.synchronize()
+    stage_pass_ms = s0.elapsed_time(s1) / n_stage_steps
+    stage_ms, n_timed = plan_t.stage_times()
     time.sleep(0.25)
 
     # end to end: pinned host inputs in, result out, every step
@@ -355,9 +404,12 @@ def run_ours(args, world, rank, local):
 
     peaks, peak_src = load_peaks()
     fc1_s = stage_ms.get("fc1_swiglu", 0.0) / 1000.0 / max(1, n_timed)
-    fc1_tflops = F_fc1 / fc1_s / 1e12 if fc1_s > 0 else None
     peak_t = float(peaks.get("bf16_tflops_sustained", PEAKS_FALLBACK["bf16_tflops_sustained"]))
-    roofline_t = max(F / (float(peaks["bf16_tflops"]) * 1e12), B / (float(peaks["hbm_gbs"]) * 1e9))
+    peak_b = float(peaks.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"]))
+    roofline_t = max(F / (float(peaks["bf16_tflops"]) * 1e12), B / (peak_b * 1e9))
+    # FC1's algorithmic bytes: W1 of the active experts, its gathered input rows, h written
+    B_fc1 = active * 2.0 * wl.I * wl.H * 2 + M * wl.H * 2.0 + M * wl.I * 2.0
+    decode_path = plan.buffers()["path"] == moe.PATH_DECODE
     traffic = None
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
@@ -377,13 +429,14 @@ def run_ours(args, world, rank, local):
         "roofline_step": {"time_ms": roofline_t * 1000.0, "frac": roofline_t / step_s,
                           "flops": F, "bytes": B, "active_experts": active,
                           "peaks": f"{peak_src}: {peaks['bf16_tflops']} TFLOP/s bf16, {peaks['hbm_gbs']} GB/s"},
-        "roofline": {"kernel": "fc1_swiglu", "bound": "tensor", "achieved": fc1_tflops, "peak": peak_t,
-                     "unit": "TFLOP/s", "frac": (fc1_tflops / peak_t) if fc1_tflops else None,
-                     "traffic": traffic, "peak_kind": f"{peak_src} sustained bf16 (kernel timed inside the step)",
-                     "flops_per_launch": F_fc1},
+        "roofline": roofline_entry(decode_path, fc1_s, F_fc1, B_fc1, peak_t, peak_b, peak_src, traffic),
         "stage_ms": {k: v / max(1, n_timed) for k, v in stage_ms.items()},
+        "stage_pass_ms_per_step": stage_pass_ms,
+        "timing": ("CUDA-graph replay of the prepared launch" if graph is not None else "prepared launch")
+                  + "; dominant-kernel time from a second pass with CUDA events around each stage",
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": kernels * args.steps,
+        "kernels_per_step": kernels,
         "clocks": clocks.summary(t_wall0, t_wall1),
         "device_status": st,
     }
@@ -404,7 +457,7 @@ def run_ours(args, world, rank, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="prefill_few_large")
@@ -412,6 +465,7 @@ def main():
     ap.add_argument("--shape", default=None,
                     help="T,H,I,E,top_k of a custom logits-routed workload (profiling runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="launch the plan directly instead of a CUDA graph")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--reference-budget", type=float, default=120.0,
                     help="seconds of oracle work for the whole --impl reference run")
