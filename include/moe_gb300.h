@@ -234,6 +234,8 @@ MOE_API int moe_forward(const moe_bf16 *x, const float *logits, const int32_t *t
 #define MOE_PATH_DECODE 2  /* weight-streaming kernels for few tokens         */
 
 #define MOE_PLAN_STAGE_TIMING 1 /* record CUDA events around each stage     */
+#define MOE_PLAN_ONE_CTA_GEMM 2 /* grouped path: one-CTA GEMM kernels instead of
+                                   the CTA-pair (2-SM MMA) kernels (comparison) */
 
 typedef struct moe_forward_desc {
     const moe_bf16 *x;

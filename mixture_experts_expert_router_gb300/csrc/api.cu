@@ -356,11 +356,12 @@ int moe_forward_prepare(const moe_forward_desc *desc, moe_plan **plan_out) {
         rc = swap_prepare(p->fc2d, false, d.w2, d.num_local, d.H, d.I, p->h, p->R, d.H,
                           p->m_indptr + 1, d.T, p->y, d.status, true);
     } else {
+      const bool pair = (d.flags & MOE_PLAN_ONE_CTA_GEMM) == 0;
       rc = gemm_prepare(p->fc1, Epi::kSwiGLU, p->xp, p->R, d.w1, d.num_local, 2 * d.I, d.H, d.I,
-                        p->m_indptr + 1, p->R, p->h, d.status);
+                        p->m_indptr + 1, p->R, p->h, d.status, pair);
       if (rc == MOE_OK)
         rc = gemm_prepare(p->fc2, Epi::kF32, p->h, p->R, d.w2, d.num_local, d.H, d.I, d.H,
-                          p->m_indptr + 1, p->R, p->y, d.status);
+                          p->m_indptr + 1, p->R, p->y, d.status, pair);
     }
     if (rc != MOE_OK) {
       delete p;

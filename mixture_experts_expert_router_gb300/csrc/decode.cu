@@ -329,8 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1) swapab_kernel(const __grid_consta
           for (int j = 0; j < BNT; ++j) {
             if (j < valid) {
               const float gg = sg[j * 64 + r];
-              const float silu = gg / (1.0f + expf(-gg));
-              h[(long)(xrow + j) * args.n_out + col] = __float2bfloat16_rn(silu * v[j]);
+              h[(long)(xrow + j) * args.n_out + col] = __float2bfloat16_rn(silu_f32(gg) * v[j]);
             }
           }
         }

@@ -297,8 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             for (int q = 0; q < 2; ++q) {
               const float uu = __uint_as_float(u[2 * i + q]);
               const float gg = __uint_as_float(g[2 * i + q]);
-              const float silu = gg / (1.0f + expf(-gg));
-              hv[q] = silu * uu;
+              hv[q] = silu_f32(gg) * uu;
             }
             packed[i] = pack_bf16x2(hv[0], hv[1]);
           }
@@ -425,7 +424,7 @@ static cudaError_t configure_gemm(const GemmPlan &p);
 
 int gemm_prepare(GemmPlan &p, Epi epi, const uint16_t *A, long a_rows, const uint16_t *B, int G,
                  int b_rows, int K, int n_out, const int32_t *group_end, long max_rows, void *out,
-                 int32_t *status) {
+                 int32_t *status, bool allow_pair) {
   p = GemmPlan();
   p.epi = epi;
   p.G = G;
@@ -447,10 +446,20 @@ int gemm_prepare(GemmPlan &p, Epi epi, const uint16_t *A, long a_rows, const uin
     p.n_tiles = n_out / p.bn;
     box_b = p.bn;
   }
+  p.pair = (allow_pair && pair_gemm_supported(epi, n_out)) ? 1 : 0;
+  if (p.pair) {  // each CTA of the pair stages 128 of the 256 B rows
+    p.bn = 256;
+    p.n_tiles = epi == Epi::kSwiGLU ? n_out / 128 : n_out / 256;
+    box_b = 128;
+  }
   int rc = encode_2d(&p.map_a, A, a_rows, K, BM);
   if (rc != MOE_OK) return rc;
   rc = encode_2d(&p.map_b, B, (long)G * b_rows, K, box_b);
   if (rc != MOE_OK) return rc;
+  if (p.pair) {
+    rc = pair_gemm_encode_extra(p, A, a_rows, B, (long)G * b_rows, K);
+    if (rc != MOE_OK) return rc;
+  }
   // Keep the operand that the inner tile loop re-reads in L2: when one
   // group's weights fit comfortably, run column blocks innermost (m-major).
   const double b_group_bytes = (double)b_rows * K * 2.0;
@@ -460,8 +469,15 @@ int gemm_prepare(GemmPlan &p, Epi epi, const uint16_t *A, long a_rows, const uin
     case 128: p.smem = Cfg<128>::smem_bytes(G); break;
     default: p.smem = Cfg<64>::smem_bytes(G); break;
   }
-  const long max_tiles = ((max_rows + BM - 1) / BM + G) * (long)p.n_tiles;
   const long sms = device_sm_count();
+  if (p.pair) {
+    p.smem = pair_gemm_smem(G);
+    const long max_pairs = ((max_rows + 2 * BM - 1) / (2 * BM) + G) * (long)p.n_tiles;
+    const long clusters = sms / 2;
+    p.grid = 2 * (int)(max_pairs < clusters ? (max_pairs > 0 ? max_pairs : 1) : clusters);
+    return pair_gemm_configure(epi, p.smem) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  }
+  const long max_tiles = ((max_rows + BM - 1) / BM + G) * (long)p.n_tiles;
   p.grid = (int)(max_tiles < sms ? (max_tiles > 0 ? max_tiles : 1) : sms);
   return configure_gemm(p) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -483,6 +499,7 @@ static cudaError_t configure_gemm(const GemmPlan &p) {
 }
 
 cudaError_t launch_gemm(const GemmPlan &p, const Launch &l) {
+  if (p.pair) return launch_pair_gemm(p, l);
   if (p.epi == Epi::kSwiGLU) {
     if (p.bn == 256) return launch_inst<256, (int)Epi::kSwiGLU>(p, l);
     return launch_inst<128, (int)Epi::kSwiGLU>(p, l);

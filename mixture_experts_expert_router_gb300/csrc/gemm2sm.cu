@@ -1,0 +1,534 @@
+// S4 / S5 / S8 on CTA pairs: the persistent ragged grouped GEMM issued as
+// 2-SM tensor-core MMAs (tcgen05.mma.cta_group::2, M = 256).
+//
+// A cluster of two CTAs shares one tcgen05 MMA stream.  Each group's rows are
+// covered by two kinds of tiles, both 256 x (columns of one n-block):
+//
+//   main tile  256 token rows: each CTA stages 128 token rows (A) and half of
+//              the 256 weight rows (B); D = tokens x weights, each CTA's TMEM
+//              holding its own 128 token rows.
+//   tail tile  the group's last r <= 128 rows (r = rows mod 256, groups of at
+//              most 128 rows are a tail only): operands swapped, the 256
+//              weight rows take the M side (128 staged by each CTA) and the r
+//              token rows the N side (N = 16, 32, 64 or 128, half staged by
+//              each CTA); D = weights x tokens, each CTA's TMEM holding its own
+//              128 weight rows for all N tokens.  The MMA work scales with r,
+//              and the weight rows are the ones the group's main tiles of the
+//              same n-block read, so they come from L2.
+//
+// A group with 128 < r < 256 rows left over gets one more main tile whose
+// second CTA is only partly used.  Tiles past a group's rows are computed but
+// never stored.
+//
+// For FC1 (SwiGLU) a main tile's weights are 128 up rows (first CTA) and the
+// matching 128 gate rows (second CTA), so D columns 0..127 are u and 128..255
+// are g for the same outputs; a tail tile's weights are, in each CTA, 64 up
+// rows followed by the matching 64 gate rows, and the gate half hands its
+// values to the up half through shared memory.
+//
+// Synchronisation across the pair:
+//   full[s]   leader only; both CTAs' TMA loads signal it (the leader arms the
+//             transaction bytes of both);
+//   empty[s]  each CTA; arrived by the leader's commit, multicast to both;
+//   tfull[a]  each CTA; arrived by the leader's commit, multicast to both;
+//   tempty[a] leader only; one arrival per epilogue warp of both CTAs.
+// Every wait is bounded (see ptx.cuh); the pair meets at cluster barriers
+// before any CTA touches the other's shared memory and before it exits.
+#include <cuda_bf16.h>
+
+#include "launch.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;  // token (main) or weight (tail) rows per CTA
+constexpr int BN = 256;  // main tile MMA N (weight rows per pair; 128 staged by each CTA)
+constexpr int BK = 64;
+constexpr int kThreads = 192;
+constexpr int STAGES = 6;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = (BN / 2) * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // per CTA, the largest stage
+constexpr int NBARS = 2 * STAGES + 5;
+constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
+constexpr int SG_OFF = MISC_OFF + 16;           // tail gate hand-off [16][64] fp32
+constexpr int TAB_OFF = SG_OFF + 16 * 64 * 4;
+constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr uint32_t IDESC_MAIN = idesc_bf16_f32(2 * BM, BN);
+constexpr int kTailMax = 128;
+
+struct PairArgs {
+  CUtensorMap map_a;      // tokens [rows, K], box {64, 128}
+  CUtensorMap map_b;      // weights [G * b_rows, K], box {64, 128}
+  CUtensorMap map_w64;    // weights, box {64, 64} (FC1 tail tiles)
+  CUtensorMap map_t[4];   // tokens, box {64, 8 / 16 / 32 / 64} (tail tiles, N = 16..128)
+  const int32_t *group_end;
+  void *out;
+  int32_t *status;
+  long max_rows;
+  int G, K, n_out, b_rows, n_tiles, m_major;
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Barrier over the four epilogue warps of this CTA that ORs a flag across them.
+__device__ __forceinline__ bool epi_bar_any(bool flag) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, 1, 128, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)flag)
+      : "memory");
+  return r != 0;
+}
+
+// Tail tile N for r tail rows (1..128): the smallest of 16, 32, 64, 128.
+__device__ __forceinline__ int tail_n(int r) { return r <= 16 ? 16 : (r <= 32 ? 32 : (r <= 64 ? 64 : 128)); }
+__device__ __forceinline__ int tail_map(int n) { return n == 16 ? 0 : (n == 32 ? 1 : (n == 64 ? 2 : 3)); }
+
+struct PairTile {
+  int g, mp, n;   // group, m-pair index inside the group, n-block
+  int gstart;     // first row of the group
+  int tail;       // 0: main tile; else the tail's row count r (1..128)
+};
+
+// Per group: full pairs cnt / 256 plus one more tile when rows are left.
+__device__ __forceinline__ int group_pairs(int cnt) { return cnt > 0 ? (cnt + 2 * BM - 1) / (2 * BM) : 0; }
+
+__device__ __forceinline__ PairTile decode_pair_tile(int t, const int *tile_start, const int *gend, int G,
+                                                     int n_tiles, int m_major) {
+  int lo = 0, hi = G;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (tile_start[mid] * n_tiles <= t) lo = mid;
+    else hi = mid;
+  }
+  PairTile c;
+  c.g = lo;
+  const int mp = tile_start[lo + 1] - tile_start[lo];
+  const int local = t - tile_start[lo] * n_tiles;
+  if (m_major) {
+    c.mp = local / n_tiles;
+    c.n = local - c.mp * n_tiles;
+  } else {
+    c.n = local / mp;
+    c.mp = local - c.n * mp;
+  }
+  c.gstart = lo == 0 ? 0 : gend[lo - 1];
+  const int r = gend[lo] - c.gstart - c.mp * 2 * BM;  // rows from this tile's first row to the group's end
+  c.tail = (r > 0 && r <= kTailMax) ? r : 0;
+  return c;
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_constant__ PairArgs args) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char *smem = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t smem_base = smem_u32(smem);
+  const uint32_t bar_base = smem_base + BAR_OFF;
+  auto full_bar = [&](int s) { return bar_base + 8u * s; };
+  auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + 2 + a); };
+  const uint32_t drain_bar = bar_base + 8u * (2 * STAGES + 4);
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + MISC_OFF);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + MISC_OFF + 4);
+  float *sg = reinterpret_cast<float *>(smem + SG_OFF);
+  int *tile_start = reinterpret_cast<int *>(smem + TAB_OFF);
+  int *gend = tile_start + (args.G + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0 = leader
+  const int G = args.G;
+  constexpr bool kSwiGLU = EPI == (int)Epi::kSwiGLU;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 8);  // 4 epilogue warps x 2 CTAs
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&args.map_a);
+    tma_prefetch_desc(&args.map_b);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_holder), TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  pdl_wait();
+  for (int g = threadIdx.x; g < G; g += kThreads) {
+    long e = args.group_end[g];
+    e = e < 0 ? 0 : (e > args.max_rows ? args.max_rows : e);
+    gend[g] = (int)e;
+  }
+  __syncthreads();
+  if (warp == 0) {  // tile_start = prefix of per-group tile counts (per n-block)
+    int carry = 0;
+    if (lane == 0) tile_start[0] = 0;
+    for (int base = 0; base < G; base += 32) {
+      const int g = base + lane;
+      int mp = 0;
+      if (g < G) mp = group_pairs(gend[g] - (g == 0 ? 0 : gend[g - 1]));
+      int inc = mp;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+      }
+      if (g < G) tile_start[g + 1] = carry + inc;
+      carry += __shfl_sync(0xffffffffu, inc, 31);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers and TMEM exist before any cross-CTA traffic
+  tc_fence_after();
+  pdl_launch_dependents();
+
+  const uint32_t tmem_base = *tmem_holder;
+  const int total = tile_start[G] * args.n_tiles;
+  const int num_kb = args.K / BK;
+  const int cluster = blockIdx.x >> 1;
+  const int nclusters = gridDim.x >> 1;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- producers --
+      const uint64_t pol = policy_evict_normal();
+      int it = 0;
+      bool ok = true;
+      for (int t = cluster; t < total && ok; t += nclusters) {
+        const PairTile c = decode_pair_tile(t, tile_start, gend, G, args.n_tiles, args.m_major);
+        // coordinates and bytes of this CTA's operand boxes
+        int a_row, b_row, b_row2 = 0, tmap = 0;
+        uint32_t bytes;
+        if (!c.tail) {
+          a_row = c.gstart + (2 * c.mp + (int)rank) * BM;  // tokens
+          if (kSwiGLU)  // leader stages the up rows, the peer the gate rows
+            b_row = c.g * args.b_rows + c.n * (BN / 2) + (int)rank * (args.b_rows / 2);
+          else
+            b_row = c.g * args.b_rows + c.n * BN + (int)rank * (BN / 2);
+          bytes = STAGE_BYTES;
+        } else {
+          const int n = tail_n(c.tail);
+          tmap = tail_map(n);
+          if (kSwiGLU) {  // 64 up rows then the matching 64 gate rows
+            a_row = c.g * args.b_rows + c.n * (BN / 2) + (int)rank * 64;
+            b_row2 = a_row + args.b_rows / 2;
+          } else {
+            a_row = c.g * args.b_rows + c.n * BN + (int)rank * BM;
+          }
+          b_row = c.gstart + c.mp * 2 * BM + (int)rank * (n / 2);  // tail tokens
+          bytes = A_BYTES + (uint32_t)(n / 2) * BK * 2;
+        }
+        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+          if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, args.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t leader_full = mapa_shared(full_bar(s), 0);
+          if (rank == 0) mbar_arrive_expect_tx(full_bar(s), 2 * bytes);
+          const uint32_t a_dst = smem_base + s * STAGE_BYTES;
+          if (!c.tail) {
+            tma_load_2d_pair(a_dst, &args.map_a, leader_full, kb * BK, a_row, pol);
+            tma_load_2d_pair(a_dst + A_BYTES, &args.map_b, leader_full, kb * BK, b_row, pol);
+          } else {
+            if (kSwiGLU) {
+              tma_load_2d_pair(a_dst, &args.map_w64, leader_full, kb * BK, a_row, pol);
+              tma_load_2d_pair(a_dst + 64 * 128, &args.map_w64, leader_full, kb * BK, b_row2, pol);
+            } else {
+              tma_load_2d_pair(a_dst, &args.map_b, leader_full, kb * BK, a_row, pol);
+            }
+            tma_load_2d_pair(a_dst + A_BYTES, &args.map_t[tmap], leader_full, kb * BK, b_row, pol);
+          }
+        }
+      }
+      if (rank == 0) {  // let both CTAs' last copies land (they all signal the leader)
+        for (int j = it > STAGES ? it - STAGES : 0; j < it; ++j)
+          mbar_wait(full_bar(j % STAGES), (uint32_t)(j / STAGES) & 1u, nullptr, args.status);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ----------------------------------------------------- MMA issuer (leader) --
+      int it = 0, tc = 0;
+      bool ok = true;
+      for (int t = cluster; t < total && ok; t += nclusters, ++tc) {
+        const PairTile c = decode_pair_tile(t, tile_start, gend, G, args.n_tiles, args.m_major);
+        const uint32_t idesc = c.tail ? idesc_bf16_f32(2 * BM, (uint32_t)tail_n(c.tail)) : IDESC_MAIN;
+        const int acc = tc & 1;
+        const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
+        if (!mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag, args.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+          if (!mbar_wait(full_bar(s), ph, abort_flag, args.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_base + s * STAGE_BYTES;
+          const uint64_t a_desc = smem_desc_k_sw128(a_addr);
+          const uint64_t b_desc = smem_desc_k_sw128(a_addr + A_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            umma_bf16_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, (kb | k) != 0);
+          umma_commit_pair(empty_bar(s), 0x3);
+        }
+        if (ok) umma_commit_pair(tfull_bar(acc), 0x3);
+      }
+      umma_commit_pair(drain_bar, 0x1);
+      mbar_wait(drain_bar, 0, nullptr, args.status);
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue --
+    const int quarter = warp & 3;
+    const int r_in_tile = quarter * 32 + lane;  // TMEM lane: token row (main) or weight row (tail)
+    const uint32_t leader_tempty0 = mapa_shared(tempty_bar(0), 0);
+    const uint32_t leader_tempty1 = mapa_shared(tempty_bar(1), 0);
+    int tc = 0;
+    for (int t = cluster; t < total; t += nclusters, ++tc) {
+      const PairTile c = decode_pair_tile(t, tile_start, gend, G, args.n_tiles, args.m_major);
+      const int acc = tc & 1;
+      const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
+      const bool got = mbar_wait(tfull_bar(acc), aph, abort_flag, args.status);
+      if (epi_bar_any(!got)) break;  // all four warps stop together
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+      if (!c.tail) {
+        const int row0 = c.gstart + (2 * c.mp + (int)rank) * BM;
+        const int valid = gend[c.g] - row0;  // may be <= 0 for the second CTA's rows
+        const bool row_ok = r_in_tile < valid;
+        const long orow = (long)row0 + r_in_tile;
+        if (kSwiGLU) {
+          uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(args.out) +
+                                                 orow * args.n_out + (long)c.n * (BN / 2));
+#pragma unroll 1
+          for (int col = 0; col < BN / 2; col += 32) {
+            uint32_t u[32], g[32];
+            tmem_ld_32x32b_x32(taddr + col, u);
+            tmem_ld_32x32b_x32(taddr + BN / 2 + col, g);
+            tmem_ld_wait();
+            uint32_t packed[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              packed[i] = pack_bf16x2(silu_f32(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]),
+                                      silu_f32(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]));
+            if (row_ok) {
+#pragma unroll
+              for (int v = 0; v < 4; ++v)
+                dst[col / 8 + v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
+                                              packed[4 * v + 3]);
+            }
+          }
+        } else if (EPI == (int)Epi::kF32) {
+          uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<float *>(args.out) +
+                                                 orow * args.n_out + (long)c.n * BN);
+#pragma unroll 1
+          for (int col = 0; col < BN; col += 32) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(taddr + col, r);
+            tmem_ld_wait();
+            if (row_ok) {
+#pragma unroll
+              for (int v = 0; v < 8; ++v)
+                dst[col / 4 + v] = make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+            }
+          }
+        } else {
+          uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(args.out) +
+                                                 orow * args.n_out + (long)c.n * BN);
+#pragma unroll 1
+          for (int col = 0; col < BN; col += 32) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(taddr + col, r);
+            tmem_ld_wait();
+            if (row_ok) {
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                uint4 o;
+                o.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
+                o.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+                o.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+                o.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+                dst[col / 8 + v] = o;
+              }
+            }
+          }
+        }
+      } else {
+        // tail tile: lanes are weight rows, columns are the tail's tokens
+        const int n = tail_n(c.tail);
+        const long tok0 = (long)c.gstart + c.mp * 2 * BM;
+#pragma unroll 1
+        for (int c0 = 0; c0 < n; c0 += 16) {
+          uint32_t r[16];
+          asm volatile(
+              "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+              "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+              : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+                "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+              : "r"(taddr + (uint32_t)c0));
+          tmem_ld_wait();
+          if (kSwiGLU) {
+            if (r_in_tile >= 64) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) sg[j * 64 + (r_in_tile - 64)] = __uint_as_float(r[j]);
+            }
+            epi_bar();
+            if (r_in_tile < 64) {
+              __nv_bfloat16 *h = reinterpret_cast<__nv_bfloat16 *>(args.out);
+              const long col = (long)c.n * (BN / 2) + (int)rank * 64 + r_in_tile;
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (c0 + j < c.tail)
+                  h[(tok0 + c0 + j) * args.n_out + col] =
+                      __float2bfloat16_rn(silu_f32(sg[j * 64 + r_in_tile]) * __uint_as_float(r[j]));
+            }
+            epi_bar();
+          } else {
+            const long col = (long)c.n * BN + (int)rank * BM + r_in_tile;
+            if (EPI == (int)Epi::kF32) {
+              float *y = reinterpret_cast<float *>(args.out);
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (c0 + j < c.tail) y[(tok0 + c0 + j) * args.n_out + col] = __uint_as_float(r[j]);
+            } else {
+              __nv_bfloat16 *y = reinterpret_cast<__nv_bfloat16 *>(args.out);
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (c0 + j < c.tail)
+                  y[(tok0 + c0 + j) * args.n_out + col] = __float2bfloat16_rn(__uint_as_float(r[j]));
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acc ? leader_tempty1 : leader_tempty0);
+    }
+  }
+
+  __syncthreads();
+  cluster_sync();  // the peer no longer reads this CTA's shared memory or TMEM
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
+  }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+int encode(CUtensorMap *map, const void *ptr, long rows, int K, int box_rows) {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return MOE_ERR_DEVICE;
+    fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)(rows > 0 ? rows : 1)};
+  cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_TENSOR_MAP;
+}
+
+}  // namespace
+
+size_t pair_gemm_smem(int G) { return 1024 + TAB_OFF + (size_t)(2 * G + 2) * 4; }
+
+bool pair_gemm_supported(Epi epi, int n_out) {
+  return epi == Epi::kSwiGLU ? (n_out % (BN / 2) == 0) : (n_out % BN == 0);
+}
+
+int pair_gemm_encode_extra(GemmPlan &p, const uint16_t *A, long a_rows, const uint16_t *B,
+                           long b_rows_total, int K) {
+  int rc = encode(&p.map_w64, B, b_rows_total, K, 64);
+  for (int i = 0; i < 4 && rc == MOE_OK; ++i) rc = encode(&p.map_t[i], A, a_rows, K, 8 << i);
+  return rc;
+}
+
+cudaError_t pair_gemm_configure(Epi epi, size_t smem) {
+  if (epi == Epi::kSwiGLU)
+    return cudaFuncSetAttribute(pair_gemm_kernel<(int)Epi::kSwiGLU>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (epi == Epi::kF32)
+    return cudaFuncSetAttribute(pair_gemm_kernel<(int)Epi::kF32>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  return cudaFuncSetAttribute(pair_gemm_kernel<(int)Epi::kBf16>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+}
+
+cudaError_t launch_pair_gemm(const GemmPlan &p, const Launch &l) {
+  PairArgs a;
+  a.map_a = p.map_a;
+  a.map_b = p.map_b;
+  a.map_w64 = p.map_w64;
+  for (int i = 0; i < 4; ++i) a.map_t[i] = p.map_t[i];
+  a.group_end = p.group_end;
+  a.out = p.out;
+  a.status = p.status;
+  a.max_rows = p.max_rows;
+  a.G = p.G;
+  a.K = p.K;
+  a.n_out = p.n_out;
+  a.b_rows = p.b_rows;
+  a.n_tiles = p.n_tiles;
+  a.m_major = p.m_major;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = p.smem;
+  cfg.stream = l.stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = l.pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  if (p.epi == Epi::kSwiGLU) return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<(int)Epi::kSwiGLU>, a);
+  if (p.epi == Epi::kF32) return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<(int)Epi::kF32>, a);
+  return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<(int)Epi::kBf16>, a);
+}
+
+}  // namespace moe

@@ -50,6 +50,8 @@ enum class Epi : int { kBf16 = 0, kSwiGLU = 1, kF32 = 2 };
 struct GemmPlan {
   CUtensorMap map_a;            // A [rows, K] bf16, box {64, 128}
   CUtensorMap map_b;            // B [G * b_rows, K] bf16, box {64, box_b}
+  CUtensorMap map_w64;          // pair kernel: B with box {64, 64} (FC1 tail tiles)
+  CUtensorMap map_t[4];         // pair kernel: A with box {64, 8/16/32/64} (tail tiles)
   const int32_t *group_end;     // [G] cumulative group ends (device)
   int G = 0;                    // groups
   int K = 0;                    // reduction length
@@ -61,16 +63,26 @@ struct GemmPlan {
   long max_rows = 0;            // bound on total rows (grid sizing)
   void *out = nullptr;          // bf16 or fp32 output, row stride n_out
   Epi epi = Epi::kBf16;
+  int pair = 0;                 // 1: CTA-pair kernel (gemm2sm.cu), 0: one-CTA kernel
   int grid = 0;
   size_t smem = 0;
   int32_t *status = nullptr;
 };
 
-// Encodes the tensor maps and picks tile shapes; host only.
+// Encodes the tensor maps and picks tile shapes; host only.  allow_pair lets
+// it choose the CTA-pair kernel when the shape allows.
 int gemm_prepare(GemmPlan &p, Epi epi, const uint16_t *A, long a_rows, const uint16_t *B, int G,
                  int b_rows, int K, int n_out, const int32_t *group_end, long max_rows, void *out,
-                 int32_t *status);
+                 int32_t *status, bool allow_pair = true);
 cudaError_t launch_gemm(const GemmPlan &p, const Launch &l);
+
+// CTA-pair form (gemm2sm.cu)
+size_t pair_gemm_smem(int G);
+int pair_gemm_encode_extra(GemmPlan &p, const uint16_t *A, long a_rows, const uint16_t *B,
+                           long b_rows_total, int K);
+bool pair_gemm_supported(Epi epi, int n_out);
+cudaError_t pair_gemm_configure(Epi epi, size_t smem);
+cudaError_t launch_pair_gemm(const GemmPlan &p, const Launch &l);
 
 // S7: swap-AB weight-streaming GEMMs for few tokens per expert (decode.cu) ----
 struct SwapPlan {

@@ -123,7 +123,7 @@ def _rows_sample(m_indptr, n_rand, seed):
 
 
 @pytest.mark.parametrize("T,H,I,E,k", [(16, 128, 128, 4, 2), (200, 256, 192, 5, 2), (700, 512, 256, 9, 3),
-                                       (64, 128, 64, 128, 8)])
+                                       (64, 128, 64, 128, 8), (900, 256, 384, 40, 4), (300, 512, 128, 3, 3)])
 def test_fc1_fc2_stage_parity(T, H, I, E, k):
     wl = W.make_moe(T=T, H=H, I=I, E=E, top_k=k, mode="logits", seed=T)
     x, w1, w2 = W.bf16_bits(wl.x), W.bf16_bits(wl.w1), W.bf16_bits(wl.w2)
@@ -151,7 +151,9 @@ def test_fc1_fc2_stage_parity(T, H, I, E, k):
     ([5, 0, 0, 260, 1], 256, 256),
     ([130, 70, 1, 0, 64], 192, 64),
     ([1000, 3, 500], 64, 320),
-    ([0, 0, 0, 7], 1536, 512)])
+    ([0, 0, 0, 7], 1536, 512),
+    ([20, 33, 300, 0, 17, 100, 256, 512, 384, 129, 65], 512, 192),
+    ([1, 16, 32, 64, 128, 200, 255, 257], 256, 128)])
 def test_grouped_gemm_parity(sizes, N, K):
     d = W.make_grouped_gemm(seed=len(sizes), sizes=sizes, N=N, K=K)
     X, Wt, offs = d["X"].to(DEV), d["W"].to(DEV), d["offs"].to(DEV)
