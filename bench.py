@@ -245,6 +245,22 @@ def make_workload(args, rank, weights_device):
     return W.make_moe(args.config, seed=args.seed + rank, device="cpu", weights_device=weights_device)
 
 
+def recorded_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch recorded from an ncu capture under profiles/, or
+    None when none exists or the kernel source changed since it was taken."""
+    import hashlib
+    src = os.path.join(ROOT, "mixture_experts_expert_router_gb300", "csrc", "gemm2sm.cu")
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        for line in open(os.path.join(ROOT, "profiles", "pair_gemm_dram_prefill.md")):
+            f = line.split()
+            if len(f) == 5 and f[0] == "traffic" and f[1] == workload and f[2] == kernel:
+                return int(f[3]) if f[4] == sha else None
+    except OSError:
+        pass
+    return None
+
+
 def roofline_entry(decode_path, fc1_s, F_fc1, B_fc1, peak_t, peak_b, peak_src, traffic):
     """Dominant kernel (FC1 + SwiGLU): tensor-bound on the grouped path,
     HBM-bound (weight streaming) on the decode path."""
@@ -410,12 +426,7 @@ def run_ours(args, world, rank, local):
     # FC1's algorithmic bytes: W1 of the active experts, its gathered input rows, h written
     B_fc1 = active * 2.0 * wl.I * wl.H * 2 + M * wl.H * 2.0 + M * wl.I * 2.0
     decode_path = plan.buffers()["path"] == moe.PATH_DECODE
-    traffic = None
-    try:
-        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            traffic = json.load(f).get(wl.name, {}).get("fc1_swiglu")
-    except Exception:
-        traffic = None
+    traffic = None if decode_path else recorded_traffic(wl.name, "fc1_swiglu")
 
     if rank != 0:
         return 0
