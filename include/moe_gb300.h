@@ -157,6 +157,22 @@ MOE_API int moe_fc1_swiglu(const moe_bf16 *xp, const moe_bf16 *w1,
                    const int32_t *m_indptr, int max_rows, int H, int I,
                    int num_local, moe_bf16 *h, void *stream);
 
+/* ---- S3 + S4 fused: FC1 + SwiGLU reading its rows through the permutation --------
+ * h[p] = bf16_rne(silu(g) * u) for permuted row p < M with the activations
+ * taken straight from x: row p is x[perm_to_exp[p] / top_k] (no xp buffer).
+ * The producer loads four rows per TMA row-gather.  Same result as
+ * moe_gather followed by moe_fc1_swiglu, without the [T*top_k, H] buffer of
+ * gathered rows, but slower: 32 row-gathers per 128-row k-block cost more
+ * than the extra pass (measured 4.2 ms against 1.34 ms + 0.02 ms for the
+ * gather at T=4096, H=4096, I=14336, E=8, top-2); moe_forward uses the gather
+ * kernel. */
+ *   x [T, H] bf16, perm_to_exp [T*top_k], m_indptr [L+1], w1 [L, 2I, H],
+ *   h [T*top_k, I] bf16.  H % 64 == 0, I % 128 == 0. */
+MOE_API int moe_fc1_swiglu_gathered(const moe_bf16 *x, const int32_t *perm_to_exp,
+                                    const int32_t *m_indptr, int T, int top_k,
+                                    const moe_bf16 *w1, int H, int I, int num_local,
+                                    moe_bf16 *h, void *stream);
+
 /* ---- S5 FC2 ------------------------------------------------------------------------
  * y[p] = h[p] . W2[i]^T, fp32, unscaled and unrounded (cute_dsl_fused_moe_bf16,
  * Parameters, use_fused_finalize=False).

@@ -24,7 +24,7 @@ import torch
 __all__ = [
     "MoEError", "library", "library_path", "moe_status_string", "moe_route", "moe_sort", "moe_sort_no_alloc",
     "moe_sort_workspace_size", "moe_gather", "moe_fc1_swiglu", "moe_fc2", "moe_finalize",
-    "moe_fc1_swiglu_swapab", "moe_fc2_swapab",
+    "moe_fc1_swiglu_swapab", "moe_fc2_swapab", "moe_fc1_swiglu_gathered",
     "grouped_gemm_fwd", "moe_workspace_size", "moe_forward", "MoEPlan", "ABI_SYMBOLS",
     "PATH_AUTO", "PATH_GROUPED", "PATH_DECODE", "DEV_BAD_EXPERT", "DEV_TIMEOUT",
 ]
@@ -45,7 +45,7 @@ ABI_SYMBOLS = [
     "moe_workspace_size", "moe_forward", "moe_forward_prepare", "moe_plan_launch",
     "moe_plan_buffers_get", "moe_plan_stage_count", "moe_plan_stage_name", "moe_plan_stage_times",
     "moe_plan_stage_reset", "moe_plan_kernels_per_launch", "moe_plan_destroy", "moe_sort_no_alloc",
-    "moe_fc1_swiglu_swapab", "moe_fc2_swapab",
+    "moe_fc1_swiglu_swapab", "moe_fc2_swapab", "moe_fc1_swiglu_gathered",
 ]
 
 
@@ -101,6 +101,7 @@ def library():
             "moe_fc1_swiglu": ([P, P, P, I, I, I, I, P, P], I),
             "moe_fc2": ([P, P, P, I, I, I, I, P, P], I),
             "moe_fc1_swiglu_swapab": ([P, P, P, I, I, I, I, I, P, P], I),
+            "moe_fc1_swiglu_gathered": ([P, P, P, I, I, P, I, I, I, P, P], I),
             "moe_fc2_swapab": ([P, P, P, I, I, I, I, I, P, P], I),
             "moe_finalize": ([P, P, P, I, I, I, P, P], I),
             "grouped_gemm_fwd": ([P, P, P, I, I, I, I, P, P], I),
@@ -266,6 +267,25 @@ def moe_fc2(h: torch.Tensor, w2: torch.Tensor, m_indptr: torch.Tensor, y=None):
     _check(library().moe_fc2(_ptr(h), _ptr(w2), _ptr(m_indptr), rows, H, I, L, _ptr(y),
                              _stream(h.device)), "moe_fc2")
     return y
+
+
+def moe_fc1_swiglu_gathered(x: torch.Tensor, perm_to_exp: torch.Tensor, m_indptr: torch.Tensor, top_k: int,
+                            w1: torch.Tensor, h=None):
+    """FC1 + SwiGLU with the rows taken straight from x through the permutation."""
+    _need(x, torch.bfloat16, "x")
+    _need(perm_to_exp, torch.int32, "perm_to_exp")
+    _need(m_indptr, torch.int32, "m_indptr")
+    _need(w1, torch.bfloat16, "w1")
+    T, H = x.shape
+    L, twoI, H2 = w1.shape
+    if H2 != H or twoI % 2:
+        raise ValueError("w1 must be [L, 2I, H]")
+    I = twoI // 2
+    h = torch.empty((T * top_k, I), dtype=torch.bfloat16, device=x.device) if h is None else h
+    _need(h, torch.bfloat16, "h", (T * top_k, I), x.device)
+    _check(library().moe_fc1_swiglu_gathered(_ptr(x), _ptr(perm_to_exp), _ptr(m_indptr), T, top_k, _ptr(w1),
+                                             H, I, L, _ptr(h), _stream(x.device)), "moe_fc1_swiglu_gathered")
+    return h
 
 
 def moe_fc1_swiglu_swapab(xp: torch.Tensor, w1: torch.Tensor, m_indptr: torch.Tensor, max_group_rows: int,

@@ -103,6 +103,7 @@ struct moe_plan {
   float *y;
   GemmPlan fc1, fc2;
   SwapPlan fc1d, fc2d;  // decode path
+  bool fused_gather;    // grouped path: FC1 gathers its rows itself
   bool timing;
   cudaEvent_t (*ev)[kNumStages + 1];
   long n_recorded;
@@ -235,6 +236,26 @@ int moe_fc2(const moe_bf16 *h, const moe_bf16 *w2, const int32_t *m_indptr, int 
   return cuda_rc(launch_gemm(p, l));
 }
 
+int moe_fc1_swiglu_gathered(const moe_bf16 *x, const int32_t *perm_to_exp,
+                            const int32_t *m_indptr, int T, int top_k, const moe_bf16 *w1, int H,
+                            int I, int num_local, moe_bf16 *h, void *stream) {
+  if (T < 0 || top_k < 1 || top_k > MOE_MAX_TOP_K || H <= 0 || H % 64 || I <= 0 || I % 128 ||
+      num_local < 1 || num_local > MOE_MAX_EXPERTS)
+    return MOE_ERR_SHAPE;
+  if (T == 0) return MOE_OK;
+  if (!x || !perm_to_exp || !m_indptr || !w1 || !h) return MOE_ERR_NULL;
+  if (!aligned16(x) || !aligned16(w1) || !aligned16(h)) return MOE_ERR_ALIGN;
+  if (int rc = check_device()) return rc;
+  GemmPlan p;
+  const long R = (long)T * top_k;
+  if (int rc = gemm_prepare_gather(p, x, T, perm_to_exp, top_k, w1, num_local, I, H, m_indptr + 1,
+                                   R, h, nullptr))
+    return rc;
+  Launch l;
+  l.stream = static_cast<cudaStream_t>(stream);
+  return cuda_rc(launch_gemm(p, l));
+}
+
 int moe_fc1_swiglu_swapab(const moe_bf16 *xp, const moe_bf16 *w1, const int32_t *m_indptr,
                           int max_rows, int max_group_rows, int H, int I, int num_local,
                           moe_bf16 *h, void *stream) {
@@ -357,8 +378,16 @@ int moe_forward_prepare(const moe_forward_desc *desc, moe_plan **plan_out) {
                           p->m_indptr + 1, d.T, p->y, d.status, true);
     } else {
       const bool pair = (d.flags & MOE_PLAN_ONE_CTA_GEMM) == 0;
-      rc = gemm_prepare(p->fc1, Epi::kSwiGLU, p->xp, p->R, d.w1, d.num_local, 2 * d.I, d.H, d.I,
-                        p->m_indptr + 1, p->R, p->h, d.status, pair);
+      // The gather kernel builds xp: one 128-row TMA box per k-block feeds
+      // the tensor cores, while gathering the rows inside FC1 (four rows per
+      // TMA row-gather, moe_fc1_swiglu_gathered) measured 3x slower for FC1.
+      p->fused_gather = false;
+      if (p->fused_gather)
+        rc = gemm_prepare_gather(p->fc1, d.x, d.T, p->p2e, d.top_k, d.w1, d.num_local, d.I, d.H,
+                                 p->m_indptr + 1, p->R, p->h, d.status);
+      else
+        rc = gemm_prepare(p->fc1, Epi::kSwiGLU, p->xp, p->R, d.w1, d.num_local, 2 * d.I, d.H, d.I,
+                          p->m_indptr + 1, p->R, p->h, d.status, pair);
       if (rc == MOE_OK)
         rc = gemm_prepare(p->fc2, Epi::kF32, p->h, p->R, d.w2, d.num_local, d.H, d.I, d.H,
                           p->m_indptr + 1, p->R, p->y, d.status, pair);
@@ -414,8 +443,9 @@ int moe_plan_launch(moe_plan *p, void *stream) {
                   p->sort_ws, d.status, l) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (!mark(kGather)) return MOE_ERR_CUDA;
-  if (launch_gather(d.x, p->p2e, p->m_indptr + d.num_local, d.H, d.top_k, p->R, p->xp, l) !=
-      cudaSuccess)
+  if (!p->fused_gather &&
+      launch_gather(d.x, p->p2e, p->m_indptr + d.num_local, d.H, d.top_k, p->R, p->xp, l) !=
+          cudaSuccess)
     return MOE_ERR_CUDA;
   const bool dec = p->path == MOE_PATH_DECODE;
   if (!mark(kFc1)) return MOE_ERR_CUDA;
@@ -475,7 +505,7 @@ int moe_plan_kernels_per_launch(const moe_plan *p) {
   if (!p || p->d.T == 0) return 0;
   int n = p->logits_mode ? 1 : 0;                       // route
   n += p->R <= kSortSingleMax ? 1 : 3;                  // sort
-  n += 1 + 1 + 1 + 1;                                   // gather, fc1, fc2, finalize
+  n += (p->fused_gather ? 0 : 1) + 1 + 1 + 1;           // gather, fc1, fc2, finalize
   return n;
 }
 

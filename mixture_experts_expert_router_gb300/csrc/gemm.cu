@@ -498,6 +498,21 @@ static cudaError_t configure_gemm(const GemmPlan &p) {
   return configure_inst<64, (int)Epi::kBf16>(p);
 }
 
+int gemm_prepare_gather(GemmPlan &p, const uint16_t *x, long x_rows, const int32_t *p2e, int k,
+                        const uint16_t *W1, int G, int I, int H, const int32_t *group_end,
+                        long max_rows, void *h, int32_t *status) {
+  if (!pair_gemm_supported(Epi::kSwiGLU, I) || k < 1) return MOE_ERR_SHAPE;
+  // the direct-row maps still need a valid base: point them at x
+  int rc = gemm_prepare(p, Epi::kSwiGLU, x, x_rows, W1, G, 2 * I, H, I, group_end, max_rows, h,
+                        status, true);
+  if (rc != MOE_OK) return rc;
+  p.gather_x = x;
+  p.gather_p2e = p2e;
+  p.gather_rows = x_rows;
+  p.gather_k = k;
+  return pair_gemm_encode_extra(p, x, x_rows, W1, (long)G * 2 * I, H);
+}
+
 cudaError_t launch_gemm(const GemmPlan &p, const Launch &l) {
   if (p.pair) return launch_pair_gemm(p, l);
   if (p.epi == Epi::kSwiGLU) {

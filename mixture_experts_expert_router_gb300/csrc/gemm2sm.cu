@@ -64,6 +64,10 @@ struct PairArgs {
   CUtensorMap map_b;      // weights [G * b_rows, K], box {64, 128}
   CUtensorMap map_w64;    // weights, box {64, 64} (FC1 tail tiles)
   CUtensorMap map_t[4];   // tokens, box {64, 8 / 16 / 32 / 64} (tail tiles, N = 16..128)
+  CUtensorMap map_xg;     // gather mode: token rows of x [x_rows, K], box {64, 1}
+  const int32_t *p2e;     // gather mode: permuted row -> expanded index
+  long x_rows;
+  int gather_k;           // gather mode: top_k (token = p2e[row] / top_k); 0 = rows given directly
   const int32_t *group_end;
   void *out;
   int32_t *status;
@@ -212,63 +216,102 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
   const int nclusters = gridDim.x >> 1;
 
   if (warp == 0) {
-    if (lane == 0) {
-      // ---------------------------------------------------------- producers --
-      const uint64_t pol = policy_evict_normal();
-      int it = 0;
-      bool ok = true;
-      for (int t = cluster; t < total && ok; t += nclusters) {
-        const PairTile c = decode_pair_tile(t, tile_start, gend, G, args.n_tiles, args.m_major);
-        // coordinates and bytes of this CTA's operand boxes
-        int a_row, b_row, b_row2 = 0, tmap = 0;
-        uint32_t bytes;
-        if (!c.tail) {
-          a_row = c.gstart + (2 * c.mp + (int)rank) * BM;  // tokens
-          if (kSwiGLU)  // leader stages the up rows, the peer the gate rows
-            b_row = c.g * args.b_rows + c.n * (BN / 2) + (int)rank * (args.b_rows / 2);
-          else
-            b_row = c.g * args.b_rows + c.n * BN + (int)rank * (BN / 2);
-          bytes = STAGE_BYTES;
+    // -------------------------------------------------------------- producers --
+    // Lane 0 waits, arms the leader's barrier and loads the weights; in
+    // gather mode every lane also loads four token rows of x per k-block.
+    const uint64_t pol = policy_evict_normal();
+    const bool gath = args.gather_k > 0;
+    const int m_total = G > 0 ? gend[G - 1] : 0;
+    int it = 0;
+    bool ok = true;
+    for (int t = cluster; t < total && ok; t += nclusters) {
+      const PairTile c = decode_pair_tile(t, tile_start, gend, G, args.n_tiles, args.m_major);
+      // coordinates and bytes of this CTA's operand boxes
+      int a_row, b_row, b_row2 = 0, tmap = 0, tok_rows;
+      uint32_t bytes;
+      if (!c.tail) {
+        a_row = c.gstart + (2 * c.mp + (int)rank) * BM;  // tokens
+        if (kSwiGLU)  // leader stages the up rows, the peer the gate rows
+          b_row = c.g * args.b_rows + c.n * (BN / 2) + (int)rank * (args.b_rows / 2);
+        else
+          b_row = c.g * args.b_rows + c.n * BN + (int)rank * (BN / 2);
+        bytes = STAGE_BYTES;
+        tok_rows = BM;
+      } else {
+        const int n = tail_n(c.tail);
+        tmap = tail_map(n);
+        if (kSwiGLU) {  // 64 up rows then the matching 64 gate rows
+          a_row = c.g * args.b_rows + c.n * (BN / 2) + (int)rank * 64;
+          b_row2 = a_row + args.b_rows / 2;
         } else {
-          const int n = tail_n(c.tail);
-          tmap = tail_map(n);
-          if (kSwiGLU) {  // 64 up rows then the matching 64 gate rows
-            a_row = c.g * args.b_rows + c.n * (BN / 2) + (int)rank * 64;
-            b_row2 = a_row + args.b_rows / 2;
-          } else {
-            a_row = c.g * args.b_rows + c.n * BN + (int)rank * BM;
-          }
-          b_row = c.gstart + c.mp * 2 * BM + (int)rank * (n / 2);  // tail tokens
-          bytes = A_BYTES + (uint32_t)(n / 2) * BK * 2;
+          a_row = c.g * args.b_rows + c.n * BN + (int)rank * BM;
         }
-        for (int kb = 0; kb < num_kb; ++kb, ++it) {
-          const int s = it % STAGES;
-          const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
-          if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, args.status)) {
-            ok = false;
-            break;
-          }
-          const uint32_t leader_full = mapa_shared(full_bar(s), 0);
-          if (rank == 0) mbar_arrive_expect_tx(full_bar(s), 2 * bytes);
-          const uint32_t a_dst = smem_base + s * STAGE_BYTES;
-          if (!c.tail) {
+        b_row = c.gstart + c.mp * 2 * BM + (int)rank * (n / 2);  // tail tokens
+        bytes = A_BYTES + (uint32_t)(n / 2) * BK * 2;
+        tok_rows = n / 2;
+      }
+      // gather mode: this lane's four token rows (rows past the routed ones read row 0)
+      int tr0 = 0, tr1 = 0, tr2 = 0, tr3 = 0;
+      const bool tok_lane = gath && lane < tok_rows / 4;
+      if (tok_lane) {
+        const int p0 = (c.tail ? b_row : a_row) + 4 * lane;
+        int tr[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int p = p0 + i;
+          const int tkn = p < m_total ? args.p2e[p] / args.gather_k : 0;
+          tr[i] = (tkn < 0 || tkn >= args.x_rows) ? 0 : tkn;
+        }
+        tr0 = tr[0];
+        tr1 = tr[1];
+        tr2 = tr[2];
+        tr3 = tr[3];
+      }
+      for (int kb = 0; kb < num_kb; ++kb, ++it) {
+        const int s = it % STAGES;
+        const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+        int w_ok = 1;
+        if (lane == 0) w_ok = mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, args.status) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
+          ok = false;
+          break;
+        }
+        const uint32_t leader_full = mapa_shared(full_bar(s), 0);
+        if (lane == 0 && rank == 0) mbar_arrive_expect_tx(full_bar(s), 2 * bytes);
+        __syncwarp();
+        const uint32_t a_dst = smem_base + s * STAGE_BYTES;
+        if (!c.tail) {
+          if (gath) {
+            if (tok_lane)
+              tma_gather4_pair(a_dst + lane * 512, &args.map_xg, leader_full, kb * BK, tr0, tr1, tr2,
+                               tr3, pol);
+          } else if (lane == 0) {
             tma_load_2d_pair(a_dst, &args.map_a, leader_full, kb * BK, a_row, pol);
+          }
+          if (lane == 0)
             tma_load_2d_pair(a_dst + A_BYTES, &args.map_b, leader_full, kb * BK, b_row, pol);
-          } else {
+        } else {
+          if (lane == 0) {
             if (kSwiGLU) {
               tma_load_2d_pair(a_dst, &args.map_w64, leader_full, kb * BK, a_row, pol);
               tma_load_2d_pair(a_dst + 64 * 128, &args.map_w64, leader_full, kb * BK, b_row2, pol);
             } else {
               tma_load_2d_pair(a_dst, &args.map_b, leader_full, kb * BK, a_row, pol);
             }
+          }
+          if (gath) {
+            if (tok_lane)
+              tma_gather4_pair(a_dst + A_BYTES + lane * 512, &args.map_xg, leader_full, kb * BK, tr0,
+                               tr1, tr2, tr3, pol);
+          } else if (lane == 0) {
             tma_load_2d_pair(a_dst + A_BYTES, &args.map_t[tmap], leader_full, kb * BK, b_row, pol);
           }
         }
       }
-      if (rank == 0) {  // let both CTAs' last copies land (they all signal the leader)
-        for (int j = it > STAGES ? it - STAGES : 0; j < it; ++j)
-          mbar_wait(full_bar(j % STAGES), (uint32_t)(j / STAGES) & 1u, nullptr, args.status);
-      }
+    }
+    if (lane == 0 && rank == 0) {  // let both CTAs' last copies land (they all signal the leader)
+      for (int j = it > STAGES ? it - STAGES : 0; j < it; ++j)
+        mbar_wait(full_bar(j % STAGES), (uint32_t)(j / STAGES) & 1u, nullptr, args.status);
     }
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
@@ -482,6 +525,7 @@ int pair_gemm_encode_extra(GemmPlan &p, const uint16_t *A, long a_rows, const ui
                            long b_rows_total, int K) {
   int rc = encode(&p.map_w64, B, b_rows_total, K, 64);
   for (int i = 0; i < 4 && rc == MOE_OK; ++i) rc = encode(&p.map_t[i], A, a_rows, K, 8 << i);
+  if (rc == MOE_OK && p.gather_k > 0) rc = encode(&p.map_xg, p.gather_x, p.gather_rows, K, 1);
   return rc;
 }
 
@@ -502,6 +546,10 @@ cudaError_t launch_pair_gemm(const GemmPlan &p, const Launch &l) {
   a.map_b = p.map_b;
   a.map_w64 = p.map_w64;
   for (int i = 0; i < 4; ++i) a.map_t[i] = p.map_t[i];
+  a.map_xg = p.map_xg;
+  a.p2e = p.gather_p2e;
+  a.x_rows = p.gather_rows;
+  a.gather_k = p.gather_k;
   a.group_end = p.group_end;
   a.out = p.out;
   a.status = p.status;

@@ -52,6 +52,11 @@ struct GemmPlan {
   CUtensorMap map_b;            // B [G * b_rows, K] bf16, box {64, box_b}
   CUtensorMap map_w64;          // pair kernel: B with box {64, 64} (FC1 tail tiles)
   CUtensorMap map_t[4];         // pair kernel: A with box {64, 8/16/32/64} (tail tiles)
+  CUtensorMap map_xg;           // pair kernel, gather mode: x with box {64, 1}
+  const uint16_t *gather_x = nullptr;   // gather mode: rows of A are x[p2e[p] / k]
+  const int32_t *gather_p2e = nullptr;
+  long gather_rows = 0;
+  int gather_k = 0;             // 0: A rows are given directly
   const int32_t *group_end;     // [G] cumulative group ends (device)
   int G = 0;                    // groups
   int K = 0;                    // reduction length
@@ -74,6 +79,11 @@ struct GemmPlan {
 int gemm_prepare(GemmPlan &p, Epi epi, const uint16_t *A, long a_rows, const uint16_t *B, int G,
                  int b_rows, int K, int n_out, const int32_t *group_end, long max_rows, void *out,
                  int32_t *status, bool allow_pair = true);
+// The same for FC1 reading its rows straight from x through the permutation
+// (row p of A = x[p2e[p] / k]); CTA-pair kernel only (MOE_ERR_SHAPE otherwise).
+int gemm_prepare_gather(GemmPlan &p, const uint16_t *x, long x_rows, const int32_t *p2e, int k,
+                        const uint16_t *W1, int G, int I, int H, const int32_t *group_end,
+                        long max_rows, void *h, int32_t *status);
 cudaError_t launch_gemm(const GemmPlan &p, const Launch &l);
 
 // CTA-pair form (gemm2sm.cu)

@@ -296,3 +296,33 @@ __device__ __forceinline__ void umma_commit_pair(uint32_t bar, uint16_t mask) {
 }
 
 }  // namespace moe
+
+namespace moe {
+
+// Row-gather TMA: four rows of a 2-D tensor (row indices r0..r3, any order),
+// columns x .. x+63, into 512 consecutive bytes of shared memory with the
+// tensor map's swizzle.  The tensor map's box is {64, 1}.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int32_t x, int32_t r0, int32_t r1, int32_t r2,
+                                            int32_t r3, uint64_t cache_policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar),
+      "l"(cache_policy)
+      : "memory");
+}
+
+// The same, signalling an mbarrier of either CTA of a pair.
+__device__ __forceinline__ void tma_gather4_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                                 int32_t x, int32_t r0, int32_t r1, int32_t r2,
+                                                 int32_t r3, uint64_t cache_policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4.mbarrier::"
+      "complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar),
+      "l"(cache_policy)
+      : "memory");
+}
+
+}  // namespace moe

@@ -201,3 +201,24 @@ def test_swapab_fc1_fc2_stage_parity(T, H, I, E, k, max_group):
     # the decode-form and grouped FC2 read the same h: compare the two kernels too
     y_grouped = moe.moe_fc2(W.from_bf16_bits(h_full).to(DEV), wl.w2.to(DEV), m_d)
     check_f32_close(y_g.cpu().numpy()[rows], y_grouped.cpu().numpy()[rows], "y swap-AB vs grouped")
+
+
+@pytest.mark.parametrize("T,H,I,E,k", [(16, 128, 128, 4, 2), (700, 512, 256, 9, 3), (900, 256, 384, 40, 4),
+                                       (300, 192, 128, 3, 3), (5, 64, 128, 64, 8)])
+def test_fc1_gathered_stage_parity(T, H, I, E, k):
+    """FC1 taking its rows straight from x through the permutation (TMA row
+    gathers) against the oracle's FC1 on the gathered rows."""
+    wl = W.make_moe(T=T, H=H, I=I, E=E, top_k=k, mode="logits", seed=T + 3)
+    x, w1 = W.bf16_bits(wl.x), W.bf16_bits(wl.w1)
+    ids, _ = oracle.route(wl.logits.numpy(), k)
+    m, p2e, e2p, _ = oracle.sort(ids, E)
+    R = T * k
+    p2e_full = np.zeros(R, np.int32)
+    p2e_full[:len(p2e)] = p2e
+    h_g = moe.moe_fc1_swiglu_gathered(wl.x.to(DEV), torch.from_numpy(p2e_full).to(DEV),
+                                      torch.from_numpy(m).to(DEV), k, wl.w1.to(DEV))
+    rows = np.arange(len(p2e), dtype=np.int32)
+    xp = np.zeros((R, H), np.uint16)
+    xp[:len(p2e)] = x[p2e // k]
+    h_o = oracle.fc1_swiglu_rows(xp, w1, m[1:], rows)
+    check_bf16_close(W.bf16_bits(h_g)[rows], h_o, "h (gathered rows)")
