@@ -295,12 +295,13 @@ def run_ours(args, world, rank, local):
     tids = wl.topk_ids.to(dev) if wl.topk_ids is not None else None
     tw = wl.topk_w.to(dev) if wl.topk_w is not None else None
     status = torch.zeros(1, dtype=torch.int32, device=dev)
+    opts = dict(decode_chain=args.decode_chain, one_cta_gemm=args.one_cta_gemm)
     plan = moe.MoEPlan(x, wl.w1, wl.w2, wl.E, wl.top_k, logits=logits, topk_ids=tids, topk_w=tw,
-                       local_offset=wl.local_offset, status=status)
+                       local_offset=wl.local_offset, status=status, **opts)
     # a second plan on the same buffers records CUDA events around every stage
     plan_t = moe.MoEPlan(x, wl.w1, wl.w2, wl.E, wl.top_k, logits=logits, topk_ids=tids, topk_w=tw,
                          local_offset=wl.local_offset, status=status, out=plan.out,
-                         workspace=plan.workspace, stage_timing=True)
+                         workspace=plan.workspace, stage_timing=True, **opts)
     kernels = plan.kernels_per_launch()
     stream = torch.cuda.current_stream(dev)
 
@@ -477,6 +478,8 @@ def main():
                     help="T,H,I,E,top_k of a custom logits-routed workload (profiling runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch the plan directly instead of a CUDA graph")
+    ap.add_argument("--decode-chain", action="store_true", help="decode path: two-kernel chain (comparison)")
+    ap.add_argument("--one-cta-gemm", action="store_true", help="grouped path: one-CTA GEMMs (comparison)")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--reference-budget", type=float, default=120.0,
                     help="seconds of oracle work for the whole --impl reference run")

@@ -165,7 +165,7 @@ MOE_API int moe_fc1_swiglu(const moe_bf16 *xp, const moe_bf16 *w1,
  * gathered rows, but slower: 32 row-gathers per 128-row k-block cost more
  * than the extra pass (measured 4.2 ms against 1.34 ms + 0.02 ms for the
  * gather at T=4096, H=4096, I=14336, E=8, top-2); moe_forward uses the gather
- * kernel. */
+ * kernel.
  *   x [T, H] bf16, perm_to_exp [T*top_k], m_indptr [L+1], w1 [L, 2I, H],
  *   h [T*top_k, I] bf16.  H % 64 == 0, I % 128 == 0. */
 MOE_API int moe_fc1_swiglu_gathered(const moe_bf16 *x, const int32_t *perm_to_exp,
@@ -252,6 +252,9 @@ MOE_API int moe_forward(const moe_bf16 *x, const float *logits, const int32_t *t
 #define MOE_PLAN_STAGE_TIMING 1 /* record CUDA events around each stage     */
 #define MOE_PLAN_ONE_CTA_GEMM 2 /* grouped path: one-CTA GEMM kernels instead of
                                    the CTA-pair (2-SM MMA) kernels (comparison) */
+#define MOE_PLAN_DECODE_CHAIN 4 /* decode path, T*top_k <= 1024: two kernels with
+                                   the sort, gather and finalize folded in, instead
+                                   of five (fewer launches; measured slower) */
 
 typedef struct moe_forward_desc {
     const moe_bf16 *x;

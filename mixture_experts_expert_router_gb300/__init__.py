@@ -35,6 +35,7 @@ _LIB_PATH = os.path.join(_HERE, "libmoe_gb300.so")
 PATH_AUTO, PATH_GROUPED, PATH_DECODE = 0, 1, 2
 PLAN_STAGE_TIMING = 1
 PLAN_ONE_CTA_GEMM = 2
+PLAN_DECODE_CHAIN = 4
 DEV_BAD_EXPERT, DEV_TIMEOUT = 1, 2
 MAX_EXPERTS, MAX_TOP_K = 1024, 16
 
@@ -403,7 +404,7 @@ class MoEPlan:
 
     def __init__(self, x, w1, w2, num_experts: int, top_k: int, logits=None, topk_ids=None, topk_w=None,
                  local_offset: int = 0, out=None, workspace=None, status=None, path: int = PATH_AUTO,
-                 stage_timing: bool = False, one_cta_gemm: bool = False):
+                 stage_timing: bool = False, one_cta_gemm: bool = False, decode_chain: bool = False):
         T, H, I, L, out = _layer_args(x, w1, w2, num_experts, top_k, logits, topk_ids, topk_w,
                                       local_offset, out)
         dev = x.device
@@ -421,7 +422,8 @@ class MoEPlan:
                   w1=_ptr(w1), w2=_ptr(w2), out=_ptr(out), workspace=_ptr(workspace),
                   workspace_bytes=workspace.numel(), status=_ptr(status), T=T, H=H, I=I, E=num_experts,
                   top_k=top_k, local_offset=local_offset, num_local=L, path=path,
-                  flags=(PLAN_STAGE_TIMING if stage_timing else 0) | (PLAN_ONE_CTA_GEMM if one_cta_gemm else 0))
+                  flags=(PLAN_STAGE_TIMING if stage_timing else 0) | (PLAN_ONE_CTA_GEMM if one_cta_gemm else 0)
+                  | (PLAN_DECODE_CHAIN if decode_chain else 0))
         handle = ctypes.c_void_p()
         _check(library().moe_forward_prepare(ctypes.byref(d), ctypes.byref(handle)), "moe_forward_prepare")
         self._h = handle

@@ -46,7 +46,7 @@ int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct WsLayout {
-  size_t ids, w, m_indptr, p2e, e2p, sort_ws, xp, h, y, total;
+  size_t ids, w, m_indptr, p2e, e2p, sort_ws, xp, h, y, comb, total;
 };
 
 WsLayout ws_layout(long T, int H, int I, int k, int L) {
@@ -67,6 +67,7 @@ WsLayout ws_layout(long T, int H, int I, int k, int L) {
   o.xp = take(R * (size_t)H * 2);
   o.h = take(R * (size_t)I * 2);
   o.y = take(R * (size_t)H * 4);
+  o.comb = take(chain_comb_ints((int)T, H) * 4);
   o.total = off;
   return o;
 }
@@ -102,7 +103,9 @@ struct moe_plan {
   uint16_t *xp, *h;
   float *y;
   GemmPlan fc1, fc2;
-  SwapPlan fc1d, fc2d;  // decode path
+  SwapPlan fc1d, fc2d;  // decode path, separate kernels
+  ChainPlan chain;      // decode path, two-kernel chain
+  bool use_chain;
   bool fused_gather;    // grouped path: FC1 gathers its rows itself
   bool timing;
   cudaEvent_t (*ev)[kNumStages + 1];
@@ -370,7 +373,36 @@ int moe_forward_prepare(const moe_forward_desc *desc, moe_plan **plan_out) {
     p->h = reinterpret_cast<uint16_t *>(ws + lay.h);
     p->y = reinterpret_cast<float *>(ws + lay.y);
     int rc;
-    if (p->path == MOE_PATH_DECODE) {
+    // The separate decode kernels measured faster than the chain (its in-kernel
+    // row gathers and combine cost more than the three launches they save),
+    // so the chain runs only when asked for.
+    p->use_chain = p->path == MOE_PATH_DECODE && p->R <= kChainMaxRoutes &&
+                   (d.flags & MOE_PLAN_DECODE_CHAIN) != 0;
+    if (p->use_chain) {
+      ChainPlan &c = p->chain;
+      c.x = d.x;
+      c.w1 = d.w1;
+      c.w2 = d.w2;
+      c.ids = p->ids;
+      c.w = p->w;
+      c.h = p->h;
+      c.y = p->y;
+      c.out = d.out;
+      c.comb = reinterpret_cast<int32_t *>(ws + lay.comb);
+      c.m_indptr = p->m_indptr;
+      c.p2e = p->p2e;
+      c.e2p = p->e2p;
+      c.status = d.status;
+      c.T = d.T;
+      c.k = d.top_k;
+      c.E = d.E;
+      c.off = d.local_offset;
+      c.L = d.num_local;
+      c.H = d.H;
+      c.I = d.I;
+      c.ids_early = !logits_mode;
+      rc = chain_prepare(c);
+    } else if (p->path == MOE_PATH_DECODE) {
       rc = swap_prepare(p->fc1d, true, d.w1, d.num_local, 2 * d.I, d.H, p->xp, p->R, d.I,
                         p->m_indptr + 1, d.T, p->h, d.status, true);
       if (rc == MOE_OK)
@@ -424,7 +456,9 @@ int moe_plan_launch(moe_plan *p, void *stream) {
   if (!p) return MOE_ERR_NULL;
   const moe_forward_desc &d = p->d;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (d.status && cudaMemsetAsync(d.status, 0, sizeof(int32_t), s) != cudaSuccess)
+  // the decode chain's first kernel clears the status word itself
+  if (d.status && (d.T == 0 || !p->use_chain) &&
+      cudaMemsetAsync(d.status, 0, sizeof(int32_t), s) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (d.T == 0) return MOE_OK;
   Launch l;
@@ -437,6 +471,15 @@ int moe_plan_launch(moe_plan *p, void *stream) {
   if (!mark(kRoute)) return MOE_ERR_CUDA;
   if (p->logits_mode) {
     if (launch_route(d.logits, d.T, d.E, d.top_k, p->ids, p->w, l) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  if (p->use_chain) {  // sort, gather and finalize run inside the two GEMM kernels
+    if (!mark(kSort) || !mark(kGather) || !mark(kFc1)) return MOE_ERR_CUDA;
+    if (launch_chain(p->chain, true, l) != cudaSuccess) return MOE_ERR_CUDA;
+    if (!mark(kFc2)) return MOE_ERR_CUDA;
+    if (launch_chain(p->chain, false, l) != cudaSuccess) return MOE_ERR_CUDA;
+    if (!mark(kFinalize) || !mark(kNumStages)) return MOE_ERR_CUDA;
+    if (ev) ++p->n_recorded;
+    return MOE_OK;
   }
   if (!mark(kSort)) return MOE_ERR_CUDA;
   if (launch_sort(p->ids, p->R, d.E, d.local_offset, d.num_local, p->m_indptr, p->p2e, p->e2p,
@@ -503,6 +546,7 @@ int moe_plan_stage_times(moe_plan *p, float *ms, int max_stages, int *n_launches
 
 int moe_plan_kernels_per_launch(const moe_plan *p) {
   if (!p || p->d.T == 0) return 0;
+  if (p->use_chain) return (p->logits_mode ? 1 : 0) + 2;
   int n = p->logits_mode ? 1 : 0;                       // route
   n += p->R <= kSortSingleMax ? 1 : 3;                  // sort
   n += (p->fused_gather ? 0 : 1) + 1 + 1 + 1;           // gather, fc1, fc2, finalize

@@ -1,0 +1,576 @@
+// S7 for few tokens as a two-kernel chain: FC1 and FC2 of the decode regime
+// with the sort, the gather and the finalize folded in.
+//
+// For T*top_k <= kMaxRoutes routes each CTA sorts the routes itself in shared
+// memory (the same stable counting sort as sort.cu: ascending expanded index
+// inside each local expert), so no sort kernel runs and no CTA waits for
+// another.  Both kernels are swap-AB weight-streaming GEMMs (decode.cu):
+// 128 weight rows on the MMA's M side, the expert's tokens on N.
+//
+//   FC1  the producer warp gathers the expert's token rows straight from x
+//        (four rows per TMA row-gather), the epilogue writes
+//        h[p] = bf16(silu(g) * u); its first CTA also clears the status word,
+//        publishes the sort (m_indptr, perm_to_exp, exp_to_perm) and zeroes
+//        the combine counters.
+//   FC2  streams W2 (the first ring of weight boxes before it waits for FC1),
+//        writes the unscaled fp32 rows y, and combines: every (token, 128-col
+//        block) has a counter; the tile that brings it to the token's number
+//        of local routes sums the token's rows in ascending slot order,
+//        out = bf16(sum_j w_j * y_j), exactly the finalize kernel's
+//        arithmetic, so the result does not depend on which tile is last.
+//
+// Programmatic dependent launch: each kernel reads only the layer's inputs
+// (and, in logits mode, the routing kernel's output, waited for) before its
+// griddepcontrol.wait; it writes nothing before it.
+#include <cuda_bf16.h>
+
+#include "launch.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BK = 64;
+constexpr int kThreads = 192;
+constexpr int kEpiThreads = 128;
+
+struct ChainArgs {
+  CUtensorMap map_w;  // FC1: W1 [L*2I, H] box {64, 64};  FC2: W2 [L*H, I] box {64, 128}
+  CUtensorMap map_x;  // FC1: x [T, H] box {64, 1} (row gathers);  FC2: h [R, I] box {64, BNT}
+  const int32_t *ids;  // [T*k] global expert ids
+  const float *w;      // [T*k] routing weights
+  uint16_t *h;         // [R, I] bf16: FC1 writes, FC2 reads
+  float *y;            // [R, H] fp32: FC2
+  uint16_t *out;       // [T, H] bf16: FC2
+  int32_t *comb;       // [T * m_tiles2] combine counters
+  int32_t *m_indptr_out, *p2e_out, *e2p_out;  // published by FC1's first CTA
+  int32_t *status;
+  int T, k, E, off, L, K, n_out, w_rows, m_tiles, m_tiles2, ids_early;
+};
+
+template <int BNT>
+struct ChainCfg {
+  static constexpr int A_BYTES = 128 * BK * 2;
+  static constexpr int B_BYTES = BNT * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = BNT == 64 ? 6 : (BNT == 32 ? 7 : 8);
+  static constexpr int NBARS = 2 * STAGES + 5;
+  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+  static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;         // tmem base, abort, bad flag
+  static constexpr int SG_OFF = (MISC_OFF + 16 + 15) & ~15;    // [BNT][64] fp32 (FC1) / flags (FC2)
+  static constexpr int TAB_OFF = SG_OFF + BNT * 64 * 4;
+  static constexpr uint32_t TMEM_COLS = 2 * BNT < 32 ? 32 : 2 * BNT;
+  static constexpr uint32_t IDESC = idesc_bf16_f32(128, BNT);
+  // tables: m_indptr [L+1], next [L+1], tile_start [L+1], p2e [R], e2p [R], tok_n [T]
+  static size_t smem_bytes(int L, int R, int T) {
+    return 1024 + TAB_OFF + (size_t)(3 * (L + 1) + 2 * R + T + 8) * 4;
+  }
+};
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ bool epi_bar_any(bool flag) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, 1, 128, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)flag)
+      : "memory");
+  return r != 0;
+}
+
+// Stable counting sort of the R routes by local expert, in shared memory; all
+// threads of the CTA call it.  m_indptr[L+1], p2e[R] (first M valid),
+// e2p[R] (-1 for a route that is not local or has a bad id).
+__device__ void cta_sort(const int32_t *ids, int R, int E, int off, int L, int *m_indptr, int *next,
+                         int *p2e, int *e2p, volatile int *bad) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int x = tid; x < L; x += kThreads) m_indptr[x] = 0;
+  if (tid == 0) *bad = 0;
+  __syncthreads();
+  for (int r = tid; r < R; r += kThreads) {
+    const int g = ids[r];
+    if (g < 0 || g >= E) *bad = 1;
+    else if (g >= off && g < off + L) atomicAdd(&m_indptr[g - off], 1);
+  }
+  __syncthreads();
+  if (warp == 0) {  // exclusive scan of the counts; m_indptr[L] = M
+    int carry = 0;
+    for (int base = 0; base < L; base += 32) {
+      const int x = base + lane;
+      const int v = x < L ? m_indptr[x] : 0;
+      int inc = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+      }
+      if (x < L) {
+        m_indptr[x] = carry + inc - v;
+        next[x] = carry + inc - v;
+      }
+      carry += __shfl_sync(0xffffffffu, inc, 31);
+    }
+    if (lane == 0) m_indptr[L] = carry;
+    __syncwarp();
+    // placement, 32 routes at a time in ascending r
+    for (int base = 0; base < R; base += 32) {
+      const int r = base + lane;
+      int e = -1;
+      if (r < R) {
+        const int g = ids[r];
+        if (g >= off && g < off + L && g < E) e = g - off;
+      }
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      if (e >= 0) {
+        const int p = next[e] + rank;
+        p2e[p] = r;
+        e2p[r] = p;
+      } else if (r < R) {
+        e2p[r] = -1;
+      }
+      __syncwarp();
+      if (e >= 0 && rank == 0) next[e] += __popc(peers);
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+}
+
+struct Tile {
+  int g, m, n;
+};
+
+__device__ __forceinline__ Tile decode_tile(int t, const int *tile_start, int L, int m_tiles) {
+  int lo = 0, hi = L;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (tile_start[mid] <= t) lo = mid;
+    else hi = mid;
+  }
+  Tile c;
+  c.g = lo;
+  const int local = t - tile_start[lo];
+  const int nt = (tile_start[lo + 1] - tile_start[lo]) / m_tiles;
+  c.m = local / nt;
+  c.n = local - c.m * nt;
+  return c;
+}
+
+template <int BNT, bool FC1>
+__global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constant__ ChainArgs a) {
+  using C = ChainCfg<BNT>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char *smem = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t smem_base = smem_u32(smem);
+  const uint32_t bar_base = smem_base + C::BAR_OFF;
+  auto full_bar = [&](int s) { return bar_base + 8u * s; };
+  auto empty_bar = [&](int s) { return bar_base + 8u * (C::STAGES + s); };
+  auto tfull_bar = [&](int x) { return bar_base + 8u * (2 * C::STAGES + x); };
+  auto tempty_bar = [&](int x) { return bar_base + 8u * (2 * C::STAGES + 2 + x); };
+  const uint32_t drain_bar = bar_base + 8u * (2 * C::STAGES + 4);
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
+  volatile int *bad = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 8);
+  float *sg = reinterpret_cast<float *>(smem + C::SG_OFF);
+  int *sflag = reinterpret_cast<int *>(smem + C::SG_OFF);  // FC2: last-arriver tokens [BNT]
+  const int L = a.L, T = a.T, R = a.T * a.k;
+  int *m_indptr = reinterpret_cast<int *>(smem + C::TAB_OFF);
+  int *next = m_indptr + (L + 1);
+  int *tile_start = next + (L + 1);
+  int *p2e = tile_start + (L + 1);
+  int *e2p = p2e + R;
+  int *tok_n = e2p + R;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(tfull_bar(x), 1);
+      mbar_init(tempty_bar(x), kEpiThreads);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&a.map_w);
+    tma_prefetch_desc(&a.map_x);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (!a.ids_early) pdl_wait();  // the routing kernel wrote ids and weights
+
+  cta_sort(a.ids, R, a.E, a.off, L, m_indptr, next, p2e, e2p, bad);
+  if (!FC1) {
+    for (int t = threadIdx.x; t < T; t += kThreads) {
+      int n = 0;
+      for (int j = 0; j < a.k; ++j) n += e2p[t * a.k + j] >= 0;
+      tok_n[t] = n;
+    }
+  }
+  if (warp == 0) {  // tiles: per non-empty expert, m_tiles x ceil(cnt / BNT)
+    int carry = 0;
+    if (lane == 0) tile_start[0] = 0;
+    for (int base = 0; base < L; base += 32) {
+      const int g = base + lane;
+      int nt = 0;
+      if (g < L) {
+        const int cnt = m_indptr[g + 1] - m_indptr[g];
+        nt = cnt > 0 ? ((cnt + BNT - 1) / BNT) * a.m_tiles : 0;
+      }
+      int inc = nt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+      }
+      if (g < L) tile_start[g + 1] = carry + inc;
+      carry += __shfl_sync(0xffffffffu, inc, 31);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  pdl_launch_dependents();
+
+  const uint32_t tmem_base = *tmem_holder;
+  const int total = tile_start[L];
+  const int num_kb = a.K / BK;
+  const int rows_per_box = FC1 ? 64 : 128;
+  const int M = m_indptr[L];
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer --
+    const uint64_t pol_w = policy_evict_first();  // each weight byte is read once
+    const uint64_t pol_x = policy_evict_last();
+    int it = 0;
+    bool ok = true;
+    int pending = 0;          // FC2: first-ring stages waiting for their h box
+    bool waited = FC1;        // FC1 reads only inputs: it never waits here
+    int first_xrow = 0;
+    auto finish_wait = [&]() {  // FC2: FC1 has finished; load the pending h boxes
+      pdl_wait();
+      waited = true;
+      if (lane == 0)
+        for (int j = 0; j < pending; ++j)
+          tma_load_2d(smem_base + j * C::STAGE_BYTES + C::A_BYTES, &a.map_x, full_bar(j), j * BK,
+                      first_xrow, pol_x);
+      pending = 0;
+    };
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      if (!waited && t != (int)blockIdx.x) finish_wait();
+      const Tile c = decode_tile(t, tile_start, L, a.m_tiles);
+      const int wrow = c.g * a.w_rows + c.m * rows_per_box;
+      const int xrow = m_indptr[c.g] + c.n * BNT;
+      if (t == (int)blockIdx.x) first_xrow = xrow;
+      int tr0 = 0, tr1 = 0, tr2 = 0, tr3 = 0;  // FC1: this lane's four token rows of x
+      const bool tok_lane = FC1 && lane < BNT / 4;
+      if (tok_lane) {
+        int tr[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int p = xrow + 4 * lane + i;
+          tr[i] = p < M ? p2e[p] / a.k : 0;
+        }
+        tr0 = tr[0];
+        tr1 = tr[1];
+        tr2 = tr[2];
+        tr3 = tr[3];
+      }
+      for (int kb = 0; kb < num_kb; ++kb, ++it) {
+        const int s = it % C::STAGES;
+        const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
+        if (!waited && it >= C::STAGES) finish_wait();
+        int w_ok = 1;
+        if (lane == 0) w_ok = mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, a.status) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
+          ok = false;
+          break;
+        }
+        const uint32_t a_dst = smem_base + s * C::STAGE_BYTES;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(full_bar(s), C::STAGE_BYTES);
+          if (FC1) {
+            tma_load_2d(a_dst, &a.map_w, full_bar(s), kb * BK, wrow, pol_w);
+            tma_load_2d(a_dst + 64 * 128, &a.map_w, full_bar(s), kb * BK, wrow + a.w_rows / 2, pol_w);
+          } else {
+            tma_load_2d(a_dst, &a.map_w, full_bar(s), kb * BK, wrow, pol_w);
+          }
+        }
+        __syncwarp();
+        if (FC1) {
+          if (tok_lane)
+            tma_gather4(a_dst + C::A_BYTES + lane * 512, &a.map_x, full_bar(s), kb * BK, tr0, tr1, tr2,
+                        tr3, pol_x);
+        } else if (waited) {
+          if (lane == 0) tma_load_2d(a_dst + C::A_BYTES, &a.map_x, full_bar(s), kb * BK, xrow, pol_x);
+        } else {
+          ++pending;
+        }
+      }
+    }
+    if (!waited) finish_wait();
+    if (lane == 0)
+      for (int j = it > C::STAGES ? it - C::STAGES : 0; j < it; ++j)
+        mbar_wait(full_bar(j % C::STAGES), (uint32_t)(j / C::STAGES) & 1u, nullptr, a.status);
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // -------------------------------------------------------------- MMA issuer --
+      int it = 0, tc = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tc) {
+        const int acc = tc & 1;
+        const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
+        if (!mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag, a.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BNT);
+        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+          const int s = it % C::STAGES;
+          const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
+          if (!mbar_wait(full_bar(s), ph, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_base + s * C::STAGE_BYTES;
+          const uint64_t a_desc = smem_desc_k_sw128(a_addr);
+          const uint64_t b_desc = smem_desc_k_sw128(a_addr + C::A_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            umma_bf16(d_tmem, a_desc + 2u * kk, b_desc + 2u * kk, C::IDESC, (kb | kk) != 0);
+          umma_commit(empty_bar(s));
+        }
+        if (ok) umma_commit(tfull_bar(acc));
+      }
+      umma_commit(drain_bar);
+      mbar_wait(drain_bar, 0, nullptr, a.status);
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue --
+    pdl_wait();  // the previous kernel may still read what this one writes
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // weight row inside the tile (TMEM lane)
+    const int etid = threadIdx.x - 64;  // 0..127
+    if (blockIdx.x == 0) {
+      if (FC1) {
+        if (etid == 0 && a.status) {
+          *reinterpret_cast<volatile int32_t *>(a.status) = 0;
+          if (*bad) atomicOr(reinterpret_cast<unsigned int *>(a.status), MOE_DEV_BAD_EXPERT);
+        }
+        for (int x = etid; x <= L; x += kEpiThreads) a.m_indptr_out[x] = m_indptr[x];
+        for (int x = etid; x < R; x += kEpiThreads) {
+          a.e2p_out[x] = e2p[x];
+          if (x < M) a.p2e_out[x] = p2e[x];
+        }
+        for (int x = etid; x < T * a.m_tiles2; x += kEpiThreads) a.comb[x] = 0;
+      } else {  // tokens with no local route: their output row is zero
+        for (int t = 0; t < T; ++t)
+          if (tok_n[t] == 0)
+            for (int x = etid; x < a.n_out; x += kEpiThreads) a.out[(long)t * a.n_out + x] = 0;
+      }
+    }
+    int tc = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++tc) {
+      const Tile c = decode_tile(t, tile_start, L, a.m_tiles);
+      const int xrow = m_indptr[c.g] + c.n * BNT;
+      const int valid = m_indptr[c.g + 1] - xrow;  // tokens of this tile (> 0)
+      const int acc = tc & 1;
+      const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
+      const bool got = mbar_wait(tfull_bar(acc), aph, abort_flag, a.status);
+      if (epi_bar_any(!got)) break;
+      float v[BNT];
+      tc_fence_after();
+#pragma unroll
+      for (int c0 = 0; c0 < BNT; c0 += 16) {
+        uint32_t q[16];
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+            "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+            : "=r"(q[0]), "=r"(q[1]), "=r"(q[2]), "=r"(q[3]), "=r"(q[4]), "=r"(q[5]), "=r"(q[6]),
+              "=r"(q[7]), "=r"(q[8]), "=r"(q[9]), "=r"(q[10]), "=r"(q[11]), "=r"(q[12]),
+              "=r"(q[13]), "=r"(q[14]), "=r"(q[15])
+            : "r"(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BNT + c0)));
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[c0 + i] = __uint_as_float(q[i]);
+      }
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(tempty_bar(acc));
+      if (FC1) {
+        if (r >= 64) {
+#pragma unroll
+          for (int j = 0; j < BNT; ++j) sg[j * 64 + (r - 64)] = v[j];
+        }
+        epi_bar();
+        if (r < 64) {
+          __nv_bfloat16 *h = reinterpret_cast<__nv_bfloat16 *>(a.h);
+          const long col = (long)c.m * 64 + r;
+#pragma unroll
+          for (int j = 0; j < BNT; ++j)
+            if (j < valid)
+              h[(long)(xrow + j) * a.n_out + col] = __float2bfloat16_rn(silu_f32(sg[j * 64 + r]) * v[j]);
+        }
+        epi_bar();
+      } else {
+        const int col = c.m * 128 + r;
+        if (col < a.n_out) {
+#pragma unroll
+          for (int j = 0; j < BNT; ++j)
+            if (j < valid) a.y[(long)(xrow + j) * a.n_out + col] = v[j];
+        }
+        __threadfence();
+        epi_bar();
+        // one counter per (token, column block): the tile that completes it combines
+        if (etid < BNT) {
+          int last = -1;
+          if (etid < valid) {
+            const int tkn = p2e[xrow + etid] / a.k;
+            const int old = atomicAdd(&a.comb[tkn * a.m_tiles2 + c.m], 1);
+            if (old == tok_n[tkn] - 1) last = tkn;
+          }
+          sflag[etid] = last;
+        }
+        epi_bar();
+        __threadfence();
+#pragma unroll 1
+        for (int j = 0; j < BNT && j < valid; ++j) {
+          const int tkn = sflag[j];
+          if (tkn < 0 || col >= a.n_out) continue;
+          float sum = 0.f;
+          for (int s = 0; s < a.k; ++s) {
+            const int pp = e2p[tkn * a.k + s];
+            if (pp < 0) continue;
+            sum = __fadd_rn(sum, __fmul_rn(a.w[tkn * a.k + s], __ldcg(a.y + (long)pp * a.n_out + col)));
+          }
+          reinterpret_cast<__nv_bfloat16 *>(a.out)[(long)tkn * a.n_out + col] = __float2bfloat16_rn(sum);
+        }
+        epi_bar();
+      }
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+int encode(CUtensorMap *map, const void *ptr, long rows, int K, int box_rows) {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return MOE_ERR_DEVICE;
+    fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)(rows > 0 ? rows : 1)};
+  cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_TENSOR_MAP;
+}
+
+template <int BNT, bool FC1>
+cudaError_t configure(size_t smem) {
+  return cudaFuncSetAttribute(chain_kernel<BNT, FC1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)smem);
+}
+
+template <int BNT, bool FC1>
+cudaError_t launch_inst(const ChainPlan &p, const Launch &l) {
+  ChainArgs a;
+  a.map_w = FC1 ? p.map_w1 : p.map_w2;
+  a.map_x = FC1 ? p.map_x : p.map_h;
+  a.ids = p.ids;
+  a.w = p.w;
+  a.h = p.h;
+  a.y = p.y;
+  a.out = p.out;
+  a.comb = p.comb;
+  a.m_indptr_out = p.m_indptr;
+  a.p2e_out = p.p2e;
+  a.e2p_out = p.e2p;
+  a.status = p.status;
+  a.T = p.T;
+  a.k = p.k;
+  a.E = p.E;
+  a.off = p.off;
+  a.L = p.L;
+  a.K = FC1 ? p.H : p.I;
+  a.n_out = FC1 ? p.I : p.H;
+  a.w_rows = FC1 ? 2 * p.I : p.H;
+  a.m_tiles = FC1 ? p.I / 64 : (p.H + 127) / 128;
+  a.m_tiles2 = (p.H + 127) / 128;
+  a.ids_early = p.ids_early && l.pdl ? 1 : 0;
+  return launch_kernel(chain_kernel<BNT, FC1>, dim3(FC1 ? p.grid1 : p.grid2), dim3(kThreads),
+                       p.smem, l, a);
+}
+
+}  // namespace
+
+size_t chain_comb_ints(int T, int H) { return (size_t)T * ((H + 127) / 128); }
+
+int chain_prepare(ChainPlan &p) {
+  if ((long)p.T * p.k > kChainMaxRoutes || p.I % 64 || p.H % 64) return MOE_ERR_SHAPE;
+  p.bnt = p.T <= 16 ? 16 : (p.T <= 32 ? 32 : 64);
+  int rc = encode(&p.map_w1, p.w1, (long)p.L * 2 * p.I, p.H, 64);
+  if (rc == MOE_OK) rc = encode(&p.map_x, p.x, p.T, p.H, 1);
+  if (rc == MOE_OK) rc = encode(&p.map_w2, p.w2, (long)p.L * p.H, p.I, 128);
+  if (rc == MOE_OK) rc = encode(&p.map_h, p.h, (long)p.T * p.k, p.I, p.bnt);
+  if (rc != MOE_OK) return rc;
+  const long R = (long)p.T * p.k;
+  p.smem = p.bnt == 16 ? ChainCfg<16>::smem_bytes(p.L, (int)R, p.T)
+                       : (p.bnt == 32 ? ChainCfg<32>::smem_bytes(p.L, (int)R, p.T)
+                                      : ChainCfg<64>::smem_bytes(p.L, (int)R, p.T));
+  if (p.smem > 227 * 1024) return MOE_ERR_SHAPE;
+  const long groups = p.L < R ? p.L : R;
+  const long sms = device_sm_count();
+  const long t1 = (long)(p.I / 64) * ((R + p.bnt - 1) / p.bnt + groups);
+  const long t2 = (long)((p.H + 127) / 128) * ((R + p.bnt - 1) / p.bnt + groups);
+  p.grid1 = (int)(t1 < sms ? t1 : sms);
+  p.grid2 = (int)(t2 < sms ? t2 : sms);
+  cudaError_t e;
+  if (p.bnt == 16) {
+    if ((e = configure<16, true>(p.smem)) == cudaSuccess) e = configure<16, false>(p.smem);
+  } else if (p.bnt == 32) {
+    if ((e = configure<32, true>(p.smem)) == cudaSuccess) e = configure<32, false>(p.smem);
+  } else {
+    if ((e = configure<64, true>(p.smem)) == cudaSuccess) e = configure<64, false>(p.smem);
+  }
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+cudaError_t launch_chain(const ChainPlan &p, bool fc1, const Launch &l) {
+  if (p.bnt == 16) return fc1 ? launch_inst<16, true>(p, l) : launch_inst<16, false>(p, l);
+  if (p.bnt == 32) return fc1 ? launch_inst<32, true>(p, l) : launch_inst<32, false>(p, l);
+  return fc1 ? launch_inst<64, true>(p, l) : launch_inst<64, false>(p, l);
+}
+
+}  // namespace moe

@@ -113,4 +113,23 @@ int swap_prepare(SwapPlan &p, bool swiglu, const uint16_t *W, int G, int w_rows,
                  long max_group_rows, void *out, int32_t *status, bool early);
 cudaError_t launch_swap(const SwapPlan &p, const Launch &l);
 
+// S7 as a two-kernel chain with the sort, gather and finalize folded in
+// (decode_chain.cu); for T * top_k <= kChainMaxRoutes.
+constexpr int kChainMaxRoutes = 1024;
+struct ChainPlan {
+  CUtensorMap map_w1, map_x, map_w2, map_h;
+  const uint16_t *x = nullptr, *w1 = nullptr, *w2 = nullptr;
+  const int32_t *ids = nullptr;
+  const float *w = nullptr;
+  uint16_t *h = nullptr, *out = nullptr;
+  float *y = nullptr;
+  int32_t *comb = nullptr, *m_indptr = nullptr, *p2e = nullptr, *e2p = nullptr, *status = nullptr;
+  int T = 0, k = 0, E = 0, off = 0, L = 0, H = 0, I = 0, bnt = 0, grid1 = 0, grid2 = 0;
+  bool ids_early = false;  // ids are layer inputs (pre-routed), not the routing kernel's output
+  size_t smem = 0;
+};
+size_t chain_comb_ints(int T, int H);
+int chain_prepare(ChainPlan &p);
+cudaError_t launch_chain(const ChainPlan &p, bool fc1, const Launch &l);
+
 }  // namespace moe

@@ -41,10 +41,10 @@ def _oracle_out(wl, tokens=None, w1=None, w2=None):
     return out, st
 
 
-def _forward(wl, d, path=moe.PATH_AUTO, status=None, one_cta_gemm=False):
+def _forward(wl, d, path=moe.PATH_AUTO, status=None, one_cta_gemm=False, decode_chain=False):
     plan = moe.MoEPlan(d["x"], d["w1"], d["w2"], wl.E, wl.top_k, logits=d["logits"],
                        topk_ids=d["topk_ids"], topk_w=d["topk_w"], local_offset=wl.local_offset,
-                       status=status, path=path, one_cta_gemm=one_cta_gemm)
+                       status=status, path=path, one_cta_gemm=one_cta_gemm, decode_chain=decode_chain)
     out = plan.launch()
     torch.cuda.synchronize()
     return out, plan
@@ -197,11 +197,12 @@ def test_all_tokens_on_one_expert():
 
 # ---------------------------------------------------------- workload shapes --
 
+@pytest.mark.parametrize("chain", [False, True])
 @pytest.mark.parametrize("name", ["decode_t1", "decode_t8", "decode_t64"])
 @pytest.mark.parametrize("path", PATHS)
-def test_decode_configs_full(name, path):
+def test_decode_configs_full(name, path, chain):
     wl = W.make_moe(name)
-    out, _ = _forward(wl, _dev(wl), path)
+    out, _ = _forward(wl, _dev(wl), path, decode_chain=chain)
     want, _ = _oracle_out(wl)
     check_bf16_end_to_end(W.bf16_bits(out), want, name)
 
@@ -299,3 +300,81 @@ def test_stage_chain_prefill_configs(name):
     wl = W.make_moe(name, weights_device=DEV)
     ids, _ = _oracle_route(wl)
     _stage_chain(wl, _sample_tokens(ids, wl.T, 512, 1))
+
+
+# ------------------------------------------------- decode chain (T * k <= 1024) --
+
+@pytest.mark.parametrize("name", ["decode_t1", "decode_t8", "decode_t64"])
+def test_decode_chain_replays_bitwise_and_graph(name):
+    """The two-kernel decode chain combines each (token, column block) in the
+    tile that arrives last; the sum order is fixed, so replays, in any arrival
+    order, are bitwise identical."""
+    wl = W.make_moe(name)
+    d = _dev(wl)
+    plan = moe.MoEPlan(d["x"], d["w1"], d["w2"], wl.E, wl.top_k, topk_ids=d["topk_ids"], topk_w=d["topk_w"],
+                       path=moe.PATH_DECODE, decode_chain=True)
+    assert plan.kernels_per_launch() == 2
+    ref = plan.launch().clone()
+    torch.cuda.synchronize()
+    for _ in range(5):
+        plan.out.fill_(1.0)
+        plan.launch()
+        torch.cuda.synchronize()
+        assert torch.equal(plan.out, ref)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        plan.launch()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        plan.launch()
+    for _ in range(3):
+        plan.out.fill_(2.0)
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(plan.out, ref)
+    want, _ = _oracle_out(wl)
+    check_bf16_end_to_end(W.bf16_bits(ref), want, f"{name} chain")
+    # the chain publishes its sort like the sort kernel would
+    b = plan.buffers()
+    ids = wl.topk_ids.numpy()
+    m_o, p2e_o, e2p_o, _ = oracle.sort(ids, wl.E)
+    ws = plan.workspace
+    R = wl.T * wl.top_k
+
+    def view(name, n):
+        off = b[name] - ws.data_ptr()
+        return ws[off:off + 4 * n].view(torch.int32).cpu().numpy()
+    assert np.array_equal(view("m_indptr", wl.E + 1), m_o)
+    assert np.array_equal(view("exp_to_perm", R), e2p_o)
+    assert np.array_equal(view("perm_to_exp", len(p2e_o)), p2e_o)
+
+
+def test_decode_chain_status_and_bad_ids():
+    wl = W.make_moe(T=6, H=128, I=128, E=9, top_k=3, mode="prerouted", seed=12)
+    ids = wl.topk_ids.clone()
+    ids[2, 1] = 40
+    wl.topk_ids = ids
+    status = torch.full((1,), 0x40, dtype=torch.int32, device=DEV)  # stale bits are cleared
+    out, plan = _forward(wl, _dev(wl), moe.PATH_DECODE, status=status, decode_chain=True)
+    assert plan.kernels_per_launch() == 2
+    assert int(status.item()) == moe.DEV_BAD_EXPERT
+    want, _ = _oracle_out(wl)
+    check_bf16_end_to_end(W.bf16_bits(out), want, "chain bad ids")
+    wl.topk_ids = wl.topk_ids.clamp(0, 8)
+    d = _dev(wl)
+    out2, _ = _forward(wl, d, moe.PATH_DECODE, status=status, decode_chain=True)
+    assert int(status.item()) == 0
+
+
+@pytest.mark.parametrize("off,L", [(0, 5), (5, 4), (2, 1)])
+def test_decode_chain_expert_shard(off, L):
+    full = W.make_moe(T=12, H=192, I=128, E=9, top_k=4, mode="logits", seed=21)
+    wl = W.make_moe(T=12, H=192, I=128, E=9, top_k=4, mode="logits", seed=21)
+    wl.w1, wl.w2 = full.w1[off:off + L].contiguous(), full.w2[off:off + L].contiguous()
+    wl.local_offset, wl.num_local = off, L
+    out, plan = _forward(wl, _dev(wl), moe.PATH_DECODE, decode_chain=True)
+    assert plan.kernels_per_launch() == 3  # route + the two chain kernels
+    want, _ = _oracle_out(wl)
+    check_bf16_end_to_end(W.bf16_bits(out), want, f"chain shard {off}+{L}")
