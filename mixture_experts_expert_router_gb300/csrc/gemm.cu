@@ -471,7 +471,7 @@ int gemm_prepare(GemmPlan &p, Epi epi, const uint16_t *A, long a_rows, const uin
   }
   const long sms = device_sm_count();
   if (p.pair) {
-    p.smem = pair_gemm_smem(G);
+    p.smem = pair_gemm_smem(epi, G);
     const long max_pairs = ((max_rows + 2 * BM - 1) / (2 * BM) + G) * (long)p.n_tiles;
     const long clusters = sms / 2;
     p.grid = 2 * (int)(max_pairs < clusters ? (max_pairs > 0 ? max_pairs : 1) : clusters);

@@ -46,15 +46,23 @@ constexpr int BM = 128;  // token (main) or weight (tail) rows per CTA
 constexpr int BN = 256;  // main tile MMA N (weight rows per pair; 128 staged by each CTA)
 constexpr int BK = 64;
 constexpr int kThreads = 192;
-constexpr int STAGES = 6;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = (BN / 2) * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // per CTA, the largest stage
-constexpr int NBARS = 2 * STAGES + 5;
-constexpr int BAR_OFF = STAGES * STAGE_BYTES;
-constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
-constexpr int SG_OFF = MISC_OFF + 16;           // tail gate hand-off [16][64] fp32
-constexpr int TAB_OFF = SG_OFF + 16 * 64 * 4;
+constexpr int STG_BYTES = BM * 32 * 4;          // fp32 store staging: 128 rows x 32 columns
+
+// Shared-memory layout per epilogue kind.  The fp32 form trades a ring stage
+// for two store-staging buffers.
+template <int EPI>
+struct PairLayout {
+  static constexpr int STAGES = EPI == (int)Epi::kF32 ? 5 : 6;
+  static constexpr int NBARS = 2 * STAGES + 5;
+  static constexpr int STG_OFF = STAGES * STAGE_BYTES;
+  static constexpr int BAR_OFF = STG_OFF + (EPI == (int)Epi::kF32 ? 2 * STG_BYTES : 0);
+  static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
+  static constexpr int SG_OFF = MISC_OFF + 16;  // tail gate hand-off [16][64] fp32
+  static constexpr int TAB_OFF = SG_OFF + 16 * 64 * 4;
+};
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr uint32_t IDESC_MAIN = idesc_bf16_f32(2 * BM, BN);
 constexpr int kTailMax = 128;
@@ -65,6 +73,7 @@ struct PairArgs {
   CUtensorMap map_w64;    // weights, box {64, 64} (FC1 tail tiles)
   CUtensorMap map_t[4];   // tokens, box {64, 8 / 16 / 32 / 64} (tail tiles, N = 16..128)
   CUtensorMap map_xg;     // gather mode: token rows of x [x_rows, K], box {64, 1}
+  CUtensorMap map_y;      // fp32 output [rows, n_out], box {32, 128}, 128-byte swizzle (TMA stores)
   const int32_t *p2e;     // gather mode: permuted row -> expanded index
   long x_rows;
   int gather_k;           // gather mode: top_k (token = p2e[row] / top_k); 0 = rows given directly
@@ -109,6 +118,11 @@ struct PairTile {
 // Per group: full pairs cnt / 256 plus one more tile when rows are left.
 __device__ __forceinline__ int group_pairs(int cnt) { return cnt > 0 ? (cnt + 2 * BM - 1) / (2 * BM) : 0; }
 
+// Tile order: group-major; inside a group the m-pairs or the n-blocks run
+// innermost as chosen on the host.  tile_start[g] is the prefix of the
+// groups' pair counts.  (Spreading the tiles of the groups of at most 128 rows
+// evenly among the others was measured slower: their once-read weight
+// streams then evict the large groups' reused weight blocks from L2.)
 __device__ __forceinline__ PairTile decode_pair_tile(int t, const int *tile_start, const int *gend, int G,
                                                      int n_tiles, int m_major) {
   int lo = 0, hi = G;
@@ -136,6 +150,12 @@ __device__ __forceinline__ PairTile decode_pair_tile(int t, const int *tile_star
 
 template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_constant__ PairArgs args) {
+  using Lay = PairLayout<EPI>;
+  constexpr int STAGES = Lay::STAGES;
+  constexpr int BAR_OFF = Lay::BAR_OFF;
+  constexpr int MISC_OFF = Lay::MISC_OFF;
+  constexpr int SG_OFF = Lay::SG_OFF;
+  constexpr int TAB_OFF = Lay::TAB_OFF;
   extern __shared__ unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -219,13 +239,16 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
     // -------------------------------------------------------------- producers --
     // Lane 0 waits, arms the leader's barrier and loads the weights; in
     // gather mode every lane also loads four token rows of x per k-block.
-    const uint64_t pol = policy_evict_normal();
+    const uint64_t pol_first = policy_evict_first(), pol_last = policy_evict_last();
     const bool gath = args.gather_k > 0;
     const int m_total = G > 0 ? gend[G - 1] : 0;
     int it = 0;
     bool ok = true;
     for (int t = cluster; t < total && ok; t += nclusters) {
       const PairTile c = decode_pair_tile(t, tile_start, gend, G, args.n_tiles, args.m_major);
+      // L2: a group that is only this tail reads its weights once (stream them
+      // through); everything else is read again by neighbouring tiles (keep it)
+      const uint64_t pol = (c.tail && c.mp == 0) ? pol_first : pol_last;
       // coordinates and bytes of this CTA's operand boxes
       int a_row, b_row, b_row2 = 0, tmap = 0, tok_rows;
       uint32_t bytes;
@@ -389,17 +412,49 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
             }
           }
         } else if (EPI == (int)Epi::kF32) {
-          uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<float *>(args.out) +
-                                                 orow * args.n_out + (long)c.n * BN);
+          if (valid >= BM) {
+            // full tile: 32-column chunks staged in swizzled shared memory and
+            // written by TMA stores (whole 128-byte rows), two buffers in turn
+            const int etid = threadIdx.x - 64;
 #pragma unroll 1
-          for (int col = 0; col < BN; col += 32) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(taddr + col, r);
-            tmem_ld_wait();
-            if (row_ok) {
+            for (int col = 0; col < BN; col += 32) {
+              const int buf = (col >> 5) & 1;
+              if (col >= 64) {  // the store that used this buffer two chunks ago has read it
+                if (etid == 0) bulk_wait_read<1>();
+                epi_bar();
+              }
+              uint32_t r[32];
+              tmem_ld_32x32b_x32(taddr + col, r);
+              tmem_ld_wait();
+              const uint32_t row_addr = smem_base + Lay::STG_OFF + buf * STG_BYTES + r_in_tile * 128;
 #pragma unroll
               for (int v = 0; v < 8; ++v)
-                dst[col / 4 + v] = make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                 row_addr + (uint32_t)((v ^ (r_in_tile & 7)) * 16)),
+                             "r"(r[4 * v]), "r"(r[4 * v + 1]), "r"(r[4 * v + 2]), "r"(r[4 * v + 3])
+                             : "memory");
+              fence_proxy_async_smem();
+              epi_bar();
+              if (etid == 0) {
+                tma_store_2d(&args.map_y, smem_base + Lay::STG_OFF + buf * STG_BYTES, c.n * BN + col, row0);
+                bulk_commit();
+              }
+            }
+            if (etid == 0) bulk_wait_read<0>();
+            epi_bar();
+          } else {
+            uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<float *>(args.out) +
+                                                   orow * args.n_out + (long)c.n * BN);
+#pragma unroll 1
+            for (int col = 0; col < BN; col += 32) {
+              uint32_t r[32];
+              tmem_ld_32x32b_x32(taddr + col, r);
+              tmem_ld_wait();
+              if (row_ok) {
+#pragma unroll
+                for (int v = 0; v < 8; ++v)
+                  dst[col / 4 + v] = make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+              }
             }
           }
         } else {
@@ -477,6 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
     }
   }
 
+  if (EPI == (int)Epi::kF32 && threadIdx.x == 64) bulk_wait_all();  // TMA stores complete
   __syncthreads();
   cluster_sync();  // the peer no longer reads this CTA's shared memory or TMEM
   if (warp == 1) {
@@ -513,9 +569,34 @@ int encode(CUtensorMap *map, const void *ptr, long rows, int K, int box_rows) {
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_TENSOR_MAP;
 }
 
+// fp32 [rows, cols] row-major for TMA stores: box {32, 128}, 128-byte swizzle.
+int encode_f32_store(CUtensorMap *map, void *ptr, long rows, int cols) {
+  EncodeTiledFn fn = nullptr;
+  {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return MOE_ERR_DEVICE;
+    fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)(rows > 0 ? rows : 1)};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
+  cuuint32_t box[2] = {32, (cuuint32_t)BM};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_TENSOR_MAP;
+}
+
 }  // namespace
 
-size_t pair_gemm_smem(int G) { return 1024 + TAB_OFF + (size_t)(2 * G + 2) * 4; }
+size_t pair_gemm_smem(Epi epi, int G) {
+  const int tab = epi == Epi::kF32 ? PairLayout<(int)Epi::kF32>::TAB_OFF : PairLayout<(int)Epi::kBf16>::TAB_OFF;
+  return 1024 + tab + (size_t)(2 * G + 2) * 4;
+}
 
 bool pair_gemm_supported(Epi epi, int n_out) {
   return epi == Epi::kSwiGLU ? (n_out % (BN / 2) == 0) : (n_out % BN == 0);
@@ -526,6 +607,7 @@ int pair_gemm_encode_extra(GemmPlan &p, const uint16_t *A, long a_rows, const ui
   int rc = encode(&p.map_w64, B, b_rows_total, K, 64);
   for (int i = 0; i < 4 && rc == MOE_OK; ++i) rc = encode(&p.map_t[i], A, a_rows, K, 8 << i);
   if (rc == MOE_OK && p.gather_k > 0) rc = encode(&p.map_xg, p.gather_x, p.gather_rows, K, 1);
+  if (rc == MOE_OK && p.epi == Epi::kF32) rc = encode_f32_store(&p.map_y, p.out, p.max_rows, p.n_out);
   return rc;
 }
 
@@ -547,6 +629,7 @@ cudaError_t launch_pair_gemm(const GemmPlan &p, const Launch &l) {
   a.map_w64 = p.map_w64;
   for (int i = 0; i < 4; ++i) a.map_t[i] = p.map_t[i];
   a.map_xg = p.map_xg;
+  a.map_y = p.map_y;
   a.p2e = p.gather_p2e;
   a.x_rows = p.gather_rows;
   a.gather_k = p.gather_k;

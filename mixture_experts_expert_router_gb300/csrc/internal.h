@@ -53,6 +53,7 @@ struct GemmPlan {
   CUtensorMap map_w64;          // pair kernel: B with box {64, 64} (FC1 tail tiles)
   CUtensorMap map_t[4];         // pair kernel: A with box {64, 8/16/32/64} (tail tiles)
   CUtensorMap map_xg;           // pair kernel, gather mode: x with box {64, 1}
+  CUtensorMap map_y;            // pair kernel, fp32 output: TMA-store map
   const uint16_t *gather_x = nullptr;   // gather mode: rows of A are x[p2e[p] / k]
   const int32_t *gather_p2e = nullptr;
   long gather_rows = 0;
@@ -87,7 +88,7 @@ int gemm_prepare_gather(GemmPlan &p, const uint16_t *x, long x_rows, const int32
 cudaError_t launch_gemm(const GemmPlan &p, const Launch &l);
 
 // CTA-pair form (gemm2sm.cu)
-size_t pair_gemm_smem(int G);
+size_t pair_gemm_smem(Epi epi, int G);
 int pair_gemm_encode_extra(GemmPlan &p, const uint16_t *A, long a_rows, const uint16_t *B,
                            long b_rows_total, int K);
 bool pair_gemm_supported(Epi epi, int n_out);
