@@ -65,6 +65,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Wait until the phase with the given parity of barrier `bar` has completed.
 // Gives up (returns false) when *abort becomes non-zero or after
 // kWaitLimitNs; on a timeout it raises MOE_DEV_TIMEOUT and sets *abort.
+// `abort` may be null (the final drains, which must run to the end or the
+// time limit whatever the other roles did).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
                                           int32_t *status) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -72,9 +74,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0u) {
-      if (*abort) return false;
+      if (abort != nullptr && *abort) return false;
       if (global_timer_ns() - t0 > kWaitLimitNs) {
-        *abort = 1;
+        if (abort != nullptr) *abort = 1;
         if (status) atomicOr(reinterpret_cast<unsigned int *>(status), MOE_DEV_TIMEOUT);
         return false;
       }

@@ -29,15 +29,16 @@ __global__ void __launch_bounds__(256)
     const uint4 *src = x + t * vec;
     uint4 *dst = xp + p * vec;
     int i = lane;
-    for (; i + 96 < vec; i += 128) {
-      const uint4 a = __ldg(src + i), b = __ldg(src + i + 32), c = __ldg(src + i + 64),
-                  d = __ldg(src + i + 96);
-      dst[i] = a;
-      dst[i + 32] = b;
-      dst[i + 64] = c;
-      dst[i + 96] = d;
+    // eight 16-byte loads in flight per lane; xp is written once and read by
+    // the next kernel, so the stores stream past L1
+    for (; i + 224 < vec; i += 256) {
+      uint4 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = __ldg(src + i + 32 * j);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) __stcs(dst + i + 32 * j, v[j]);
     }
-    for (; i < vec; i += 32) dst[i] = __ldg(src + i);
+    for (; i < vec; i += 32) __stcs(dst + i, __ldg(src + i));
   }
 }
 
