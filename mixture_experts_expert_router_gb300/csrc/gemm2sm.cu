@@ -45,7 +45,10 @@ namespace {
 constexpr int BM = 128;  // token (main) or weight (tail) rows per CTA
 constexpr int BN = 256;  // main tile MMA N (weight rows per pair; 128 staged by each CTA)
 constexpr int BK = 64;
-constexpr int kThreads = 192;
+// warps: 0 token producer, 1 TMEM owner + MMA issuer, 2..5 epilogue (TMEM
+// lane quarters warp % 4), 6 weight producer
+constexpr int kThreads = 224;
+constexpr int kWeightWarp = 6;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = (BN / 2) * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // per CTA, the largest stage
@@ -148,6 +151,43 @@ __device__ __forceinline__ PairTile decode_pair_tile(int t, const int *tile_star
   return c;
 }
 
+// This CTA's operand boxes for a tile: the token box (rows tok_row ..
+// tok_row + tok_rows) and the weight box(es), and the bytes both bring per
+// k-block.
+struct PairOperands {
+  int tok_row, tok_rows, tmap, w_row, w_row2;
+  uint32_t bytes;
+};
+
+template <bool SWIGLU>
+__device__ __forceinline__ PairOperands pair_operands(const PairTile &c, uint32_t rank, int b_rows) {
+  PairOperands o;
+  o.w_row2 = 0;
+  o.tmap = 0;
+  if (!c.tail) {
+    o.tok_row = c.gstart + (2 * c.mp + (int)rank) * BM;
+    if (SWIGLU)  // leader stages the up rows, the peer the gate rows
+      o.w_row = c.g * b_rows + c.n * (BN / 2) + (int)rank * (b_rows / 2);
+    else
+      o.w_row = c.g * b_rows + c.n * BN + (int)rank * (BN / 2);
+    o.bytes = STAGE_BYTES;
+    o.tok_rows = BM;
+  } else {
+    const int n = tail_n(c.tail);
+    o.tmap = tail_map(n);
+    if (SWIGLU) {  // 64 up rows then the matching 64 gate rows
+      o.w_row = c.g * b_rows + c.n * (BN / 2) + (int)rank * 64;
+      o.w_row2 = o.w_row + b_rows / 2;
+    } else {
+      o.w_row = c.g * b_rows + c.n * BN + (int)rank * BM;
+    }
+    o.tok_row = c.gstart + c.mp * 2 * BM + (int)rank * (n / 2);
+    o.bytes = A_BYTES + (uint32_t)(n / 2) * BK * 2;
+    o.tok_rows = n / 2;
+  }
+  return o;
+}
+
 template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_constant__ PairArgs args) {
   using Lay = PairLayout<EPI>;
@@ -236,9 +276,9 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
   const int nclusters = gridDim.x >> 1;
 
   if (warp == 0) {
-    // -------------------------------------------------------------- producers --
-    // Lane 0 waits, arms the leader's barrier and loads the weights; in
-    // gather mode every lane also loads four token rows of x per k-block.
+    // --------------------------------------------------------- token producer --
+    // Lane 0 waits, arms the leader's barrier and loads the token box; in
+    // gather mode every lane loads four token rows of x per k-block instead.
     const uint64_t pol_first = policy_evict_first(), pol_last = policy_evict_last();
     const bool gath = args.gather_k > 0;
     const int m_total = G > 0 ? gend[G - 1] : 0;
@@ -246,38 +286,13 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
     bool ok = true;
     for (int t = cluster; t < total && ok; t += nclusters) {
       const PairTile c = decode_pair_tile(t, tile_start, gend, G, args.n_tiles, args.m_major);
-      // L2: a group that is only this tail reads its weights once (stream them
-      // through); everything else is read again by neighbouring tiles (keep it)
       const uint64_t pol = (c.tail && c.mp == 0) ? pol_first : pol_last;
-      // coordinates and bytes of this CTA's operand boxes
-      int a_row, b_row, b_row2 = 0, tmap = 0, tok_rows;
-      uint32_t bytes;
-      if (!c.tail) {
-        a_row = c.gstart + (2 * c.mp + (int)rank) * BM;  // tokens
-        if (kSwiGLU)  // leader stages the up rows, the peer the gate rows
-          b_row = c.g * args.b_rows + c.n * (BN / 2) + (int)rank * (args.b_rows / 2);
-        else
-          b_row = c.g * args.b_rows + c.n * BN + (int)rank * (BN / 2);
-        bytes = STAGE_BYTES;
-        tok_rows = BM;
-      } else {
-        const int n = tail_n(c.tail);
-        tmap = tail_map(n);
-        if (kSwiGLU) {  // 64 up rows then the matching 64 gate rows
-          a_row = c.g * args.b_rows + c.n * (BN / 2) + (int)rank * 64;
-          b_row2 = a_row + args.b_rows / 2;
-        } else {
-          a_row = c.g * args.b_rows + c.n * BN + (int)rank * BM;
-        }
-        b_row = c.gstart + c.mp * 2 * BM + (int)rank * (n / 2);  // tail tokens
-        bytes = A_BYTES + (uint32_t)(n / 2) * BK * 2;
-        tok_rows = n / 2;
-      }
+      const PairOperands o = pair_operands<kSwiGLU>(c, rank, args.b_rows);
       // gather mode: this lane's four token rows (rows past the routed ones read row 0)
       int tr0 = 0, tr1 = 0, tr2 = 0, tr3 = 0;
-      const bool tok_lane = gath && lane < tok_rows / 4;
+      const bool tok_lane = gath && lane < o.tok_rows / 4;
       if (tok_lane) {
-        const int p0 = (c.tail ? b_row : a_row) + 4 * lane;
+        const int p0 = o.tok_row + 4 * lane;
         int tr[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -290,6 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
         tr2 = tr[2];
         tr3 = tr[3];
       }
+      const CUtensorMap *tok_map = c.tail ? &args.map_t[o.tmap] : &args.map_a;
       for (int kb = 0; kb < num_kb; ++kb, ++it) {
         const int s = it % STAGES;
         const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
@@ -300,41 +316,52 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
           break;
         }
         const uint32_t leader_full = mapa_shared(full_bar(s), 0);
-        if (lane == 0 && rank == 0) mbar_arrive_expect_tx(full_bar(s), 2 * bytes);
+        if (lane == 0 && rank == 0) mbar_arrive_expect_tx(full_bar(s), 2 * o.bytes);
         __syncwarp();
-        const uint32_t a_dst = smem_base + s * STAGE_BYTES;
-        if (!c.tail) {
-          if (gath) {
-            if (tok_lane)
-              tma_gather4_pair(a_dst + lane * 512, &args.map_xg, leader_full, kb * BK, tr0, tr1, tr2,
-                               tr3, pol);
-          } else if (lane == 0) {
-            tma_load_2d_pair(a_dst, &args.map_a, leader_full, kb * BK, a_row, pol);
-          }
-          if (lane == 0)
-            tma_load_2d_pair(a_dst + A_BYTES, &args.map_b, leader_full, kb * BK, b_row, pol);
-        } else {
-          if (lane == 0) {
-            if (kSwiGLU) {
-              tma_load_2d_pair(a_dst, &args.map_w64, leader_full, kb * BK, a_row, pol);
-              tma_load_2d_pair(a_dst + 64 * 128, &args.map_w64, leader_full, kb * BK, b_row2, pol);
-            } else {
-              tma_load_2d_pair(a_dst, &args.map_b, leader_full, kb * BK, a_row, pol);
-            }
-          }
-          if (gath) {
-            if (tok_lane)
-              tma_gather4_pair(a_dst + A_BYTES + lane * 512, &args.map_xg, leader_full, kb * BK, tr0,
-                               tr1, tr2, tr3, pol);
-          } else if (lane == 0) {
-            tma_load_2d_pair(a_dst + A_BYTES, &args.map_t[tmap], leader_full, kb * BK, b_row, pol);
-          }
+        const uint32_t t_dst = smem_base + s * STAGE_BYTES + (c.tail ? A_BYTES : 0);
+        if (gath) {
+          if (tok_lane)
+            tma_gather4_pair(t_dst + lane * 512, &args.map_xg, leader_full, kb * BK, tr0, tr1, tr2, tr3, pol);
+        } else if (lane == 0) {
+          tma_load_2d_pair(t_dst, tok_map, leader_full, kb * BK, o.tok_row, pol);
         }
       }
     }
     if (lane == 0 && rank == 0) {  // let both CTAs' last copies land (they all signal the leader)
       for (int j = it > STAGES ? it - STAGES : 0; j < it; ++j)
         mbar_wait(full_bar(j % STAGES), (uint32_t)(j / STAGES) & 1u, nullptr, args.status);
+    }
+  } else if (warp == kWeightWarp) {
+    // -------------------------------------------------------- weight producer --
+    // A second issuing thread: one thread's TMA copies run at about half of
+    // what an SM can take in, so weights and tokens are issued separately.
+    if (lane == 0) {
+      const uint64_t pol_first = policy_evict_first(), pol_last = policy_evict_last();
+      int it = 0;
+      bool ok = true;
+      for (int t = cluster; t < total && ok; t += nclusters) {
+        const PairTile c = decode_pair_tile(t, tile_start, gend, G, args.n_tiles, args.m_major);
+        // L2: a group that is only this tail reads its weights once (stream them
+        // through); everything else is read again by neighbouring tiles (keep it)
+        const uint64_t pol = (c.tail && c.mp == 0) ? pol_first : pol_last;
+        const PairOperands o = pair_operands<kSwiGLU>(c, rank, args.b_rows);
+        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+          if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, args.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t leader_full = mapa_shared(full_bar(s), 0);
+          const uint32_t w_dst = smem_base + s * STAGE_BYTES + (c.tail ? 0 : A_BYTES);
+          if (c.tail && kSwiGLU) {  // 64 up rows then the matching 64 gate rows
+            tma_load_2d_pair(w_dst, &args.map_w64, leader_full, kb * BK, o.w_row, pol);
+            tma_load_2d_pair(w_dst + 64 * 128, &args.map_w64, leader_full, kb * BK, o.w_row2, pol);
+          } else {
+            tma_load_2d_pair(w_dst, &args.map_b, leader_full, kb * BK, o.w_row, pol);
+          }
+        }
+      }
     }
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
@@ -370,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
       umma_commit_pair(drain_bar, 0x1);
       mbar_wait(drain_bar, 0, nullptr, args.status);
     }
-  } else {
+  } else if (warp >= 2 && warp <= 5) {
     // ------------------------------------------------------------------ epilogue --
     const int quarter = warp & 3;
     const int r_in_tile = quarter * 32 + lane;  // TMEM lane: token row (main) or weight row (tail)

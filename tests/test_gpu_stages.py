@@ -166,6 +166,19 @@ def test_grouped_gemm_parity(sizes, N, K):
     assert torch.all(sentinel[d["sum_m"]:] == -7.0)  # nothing written past the last group
 
 
+def test_grouped_gemm_many_small_groups_parity():
+    """800 groups of 0..40 rows (nearly all of them tail tiles, the group
+    tables filling a large part of shared memory); K = 192 is an odd number of
+    64-wide k-blocks."""
+    sizes = np.random.default_rng(800).integers(0, 41, 800).tolist()
+    d = W.make_grouped_gemm(seed=800, sizes=sizes, N=256, K=192)
+    X, Wt, offs = d["X"].to(DEV), d["W"].to(DEV), d["offs"].to(DEV)
+    Y = moe.grouped_gemm_fwd(X, Wt, offs)
+    torch.cuda.synchronize()
+    Yo = oracle.grouped_gemm_rows(W.bf16_bits(d["X"]), W.bf16_bits(d["W"]), d["offs"].numpy())
+    check_bf16_close(W.bf16_bits(Y), Yo, "Y")
+
+
 def test_grouped_gemm_rows_beyond_offsets_untouched():
     d = W.make_grouped_gemm(seed=3, sizes=[40, 0, 90], N=128, K=128)
     X = torch.cat([d["X"], torch.ones(50, 128, dtype=torch.bfloat16)]).to(DEV)
