@@ -13,10 +13,15 @@
 //        h[p, n0 + r] = bf16(silu(D[64 + r, p]) * D[r, p])
 //   FC2: D[128 x n] = W2 rows c0..c0+127 . h^T,  y[p, c0 + r] = D[r, p] (fp32)
 //
-// Same CTA organisation as the grouped GEMM (TMA producer warp, MMA warp,
-// four epilogue warps, mbarrier ring, two TMEM accumulators).  The epilogue
-// copies its accumulator to registers and releases TMEM at once; for FC1 the
-// gate half is handed to the up half through shared memory.
+// The k-loop runs as two half-pipelines over one mbarrier ring: the even
+// k-blocks are loaded by one producer thread and multiplied by one MMA thread
+// into accumulator 0, the odd k-blocks by another pair into accumulator 1; the
+// epilogue adds the two.  (A weight-streaming MMA here has a tiny N, and one
+// issuing thread starts a new-operand tcgen05.mma only about every 80 ns, which
+// caps one thread near 50 GB/s of weights per SM; two get about twice that.)
+// Two TMEM accumulator pairs alternate between tiles.  The epilogue copies its
+// accumulators to registers and releases TMEM at once; for FC1 the gate half
+// is handed to the up half through shared memory.
 //
 // In a prepared chain (sort -> gather -> FC1 -> FC2) the group offsets were
 // written two kernels earlier, so a kernel started early by programmatic
@@ -31,7 +36,11 @@ namespace moe {
 namespace {
 
 constexpr int BK = 64;
-constexpr int kThreads = 192;
+// warps: 0 / 6 producers of the even / odd k-blocks, 1 / 7 their MMA issuers
+// (1 also owns TMEM), 2..5 epilogue
+constexpr int kThreads = 256;
+constexpr int kProd1Warp = 6;
+constexpr int kMma1Warp = 7;
 constexpr int kEpiThreads = 128;
 
 struct SwapArgs {
@@ -49,14 +58,14 @@ struct SwapCfg {
   static constexpr int A_BYTES = 128 * BK * 2;
   static constexpr int B_BYTES = BNT * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = BNT == 64 ? 7 : (BNT == 32 ? 8 : 9);
+  static constexpr int STAGES = BNT == 64 ? 8 : 10;
   static constexpr int TILE_BYTES = STAGES * STAGE_BYTES;
-  static constexpr int NBARS = 2 * STAGES + 5;
+  static constexpr int NBARS = 2 * STAGES + 6;
   static constexpr int BAR_OFF = TILE_BYTES;
   static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
   static constexpr int SG_OFF = (MISC_OFF + 16 + 15) & ~15;        // gate hand-off [BNT][64] fp32
   static constexpr int TAB_OFF = SG_OFF + BNT * 64 * 4;
-  static constexpr uint32_t TMEM_COLS = 2 * BNT < 32 ? 32 : 2 * BNT;
+  static constexpr uint32_t TMEM_COLS = 4 * BNT;  // [tile buffer][half-pipeline] accumulators
   static constexpr uint32_t IDESC = idesc_bf16_f32(128, BNT);
   static size_t smem_bytes(int G) { return 1024 + TAB_OFF + (size_t)(2 * G + 2) * 4; }
 };
@@ -129,7 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1) swapab_kernel(const __grid_consta
   auto empty_bar = [&](int s) { return bar_base + 8u * (C::STAGES + s); };
   auto tfull_bar = [&](int a) { return bar_base + 8u * (2 * C::STAGES + a); };
   auto tempty_bar = [&](int a) { return bar_base + 8u * (2 * C::STAGES + 2 + a); };
-  const uint32_t drain_bar = bar_base + 8u * (2 * C::STAGES + 4);
+  auto drain_bar = [&](int q) { return bar_base + 8u * (2 * C::STAGES + 4 + q); };
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
   float *sg = reinterpret_cast<float *>(smem + C::SG_OFF);
@@ -147,10 +156,10 @@ __global__ void __launch_bounds__(kThreads, 1) swapab_kernel(const __grid_consta
       mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
-      mbar_init(tfull_bar(a), 1);
+      mbar_init(tfull_bar(a), 2);  // both MMA issuers commit
       mbar_init(tempty_bar(a), kEpiThreads);
+      mbar_init(drain_bar(a), 1);
     }
-    mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -205,97 +214,103 @@ __global__ void __launch_bounds__(kThreads, 1) swapab_kernel(const __grid_consta
   const int total = tile_start[G];
   const int num_kb = args.K / BK;
 
-  if (warp == 0) {
-    if (lane == 0) {
-      // ------------------------------------------------------------- producer --
-      const uint64_t pol_w = policy_evict_first();  // weights are read once
-      const uint64_t pol_x = policy_evict_last();   // token rows are re-read
-      int it = 0;
-      bool ok = true;
-      // In early mode the weight boxes of the first ring's worth of k-blocks
-      // go out before the wait for the predecessor; their activation boxes
-      // follow it.
-      int pending_x = 0;
-      bool waited = !args.early;
-      // Activation boxes of the early k-blocks (all of the first tile, k-block
-      // j in ring stage j) go out once the predecessor has finished.
-      auto finish_wait = [&]() {
-        pdl_wait();
-        waited = true;
-        if (pending_x == 0) return;
-        const Tile c0 = decode_swap_tile(blockIdx.x, tile_start, gend, G, args.m_tiles);
-        const int xr0 = (c0.g == 0 ? 0 : gend[c0.g - 1]) + c0.n * BNT;
-        for (int j = 0; j < pending_x; ++j)
-          tma_load_2d(smem_base + j * C::STAGE_BYTES + C::A_BYTES, &args.map_x, full_bar(j), j * BK,
-                      xr0, pol_x);
-        pending_x = 0;
-      };
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        if (!waited && t != (int)blockIdx.x) finish_wait();
-        const Tile c = decode_swap_tile(t, tile_start, gend, G, args.m_tiles);
-        const int wrow = c.g * args.w_rows + c.m * rows_per_tile;
-        const int xrow = (c.g == 0 ? 0 : gend[c.g - 1]) + c.n * BNT;
-        for (int kb = 0; kb < num_kb; ++kb, ++it) {
-          const int s = it % C::STAGES;
-          const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
-          if (!waited && it >= C::STAGES) finish_wait();  // the ring is full of early loads
-          if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, args.status)) {
-            ok = false;
-            break;
-          }
-          const uint32_t a_dst = smem_base + s * C::STAGE_BYTES;
-          mbar_arrive_expect_tx(full_bar(s), C::STAGE_BYTES);
-          if (SWIGLU) {
-            tma_load_2d(a_dst, &args.map_w, full_bar(s), kb * BK, wrow, pol_w);
-            tma_load_2d(a_dst + 64 * 128, &args.map_w, full_bar(s), kb * BK, wrow + args.w_rows / 2,
-                        pol_w);
-          } else {
-            tma_load_2d(a_dst, &args.map_w, full_bar(s), kb * BK, wrow, pol_w);
-          }
-          if (waited) {
-            tma_load_2d(a_dst + C::A_BYTES, &args.map_x, full_bar(s), kb * BK, xrow, pol_x);
-          } else {
-            ++pending_x;
-          }
+  if ((warp == 0 || warp == kProd1Warp) && lane == 0) {
+    // ------------------------------------------------------------ producers --
+    // Producer q loads the k-blocks kb with kb % 2 == q of every tile.
+    const int q = warp == 0 ? 0 : 1;
+    const uint64_t pol_w = policy_evict_first();  // weights are read once
+    const uint64_t pol_x = policy_evict_last();   // token rows are re-read
+    int it = 0;
+    bool ok = true;
+    // In early mode the weight boxes of the first ring's worth of k-blocks go
+    // out before the wait for the predecessor; their activation boxes (listed
+    // here) follow it.  Every producer flushes its list before its first wait
+    // on a ring slot, so no slot waits on a k-block whose tokens are held back.
+    int pend_s[C::STAGES], pend_kb[C::STAGES], pend_row[C::STAGES];
+    int n_pend = 0;
+    bool waited = !args.early;
+    auto finish_wait = [&]() {
+      pdl_wait();
+      waited = true;
+      for (int j = 0; j < n_pend; ++j)
+        tma_load_2d(smem_base + pend_s[j] * C::STAGE_BYTES + C::A_BYTES, &args.map_x, full_bar(pend_s[j]),
+                    pend_kb[j] * BK, pend_row[j], pol_x);
+      n_pend = 0;
+    };
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const Tile c = decode_swap_tile(t, tile_start, gend, G, args.m_tiles);
+      const int wrow = c.g * args.w_rows + c.m * rows_per_tile;
+      const int xrow = (c.g == 0 ? 0 : gend[c.g - 1]) + c.n * BNT;
+      for (int kb = 0; kb < num_kb; ++kb, ++it) {
+        if ((kb & 1) != q) continue;
+        const int s = it % C::STAGES;
+        const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
+        if (!waited && it >= C::STAGES) finish_wait();  // the ring is full of early loads
+        if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, args.status)) {
+          ok = false;
+          break;
+        }
+        const uint32_t a_dst = smem_base + s * C::STAGE_BYTES;
+        mbar_arrive_expect_tx(full_bar(s), C::STAGE_BYTES);
+        if (SWIGLU) {
+          tma_load_2d(a_dst, &args.map_w, full_bar(s), kb * BK, wrow, pol_w);
+          tma_load_2d(a_dst + 64 * 128, &args.map_w, full_bar(s), kb * BK, wrow + args.w_rows / 2,
+                      pol_w);
+        } else {
+          tma_load_2d(a_dst, &args.map_w, full_bar(s), kb * BK, wrow, pol_w);
+        }
+        if (waited) {
+          tma_load_2d(a_dst + C::A_BYTES, &args.map_x, full_bar(s), kb * BK, xrow, pol_x);
+        } else {
+          pend_s[n_pend] = s;
+          pend_kb[n_pend] = kb;
+          pend_row[n_pend] = xrow;
+          ++n_pend;
         }
       }
-      if (!waited) finish_wait();  // fewer k-blocks in total than ring stages
+    }
+    if (!waited) finish_wait();  // fewer k-blocks in total than ring stages
+    if (q == 0) {  // let the last copies of both producers land
       for (int j = it > C::STAGES ? it - C::STAGES : 0; j < it; ++j)
         mbar_wait(full_bar(j % C::STAGES), (uint32_t)(j / C::STAGES) & 1u, nullptr, args.status);
     }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // ------------------------------------------------------------ MMA issuer --
-      int it = 0, tc = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tc) {
-        const int acc = tc & 1;
-        const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
-        if (!mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag, args.status)) break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BNT);
-        for (int kb = 0; kb < num_kb; ++kb, ++it) {
-          const int s = it % C::STAGES;
-          const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
-          if (!mbar_wait(full_bar(s), ph, abort_flag, args.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a_addr = smem_base + s * C::STAGE_BYTES;
-          const uint64_t a_desc = smem_desc_k_sw128(a_addr);
-          const uint64_t b_desc = smem_desc_k_sw128(a_addr + C::A_BYTES);
-#pragma unroll
-          for (int k = 0; k < BK / 16; ++k)
-            umma_bf16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, C::IDESC, (kb | k) != 0);
-          umma_commit(empty_bar(s));
+  } else if ((warp == 1 || warp == kMma1Warp) && lane == 0) {
+    // ----------------------------------------------------------- MMA issuers --
+    // Issuer q multiplies the k-blocks kb % 2 == q into accumulator q of the
+    // tile's buffer and commits the tile once its last one is issued.
+    const int q = warp == 1 ? 0 : 1;
+    int it = 0, tc = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tc) {
+      const int acc = tc & 1;
+      const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
+      if (!mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag, args.status)) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + (uint32_t)((2 * acc + q) * BNT);
+      bool first = true;
+      for (int kb = 0; kb < num_kb; ++kb, ++it) {
+        if ((kb & 1) != q) continue;
+        const int s = it % C::STAGES;
+        const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
+        if (!mbar_wait(full_bar(s), ph, abort_flag, args.status)) {
+          ok = false;
+          break;
         }
-        if (ok) umma_commit(tfull_bar(acc));
+        tc_fence_after();
+        const uint32_t a_addr = smem_base + s * C::STAGE_BYTES;
+        const uint64_t a_desc = smem_desc_k_sw128(a_addr);
+        const uint64_t b_desc = smem_desc_k_sw128(a_addr + C::A_BYTES);
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k)
+          umma_bf16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, C::IDESC, (first && k == 0) ? 0u : 1u);
+        first = false;
+        umma_commit(empty_bar(s));
       }
-      umma_commit(drain_bar);
-      mbar_wait(drain_bar, 0, nullptr, args.status);
+      if (ok) umma_commit(tfull_bar(acc));
     }
-  } else {
+    umma_commit(drain_bar(q));
+    mbar_wait(drain_bar(q), 0, nullptr, args.status);
+  } else if (warp >= 2 && warp <= 5) {
     // ------------------------------------------------------------------ epilogue --
     if (args.early) pdl_wait();
     const int quarter = warp & 3;
@@ -311,7 +326,15 @@ __global__ void __launch_bounds__(kThreads, 1) swapab_kernel(const __grid_consta
       if (epi_bar_any(!got)) break;  // a wait gave up somewhere: all four warps stop together
       float v[BNT];
       tc_fence_after();
-      tmem_ld_cols<BNT>(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BNT), v);
+      const uint32_t lane_addr = tmem_base + ((uint32_t)(quarter * 32) << 16);
+      tmem_ld_cols<BNT>(lane_addr + (uint32_t)(2 * acc * BNT), v);
+      if (num_kb > 1) {  // the odd k-blocks' accumulator
+        float v1[BNT];
+        tmem_ld_cols<BNT>(lane_addr + (uint32_t)((2 * acc + 1) * BNT), v1);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < BNT; ++j) v[j] = __fadd_rn(v[j], v1[j]);
+      }
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(tempty_bar(acc));
