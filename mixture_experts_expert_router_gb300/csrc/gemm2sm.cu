@@ -44,24 +44,31 @@ namespace {
 
 constexpr int BM = 128;  // token (main) or weight (tail) rows per CTA
 constexpr int BN = 256;  // main tile MMA N (weight rows per pair; 128 staged by each CTA)
-constexpr int BK = 64;
+constexpr int BK = 64;  // k-block: one 128-byte-wide TMA box, four K = 16 MMAs
+// A ring stage holds KH k-blocks: one wait, 4 * KH MMAs and one commit per
+// stage.  A stage round (producer wait, arm, copies; MMA thread wait, MMAs,
+// commit) carries a fixed cost of the order of 200 ns; with one k-block per
+// stage that cost, not the tensor pipe, set the pace of a 256 x 256 tile
+// (about 84 ns per MMA instead of the 66 ns the pipe needs).
+constexpr int KH = 2;
 // warps: 0 token producer, 1 TMEM owner + MMA issuer, 2..5 epilogue (TMEM
 // lane quarters warp % 4), 6 weight producer
 constexpr int kThreads = 224;
 constexpr int kWeightWarp = 6;
-constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = (BN / 2) * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // per CTA, the largest stage
-constexpr int STG_BYTES = BM * 32 * 4;          // fp32 store staging: 128 rows x 32 columns
+constexpr int A_BYTES = BM * BK * 2;        // one k-block of the M-side operand
+constexpr int B_BYTES = (BN / 2) * BK * 2;  // one k-block of this CTA's half of the N side
+constexpr int A_STAGE = KH * A_BYTES;
+constexpr int STAGE_BYTES = KH * (A_BYTES + B_BYTES);  // per CTA: [A k-blocks][B k-blocks]
+constexpr int STG_BYTES = BM * 32 * 4;                 // fp32 store staging: 128 rows x 32 columns
 
-// Shared-memory layout per epilogue kind.  The fp32 form trades a ring stage
-// for two store-staging buffers.
+// Shared-memory layout per epilogue kind (the fp32 form adds one store-staging
+// buffer).
 template <int EPI>
 struct PairLayout {
-  static constexpr int STAGES = EPI == (int)Epi::kF32 ? 5 : 6;
+  static constexpr int STAGES = 3;
   static constexpr int NBARS = 2 * STAGES + 5;
   static constexpr int STG_OFF = STAGES * STAGE_BYTES;
-  static constexpr int BAR_OFF = STG_OFF + (EPI == (int)Epi::kF32 ? 2 * STG_BYTES : 0);
+  static constexpr int BAR_OFF = STG_OFF + (EPI == (int)Epi::kF32 ? STG_BYTES : 0);
   static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
   static constexpr int SG_OFF = MISC_OFF + 16;  // tail gate hand-off [16][64] fp32
   static constexpr int TAB_OFF = SG_OFF + 16 * 64 * 4;
@@ -170,7 +177,7 @@ __device__ __forceinline__ PairOperands pair_operands(const PairTile &c, uint32_
       o.w_row = c.g * b_rows + c.n * (BN / 2) + (int)rank * (b_rows / 2);
     else
       o.w_row = c.g * b_rows + c.n * BN + (int)rank * (BN / 2);
-    o.bytes = STAGE_BYTES;
+    o.bytes = A_BYTES + B_BYTES;
     o.tok_rows = BM;
   } else {
     const int n = tail_n(c.tail);
@@ -272,6 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
   const uint32_t tmem_base = *tmem_holder;
   const int total = tile_start[G] * args.n_tiles;
   const int num_kb = args.K / BK;
+  const int n_rounds = (num_kb + KH - 1) / KH;  // ring stages per tile
   const int cluster = blockIdx.x >> 1;
   const int nclusters = gridDim.x >> 1;
 
@@ -306,9 +314,10 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
         tr3 = tr[3];
       }
       const CUtensorMap *tok_map = c.tail ? &args.map_t[o.tmap] : &args.map_a;
-      for (int kb = 0; kb < num_kb; ++kb, ++it) {
+      for (int kr = 0; kr < n_rounds; ++kr, ++it) {
         const int s = it % STAGES;
         const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+        const int nk = min(KH, num_kb - kr * KH);
         int w_ok = 1;
         if (lane == 0) w_ok = mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, args.status) ? 1 : 0;
         if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
@@ -316,14 +325,17 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
           break;
         }
         const uint32_t leader_full = mapa_shared(full_bar(s), 0);
-        if (lane == 0 && rank == 0) mbar_arrive_expect_tx(full_bar(s), 2 * o.bytes);
+        if (lane == 0 && rank == 0) mbar_arrive_expect_tx(full_bar(s), 2 * o.bytes * (uint32_t)nk);
         __syncwarp();
-        const uint32_t t_dst = smem_base + s * STAGE_BYTES + (c.tail ? A_BYTES : 0);
-        if (gath) {
-          if (tok_lane)
-            tma_gather4_pair(t_dst + lane * 512, &args.map_xg, leader_full, kb * BK, tr0, tr1, tr2, tr3, pol);
-        } else if (lane == 0) {
-          tma_load_2d_pair(t_dst, tok_map, leader_full, kb * BK, o.tok_row, pol);
+        for (int h = 0; h < nk; ++h) {
+          const int kx = (kr * KH + h) * BK;
+          const uint32_t t_dst = smem_base + s * STAGE_BYTES + (c.tail ? A_STAGE + h * B_BYTES : h * A_BYTES);
+          if (gath) {
+            if (tok_lane)
+              tma_gather4_pair(t_dst + lane * 512, &args.map_xg, leader_full, kx, tr0, tr1, tr2, tr3, pol);
+          } else if (lane == 0) {
+            tma_load_2d_pair(t_dst, tok_map, leader_full, kx, o.tok_row, pol);
+          }
         }
       }
     }
@@ -345,20 +357,24 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
         // through); everything else is read again by neighbouring tiles (keep it)
         const uint64_t pol = (c.tail && c.mp == 0) ? pol_first : pol_last;
         const PairOperands o = pair_operands<kSwiGLU>(c, rank, args.b_rows);
-        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+        for (int kr = 0; kr < n_rounds; ++kr, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+          const int nk = min(KH, num_kb - kr * KH);
           if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, args.status)) {
             ok = false;
             break;
           }
           const uint32_t leader_full = mapa_shared(full_bar(s), 0);
-          const uint32_t w_dst = smem_base + s * STAGE_BYTES + (c.tail ? 0 : A_BYTES);
-          if (c.tail && kSwiGLU) {  // 64 up rows then the matching 64 gate rows
-            tma_load_2d_pair(w_dst, &args.map_w64, leader_full, kb * BK, o.w_row, pol);
-            tma_load_2d_pair(w_dst + 64 * 128, &args.map_w64, leader_full, kb * BK, o.w_row2, pol);
-          } else {
-            tma_load_2d_pair(w_dst, &args.map_b, leader_full, kb * BK, o.w_row, pol);
+          for (int h = 0; h < nk; ++h) {
+            const int kx = (kr * KH + h) * BK;
+            const uint32_t w_dst = smem_base + s * STAGE_BYTES + (c.tail ? h * A_BYTES : A_STAGE + h * B_BYTES);
+            if (c.tail && kSwiGLU) {  // 64 up rows then the matching 64 gate rows
+              tma_load_2d_pair(w_dst, &args.map_w64, leader_full, kx, o.w_row, pol);
+              tma_load_2d_pair(w_dst + 64 * 128, &args.map_w64, leader_full, kx, o.w_row2, pol);
+            } else {
+              tma_load_2d_pair(w_dst, &args.map_b, leader_full, kx, o.w_row, pol);
+            }
           }
         }
       }
@@ -376,20 +392,23 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
         if (!mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag, args.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+        for (int kr = 0; kr < n_rounds; ++kr, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+          const int nk = min(KH, num_kb - kr * KH);
           if (!mbar_wait(full_bar(s), ph, abort_flag, args.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_base + s * STAGE_BYTES;
-          const uint64_t a_desc = smem_desc_k_sw128(a_addr);
-          const uint64_t b_desc = smem_desc_k_sw128(a_addr + A_BYTES);
+          const uint32_t st = smem_base + s * STAGE_BYTES;
+          for (int h = 0; h < nk; ++h) {
+            const uint64_t a_desc = smem_desc_k_sw128(st + h * A_BYTES);
+            const uint64_t b_desc = smem_desc_k_sw128(st + A_STAGE + h * B_BYTES);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k)
-            umma_bf16_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, (kb | k) != 0);
+            for (int k = 0; k < BK / 16; ++k)
+              umma_bf16_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, (kr | h | k) != 0);
+          }
           umma_commit_pair(empty_bar(s), 0x3);
         }
         if (ok) umma_commit_pair(tfull_bar(acc), 0x3);
@@ -441,19 +460,18 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
         } else if (EPI == (int)Epi::kF32) {
           if (valid >= BM) {
             // full tile: 32-column chunks staged in swizzled shared memory and
-            // written by TMA stores (whole 128-byte rows), two buffers in turn
+            // written by TMA stores (whole 128-byte rows)
             const int etid = threadIdx.x - 64;
 #pragma unroll 1
             for (int col = 0; col < BN; col += 32) {
-              const int buf = (col >> 5) & 1;
-              if (col >= 64) {  // the store that used this buffer two chunks ago has read it
-                if (etid == 0) bulk_wait_read<1>();
+              if (col > 0) {  // the previous chunk's store has read the staging buffer
+                if (etid == 0) bulk_wait_read<0>();
                 epi_bar();
               }
               uint32_t r[32];
               tmem_ld_32x32b_x32(taddr + col, r);
               tmem_ld_wait();
-              const uint32_t row_addr = smem_base + Lay::STG_OFF + buf * STG_BYTES + r_in_tile * 128;
+              const uint32_t row_addr = smem_base + Lay::STG_OFF + r_in_tile * 128;
 #pragma unroll
               for (int v = 0; v < 8; ++v)
                 asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
@@ -463,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
               fence_proxy_async_smem();
               epi_bar();
               if (etid == 0) {
-                tma_store_2d(&args.map_y, smem_base + Lay::STG_OFF + buf * STG_BYTES, c.n * BN + col, row0);
+                tma_store_2d(&args.map_y, smem_base + Lay::STG_OFF, c.n * BN + col, row0);
                 bulk_commit();
               }
             }
