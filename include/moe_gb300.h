@@ -252,9 +252,12 @@ MOE_API int moe_forward(const moe_bf16 *x, const float *logits, const int32_t *t
 #define MOE_PLAN_STAGE_TIMING 1 /* record CUDA events around each stage     */
 #define MOE_PLAN_ONE_CTA_GEMM 2 /* grouped path: one-CTA GEMM kernels instead of
                                    the CTA-pair (2-SM MMA) kernels (comparison) */
-#define MOE_PLAN_DECODE_CHAIN 4 /* decode path, T*top_k <= 1024: two kernels with
-                                   the sort, gather and finalize folded in, instead
-                                   of five (fewer launches; measured slower) */
+#define MOE_PLAN_DECODE_CHAIN 4 /* decode path, T*top_k <= 1024: always the two
+                                   kernels with the sort, gather and finalize
+                                   folded in (without either flag the chain runs
+                                   for T*top_k <= 8, where it measured faster) */
+#define MOE_PLAN_DECODE_SEPARATE 8 /* decode path: always the five separate
+                                      kernels (sort, gather, FC1, FC2, finalize) */
 
 typedef struct moe_forward_desc {
     const moe_bf16 *x;

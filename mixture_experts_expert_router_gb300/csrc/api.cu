@@ -373,11 +373,13 @@ int moe_forward_prepare(const moe_forward_desc *desc, moe_plan **plan_out) {
     p->h = reinterpret_cast<uint16_t *>(ws + lay.h);
     p->y = reinterpret_cast<float *>(ws + lay.y);
     int rc;
-    // The separate decode kernels measured faster than the chain (its in-kernel
-    // row gathers and combine cost more than the three launches they save),
-    // so the chain runs only when asked for.
-    p->use_chain = p->path == MOE_PATH_DECODE && p->R <= kChainMaxRoutes &&
-                   (d.flags & MOE_PLAN_DECODE_CHAIN) != 0;
+    // Decode: the two-kernel chain saves three launches but gathers its token
+    // rows and combines inside the GEMM kernels; it is the faster form only for
+    // very few routes, so without a flag it runs up to kChainAutoRoutes routes.
+    const bool force_chain = (d.flags & MOE_PLAN_DECODE_CHAIN) != 0;
+    const bool auto_chain = (d.flags & MOE_PLAN_DECODE_SEPARATE) == 0 && p->R <= kChainAutoRoutes &&
+                            d.H % 64 == 0 && d.I % 64 == 0;
+    p->use_chain = p->path == MOE_PATH_DECODE && p->R <= kChainMaxRoutes && (force_chain || auto_chain);
     if (p->use_chain) {
       ChainPlan &c = p->chain;
       c.x = d.x;

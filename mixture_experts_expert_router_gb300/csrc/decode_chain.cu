@@ -19,6 +19,10 @@
 //        out = bf16(sum_j w_j * y_j), exactly the finalize kernel's
 //        arithmetic, so the result does not depend on which tile is last.
 //
+// The k-loop of both kernels runs as two half-pipelines (even / odd k-blocks,
+// each with its own producer, MMA thread and TMEM accumulator; the epilogue
+// adds the two), as in decode.cu.
+//
 // Programmatic dependent launch: each kernel reads only the layer's inputs
 // (and, in logits mode, the routing kernel's output, waited for) before its
 // griddepcontrol.wait; it writes nothing before it.
@@ -31,7 +35,11 @@ namespace moe {
 namespace {
 
 constexpr int BK = 64;
-constexpr int kThreads = 192;
+// warps: 0 / 6 producers of the even / odd k-blocks, 1 / 7 their MMA issuers
+// (1 also owns TMEM), 2..5 epilogue
+constexpr int kThreads = 256;
+constexpr int kProd1Warp = 6;
+constexpr int kMma1Warp = 7;
 constexpr int kEpiThreads = 128;
 
 struct ChainArgs {
@@ -54,12 +62,12 @@ struct ChainCfg {
   static constexpr int B_BYTES = BNT * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = BNT == 64 ? 6 : (BNT == 32 ? 7 : 8);
-  static constexpr int NBARS = 2 * STAGES + 5;
+  static constexpr int NBARS = 2 * STAGES + 6;
   static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
   static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;         // tmem base, abort, bad flag
   static constexpr int SG_OFF = (MISC_OFF + 16 + 15) & ~15;    // [BNT][64] fp32 (FC1) / flags (FC2)
   static constexpr int TAB_OFF = SG_OFF + BNT * 64 * 4;
-  static constexpr uint32_t TMEM_COLS = 2 * BNT < 32 ? 32 : 2 * BNT;
+  static constexpr uint32_t TMEM_COLS = 4 * BNT;  // [tile buffer][half-pipeline] accumulators
   static constexpr uint32_t IDESC = idesc_bf16_f32(128, BNT);
   // tables: m_indptr [L+1], next [L+1], tile_start [L+1], p2e [R], e2p [R], tok_n [T]
   static size_t smem_bytes(int L, int R, int T) {
@@ -145,6 +153,17 @@ struct Tile {
   int g, m, n;
 };
 
+// 16 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
 __device__ __forceinline__ Tile decode_tile(int t, const int *tile_start, int L, int m_tiles) {
   int lo = 0, hi = L;
   while (hi - lo > 1) {
@@ -173,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
   auto empty_bar = [&](int s) { return bar_base + 8u * (C::STAGES + s); };
   auto tfull_bar = [&](int x) { return bar_base + 8u * (2 * C::STAGES + x); };
   auto tempty_bar = [&](int x) { return bar_base + 8u * (2 * C::STAGES + 2 + x); };
-  const uint32_t drain_bar = bar_base + 8u * (2 * C::STAGES + 4);
+  auto drain_bar = [&](int q) { return bar_base + 8u * (2 * C::STAGES + 4 + q); };
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
   volatile int *bad = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 8);
@@ -196,10 +215,10 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
       mbar_init(empty_bar(s), 1);
     }
     for (int x = 0; x < 2; ++x) {
-      mbar_init(tfull_bar(x), 1);
+      mbar_init(tfull_bar(x), 2);  // both MMA issuers commit
       mbar_init(tempty_bar(x), kEpiThreads);
+      mbar_init(drain_bar(x), 1);
     }
-    mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -252,23 +271,30 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
   const int rows_per_box = FC1 ? 64 : 128;
   const int M = m_indptr[L];
 
-  if (warp == 0) {
-    // ---------------------------------------------------------------- producer --
+  if ((warp == 0 || warp == kProd1Warp)) {
+    // --------------------------------------------------------------- producers --
+    // Producer q (warp 0: q = 0, warp 6: q = 1) loads the k-blocks kb % 2 == q
+    // of every tile; FC1's token rows come from the lanes, four rows each.
+    const int q = warp == 0 ? 0 : 1;
     const uint64_t pol_w = policy_evict_first();  // each weight byte is read once
     const uint64_t pol_x = policy_evict_last();
     int it = 0;
     bool ok = true;
-    int pending = 0;          // FC2: first-ring stages waiting for their h box
-    bool waited = FC1;        // FC1 reads only inputs: it never waits here
+    // FC2 in early mode: the h boxes of the first tile's k-blocks that went out
+    // before FC1 had finished, listed here and loaded once it has.  Every
+    // producer flushes its list before its first wait on a ring slot.
+    int pend_s[C::STAGES], pend_kb[C::STAGES];
+    int n_pend = 0;
+    bool waited = FC1;  // FC1 reads only inputs: it never waits here
     int first_xrow = 0;
-    auto finish_wait = [&]() {  // FC2: FC1 has finished; load the pending h boxes
+    auto finish_wait = [&]() {
       pdl_wait();
       waited = true;
       if (lane == 0)
-        for (int j = 0; j < pending; ++j)
-          tma_load_2d(smem_base + j * C::STAGE_BYTES + C::A_BYTES, &a.map_x, full_bar(j), j * BK,
-                      first_xrow, pol_x);
-      pending = 0;
+        for (int j = 0; j < n_pend; ++j)
+          tma_load_2d(smem_base + pend_s[j] * C::STAGE_BYTES + C::A_BYTES, &a.map_x, full_bar(pend_s[j]),
+                      pend_kb[j] * BK, first_xrow, pol_x);
+      n_pend = 0;
     };
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       if (!waited && t != (int)blockIdx.x) finish_wait();
@@ -291,6 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         tr3 = tr[3];
       }
       for (int kb = 0; kb < num_kb; ++kb, ++it) {
+        if ((kb & 1) != q) continue;
         const int s = it % C::STAGES;
         const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
         if (!waited && it >= C::STAGES) finish_wait();
@@ -318,47 +345,53 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         } else if (waited) {
           if (lane == 0) tma_load_2d(a_dst + C::A_BYTES, &a.map_x, full_bar(s), kb * BK, xrow, pol_x);
         } else {
-          ++pending;
+          pend_s[n_pend] = s;
+          pend_kb[n_pend] = kb;
+          ++n_pend;
         }
       }
     }
     if (!waited) finish_wait();
-    if (lane == 0)
+    if (q == 0 && lane == 0)  // let the last copies of both producers land
       for (int j = it > C::STAGES ? it - C::STAGES : 0; j < it; ++j)
         mbar_wait(full_bar(j % C::STAGES), (uint32_t)(j / C::STAGES) & 1u, nullptr, a.status);
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // -------------------------------------------------------------- MMA issuer --
-      int it = 0, tc = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tc) {
-        const int acc = tc & 1;
-        const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
-        if (!mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag, a.status)) break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BNT);
-        for (int kb = 0; kb < num_kb; ++kb, ++it) {
-          const int s = it % C::STAGES;
-          const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
-          if (!mbar_wait(full_bar(s), ph, abort_flag, a.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a_addr = smem_base + s * C::STAGE_BYTES;
-          const uint64_t a_desc = smem_desc_k_sw128(a_addr);
-          const uint64_t b_desc = smem_desc_k_sw128(a_addr + C::A_BYTES);
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            umma_bf16(d_tmem, a_desc + 2u * kk, b_desc + 2u * kk, C::IDESC, (kb | kk) != 0);
-          umma_commit(empty_bar(s));
+  } else if ((warp == 1 || warp == kMma1Warp) && lane == 0) {
+    // ------------------------------------------------------------- MMA issuers --
+    // Issuer q multiplies the k-blocks kb % 2 == q into accumulator q of the
+    // tile's buffer; both commit every tile.
+    const int q = warp == 1 ? 0 : 1;
+    int it = 0, tc = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tc) {
+      const int acc = tc & 1;
+      const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
+      if (!mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag, a.status)) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + (uint32_t)((2 * acc + q) * BNT);
+      bool first = true;
+      for (int kb = 0; kb < num_kb; ++kb, ++it) {
+        if ((kb & 1) != q) continue;
+        const int s = it % C::STAGES;
+        const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
+        if (!mbar_wait(full_bar(s), ph, abort_flag, a.status)) {
+          ok = false;
+          break;
         }
-        if (ok) umma_commit(tfull_bar(acc));
+        tc_fence_after();
+        const uint32_t a_addr = smem_base + s * C::STAGE_BYTES;
+        const uint64_t a_desc = smem_desc_k_sw128(a_addr);
+        const uint64_t b_desc = smem_desc_k_sw128(a_addr + C::A_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          umma_bf16(d_tmem, a_desc + 2u * kk, b_desc + 2u * kk, C::IDESC, (first && kk == 0) ? 0u : 1u);
+        first = false;
+        umma_commit(empty_bar(s));
       }
-      umma_commit(drain_bar);
-      mbar_wait(drain_bar, 0, nullptr, a.status);
+      if (ok) umma_commit(tfull_bar(acc));
     }
-  } else {
+    umma_commit(drain_bar(q));
+    mbar_wait(drain_bar(q), 0, nullptr, a.status);
+  } else if (warp >= 2 && warp <= 5) {
     // ---------------------------------------------------------------- epilogue --
     pdl_wait();  // the previous kernel may still read what this one writes
     const int quarter = warp & 3;
@@ -393,20 +426,23 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
       if (epi_bar_any(!got)) break;
       float v[BNT];
       tc_fence_after();
+      const uint32_t lane_addr = tmem_base + ((uint32_t)(quarter * 32) << 16);
 #pragma unroll
       for (int c0 = 0; c0 < BNT; c0 += 16) {
         uint32_t q[16];
-        asm volatile(
-            "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-            "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-            : "=r"(q[0]), "=r"(q[1]), "=r"(q[2]), "=r"(q[3]), "=r"(q[4]), "=r"(q[5]), "=r"(q[6]),
-              "=r"(q[7]), "=r"(q[8]), "=r"(q[9]), "=r"(q[10]), "=r"(q[11]), "=r"(q[12]),
-              "=r"(q[13]), "=r"(q[14]), "=r"(q[15])
-            : "r"(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BNT + c0)));
+        tmem_ld_x16(lane_addr + (uint32_t)(2 * acc * BNT + c0), q);
+        if (num_kb > 1) {  // the odd k-blocks' accumulator
+          uint32_t q1[16];
+          tmem_ld_x16(lane_addr + (uint32_t)((2 * acc + 1) * BNT + c0), q1);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            q[i] = __float_as_uint(__fadd_rn(__uint_as_float(q[i]), __uint_as_float(q1[i])));
+        }
+        tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < 16; ++i) v[c0 + i] = __uint_as_float(q[i]);
       }
-      tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(tempty_bar(acc));
       if (FC1) {

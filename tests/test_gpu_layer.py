@@ -197,7 +197,7 @@ def test_all_tokens_on_one_expert():
 
 # ---------------------------------------------------------- workload shapes --
 
-@pytest.mark.parametrize("chain", [False, True])
+@pytest.mark.parametrize("chain", [False, True, None])
 @pytest.mark.parametrize("name", ["decode_t1", "decode_t8", "decode_t64"])
 @pytest.mark.parametrize("path", PATHS)
 def test_decode_configs_full(name, path, chain):
@@ -205,6 +205,29 @@ def test_decode_configs_full(name, path, chain):
     out, _ = _forward(wl, _dev(wl), path, decode_chain=chain)
     want, _ = _oracle_out(wl)
     check_bf16_end_to_end(W.bf16_bits(out), want, name)
+
+
+@pytest.mark.parametrize("T,kernels", [(1, 2), (8, 5)])
+def test_decode_form_chosen_by_route_count(T, kernels):
+    """Without a flag the decode path runs the two-kernel chain for at most 8
+    routes (T = 1 at top-8) and the five separate kernels above that."""
+    wl = W.make_moe(T=T, H=256, I=128, E=16, top_k=8, mode="prerouted", seed=T)
+    out, plan = _forward(wl, _dev(wl), moe.PATH_AUTO, decode_chain=None)
+    assert plan.kernels_per_launch() == kernels
+    want, _ = _oracle_out(wl)
+    check_bf16_end_to_end(W.bf16_bits(out), want, f"T={T} automatic decode form")
+
+
+@pytest.mark.parametrize("T,H,I,E,k,mode", [(3, 64, 192, 8, 2, "prerouted"), (5, 192, 64, 6, 3, "logits"),
+                                             (40, 128, 320, 16, 4, "prerouted")])
+def test_decode_chain_small_shapes(T, H, I, E, k, mode):
+    """The two-kernel decode chain at shapes with one k-block (FC1 at H = 64,
+    FC2 at I = 64) and odd k-block counts (H = 192, I = 320, 192): the
+    k-blocks alternate between two accumulators."""
+    wl = W.make_moe(T=T, H=H, I=I, E=E, top_k=k, mode=mode, seed=T + H)
+    out, _ = _forward(wl, _dev(wl), moe.PATH_DECODE, decode_chain=True)
+    want, _ = _oracle_out(wl)
+    check_bf16_end_to_end(W.bf16_bits(out), want, "decode chain")
 
 
 def _sample_tokens(ids, T, n, seed):
