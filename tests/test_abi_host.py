@@ -88,3 +88,20 @@ def test_workspace_size_and_prepare_errors(lib):
     assert lib.moe_forward_prepare(ctypes.byref(d), ctypes.byref(h)) == -2   # top_k > E
     assert lib.moe_plan_launch(None, None) == -1
     assert lib.moe_plan_destroy(None) == 0
+
+
+def test_binding_constants_match_header():
+    """The Python binding's path, plan-flag and device-status constants carry
+    the values include/moe_gb300.h defines."""
+    text = open(HEADER).read()
+    defines = {m.group(1): int(m.group(2)) for m in re.finditer(r"^#define\s+(MOE_\w+)\s+(-?\d+)", text, re.M)}
+    pairs = {"MOE_PATH_AUTO": moe.PATH_AUTO, "MOE_PATH_GROUPED": moe.PATH_GROUPED,
+             "MOE_PATH_DECODE": moe.PATH_DECODE, "MOE_PLAN_STAGE_TIMING": moe.PLAN_STAGE_TIMING,
+             "MOE_PLAN_ONE_CTA_GEMM": moe.PLAN_ONE_CTA_GEMM, "MOE_PLAN_DECODE_CHAIN": moe.PLAN_DECODE_CHAIN,
+             "MOE_PLAN_DECODE_SEPARATE": moe.PLAN_DECODE_SEPARATE,
+             "MOE_DEV_BAD_EXPERT": moe.DEV_BAD_EXPERT, "MOE_DEV_TIMEOUT": moe.DEV_TIMEOUT}
+    for name, value in pairs.items():
+        assert defines.get(name) == value, name
+    plan_flags = {k: v for k, v in defines.items() if k.startswith("MOE_PLAN_")}
+    assert len(set(plan_flags.values())) == len(plan_flags)  # distinct bits
+    assert all(v & (v - 1) == 0 for v in plan_flags.values())
