@@ -58,7 +58,8 @@ struct SwapCfg {
   static constexpr int A_BYTES = 128 * BK * 2;
   static constexpr int B_BYTES = BNT * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = BNT == 64 ? 8 : 10;
+  static constexpr int STAGES = BNT == 64 ? 8 : 10;  // two private halves, one per half-pipeline
+  static_assert(STAGES % 2 == 0, "the ring splits evenly between the half-pipelines");
   static constexpr int TILE_BYTES = STAGES * STAGE_BYTES;
   static constexpr int NBARS = 2 * STAGES + 6;
   static constexpr int BAR_OFF = TILE_BYTES;
@@ -213,6 +214,10 @@ __global__ void __launch_bounds__(kThreads, 1) swapab_kernel(const __grid_consta
   const uint32_t tmem_base = *tmem_holder;
   const int total = tile_start[G];
   const int num_kb = args.K / BK;
+  // Each half-pipeline owns half of the ring (slots q * HS .. q * HS + HS - 1),
+  // so a slot is only ever filled and drained by one producer / MMA pair and
+  // every wait on it is for the phase right after the one it last saw.
+  constexpr int HS = C::STAGES / 2;
 
   if ((warp == 0 || warp == kProd1Warp) && lane == 0) {
     // ------------------------------------------------------------ producers --
@@ -220,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1) swapab_kernel(const __grid_consta
     const int q = warp == 0 ? 0 : 1;
     const uint64_t pol_w = policy_evict_first();  // weights are read once
     const uint64_t pol_x = policy_evict_last();   // token rows are re-read
-    int it = 0;
+    int iq = 0;  // this pipeline's k-blocks so far: its private ring slots q * HS + iq % HS
     bool ok = true;
     // In early mode the weight boxes of the first ring's worth of k-blocks go
     // out before the wait for the predecessor; their activation boxes (listed
@@ -241,11 +246,12 @@ __global__ void __launch_bounds__(kThreads, 1) swapab_kernel(const __grid_consta
       const Tile c = decode_swap_tile(t, tile_start, gend, G, args.m_tiles);
       const int wrow = c.g * args.w_rows + c.m * rows_per_tile;
       const int xrow = (c.g == 0 ? 0 : gend[c.g - 1]) + c.n * BNT;
-      for (int kb = 0; kb < num_kb; ++kb, ++it) {
+      for (int kb = 0; kb < num_kb; ++kb) {
         if ((kb & 1) != q) continue;
-        const int s = it % C::STAGES;
-        const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
-        if (!waited && it >= C::STAGES) finish_wait();  // the ring is full of early loads
+        const int s = q * HS + iq % HS;
+        const uint32_t ph = (uint32_t)(iq / HS) & 1u;
+        ++iq;
+        if (!waited && iq > HS) finish_wait();  // this pipeline's ring is full of early loads
         if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, args.status)) {
           ok = false;
           break;
@@ -270,16 +276,15 @@ __global__ void __launch_bounds__(kThreads, 1) swapab_kernel(const __grid_consta
       }
     }
     if (!waited) finish_wait();  // fewer k-blocks in total than ring stages
-    if (q == 0) {  // let the last copies of both producers land
-      for (int j = it > C::STAGES ? it - C::STAGES : 0; j < it; ++j)
-        mbar_wait(full_bar(j % C::STAGES), (uint32_t)(j / C::STAGES) & 1u, nullptr, args.status);
-    }
+    // let this pipeline's last copies land
+    for (int j = iq > HS ? iq - HS : 0; j < iq; ++j)
+      mbar_wait(full_bar(q * HS + j % HS), (uint32_t)(j / HS) & 1u, nullptr, args.status);
   } else if ((warp == 1 || warp == kMma1Warp) && lane == 0) {
     // ----------------------------------------------------------- MMA issuers --
     // Issuer q multiplies the k-blocks kb % 2 == q into accumulator q of the
     // tile's buffer and commits the tile once its last one is issued.
     const int q = warp == 1 ? 0 : 1;
-    int it = 0, tc = 0;
+    int iq = 0, tc = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tc) {
       const int acc = tc & 1;
@@ -288,10 +293,11 @@ __global__ void __launch_bounds__(kThreads, 1) swapab_kernel(const __grid_consta
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)((2 * acc + q) * BNT);
       bool first = true;
-      for (int kb = 0; kb < num_kb; ++kb, ++it) {
+      for (int kb = 0; kb < num_kb; ++kb) {
         if ((kb & 1) != q) continue;
-        const int s = it % C::STAGES;
-        const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
+        const int s = q * HS + iq % HS;
+        const uint32_t ph = (uint32_t)(iq / HS) & 1u;
+        ++iq;
         if (!mbar_wait(full_bar(s), ph, abort_flag, args.status)) {
           ok = false;
           break;

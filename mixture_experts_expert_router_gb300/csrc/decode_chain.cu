@@ -61,7 +61,8 @@ struct ChainCfg {
   static constexpr int A_BYTES = 128 * BK * 2;
   static constexpr int B_BYTES = BNT * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = BNT == 64 ? 6 : (BNT == 32 ? 7 : 8);
+  static constexpr int STAGES = BNT == 64 ? 6 : 8;  // two private halves, one per half-pipeline
+  static_assert(STAGES % 2 == 0, "the ring splits evenly between the half-pipelines");
   static constexpr int NBARS = 2 * STAGES + 6;
   static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
   static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;         // tmem base, abort, bad flag
@@ -268,6 +269,10 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
   const uint32_t tmem_base = *tmem_holder;
   const int total = tile_start[L];
   const int num_kb = a.K / BK;
+  // Each half-pipeline owns half of the ring (slots q * HS .. q * HS + HS - 1),
+  // so a slot is only ever filled and drained by one producer / MMA pair and
+  // every wait on it is for the phase right after the one it last saw.
+  constexpr int HS = C::STAGES / 2;
   const int rows_per_box = FC1 ? 64 : 128;
   const int M = m_indptr[L];
 
@@ -278,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
     const int q = warp == 0 ? 0 : 1;
     const uint64_t pol_w = policy_evict_first();  // each weight byte is read once
     const uint64_t pol_x = policy_evict_last();
-    int it = 0;
+    int iq = 0;  // this pipeline's k-blocks so far: its private ring slots q * HS + iq % HS
     bool ok = true;
     // FC2 in early mode: the h boxes of the first tile's k-blocks that went out
     // before FC1 had finished, listed here and loaded once it has.  Every
@@ -316,11 +321,12 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         tr2 = tr[2];
         tr3 = tr[3];
       }
-      for (int kb = 0; kb < num_kb; ++kb, ++it) {
+      for (int kb = 0; kb < num_kb; ++kb) {
         if ((kb & 1) != q) continue;
-        const int s = it % C::STAGES;
-        const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
-        if (!waited && it >= C::STAGES) finish_wait();
+        const int s = q * HS + iq % HS;
+        const uint32_t ph = (uint32_t)(iq / HS) & 1u;
+        ++iq;
+        if (!waited && iq > HS) finish_wait();
         int w_ok = 1;
         if (lane == 0) w_ok = mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, a.status) ? 1 : 0;
         if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
@@ -352,15 +358,15 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
       }
     }
     if (!waited) finish_wait();
-    if (q == 0 && lane == 0)  // let the last copies of both producers land
-      for (int j = it > C::STAGES ? it - C::STAGES : 0; j < it; ++j)
-        mbar_wait(full_bar(j % C::STAGES), (uint32_t)(j / C::STAGES) & 1u, nullptr, a.status);
+    if (lane == 0)  // let this pipeline's last copies land
+      for (int j = iq > HS ? iq - HS : 0; j < iq; ++j)
+        mbar_wait(full_bar(q * HS + j % HS), (uint32_t)(j / HS) & 1u, nullptr, a.status);
   } else if ((warp == 1 || warp == kMma1Warp) && lane == 0) {
     // ------------------------------------------------------------- MMA issuers --
     // Issuer q multiplies the k-blocks kb % 2 == q into accumulator q of the
     // tile's buffer; both commit every tile.
     const int q = warp == 1 ? 0 : 1;
-    int it = 0, tc = 0;
+    int iq = 0, tc = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tc) {
       const int acc = tc & 1;
@@ -369,10 +375,11 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)((2 * acc + q) * BNT);
       bool first = true;
-      for (int kb = 0; kb < num_kb; ++kb, ++it) {
+      for (int kb = 0; kb < num_kb; ++kb) {
         if ((kb & 1) != q) continue;
-        const int s = it % C::STAGES;
-        const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
+        const int s = q * HS + iq % HS;
+        const uint32_t ph = (uint32_t)(iq / HS) & 1u;
+        ++iq;
         if (!mbar_wait(full_bar(s), ph, abort_flag, a.status)) {
           ok = false;
           break;

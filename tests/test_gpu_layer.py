@@ -219,11 +219,13 @@ def test_decode_form_chosen_by_route_count(T, kernels):
 
 
 @pytest.mark.parametrize("T,H,I,E,k,mode", [(3, 64, 192, 8, 2, "prerouted"), (5, 192, 64, 6, 3, "logits"),
-                                             (40, 128, 320, 16, 4, "prerouted")])
+                                             (40, 128, 320, 16, 4, "prerouted"),
+                                             (20, 192, 320, 64, 8, "prerouted"), (64, 192, 320, 128, 8, "logits")])
 def test_decode_chain_small_shapes(T, H, I, E, k, mode):
     """The two-kernel decode chain at shapes with one k-block (FC1 at H = 64,
     FC2 at I = 64) and odd k-block counts (H = 192, I = 320, 192): the
-    k-blocks alternate between two accumulators."""
+    k-blocks alternate between two accumulators.  T = 20 takes the 32-token
+    tile form; the last two shapes give CTAs several tiles."""
     wl = W.make_moe(T=T, H=H, I=I, E=E, top_k=k, mode=mode, seed=T + H)
     out, _ = _forward(wl, _dev(wl), moe.PATH_DECODE, decode_chain=True)
     want, _ = _oracle_out(wl)

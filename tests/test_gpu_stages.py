@@ -190,12 +190,14 @@ def test_grouped_gemm_rows_beyond_offsets_untouched():
 
 @pytest.mark.parametrize("T,H,I,E,k,max_group", [(1, 2048, 768, 128, 8, 1), (8, 256, 128, 16, 4, 8),
                                                  (64, 192, 320, 32, 8, 64), (40, 128, 64, 3, 2, 16),
-                                                 (300, 128, 128, 5, 2, 32), (6, 64, 128, 4, 2, 16)])
+                                                 (300, 128, 128, 5, 2, 32), (6, 64, 128, 4, 2, 16),
+                                                 (64, 192, 320, 128, 8, 64)])
 def test_swapab_fc1_fc2_stage_parity(T, H, I, E, k, max_group):
     """Decode-form kernels (weights on the MMA's M side) on the oracle's own
     intermediates; groups larger than the N tile run in several N tiles.  The
     k-blocks alternate between two accumulators: the shapes include one k-block
-    (H = 64 for FC1, I = 64 for FC2) and odd counts (H = 192, I = 320)."""
+    (H = 64 for FC1, I = 64 for FC2) and odd counts (H = 192, I = 320), the
+    last also with several tiles per CTA (hundreds of expert tiles)."""
     wl = W.make_moe(T=T, H=H, I=I, E=E, top_k=k, mode="logits", seed=T + 11)
     x, w1, w2 = W.bf16_bits(wl.x), W.bf16_bits(wl.w1), W.bf16_bits(wl.w2)
     ids, w = oracle.route(wl.logits.numpy(), k)
