@@ -12,9 +12,10 @@
 //              weight rows take the M side (128 staged by each CTA) and the r
 //              token rows the N side (N = 16, 32, 64 or 128, half staged by
 //              each CTA); D = weights x tokens, each CTA's TMEM holding its own
-//              128 weight rows for all N tokens.  The MMA work scales with r,
-//              and the weight rows are the ones the group's main tiles of the
-//              same n-block read, so they come from L2.
+//              128 weight rows for all N tokens.  The MMA work scales with r.
+//              In a group that also has main tiles, the weight rows are the
+//              ones its main tiles of the same n-block read, so they come from
+//              L2; a group of at most 128 rows streams its weights from HBM.
 //
 // A group with 128 < r < 256 rows left over gets one more main tile whose
 // second CTA is only partly used.  Tiles past a group's rows are computed but
@@ -46,10 +47,11 @@ constexpr int BM = 128;  // token (main) or weight (tail) rows per CTA
 constexpr int BN = 256;  // main tile MMA N (weight rows per pair; 128 staged by each CTA)
 constexpr int BK = 64;  // k-block: one 128-byte-wide TMA box, four K = 16 MMAs
 // A ring stage holds KH k-blocks: one wait, 4 * KH MMAs and one commit per
-// stage.  A stage round (producer wait, arm, copies; MMA thread wait, MMAs,
-// commit) carries a fixed cost of the order of 200 ns; with one k-block per
-// stage that cost, not the tensor pipe, set the pace of a 256 x 256 tile
-// (about 84 ns per MMA instead of the 66 ns the pipe needs).
+// stage.  In a stand-alone loop a stage round (producer wait, arm, copies; MMA
+// thread wait, MMAs, commit) cost of the order of 200 ns, enough to hold one
+// k-block per round at about 84 ns per MMA against the 66 ns the tensor pipe
+// needs; here two k-blocks per stage (three stages) shortened FC1 at the
+// default workload by about 2 %.
 constexpr int KH = 2;
 // warps: 0 token producer, 1 TMEM owner + MMA issuer, 2..5 epilogue (TMEM
 // lane quarters warp % 4), 6 weight producer
