@@ -13,10 +13,12 @@
 //        h[p, n0 + r] = bf16(silu(D[64 + r, p]) * D[r, p])
 //   FC2: D[128 x n] = W2 rows c0..c0+127 . h^T,  y[p, c0 + r] = D[r, p] (fp32)
 //
-// The k-loop runs as two half-pipelines over one mbarrier ring: the even
-// k-blocks are loaded by one producer thread and multiplied by one MMA thread
-// into accumulator 0, the odd k-blocks by another pair into accumulator 1; the
-// epilogue adds the two.  (A weight-streaming MMA here has a tiny N, and one
+// The k-loop runs as two half-pipelines: the even k-blocks are loaded by one
+// producer thread and multiplied by one MMA thread into accumulator 0, the odd
+// k-blocks by another pair into accumulator 1; the epilogue adds the two.  Each
+// half owns its own half of the mbarrier ring, so every slot always passes
+// between the same producer and consumer and its phase parity cannot alias
+// whatever the number of k-blocks per tile.  (A weight-streaming MMA here has a tiny N, and one
 // issuing thread starts a new-operand tcgen05.mma only about every 80 ns, which
 // caps one thread near 50 GB/s of weights per SM; two get about twice that.)
 // Two TMEM accumulator pairs alternate between tiles.  The epilogue copies its
