@@ -296,7 +296,7 @@ def run_ours(args, world, rank, local):
     tw = wl.topk_w.to(dev) if wl.topk_w is not None else None
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     opts = dict(decode_chain=True if args.decode_chain else (False if args.decode_separate else None),
-                one_cta_gemm=args.one_cta_gemm)
+                one_cta_gemm=args.one_cta_gemm, fused_gather=args.fused_gather)
     plan = moe.MoEPlan(x, wl.w1, wl.w2, wl.E, wl.top_k, logits=logits, topk_ids=tids, topk_w=tw,
                        local_offset=wl.local_offset, status=status, **opts)
     # a second plan on the same buffers records CUDA events around every stage
@@ -571,6 +571,8 @@ def main():
     ap.add_argument("--decode-separate", action="store_true",
                     help="decode path: always the five separate kernels (comparison)")
     ap.add_argument("--one-cta-gemm", action="store_true", help="grouped path: one-CTA GEMMs (comparison)")
+    ap.add_argument("--fused-gather", action="store_true",
+                    help="grouped path: FC1 copies its token rows from x (no gather kernel)")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--reference-budget", type=float, default=120.0,
                     help="seconds of oracle work for the whole --impl reference run")

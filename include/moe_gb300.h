@@ -160,12 +160,15 @@ MOE_API int moe_fc1_swiglu(const moe_bf16 *xp, const moe_bf16 *w1,
 /* ---- S3 + S4 fused: FC1 + SwiGLU reading its rows through the permutation --------
  * h[p] = bf16_rne(silu(g) * u) for permuted row p < M with the activations
  * taken straight from x: row p is x[perm_to_exp[p] / top_k] (no xp buffer).
- * The producer loads four rows per TMA row-gather.  Same result as
+ * Three gather warps (one per ring slot) copy the rows with 16-byte
+ * cp.async into the swizzled layout of a TMA box.  Bitwise the same result as
  * moe_gather followed by moe_fc1_swiglu, without the [T*top_k, H] buffer of
- * gathered rows, but slower: 32 row-gathers per 128-row k-block cost more
- * than the extra pass (measured 4.2 ms against 1.34 ms + 0.02 ms for the
- * gather at T=4096, H=4096, I=14336, E=8, top-2); moe_forward uses the gather
- * kernel.
+ * gathered rows, but slower: the copies of one slot take longer to land than
+ * the tensor cores take for the other two (FC1 measured 1.95 ms against
+ * 1.26 ms + 0.02 ms for the gather at T=4096, H=4096, I=14336, E=8, top-2,
+ * and 4.63 ms against 3.10 ms + 0.26 ms at T=8192, H=7168, I=2048, E=256,
+ * top-8).  moe_forward uses the gather kernel unless the plan sets
+ * MOE_PLAN_FUSED_GATHER.
  *   x [T, H] bf16, perm_to_exp [T*top_k], m_indptr [L+1], w1 [L, 2I, H],
  *   h [T*top_k, I] bf16.  H % 64 == 0, I % 128 == 0. */
 MOE_API int moe_fc1_swiglu_gathered(const moe_bf16 *x, const int32_t *perm_to_exp,
@@ -258,6 +261,10 @@ MOE_API int moe_forward(const moe_bf16 *x, const float *logits, const int32_t *t
                                    for T*top_k <= 8, where it measured faster) */
 #define MOE_PLAN_DECODE_SEPARATE 8 /* decode path: always the five separate
                                       kernels (sort, gather, FC1, FC2, finalize) */
+#define MOE_PLAN_FUSED_GATHER 16 /* grouped path, CTA-pair GEMMs: FC1 copies its
+                                    token rows straight from x (no gather kernel,
+                                    no permuted copy of x; measured slower, see
+                                    moe_fc1_swiglu_gathered) */
 
 typedef struct moe_forward_desc {
     const moe_bf16 *x;

@@ -412,10 +412,10 @@ int moe_forward_prepare(const moe_forward_desc *desc, moe_plan **plan_out) {
                           p->m_indptr + 1, d.T, p->y, d.status, true);
     } else {
       const bool pair = (d.flags & MOE_PLAN_ONE_CTA_GEMM) == 0;
-      // The gather kernel builds xp: one 128-row TMA box per k-block feeds
-      // the tensor cores, while gathering the rows inside FC1 (four rows per
-      // TMA row-gather, moe_fc1_swiglu_gathered) measured 3x slower for FC1.
-      p->fused_gather = false;
+      // Either the gather kernel builds xp (one 128-row TMA box per k-block
+      // feeds the tensor cores) or FC1's gather warps copy the rows from x.
+      p->fused_gather = pair && (d.flags & MOE_PLAN_FUSED_GATHER) != 0 &&
+                        pair_gemm_supported(Epi::kSwiGLU, d.I);
       if (p->fused_gather)
         rc = gemm_prepare_gather(p->fc1, d.x, d.T, p->p2e, d.top_k, d.w1, d.num_local, d.I, d.H,
                                  p->m_indptr + 1, p->R, p->h, d.status);
@@ -488,11 +488,13 @@ int moe_plan_launch(moe_plan *p, void *stream) {
                   p->sort_ws, d.status, l) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (!mark(kGather)) return MOE_ERR_CUDA;
-  if (!p->fused_gather &&
-      launch_gather(d.x, p->p2e, p->m_indptr + d.num_local, d.H, d.top_k, p->R, p->xp, l) !=
-          cudaSuccess)
-    return MOE_ERR_CUDA;
   const bool dec = p->path == MOE_PATH_DECODE;
+  // grouped path: one warp per token (x read once); decode path: one warp
+  // per route (a handful of tokens would leave most of the GPU idle)
+  if (!p->fused_gather &&
+      (dec ? launch_gather(d.x, p->p2e, p->m_indptr + d.num_local, d.H, d.top_k, p->R, p->xp, l)
+           : launch_gather_tokens(d.x, p->e2p, d.T, d.H, d.top_k, p->R, p->xp, l)) != cudaSuccess)
+    return MOE_ERR_CUDA;
   if (!mark(kFc1)) return MOE_ERR_CUDA;
   if ((dec ? launch_swap(p->fc1d, l) : launch_gemm(p->fc1, l)) != cudaSuccess) return MOE_ERR_CUDA;
   if (!mark(kFc2)) return MOE_ERR_CUDA;

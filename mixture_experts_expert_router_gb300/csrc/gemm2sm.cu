@@ -54,9 +54,12 @@ constexpr int BK = 64;  // k-block: one 128-byte-wide TMA box, four K = 16 MMAs
 // default workload by about 2 %.
 constexpr int KH = 2;
 // warps: 0 token producer, 1 TMEM owner + MMA issuer, 2..5 epilogue (TMEM
-// lane quarters warp % 4), 6 weight producer
+// lane quarters warp % 4), 6 weight producer; in gather mode warps 7..9 copy
+// the token rows (one ring slot each) and warp 0 only drains the ring.
 constexpr int kThreads = 224;
 constexpr int kWeightWarp = 6;
+constexpr int kGatherWarp0 = 7;
+constexpr int kThreadsGather = 320;
 constexpr int A_BYTES = BM * BK * 2;        // one k-block of the M-side operand
 constexpr int B_BYTES = (BN / 2) * BK * 2;  // one k-block of this CTA's half of the N side
 constexpr int A_STAGE = KH * A_BYTES;
@@ -84,8 +87,8 @@ struct PairArgs {
   CUtensorMap map_b;      // weights [G * b_rows, K], box {64, 128}
   CUtensorMap map_w64;    // weights, box {64, 64} (FC1 tail tiles)
   CUtensorMap map_t[4];   // tokens, box {64, 8 / 16 / 32 / 64} (tail tiles, N = 16..128)
-  CUtensorMap map_xg;     // gather mode: token rows of x [x_rows, K], box {64, 1}
   CUtensorMap map_y;      // fp32 output [rows, n_out], box {32, 128}, 128-byte swizzle (TMA stores)
+  const uint16_t *x;      // gather mode: token rows x [x_rows, K]
   const int32_t *p2e;     // gather mode: permuted row -> expanded index
   long x_rows;
   int gather_k;           // gather mode: top_k (token = p2e[row] / top_k); 0 = rows given directly
@@ -165,7 +168,8 @@ __device__ __forceinline__ PairTile decode_pair_tile(int t, const int *tile_star
 // k-block.
 struct PairOperands {
   int tok_row, tok_rows, tmap, w_row, w_row2;
-  uint32_t bytes;
+  uint32_t bytes;    // token + weight box bytes per k-block
+  uint32_t w_bytes;  // weight box bytes per k-block
 };
 
 template <bool SWIGLU>
@@ -180,6 +184,7 @@ __device__ __forceinline__ PairOperands pair_operands(const PairTile &c, uint32_
     else
       o.w_row = c.g * b_rows + c.n * BN + (int)rank * (BN / 2);
     o.bytes = A_BYTES + B_BYTES;
+    o.w_bytes = B_BYTES;
     o.tok_rows = BM;
   } else {
     const int n = tail_n(c.tail);
@@ -192,15 +197,18 @@ __device__ __forceinline__ PairOperands pair_operands(const PairTile &c, uint32_
     }
     o.tok_row = c.gstart + c.mp * 2 * BM + (int)rank * (n / 2);
     o.bytes = A_BYTES + (uint32_t)(n / 2) * BK * 2;
+    o.w_bytes = A_BYTES;
     o.tok_rows = n / 2;
   }
   return o;
 }
 
-template <int EPI>
-__global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_constant__ PairArgs args) {
+template <int EPI, bool GATH>
+__global__ void __launch_bounds__(GATH ? kThreadsGather : kThreads, 1)
+    pair_gemm_kernel(const __grid_constant__ PairArgs args) {
   using Lay = PairLayout<EPI>;
   constexpr int STAGES = Lay::STAGES;
+  static_assert(kThreadsGather / 32 - kGatherWarp0 == STAGES, "one gather warp per ring slot");
   constexpr int BAR_OFF = Lay::BAR_OFF;
   constexpr int MISC_OFF = Lay::MISC_OFF;
   constexpr int SG_OFF = Lay::SG_OFF;
@@ -229,7 +237,8 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 1);
+      // gather mode: the leader's weight arm plus one arrival per CTA's gather warp
+      mbar_init(full_bar(s), GATH ? 3 : 1);
       mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -249,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
     tmem_relinquish_pair();
   }
   pdl_wait();
-  for (int g = threadIdx.x; g < G; g += kThreads) {
+  for (int g = threadIdx.x; g < G; g += (int)blockDim.x) {
     long e = args.group_end[g];
     e = e < 0 ? 0 : (e > args.max_rows ? args.max_rows : e);
     gend[g] = (int)e;
@@ -287,59 +296,40 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
 
   if (warp == 0) {
     // --------------------------------------------------------- token producer --
-    // Lane 0 waits, arms the leader's barrier and loads the token box; in
-    // gather mode every lane loads four token rows of x per k-block instead.
+    // Lane 0 waits, arms the leader's barrier and loads the token box.  In
+    // gather mode the gather warps fill the token boxes and the weight
+    // producer arms; this warp only counts the rounds for the final drain.
     const uint64_t pol_first = policy_evict_first(), pol_last = policy_evict_last();
-    const bool gath = args.gather_k > 0;
-    const int m_total = G > 0 ? gend[G - 1] : 0;
     int it = 0;
     bool ok = true;
     for (int t = cluster; t < total && ok; t += nclusters) {
+      if (GATH) {
+        it += n_rounds;
+        continue;
+      }
       const PairTile c = decode_pair_tile(t, tile_start, gend, G, args.n_tiles, args.m_major);
       const uint64_t pol = (c.tail && c.mp == 0) ? pol_first : pol_last;
       const PairOperands o = pair_operands<kSwiGLU>(c, rank, args.b_rows);
-      // gather mode: this lane's four token rows (rows past the routed ones read row 0)
-      int tr0 = 0, tr1 = 0, tr2 = 0, tr3 = 0;
-      const bool tok_lane = gath && lane < o.tok_rows / 4;
-      if (tok_lane) {
-        const int p0 = o.tok_row + 4 * lane;
-        int tr[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int p = p0 + i;
-          const int tkn = p < m_total ? args.p2e[p] / args.gather_k : 0;
-          tr[i] = (tkn < 0 || tkn >= args.x_rows) ? 0 : tkn;
-        }
-        tr0 = tr[0];
-        tr1 = tr[1];
-        tr2 = tr[2];
-        tr3 = tr[3];
-      }
       const CUtensorMap *tok_map = c.tail ? &args.map_t[o.tmap] : &args.map_a;
       for (int kr = 0; kr < n_rounds; ++kr, ++it) {
         const int s = it % STAGES;
         const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
         const int nk = min(KH, num_kb - kr * KH);
-        int w_ok = 1;
-        if (lane == 0) w_ok = mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, args.status) ? 1 : 0;
-        if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
-          ok = false;
-          break;
-        }
-        const uint32_t leader_full = mapa_shared(full_bar(s), 0);
-        if (lane == 0 && rank == 0) mbar_arrive_expect_tx(full_bar(s), 2 * o.bytes * (uint32_t)nk);
-        __syncwarp();
-        for (int h = 0; h < nk; ++h) {
-          const int kx = (kr * KH + h) * BK;
-          const uint32_t t_dst = smem_base + s * STAGE_BYTES + (c.tail ? A_STAGE + h * B_BYTES : h * A_BYTES);
-          if (gath) {
-            if (tok_lane)
-              tma_gather4_pair(t_dst + lane * 512, &args.map_xg, leader_full, kx, tr0, tr1, tr2, tr3, pol);
-          } else if (lane == 0) {
+        if (lane == 0) {
+          if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, args.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t leader_full = mapa_shared(full_bar(s), 0);
+          if (rank == 0) mbar_arrive_expect_tx(full_bar(s), 2 * o.bytes * (uint32_t)nk);
+          for (int h = 0; h < nk; ++h) {
+            const int kx = (kr * KH + h) * BK;
+            const uint32_t t_dst = smem_base + s * STAGE_BYTES + (c.tail ? A_STAGE + h * B_BYTES : h * A_BYTES);
             tma_load_2d_pair(t_dst, tok_map, leader_full, kx, o.tok_row, pol);
           }
         }
       }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     }
     if (lane == 0 && rank == 0) {  // let both CTAs' last copies land (they all signal the leader)
       for (int j = it > STAGES ? it - STAGES : 0; j < it; ++j)
@@ -368,6 +358,8 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
             break;
           }
           const uint32_t leader_full = mapa_shared(full_bar(s), 0);
+          // gather mode: only the weight boxes are counted as transaction bytes
+          if (GATH && rank == 0) mbar_arrive_expect_tx(full_bar(s), 2 * o.w_bytes * (uint32_t)nk);
           for (int h = 0; h < nk; ++h) {
             const int kx = (kr * KH + h) * BK;
             const uint32_t w_dst = smem_base + s * STAGE_BYTES + (c.tail ? h * A_BYTES : A_STAGE + h * B_BYTES);
@@ -398,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
           const int s = it % STAGES;
           const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
           const int nk = min(KH, num_kb - kr * KH);
-          if (!mbar_wait(full_bar(s), ph, abort_flag, args.status)) {
+          if (!mbar_wait<GATH>(full_bar(s), ph, abort_flag, args.status)) {
             ok = false;
             break;
           }
@@ -577,6 +569,69 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acc ? leader_tempty1 : leader_tempty0);
     }
+  } else if (GATH && warp >= kGatherWarp0) {
+    // -------------------------------------------------------- token row gather --
+    // Gather warp j fills the token boxes of ring slot j only, straight from x:
+    // row q of a box is x[p2e[p] / top_k] for its permuted row p.  Per k-block
+    // lane l copies 16-byte chunk l % 8 of rows l / 8, l / 8 + 4, ... into the
+    // 128-byte-swizzled layout a TMA box has (chunk c of row q at q * 128 +
+    // ((c ^ (q % 8)) * 16)).  Once its copies have landed the warp makes them
+    // visible to the tensor cores and arrives on the leader's full barrier.
+    // (Rows past the last routed row read row 0 of x; their results are
+    // never stored.)
+    const int j = warp - kGatherWarp0;
+    const uint64_t pol = policy_evict_last();  // each token row is read by top_k groups
+    const int m_total = G > 0 ? gend[G - 1] : 0;
+    const int sub = lane >> 3, chunk = lane & 7;
+    const char *xb = reinterpret_cast<const char *>(args.x) + chunk * 16;
+    const long row_bytes = (long)args.K * 2;
+    const uint32_t leader_full = mapa_shared(full_bar(j), 0);
+    int it = 0;
+    bool ok = true;
+    for (int t = cluster; t < total && ok; t += nclusters) {
+      const PairTile c = decode_pair_tile(t, tile_start, gend, G, args.n_tiles, args.m_major);
+      const PairOperands o = pair_operands<kSwiGLU>(c, rank, args.b_rows);
+      const int r4 = o.tok_rows / 4;  // rows per lane: 2 .. 32
+      int tok[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        tok[i] = 0;
+        if (i < r4) {
+          const int p = o.tok_row + sub + 4 * i;
+          const int tk = p < m_total ? args.p2e[p] / args.gather_k : 0;
+          tok[i] = (tk < 0 || tk >= args.x_rows) ? 0 : tk;
+        }
+      }
+      for (int kr = 0; kr < n_rounds; ++kr, ++it) {
+        if (it % STAGES != j) continue;
+        const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+        const int nk = min(KH, num_kb - kr * KH);
+        int w_ok = 1;
+        if (lane == 0) w_ok = mbar_wait(empty_bar(j), ph ^ 1u, abort_flag, args.status) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
+          ok = false;
+          break;
+        }
+        for (int h = 0; h < nk; ++h) {
+          const long kx_bytes = (long)(kr * KH + h) * BK * 2;
+          const uint32_t dst0 = smem_base + j * STAGE_BYTES + (c.tail ? A_STAGE + h * B_BYTES : h * A_BYTES) +
+                                (uint32_t)sub * 128;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            if (i < r4) {
+              // row q = sub + 4 i, so q % 8 = sub + 4 (i % 2)
+              const uint32_t dst = dst0 + (uint32_t)i * 512 + (uint32_t)((chunk ^ (sub + 4 * (i & 1))) << 4);
+              cp_async_16(dst, xb + (long)tok[i] * row_bytes + kx_bytes, pol);
+            }
+          }
+        }
+        cp_async_commit();
+        cp_async_wait_all();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(leader_full);
+      }
+    }
   }
 
   if (EPI == (int)Epi::kF32 && threadIdx.x == 64) bulk_wait_all();  // TMA stores complete
@@ -653,20 +708,19 @@ int pair_gemm_encode_extra(GemmPlan &p, const uint16_t *A, long a_rows, const ui
                            long b_rows_total, int K) {
   int rc = encode(&p.map_w64, B, b_rows_total, K, 64);
   for (int i = 0; i < 4 && rc == MOE_OK; ++i) rc = encode(&p.map_t[i], A, a_rows, K, 8 << i);
-  if (rc == MOE_OK && p.gather_k > 0) rc = encode(&p.map_xg, p.gather_x, p.gather_rows, K, 1);
   if (rc == MOE_OK && p.epi == Epi::kF32) rc = encode_f32_store(&p.map_y, p.out, p.max_rows, p.n_out);
   return rc;
 }
 
 cudaError_t pair_gemm_configure(Epi epi, size_t smem) {
-  if (epi == Epi::kSwiGLU)
-    return cudaFuncSetAttribute(pair_gemm_kernel<(int)Epi::kSwiGLU>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (epi == Epi::kF32)
-    return cudaFuncSetAttribute(pair_gemm_kernel<(int)Epi::kF32>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  return cudaFuncSetAttribute(pair_gemm_kernel<(int)Epi::kBf16>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  constexpr auto kAttr = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  if (epi == Epi::kSwiGLU) {
+    const cudaError_t e = cudaFuncSetAttribute(pair_gemm_kernel<(int)Epi::kSwiGLU, false>, kAttr, (int)smem);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(pair_gemm_kernel<(int)Epi::kSwiGLU, true>, kAttr, (int)smem);
+  }
+  if (epi == Epi::kF32) return cudaFuncSetAttribute(pair_gemm_kernel<(int)Epi::kF32, false>, kAttr, (int)smem);
+  return cudaFuncSetAttribute(pair_gemm_kernel<(int)Epi::kBf16, false>, kAttr, (int)smem);
 }
 
 cudaError_t launch_pair_gemm(const GemmPlan &p, const Launch &l) {
@@ -675,7 +729,7 @@ cudaError_t launch_pair_gemm(const GemmPlan &p, const Launch &l) {
   a.map_b = p.map_b;
   a.map_w64 = p.map_w64;
   for (int i = 0; i < 4; ++i) a.map_t[i] = p.map_t[i];
-  a.map_xg = p.map_xg;
+  a.x = p.gather_x;
   a.map_y = p.map_y;
   a.p2e = p.gather_p2e;
   a.x_rows = p.gather_rows;
@@ -692,7 +746,8 @@ cudaError_t launch_pair_gemm(const GemmPlan &p, const Launch &l) {
   a.m_major = p.m_major;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.grid);
-  cfg.blockDim = dim3(kThreads);
+  const bool gath = p.gather_k > 0 && p.epi == Epi::kSwiGLU;
+  cfg.blockDim = dim3(gath ? kThreadsGather : kThreads);
   cfg.dynamicSmemBytes = p.smem;
   cfg.stream = l.stream;
   cudaLaunchAttribute attr[2];
@@ -704,9 +759,10 @@ cudaError_t launch_pair_gemm(const GemmPlan &p, const Launch &l) {
   attr[1].val.programmaticStreamSerializationAllowed = l.pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  if (p.epi == Epi::kSwiGLU) return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<(int)Epi::kSwiGLU>, a);
-  if (p.epi == Epi::kF32) return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<(int)Epi::kF32>, a);
-  return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<(int)Epi::kBf16>, a);
+  if (gath) return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<(int)Epi::kSwiGLU, true>, a);
+  if (p.epi == Epi::kSwiGLU) return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<(int)Epi::kSwiGLU, false>, a);
+  if (p.epi == Epi::kF32) return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<(int)Epi::kF32, false>, a);
+  return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<(int)Epi::kBf16, false>, a);
 }
 
 }  // namespace moe

@@ -41,6 +41,9 @@ cudaError_t static_sort_scratch(int32_t **out);
 // S3 / S6 -----------------------------------------------------------------------
 cudaError_t launch_gather(const uint16_t *x, const int32_t *p2e, const int32_t *m_total, int H,
                           int k, long max_rows, uint16_t *xp, const Launch &l);
+// The same rows written token by token through exp_to_perm (x read once).
+cudaError_t launch_gather_tokens(const uint16_t *x, const int32_t *e2p, int T, int H, int k,
+                                 long max_rows, uint16_t *xp, const Launch &l);
 cudaError_t launch_finalize(const float *y, const int32_t *e2p, const float *w, int T, int k,
                             int H, uint16_t *out, const Launch &l);
 
@@ -52,7 +55,6 @@ struct GemmPlan {
   CUtensorMap map_b;            // B [G * b_rows, K] bf16, box {64, box_b}
   CUtensorMap map_w64;          // pair kernel: B with box {64, 64} (FC1 tail tiles)
   CUtensorMap map_t[4];         // pair kernel: A with box {64, 8/16/32/64} (tail tiles)
-  CUtensorMap map_xg;           // pair kernel, gather mode: x with box {64, 1}
   CUtensorMap map_y;            // pair kernel, fp32 output: TMA-store map
   const uint16_t *gather_x = nullptr;   // gather mode: rows of A are x[p2e[p] / k]
   const int32_t *gather_p2e = nullptr;

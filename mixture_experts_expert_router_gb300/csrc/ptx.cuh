@@ -50,15 +50,25 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
+  if (kCluster)  // acquire at cluster scope: the phase was completed by the peer CTA's threads
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
   return ok != 0;
 }
 
@@ -66,13 +76,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Gives up (returns false) when *abort becomes non-zero or after
 // kWaitLimitNs; on a timeout it raises MOE_DEV_TIMEOUT and sets *abort.
 // `abort` may be null (the final drains, which must run to the end or the
-// time limit whatever the other roles did).
+// time limit whatever the other roles did).  kCluster: acquire at cluster
+// scope, for phases completed by arrivals of the peer CTA's threads.
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
                                           int32_t *status) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait<kCluster>(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait<kCluster>(bar, parity)) return true;
     if ((it & 63u) == 0u) {
       if (abort != nullptr && *abort) return false;
       if (global_timer_ns() - t0 > kWaitLimitNs) {
@@ -315,18 +327,6 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
-// The same, signalling an mbarrier of either CTA of a pair.
-__device__ __forceinline__ void tma_gather4_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar,
-                                                 int32_t x, int32_t r0, int32_t r1, int32_t r2,
-                                                 int32_t r3, uint64_t cache_policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4.mbarrier::"
-      "complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar),
-      "l"(cache_policy)
-      : "memory");
-}
-
 }  // namespace moe
 
 namespace moe {
@@ -350,5 +350,17 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+
+// ------------------------------------------------- 16-byte asynchronous copies --
+// cp.async (not the bulk copy engine): one 16-byte global -> shared copy per
+// thread, L1 bypassed, with an L2 eviction policy.  Both addresses must be
+// 16-byte aligned.  Completion is per thread: commit, then wait for the group.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint64_t cache_policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst),
+               "l"(src), "l"(cache_policy)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 }  // namespace moe

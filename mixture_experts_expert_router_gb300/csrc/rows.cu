@@ -2,7 +2,9 @@
 // grouped GEMMs.  Both are HBM-bound streams of 16-byte vector accesses.
 //
 // Gather builds the expanded per-route activations (one row per (token, slot)
-// in expert order) that GEMM1 reads.  Finalize is the deterministic combine of
+// in expert order) that GEMM1 reads: either row by row through perm_to_exp
+// (moe_gather, the decode path) or token by token through exp_to_perm, which
+// reads each token row of x once for all its routes (the grouped path).  Finalize is the deterministic combine of
 // flashinfer.fused_moe.cute_dsl_fused_moe_bf16 (Parameters,
 // use_fused_finalize=False): each output row has one owner that sums its
 // top_k unscaled GEMM2 rows, scaled by the routing weights, in fp32 in
@@ -39,6 +41,47 @@ __global__ void __launch_bounds__(256)
       for (int j = 0; j < 8; ++j) __stcs(dst + i + 32 * j, v[j]);
     }
     for (; i < vec; i += 32) __stcs(dst + i, __ldg(src + i));
+  }
+}
+
+// The same copy driven by the tokens: each warp reads one token row of x
+// once and writes it to the permuted rows of all its local routes
+// (exp_to_perm, negative for routes outside the shard).  x is read from HBM
+// once instead of once per route.
+__global__ void __launch_bounds__(256)
+    gather_tokens_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ e2p, int T, int k,
+                         int vec, long max_rows, uint4 *__restrict__ xp) {
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const long warp = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const long nwarps = ((long)gridDim.x * blockDim.x) >> 5;
+  pdl_launch_dependents();
+  for (long t = warp; t < T; t += nwarps) {
+    const int my_p = lane < k ? e2p[t * k + lane] : -1;
+    const uint4 *src = x + t * vec;
+    // warp-uniform loop bounds: every lane reaches each shuffle
+    int b = 0;
+    for (; b + 256 <= vec; b += 256) {
+      uint4 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = __ldg(src + b + lane + 32 * j);
+      for (int s = 0; s < k; ++s) {
+        const int p = __shfl_sync(0xffffffffu, my_p, s);
+        if (p < 0 || p >= max_rows) continue;
+        uint4 *dst = xp + (long)p * vec + b + lane;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) __stcs(dst + 32 * j, v[j]);
+      }
+    }
+    for (; b < vec; b += 32) {
+      const int i = b + lane;
+      const bool in = i < vec;
+      const uint4 v = in ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
+      for (int s = 0; s < k; ++s) {
+        const int p = __shfl_sync(0xffffffffu, my_p, s);
+        if (p >= 0 && p < max_rows && in) __stcs(xp + (long)p * vec + i, v);
+      }
+    }
   }
 }
 
@@ -100,6 +143,17 @@ cudaError_t launch_gather(const uint16_t *x, const int32_t *p2e, const int32_t *
   const int blocks = (int)(want_blocks < cap ? want_blocks : cap);
   return launch_kernel(gather_kernel, dim3(blocks), dim3(256), 0, l,
                        reinterpret_cast<const uint4 *>(x), p2e, m_total, H / 8, k,
+                       reinterpret_cast<uint4 *>(xp));
+}
+
+cudaError_t launch_gather_tokens(const uint16_t *x, const int32_t *e2p, int T, int H, int k,
+                                 long max_rows, uint16_t *xp, const Launch &l) {
+  if (T <= 0) return cudaSuccess;
+  const long want_blocks = ((long)T + 7) / 8;  // 8 warps per block, one token per warp
+  const long cap = (long)device_sm_count() * 8;
+  const int blocks = (int)(want_blocks < cap ? want_blocks : cap);
+  return launch_kernel(gather_tokens_kernel, dim3(blocks), dim3(256), 0, l,
+                       reinterpret_cast<const uint4 *>(x), e2p, T, k, H / 8, max_rows,
                        reinterpret_cast<uint4 *>(xp));
 }
 

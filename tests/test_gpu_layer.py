@@ -41,10 +41,12 @@ def _oracle_out(wl, tokens=None, w1=None, w2=None):
     return out, st
 
 
-def _forward(wl, d, path=moe.PATH_AUTO, status=None, one_cta_gemm=False, decode_chain=False):
+def _forward(wl, d, path=moe.PATH_AUTO, status=None, one_cta_gemm=False, decode_chain=False,
+             fused_gather=False):
     plan = moe.MoEPlan(d["x"], d["w1"], d["w2"], wl.E, wl.top_k, logits=d["logits"],
                        topk_ids=d["topk_ids"], topk_w=d["topk_w"], local_offset=wl.local_offset,
-                       status=status, path=path, one_cta_gemm=one_cta_gemm, decode_chain=decode_chain)
+                       status=status, path=path, one_cta_gemm=one_cta_gemm, decode_chain=decode_chain,
+                       fused_gather=fused_gather)
     out = plan.launch()
     torch.cuda.synchronize()
     return out, plan
@@ -70,15 +72,34 @@ def test_tiny_both_routing_modes(path):
     check_bf16_close(W.bf16_bits(out_r), want, "tiny pre-routed")
 
 
+ODD_SHAPES = [(1, 64, 64, 1, 1), (77, 192, 128, 6, 2), (300, 256, 320, 16, 4),
+              (513, 128, 64, 3, 3), (40, 128, 128, 20, 8), (700, 512, 256, 5, 2)]
+
+
 @pytest.mark.parametrize("one_cta", [False, True])
 @pytest.mark.parametrize("path", PATHS)
-@pytest.mark.parametrize("T,H,I,E,k", [(1, 64, 64, 1, 1), (77, 192, 128, 6, 2), (300, 256, 320, 16, 4),
-                                       (513, 128, 64, 3, 3), (40, 128, 128, 20, 8), (700, 512, 256, 5, 2)])
+@pytest.mark.parametrize("T,H,I,E,k", ODD_SHAPES)
 def test_odd_shapes(path, T, H, I, E, k, one_cta):
     wl = W.make_moe(T=T, H=H, I=I, E=E, top_k=k, mode="logits", seed=T + E)
     out, _ = _forward(wl, _dev(wl), path, one_cta_gemm=one_cta)
     want, _ = _oracle_out(wl)
     check_bf16_end_to_end(W.bf16_bits(out), want, f"T={T} H={H} I={I} E={E} k={k}")
+
+
+@pytest.mark.parametrize("T,H,I,E,k", ODD_SHAPES + [(2000, 320, 384, 7, 2), (1500, 256, 256, 64, 6)])
+def test_fused_gather_matches_gather_kernel(T, H, I, E, k):
+    """FC1 copying its rows from x (gather warps) runs the same MMAs on the
+    same rows as FC1 on the gather kernel's copy: the outputs are bitwise
+    equal, and equal the oracle within the acceptance rule."""
+    wl = W.make_moe(T=T, H=H, I=I, E=E, top_k=k, mode="logits", seed=T + E)
+    d = _dev(wl)
+    out_f, plan_f = _forward(wl, d, moe.PATH_GROUPED, fused_gather=True)
+    out_f = out_f.clone()
+    out_g, _ = _forward(wl, d, moe.PATH_GROUPED)
+    assert int(plan_f.status.item()) == 0
+    assert torch.equal(out_f, out_g), f"fused gather differs: T={T} H={H} I={I} E={E} k={k}"
+    want, _ = _oracle_out(wl)
+    check_bf16_end_to_end(W.bf16_bits(out_f), want, f"fused gather T={T} H={H} I={I} E={E} k={k}")
 
 
 def test_replays_bitwise_identical_and_graph_capture():
@@ -248,12 +269,12 @@ def _sample_tokens(ids, T, n, seed):
     return np.array(sorted(chosen), dtype=np.int32)
 
 
-@pytest.mark.parametrize("one_cta", [False, True])
+@pytest.mark.parametrize("form", ["pair", "one_cta", "fused_gather"])
 @pytest.mark.parametrize("name", ["prefill_few_large", "prefill_many_fine"])
-def test_prefill_configs_sampled(name, one_cta):
+def test_prefill_configs_sampled(name, form):
     wl = W.make_moe(name, weights_device=DEV)
     d = _dev(wl)
-    out, _ = _forward(wl, d, one_cta_gemm=one_cta)
+    out, _ = _forward(wl, d, one_cta_gemm=form == "one_cta", fused_gather=form == "fused_gather")
     ids, _ = _oracle_route(wl)
     tokens = _sample_tokens(ids, wl.T, 1024, 0)
     want, _ = _oracle_out(wl, tokens=tokens, w1=W.bf16_bits(wl.w1), w2=W.bf16_bits(wl.w2))

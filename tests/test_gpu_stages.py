@@ -223,8 +223,9 @@ def test_swapab_fc1_fc2_stage_parity(T, H, I, E, k, max_group):
 @pytest.mark.parametrize("T,H,I,E,k", [(16, 128, 128, 4, 2), (700, 512, 256, 9, 3), (900, 256, 384, 40, 4),
                                        (300, 192, 128, 3, 3), (5, 64, 128, 64, 8)])
 def test_fc1_gathered_stage_parity(T, H, I, E, k):
-    """FC1 taking its rows straight from x through the permutation (TMA row
-    gathers) against the oracle's FC1 on the gathered rows."""
+    """FC1 taking its rows straight from x through the permutation (copied
+    by the gather warps) against the oracle's FC1 on the gathered rows, and
+    bitwise against FC1 on the gathered copy."""
     wl = W.make_moe(T=T, H=H, I=I, E=E, top_k=k, mode="logits", seed=T + 3)
     x, w1 = W.bf16_bits(wl.x), W.bf16_bits(wl.w1)
     ids, _ = oracle.route(wl.logits.numpy(), k)
@@ -239,3 +240,6 @@ def test_fc1_gathered_stage_parity(T, H, I, E, k):
     xp[:len(p2e)] = x[p2e // k]
     h_o = oracle.fc1_swiglu_rows(xp, w1, m[1:], rows)
     check_bf16_close(W.bf16_bits(h_g)[rows], h_o, "h (gathered rows)")
+    h_c = moe.moe_fc1_swiglu(W.from_bf16_bits(xp).to(DEV), wl.w1.to(DEV), torch.from_numpy(m).to(DEV))
+    torch.cuda.synchronize()
+    assert np.array_equal(W.bf16_bits(h_g)[rows], W.bf16_bits(h_c)[rows])
