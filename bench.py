@@ -296,7 +296,8 @@ def run_ours(args, world, rank, local):
     tw = wl.topk_w.to(dev) if wl.topk_w is not None else None
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     opts = dict(decode_chain=True if args.decode_chain else (False if args.decode_separate else None),
-                one_cta_gemm=args.one_cta_gemm, fused_gather=args.fused_gather)
+                one_cta_gemm=args.one_cta_gemm, fused_gather=args.fused_gather,
+                decode_one_launch=args.decode_one_launch)
     plan = moe.MoEPlan(x, wl.w1, wl.w2, wl.E, wl.top_k, logits=logits, topk_ids=tids, topk_w=tw,
                        local_offset=wl.local_offset, status=status, **opts)
     # a second plan on the same buffers records CUDA events around every stage
@@ -568,6 +569,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch the plan directly instead of a CUDA graph")
     ap.add_argument("--decode-chain", action="store_true", help="decode path: always the two-kernel chain")
+    ap.add_argument("--decode-one-launch", action="store_true",
+                    help="decode path: the two-kernel chain as one kernel")
     ap.add_argument("--decode-separate", action="store_true",
                     help="decode path: always the five separate kernels (comparison)")
     ap.add_argument("--one-cta-gemm", action="store_true", help="grouped path: one-CTA GEMMs (comparison)")

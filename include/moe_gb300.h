@@ -265,6 +265,10 @@ MOE_API int moe_forward(const moe_bf16 *x, const float *logits, const int32_t *t
                                     token rows straight from x (no gather kernel,
                                     no permuted copy of x; measured slower, see
                                     moe_fc1_swiglu_gathered) */
+#define MOE_PLAN_DECODE_ONE_LAUNCH 32 /* decode path: the chain's FC1 and FC2 as one
+                                         kernel; CTAs without FC1 work stream their
+                                         W2 tile while FC1 runs and wait (bounded)
+                                         until the FC1 tiles of its expert are done */
 
 typedef struct moe_forward_desc {
     const moe_bf16 *x;

@@ -38,6 +38,7 @@ PLAN_ONE_CTA_GEMM = 2
 PLAN_DECODE_CHAIN = 4
 PLAN_DECODE_SEPARATE = 8
 PLAN_FUSED_GATHER = 16
+PLAN_DECODE_ONE_LAUNCH = 32
 DEV_BAD_EXPERT, DEV_TIMEOUT = 1, 2
 MAX_EXPERTS, MAX_TOP_K = 1024, 16
 
@@ -407,11 +408,12 @@ class MoEPlan:
     def __init__(self, x, w1, w2, num_experts: int, top_k: int, logits=None, topk_ids=None, topk_w=None,
                  local_offset: int = 0, out=None, workspace=None, status=None, path: int = PATH_AUTO,
                  stage_timing: bool = False, one_cta_gemm: bool = False, decode_chain: bool | None = None,
-                 fused_gather: bool = False):
+                 fused_gather: bool = False, decode_one_launch: bool = False):
         """decode_chain: None lets the library choose the decode form (the
         two-kernel chain for very few routes), True forces the chain, False
-        the five separate kernels.  fused_gather: on the grouped path FC1
-        copies its token rows straight from x instead of a gather kernel."""
+        the five separate kernels.  decode_one_launch: the chain's two
+        kernels as one launch.  fused_gather: on the grouped path FC1 copies
+        its token rows straight from x instead of a gather kernel."""
         T, H, I, L, out = _layer_args(x, w1, w2, num_experts, top_k, logits, topk_ids, topk_w,
                                       local_offset, out)
         dev = x.device
@@ -432,7 +434,8 @@ class MoEPlan:
                   flags=(PLAN_STAGE_TIMING if stage_timing else 0) | (PLAN_ONE_CTA_GEMM if one_cta_gemm else 0)
                   | (PLAN_DECODE_CHAIN if decode_chain is True else 0)
                   | (PLAN_DECODE_SEPARATE if decode_chain is False else 0)
-                  | (PLAN_FUSED_GATHER if fused_gather else 0))
+                  | (PLAN_FUSED_GATHER if fused_gather else 0)
+                  | (PLAN_DECODE_ONE_LAUNCH if decode_one_launch else 0))
         handle = ctypes.c_void_p()
         _check(library().moe_forward_prepare(ctypes.byref(d), ctypes.byref(handle)), "moe_forward_prepare")
         self._h = handle

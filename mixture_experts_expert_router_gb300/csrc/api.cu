@@ -46,7 +46,7 @@ int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct WsLayout {
-  size_t ids, w, m_indptr, p2e, e2p, sort_ws, xp, h, y, comb, total;
+  size_t ids, w, m_indptr, p2e, e2p, sort_ws, xp, h, y, comb, done1, total;
 };
 
 WsLayout ws_layout(long T, int H, int I, int k, int L) {
@@ -68,6 +68,7 @@ WsLayout ws_layout(long T, int H, int I, int k, int L) {
   o.h = take(R * (size_t)I * 2);
   o.y = take(R * (size_t)H * 4);
   o.comb = take(chain_comb_ints((int)T, H) * 4);
+  o.done1 = take(((size_t)L + 1) * 4);
   o.total = off;
   return o;
 }
@@ -376,7 +377,7 @@ int moe_forward_prepare(const moe_forward_desc *desc, moe_plan **plan_out) {
     // Decode: the two-kernel chain saves three launches but gathers its token
     // rows and combines inside the GEMM kernels; it is the faster form only for
     // very few routes, so without a flag it runs up to kChainAutoRoutes routes.
-    const bool force_chain = (d.flags & MOE_PLAN_DECODE_CHAIN) != 0;
+    const bool force_chain = (d.flags & (MOE_PLAN_DECODE_CHAIN | MOE_PLAN_DECODE_ONE_LAUNCH)) != 0;
     const bool auto_chain = (d.flags & MOE_PLAN_DECODE_SEPARATE) == 0 && p->R <= kChainAutoRoutes &&
                             d.H % 64 == 0 && d.I % 64 == 0;
     p->use_chain = p->path == MOE_PATH_DECODE && p->R <= kChainMaxRoutes && (force_chain || auto_chain);
@@ -391,6 +392,8 @@ int moe_forward_prepare(const moe_forward_desc *desc, moe_plan **plan_out) {
       c.y = p->y;
       c.out = d.out;
       c.comb = reinterpret_cast<int32_t *>(ws + lay.comb);
+      c.done1 = reinterpret_cast<int32_t *>(ws + lay.done1);
+      c.one_launch = (d.flags & MOE_PLAN_DECODE_ONE_LAUNCH) != 0;
       c.m_indptr = p->m_indptr;
       c.p2e = p->p2e;
       c.e2p = p->e2p;
@@ -474,11 +477,16 @@ int moe_plan_launch(moe_plan *p, void *stream) {
   if (p->logits_mode) {
     if (launch_route(d.logits, d.T, d.E, d.top_k, p->ids, p->w, l) != cudaSuccess) return MOE_ERR_CUDA;
   }
-  if (p->use_chain) {  // sort, gather and finalize run inside the two GEMM kernels
+  if (p->use_chain) {  // sort, gather and finalize run inside the GEMM kernels
     if (!mark(kSort) || !mark(kGather) || !mark(kFc1)) return MOE_ERR_CUDA;
-    if (launch_chain(p->chain, true, l) != cudaSuccess) return MOE_ERR_CUDA;
-    if (!mark(kFc2)) return MOE_ERR_CUDA;
-    if (launch_chain(p->chain, false, l) != cudaSuccess) return MOE_ERR_CUDA;
+    if (p->chain.one_launch) {
+      if (launch_chain(p->chain, 0, l) != cudaSuccess) return MOE_ERR_CUDA;
+      if (!mark(kFc2)) return MOE_ERR_CUDA;
+    } else {
+      if (launch_chain(p->chain, 1, l) != cudaSuccess) return MOE_ERR_CUDA;
+      if (!mark(kFc2)) return MOE_ERR_CUDA;
+      if (launch_chain(p->chain, 2, l) != cudaSuccess) return MOE_ERR_CUDA;
+    }
     if (!mark(kFinalize) || !mark(kNumStages)) return MOE_ERR_CUDA;
     if (ev) ++p->n_recorded;
     return MOE_OK;
@@ -550,7 +558,7 @@ int moe_plan_stage_times(moe_plan *p, float *ms, int max_stages, int *n_launches
 
 int moe_plan_kernels_per_launch(const moe_plan *p) {
   if (!p || p->d.T == 0) return 0;
-  if (p->use_chain) return (p->logits_mode ? 1 : 0) + 2;
+  if (p->use_chain) return (p->logits_mode ? 1 : 0) + (p->chain.one_launch ? 1 : 2);
   int n = p->logits_mode ? 1 : 0;                       // route
   n += p->R <= kSortSingleMax ? 1 : 3;                  // sort
   n += (p->fused_gather ? 0 : 1) + 1 + 1 + 1;           // gather, fc1, fc2, finalize

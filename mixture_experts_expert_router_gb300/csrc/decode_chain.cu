@@ -42,18 +42,24 @@ constexpr int kProd1Warp = 6;
 constexpr int kMma1Warp = 7;
 constexpr int kEpiThreads = 128;
 
+// Kernel modes: the two kernels of the chain, or both phases in one launch.
+constexpr int kModeFc2 = 0, kModeFc1 = 1, kModeBoth = 2;
+
 struct ChainArgs {
-  CUtensorMap map_w;  // FC1: W1 [L*2I, H] box {64, 64};  FC2: W2 [L*H, I] box {64, 128}
-  CUtensorMap map_x;  // FC1: x [T, H] box {64, 1} (row gathers);  FC2: h [R, I] box {64, BNT}
+  CUtensorMap map_w1;  // W1 [L*2I, H] box {64, 64}
+  CUtensorMap map_x;   // x [T, H] box {64, 1} (row gathers)
+  CUtensorMap map_w2;  // W2 [L*H, I] box {64, 128}
+  CUtensorMap map_h;   // h [R, I] box {64, BNT}
   const int32_t *ids;  // [T*k] global expert ids
   const float *w;      // [T*k] routing weights
   uint16_t *h;         // [R, I] bf16: FC1 writes, FC2 reads
   float *y;            // [R, H] fp32: FC2
   uint16_t *out;       // [T, H] bf16: FC2
   int32_t *comb;       // [T * m_tiles2] combine counters
-  int32_t *m_indptr_out, *p2e_out, *e2p_out;  // published by FC1's first CTA
+  int32_t *done1;      // one launch: [L] finished FC1 tiles per expert, then the exit counter
+  int32_t *m_indptr_out, *p2e_out, *e2p_out;  // published by the first CTA of FC1
   int32_t *status;
-  int T, k, E, off, L, K, n_out, w_rows, m_tiles, m_tiles2, ids_early;
+  int T, k, E, off, L, H, I, m_tiles1, m_tiles2, ids_early;
 };
 
 template <int BNT>
@@ -165,23 +171,33 @@ __device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {
       : "r"(taddr));
 }
 
-__device__ __forceinline__ Tile decode_tile(int t, const int *tile_start, int L, int m_tiles) {
+// Tile t of a list with m_tiles weight tiles per row block of each expert:
+// nbp is the prefix of the experts' row-block counts; tiles run expert by
+// expert, then weight tile, then row block.
+__device__ __forceinline__ Tile decode_tile(int t, const int *nbp, int L, int m_tiles) {
   int lo = 0, hi = L;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (tile_start[mid] <= t) lo = mid;
+    if (m_tiles * nbp[mid] <= t) lo = mid;
     else hi = mid;
   }
   Tile c;
   c.g = lo;
-  const int local = t - tile_start[lo];
-  const int nt = (tile_start[lo + 1] - tile_start[lo]) / m_tiles;
+  const int local = t - m_tiles * nbp[lo];
+  const int nt = nbp[lo + 1] - nbp[lo];
   c.m = local / nt;
   c.n = local - c.m * nt;
   return c;
 }
 
-template <int BNT, bool FC1>
+// One work item: a weight tile (128 weight rows) times a block of BNT
+// permuted rows of one expert, from FC1 or from FC2.
+struct Item {
+  bool fc1;
+  Tile c;
+};
+
+template <int BNT, int MODE>
 __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constant__ ChainArgs a) {
   using C = ChainCfg<BNT>;
   extern __shared__ unsigned char smem_raw[];
@@ -197,13 +213,14 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
   volatile int *bad = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 8);
+  volatile int *last_cta = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 12);
   float *sg = reinterpret_cast<float *>(smem + C::SG_OFF);
   int *sflag = reinterpret_cast<int *>(smem + C::SG_OFF);  // FC2: last-arriver tokens [BNT]
   const int L = a.L, T = a.T, R = a.T * a.k;
   int *m_indptr = reinterpret_cast<int *>(smem + C::TAB_OFF);
   int *next = m_indptr + (L + 1);
-  int *tile_start = next + (L + 1);
-  int *p2e = tile_start + (L + 1);
+  int *nbp = next + (L + 1);  // prefix of the experts' row blocks ceil(rows / BNT)
+  int *p2e = nbp + (L + 1);
   int *e2p = p2e + R;
   int *tok_n = e2p + R;
 
@@ -224,8 +241,14 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&a.map_w);
-    tma_prefetch_desc(&a.map_x);
+    if (MODE != kModeFc2) {
+      tma_prefetch_desc(&a.map_w1);
+      tma_prefetch_desc(&a.map_x);
+    }
+    if (MODE != kModeFc1) {
+      tma_prefetch_desc(&a.map_w2);
+      tma_prefetch_desc(&a.map_h);
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
@@ -234,30 +257,27 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
   if (!a.ids_early) pdl_wait();  // the routing kernel wrote ids and weights
 
   cta_sort(a.ids, R, a.E, a.off, L, m_indptr, next, p2e, e2p, bad);
-  if (!FC1) {
+  if (MODE != kModeFc1) {
     for (int t = threadIdx.x; t < T; t += kThreads) {
       int n = 0;
       for (int j = 0; j < a.k; ++j) n += e2p[t * a.k + j] >= 0;
       tok_n[t] = n;
     }
   }
-  if (warp == 0) {  // tiles: per non-empty expert, m_tiles x ceil(cnt / BNT)
+  if (warp == 0) {  // row blocks per non-empty expert: ceil(cnt / BNT)
     int carry = 0;
-    if (lane == 0) tile_start[0] = 0;
+    if (lane == 0) nbp[0] = 0;
     for (int base = 0; base < L; base += 32) {
       const int g = base + lane;
-      int nt = 0;
-      if (g < L) {
-        const int cnt = m_indptr[g + 1] - m_indptr[g];
-        nt = cnt > 0 ? ((cnt + BNT - 1) / BNT) * a.m_tiles : 0;
-      }
-      int inc = nt;
+      int nb = 0;
+      if (g < L) nb = (m_indptr[g + 1] - m_indptr[g] + BNT - 1) / BNT;
+      int inc = nb;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_up_sync(0xffffffffu, inc, o);
         if (lane >= o) inc += y;
       }
-      if (g < L) tile_start[g + 1] = carry + inc;
+      if (g < L) nbp[g + 1] = carry + inc;
       carry += __shfl_sync(0xffffffffu, inc, 31);
     }
   }
@@ -267,48 +287,71 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
   pdl_launch_dependents();
 
   const uint32_t tmem_base = *tmem_holder;
-  const int total = tile_start[L];
-  const int num_kb = a.K / BK;
+  // FC1 tiles: I / 64 weight tiles (64 up + 64 gate rows) per row block; FC2
+  // tiles: H / 128 weight tiles per row block.  In one launch the FC1 items
+  // come first, so a CTA finishes all its FC1 items before its first FC2 item.
+  const int total1 = MODE == kModeFc2 ? 0 : a.m_tiles1 * nbp[L];
+  const int total2 = MODE == kModeFc1 ? 0 : a.m_tiles2 * nbp[L];
+  const int total = total1 + total2;
+  auto item = [&](int w) {
+    Item it;
+    it.fc1 = w < total1;
+    it.c = it.fc1 ? decode_tile(w, nbp, L, a.m_tiles1) : decode_tile(w - total1, nbp, L, a.m_tiles2);
+    return it;
+  };
   // Each half-pipeline owns half of the ring (slots q * HS .. q * HS + HS - 1),
   // so a slot is only ever filled and drained by one producer / MMA pair and
   // every wait on it is for the phase right after the one it last saw.
   constexpr int HS = C::STAGES / 2;
-  const int rows_per_box = FC1 ? 64 : 128;
   const int M = m_indptr[L];
 
   if ((warp == 0 || warp == kProd1Warp)) {
     // --------------------------------------------------------------- producers --
     // Producer q (warp 0: q = 0, warp 6: q = 1) loads the k-blocks kb % 2 == q
-    // of every tile; FC1's token rows come from the lanes, four rows each.
+    // of every item; FC1's token rows come from the lanes, four rows each.
+    // FC2's h rows are written by FC1: by the previous kernel of the chain
+    // (programmatic dependent launch) or, in one launch, by other CTAs, which
+    // count each finished FC1 tile per expert.  Until they are there the
+    // weight boxes go out and the h boxes are listed, then loaded once h is
+    // ready; a producer never waits on a slot that holds a listed box.
     const int q = warp == 0 ? 0 : 1;
     const uint64_t pol_w = policy_evict_first();  // each weight byte is read once
     const uint64_t pol_x = policy_evict_last();
     int iq = 0;  // this pipeline's k-blocks so far: its private ring slots q * HS + iq % HS
     bool ok = true;
-    // FC2 in early mode: the h boxes of the first tile's k-blocks that went out
-    // before FC1 had finished, listed here and loaded once it has.  Every
-    // producer flushes its list before its first wait on a ring slot.
-    int pend_s[C::STAGES], pend_kb[C::STAGES];
+    int pend_s[HS], pend_kb[HS];
     int n_pend = 0;
-    bool waited = FC1;  // FC1 reads only inputs: it never waits here
-    int first_xrow = 0;
-    auto finish_wait = [&]() {
-      pdl_wait();
-      waited = true;
-      if (lane == 0)
-        for (int j = 0; j < n_pend; ++j)
-          tma_load_2d(smem_base + pend_s[j] * C::STAGE_BYTES + C::A_BYTES, &a.map_x, full_bar(pend_s[j]),
-                      pend_kb[j] * BK, first_xrow, pol_x);
-      n_pend = 0;
-    };
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      if (!waited && t != (int)blockIdx.x) finish_wait();
-      const Tile c = decode_tile(t, tile_start, L, a.m_tiles);
-      const int wrow = c.g * a.w_rows + c.m * rows_per_box;
+    bool pdl_done = false;
+    for (int wi = blockIdx.x; wi < total && ok; wi += gridDim.x) {
+      const Item it = item(wi);
+      const Tile c = it.c;
+      const int num_kb = (it.fc1 ? a.H : a.I) / BK;
+      const int wrow = it.fc1 ? c.g * 2 * a.I + c.m * 64 : c.g * a.H + c.m * 128;
       const int xrow = m_indptr[c.g] + c.n * BNT;
-      if (t == (int)blockIdx.x) first_xrow = xrow;
+      // h of this item may be loaded: always for FC1; for FC2 once the chain's
+      // first kernel has finished, or in one launch once every FC1 tile of the
+      // expert has
+      bool dep_ok = it.fc1 || (MODE == kModeFc2 && pdl_done);
+      const int need = a.m_tiles1 * (nbp[c.g + 1] - nbp[c.g]);
+      auto finish = [&]() {
+        pdl_wait();
+        pdl_done = true;
+        int w_ok = 1;
+        if (MODE == kModeBoth && lane == 0)
+          w_ok = counter_wait(a.done1 + c.g, need, abort_flag, a.status) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, w_ok, 0)) ok = false;
+        if (MODE == kModeBoth) fence_proxy_async_global();
+        // the listed boxes go out even after a failed wait (their reads stay in
+        // bounds), so that every armed slot completes and the drain below ends
+        if (lane == 0)
+          for (int j = 0; j < n_pend; ++j)
+            tma_load_2d(smem_base + pend_s[j] * C::STAGE_BYTES + C::A_BYTES, &a.map_h, full_bar(pend_s[j]),
+                        pend_kb[j] * BK, xrow, pol_x);
+        n_pend = 0;
+        dep_ok = true;
+      };
       int tr0 = 0, tr1 = 0, tr2 = 0, tr3 = 0;  // FC1: this lane's four token rows of x
-      const bool tok_lane = FC1 && lane < BNT / 4;
+      const bool tok_lane = it.fc1 && lane < BNT / 4;
       if (tok_lane) {
         int tr[4];
 #pragma unroll
@@ -321,12 +364,15 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         tr2 = tr[2];
         tr3 = tr[3];
       }
-      for (int kb = 0; kb < num_kb; ++kb) {
+      for (int kb = 0; kb < num_kb && ok; ++kb) {
         if ((kb & 1) != q) continue;
+        if (!dep_ok && n_pend == HS) {  // the next slot holds a listed box
+          finish();
+          if (!ok) break;
+        }
         const int s = q * HS + iq % HS;
         const uint32_t ph = (uint32_t)(iq / HS) & 1u;
         ++iq;
-        if (!waited && iq > HS) finish_wait();
         int w_ok = 1;
         if (lane == 0) w_ok = mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, a.status) ? 1 : 0;
         if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
@@ -336,39 +382,40 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         const uint32_t a_dst = smem_base + s * C::STAGE_BYTES;
         if (lane == 0) {
           mbar_arrive_expect_tx(full_bar(s), C::STAGE_BYTES);
-          if (FC1) {
-            tma_load_2d(a_dst, &a.map_w, full_bar(s), kb * BK, wrow, pol_w);
-            tma_load_2d(a_dst + 64 * 128, &a.map_w, full_bar(s), kb * BK, wrow + a.w_rows / 2, pol_w);
+          if (it.fc1) {
+            tma_load_2d(a_dst, &a.map_w1, full_bar(s), kb * BK, wrow, pol_w);
+            tma_load_2d(a_dst + 64 * 128, &a.map_w1, full_bar(s), kb * BK, wrow + a.I, pol_w);
           } else {
-            tma_load_2d(a_dst, &a.map_w, full_bar(s), kb * BK, wrow, pol_w);
+            tma_load_2d(a_dst, &a.map_w2, full_bar(s), kb * BK, wrow, pol_w);
           }
         }
         __syncwarp();
-        if (FC1) {
+        if (it.fc1) {
           if (tok_lane)
             tma_gather4(a_dst + C::A_BYTES + lane * 512, &a.map_x, full_bar(s), kb * BK, tr0, tr1, tr2,
                         tr3, pol_x);
-        } else if (waited) {
-          if (lane == 0) tma_load_2d(a_dst + C::A_BYTES, &a.map_x, full_bar(s), kb * BK, xrow, pol_x);
+        } else if (dep_ok) {
+          if (lane == 0) tma_load_2d(a_dst + C::A_BYTES, &a.map_h, full_bar(s), kb * BK, xrow, pol_x);
         } else {
           pend_s[n_pend] = s;
           pend_kb[n_pend] = kb;
           ++n_pend;
         }
       }
+      if (ok && !dep_ok) finish();
     }
-    if (!waited) finish_wait();
     if (lane == 0)  // let this pipeline's last copies land
       for (int j = iq > HS ? iq - HS : 0; j < iq; ++j)
         mbar_wait(full_bar(q * HS + j % HS), (uint32_t)(j / HS) & 1u, nullptr, a.status);
   } else if ((warp == 1 || warp == kMma1Warp) && lane == 0) {
     // ------------------------------------------------------------- MMA issuers --
     // Issuer q multiplies the k-blocks kb % 2 == q into accumulator q of the
-    // tile's buffer; both commit every tile.
+    // item's buffer; both commit every item.
     const int q = warp == 1 ? 0 : 1;
     int iq = 0, tc = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tc) {
+    for (int wi = blockIdx.x; wi < total && ok; wi += gridDim.x, ++tc) {
+      const int num_kb = (wi < total1 ? a.H : a.I) / BK;
       const int acc = tc & 1;
       const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
       if (!mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag, a.status)) break;
@@ -405,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
     const int r = quarter * 32 + lane;  // weight row inside the tile (TMEM lane)
     const int etid = threadIdx.x - 64;  // 0..127
     if (blockIdx.x == 0) {
-      if (FC1) {
+      if (MODE != kModeFc2) {
         if (etid == 0 && a.status) {
           *reinterpret_cast<volatile int32_t *>(a.status) = 0;
           if (*bad) atomicOr(reinterpret_cast<unsigned int *>(a.status), MOE_DEV_BAD_EXPERT);
@@ -415,18 +462,24 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
           a.e2p_out[x] = e2p[x];
           if (x < M) a.p2e_out[x] = p2e[x];
         }
-        for (int x = etid; x < T * a.m_tiles2; x += kEpiThreads) a.comb[x] = 0;
-      } else {  // tokens with no local route: their output row is zero
+        // the chain's second kernel counts from zero (one launch resets its
+        // counters when it ends instead)
+        if (MODE == kModeFc1)
+          for (int x = etid; x < T * a.m_tiles2; x += kEpiThreads) a.comb[x] = 0;
+      }
+      if (MODE != kModeFc1) {  // tokens with no local route: their output row is zero
         for (int t = 0; t < T; ++t)
           if (tok_n[t] == 0)
-            for (int x = etid; x < a.n_out; x += kEpiThreads) a.out[(long)t * a.n_out + x] = 0;
+            for (int x = etid; x < a.H; x += kEpiThreads) a.out[(long)t * a.H + x] = 0;
       }
     }
     int tc = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x, ++tc) {
-      const Tile c = decode_tile(t, tile_start, L, a.m_tiles);
+    for (int wi = blockIdx.x; wi < total; wi += gridDim.x, ++tc) {
+      const Item it = item(wi);
+      const Tile c = it.c;
+      const int num_kb = (it.fc1 ? a.H : a.I) / BK;
       const int xrow = m_indptr[c.g] + c.n * BNT;
-      const int valid = m_indptr[c.g + 1] - xrow;  // tokens of this tile (> 0)
+      const int valid = m_indptr[c.g + 1] - xrow;  // rows of this item (> 0)
       const int acc = tc & 1;
       const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
       const bool got = mbar_wait(tfull_bar(acc), aph, abort_flag, a.status);
@@ -436,23 +489,23 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
       const uint32_t lane_addr = tmem_base + ((uint32_t)(quarter * 32) << 16);
 #pragma unroll
       for (int c0 = 0; c0 < BNT; c0 += 16) {
-        uint32_t q[16];
-        tmem_ld_x16(lane_addr + (uint32_t)(2 * acc * BNT + c0), q);
+        uint32_t qv[16];
+        tmem_ld_x16(lane_addr + (uint32_t)(2 * acc * BNT + c0), qv);
         if (num_kb > 1) {  // the odd k-blocks' accumulator
           uint32_t q1[16];
           tmem_ld_x16(lane_addr + (uint32_t)((2 * acc + 1) * BNT + c0), q1);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            q[i] = __float_as_uint(__fadd_rn(__uint_as_float(q[i]), __uint_as_float(q1[i])));
+            qv[i] = __float_as_uint(__fadd_rn(__uint_as_float(qv[i]), __uint_as_float(q1[i])));
         }
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[c0 + i] = __uint_as_float(q[i]);
+        for (int i = 0; i < 16; ++i) v[c0 + i] = __uint_as_float(qv[i]);
       }
       tc_fence_before();
       mbar_arrive(tempty_bar(acc));
-      if (FC1) {
+      if (it.fc1) {
         if (r >= 64) {
 #pragma unroll
           for (int j = 0; j < BNT; ++j) sg[j * 64 + (r - 64)] = v[j];
@@ -464,15 +517,17 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
 #pragma unroll
           for (int j = 0; j < BNT; ++j)
             if (j < valid)
-              h[(long)(xrow + j) * a.n_out + col] = __float2bfloat16_rn(silu_f32(sg[j * 64 + r]) * v[j]);
+              h[(long)(xrow + j) * a.I + col] = __float2bfloat16_rn(silu_f32(sg[j * 64 + r]) * v[j]);
         }
+        if (MODE == kModeBoth) __threadfence();  // h before the expert's count
         epi_bar();
+        if (MODE == kModeBoth && etid == 0) atomicAdd(a.done1 + c.g, 1);
       } else {
         const int col = c.m * 128 + r;
-        if (col < a.n_out) {
+        if (col < a.H) {
 #pragma unroll
           for (int j = 0; j < BNT; ++j)
-            if (j < valid) a.y[(long)(xrow + j) * a.n_out + col] = v[j];
+            if (j < valid) a.y[(long)(xrow + j) * a.H + col] = v[j];
         }
         __threadfence();
         epi_bar();
@@ -491,14 +546,14 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
 #pragma unroll 1
         for (int j = 0; j < BNT && j < valid; ++j) {
           const int tkn = sflag[j];
-          if (tkn < 0 || col >= a.n_out) continue;
+          if (tkn < 0 || col >= a.H) continue;
           float sum = 0.f;
           for (int s = 0; s < a.k; ++s) {
             const int pp = e2p[tkn * a.k + s];
             if (pp < 0) continue;
-            sum = __fadd_rn(sum, __fmul_rn(a.w[tkn * a.k + s], __ldcg(a.y + (long)pp * a.n_out + col)));
+            sum = __fadd_rn(sum, __fmul_rn(a.w[tkn * a.k + s], __ldcg(a.y + (long)pp * a.H + col)));
           }
-          reinterpret_cast<__nv_bfloat16 *>(a.out)[(long)tkn * a.n_out + col] = __float2bfloat16_rn(sum);
+          reinterpret_cast<__nv_bfloat16 *>(a.out)[(long)tkn * a.H + col] = __float2bfloat16_rn(sum);
         }
         epi_bar();
       }
@@ -506,6 +561,22 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
   }
 
   __syncthreads();
+  if (MODE == kModeBoth) {
+    // The last CTA to get here resets the counters for the next launch: every
+    // other CTA has finished with them.
+    if (threadIdx.x == 0) {
+      __threadfence();
+      *last_cta = atomicAdd(a.done1 + L, 1) == (int)gridDim.x - 1 ? 1 : 0;
+    }
+    __syncthreads();
+    if (*last_cta) {
+      __threadfence();
+      for (int g = threadIdx.x; g < L; g += kThreads)
+        if (m_indptr[g + 1] > m_indptr[g]) a.done1[g] = 0;
+      for (int x = threadIdx.x; x < T * a.m_tiles2; x += kThreads) a.comb[x] = 0;
+      if (threadIdx.x == 0) a.done1[L] = 0;
+    }
+  }
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -540,23 +611,29 @@ int encode(CUtensorMap *map, const void *ptr, long rows, int K, int box_rows) {
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_TENSOR_MAP;
 }
 
-template <int BNT, bool FC1>
+template <int BNT>
 cudaError_t configure(size_t smem) {
-  return cudaFuncSetAttribute(chain_kernel<BNT, FC1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)smem);
+  constexpr auto kAttr = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  cudaError_t e = cudaFuncSetAttribute(chain_kernel<BNT, kModeFc1>, kAttr, (int)smem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(chain_kernel<BNT, kModeFc2>, kAttr, (int)smem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(chain_kernel<BNT, kModeBoth>, kAttr, (int)smem);
+  return e;
 }
 
-template <int BNT, bool FC1>
+template <int BNT, int MODE>
 cudaError_t launch_inst(const ChainPlan &p, const Launch &l) {
   ChainArgs a;
-  a.map_w = FC1 ? p.map_w1 : p.map_w2;
-  a.map_x = FC1 ? p.map_x : p.map_h;
+  a.map_w1 = p.map_w1;
+  a.map_x = p.map_x;
+  a.map_w2 = p.map_w2;
+  a.map_h = p.map_h;
   a.ids = p.ids;
   a.w = p.w;
   a.h = p.h;
   a.y = p.y;
   a.out = p.out;
   a.comb = p.comb;
+  a.done1 = p.done1;
   a.m_indptr_out = p.m_indptr;
   a.p2e_out = p.p2e;
   a.e2p_out = p.e2p;
@@ -566,14 +643,20 @@ cudaError_t launch_inst(const ChainPlan &p, const Launch &l) {
   a.E = p.E;
   a.off = p.off;
   a.L = p.L;
-  a.K = FC1 ? p.H : p.I;
-  a.n_out = FC1 ? p.I : p.H;
-  a.w_rows = FC1 ? 2 * p.I : p.H;
-  a.m_tiles = FC1 ? p.I / 64 : (p.H + 127) / 128;
+  a.H = p.H;
+  a.I = p.I;
+  a.m_tiles1 = p.I / 64;
   a.m_tiles2 = (p.H + 127) / 128;
   a.ids_early = p.ids_early && l.pdl ? 1 : 0;
-  return launch_kernel(chain_kernel<BNT, FC1>, dim3(FC1 ? p.grid1 : p.grid2), dim3(kThreads),
-                       p.smem, l, a);
+  const int grid = MODE == kModeFc1 ? p.grid1 : (MODE == kModeFc2 ? p.grid2 : p.grid_one);
+  return launch_kernel(chain_kernel<BNT, MODE>, dim3(grid), dim3(kThreads), p.smem, l, a);
+}
+
+template <int BNT>
+cudaError_t launch_bnt(const ChainPlan &p, int part, const Launch &l) {
+  if (part == 1) return launch_inst<BNT, kModeFc1>(p, l);
+  if (part == 2) return launch_inst<BNT, kModeFc2>(p, l);
+  return launch_inst<BNT, kModeBoth>(p, l);
 }
 
 }  // namespace
@@ -599,21 +682,21 @@ int chain_prepare(ChainPlan &p) {
   const long t2 = (long)((p.H + 127) / 128) * ((R + p.bnt - 1) / p.bnt + groups);
   p.grid1 = (int)(t1 < sms ? t1 : sms);
   p.grid2 = (int)(t2 < sms ? t2 : sms);
-  cudaError_t e;
-  if (p.bnt == 16) {
-    if ((e = configure<16, true>(p.smem)) == cudaSuccess) e = configure<16, false>(p.smem);
-  } else if (p.bnt == 32) {
-    if ((e = configure<32, true>(p.smem)) == cudaSuccess) e = configure<32, false>(p.smem);
-  } else {
-    if ((e = configure<64, true>(p.smem)) == cudaSuccess) e = configure<64, false>(p.smem);
-  }
+  // one launch: at most one CTA per SM (each takes most of an SM's shared
+  // memory), so every CTA whose FC1 tiles others wait for gets an SM
+  p.grid_one = (int)(t1 + t2 < sms ? t1 + t2 : sms);
+  cudaError_t e = p.bnt == 16 ? configure<16>(p.smem) : (p.bnt == 32 ? configure<32>(p.smem) : configure<64>(p.smem));
+  if (e == cudaSuccess && p.one_launch && p.done1)  // the counters start from zero
+    e = cudaMemset(p.done1, 0, ((size_t)p.L + 1) * sizeof(int32_t));
+  if (e == cudaSuccess && p.one_launch && p.comb) e = cudaMemset(p.comb, 0, chain_comb_ints(p.T, p.H) * 4);
+  if (e == cudaSuccess && p.one_launch) e = cudaDeviceSynchronize();
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
-cudaError_t launch_chain(const ChainPlan &p, bool fc1, const Launch &l) {
-  if (p.bnt == 16) return fc1 ? launch_inst<16, true>(p, l) : launch_inst<16, false>(p, l);
-  if (p.bnt == 32) return fc1 ? launch_inst<32, true>(p, l) : launch_inst<32, false>(p, l);
-  return fc1 ? launch_inst<64, true>(p, l) : launch_inst<64, false>(p, l);
+cudaError_t launch_chain(const ChainPlan &p, int part, const Launch &l) {
+  if (p.bnt == 16) return launch_bnt<16>(p, part, l);
+  if (p.bnt == 32) return launch_bnt<32>(p, part, l);
+  return launch_bnt<64>(p, part, l);
 }
 
 }  // namespace moe

@@ -131,12 +131,15 @@ struct ChainPlan {
   uint16_t *h = nullptr, *out = nullptr;
   float *y = nullptr;
   int32_t *comb = nullptr, *m_indptr = nullptr, *p2e = nullptr, *e2p = nullptr, *status = nullptr;
-  int T = 0, k = 0, E = 0, off = 0, L = 0, H = 0, I = 0, bnt = 0, grid1 = 0, grid2 = 0;
+  int32_t *done1 = nullptr;  // one launch: [L + 1] FC1 tile counts per expert, exit counter
+  int T = 0, k = 0, E = 0, off = 0, L = 0, H = 0, I = 0, bnt = 0, grid1 = 0, grid2 = 0, grid_one = 0;
   bool ids_early = false;  // ids are layer inputs (pre-routed), not the routing kernel's output
+  bool one_launch = false; // FC1 and FC2 in one kernel (CTAs wait for the FC1 tiles of an expert)
   size_t smem = 0;
 };
 size_t chain_comb_ints(int T, int H);
 int chain_prepare(ChainPlan &p);
-cudaError_t launch_chain(const ChainPlan &p, bool fc1, const Launch &l);
+// part 1: FC1 kernel, 2: FC2 kernel, 0: both phases in one kernel
+cudaError_t launch_chain(const ChainPlan &p, int part, const Launch &l);
 
 }  // namespace moe

@@ -351,6 +351,39 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Order this thread's generic view of global memory (data another CTA wrote
+// and released) before its later async-proxy (TMA) reads.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int *p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Wait until *counter >= need (another CTA of this grid counts up and
+// releases).  Bounded like mbar_wait: gives up when *abort becomes non-zero or
+// after kWaitLimitNs, raising MOE_DEV_TIMEOUT and setting *abort.
+__device__ __forceinline__ bool counter_wait(const int *counter, int need, volatile int *abort,
+                                             int32_t *status) {
+  if (ld_acquire_gpu(counter) >= need) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(32);
+    if (ld_acquire_gpu(counter) >= need) return true;
+    if ((it & 15u) == 0u) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        *abort = 1;
+        if (status) atomicOr(reinterpret_cast<unsigned int *>(status), MOE_DEV_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
 // ------------------------------------------------- 16-byte asynchronous copies --
 // cp.async (not the bulk copy engine): one 16-byte global -> shared copy per
 // thread, L1 bypassed, with an L2 eviction policy.  Both addresses must be

@@ -98,7 +98,8 @@ def test_binding_constants_match_header():
     pairs = {"MOE_PATH_AUTO": moe.PATH_AUTO, "MOE_PATH_GROUPED": moe.PATH_GROUPED,
              "MOE_PATH_DECODE": moe.PATH_DECODE, "MOE_PLAN_STAGE_TIMING": moe.PLAN_STAGE_TIMING,
              "MOE_PLAN_ONE_CTA_GEMM": moe.PLAN_ONE_CTA_GEMM, "MOE_PLAN_DECODE_CHAIN": moe.PLAN_DECODE_CHAIN,
-             "MOE_PLAN_DECODE_SEPARATE": moe.PLAN_DECODE_SEPARATE,
+             "MOE_PLAN_DECODE_SEPARATE": moe.PLAN_DECODE_SEPARATE, "MOE_PLAN_FUSED_GATHER": moe.PLAN_FUSED_GATHER,
+             "MOE_PLAN_DECODE_ONE_LAUNCH": moe.PLAN_DECODE_ONE_LAUNCH,
              "MOE_DEV_BAD_EXPERT": moe.DEV_BAD_EXPERT, "MOE_DEV_TIMEOUT": moe.DEV_TIMEOUT}
     for name, value in pairs.items():
         assert defines.get(name) == value, name

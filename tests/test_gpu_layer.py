@@ -42,11 +42,11 @@ def _oracle_out(wl, tokens=None, w1=None, w2=None):
 
 
 def _forward(wl, d, path=moe.PATH_AUTO, status=None, one_cta_gemm=False, decode_chain=False,
-             fused_gather=False):
+             fused_gather=False, one_launch=False):
     plan = moe.MoEPlan(d["x"], d["w1"], d["w2"], wl.E, wl.top_k, logits=d["logits"],
                        topk_ids=d["topk_ids"], topk_w=d["topk_w"], local_offset=wl.local_offset,
                        status=status, path=path, one_cta_gemm=one_cta_gemm, decode_chain=decode_chain,
-                       fused_gather=fused_gather)
+                       fused_gather=fused_gather, decode_one_launch=one_launch)
     out = plan.launch()
     torch.cuda.synchronize()
     return out, plan
@@ -218,12 +218,13 @@ def test_all_tokens_on_one_expert():
 
 # ---------------------------------------------------------- workload shapes --
 
-@pytest.mark.parametrize("chain", [False, True, None])
+@pytest.mark.parametrize("chain", [False, True, None, "one_launch"])
 @pytest.mark.parametrize("name", ["decode_t1", "decode_t8", "decode_t64"])
 @pytest.mark.parametrize("path", PATHS)
 def test_decode_configs_full(name, path, chain):
     wl = W.make_moe(name)
-    out, _ = _forward(wl, _dev(wl), path, decode_chain=chain)
+    one = chain == "one_launch"
+    out, _ = _forward(wl, _dev(wl), path, decode_chain=True if one else chain, one_launch=one)
     want, _ = _oracle_out(wl)
     check_bf16_end_to_end(W.bf16_bits(out), want, name)
 
@@ -242,13 +243,15 @@ def test_decode_form_chosen_by_route_count(T, kernels):
 @pytest.mark.parametrize("T,H,I,E,k,mode", [(3, 64, 192, 8, 2, "prerouted"), (5, 192, 64, 6, 3, "logits"),
                                              (40, 128, 320, 16, 4, "prerouted"),
                                              (20, 192, 320, 64, 8, "prerouted"), (64, 192, 320, 128, 8, "logits")])
-def test_decode_chain_small_shapes(T, H, I, E, k, mode):
-    """The two-kernel decode chain at shapes with one k-block (FC1 at H = 64,
-    FC2 at I = 64) and odd k-block counts (H = 192, I = 320, 192): the
-    k-blocks alternate between two accumulators.  T = 20 takes the 32-token
-    tile form; the last two shapes give CTAs several tiles."""
+@pytest.mark.parametrize("one", [False, True])
+def test_decode_chain_small_shapes(T, H, I, E, k, mode, one):
+    """The decode chain (two kernels, or one launch) at shapes with one
+    k-block (FC1 at H = 64, FC2 at I = 64) and odd k-block counts (H = 192,
+    I = 320, 192): the k-blocks alternate between two accumulators.  T = 20
+    takes the 32-token tile form; the last two shapes give CTAs several
+    tiles (in one launch, FC1 tiles and then FC2 tiles)."""
     wl = W.make_moe(T=T, H=H, I=I, E=E, top_k=k, mode=mode, seed=T + H)
-    out, _ = _forward(wl, _dev(wl), moe.PATH_DECODE, decode_chain=True)
+    out, _ = _forward(wl, _dev(wl), moe.PATH_DECODE, decode_chain=True, one_launch=one)
     want, _ = _oracle_out(wl)
     check_bf16_end_to_end(W.bf16_bits(out), want, "decode chain")
 
@@ -350,16 +353,18 @@ def test_stage_chain_prefill_configs(name):
 
 # ------------------------------------------------- decode chain (T * k <= 1024) --
 
+@pytest.mark.parametrize("one", [False, True])
 @pytest.mark.parametrize("name", ["decode_t1", "decode_t8", "decode_t64"])
-def test_decode_chain_replays_bitwise_and_graph(name):
-    """The two-kernel decode chain combines each (token, column block) in the
-    tile that arrives last; the sum order is fixed, so replays, in any arrival
-    order, are bitwise identical."""
+def test_decode_chain_replays_bitwise_and_graph(name, one):
+    """The decode chain combines each (token, column block) in the tile that
+    arrives last; the sum order is fixed, so replays, in any arrival order,
+    are bitwise identical.  In one launch this also checks that the
+    per-expert counters start from zero again at every launch."""
     wl = W.make_moe(name)
     d = _dev(wl)
     plan = moe.MoEPlan(d["x"], d["w1"], d["w2"], wl.E, wl.top_k, topk_ids=d["topk_ids"], topk_w=d["topk_w"],
-                       path=moe.PATH_DECODE, decode_chain=True)
-    assert plan.kernels_per_launch() == 2
+                       path=moe.PATH_DECODE, decode_chain=True, decode_one_launch=one)
+    assert plan.kernels_per_launch() == (1 if one else 2)
     ref = plan.launch().clone()
     torch.cuda.synchronize()
     for _ in range(5):
@@ -397,30 +402,32 @@ def test_decode_chain_replays_bitwise_and_graph(name):
     assert np.array_equal(view("perm_to_exp", len(p2e_o)), p2e_o)
 
 
-def test_decode_chain_status_and_bad_ids():
+@pytest.mark.parametrize("one", [False, True])
+def test_decode_chain_status_and_bad_ids(one):
     wl = W.make_moe(T=6, H=128, I=128, E=9, top_k=3, mode="prerouted", seed=12)
     ids = wl.topk_ids.clone()
     ids[2, 1] = 40
     wl.topk_ids = ids
     status = torch.full((1,), 0x40, dtype=torch.int32, device=DEV)  # stale bits are cleared
-    out, plan = _forward(wl, _dev(wl), moe.PATH_DECODE, status=status, decode_chain=True)
-    assert plan.kernels_per_launch() == 2
+    out, plan = _forward(wl, _dev(wl), moe.PATH_DECODE, status=status, decode_chain=True, one_launch=one)
+    assert plan.kernels_per_launch() == (1 if one else 2)
     assert int(status.item()) == moe.DEV_BAD_EXPERT
     want, _ = _oracle_out(wl)
     check_bf16_end_to_end(W.bf16_bits(out), want, "chain bad ids")
     wl.topk_ids = wl.topk_ids.clamp(0, 8)
     d = _dev(wl)
-    out2, _ = _forward(wl, d, moe.PATH_DECODE, status=status, decode_chain=True)
+    out2, _ = _forward(wl, d, moe.PATH_DECODE, status=status, decode_chain=True, one_launch=one)
     assert int(status.item()) == 0
 
 
+@pytest.mark.parametrize("one", [False, True])
 @pytest.mark.parametrize("off,L", [(0, 5), (5, 4), (2, 1)])
-def test_decode_chain_expert_shard(off, L):
+def test_decode_chain_expert_shard(off, L, one):
     full = W.make_moe(T=12, H=192, I=128, E=9, top_k=4, mode="logits", seed=21)
     wl = W.make_moe(T=12, H=192, I=128, E=9, top_k=4, mode="logits", seed=21)
     wl.w1, wl.w2 = full.w1[off:off + L].contiguous(), full.w2[off:off + L].contiguous()
     wl.local_offset, wl.num_local = off, L
-    out, plan = _forward(wl, _dev(wl), moe.PATH_DECODE, decode_chain=True)
-    assert plan.kernels_per_launch() == 3  # route + the two chain kernels
+    out, plan = _forward(wl, _dev(wl), moe.PATH_DECODE, decode_chain=True, one_launch=one)
+    assert plan.kernels_per_launch() == (2 if one else 3)  # route + the chain kernel(s)
     want, _ = _oracle_out(wl)
     check_bf16_end_to_end(W.bf16_bits(out), want, f"chain shard {off}+{L}")
