@@ -255,20 +255,22 @@ MOE_API int moe_forward(const moe_bf16 *x, const float *logits, const int32_t *t
 #define MOE_PLAN_STAGE_TIMING 1 /* record CUDA events around each stage     */
 #define MOE_PLAN_ONE_CTA_GEMM 2 /* grouped path: one-CTA GEMM kernels instead of
                                    the CTA-pair (2-SM MMA) kernels (comparison) */
-#define MOE_PLAN_DECODE_CHAIN 4 /* decode path, T*top_k <= 1024: always the two
-                                   kernels with the sort, gather and finalize
-                                   folded in (without either flag the chain runs
-                                   for T*top_k <= 8, where it measured faster) */
+#define MOE_PLAN_DECODE_CHAIN 4 /* decode path, T*top_k <= 1024: always the
+                                   chain (sort, gather and finalize folded into
+                                   the GEMM kernels) as two kernels; without a
+                                   decode flag the chain runs as one launch for
+                                   T*top_k <= 32, where it measured faster */
 #define MOE_PLAN_DECODE_SEPARATE 8 /* decode path: always the five separate
                                       kernels (sort, gather, FC1, FC2, finalize) */
 #define MOE_PLAN_FUSED_GATHER 16 /* grouped path, CTA-pair GEMMs: FC1 copies its
                                     token rows straight from x (no gather kernel,
                                     no permuted copy of x; measured slower, see
                                     moe_fc1_swiglu_gathered) */
-#define MOE_PLAN_DECODE_ONE_LAUNCH 32 /* decode path: the chain's FC1 and FC2 as one
-                                         kernel; CTAs without FC1 work stream their
-                                         W2 tile while FC1 runs and wait (bounded)
-                                         until the FC1 tiles of its expert are done */
+#define MOE_PLAN_DECODE_ONE_LAUNCH 32 /* decode path, T*top_k <= 1024: always the
+                                         chain as one kernel; CTAs without FC1 work
+                                         stream their W2 tile while FC1 runs and wait
+                                         (bounded) until the FC1 tiles of its expert
+                                         are done */
 
 typedef struct moe_forward_desc {
     const moe_bf16 *x;

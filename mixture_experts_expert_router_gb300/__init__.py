@@ -410,9 +410,9 @@ class MoEPlan:
                  stage_timing: bool = False, one_cta_gemm: bool = False, decode_chain: bool | None = None,
                  fused_gather: bool = False, decode_one_launch: bool = False):
         """decode_chain: None lets the library choose the decode form (the
-        two-kernel chain for very few routes), True forces the chain, False
-        the five separate kernels.  decode_one_launch: the chain's two
-        kernels as one launch.  fused_gather: on the grouped path FC1 copies
+        chain in one launch for few routes, else five kernels), True forces
+        the chain as two kernels, False the five separate kernels.
+        decode_one_launch: always the chain in one launch.  fused_gather: on the grouped path FC1 copies
         its token rows straight from x instead of a gather kernel."""
         T, H, I, L, out = _layer_args(x, w1, w2, num_experts, top_k, logits, topk_ids, topk_w,
                                       local_offset, out)

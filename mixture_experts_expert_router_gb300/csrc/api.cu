@@ -374,9 +374,10 @@ int moe_forward_prepare(const moe_forward_desc *desc, moe_plan **plan_out) {
     p->h = reinterpret_cast<uint16_t *>(ws + lay.h);
     p->y = reinterpret_cast<float *>(ws + lay.y);
     int rc;
-    // Decode: the two-kernel chain saves three launches but gathers its token
-    // rows and combines inside the GEMM kernels; it is the faster form only for
-    // very few routes, so without a flag it runs up to kChainAutoRoutes routes.
+    // Decode: the chain saves launches but gathers its token rows and
+    // combines inside the GEMM kernels; it is the faster form only for few
+    // routes, so without a flag it runs, as one launch, up to kChainAutoRoutes
+    // routes.  MOE_PLAN_DECODE_CHAIN alone asks for its two-kernel form.
     const bool force_chain = (d.flags & (MOE_PLAN_DECODE_CHAIN | MOE_PLAN_DECODE_ONE_LAUNCH)) != 0;
     const bool auto_chain = (d.flags & MOE_PLAN_DECODE_SEPARATE) == 0 && p->R <= kChainAutoRoutes &&
                             d.H % 64 == 0 && d.I % 64 == 0;
@@ -393,7 +394,7 @@ int moe_forward_prepare(const moe_forward_desc *desc, moe_plan **plan_out) {
       c.out = d.out;
       c.comb = reinterpret_cast<int32_t *>(ws + lay.comb);
       c.done1 = reinterpret_cast<int32_t *>(ws + lay.done1);
-      c.one_launch = (d.flags & MOE_PLAN_DECODE_ONE_LAUNCH) != 0;
+      c.one_launch = (d.flags & MOE_PLAN_DECODE_ONE_LAUNCH) != 0 || !force_chain;
       c.m_indptr = p->m_indptr;
       c.p2e = p->p2e;
       c.e2p = p->e2p;

@@ -116,13 +116,15 @@ int swap_prepare(SwapPlan &p, bool swiglu, const uint16_t *W, int G, int w_rows,
                  long max_group_rows, void *out, int32_t *status, bool early);
 cudaError_t launch_swap(const SwapPlan &p, const Launch &l);
 
-// S7 as a two-kernel chain with the sort, gather and finalize folded in
-// (decode_chain.cu); for T * top_k <= kChainMaxRoutes.
+// S7 as a chain with the sort, gather and finalize folded in (decode_chain.cu):
+// two kernels, or both phases in one launch; for T * top_k <= kChainMaxRoutes.
 constexpr int kChainMaxRoutes = 1024;
-// Without a plan flag the decode path takes the chain up to this many routes
-// (T = 1 at top-8: 28.7 us against 31.1 us for the five kernels; at T = 8 the
-// five kernels are faster, 90.6 us against 96.0 us).
-constexpr int kChainAutoRoutes = 8;
+// Without a plan flag the decode path runs the chain in one launch up to this
+// many routes.  Measured at H = 2048, I = 768, E = 128, top-8, pre-routed
+// (one launch / two kernels / five kernels): T = 1: 28.2 / 28.7 / 31.1 us;
+// T = 2: 41.2 / 47.1 us (one launch / two kernels); T = 4: 61.6 / 70.1 /
+// 63.9 us; T = 8: 90.8 / 93.8 / 89.2 us.
+constexpr int kChainAutoRoutes = 32;
 struct ChainPlan {
   CUtensorMap map_w1, map_x, map_w2, map_h;
   const uint16_t *x = nullptr, *w1 = nullptr, *w2 = nullptr;

@@ -229,10 +229,10 @@ def test_decode_configs_full(name, path, chain):
     check_bf16_end_to_end(W.bf16_bits(out), want, name)
 
 
-@pytest.mark.parametrize("T,kernels", [(1, 2), (8, 5)])
+@pytest.mark.parametrize("T,kernels", [(1, 1), (4, 1), (8, 5)])
 def test_decode_form_chosen_by_route_count(T, kernels):
-    """Without a flag the decode path runs the two-kernel chain for at most 8
-    routes (T = 1 at top-8) and the five separate kernels above that."""
+    """Without a flag the decode path runs the chain as one launch for at
+    most 32 routes (T <= 4 at top-8) and the five separate kernels above."""
     wl = W.make_moe(T=T, H=256, I=128, E=16, top_k=8, mode="prerouted", seed=T)
     out, plan = _forward(wl, _dev(wl), moe.PATH_AUTO, decode_chain=None)
     assert plan.kernels_per_launch() == kernels
