@@ -224,7 +224,7 @@ def run_reference(args, world, rank):
         "steps": steps, "warmup": warm, "ms_per_step": 1000.0 * total_t / steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded)",
-        "config": config_dict(wl, world),
+        "config": config_dict(wl, world, weight_banks(wl)),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                          "sample": f"{n_tok} random tokens of the {wl.T}-token batch per step "
                                    f"(routing + FC1/SwiGLU + FC2 + combine for those tokens)"},
@@ -243,6 +243,18 @@ def make_workload(args, rank, weights_device):
         wl.name = f"custom_T{T}_H{H}_I{I}_E{E}_k{k}"
         return wl
     return W.make_moe(args.config, seed=args.seed + rank, device="cpu", weights_device=weights_device)
+
+
+def timed_steps(fn, steps, stream):
+    """Device time (ms) of `steps` back-to-back calls of fn, by CUDA events
+    on `stream`."""
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
 
 
 def recorded_traffic(workload: str, kernel: str):
@@ -284,11 +296,32 @@ def roofline_entry(decode_path, fc1_s, F_fc1, B_fc1, peak_t, peak_b, peak_src, t
             "peak_kind": f"{peak_src} sustained bf16 (kernel timed inside the step)", "flops_per_launch": F_fc1}
 
 
-def config_dict(wl, world):
+L2_NOMINAL = 128 << 20  # GB300's L2, rounded
+MAX_BANKS = 32
+
+
+def weight_banks(wl) -> int:
+    """Copies of the expert banks the steps rotate over (one per layer of a
+    model), so that the active weights of all copies exceed three times the
+    L2: every step streams its own weights from HBM.  1 when one step's
+    active weights already do (every routed expert distinct)."""
+    experts = min(wl.num_local, wl.T * wl.top_k)
+    active = experts * 3.0 * wl.H * wl.I * 2
+    return 1 if active >= 3 * L2_NOMINAL else min(MAX_BANKS, int(np.ceil(3 * L2_NOMINAL / active)))
+
+
+def config_dict(wl, world, banks=1):
+    experts = min(wl.num_local, wl.T * wl.top_k)
+    rotated = banks * experts * 3.0 * wl.H * wl.I * 2
     return {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "top_k": wl.top_k,
             "routing": wl.mode, "global_batch": wl.T * world,
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-            "l2": "inputs larger than L2: the expert weights stream from HBM every step"}
+            "l2": ("inputs larger than L2: the expert weights stream from HBM every step" if banks == 1 else
+                   f"inputs larger than L2: consecutive steps rotate over {banks} copies of the expert "
+                   f"banks (one per layer), whose active weights together exceed three times the L2, "
+                   f"so every step streams its weights from HBM" if rotated >= 3 * L2_NOMINAL else
+                   f"small workload: the steps rotate over {banks} copies of the expert banks, which "
+                   f"still fit in L2")}
 
 
 def run_ours(args, world, rank, local):
@@ -305,12 +338,21 @@ def run_ours(args, world, rank, local):
     opts = dict(decode_chain=True if args.decode_chain else (False if args.decode_separate else None),
                 one_cta_gemm=args.one_cta_gemm, fused_gather=args.fused_gather,
                 decode_one_launch=args.decode_one_launch)
-    plan = moe.MoEPlan(x, wl.w1, wl.w2, wl.E, wl.top_k, logits=logits, topk_ids=tids, topk_w=tw,
-                       local_offset=wl.local_offset, status=status, **opts)
-    # a second plan on the same buffers records CUDA events around every stage
-    plan_t = moe.MoEPlan(x, wl.w1, wl.w2, wl.E, wl.top_k, logits=logits, topk_ids=tids, topk_w=tw,
-                         local_offset=wl.local_offset, status=status, out=plan.out,
-                         workspace=plan.workspace, stage_timing=True, **opts)
+    # one plan per copy of the expert banks; the steps rotate over them
+    banks = weight_banks(wl)
+    w1s = [wl.w1] + [wl.w1.clone() for _ in range(banks - 1)]
+    w2s = [wl.w2] + [wl.w2.clone() for _ in range(banks - 1)]
+    plans, plans_t = [], []
+    for b in range(banks):
+        p_b = moe.MoEPlan(x, w1s[b], w2s[b], wl.E, wl.top_k, logits=logits, topk_ids=tids, topk_w=tw,
+                          local_offset=wl.local_offset, status=status,
+                          out=plans[0].out if plans else None, **opts)
+        # a second plan on the same buffers records CUDA events around every stage
+        plans_t.append(moe.MoEPlan(x, w1s[b], w2s[b], wl.E, wl.top_k, logits=logits, topk_ids=tids,
+                                   topk_w=tw, local_offset=wl.local_offset, status=status, out=p_b.out,
+                                   workspace=p_b.workspace, stage_timing=True, **opts))
+        plans.append(p_b)
+    plan, plan_t = plans[0], plans_t[0]
     kernels = plan.kernels_per_launch()
     stream = torch.cuda.current_stream(dev)
 
@@ -334,15 +376,28 @@ def run_ours(args, world, rank, local):
     side.wait_stream(stream)
     with torch.cuda.stream(side):
         for _ in range(3):
-            plan.launch()
+            for p_b in plans:
+                p_b.launch()
     stream.wait_stream(side)
     torch.cuda.synchronize()
-    graph = None
+    graphs = []
     if not args.no_graph:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            plan.launch()
-    step = graph.replay if graph is not None else plan.launch
+        for p_b in plans:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                p_b.launch()
+            graphs.append(g)
+    calls = [g.replay for g in graphs] if graphs else [p_b.launch for p_b in plans]
+    graph = graphs[0] if graphs else None
+
+    def rotating(fns):
+        k = [0]
+
+        def call():
+            fns[k[0] % len(fns)]()
+            k[0] += 1
+        return call
+    step = rotating(calls)
 
     dev_index = str(local)
     try:
@@ -357,32 +412,27 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t_wall0 = time.time()
-    ev0.record(stream)
-    for _ in range(args.steps):
-        step()
-    ev1.record(stream)
-    torch.cuda.synchronize()
+    ms_local = timed_steps(step, args.steps, stream)
     t_wall1 = time.time()
     barrier(world)
-    ms_local = ev0.elapsed_time(ev1)
 
     # stage pass: the same steps with CUDA events between the stages (no PDL
     # overlap between them); gives each kernel's mean duration
     for _ in range(3):
-        plan_t.launch()
+        for p_b in plans_t:
+            p_b.launch()
     torch.cuda.synchronize()
-    plan_t.stage_reset()
+    for p_b in plans_t:
+        p_b.stage_reset()
     n_stage_steps = min(args.steps, 200)
-    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s0.record(stream)
-    for _ in range(n_stage_steps):
-        plan_t.launch()
-    s1.record(stream)
-    torch.cuda.synchronize()
-    stage_pass_ms = s0.elapsed_time(s1) / n_stage_steps
-    stage_ms, n_timed = plan_t.stage_times()
+    stage_pass_ms = timed_steps(rotating([p_b.launch for p_b in plans_t]), n_stage_steps, stream) / n_stage_steps
+    stage_ms, n_timed = {}, 0
+    for p_b in plans_t:
+        ms_b, n_b = p_b.stage_times()
+        n_timed += n_b
+        for key, v in ms_b.items():
+            stage_ms[key] = stage_ms.get(key, 0.0) + v
     time.sleep(0.25)
 
     # end to end: pinned host inputs in, result out, every step
@@ -395,6 +445,8 @@ def run_ours(args, world, rank, local):
         (ids_h.numel() * 4 + w_h.numel() * 4 if ids_h is not None else 0)
     d2h = out_h.numel() * 2
 
+    e2e_launch = rotating([p_b.launch for p_b in plans])
+
     def e2e_step():
         x.copy_(x_h, non_blocking=True)
         if lg_h is not None:
@@ -402,7 +454,7 @@ def run_ours(args, world, rank, local):
         if ids_h is not None:
             tids.copy_(ids_h, non_blocking=True)
             tw.copy_(w_h, non_blocking=True)
-        plan.launch()
+        e2e_launch()
         out_h.copy_(plan.out, non_blocking=True)
 
     for _ in range(max(1, args.warmup)):
@@ -410,15 +462,9 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
+    ms_e2e_local = timed_steps(e2e_step, args.steps, stream)
     barrier(world)
     clocks.stop()
-    ms_e2e_local = e0.elapsed_time(e1)
     st = int(status.item())
 
     ms = max_over_ranks(world, ms_local)
@@ -446,7 +492,7 @@ def run_ours(args, world, rank, local):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded)",
-        "config": config_dict(wl, world),
+        "config": config_dict(wl, world, banks),
         "tflops": F * world / step_s / 1e12,
         "hbm_gbs": B * world / step_s / 1e9,
         "roofline_step": {"time_ms": roofline_t * 1000.0, "frac": roofline_t / step_s,

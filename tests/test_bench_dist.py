@@ -68,3 +68,26 @@ def test_reference_arm_line_on_rank0(capsys):
     assert line["impl"] == "reference" and line["unit"] == "tokens/s" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
     assert line["metric"] == bench.METRIC
+
+
+def test_weight_banks_keep_every_step_in_hbm():
+    """Workloads whose active weights fit in L2 rotate over enough copies of
+    the expert banks that the copies' active weights exceed three times the
+    L2; the others use one bank."""
+    import bench
+    from mixture_experts_expert_router_gb300 import workloads as W
+
+    class Shape:
+        def __init__(self, T, H, I, E, k):
+            self.T, self.H, self.I, self.num_local, self.top_k = T, H, I, E, k
+
+    for name in ("decode_t1", "decode_t8", "decode_t64", "prefill_few_large", "prefill_many_fine"):
+        c = W.MOE_CONFIGS[name]
+        s = Shape(c["T"], c["H"], c["I"], c["E"], c["top_k"])
+        active = min(s.num_local, s.T * s.top_k) * 3 * s.H * s.I * 2
+        n = bench.weight_banks(s)
+        if active >= 3 * bench.L2_NOMINAL:
+            assert n == 1, name
+        else:
+            assert n * active >= 3 * bench.L2_NOMINAL and (n - 1) * active < 3 * bench.L2_NOMINAL, name
+    assert bench.weight_banks(Shape(1, 2048, 768, 128, 8)) == 6  # 8 experts x 9.4 MB
