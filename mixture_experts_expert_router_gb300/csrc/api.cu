@@ -105,7 +105,7 @@ struct moe_plan {
   float *y;
   GemmPlan fc1, fc2;
   SwapPlan fc1d, fc2d;  // decode path, separate kernels
-  ChainPlan chain;      // decode path, two-kernel chain
+  ChainPlan chain;      // decode path: the chain (one launch or two kernels)
   bool use_chain;
   bool fused_gather;    // grouped path: FC1 gathers its rows itself
   bool timing;

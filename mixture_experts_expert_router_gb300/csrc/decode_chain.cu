@@ -1,27 +1,35 @@
-// S7 for few tokens as a two-kernel chain: FC1 and FC2 of the decode regime
-// with the sort, the gather and the finalize folded in.
+// S7 for few tokens as a chain: FC1 and FC2 of the decode regime with the
+// sort, the gather and the finalize folded in, as two kernels or as one.
 //
 // For T*top_k <= kMaxRoutes routes each CTA sorts the routes itself in shared
 // memory (the same stable counting sort as sort.cu: ascending expanded index
-// inside each local expert), so no sort kernel runs and no CTA waits for
-// another.  Both kernels are swap-AB weight-streaming GEMMs (decode.cu):
-// 128 weight rows on the MMA's M side, the expert's tokens on N.
+// inside each local expert), so no sort kernel runs.  Both phases are swap-AB
+// weight-streaming GEMMs (decode.cu): 128 weight rows on the MMA's M side,
+// the expert's tokens on N.
 //
 //   FC1  the producer warp gathers the expert's token rows straight from x
 //        (four rows per TMA row-gather), the epilogue writes
-//        h[p] = bf16(silu(g) * u); its first CTA also clears the status word,
-//        publishes the sort (m_indptr, perm_to_exp, exp_to_perm) and zeroes
-//        the combine counters.
-//   FC2  streams W2 (the first ring of weight boxes before it waits for FC1),
+//        h[p] = bf16(silu(g) * u); the first CTA also clears the status word
+//        and publishes the sort (m_indptr, perm_to_exp, exp_to_perm).
+//   FC2  streams W2 (the first ring of weight boxes before h is ready),
 //        writes the unscaled fp32 rows y, and combines: every (token, 128-col
 //        block) has a counter; the tile that brings it to the token's number
 //        of local routes sums the token's rows in ascending slot order,
 //        out = bf16(sum_j w_j * y_j), exactly the finalize kernel's
 //        arithmetic, so the result does not depend on which tile is last.
 //
-// The k-loop of both kernels runs as two half-pipelines (even / odd k-blocks,
-// each with its own producer, MMA thread and TMEM accumulator; the epilogue
-// adds the two), as in decode.cu.
+// Two kernels: FC2 waits for FC1 by programmatic dependent launch, and FC1's
+// first CTA zeroes the combine counters.  One launch: every CTA runs its FC1
+// tiles first and then its FC2 tiles; an FC2 tile loads h once the count of
+// finished FC1 tiles of its expert is complete (a bounded wait on a counter
+// that FC1 epilogues raise after their h stores), and the last CTA to finish
+// zeroes the counters for the next launch.  With at most one CTA per SM and
+// no more CTAs than SMs, every CTA that others wait for has an SM, and FC1
+// tiles wait for nothing.
+//
+// The k-loop runs as two half-pipelines (even / odd k-blocks, each with its
+// own producer, MMA thread and TMEM accumulator; the epilogue adds the two),
+// as in decode.cu.
 //
 // Programmatic dependent launch: each kernel reads only the layer's inputs
 // (and, in logits mode, the routing kernel's output, waited for) before its
