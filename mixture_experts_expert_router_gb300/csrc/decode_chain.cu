@@ -1,7 +1,7 @@
 // S7 for few tokens as a chain: FC1 and FC2 of the decode regime with the
 // sort, the gather and the finalize folded in, as two kernels or as one.
 //
-// For T*top_k <= kMaxRoutes routes each CTA sorts the routes itself in shared
+// For T*top_k <= kChainMaxRoutes routes each CTA sorts the routes itself in shared
 // memory (the same stable counting sort as sort.cu: ascending expanded index
 // inside each local expert), so no sort kernel runs.  Both phases are swap-AB
 // weight-streaming GEMMs (decode.cu): 128 weight rows on the MMA's M side,
