@@ -244,11 +244,12 @@ MOE_API int moe_forward(const moe_bf16 *x, const float *logits, const int32_t *t
  * Prepare once, launch many (flashinfer.experimental.cake_stepfun_moe,
  * Prepared launches; Cake ragged BF16 grouped GEMM, Prepared launches):
  * moe_forward_prepare validates the descriptor, lays out the workspace and
- * encodes the TMA tensor maps; for the decode chain in one launch it also
- * zeroes the counters that launch keeps in the workspace (a blocking
- * cudaMemset, once).  moe_plan_launch then only enqueues kernels: no
- * allocation, no host synchronisation, capturable in a CUDA graph, and valid
- * for new VALUES written into the bound buffers.  The workspace is every
+ * encodes the TMA tensor maps (host memory only).  moe_plan_launch then only
+ * enqueues work: no allocation, no host synchronisation, capturable in a
+ * CUDA graph, and valid for new VALUES written into the bound buffers.  (For
+ * the decode chain in one launch, a plan's first launch also zeroes the
+ * counters that the kernel keeps in the workspace, with cudaMemsetAsync on
+ * the launch stream; every launch leaves them at zero.)  The workspace is every
  * launch's scratch: launches of one plan (or of plans sharing a workspace)
  * must run one after another (one stream, or streams ordered by events).
  */

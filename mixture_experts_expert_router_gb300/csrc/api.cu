@@ -107,6 +107,7 @@ struct moe_plan {
   SwapPlan fc1d, fc2d;  // decode path, separate kernels
   ChainPlan chain;      // decode path: the chain (one launch or two kernels)
   bool use_chain;
+  bool counters_zeroed;  // one-launch chain: its counters were zeroed before the first launch
   bool fused_gather;    // grouped path: FC1 gathers its rows itself
   bool timing;
   cudaEvent_t (*ev)[kNumStages + 1];
@@ -479,6 +480,10 @@ int moe_plan_launch(moe_plan *p, void *stream) {
     if (launch_route(d.logits, d.T, d.E, d.top_k, p->ids, p->w, l) != cudaSuccess) return MOE_ERR_CUDA;
   }
   if (p->use_chain) {  // sort, gather and finalize run inside the GEMM kernels
+    if (p->chain.one_launch && !p->counters_zeroed) {
+      if (chain_zero_counters(p->chain, s) != cudaSuccess) return MOE_ERR_CUDA;
+      p->counters_zeroed = true;
+    }
     if (!mark(kSort) || !mark(kGather) || !mark(kFc1)) return MOE_ERR_CUDA;
     if (p->chain.one_launch) {
       if (launch_chain(p->chain, 0, l) != cudaSuccess) return MOE_ERR_CUDA;

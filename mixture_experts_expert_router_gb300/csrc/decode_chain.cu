@@ -694,11 +694,13 @@ int chain_prepare(ChainPlan &p) {
   // memory), so every CTA whose FC1 tiles others wait for gets an SM
   p.grid_one = (int)(t1 + t2 < sms ? t1 + t2 : sms);
   cudaError_t e = p.bnt == 16 ? configure<16>(p.smem) : (p.bnt == 32 ? configure<32>(p.smem) : configure<64>(p.smem));
-  if (e == cudaSuccess && p.one_launch && p.done1)  // the counters start from zero
-    e = cudaMemset(p.done1, 0, ((size_t)p.L + 1) * sizeof(int32_t));
-  if (e == cudaSuccess && p.one_launch && p.comb) e = cudaMemset(p.comb, 0, chain_comb_ints(p.T, p.H) * 4);
-  if (e == cudaSuccess && p.one_launch) e = cudaDeviceSynchronize();
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+cudaError_t chain_zero_counters(const ChainPlan &p, cudaStream_t stream) {
+  cudaError_t e = cudaMemsetAsync(p.done1, 0, ((size_t)p.L + 1) * sizeof(int32_t), stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(p.comb, 0, chain_comb_ints(p.T, p.H) * sizeof(int32_t), stream);
+  return e;
 }
 
 cudaError_t launch_chain(const ChainPlan &p, int part, const Launch &l) {

@@ -143,5 +143,8 @@ size_t chain_comb_ints(int T, int H);
 int chain_prepare(ChainPlan &p);
 // part 1: FC1 kernel, 2: FC2 kernel, 0: both phases in one kernel
 cudaError_t launch_chain(const ChainPlan &p, int part, const Launch &l);
+// One launch keeps counters in the workspace that every launch leaves at
+// zero; before the first launch of a plan they are zeroed on its stream.
+cudaError_t chain_zero_counters(const ChainPlan &p, cudaStream_t stream);
 
 }  // namespace moe

@@ -176,14 +176,23 @@ def test_expert_parallel_shard(off, L):
     check_bf16_end_to_end(W.bf16_bits(out), want, f"shard {off}+{L}")
 
 
-def test_shard_with_no_routed_tokens_is_zero():
-    wl = W.make_moe(T=32, H=128, I=64, E=8, top_k=2, mode="prerouted", seed=5)
+@pytest.mark.parametrize("T,path,chain", [(32, moe.PATH_AUTO, None), (8, moe.PATH_DECODE, None),
+                                          (8, moe.PATH_DECODE, True), (200, moe.PATH_GROUPED, False)])
+def test_shard_with_no_routed_tokens_is_zero(T, path, chain):
+    """No route lands in the local shard: every form (five decode kernels,
+    the chain in one launch or two kernels, the grouped path) writes zeros."""
+    wl = W.make_moe(T=T, H=128, I=128, E=8, top_k=2, mode="prerouted", seed=5)
     wl.topk_ids = torch.zeros_like(wl.topk_ids)
     wl.topk_ids[:, 1] = 1
     wl.w1, wl.w2 = wl.w1[4:6].contiguous(), wl.w2[4:6].contiguous()
     wl.local_offset, wl.num_local = 4, 2
-    out, _ = _forward(wl, _dev(wl))
+    d = _dev(wl)
+    out, plan = _forward(wl, d, path, decode_chain=chain)
     assert torch.all(out == 0)
+    plan.out.fill_(3.0)  # a second launch writes the zeros again (the chain's counters reset)
+    plan.launch()
+    torch.cuda.synchronize()
+    assert torch.all(plan.out == 0)
 
 
 def test_bad_expert_ids_flagged_and_dropped():
