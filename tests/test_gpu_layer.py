@@ -411,6 +411,30 @@ def test_decode_chain_replays_bitwise_and_graph(name, one):
     assert np.array_equal(view("perm_to_exp", len(p2e_o)), p2e_o)
 
 
+def test_decode_one_launch_first_launch_captured():
+    """A one-launch chain plan whose first launch is captured in a CUDA graph:
+    the graph holds the zeroing of the plan's counters, and every replay gives
+    the oracle's output."""
+    wl = W.make_moe(T=2, H=256, I=192, E=16, top_k=4, mode="prerouted", seed=31)
+    d = _dev(wl)
+    plan = moe.MoEPlan(d["x"], d["w1"], d["w2"], wl.E, wl.top_k, topk_ids=d["topk_ids"], topk_w=d["topk_w"],
+                       path=moe.PATH_DECODE, decode_one_launch=True)
+    assert plan.kernels_per_launch() == 1
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        plan.launch()
+    want, _ = _oracle_out(wl)
+    for _ in range(3):
+        plan.out.fill_(5.0)
+        g.replay()
+        torch.cuda.synchronize()
+        check_bf16_end_to_end(W.bf16_bits(plan.out), want, "captured first launch")
+    plan.out.fill_(5.0)
+    plan.launch()  # and a direct launch after the replays
+    torch.cuda.synchronize()
+    check_bf16_end_to_end(W.bf16_bits(plan.out), want, "launch after replays")
+
+
 @pytest.mark.parametrize("one", [False, True])
 def test_decode_chain_status_and_bad_ids(one):
     wl = W.make_moe(T=6, H=128, I=128, E=9, top_k=3, mode="prerouted", seed=12)
