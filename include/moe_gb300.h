@@ -275,7 +275,10 @@ MOE_API int moe_forward(const moe_bf16 *x, const float *logits, const int32_t *t
                                          chain as one kernel; CTAs without FC1 work
                                          stream their W2 tile while FC1 runs and wait
                                          (bounded) until the FC1 tiles of its expert
-                                         are done */
+                                         are done.  The kernel takes at most one CTA
+                                         per SM; if other work holds SMs for longer
+                                         than the wait limit, the launch reports
+                                         MOE_DEV_TIMEOUT in the status word. */
 
 typedef struct moe_forward_desc {
     const moe_bf16 *x;
