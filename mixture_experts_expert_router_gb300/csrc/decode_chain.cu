@@ -264,6 +264,63 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
   }
   if (!a.ids_early) pdl_wait();  // the routing kernel wrote ids and weights
 
+  // Early weights.  With T <= BNT every active expert has exactly one row
+  // block (an expert gets at most one route per token), so a CTA's first item
+  // follows from the rank of its expert among the distinct local experts of
+  // the routes, in ascending order.  For at most 32 routes each producer warp
+  // works that out from the ids and issues the weight boxes of its first
+  // k-blocks (the first use of its ring slots) before the sort below; the
+  // item's token boxes go out once the sort is done.
+  constexpr int HS0 = C::STAGES / 2;
+  int n_early = 0;
+  if ((warp == 0 || warp == kProd1Warp) && T <= BNT && R <= 32) {
+    asm volatile("bar.sync 2, 64;" ::: "memory");  // warp 6 sees the barriers warp 0 initialised
+    const int q = warp == 0 ? 0 : 1;
+    int g = -1;
+    if (lane < R) {
+      const int id = a.ids[lane];
+      if (id >= a.off && id < a.off + L) g = id - a.off;
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, g);
+    const bool first = g >= 0 && (peers & ((1u << lane) - 1u)) == 0u;
+    // one row block per expert also needs at most BNT routes per expert (more
+    // only with repeated ids inside a token's routes): otherwise no early issue
+    const bool one_block = __all_sync(0xffffffffu, g < 0 || __popc(peers) <= BNT);
+    int rank = 0;  // distinct local experts below g
+    for (int j = 0; j < 32; ++j) {
+      const int gj = __shfl_sync(0xffffffffu, g, j);
+      const bool fj = __shfl_sync(0xffffffffu, first ? 1 : 0, j) != 0;
+      if (fj && gj < g) ++rank;
+    }
+    const int n_act = __popc(__ballot_sync(0xffffffffu, first));
+    const int t1 = MODE == kModeFc2 ? 0 : a.m_tiles1 * n_act;
+    const int t2 = MODE == kModeFc1 ? 0 : a.m_tiles2 * n_act;
+    const int w = (int)blockIdx.x;
+    if (one_block && w < t1 + t2) {
+      const bool fc1 = w < t1;
+      const int e = fc1 ? w / a.m_tiles1 : (w - t1) / a.m_tiles2;
+      const int m = fc1 ? w - e * a.m_tiles1 : (w - t1) - e * a.m_tiles2;
+      const unsigned sel = __ballot_sync(0xffffffffu, first && rank == e);
+      const int ge = __shfl_sync(0xffffffffu, g, sel ? __ffs(sel) - 1 : 0);
+      const int wrow = fc1 ? ge * 2 * a.I + m * 64 : ge * a.H + m * 128;
+      const int nkb = (fc1 ? a.H : a.I) / BK;
+      const uint64_t pol_w = policy_evict_first();
+      for (int kb = q; kb < nkb && n_early < HS0 && sel != 0u; kb += 2, ++n_early) {
+        const int s = q * HS0 + n_early;
+        const uint32_t a_dst = smem_base + s * C::STAGE_BYTES;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(full_bar(s), C::STAGE_BYTES);
+          if (fc1) {
+            tma_load_2d(a_dst, &a.map_w1, full_bar(s), kb * BK, wrow, pol_w);
+            tma_load_2d(a_dst + 64 * 128, &a.map_w1, full_bar(s), kb * BK, wrow + a.I, pol_w);
+          } else {
+            tma_load_2d(a_dst, &a.map_w2, full_bar(s), kb * BK, wrow, pol_w);
+          }
+        }
+      }
+    }
+  }
+
   cta_sort(a.ids, R, a.E, a.off, L, m_indptr, next, p2e, e2p, bad);
   if (MODE != kModeFc1) {
     for (int t = threadIdx.x; t < T; t += kThreads) {
@@ -325,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
     const int q = warp == 0 ? 0 : 1;
     const uint64_t pol_w = policy_evict_first();  // each weight byte is read once
     const uint64_t pol_x = policy_evict_last();
-    int iq = 0;  // this pipeline's k-blocks so far: its private ring slots q * HS + iq % HS
+    int iq = n_early;  // this pipeline's k-blocks so far: its private ring slots q * HS + iq % HS
     bool ok = true;
     int pend_s[HS], pend_kb[HS];
     int n_pend = 0;
@@ -372,8 +429,26 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         tr2 = tr[2];
         tr3 = tr[3];
       }
+      // the first item's early k-blocks: their weight boxes are out; now
+      // their token boxes (FC1) or h boxes (FC2, listed until h is ready)
+      const int early = wi == (int)blockIdx.x ? n_early : 0;
+      for (int j = 0; j < early; ++j) {
+        const int s = q * HS + j, kb = q + 2 * j;
+        const uint32_t a_dst = smem_base + s * C::STAGE_BYTES;
+        if (it.fc1) {
+          if (tok_lane)
+            tma_gather4(a_dst + C::A_BYTES + lane * 512, &a.map_x, full_bar(s), kb * BK, tr0, tr1, tr2, tr3, pol_x);
+        } else if (dep_ok) {
+          if (lane == 0) tma_load_2d(a_dst + C::A_BYTES, &a.map_h, full_bar(s), kb * BK, xrow, pol_x);
+        } else {
+          pend_s[n_pend] = s;
+          pend_kb[n_pend] = kb;
+          ++n_pend;
+        }
+      }
       for (int kb = 0; kb < num_kb && ok; ++kb) {
         if ((kb & 1) != q) continue;
+        if (kb < q + 2 * early) continue;  // issued early
         if (!dep_ok && n_pend == HS) {  // the next slot holds a listed box
           finish();
           if (!ok) break;

@@ -411,6 +411,19 @@ def test_decode_chain_replays_bitwise_and_graph(name, one):
     assert np.array_equal(view("perm_to_exp", len(p2e_o)), p2e_o)
 
 
+@pytest.mark.parametrize("one", [False, True])
+@pytest.mark.parametrize("T", [1, 3])
+def test_decode_chain_repeated_ids(T, one):
+    """Pre-routed ids may repeat an expert inside a token's routes: every
+    route lands on expert 2, giving it 8 (T = 1) or 24 (T = 3, more than one
+    16-row block) rows; the chain still matches the oracle."""
+    wl = W.make_moe(T=T, H=256, I=192, E=16, top_k=8, mode="prerouted", seed=40 + T)
+    wl.topk_ids = torch.full_like(wl.topk_ids, 2)
+    out, _ = _forward(wl, _dev(wl), moe.PATH_DECODE, decode_chain=True, one_launch=one)
+    want, _ = _oracle_out(wl)
+    check_bf16_end_to_end(W.bf16_bits(out), want, f"repeated ids T={T}")
+
+
 def test_decode_one_launch_first_launch_captured():
     """A one-launch chain plan whose first launch is captured in a CUDA graph:
     the graph holds the zeroing of the plan's counters, and every replay gives
