@@ -91,3 +91,28 @@ def test_weight_banks_keep_every_step_in_hbm():
         else:
             assert n * active >= 3 * bench.L2_NOMINAL and (n - 1) * active < 3 * bench.L2_NOMINAL, name
     assert bench.weight_banks(Shape(1, 2048, 768, 128, 8)) == 6  # 8 experts x 9.4 MB
+
+
+def test_bench_accounting_matches_published_targets():
+    """The benchmark's algorithmic FLOPs and bytes for the default workload
+    (8 experts, all active; logits routing) equal the target table's
+    2.886 TFLOP and 2.886 GB, and the decode T=1 bytes (8 distinct experts,
+    pre-routed) its 75.5 MB."""
+    import numpy as np
+    import bench
+
+    class Shape:
+        def __init__(self, T, H, I, E, k, mode):
+            self.T, self.H, self.I, self.E, self.top_k, self.mode = T, H, I, E, k, mode
+            self.num_local, self.local_offset = E, 0
+
+    wl = Shape(4096, 4096, 14336, 8, 2, "logits")
+    ids = np.tile(np.arange(8, dtype=np.int32), 4096 * 2 // 8)
+    F = bench.layer_flops(len(ids), wl.H, wl.I)
+    B, active = bench.layer_bytes(wl, ids)
+    assert active == 8
+    assert abs(F / 1e12 - 2.886) < 0.0005
+    assert abs(B / 1e9 - 2.886) < 0.0005
+    wl = Shape(1, 2048, 768, 128, 8, "prerouted")
+    B, active = bench.layer_bytes(wl, np.array([3, 9, 17, 40, 41, 77, 100, 127], np.int32))
+    assert active == 8 and abs(B / 1e6 - 75.5) < 0.05
