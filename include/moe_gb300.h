@@ -126,8 +126,11 @@ MOE_API int moe_sort(const int32_t *topk_ids, int T, int top_k, int E, int local
  *   Limit: ceil(T*top_k / 4096) * num_local <= 262144 table entries (T*top_k
  *   <= 2048 uses no table at all); larger problems return MOE_ERR_WORKSPACE
  *   before anything is enqueued.
- *   The array's device address is looked up on the first call on each device,
- *   with that device current; make that first call before any stream capture.
+ *   The array's device address is looked up, with the calling device
+ *   current, on every call made outside stream capture; a call being captured
+ *   reuses the address of the last such lookup on its device, so make one call
+ *   on each device before any stream capture (a captured call without one
+ *   returns MOE_ERR_CUDA).
  *   All calls share the array: calls whose kernels overlap on the GPU (for
  *   example on two streams) race on it and must be serialised by the caller.
  *   The kernels write every entry they read, so no clearing is needed. */

@@ -107,7 +107,6 @@ struct moe_plan {
   SwapPlan fc1d, fc2d;  // decode path, separate kernels
   ChainPlan chain;      // decode path: the chain (one launch or two kernels)
   bool use_chain;
-  bool counters_zeroed;  // one-launch chain: its counters were zeroed before the first launch
   bool fused_gather;    // grouped path: FC1 gathers its rows itself
   bool timing;
   cudaEvent_t (*ev)[kNumStages + 1];
@@ -187,7 +186,8 @@ int moe_sort_no_alloc(const int32_t *topk_ids, int T, int top_k, int E, int loca
   if (R > 0 && (!topk_ids || !perm_to_exp || !exp_to_perm)) return MOE_ERR_NULL;
   if (int rc = check_device()) return rc;
   int32_t *scratch = nullptr;
-  if (need > 0 && static_sort_scratch(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
+  if (need > 0 && static_sort_scratch(static_cast<cudaStream_t>(stream), &scratch) != cudaSuccess)
+    return MOE_ERR_CUDA;
   return moe_sort(topk_ids, T, top_k, E, local_offset, num_local, m_indptr, perm_to_exp,
                   exp_to_perm, scratch, need * sizeof(int32_t), status, stream);
 }
@@ -463,9 +463,9 @@ int moe_plan_launch(moe_plan *p, void *stream) {
   if (!p) return MOE_ERR_NULL;
   const moe_forward_desc &d = p->d;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // the decode chain's first kernel clears the status word itself
-  if (d.status && (d.T == 0 || !p->use_chain) &&
-      cudaMemsetAsync(d.status, 0, sizeof(int32_t), s) != cudaSuccess)
+  // The status word is cleared on the stream before any kernel of the launch
+  // can OR a bit into it.
+  if (d.status && cudaMemsetAsync(d.status, 0, sizeof(int32_t), s) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (d.T == 0) return MOE_OK;
   Launch l;
@@ -480,10 +480,9 @@ int moe_plan_launch(moe_plan *p, void *stream) {
     if (launch_route(d.logits, d.T, d.E, d.top_k, p->ids, p->w, l) != cudaSuccess) return MOE_ERR_CUDA;
   }
   if (p->use_chain) {  // sort, gather and finalize run inside the GEMM kernels
-    if (p->chain.one_launch && !p->counters_zeroed) {
-      if (chain_zero_counters(p->chain, s) != cudaSuccess) return MOE_ERR_CUDA;
-      p->counters_zeroed = true;
-    }
+    // The one-launch kernel's counters live in the workspace, which other
+    // plans may share: every launch zeroes them first.
+    if (p->chain.one_launch && chain_zero_counters(p->chain, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (!mark(kSort) || !mark(kGather) || !mark(kFc1)) return MOE_ERR_CUDA;
     if (p->chain.one_launch) {
       if (launch_chain(p->chain, 0, l) != cudaSuccess) return MOE_ERR_CUDA;

@@ -9,8 +9,8 @@
 //
 //   FC1  the producer warp gathers the expert's token rows straight from x
 //        (four rows per TMA row-gather), the epilogue writes
-//        h[p] = bf16(silu(g) * u); the first CTA also clears the status word
-//        and publishes the sort (m_indptr, perm_to_exp, exp_to_perm).
+//        h[p] = bf16(silu(g) * u); the first CTA also publishes the sort
+//        (m_indptr, perm_to_exp, exp_to_perm).
 //   FC2  streams W2 (the first ring of weight boxes before h is ready),
 //        writes the unscaled fp32 rows y, and combines: every (token, 128-col
 //        block) has a counter; the tile that brings it to the token's number
@@ -22,8 +22,10 @@
 // first CTA zeroes the combine counters.  One launch: every CTA runs its FC1
 // tiles first and then its FC2 tiles; an FC2 tile loads h once the count of
 // finished FC1 tiles of its expert is complete (a bounded wait on a counter
-// that FC1 epilogues raise after their h stores), and the last CTA to finish
-// zeroes the counters for the next launch.  With at most one CTA per SM and
+// that FC1 epilogues raise after their h stores).  Every launch zeroes the
+// counters and clears the status word on its stream before the kernel starts
+// (chain_zero_counters), so no state carries over from another launch or from
+// another plan that shares the workspace.  With at most one CTA per SM and
 // no more CTAs than SMs, every CTA that others wait for has an SM, and FC1
 // tiles wait for nothing.
 //
@@ -64,7 +66,7 @@ struct ChainArgs {
   float *y;            // [R, H] fp32: FC2
   uint16_t *out;       // [T, H] bf16: FC2
   int32_t *comb;       // [T * m_tiles2] combine counters
-  int32_t *done1;      // one launch: [L] finished FC1 tiles per expert, then the exit counter
+  int32_t *done1;      // one launch: [L] finished FC1 tiles per expert
   int32_t *m_indptr_out, *p2e_out, *e2p_out;  // published by the first CTA of FC1
   int32_t *status;
   int T, k, E, off, L, H, I, m_tiles1, m_tiles2, ids_early;
@@ -221,7 +223,6 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
   volatile int *bad = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 8);
-  volatile int *last_cta = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 12);
   float *sg = reinterpret_cast<float *>(smem + C::SG_OFF);
   int *sflag = reinterpret_cast<int *>(smem + C::SG_OFF);  // FC2: last-arriver tokens [BNT]
   const int L = a.L, T = a.T, R = a.T * a.k;
@@ -536,10 +537,10 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
     const int etid = threadIdx.x - 64;  // 0..127
     if (blockIdx.x == 0) {
       if (MODE != kModeFc2) {
-        if (etid == 0 && a.status) {
-          *reinterpret_cast<volatile int32_t *>(a.status) = 0;
-          if (*bad) atomicOr(reinterpret_cast<unsigned int *>(a.status), MOE_DEV_BAD_EXPERT);
-        }
+        // the launch clears the status word on the stream before this kernel
+        // runs; a kernel only ORs bits into it
+        if (etid == 0 && a.status && *bad)
+          atomicOr(reinterpret_cast<unsigned int *>(a.status), MOE_DEV_BAD_EXPERT);
         for (int x = etid; x <= L; x += kEpiThreads) a.m_indptr_out[x] = m_indptr[x];
         for (int x = etid; x < R; x += kEpiThreads) {
           a.e2p_out[x] = e2p[x];
@@ -644,22 +645,6 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
   }
 
   __syncthreads();
-  if (MODE == kModeBoth) {
-    // The last CTA to get here resets the counters for the next launch: every
-    // other CTA has finished with them.
-    if (threadIdx.x == 0) {
-      __threadfence();
-      *last_cta = atomicAdd(a.done1 + L, 1) == (int)gridDim.x - 1 ? 1 : 0;
-    }
-    __syncthreads();
-    if (*last_cta) {
-      __threadfence();
-      for (int g = threadIdx.x; g < L; g += kThreads)
-        if (m_indptr[g + 1] > m_indptr[g]) a.done1[g] = 0;
-      for (int x = threadIdx.x; x < T * a.m_tiles2; x += kThreads) a.comb[x] = 0;
-      if (threadIdx.x == 0) a.done1[L] = 0;
-    }
-  }
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -773,6 +758,11 @@ int chain_prepare(ChainPlan &p) {
 }
 
 cudaError_t chain_zero_counters(const ChainPlan &p, cudaStream_t stream) {
+  // the plan lays out done1 right after comb, so one memset covers both
+  const char *lo = reinterpret_cast<const char *>(p.comb);
+  const char *hi = reinterpret_cast<const char *>(p.done1 + p.L + 1);
+  if (hi > lo && (size_t)(reinterpret_cast<const char *>(p.done1) - lo) < (1u << 20))
+    return cudaMemsetAsync(p.comb, 0, (size_t)(hi - lo), stream);
   cudaError_t e = cudaMemsetAsync(p.done1, 0, ((size_t)p.L + 1) * sizeof(int32_t), stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(p.comb, 0, chain_comb_ints(p.T, p.H) * sizeof(int32_t), stream);
   return e;

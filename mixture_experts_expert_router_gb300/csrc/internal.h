@@ -36,7 +36,7 @@ cudaError_t launch_sort(const int32_t *ids, long routes, int E, int off, int L, 
 
 // Library-owned scratch for the allocation-free sort (sort.cu).
 long static_sort_scratch_ints();
-cudaError_t static_sort_scratch(int32_t **out);
+cudaError_t static_sort_scratch(cudaStream_t stream, int32_t **out);
 
 // S3 / S6 -----------------------------------------------------------------------
 cudaError_t launch_gather(const uint16_t *x, const int32_t *p2e, const int32_t *m_total, int H,
@@ -133,7 +133,7 @@ struct ChainPlan {
   uint16_t *h = nullptr, *out = nullptr;
   float *y = nullptr;
   int32_t *comb = nullptr, *m_indptr = nullptr, *p2e = nullptr, *e2p = nullptr, *status = nullptr;
-  int32_t *done1 = nullptr;  // one launch: [L + 1] FC1 tile counts per expert, exit counter
+  int32_t *done1 = nullptr;  // one launch: [L + 1] FC1 tile counts per expert (last unused)
   int T = 0, k = 0, E = 0, off = 0, L = 0, H = 0, I = 0, bnt = 0, grid1 = 0, grid2 = 0, grid_one = 0;
   bool ids_early = false;  // ids are layer inputs (pre-routed), not the routing kernel's output
   bool one_launch = false; // FC1 and FC2 in one kernel (CTAs wait for the FC1 tiles of an expert)
@@ -143,8 +143,8 @@ size_t chain_comb_ints(int T, int H);
 int chain_prepare(ChainPlan &p);
 // part 1: FC1 kernel, 2: FC2 kernel, 0: both phases in one kernel
 cudaError_t launch_chain(const ChainPlan &p, int part, const Launch &l);
-// One launch keeps counters in the workspace that every launch leaves at
-// zero; before the first launch of a plan they are zeroed on its stream.
+// One launch keeps counters in the workspace; every launch zeroes them on its
+// stream before the kernel (one memset: done1 follows comb in the workspace).
 cudaError_t chain_zero_counters(const ChainPlan &p, cudaStream_t stream);
 
 }  // namespace moe

@@ -426,8 +426,8 @@ def test_decode_chain_repeated_ids(T, one):
 
 def test_decode_one_launch_first_launch_captured():
     """A one-launch chain plan whose first launch is captured in a CUDA graph:
-    the graph holds the zeroing of the plan's counters, and every replay gives
-    the oracle's output."""
+    the graph holds the zeroing of the kernel's counters (every launch zeroes
+    them), and every replay gives the oracle's output."""
     wl = W.make_moe(T=2, H=256, I=192, E=16, top_k=4, mode="prerouted", seed=31)
     d = _dev(wl)
     plan = moe.MoEPlan(d["x"], d["w1"], d["w2"], wl.E, wl.top_k, topk_ids=d["topk_ids"], topk_w=d["topk_w"],
@@ -446,6 +446,32 @@ def test_decode_one_launch_first_launch_captured():
     plan.launch()  # and a direct launch after the replays
     torch.cuda.synchronize()
     check_bf16_end_to_end(W.bf16_bits(plan.out), want, "launch after replays")
+
+
+def test_plans_sharing_one_workspace_alternate():
+    """A grouped-path plan and a one-launch decode plan bound to the same
+    workspace, launched alternately: the grouped path's rows overwrite the
+    bytes where the decode kernel keeps its counters, and every launch still
+    gives the oracle's output with a clean status word."""
+    wl_g = W.make_moe(T=600, H=256, I=192, E=12, top_k=3, mode="logits", seed=61)
+    wl_d = W.make_moe(T=3, H=256, I=192, E=12, top_k=4, mode="prerouted", seed=62)
+    need = max(moe.moe_workspace_size(wl.T, wl.H, wl.I, wl.E, wl.top_k, wl.num_local) for wl in (wl_g, wl_d))
+    ws = torch.empty(need, dtype=torch.uint8, device=DEV)
+    plans = []
+    for wl, path, one in ((wl_g, moe.PATH_GROUPED, False), (wl_d, moe.PATH_DECODE, True)):
+        d = _dev(wl)
+        st = torch.full((1,), 0x40, dtype=torch.int32, device=DEV)
+        p = moe.MoEPlan(d["x"], d["w1"], d["w2"], wl.E, wl.top_k, logits=d["logits"], topk_ids=d["topk_ids"],
+                        topk_w=d["topk_w"], workspace=ws, status=st, path=path, decode_one_launch=one)
+        plans.append((wl, p, _oracle_out(wl)[0]))
+    assert plans[1][1].kernels_per_launch() == 1
+    for rnd in range(3):
+        for wl, p, want in (plans[1], plans[0]) if rnd % 2 == 0 else plans:
+            p.out.fill_(3.0)
+            p.launch()
+            torch.cuda.synchronize()
+            assert int(p.status.item()) == 0
+            check_bf16_end_to_end(W.bf16_bits(p.out), want, f"shared workspace {wl.name} T={wl.T} round {rnd}")
 
 
 @pytest.mark.parametrize("one", [False, True])
