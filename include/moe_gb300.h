@@ -249,12 +249,13 @@ MOE_API int moe_forward(const moe_bf16 *x, const float *logits, const int32_t *t
  * moe_forward_prepare validates the descriptor, lays out the workspace and
  * encodes the TMA tensor maps (host memory only).  moe_plan_launch then only
  * enqueues work: no allocation, no host synchronisation, capturable in a
- * CUDA graph, and valid for new VALUES written into the bound buffers.  (For
- * the decode chain in one launch, a plan's first launch also zeroes the
- * counters that the kernel keeps in the workspace, with cudaMemsetAsync on
- * the launch stream; every launch leaves them at zero.)  The workspace is every
- * launch's scratch: launches of one plan (or of plans sharing a workspace)
- * must run one after another (one stream, or streams ordered by events).
+ * CUDA graph, and valid for new VALUES written into the bound buffers.  Every
+ * launch first clears the status word (if given) with cudaMemsetAsync on the
+ * launch stream; for the decode chain in one launch it also zeroes, the same
+ * way, the counters that the kernel keeps in the workspace, so plans may share
+ * a workspace.  The workspace is every launch's scratch: launches of one plan
+ * (or of plans sharing a workspace) must run one after another (one stream,
+ * or streams ordered by events).
  */
 #define MOE_PATH_AUTO 0    /* decided from the shape                         */
 #define MOE_PATH_GROUPED 1 /* route/sort/gather + tcgen05 grouped GEMMs       */

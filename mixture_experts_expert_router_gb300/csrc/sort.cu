@@ -256,10 +256,11 @@ cudaError_t launch_sort(const int32_t *ids, long routes, int E, int off, int L, 
 // fixed array in the library's own device memory instead, so the caller passes
 // only inputs and outputs.  The array is kStaticSortScratchInts int32 (1 MiB)
 // and exists on every device that loads the library until the process exits.
-// Its address is looked up once per device (the first call on that device,
-// with the device current).  Every call shares the array; the kernels write
-// every entry they later read, so nothing has to be cleared between calls,
-// but two calls whose kernels overlap on the GPU race on it.
+// Its address is looked up with the device current on every call outside
+// stream capture (the first call on a device must come before any capture).
+// Every call shares the array; the kernels write every entry they later read,
+// so nothing has to be cleared between calls, but two calls whose kernels
+// overlap on the GPU race on it.
 #include <mutex>
 
 namespace moe {
@@ -275,18 +276,28 @@ int32_t *g_scratch_addr[kMaxDevices] = {};
 long static_sort_scratch_ints() { return kStaticSortScratchInts; }
 
 // Device address of the scratch array on the current device (host code must
-// not pass the symbol itself: on the host it is only a stand-in).
-cudaError_t static_sort_scratch(int32_t **out) {
+// not pass the symbol itself: on the host it is only a stand-in).  Outside
+// stream capture the address is looked up on every call, so a context that was
+// destroyed and created again (cudaDeviceReset) never leaves a stale address
+// behind; during capture, where a first lookup could load the module, the
+// address of the last lookup on this device is used (the header asks for a
+// first call before any capture).
+cudaError_t static_sort_scratch(cudaStream_t stream, int32_t **out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  e = cudaStreamIsCapturing(stream, &cap);
+  if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
+  if (cap == cudaStreamCaptureStatusNone) {
     void *p = nullptr;
     e = cudaGetSymbolAddress(&p, g_sort_scratch);
     if (e != cudaSuccess) return e;
     g_scratch_addr[dev] = static_cast<int32_t *>(p);
+  } else if (!g_scratch_addr[dev]) {
+    return cudaErrorStreamCaptureUnsupported;
   }
   *out = g_scratch_addr[dev];
   return cudaSuccess;

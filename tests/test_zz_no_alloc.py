@@ -5,8 +5,9 @@ hands it only its input and output buffers, or a runtime that plans all device
 memory at start-up and forbids allocating later.  moe_sort_no_alloc serves
 them by keeping the sort's scratch table in a fixed array inside the library.
 These tests call it through the C ABI and check that it gives exactly what
-moe_sort (the workspace-taking entry point) gives, on two calls in a row, so
-that the shared array carries nothing over from one call to the next.
+moe_sort (the workspace-taking entry point) gives, and exactly what the CPU
+oracle's sort gives, on two calls in a row, so that the shared array carries
+nothing over from one call to the next.
 
 This file is collected last on purpose: if it fails, a run that stops at the
 first failure has already run every other test.
@@ -16,6 +17,7 @@ import pytest
 import torch
 
 import mixture_experts_expert_router_gb300 as moe
+import oracle
 
 
 def _ids(seed, T, k, E, skew):
@@ -59,6 +61,12 @@ def test_no_alloc_sort_matches_workspace_sort_twice_in_a_row():
         assert torch.equal(p2e_n[:M], p2e_w.cpu()[:M])
         assert torch.equal(e2p_n, e2p_w.cpu())
         assert int(st_n.item()) == int(st_w.item()) == 0
+        # and bit-exact against the oracle's stable counting sort
+        m_o, p2e_o, e2p_o, st_o = oracle.sort(ids.numpy(), E, off, L)
+        assert np.array_equal(m_n.numpy(), m_o)
+        assert np.array_equal(p2e_n[:M].numpy(), p2e_o)
+        assert np.array_equal(e2p_n.numpy(), e2p_o)
+        assert st_o == 0
 
 
 def test_no_alloc_sort_rejects_problems_beyond_its_table():
