@@ -8,7 +8,8 @@ import torch
 import mixture_experts_expert_router_gb300 as moe
 import oracle
 from mixture_experts_expert_router_gb300 import workloads as W
-from tests.tolerances import check_bf16_close, check_bf16_end_to_end
+from tests import accum_model
+from tests.tolerances import check_bf16_close, check_bf16_end_to_end, with_floor
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -33,12 +34,17 @@ def _oracle_route(wl):
 
 
 def _oracle_out(wl, tokens=None, w1=None, w2=None):
+    """The oracle's output rows for the tokens, with the end-to-end floor (the
+    tensor-core accumulation model's agreement with them) attached."""
     ids, w = _oracle_route(wl)
     w1 = W.bf16_bits(wl.w1) if w1 is None else w1
     w2 = W.bf16_bits(wl.w2) if w2 is None else w2
-    out, st = oracle.moe_tokens(W.bf16_bits(wl.x), ids, w, w1, w2, wl.E, tokens=tokens,
+    x = W.bf16_bits(wl.x)
+    out, st = oracle.moe_tokens(x, ids, w, w1, w2, wl.E, tokens=tokens,
                                 local_offset=wl.local_offset, num_local=wl.num_local)
-    return out, st
+    frac, n = accum_model.floor(x, ids, w, w1, w2, wl.E, out, tokens=tokens, local_offset=wl.local_offset,
+                                num_local=wl.num_local)
+    return with_floor(out, frac, n), st
 
 
 def _forward(wl, d, path=moe.PATH_AUTO, status=None, one_cta_gemm=False, decode_chain=False,

@@ -8,16 +8,22 @@ applies to every stage fed the oracle's own intermediate.  Routing weights:
 within 1e-6 absolute.
 
 End to end, from the layer inputs (check_bf16_end_to_end): the same per-element
-max bound; the 2-ulp fraction is reported and only guarded against gross
-errors (>= 98%).  Why: h is rounded to bf16 before GEMM2, so every fp32
-disagreement that moves an h value across a rounding boundary (0.07% of h
-values for the sequential oracle against exact arithmetic, 0.46% for the
-tensor cores) is seen again in every output element that h value feeds, and
-an output close to zero has a tiny ulp.  Two fp32 CPU implementations that
-only sum in a different order (sequential vs blocked) already agree on just
-99.88% of the outputs within 2 ulp at hidden 4096 / intermediate 14336, so no
-implementation can promise 99.9% against the oracle end to end; stage by
-stage, with the oracle's h as input, the rule holds and is enforced.
+max bound, and a 2-ulp fraction at least the FLOOR that a model of tensor-core
+accumulation reaches against the oracle on the same inputs, less a stated
+margin.  Why not 99.9% end to end: h is rounded to bf16 before GEMM2, so any
+fp32 disagreement that moves an h value across a rounding boundary is seen
+again in every output element that h value feeds, and an output close to zero
+has a tiny ulp.  A correct fp32 evaluation that only sums in blocks of 16
+(tests/accum_model.c, mode 0) already agrees with the oracle on just 99.74% /
+99.84% of the outputs within 2 ulp at hidden 4096 / intermediate 14336 and at
+hidden 7168 / intermediate 2048 (pinned in test_e2e_floor.py).  The floor
+comes from the same layer evaluated with a tensor-core accumulation model
+(blocks of 16 products aligned to the largest magnitude, two guard bits,
+truncation), computed by the caller on (a subset of) the test's own tokens
+and attached to the oracle's bits with with_floor(); the margin is 0.001 plus
+four binomial standard deviations of that fraction (floor_margin).  Stage by
+stage, with the oracle's own intermediate as input, the 99.9% rule holds and
+is enforced.
 
 Why the extra ulp: both sides round their own fp32 result to bf16 once, and
 fp32 sums taken in a different order straddle a bf16 rounding boundary now
@@ -77,10 +83,36 @@ def check_bf16_close(got_bits: np.ndarray, want_bits: np.ndarray, what: str = "o
     return ratio, frac
 
 
-def check_bf16_end_to_end(got_bits: np.ndarray, want_bits: np.ndarray, what: str = "output",
-                          guard: float = 0.98):
-    """End-to-end rule: per-element max bound as in check_bf16_close, 2-ulp
-    fraction reported (returned) and guarded at `guard`."""
+class OracleBits(np.ndarray):
+    """The oracle's bf16 output bits with the end-to-end floor attached:
+    ``floor`` = (fraction within 2 ulp that the accumulation model reaches
+    against the oracle, number of elements it was measured on)."""
+
+    def __array_finalize__(self, obj):
+        self.floor = getattr(obj, "floor", None)
+
+
+def with_floor(bits: np.ndarray, frac: float, n: int) -> OracleBits:
+    out = np.asarray(bits).view(OracleBits)
+    out.floor = (float(frac), int(n))
+    return out
+
+
+def floor_margin(frac: float, n: int) -> float:
+    """Allowance below a floor measured on n elements: 0.001 plus four binomial
+    standard deviations of the fraction over n elements (the GPU and the model
+    see the same inputs but make their own rounding errors)."""
+    if n <= 0:
+        return 1.0
+    return 1e-3 + 4.0 * float(np.sqrt(max(frac * (1.0 - frac), 1.0 / n) / n))
+
+
+def check_bf16_end_to_end(got_bits: np.ndarray, want_bits: np.ndarray, what: str = "output"):
+    """End-to-end rule: per-element max bound as in check_bf16_close, and the
+    2-ulp fraction at least the attached floor less floor_margin.  Returns the
+    fraction."""
+    floor = getattr(want_bits, "floor", None)
+    assert floor is not None, f"{what}: end-to-end check without an accumulation-model floor"
     got = bf16_to_f64(got_bits)
     want = bf16_to_f64(want_bits)
     assert got.shape == want.shape, (got.shape, want.shape)
@@ -93,8 +125,11 @@ def check_bf16_end_to_end(got_bits: np.ndarray, want_bits: np.ndarray, what: str
     assert excess.flat[worst] <= 0, (f"{what}: |diff| {abs(got.flat[worst] - want.flat[worst])} at "
                                      f"{want.flat[worst]} exceeds 1e-2*rms ({RMS_FRAC * rms}) + 1 ulp")
     frac = float(np.mean(ulp_distance(got_bits, want_bits) <= ULP_MAX))
-    print(f"[{what}] end-to-end fraction within {ULP_MAX} bf16 ulp: {frac:.5f}")
-    assert frac >= guard, f"{what}: only {frac:.5f} within {ULP_MAX} ulp (guard {guard})"
+    f_model, n_model = floor
+    need = f_model - floor_margin(f_model, n_model)
+    print(f"[{what}] end-to-end fraction within {ULP_MAX} bf16 ulp: {frac:.5f} "
+          f"(accumulation model {f_model:.5f} on {n_model} elements, floor {need:.5f})")
+    assert frac >= need, f"{what}: only {frac:.5f} within {ULP_MAX} ulp (floor {need:.5f})"
     return frac
 
 
