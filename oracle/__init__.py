@@ -60,9 +60,9 @@ def _declare(lib):
     lib.oracle_route.restype = None
     lib.oracle_sort.argtypes = [P, i, i, i, i, i, P, P, P]
     lib.oracle_sort.restype = i
-    lib.oracle_moe_tokens.argtypes = [P, P, P, P, P, i, i, i, i, i, i, i, P, i, P, P, P, i]
+    lib.oracle_moe_tokens.argtypes = [P, P, P, P, P, i, i, i, i, i, i, i, P, i, P, P, P, i, P]
     lib.oracle_moe_tokens.restype = i
-    lib.oracle_fc1_swiglu_rows.argtypes = [P, P, P, i, i, i, P, i, P, i]
+    lib.oracle_fc1_swiglu_rows.argtypes = [P, P, P, i, i, i, P, i, P, i, P]
     lib.oracle_fc1_swiglu_rows.restype = None
     lib.oracle_fc2_rows.argtypes = [P, P, P, i, i, i, P, i, P, i]
     lib.oracle_fc2_rows.restype = None
@@ -122,10 +122,11 @@ def sort(ids: np.ndarray, num_experts: int, local_offset: int = 0, num_local: in
 
 
 def moe_tokens(x, ids, w, w1, w2, num_experts, tokens=None, local_offset=0, num_local=None,
-               want_intermediates=False, nthreads=0, lib=None):
+               want_intermediates=False, nthreads=0, lib=None, clamp_limit=None):
     """Full layer for the selected tokens.
 
-    x [T,H] u16(bf16); ids/w [T,k]; w1 [L,2I,H] u16; w2 [L,H,I] u16.
+    x [T,H] u16(bf16); ids/w [T,k]; w1 [L,2I,H] u16; w2 [L,H,I] u16;
+    clamp_limit [L] fp32 per local expert (SwiGLUStep) or None (SwiGLU).
     Returns out [n_tok, H] u16 (and h [n_tok*k, I] u16, y [n_tok*k, H] f32 when asked), status."""
     lib = lib or load()
     x = _c(x, np.uint16)
@@ -147,14 +148,17 @@ def moe_tokens(x, ids, w, w1, w2, num_experts, tokens=None, local_offset=0, num_
     if want_intermediates:
         h = np.zeros((n * k, I), np.uint16)
         y = np.zeros((n * k, H), np.float32)
+    clamp = None if clamp_limit is None else _c(clamp_limit, np.float32)
+    assert clamp is None or clamp.shape == (L,)
     st = lib.oracle_moe_tokens(_p(x), _p(ids), _p(w), _p(w1), _p(w2), T, H, I, num_experts, k,
-                               local_offset, L, _p(tokens), n, _p(out), _p(h), _p(y), nthreads)
+                               local_offset, L, _p(tokens), n, _p(out), _p(h), _p(y), nthreads, _p(clamp))
     if want_intermediates:
         return out, h, y, st
     return out, st
 
 
-def fc1_swiglu_rows(xp, w1, group_end, rows, nthreads=0, lib=None):
+def fc1_swiglu_rows(xp, w1, group_end, rows, nthreads=0, lib=None, clamp_limit=None):
+    """h rows (bf16 bits) of FC1 + SwiGLU (SwiGLUStep with clamp_limit [L])."""
     lib = lib or load()
     xp = _c(xp, np.uint16)
     w1 = _c(w1, np.uint16)
@@ -163,7 +167,10 @@ def fc1_swiglu_rows(xp, w1, group_end, rows, nthreads=0, lib=None):
     L, twoI, H = w1.shape
     I = twoI // 2
     out = np.empty((rows.shape[0], I), np.uint16)
-    lib.oracle_fc1_swiglu_rows(_p(xp), _p(w1), _p(ge), L, H, I, _p(rows), rows.shape[0], _p(out), nthreads)
+    clamp = None if clamp_limit is None else _c(clamp_limit, np.float32)
+    assert clamp is None or clamp.shape == (L,)
+    lib.oracle_fc1_swiglu_rows(_p(xp), _p(w1), _p(ge), L, H, I, _p(rows), rows.shape[0], _p(out), nthreads,
+                               _p(clamp))
     return out
 
 

@@ -22,6 +22,9 @@
  *   [P2] "flashinfer.fused_moe.cake / cake_cute (MXFP4 SiTU routed MoE)",
  *        "Host plan": the canonical W1 bank holds the up rows, then the gate
  *        rows ([up | gate]).
+ *   [P1] same page, opening paragraph and "Unified MoE API opt-in": the
+ *        StepFun activation SwiGLUStep(limit) with a per-expert clamp limit
+ *        (gemm1_clamp_limit).
  *   [P3] "Cake ragged BF16 grouped GEMM (experimental)", operation table:
  *        Y[offs[e-1]:offs[e]] = X[offs[e-1]:offs[e]] . W[e]^T, offs holding
  *        cumulative group end offsets, groups may be empty.
@@ -39,6 +42,10 @@
  *   - the renormalised weight of slot j is exp(l_j - l_0) / sum_i exp(l_i - l_0)
  *     over the chosen k only (the full softmax denominator cancels);
  *   - silu(g) = g / (1 + exp(-g)) in fp32; u and g are not rounded, h is;
+ *   - SwiGLUStep(limit) clamps GEMM1's two outputs before the activation:
+ *     the gate from above at limit, the up projection to [-limit, limit];
+ *     h = bf16(silu(min(g, limit)) * clamp(u, -limit, limit)), limit taken
+ *     per local expert; no limit (or +inf) is the plain SwiGLU;
  *   - the unscaled GEMM2 rows y stay fp32;
  *   - the pre-routed mode takes ids and weights as given (the caller
  *     normalised them); ids outside [0, E) are dropped and flagged.
@@ -163,13 +170,32 @@ int oracle_sort(const int32_t *ids, int T, int k, int E, int off, int L,
     return status;
 }
 
+/* ---- SwiGLU and SwiGLUStep(limit)  [P4 formula; P1 SwiGLUStep reading] ----
+ *
+ * silu(g) * u in fp32 after clamping g from above at `limit` and u to
+ * [-limit, limit]; with limit = +inf both comparisons are false and this is
+ * the plain SwiGLU of the summary formula. */
+static float swiglu_step(float g, float u, float limit) {
+    if (g > limit) g = limit;
+    if (u > limit) u = limit;
+    if (u < -limit) u = -limit;
+    float silu_g = g / (1.0f + expf(-g));
+    return silu_g * u;
+}
+
+/* per-expert limit of local expert e, +inf without limits */
+static float limit_of(const float *clamp, int e) {
+    return clamp ? clamp[e] : INFINITY;
+}
+
 /* ---- one expert's FFN on one row  [P4 formula; P2 host plan for W1 rows] --
  *
  * x_row [H] bf16; w1e [2I, H] bf16 with rows 0..I-1 = up, I..2I-1 = gate;
- * w2e [H, I] bf16.  Writes h [I] bf16 and y [H] fp32 (unscaled, unrounded). */
+ * w2e [H, I] bf16; limit the expert's SwiGLUStep clamp (+inf: none).
+ * Writes h [I] bf16 and y [H] fp32 (unscaled, unrounded). */
 static void expert_ffn_row(const uint16_t *x_row, const uint16_t *w1e,
-                           const uint16_t *w2e, int H, int I, uint16_t *h,
-                           float *y) {
+                           const uint16_t *w2e, int H, int I, float limit,
+                           uint16_t *h, float *y) {
     for (int n = 0; n < I; ++n) {
         const uint16_t *up_row = w1e + (size_t)n * H;
         const uint16_t *gate_row = w1e + (size_t)(I + n) * H;
@@ -179,8 +205,7 @@ static void expert_ffn_row(const uint16_t *x_row, const uint16_t *w1e,
             u = u + xv * bf16_to_float(up_row[c]);
             g = g + xv * bf16_to_float(gate_row[c]);
         }
-        float silu_g = g / (1.0f + expf(-g));
-        h[n] = float_to_bf16(silu_g * u);
+        h[n] = float_to_bf16(swiglu_step(g, u, limit));
     }
     for (int c = 0; c < H; ++c) {
         const uint16_t *w2_row = w2e + (size_t)c * I;
@@ -198,13 +223,15 @@ static void expert_ffn_row(const uint16_t *x_row, const uint16_t *w1e,
  * evaluate; out [n_tok, H] bf16 row i belongs to token tokens[i].
  * Optional h_out [n_tok*k, I] bf16 and y_out [n_tok*k, H] fp32 receive the
  * per-route intermediates in (token, slot) order; rows of routes that are not
- * local are left untouched.  Returns ORACLE_BAD_EXPERT if any selected route
- * has an id outside [0, E). */
+ * local are left untouched.  clamp [L] (or NULL) holds each local expert's
+ * SwiGLUStep limit.  Returns ORACLE_BAD_EXPERT if any selected route has an
+ * id outside [0, E). */
 int oracle_moe_tokens(const uint16_t *x, const int32_t *ids, const float *w,
                       const uint16_t *w1, const uint16_t *w2, int T, int H,
                       int I, int E, int k, int off, int L,
                       const int32_t *tokens, int n_tok, uint16_t *out,
-                      uint16_t *h_out, float *y_out, int nthreads) {
+                      uint16_t *h_out, float *y_out, int nthreads,
+                      const float *clamp) {
     (void)T;
     int status = 0;
     set_threads(nthreads);
@@ -221,8 +248,8 @@ int oracle_moe_tokens(const uint16_t *x, const int32_t *ids, const float *w,
             local[j] = 1;
             const uint16_t *w1e = w1 + (size_t)(e - off) * 2 * I * H;
             const uint16_t *w2e = w2 + (size_t)(e - off) * H * I;
-            expert_ffn_row(x + (size_t)t * H, w1e, w2e, H, I, h,
-                           y + (size_t)j * H);
+            expert_ffn_row(x + (size_t)t * H, w1e, w2e, H, I,
+                           limit_of(clamp, e - off), h, y + (size_t)j * H);
             if (h_out)
                 memcpy(h_out + ((size_t)i * k + j) * I, h, sizeof(uint16_t) * I);
             if (y_out)
@@ -254,11 +281,11 @@ static int group_of_row(const int32_t *group_end, int L, int p) {
 }
 
 /* FC1 + SwiGLU on selected permuted rows: xp [*, H] bf16, w1 [L, 2I, H],
- * rows[n_rows] -> h_rows [n_rows, I] bf16. */
+ * rows[n_rows] -> h_rows [n_rows, I] bf16; clamp [L] or NULL as above. */
 void oracle_fc1_swiglu_rows(const uint16_t *xp, const uint16_t *w1,
                             const int32_t *group_end, int L, int H, int I,
                             const int32_t *rows, int n_rows, uint16_t *h_rows,
-                            int nthreads) {
+                            int nthreads, const float *clamp) {
     set_threads(nthreads);
 #pragma omp parallel for schedule(dynamic, 1)
     for (int q = 0; q < n_rows; ++q) {
@@ -273,8 +300,8 @@ void oracle_fc1_swiglu_rows(const uint16_t *xp, const uint16_t *w1,
                 u = u + xv * bf16_to_float(w1e[(size_t)n * H + c]);
                 gt = gt + xv * bf16_to_float(w1e[(size_t)(I + n) * H + c]);
             }
-            float silu_g = gt / (1.0f + expf(-gt));
-            h_rows[(size_t)q * I + n] = float_to_bf16(silu_g * u);
+            h_rows[(size_t)q * I + n] =
+                float_to_bf16(swiglu_step(gt, u, limit_of(clamp, g)));
         }
     }
 }

@@ -36,6 +36,11 @@ MUTANTS = {
                        "int p = m_indptr[e - off + 1] - 1 - (next[e - off]++ - m_indptr[e - off]);")],
     "sort_offsets_off_by_one": [("for (int i = 0; i < L; ++i) m_indptr[i + 1] = m_indptr[i] + cnt[i];",
                                  "for (int i = 0; i < L; ++i) m_indptr[i + 1] = m_indptr[i] + cnt[i] + (i == 0);")],
+    "step_clamps_gate_below": [("    if (g > limit) g = limit;\n",
+                                "    if (g > limit) g = limit;\n    if (g < -limit) g = -limit;\n")],
+    "step_up_clamped_above_only": [("    if (u < -limit) u = -limit;\n", "")],
+    "step_limit_by_global_id": [("limit_of(clamp, e - off), h, y + (size_t)j * H);",
+                                 "limit_of(clamp, e), h, y + (size_t)j * H);")],
     "finalize_skips_slot0": [("            for (int j = 0; j < k; ++j) {\n                int p = exp_to_perm[(size_t)t * k + j];",
                               "            for (int j = 1; j < k; ++j) {\n                int p = exp_to_perm[(size_t)t * k + j];")],
 }
@@ -51,6 +56,9 @@ PIN_CALLS = [
     ("stages_compose", lambda: pins.test_stage_functions_compose_to_layer()),
     ("grouped_gemm", lambda: pins.test_grouped_gemm_vs_torch_per_group()),
     ("rounding", lambda: pins.test_bf16_rounding_matches_torch()),
+    ("step_hand_worked", lambda: pins.test_swiglu_step_hand_worked()),
+    ("step_fp64", lambda: pins.test_swiglu_step_fp64_bruteforce_tiny()),
+    ("step_per_expert", lambda: pins.test_swiglu_step_infinite_limit_is_plain_swiglu_and_limits_are_per_local_expert()),
 ]
 
 

@@ -337,6 +337,103 @@ def test_stage_functions_compose_to_layer():
     assert np.array_equal(out, ref)
 
 
+# ------------------------------------------------------- SwiGLUStep(limit) --
+# Reading of "SwiGLUStep(limit) with a per-expert clamp limit"
+# (flashinfer.experimental.cake_stepfun_moe, opening paragraph; Unified MoE API
+# opt-in, gemm1_clamp_limit): GEMM1's gate output is clamped from above at the
+# expert's limit and its up output to [-limit, limit] before silu(g) * u.
+
+def _bits_exact(vals):
+    a = np.asarray(vals, np.float32).view(np.uint32)
+    assert np.all(a & 0xFFFF == 0)
+    return (a >> 16).astype(np.uint16)
+
+
+def test_swiglu_step_hand_worked():
+    """x = e_0 and W1's column 0 carry (u, g) pairs exactly; W2 = identity
+    passes h through to the output (one route of weight 1)."""
+    H = I = 64
+    gs = [-9.0, -2.0, 0.0, 3.0, 6.5, 7.0, 8.0, 20.0]
+    us = [-100.0, -7.5, -1.0, 0.5, 6.5, 7.0, 7.5, 100.0]
+    pairs = [(g, u) for g in gs for u in us][:I]
+    x = np.zeros((1, H), np.uint16)
+    x[0, 0] = _bits_exact([1.0])[0]
+    w1 = np.zeros((1, 2 * I, H), np.uint16)
+    w1[0, :I, 0] = _bits_exact([u for _, u in pairs])
+    w1[0, I:, 0] = _bits_exact([g for g, _ in pairs])
+    w2 = np.zeros((1, H, I), np.uint16)
+    w2[0, np.arange(H), np.arange(I)] = _bits_exact([1.0])[0]
+    ids = np.zeros((1, 1), np.int32)
+    w = np.ones((1, 1), np.float32)
+    for limit in (7.0, 0.75):
+        out, st = oracle.moe_tokens(x, ids, w, w1, w2, 1, clamp_limit=np.array([limit], np.float32))
+        assert st == 0
+        want = []
+        for g, u in pairs:
+            gc = min(g, limit)
+            uc = min(max(u, -limit), limit)
+            want.append(gc / (1.0 + math.exp(-gc)) * uc)
+        # the oracle's fp32 silu may differ from fp64 by an fp32 rounding: the
+        # bf16 results agree within one ulp and almost always exactly
+        ulp = ulp_distance(out[0], torch_bf16_bits(np.array(want)))
+        assert np.all(ulp <= 1) and np.mean(ulp == 0) >= 0.95, (limit, ulp)
+        # the clamp binds: g = 20 gives silu(limit) * u, not silu(20) * u
+        i = pairs.index((20.0, 0.5))
+        want_i = limit / (1 + math.exp(-limit)) * min(0.5, limit)
+        assert abs(bf16_to_f64(out[0, i:i + 1])[0] - want_i) < 0.01 * want_i
+
+
+def test_swiglu_step_fp64_bruteforce_tiny():
+    """The whole layer with per-expert limits against an fp64 dense masked
+    evaluation (h and out within one bf16 ulp, nearly all exact)."""
+    wl = W.make_moe("tiny")
+    x, w1, w2 = W.bf16_bits(wl.x), W.bf16_bits(wl.w1), W.bf16_bits(wl.w2)
+    ids, w = oracle.route(wl.logits.numpy(), wl.top_k)
+    limits = np.array([0.25, 0.6, 1.0, 50.0], np.float32)
+    out, h, y, st = oracle.moe_tokens(x, ids, w, w1, w2, wl.E, want_intermediates=True, clamp_limit=limits)
+    assert st == 0
+    G, u, g = _dense_masked_fp64(x, ids, w, w1, w2, wl.E)
+    T, k, H = wl.T, wl.top_k, wl.H
+    w2_64 = bf16_to_f64(w2)
+    n_exact, Y = 0, np.zeros((T, wl.E, H))
+    for t in range(T):
+        for j in range(k):
+            e = ids[t, j]
+            lim = float(limits[e])
+            gc = np.minimum(g[t, e], lim)
+            uc = np.clip(u[t, e], -lim, lim)
+            ulp = ulp_distance(h[t * k + j], torch_bf16_bits(gc / (1.0 + np.exp(-gc)) * uc))
+            assert np.all(ulp <= 1)
+            n_exact += int(np.sum(ulp == 0))
+            Y[t, e] = w2_64[e] @ bf16_to_f64(h[t * k + j])
+    assert n_exact >= 0.99 * T * k * wl.I
+    want = torch_bf16_bits(np.einsum("te,teh->th", G, Y))
+    assert np.all(ulp_distance(out, want) <= 1) and np.mean(ulp_distance(out, want) == 0) >= 0.99
+
+
+def test_swiglu_step_infinite_limit_is_plain_swiglu_and_limits_are_per_local_expert():
+    wl = W.make_moe(T=40, H=64, I=64, E=5, top_k=1, mode="logits", seed=8)
+    x, w1, w2 = W.bf16_bits(wl.x), W.bf16_bits(wl.w1), W.bf16_bits(wl.w2)
+    ids, w = oracle.route(wl.logits.numpy(), 1)
+    plain, _ = oracle.moe_tokens(x, ids, w, w1, w2, 5)
+    inf, _ = oracle.moe_tokens(x, ids, w, w1, w2, 5, clamp_limit=np.full(5, np.inf, np.float32))
+    assert np.array_equal(plain, inf)
+    # shard of local experts 2..4 with limits (0.3, 1.5, inf): a token's row
+    # equals the row computed with its own expert's limit everywhere
+    off, L = 2, 3
+    lims = np.array([0.3, 1.5, np.inf], np.float32)
+    sl = slice(off, off + L)
+    out, _ = oracle.moe_tokens(x, ids, w, w1[sl], w2[sl], 5, local_offset=off, num_local=L, clamp_limit=lims)
+    changed = 0
+    for i in range(L):
+        ref, _ = oracle.moe_tokens(x, ids, w, w1[sl], w2[sl], 5, local_offset=off, num_local=L,
+                                   clamp_limit=np.full(L, lims[i], np.float32))
+        rows = ids[:, 0] == off + i
+        assert np.array_equal(out[rows], ref[rows])
+        changed += int(not np.array_equal(out[rows], plain[rows]))
+    assert changed >= 2  # the two finite limits bind on these inputs
+
+
 # ------------------------------------------------------------ grouped GEMM --
 
 def test_grouped_gemm_vs_torch_per_group():
