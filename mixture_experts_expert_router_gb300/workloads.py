@@ -14,6 +14,7 @@ Distributions (one independent stream per tensor, derived from ``seed``):
            Dirichlet draw (positive, summing to 1), both per token.
   grouped GEMM sizes: Dirichlet(alpha * 1_E) proportions of sum_m, floored,
            the remainder handed to the largest fractional parts.
+  grouped GEMM upstream gradient G ~ N(0, 1)  bf16 [sum_m, N] (backward).
 
 Small tensors are drawn on the host with numpy's PCG64 generator (the same
 stream on every platform) and converted to bf16 by round-to-nearest-even.
@@ -147,9 +148,10 @@ def grouped_sizes(sum_m: int, E: int, alpha: float, seed: int) -> np.ndarray:
 
 
 def make_grouped_gemm(*, seed: int = 0, device="cpu", weights_device=None, sum_m=None, E=None, K=None,
-                      N=None, alpha=None, sizes=None) -> dict:
+                      N=None, alpha=None, sizes=None, with_grad: bool = False) -> dict:
     """Inputs of the ragged grouped GEMM: X [sum_m, K], W [E, N, K], offs [E]
-    (cumulative group ends, int32)."""
+    (cumulative group ends, int32); with_grad adds the upstream gradient
+    G [sum_m, N] of the backward (dgrad, wgrad)."""
     cfg = dict(GROUPED_GEMM_CONFIG)
     for key, val in (("sum_m", sum_m), ("E", E), ("K", K), ("N", N), ("alpha", alpha)):
         if val is not None:
@@ -163,7 +165,10 @@ def make_grouped_gemm(*, seed: int = 0, device="cpu", weights_device=None, sum_m
     X = _normal_bf16((cfg["sum_m"], cfg["K"]), 1.0, seed, 12).to(device)
     W = _normal_bf16((cfg["E"], cfg["N"], cfg["K"]), 1.0 / np.sqrt(cfg["K"]), seed, 13, wdev)
     offs = torch.from_numpy(np.cumsum(sizes).astype(np.int32)).to(device)
-    return dict(X=X, W=W, offs=offs, sizes=sizes, **cfg)
+    out = dict(X=X, W=W, offs=offs, sizes=sizes, **cfg)
+    if with_grad:
+        out["G"] = _normal_bf16((cfg["sum_m"], cfg["N"]), 1.0, seed, 14).to(device)
+    return out
 
 
 def bf16_bits(t: torch.Tensor) -> np.ndarray:

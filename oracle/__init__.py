@@ -70,6 +70,10 @@ def _declare(lib):
     lib.oracle_finalize.restype = None
     lib.oracle_grouped_gemm_rows.argtypes = [P, P, P, i, i, i, P, i, P, i]
     lib.oracle_grouped_gemm_rows.restype = None
+    lib.oracle_grouped_gemm_dgrad_rows.argtypes = [P, P, P, i, i, i, P, i, P, i]
+    lib.oracle_grouped_gemm_dgrad_rows.restype = None
+    lib.oracle_grouped_gemm_wgrad_rows.argtypes = [P, P, P, i, i, i, P, P, i, P, P, i]
+    lib.oracle_grouped_gemm_wgrad_rows.restype = None
     lib.oracle_float_to_bf16.argtypes = [ctypes.c_float]
     lib.oracle_float_to_bf16.restype = ctypes.c_uint16
     lib.oracle_bf16_to_float.argtypes = [ctypes.c_uint16]
@@ -211,6 +215,42 @@ def grouped_gemm_rows(X, W, offs, rows=None, nthreads=0, lib=None):
     out = np.empty((rows.shape[0], N), np.uint16)
     lib.oracle_grouped_gemm_rows(_p(X), _p(W), _p(offs), E, N, K, _p(rows), rows.shape[0], _p(out), nthreads)
     return out
+
+
+def grouped_gemm_dgrad_rows(G, W, offs, rows=None, nthreads=0, lib=None):
+    """dX rows (bf16 bits) of the grouped GEMM's data gradient dX = G . W[e]
+    for G [sum_m, N], W [E, N, K] (W used in place)."""
+    lib = lib or load()
+    G = _c(G, np.uint16)
+    W = _c(W, np.uint16)
+    offs = _c(offs, np.int32)
+    E, N, K = W.shape
+    assert G.shape[1] == N
+    if rows is None:
+        rows = np.arange(int(offs[-1]) if E else 0, dtype=np.int32)
+    rows = _c(rows, np.int32)
+    out = np.empty((rows.shape[0], K), np.uint16)
+    lib.oracle_grouped_gemm_dgrad_rows(_p(G), _p(W), _p(offs), E, N, K, _p(rows), rows.shape[0], _p(out), nthreads)
+    return out
+
+
+def grouped_gemm_wgrad_rows(G, X, offs, sel_e, sel_n, K=None, nthreads=0, lib=None):
+    """Rows (e, n) of the grouped GEMM's weight gradient dW[e] = G_e^T . X_e:
+    returns (fp32 [n_sel, K], bf16 bits [n_sel, K])."""
+    lib = lib or load()
+    G = _c(G, np.uint16)
+    X = _c(X, np.uint16)
+    offs = _c(offs, np.int32)
+    sel_e = _c(sel_e, np.int32)
+    sel_n = _c(sel_n, np.int32)
+    N = G.shape[1]
+    K = X.shape[1]
+    n = sel_e.shape[0]
+    f32 = np.empty((n, K), np.float32)
+    b16 = np.empty((n, K), np.uint16)
+    lib.oracle_grouped_gemm_wgrad_rows(_p(G), _p(X), _p(offs), offs.shape[0], N, K, _p(sel_e), _p(sel_n), n,
+                                       _p(f32), _p(b16), nthreads)
+    return f32, b16
 
 
 def bf16_to_f32(a: np.ndarray) -> np.ndarray:

@@ -27,7 +27,9 @@
  *        (gemm1_clamp_limit).
  *   [P3] "Cake ragged BF16 grouped GEMM (experimental)", operation table:
  *        Y[offs[e-1]:offs[e]] = X[offs[e-1]:offs[e]] . W[e]^T, offs holding
- *        cumulative group end offsets, groups may be empty.
+ *        cumulative group end offsets, groups may be empty; dgrad
+ *        dX = G . W[e] (W in place, bf16 out) and wgrad dW[e] = G^T . X
+ *        (bf16 or fp32 out, exact zeros for an empty group) per group.
  *
  * Precision: the pages fix fp32 accumulation with bf16 inputs and outputs, so
  * the oracle computes in fp32.  The only roundings to bf16 are the SwiGLU
@@ -369,6 +371,62 @@ void oracle_grouped_gemm_rows(const uint16_t *X, const uint16_t *W,
                 acc = acc + bf16_to_float(xr[c]) *
                                 bf16_to_float(we[(size_t)n * K + c]);
             Y_rows[(size_t)q * N + n] = float_to_bf16(acc);
+        }
+    }
+}
+
+/* ---- ragged grouped GEMM backward  [P3 operation table: dgrad, wgrad] -----
+ *
+ * Groups as in the forward: group e is rows [offs[e-1], offs[e]) of the
+ * packed activations (offs[-1] = 0).
+ *
+ * dgrad, W used in place: dX[p, c] = bf16( sum_{n=0..N-1} G[p,n] * W[e,n,c] )
+ * for row p of group e; G [sum_m, N], W [E, N, K], the sum sequential in n
+ * in fp32.  Writes the listed rows into dX_rows [n_rows, K]. */
+void oracle_grouped_gemm_dgrad_rows(const uint16_t *G, const uint16_t *W,
+                                    const int32_t *offs, int E, int N, int K,
+                                    const int32_t *rows, int n_rows,
+                                    uint16_t *dX_rows, int nthreads) {
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int q = 0; q < n_rows; ++q) {
+        int p = rows[q];
+        int e = group_of_row(offs, E, p);
+        const uint16_t *gr = G + (size_t)p * N;
+        const uint16_t *we = W + (size_t)e * N * K;
+        for (int c = 0; c < K; ++c) {
+            float acc = 0.0f;
+            for (int n = 0; n < N; ++n)
+                acc = acc + bf16_to_float(gr[n]) *
+                                bf16_to_float(we[(size_t)n * K + c]);
+            dX_rows[(size_t)q * K + c] = float_to_bf16(acc);
+        }
+    }
+}
+
+/* wgrad: dW[e, n, c] = sum over the rows p of group e, ascending, of
+ * G[p,n] * X[p,c] in fp32 (an empty group gives exactly 0); G [sum_m, N],
+ * X [sum_m, K].  For each listed (e, n) pair q writes the K values of row n
+ * of dW[e] into dW_f32 [n_sel, K] (fp32, when not NULL) and dW_bf16
+ * [n_sel, K] (one bf16 rounding of the fp32 sum, when not NULL). */
+void oracle_grouped_gemm_wgrad_rows(const uint16_t *G, const uint16_t *X,
+                                    const int32_t *offs, int E, int N, int K,
+                                    const int32_t *sel_e, const int32_t *sel_n,
+                                    int n_sel, float *dW_f32, uint16_t *dW_bf16,
+                                    int nthreads) {
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int q = 0; q < n_sel; ++q) {
+        int e = sel_e[q], n = sel_n[q];
+        int start = e == 0 ? 0 : offs[e - 1];
+        int end = offs[e];
+        for (int c = 0; c < K; ++c) {
+            float acc = 0.0f;
+            for (int p = start; p < end; ++p)
+                acc = acc + bf16_to_float(G[(size_t)p * N + n]) *
+                                bf16_to_float(X[(size_t)p * K + c]);
+            if (dW_f32) dW_f32[(size_t)q * K + c] = acc;
+            if (dW_bf16) dW_bf16[(size_t)q * K + c] = float_to_bf16(acc);
         }
     }
 }

@@ -41,6 +41,12 @@ MUTANTS = {
     "step_up_clamped_above_only": [("    if (u < -limit) u = -limit;\n", "")],
     "step_limit_by_global_id": [("limit_of(clamp, e - off), h, y + (size_t)j * H);",
                                  "limit_of(clamp, e), h, y + (size_t)j * H);")],
+    "dgrad_row_off_by_one": [("const uint16_t *gr = G + (size_t)p * N;",
+                              "const uint16_t *gr = G + (size_t)(p > 0 ? p - 1 : p) * N;")],
+    "dgrad_drops_last_term": [("            for (int n = 0; n < N; ++n)\n                acc = acc + bf16_to_float(gr[n]) *",
+                               "            for (int n = 0; n < N - 1; ++n)\n                acc = acc + bf16_to_float(gr[n]) *")],
+    "wgrad_takes_next_row": [("for (int p = start; p < end; ++p)",
+                              "for (int p = start; p < end + (end < offs[E - 1]); ++p)")],
     "finalize_skips_slot0": [("            for (int j = 0; j < k; ++j) {\n                int p = exp_to_perm[(size_t)t * k + j];",
                               "            for (int j = 1; j < k; ++j) {\n                int p = exp_to_perm[(size_t)t * k + j];")],
 }
@@ -58,6 +64,9 @@ PIN_CALLS = [
     ("rounding", lambda: pins.test_bf16_rounding_matches_torch()),
     ("step_hand_worked", lambda: pins.test_swiglu_step_hand_worked()),
     ("step_fp64", lambda: pins.test_swiglu_step_fp64_bruteforce_tiny()),
+    ("dgrad_torch", lambda: pins.test_grouped_gemm_dgrad_vs_torch_per_group()),
+    ("wgrad_torch", lambda: pins.test_grouped_gemm_wgrad_vs_torch_per_group_and_empty_groups_zero()),
+    ("gg_adjoint", lambda: pins.test_grouped_gemm_adjoint_identity()),
     ("step_per_expert", lambda: pins.test_swiglu_step_infinite_limit_is_plain_swiglu_and_limits_are_per_local_expert()),
 ]
 

@@ -452,6 +452,73 @@ def test_grouped_gemm_vs_torch_per_group():
         start = end
 
 
+# ------------------------------------------------- grouped GEMM backward --
+# Cake ragged BF16 grouped GEMM (experimental), operation table: dgrad
+# dX = G . W[e] (W in place, bf16), wgrad dW[e] = G^T . X (fp32 or bf16, exact
+# zeros for an empty group).
+
+def _gg_bwd(seed, **kw):
+    d = W.make_grouped_gemm(seed=seed, with_grad=True, **kw)
+    return (W.bf16_bits(d["X"]), W.bf16_bits(d["W"]), W.bf16_bits(d["G"]), d["offs"].numpy(), d["sizes"])
+
+
+def test_grouped_gemm_dgrad_vs_torch_per_group():
+    X, Wt, G, offs, sizes = _gg_bwd(2, sum_m=300, E=7, K=128, N=64, alpha=0.3)
+    assert (sizes == 0).any()
+    dX = oracle.grouped_gemm_dgrad_rows(G, Wt, offs)
+    start = 0
+    for e, end in enumerate(offs):
+        if end > start:
+            ge = torch.from_numpy(bf16_to_f64(G[start:end]).astype(np.float32))
+            we = torch.from_numpy(bf16_to_f64(Wt[e]).astype(np.float32))
+            check_bf16_close(dX[start:end], torch_bf16_bits((ge @ we).numpy()), f"dgrad group {e}")
+        start = end
+
+
+def test_grouped_gemm_wgrad_vs_torch_per_group_and_empty_groups_zero():
+    X, Wt, G, offs, sizes = _gg_bwd(3, sum_m=300, E=7, K=128, N=64, alpha=0.3)
+    E, N, K = Wt.shape
+    assert (sizes == 0).any() and (sizes > 0).any()
+    sel_e = np.repeat(np.arange(E, dtype=np.int32), N)
+    sel_n = np.tile(np.arange(N, dtype=np.int32), E)
+    f32, b16 = oracle.grouped_gemm_wgrad_rows(G, X, offs, sel_e, sel_n)
+    f32, b16 = f32.reshape(E, N, K), b16.reshape(E, N, K)
+    assert np.array_equal(b16, torch_bf16_bits(f32))  # the bf16 output is one rounding of the fp32 sum
+    start = 0
+    for e, end in enumerate(offs):
+        if end == start:
+            assert np.all(f32[e].view(np.uint32) == 0) and np.all(b16[e] == 0)  # exact +0
+        else:
+            ge = torch.from_numpy(bf16_to_f64(G[start:end]).astype(np.float32))
+            xe = torch.from_numpy(bf16_to_f64(X[start:end]).astype(np.float32))
+            want = (ge.T @ xe).numpy().astype(np.float64)
+            rms = np.sqrt(np.mean(want ** 2))
+            assert np.max(np.abs(f32[e] - want)) <= 1e-5 * rms * max(1, end - start) ** 0.5, e
+        start = end
+
+
+def test_grouped_gemm_adjoint_identity():
+    """sum(G * (X W^T)) = sum(dX * X) = sum(dW * W) over all groups (the
+    three operations of the operation table are adjoint), fp64 sums of the
+    oracle's results against the fp64 forward."""
+    X, Wt, G, offs, sizes = _gg_bwd(4, sum_m=500, E=6, K=192, N=128, alpha=0.5)
+    E, N, K = Wt.shape
+    x64, w64, g64 = bf16_to_f64(X), bf16_to_f64(Wt), bf16_to_f64(G)
+    fwd, start = 0.0, 0
+    for e, end in enumerate(offs):
+        fwd += float(np.sum(g64[start:end] * (x64[start:end] @ w64[e].T)))
+        start = end
+    dX = bf16_to_f64(oracle.grouped_gemm_dgrad_rows(G, Wt, offs))
+    sel_e = np.repeat(np.arange(E, dtype=np.int32), N)
+    sel_n = np.tile(np.arange(N, dtype=np.int32), E)
+    dW = oracle.grouped_gemm_wgrad_rows(G, X, offs, sel_e, sel_n)[0].astype(np.float64).reshape(E, N, K)
+    by_dx = float(np.sum(dX * x64[:dX.shape[0]]))
+    by_dw = float(np.sum(dW * w64))
+    scale = float(np.sqrt(np.sum(g64 ** 2) * np.sum(x64 ** 2)))
+    assert abs(by_dw - fwd) <= 1e-5 * scale, (by_dw, fwd)
+    assert abs(by_dx - fwd) <= 2e-3 * scale, (by_dx, fwd)   # dX carries one bf16 rounding
+
+
 def test_workload_generator_is_seeded():
     a = W.make_moe("tiny", seed=0)
     b = W.make_moe("tiny", seed=0)
