@@ -179,6 +179,22 @@ MOE_API int moe_fc1_swiglu_gathered(const moe_bf16 *x, const int32_t *perm_to_ex
                                     const moe_bf16 *w1, int H, int I, int num_local,
                                     moe_bf16 *h, void *stream);
 
+/* ---- S4 with the StepFun epilogue ---------------------------------------------------
+ * moe_fc1_swiglu with SwiGLUStep(limit): GEMM1's outputs are clamped before
+ * the activation, g' = min(g, limit[i]), u' = min(max(u, -limit[i]), limit[i]),
+ * h[p] = bf16_rne(silu(g') * u') for permuted rows p of local expert i (the
+ * StepFun activation "SwiGLUStep(limit) with a per-expert clamp limit",
+ * flashinfer.experimental.cake_stepfun_moe, opening paragraph; the per-expert
+ * gemm1_clamp_limit of Unified MoE API opt-in).  This clamp is the library's
+ * reading: the page names the activation and the per-expert limit only.
+ *   clamp_limit [L] fp32 (device), one limit per local expert; +inf leaves an
+ *   expert's SwiGLU unclamped (bitwise moe_fc1_swiglu).  Other arguments as
+ *   moe_fc1_swiglu.  The prepared launch takes the same limits through
+ *   moe_forward_desc.clamp_limit on every path. */
+MOE_API int moe_fc1_swiglu_step(const moe_bf16 *xp, const moe_bf16 *w1, const float *clamp_limit,
+                                const int32_t *m_indptr, int max_rows, int H, int I,
+                                int num_local, moe_bf16 *h, void *stream);
+
 /* ---- S5 FC2 ------------------------------------------------------------------------
  * y[p] = h[p] . W2[i]^T, fp32, unscaled and unrounded (cute_dsl_fused_moe_bf16,
  * Parameters, use_fused_finalize=False).
@@ -283,6 +299,15 @@ MOE_API int moe_forward(const moe_bf16 *x, const float *logits, const int32_t *t
                                          per SM; if other work holds SMs for longer
                                          than the wait limit, the launch reports
                                          MOE_DEV_TIMEOUT in the status word. */
+#define MOE_PLAN_TEST_UNREACHABLE_WAIT 64 /* test hook, not for production: the
+                                             decode chain in one launch seeds its
+                                             per-expert counts of finished FC1 tiles
+                                             with -1 instead of 0, so every FC2 tile's
+                                             wait for them runs out; the launch then
+                                             ends with MOE_DEV_TIMEOUT in the status
+                                             word (and a wrong output).  Used with
+                                             moe_plan_set_wait_limit to test that a
+                                             bounded wait returns and reports. */
 
 typedef struct moe_forward_desc {
     const moe_bf16 *x;
@@ -298,6 +323,8 @@ typedef struct moe_forward_desc {
     int T, H, I, E, top_k, local_offset, num_local;
     int path;                /* MOE_PATH_* */
     int flags;               /* MOE_PLAN_* */
+    const float *clamp_limit; /* [L] fp32 SwiGLUStep limits per local expert
+                                 (moe_fc1_swiglu_step), or NULL for SwiGLU */
 } moe_forward_desc;
 
 typedef struct moe_plan moe_plan;
@@ -320,6 +347,16 @@ typedef struct moe_plan_buffers {
 MOE_API int moe_forward_prepare(const moe_forward_desc *desc, moe_plan **plan);
 MOE_API int moe_plan_launch(moe_plan *plan, void *stream);
 MOE_API int moe_plan_buffers_get(const moe_plan *plan, moe_plan_buffers *out);
+/* Longest a single wait inside this plan's kernels may take before the kernel
+ * gives up, raises MOE_DEV_TIMEOUT in the status word and returns (every
+ * in-kernel wait is bounded: on a TMA copy, an MMA, a ring slot or another
+ * CTA's count).  Default 4 s.  MOE_WAIT_LIMIT_MIN_NS <= limit_ns <=
+ * MOE_WAIT_LIMIT_MAX_NS, else MOE_ERR_SHAPE.  Takes effect at the next launch
+ * (a CUDA graph keeps the limit it was captured with).  A limit shorter than a
+ * kernel's normal waits makes a correct launch report a timeout. */
+#define MOE_WAIT_LIMIT_MIN_NS 1000ull
+#define MOE_WAIT_LIMIT_MAX_NS 600000000000ull
+MOE_API int moe_plan_set_wait_limit(moe_plan *plan, unsigned long long limit_ns);
 /* Stage timing (plans prepared with MOE_PLAN_STAGE_TIMING): the number of
  * stages and their names; moe_plan_stage_times waits for the recorded events
  * and returns, per stage, the summed milliseconds over the launches since

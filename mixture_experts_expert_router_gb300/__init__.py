@@ -39,6 +39,8 @@ PLAN_DECODE_CHAIN = 4
 PLAN_DECODE_SEPARATE = 8
 PLAN_FUSED_GATHER = 16
 PLAN_DECODE_ONE_LAUNCH = 32
+PLAN_TEST_UNREACHABLE_WAIT = 64
+WAIT_LIMIT_MIN_NS, WAIT_LIMIT_MAX_NS = 1000, 600_000_000_000
 DEV_BAD_EXPERT, DEV_TIMEOUT = 1, 2
 MAX_EXPERTS, MAX_TOP_K = 1024, 16
 
@@ -49,7 +51,8 @@ ABI_SYMBOLS = [
     "moe_workspace_size", "moe_forward", "moe_forward_prepare", "moe_plan_launch",
     "moe_plan_buffers_get", "moe_plan_stage_count", "moe_plan_stage_name", "moe_plan_stage_times",
     "moe_plan_stage_reset", "moe_plan_kernels_per_launch", "moe_plan_destroy", "moe_sort_no_alloc",
-    "moe_fc1_swiglu_swapab", "moe_fc2_swapab", "moe_fc1_swiglu_gathered",
+    "moe_fc1_swiglu_swapab", "moe_fc2_swapab", "moe_fc1_swiglu_gathered", "moe_plan_set_wait_limit",
+    "moe_fc1_swiglu_step",
 ]
 
 
@@ -67,6 +70,7 @@ class _Desc(ctypes.Structure):
         ("status", ctypes.c_void_p), ("T", ctypes.c_int), ("H", ctypes.c_int), ("I", ctypes.c_int),
         ("E", ctypes.c_int), ("top_k", ctypes.c_int), ("local_offset", ctypes.c_int),
         ("num_local", ctypes.c_int), ("path", ctypes.c_int), ("flags", ctypes.c_int),
+        ("clamp_limit", ctypes.c_void_p),
     ]
 
 
@@ -103,6 +107,7 @@ def library():
             "moe_sort_no_alloc": ([P, I, I, I, I, I, P, P, P, P, P], I),
             "moe_gather": ([P, P, P, I, I, I, I, P, P], I),
             "moe_fc1_swiglu": ([P, P, P, I, I, I, I, P, P], I),
+            "moe_fc1_swiglu_step": ([P, P, P, P, I, I, I, I, P, P], I),
             "moe_fc2": ([P, P, P, I, I, I, I, P, P], I),
             "moe_fc1_swiglu_swapab": ([P, P, P, I, I, I, I, I, P, P], I),
             "moe_fc1_swiglu_gathered": ([P, P, P, I, I, P, I, I, I, P, P], I),
@@ -118,6 +123,7 @@ def library():
             "moe_plan_stage_name": ([P, I], ctypes.c_char_p),
             "moe_plan_stage_times": ([P, ctypes.POINTER(ctypes.c_float), I, ctypes.POINTER(I)], I),
             "moe_plan_stage_reset": ([P], I),
+            "moe_plan_set_wait_limit": ([P, ctypes.c_ulonglong], I),
             "moe_plan_kernels_per_launch": ([P], I),
             "moe_plan_destroy": ([P], I),
         }
@@ -242,7 +248,8 @@ def moe_gather(x: torch.Tensor, perm_to_exp: torch.Tensor, m_indptr: torch.Tenso
     return xp
 
 
-def moe_fc1_swiglu(xp: torch.Tensor, w1: torch.Tensor, m_indptr: torch.Tensor, h=None):
+def moe_fc1_swiglu(xp: torch.Tensor, w1: torch.Tensor, m_indptr: torch.Tensor, h=None, clamp_limit=None):
+    """FC1 + SwiGLU; with clamp_limit [L] fp32 the SwiGLUStep(limit) epilogue."""
     _need(xp, torch.bfloat16, "xp")
     _need(w1, torch.bfloat16, "w1")
     _need(m_indptr, torch.int32, "m_indptr")
@@ -253,6 +260,11 @@ def moe_fc1_swiglu(xp: torch.Tensor, w1: torch.Tensor, m_indptr: torch.Tensor, h
     I = twoI // 2
     h = torch.empty((rows, I), dtype=torch.bfloat16, device=xp.device) if h is None else h
     _need(h, torch.bfloat16, "h", (rows, I), xp.device)
+    if clamp_limit is not None:
+        _need(clamp_limit, torch.float32, "clamp_limit", (L,), xp.device)
+        _check(library().moe_fc1_swiglu_step(_ptr(xp), _ptr(w1), _ptr(clamp_limit), _ptr(m_indptr), rows, H, I,
+                                             L, _ptr(h), _stream(xp.device)), "moe_fc1_swiglu_step")
+        return h
     _check(library().moe_fc1_swiglu(_ptr(xp), _ptr(w1), _ptr(m_indptr), rows, H, I, L, _ptr(h),
                                     _stream(xp.device)), "moe_fc1_swiglu")
     return h
@@ -408,12 +420,17 @@ class MoEPlan:
     def __init__(self, x, w1, w2, num_experts: int, top_k: int, logits=None, topk_ids=None, topk_w=None,
                  local_offset: int = 0, out=None, workspace=None, status=None, path: int = PATH_AUTO,
                  stage_timing: bool = False, one_cta_gemm: bool = False, decode_chain: bool | None = None,
-                 fused_gather: bool = False, decode_one_launch: bool = False):
+                 fused_gather: bool = False, decode_one_launch: bool = False,
+                 test_unreachable_wait: bool = False, clamp_limit=None):
         """decode_chain: None lets the library choose the decode form (the
         chain in one launch for few routes, else five kernels), True forces
         the chain as two kernels, False the five separate kernels.
         decode_one_launch: always the chain in one launch.  fused_gather: on the grouped path FC1 copies
-        its token rows straight from x instead of a gather kernel."""
+        its token rows straight from x instead of a gather kernel.
+        test_unreachable_wait: test hook (MOE_PLAN_TEST_UNREACHABLE_WAIT) that
+        makes the one-launch decode chain's FC2 waits run out.
+        clamp_limit: [L] fp32 device tensor of per-expert SwiGLUStep limits
+        (None: plain SwiGLU)."""
         T, H, I, L, out = _layer_args(x, w1, w2, num_experts, top_k, logits, topk_ids, topk_w,
                                       local_offset, out)
         dev = x.device
@@ -422,7 +439,9 @@ class MoEPlan:
             workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
         if status is None:
             status = torch.zeros(1, dtype=torch.int32, device=dev)
-        self._keep = (x, w1, w2, logits, topk_ids, topk_w, out, workspace, status)
+        if clamp_limit is not None:
+            _need(clamp_limit, torch.float32, "clamp_limit", (L,), dev)
+        self._keep = (x, w1, w2, logits, topk_ids, topk_w, out, workspace, status, clamp_limit)
         self.x, self.w1, self.w2, self.logits, self.topk_ids, self.topk_w = x, w1, w2, logits, topk_ids, topk_w
         self.out, self.workspace, self.status = out, workspace, status
         self.T, self.H, self.I, self.E, self.top_k, self.L = T, H, I, num_experts, top_k, L
@@ -435,7 +454,9 @@ class MoEPlan:
                   | (PLAN_DECODE_CHAIN if decode_chain is True else 0)
                   | (PLAN_DECODE_SEPARATE if decode_chain is False else 0)
                   | (PLAN_FUSED_GATHER if fused_gather else 0)
-                  | (PLAN_DECODE_ONE_LAUNCH if decode_one_launch else 0))
+                  | (PLAN_DECODE_ONE_LAUNCH if decode_one_launch else 0)
+                  | (PLAN_TEST_UNREACHABLE_WAIT if test_unreachable_wait else 0),
+                  clamp_limit=_ptr(clamp_limit))
         handle = ctypes.c_void_p()
         _check(library().moe_forward_prepare(ctypes.byref(d), ctypes.byref(handle)), "moe_forward_prepare")
         self._h = handle
@@ -464,6 +485,10 @@ class MoEPlan:
 
     def kernels_per_launch(self) -> int:
         return int(library().moe_plan_kernels_per_launch(self._h))
+
+    def set_wait_limit(self, limit_ns: int):
+        """Longest one in-kernel wait of this plan may take (default 4 s)."""
+        _check(library().moe_plan_set_wait_limit(self._h, int(limit_ns)), "moe_plan_set_wait_limit")
 
     def stage_reset(self):
         _check(library().moe_plan_stage_reset(self._h), "moe_plan_stage_reset")

@@ -107,6 +107,7 @@ struct moe_plan {
   SwapPlan fc1d, fc2d;  // decode path, separate kernels
   ChainPlan chain;      // decode path: the chain (one launch or two kernels)
   bool use_chain;
+  bool unreachable_wait;  // test hook MOE_PLAN_TEST_UNREACHABLE_WAIT
   bool fused_gather;    // grouped path: FC1 gathers its rows itself
   bool timing;
   cudaEvent_t (*ev)[kNumStages + 1];
@@ -131,7 +132,7 @@ const char *moe_status_string(int code) {
   }
 }
 
-int moe_abi_version(void) { return 100; }
+int moe_abi_version(void) { return 101; }
 
 int moe_route(const float *logits, int T, int E, int top_k, int32_t *topk_ids, float *topk_w,
               void *stream) {
@@ -218,6 +219,26 @@ int moe_fc1_swiglu(const moe_bf16 *xp, const moe_bf16 *w1, const int32_t *m_indp
   if (int rc = gemm_prepare(p, Epi::kSwiGLU, xp, max_rows, w1, num_local, 2 * I, H, I,
                             m_indptr + 1, max_rows, h, nullptr))
     return rc;
+  Launch l;
+  l.stream = static_cast<cudaStream_t>(stream);
+  return cuda_rc(launch_gemm(p, l));
+}
+
+int moe_fc1_swiglu_step(const moe_bf16 *xp, const moe_bf16 *w1, const float *clamp_limit,
+                        const int32_t *m_indptr, int max_rows, int H, int I, int num_local, moe_bf16 *h,
+                        void *stream) {
+  if (max_rows < 0 || H <= 0 || I <= 0 || H % 64 || I % 64 || num_local < 1 ||
+      num_local > MOE_MAX_EXPERTS)
+    return MOE_ERR_SHAPE;
+  if (max_rows == 0) return MOE_OK;
+  if (!xp || !w1 || !clamp_limit || !m_indptr || !h) return MOE_ERR_NULL;
+  if (!aligned16(xp) || !aligned16(w1) || !aligned16(h)) return MOE_ERR_ALIGN;
+  if (int rc = check_device()) return rc;
+  GemmPlan p;
+  if (int rc = gemm_prepare(p, Epi::kSwiGLU, xp, max_rows, w1, num_local, 2 * I, H, I,
+                            m_indptr + 1, max_rows, h, nullptr))
+    return rc;
+  p.clamp = clamp_limit;
   Launch l;
   l.stream = static_cast<cudaStream_t>(stream);
   return cuda_rc(launch_gemm(p, l));
@@ -408,10 +429,12 @@ int moe_forward_prepare(const moe_forward_desc *desc, moe_plan **plan_out) {
       c.H = d.H;
       c.I = d.I;
       c.ids_early = !logits_mode;
+      c.clamp = d.clamp_limit;
       rc = chain_prepare(c);
     } else if (p->path == MOE_PATH_DECODE) {
       rc = swap_prepare(p->fc1d, true, d.w1, d.num_local, 2 * d.I, d.H, p->xp, p->R, d.I,
                         p->m_indptr + 1, d.T, p->h, d.status, true);
+      p->fc1d.clamp = d.clamp_limit;
       if (rc == MOE_OK)
         rc = swap_prepare(p->fc2d, false, d.w2, d.num_local, d.H, d.I, p->h, p->R, d.H,
                           p->m_indptr + 1, d.T, p->y, d.status, true);
@@ -427,6 +450,7 @@ int moe_forward_prepare(const moe_forward_desc *desc, moe_plan **plan_out) {
       else
         rc = gemm_prepare(p->fc1, Epi::kSwiGLU, p->xp, p->R, d.w1, d.num_local, 2 * d.I, d.H, d.I,
                           p->m_indptr + 1, p->R, p->h, d.status, pair);
+      p->fc1.clamp = d.clamp_limit;
       if (rc == MOE_OK)
         rc = gemm_prepare(p->fc2, Epi::kF32, p->h, p->R, d.w2, d.num_local, d.H, d.I, d.H,
                           p->m_indptr + 1, p->R, p->y, d.status, pair);
@@ -436,6 +460,7 @@ int moe_forward_prepare(const moe_forward_desc *desc, moe_plan **plan_out) {
       return rc;
     }
   }
+  p->unreachable_wait = (d.flags & MOE_PLAN_TEST_UNREACHABLE_WAIT) != 0;
   p->timing = (d.flags & MOE_PLAN_STAGE_TIMING) != 0 && d.T > 0;
   if (p->timing) {
     p->ev = new (std::nothrow) cudaEvent_t[kTimingRing][kNumStages + 1];
@@ -482,7 +507,8 @@ int moe_plan_launch(moe_plan *p, void *stream) {
   if (p->use_chain) {  // sort, gather and finalize run inside the GEMM kernels
     // The one-launch kernel's counters live in the workspace, which other
     // plans may share: every launch zeroes them first.
-    if (p->chain.one_launch && chain_zero_counters(p->chain, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (p->chain.one_launch && chain_zero_counters(p->chain, s, p->unreachable_wait) != cudaSuccess)
+      return MOE_ERR_CUDA;
     if (!mark(kSort) || !mark(kGather) || !mark(kFc1)) return MOE_ERR_CUDA;
     if (p->chain.one_launch) {
       if (launch_chain(p->chain, 0, l) != cudaSuccess) return MOE_ERR_CUDA;
@@ -531,6 +557,15 @@ int moe_plan_buffers_get(const moe_plan *p, moe_plan_buffers *out) {
   out->h = p->h;
   out->y = p->y;
   out->path = p->path;
+  return MOE_OK;
+}
+
+int moe_plan_set_wait_limit(moe_plan *p, unsigned long long limit_ns) {
+  if (!p) return MOE_ERR_NULL;
+  if (limit_ns < MOE_WAIT_LIMIT_MIN_NS || limit_ns > MOE_WAIT_LIMIT_MAX_NS) return MOE_ERR_SHAPE;
+  p->fc1.wait_ns = p->fc2.wait_ns = limit_ns;
+  p->fc1d.wait_ns = p->fc2d.wait_ns = limit_ns;
+  p->chain.wait_ns = limit_ns;
   return MOE_OK;
 }
 

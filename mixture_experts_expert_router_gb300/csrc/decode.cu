@@ -51,6 +51,8 @@ struct SwapArgs {
   const int32_t *group_end;
   void *out;
   int32_t *status;
+  unsigned long long wait_ns;  // bounded-wait limit of this launch
+  const float *clamp;         // SwiGLU epilogue: [groups] SwiGLUStep limits, or null
   long max_rows;
   int G, K, n_out, w_rows, m_tiles, early;
 };
@@ -254,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1) swapab_kernel(const __grid_consta
         const uint32_t ph = (uint32_t)(iq / HS) & 1u;
         ++iq;
         if (!waited && iq > HS) finish_wait();  // this pipeline's ring is full of early loads
-        if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, args.status)) {
+        if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, args.status, args.wait_ns)) {
           ok = false;
           break;
         }
@@ -280,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1) swapab_kernel(const __grid_consta
     if (!waited) finish_wait();  // fewer k-blocks in total than ring stages
     // let this pipeline's last copies land
     for (int j = iq > HS ? iq - HS : 0; j < iq; ++j)
-      mbar_wait(full_bar(q * HS + j % HS), (uint32_t)(j / HS) & 1u, nullptr, args.status);
+      mbar_wait(full_bar(q * HS + j % HS), (uint32_t)(j / HS) & 1u, nullptr, args.status, args.wait_ns);
   } else if ((warp == 1 || warp == kMma1Warp) && lane == 0) {
     // ----------------------------------------------------------- MMA issuers --
     // Issuer q multiplies the k-blocks kb % 2 == q into accumulator q of the
@@ -291,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1) swapab_kernel(const __grid_consta
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tc) {
       const int acc = tc & 1;
       const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
-      if (!mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag, args.status)) break;
+      if (!mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag, args.status, args.wait_ns)) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)((2 * acc + q) * BNT);
       bool first = true;
@@ -300,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1) swapab_kernel(const __grid_consta
         const int s = q * HS + iq % HS;
         const uint32_t ph = (uint32_t)(iq / HS) & 1u;
         ++iq;
-        if (!mbar_wait(full_bar(s), ph, abort_flag, args.status)) {
+        if (!mbar_wait(full_bar(s), ph, abort_flag, args.status, args.wait_ns)) {
           ok = false;
           break;
         }
@@ -317,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1) swapab_kernel(const __grid_consta
       if (ok) umma_commit(tfull_bar(acc));
     }
     umma_commit(drain_bar(q));
-    mbar_wait(drain_bar(q), 0, nullptr, args.status);
+    mbar_wait(drain_bar(q), 0, nullptr, args.status, args.wait_ns);
   } else if (warp >= 2 && warp <= 5) {
     // ------------------------------------------------------------------ epilogue --
     if (args.early) pdl_wait();
@@ -330,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1) swapab_kernel(const __grid_consta
       const int valid = gend[c.g] - xrow;  // tokens of this tile (> 0)
       const int acc = tc & 1;
       const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
-      const bool got = mbar_wait(tfull_bar(acc), aph, abort_flag, args.status);
+      const bool got = mbar_wait(tfull_bar(acc), aph, abort_flag, args.status, args.wait_ns);
       if (epi_bar_any(!got)) break;  // a wait gave up somewhere: all four warps stop together
       float v[BNT];
       tc_fence_after();
@@ -356,11 +358,12 @@ __global__ void __launch_bounds__(kThreads, 1) swapab_kernel(const __grid_consta
         if (r < 64) {
           __nv_bfloat16 *h = reinterpret_cast<__nv_bfloat16 *>(args.out);
           const long col = (long)c.m * 64 + r;
+          const float lim = step_limit(args.clamp, c.g);
 #pragma unroll
           for (int j = 0; j < BNT; ++j) {
             if (j < valid) {
               const float gg = sg[j * 64 + r];
-              h[(long)(xrow + j) * args.n_out + col] = __float2bfloat16_rn(silu_f32(gg) * v[j]);
+              h[(long)(xrow + j) * args.n_out + col] = __float2bfloat16_rn(swiglu_step(gg, v[j], lim));
             }
           }
         }
@@ -438,6 +441,8 @@ cudaError_t inst_launch(const SwapPlan &p, const Launch &l) {
   a.group_end = p.group_end;
   a.out = p.out;
   a.status = p.status;
+  a.wait_ns = p.wait_ns;
+  a.clamp = p.clamp;
   a.max_rows = p.max_rows;
   a.G = p.G;
   a.K = p.K;

@@ -69,6 +69,8 @@ struct ChainArgs {
   int32_t *done1;      // one launch: [L] finished FC1 tiles per expert
   int32_t *m_indptr_out, *p2e_out, *e2p_out;  // published by the first CTA of FC1
   int32_t *status;
+  unsigned long long wait_ns;  // bounded-wait limit of this launch
+  const float *clamp;         // SwiGLU epilogue: [groups] SwiGLUStep limits, or null
   int T, k, E, off, L, H, I, m_tiles1, m_tiles2, ids_early;
 };
 
@@ -404,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         pdl_done = true;
         int w_ok = 1;
         if (MODE == kModeBoth && lane == 0)
-          w_ok = counter_wait(a.done1 + c.g, need, abort_flag, a.status) ? 1 : 0;
+          w_ok = counter_wait(a.done1 + c.g, need, abort_flag, a.status, a.wait_ns) ? 1 : 0;
         if (!__shfl_sync(0xffffffffu, w_ok, 0)) ok = false;
         if (MODE == kModeBoth) fence_proxy_async_global();
         // the listed boxes go out even after a failed wait (their reads stay in
@@ -458,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         const uint32_t ph = (uint32_t)(iq / HS) & 1u;
         ++iq;
         int w_ok = 1;
-        if (lane == 0) w_ok = mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, a.status) ? 1 : 0;
+        if (lane == 0) w_ok = mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, a.status, a.wait_ns) ? 1 : 0;
         if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
           ok = false;
           break;
@@ -490,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
     }
     if (lane == 0)  // let this pipeline's last copies land
       for (int j = iq > HS ? iq - HS : 0; j < iq; ++j)
-        mbar_wait(full_bar(q * HS + j % HS), (uint32_t)(j / HS) & 1u, nullptr, a.status);
+        mbar_wait(full_bar(q * HS + j % HS), (uint32_t)(j / HS) & 1u, nullptr, a.status, a.wait_ns);
   } else if ((warp == 1 || warp == kMma1Warp) && lane == 0) {
     // ------------------------------------------------------------- MMA issuers --
     // Issuer q multiplies the k-blocks kb % 2 == q into accumulator q of the
@@ -502,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
       const int num_kb = (wi < total1 ? a.H : a.I) / BK;
       const int acc = tc & 1;
       const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
-      if (!mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag, a.status)) break;
+      if (!mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag, a.status, a.wait_ns)) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)((2 * acc + q) * BNT);
       bool first = true;
@@ -511,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         const int s = q * HS + iq % HS;
         const uint32_t ph = (uint32_t)(iq / HS) & 1u;
         ++iq;
-        if (!mbar_wait(full_bar(s), ph, abort_flag, a.status)) {
+        if (!mbar_wait(full_bar(s), ph, abort_flag, a.status, a.wait_ns)) {
           ok = false;
           break;
         }
@@ -528,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
       if (ok) umma_commit(tfull_bar(acc));
     }
     umma_commit(drain_bar(q));
-    mbar_wait(drain_bar(q), 0, nullptr, a.status);
+    mbar_wait(drain_bar(q), 0, nullptr, a.status, a.wait_ns);
   } else if (warp >= 2 && warp <= 5) {
     // ---------------------------------------------------------------- epilogue --
     pdl_wait();  // the previous kernel may still read what this one writes
@@ -566,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
       const int valid = m_indptr[c.g + 1] - xrow;  // rows of this item (> 0)
       const int acc = tc & 1;
       const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
-      const bool got = mbar_wait(tfull_bar(acc), aph, abort_flag, a.status);
+      const bool got = mbar_wait(tfull_bar(acc), aph, abort_flag, a.status, a.wait_ns);
       if (epi_bar_any(!got)) break;
       float v[BNT];
       tc_fence_after();
@@ -598,10 +600,11 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         if (r < 64) {
           __nv_bfloat16 *h = reinterpret_cast<__nv_bfloat16 *>(a.h);
           const long col = (long)c.m * 64 + r;
+          const float lim = step_limit(a.clamp, c.g);
 #pragma unroll
           for (int j = 0; j < BNT; ++j)
             if (j < valid)
-              h[(long)(xrow + j) * a.I + col] = __float2bfloat16_rn(silu_f32(sg[j * 64 + r]) * v[j]);
+              h[(long)(xrow + j) * a.I + col] = __float2bfloat16_rn(swiglu_step(sg[j * 64 + r], v[j], lim));
         }
         if (MODE == kModeBoth) __threadfence();  // h before the expert's count
         epi_bar();
@@ -706,6 +709,8 @@ cudaError_t launch_inst(const ChainPlan &p, const Launch &l) {
   a.p2e_out = p.p2e;
   a.e2p_out = p.e2p;
   a.status = p.status;
+  a.wait_ns = p.wait_ns;
+  a.clamp = p.clamp;
   a.T = p.T;
   a.k = p.k;
   a.E = p.E;
@@ -757,13 +762,14 @@ int chain_prepare(ChainPlan &p) {
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
-cudaError_t chain_zero_counters(const ChainPlan &p, cudaStream_t stream) {
+cudaError_t chain_zero_counters(const ChainPlan &p, cudaStream_t stream, bool unreachable) {
+  cudaError_t e;
   // the plan lays out done1 right after comb, so one memset covers both
   const char *lo = reinterpret_cast<const char *>(p.comb);
   const char *hi = reinterpret_cast<const char *>(p.done1 + p.L + 1);
-  if (hi > lo && (size_t)(reinterpret_cast<const char *>(p.done1) - lo) < (1u << 20))
+  if (!unreachable && hi > lo && (size_t)(reinterpret_cast<const char *>(p.done1) - lo) < (1u << 20))
     return cudaMemsetAsync(p.comb, 0, (size_t)(hi - lo), stream);
-  cudaError_t e = cudaMemsetAsync(p.done1, 0, ((size_t)p.L + 1) * sizeof(int32_t), stream);
+  e = cudaMemsetAsync(p.done1, unreachable ? 0xFF : 0, ((size_t)p.L + 1) * sizeof(int32_t), stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(p.comb, 0, chain_comb_ints(p.T, p.H) * sizeof(int32_t), stream);
   return e;
 }

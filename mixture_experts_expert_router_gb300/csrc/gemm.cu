@@ -52,6 +52,8 @@ struct GemmArgs {
   const int32_t *group_end;
   void *out;
   int32_t *status;
+  unsigned long long wait_ns;  // bounded-wait limit of this launch
+  const float *clamp;         // SwiGLU epilogue: [groups] SwiGLUStep limits, or null
   long max_rows;
   int G;
   int K;
@@ -211,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         for (int kb = 0; kb < num_kb; ++kb, ++it) {
           const int s = it % C::STAGES;
           const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
-          if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, args.status)) {
+          if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, args.status, args.wait_ns)) {
             ok = false;
             break;
           }
@@ -229,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       }
       // Let every copy this thread started land before the CTA can exit.
       for (int j = it > C::STAGES ? it - C::STAGES : 0; j < it; ++j)
-        mbar_wait(full_bar(j % C::STAGES), (uint32_t)(j / C::STAGES) & 1u, nullptr, args.status);
+        mbar_wait(full_bar(j % C::STAGES), (uint32_t)(j / C::STAGES) & 1u, nullptr, args.status, args.wait_ns);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -239,13 +241,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tc) {
         const int acc = tc & 1;
         const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
-        if (!mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag, args.status)) break;
+        if (!mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag, args.status, args.wait_ns)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
         for (int kb = 0; kb < num_kb; ++kb, ++it) {
           const int s = it % C::STAGES;
           const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
-          if (!mbar_wait(full_bar(s), ph, abort_flag, args.status)) {
+          if (!mbar_wait(full_bar(s), ph, abort_flag, args.status, args.wait_ns)) {
             ok = false;
             break;
           }
@@ -262,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       }
       // Wait for every MMA this thread issued before TMEM can be released.
       umma_commit(drain_bar);
-      mbar_wait(drain_bar, 0, nullptr, args.status);
+      mbar_wait(drain_bar, 0, nullptr, args.status, args.wait_ns);
     }
   } else {
     // ------------------------------------------------------------------ epilogue --
@@ -275,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       const int valid = gend[c.g] - row0;
       const int acc = tc & 1;
       const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
-      if (!mbar_wait(tfull_bar(acc), aph, abort_flag, args.status)) break;
+      if (!mbar_wait(tfull_bar(acc), aph, abort_flag, args.status, args.wait_ns)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
       const bool row_ok = r_in_tile < valid;
@@ -283,6 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       if (EPI == (int)Epi::kSwiGLU) {
         uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(args.out) +
                                                orow * args.n_out + (long)c.n * (BN / 2));
+        const float lim = step_limit(args.clamp, c.g);
 #pragma unroll 1
         for (int col = 0; col < BN / 2; col += 32) {
           uint32_t u[32], g[32];
@@ -297,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             for (int q = 0; q < 2; ++q) {
               const float uu = __uint_as_float(u[2 * i + q]);
               const float gg = __uint_as_float(g[2 * i + q]);
-              hv[q] = silu_f32(gg) * uu;
+              hv[q] = swiglu_step(gg, uu, lim);
             }
             packed[i] = pack_bf16x2(hv[0], hv[1]);
           }
@@ -408,6 +411,8 @@ cudaError_t launch_inst(const GemmPlan &p, const Launch &l) {
   a.group_end = p.group_end;
   a.out = p.out;
   a.status = p.status;
+  a.wait_ns = p.wait_ns;
+  a.clamp = p.clamp;
   a.max_rows = p.max_rows;
   a.G = p.G;
   a.K = p.K;

@@ -95,6 +95,8 @@ struct PairArgs {
   const int32_t *group_end;
   void *out;
   int32_t *status;
+  unsigned long long wait_ns;  // bounded-wait limit of this launch
+  const float *clamp;         // SwiGLU epilogue: [groups] SwiGLUStep limits, or null
   long max_rows;
   int G, K, n_out, b_rows, n_tiles, m_major;
 };
@@ -316,7 +318,7 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : kThreads, 1)
         const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
         const int nk = min(KH, num_kb - kr * KH);
         if (lane == 0) {
-          if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, args.status)) {
+          if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, args.status, args.wait_ns)) {
             ok = false;
             break;
           }
@@ -333,7 +335,7 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : kThreads, 1)
     }
     if (lane == 0 && rank == 0) {  // let both CTAs' last copies land (they all signal the leader)
       for (int j = it > STAGES ? it - STAGES : 0; j < it; ++j)
-        mbar_wait(full_bar(j % STAGES), (uint32_t)(j / STAGES) & 1u, nullptr, args.status);
+        mbar_wait(full_bar(j % STAGES), (uint32_t)(j / STAGES) & 1u, nullptr, args.status, args.wait_ns);
     }
   } else if (warp == kWeightWarp) {
     // -------------------------------------------------------- weight producer --
@@ -353,7 +355,7 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : kThreads, 1)
           const int s = it % STAGES;
           const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
           const int nk = min(KH, num_kb - kr * KH);
-          if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, args.status)) {
+          if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, args.status, args.wait_ns)) {
             ok = false;
             break;
           }
@@ -383,14 +385,14 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : kThreads, 1)
         const uint32_t idesc = c.tail ? idesc_bf16_f32(2 * BM, (uint32_t)tail_n(c.tail)) : IDESC_MAIN;
         const int acc = tc & 1;
         const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
-        if (!mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag, args.status)) break;
+        if (!mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag, args.status, args.wait_ns)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
         for (int kr = 0; kr < n_rounds; ++kr, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
           const int nk = min(KH, num_kb - kr * KH);
-          if (!mbar_wait<GATH>(full_bar(s), ph, abort_flag, args.status)) {
+          if (!mbar_wait<GATH>(full_bar(s), ph, abort_flag, args.status, args.wait_ns)) {
             ok = false;
             break;
           }
@@ -408,7 +410,7 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : kThreads, 1)
         if (ok) umma_commit_pair(tfull_bar(acc), 0x3);
       }
       umma_commit_pair(drain_bar, 0x1);
-      mbar_wait(drain_bar, 0, nullptr, args.status);
+      mbar_wait(drain_bar, 0, nullptr, args.status, args.wait_ns);
     }
   } else if (warp >= 2 && warp <= 5) {
     // ------------------------------------------------------------------ epilogue --
@@ -421,7 +423,7 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : kThreads, 1)
       const PairTile c = decode_pair_tile(t, tile_start, gend, G, args.n_tiles, args.m_major);
       const int acc = tc & 1;
       const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
-      const bool got = mbar_wait(tfull_bar(acc), aph, abort_flag, args.status);
+      const bool got = mbar_wait(tfull_bar(acc), aph, abort_flag, args.status, args.wait_ns);
       if (epi_bar_any(!got)) break;  // all four warps stop together
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
@@ -433,6 +435,7 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : kThreads, 1)
         if (kSwiGLU) {
           uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(args.out) +
                                                  orow * args.n_out + (long)c.n * (BN / 2));
+          const float lim = step_limit(args.clamp, c.g);
 #pragma unroll 1
           for (int col = 0; col < BN / 2; col += 32) {
             uint32_t u[32], g[32];
@@ -442,8 +445,8 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : kThreads, 1)
             uint32_t packed[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-              packed[i] = pack_bf16x2(silu_f32(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]),
-                                      silu_f32(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]));
+              packed[i] = pack_bf16x2(swiglu_step(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i]), lim),
+                                      swiglu_step(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1]), lim));
             if (row_ok) {
 #pragma unroll
               for (int v = 0; v < 4; ++v)
@@ -521,6 +524,7 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : kThreads, 1)
         // tail tile: lanes are weight rows, columns are the tail's tokens
         const int n = tail_n(c.tail);
         const long tok0 = (long)c.gstart + c.mp * 2 * BM;
+        const float lim = step_limit(args.clamp, c.g);
 #pragma unroll 1
         for (int c0 = 0; c0 < n; c0 += 16) {
           uint32_t r[16];
@@ -545,7 +549,7 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : kThreads, 1)
               for (int j = 0; j < 16; ++j)
                 if (c0 + j < c.tail)
                   h[(tok0 + c0 + j) * args.n_out + col] =
-                      __float2bfloat16_rn(silu_f32(sg[j * 64 + r_in_tile]) * __uint_as_float(r[j]));
+                      __float2bfloat16_rn(swiglu_step(sg[j * 64 + r_in_tile], __uint_as_float(r[j]), lim));
             }
             epi_bar();
           } else {
@@ -607,7 +611,7 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : kThreads, 1)
         const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
         const int nk = min(KH, num_kb - kr * KH);
         int w_ok = 1;
-        if (lane == 0) w_ok = mbar_wait(empty_bar(j), ph ^ 1u, abort_flag, args.status) ? 1 : 0;
+        if (lane == 0) w_ok = mbar_wait(empty_bar(j), ph ^ 1u, abort_flag, args.status, args.wait_ns) ? 1 : 0;
         if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
           ok = false;
           break;
@@ -737,6 +741,8 @@ cudaError_t launch_pair_gemm(const GemmPlan &p, const Launch &l) {
   a.group_end = p.group_end;
   a.out = p.out;
   a.status = p.status;
+  a.wait_ns = p.wait_ns;
+  a.clamp = p.clamp;
   a.max_rows = p.max_rows;
   a.G = p.G;
   a.K = p.K;

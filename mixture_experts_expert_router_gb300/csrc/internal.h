@@ -20,6 +20,10 @@ struct Launch {
 
 int device_sm_count();
 
+// Longest a single in-kernel wait may take before the kernel gives up, unless
+// the plan sets another limit (moe_plan_set_wait_limit).
+constexpr unsigned long long kWaitLimitNs = 4000000000ull;  // 4 s
+
 // S1 ---------------------------------------------------------------------------
 cudaError_t launch_route(const float *logits, int T, int E, int k, int32_t *ids, float *w,
                          const Launch &l);
@@ -75,6 +79,8 @@ struct GemmPlan {
   int grid = 0;
   size_t smem = 0;
   int32_t *status = nullptr;
+  unsigned long long wait_ns = kWaitLimitNs;
+  const float *clamp = nullptr;  // SwiGLU epilogue: [G] SwiGLUStep limits (device), or null
 };
 
 // Encodes the tensor maps and picks tile shapes; host only.  allow_pair lets
@@ -109,6 +115,8 @@ struct SwapPlan {
   size_t smem = 0;
   bool swiglu = false;
   bool early = false;           // may read group_end and stream weights before the PDL wait
+  unsigned long long wait_ns = kWaitLimitNs;
+  const float *clamp = nullptr;  // FC1: [G] SwiGLUStep limits (device), or null
 };
 
 int swap_prepare(SwapPlan &p, bool swiglu, const uint16_t *W, int G, int w_rows, int K,
@@ -138,6 +146,8 @@ struct ChainPlan {
   bool ids_early = false;  // ids are layer inputs (pre-routed), not the routing kernel's output
   bool one_launch = false; // FC1 and FC2 in one kernel (CTAs wait for the FC1 tiles of an expert)
   size_t smem = 0;
+  unsigned long long wait_ns = kWaitLimitNs;
+  const float *clamp = nullptr;  // [L] SwiGLUStep limits (device), or null
 };
 size_t chain_comb_ints(int T, int H);
 int chain_prepare(ChainPlan &p);
@@ -145,6 +155,8 @@ int chain_prepare(ChainPlan &p);
 cudaError_t launch_chain(const ChainPlan &p, int part, const Launch &l);
 // One launch keeps counters in the workspace; every launch zeroes them on its
 // stream before the kernel (one memset: done1 follows comb in the workspace).
-cudaError_t chain_zero_counters(const ChainPlan &p, cudaStream_t stream);
+// unreachable: the test hook MOE_PLAN_TEST_UNREACHABLE_WAIT, which fills the
+// per-expert FC1 counts with -1 instead, so that no FC2 wait can complete.
+cudaError_t chain_zero_counters(const ChainPlan &p, cudaStream_t stream, bool unreachable = false);
 
 }  // namespace moe

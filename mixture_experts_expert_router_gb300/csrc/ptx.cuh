@@ -9,12 +9,11 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "internal.h"
 #include "moe_gb300.h"
 
 namespace moe {
 
-// Longest a single in-kernel wait may take before the kernel gives up.
-constexpr unsigned long long kWaitLimitNs = 4000000000ull;  // 4 s
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -73,21 +72,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait until the phase with the given parity of barrier `bar` has completed.
-// Gives up (returns false) when *abort becomes non-zero or after
-// kWaitLimitNs; on a timeout it raises MOE_DEV_TIMEOUT and sets *abort.
+// Gives up (returns false) when *abort becomes non-zero or after limit_ns
+// (the launch's limit, kWaitLimitNs unless the plan set another); on a
+// timeout it raises MOE_DEV_TIMEOUT and sets *abort.
 // `abort` may be null (the final drains, which must run to the end or the
 // time limit whatever the other roles did).  kCluster: acquire at cluster
 // scope, for phases completed by arrivals of the peer CTA's threads.
 template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
-                                          int32_t *status) {
+                                          int32_t *status, unsigned long long limit_ns) {
   if (mbar_try_wait<kCluster>(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait<kCluster>(bar, parity)) return true;
     if ((it & 63u) == 0u) {
       if (abort != nullptr && *abort) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (global_timer_ns() - t0 > limit_ns) {
         if (abort != nullptr) *abort = 1;
         if (status) atomicOr(reinterpret_cast<unsigned int *>(status), MOE_DEV_TIMEOUT);
         return false;
@@ -223,6 +223,19 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
 // gives 1/inf = 0 and silu = -0, the limit.
 __device__ __forceinline__ float silu_f32(float g) {
   return g * __frcp_rn(1.0f + __expf(-g));
+}
+
+// SwiGLU of GEMM1's gate g and up u, silu(g) * u, with the SwiGLUStep(limit)
+// clamp (flashinfer.experimental.cake_stepfun_moe, opening paragraph: a
+// per-expert clamp limit): g from above at lim, u to [-lim, lim] first.  With
+// lim = +inf the clamps change nothing and this is the plain SwiGLU.
+__device__ __forceinline__ float swiglu_step(float g, float u, float lim) {
+  return silu_f32(fminf(g, lim)) * fminf(fmaxf(u, -lim), lim);
+}
+
+// The SwiGLUStep limit of group g: clamp[g], or +inf without limits.
+__device__ __forceinline__ float step_limit(const float *clamp, int g) {
+  return clamp != nullptr ? __ldg(clamp + g) : __int_as_float(0x7f800000);
 }
 
 // ---------------------------------------------------- dependent launch (PDL) --
@@ -365,9 +378,9 @@ __device__ __forceinline__ int ld_acquire_gpu(const int *p) {
 
 // Wait until *counter >= need (another CTA of this grid counts up and
 // releases).  Bounded like mbar_wait: gives up when *abort becomes non-zero or
-// after kWaitLimitNs, raising MOE_DEV_TIMEOUT and setting *abort.
+// after limit_ns, raising MOE_DEV_TIMEOUT and setting *abort.
 __device__ __forceinline__ bool counter_wait(const int *counter, int need, volatile int *abort,
-                                             int32_t *status) {
+                                             int32_t *status, unsigned long long limit_ns) {
   if (ld_acquire_gpu(counter) >= need) return true;
   const unsigned long long t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
@@ -375,7 +388,7 @@ __device__ __forceinline__ bool counter_wait(const int *counter, int need, volat
     if (ld_acquire_gpu(counter) >= need) return true;
     if ((it & 15u) == 0u) {
       if (*abort) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (global_timer_ns() - t0 > limit_ns) {
         *abort = 1;
         if (status) atomicOr(reinterpret_cast<unsigned int *>(status), MOE_DEV_TIMEOUT);
         return false;

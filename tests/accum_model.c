@@ -103,12 +103,14 @@ void am_dots(const uint16_t *A, const uint16_t *B, int M, int N, int K, int mode
 
 /* The layer for the listed tokens.  x [T,H], ids/w [T,k], w1 [L,2I,H],
  * w2 [L,H,I] (bf16 bits); routes to ids outside [off, off+L) contribute zero.
- * out [n_tok, H] bf16 bits; h_out (optional) [n_tok*k, I] bf16 bits.
+ * out [n_tok, H] bf16 bits; h_out (optional) [n_tok*k, I] bf16 bits; clamp
+ * (optional) [L] per-local-expert SwiGLUStep limits (gate clamped from above,
+ * up to [-limit, limit], before silu(g) * u).
  * Returns 0, 1 if an id is outside [0, E), 2 if host memory ran out. */
 int am_moe_tokens(const uint16_t *x, const int32_t *ids, const float *w, const uint16_t *w1,
                   const uint16_t *w2, int T, int H, int I, int E, int k, int off, int L,
                   const int32_t *tokens, int n_tok, uint16_t *out, uint16_t *h_out, int mode,
-                  int nthreads) {
+                  int nthreads, const float *clamp) {
   (void)T;
   int bad = 0;
 #ifdef _OPENMP
@@ -142,9 +144,12 @@ int am_moe_tokens(const uint16_t *x, const int32_t *ids, const float *w, const u
       const int e = g - off;
       const uint16_t *W1 = w1 + (size_t)e * 2 * I * H;
       const uint16_t *W2 = w2 + (size_t)e * H * I;
+      const float lim = clamp ? clamp[e] : INFINITY;
       for (int c = 0; c < I; ++c) {
-        const float u = (float)am_dot(xt, W1 + (size_t)c * H, H, mode);
-        const float gt = (float)am_dot(xt, W1 + (size_t)(I + c) * H, H, mode);
+        float u = (float)am_dot(xt, W1 + (size_t)c * H, H, mode);
+        float gt = (float)am_dot(xt, W1 + (size_t)(I + c) * H, H, mode);
+        gt = gt > lim ? lim : gt;
+        u = u > lim ? lim : (u < -lim ? -lim : u);
         const float silu = gt / (1.0f + expf(-gt));
         hb[c] = am_float_to_bf16(silu * u);
       }

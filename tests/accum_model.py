@@ -57,7 +57,7 @@ def load():
         lib.am_dot.restype = ctypes.c_double
         lib.am_dots.argtypes = [P, P, i, i, i, i, P]
         lib.am_dots.restype = None
-        lib.am_moe_tokens.argtypes = [P, P, P, P, P, i, i, i, i, i, i, i, P, i, P, P, i, i]
+        lib.am_moe_tokens.argtypes = [P, P, P, P, P, i, i, i, i, i, i, i, P, i, P, P, i, i, P]
         lib.am_moe_tokens.restype = i
         _lib = lib
     return _lib
@@ -86,7 +86,7 @@ def dots(A_bits: np.ndarray, B_bits: np.ndarray, mode: int) -> np.ndarray:
 
 
 def moe_tokens(x, ids, w, w1, w2, num_experts, mode, tokens=None, local_offset=0, num_local=None,
-               want_h=False, nthreads=0):
+               want_h=False, nthreads=0, clamp_limit=None):
     """out [n_tok, H] bf16 bits (and h [n_tok*k, I] when asked) for the tokens."""
     x = np.ascontiguousarray(x, np.uint16)
     ids = np.ascontiguousarray(ids, np.int32)
@@ -102,14 +102,16 @@ def moe_tokens(x, ids, w, w1, w2, num_experts, mode, tokens=None, local_offset=0
     n = tokens.shape[0]
     out = np.empty((n, H), np.uint16)
     h = np.zeros((n * k, I), np.uint16) if want_h else None
+    clamp = None if clamp_limit is None else np.ascontiguousarray(clamp_limit, np.float32)
+    assert clamp is None or clamp.shape == (L,)
     rc = load().am_moe_tokens(_p(x), _p(ids), _p(w), _p(w1), _p(w2), T, H, I, num_experts, k, local_offset, L,
-                              _p(tokens), n, _p(out), _p(h), mode, nthreads)
+                              _p(tokens), n, _p(out), _p(h), mode, nthreads, _p(clamp))
     assert rc & 2 == 0, "host memory ran out"
     return (out, h) if want_h else out
 
 
 def floor(x, ids, w, w1, w2, num_experts, want_bits, tokens=None, local_offset=0, num_local=None,
-          max_macs=1.5e10):
+          max_macs=1.5e10, clamp_limit=None):
     """(fraction within 2 bf16 ulp of want_bits, elements compared) for the
     tensor-core model on the first tokens of `tokens` (all T when None) whose
     multiply-adds stay within max_macs; want_bits holds the oracle's output
@@ -126,6 +128,6 @@ def floor(x, ids, w, w1, w2, num_experts, want_bits, tokens=None, local_offset=0
         return 1.0, 0
     sub = tokens[:n]
     out = moe_tokens(x, ids, w, w1, w2, num_experts, TENSOR_CORE, tokens=sub, local_offset=local_offset,
-                     num_local=num_local)
+                     num_local=num_local, clamp_limit=clamp_limit)
     ref = np.asarray(want_bits)[:n]
     return float(np.mean(ulp_distance(out, ref) <= 2)), int(out.size)

@@ -44,7 +44,7 @@ def test_status_strings(lib):
         s = moe.moe_status_string(code)
         assert s and s != "unknown status code"
     assert moe.moe_status_string(-99) == "unknown status code"
-    assert lib.moe_abi_version() == 100
+    assert lib.moe_abi_version() == 101
 
 
 def test_argument_errors_before_device(lib):
@@ -69,6 +69,11 @@ def test_workspace_size_and_prepare_errors(lib):
     d0 = moe._Desc(T=0, H=128, I=128, E=4, top_k=2, local_offset=0, num_local=4)
     assert lib.moe_forward_prepare(ctypes.byref(d0), ctypes.byref(h)) == 0   # T == 0: empty plan
     assert lib.moe_plan_kernels_per_launch(h) == 0
+    # the bounded-wait limit is range-checked on the host
+    assert lib.moe_plan_set_wait_limit(h, moe.WAIT_LIMIT_MIN_NS - 1) == -2
+    assert lib.moe_plan_set_wait_limit(h, moe.WAIT_LIMIT_MAX_NS + 1) == -2
+    assert lib.moe_plan_set_wait_limit(h, 2_000_000) == 0
+    assert lib.moe_plan_set_wait_limit(None, 2_000_000) == -1
     assert lib.moe_plan_destroy(h) == 0
     d = moe._Desc(T=4, H=128, I=128, E=4, top_k=2, local_offset=0, num_local=4)
     assert lib.moe_forward_prepare(ctypes.byref(d), ctypes.byref(h)) == -5   # no routing input
@@ -100,6 +105,8 @@ def test_binding_constants_match_header():
              "MOE_PLAN_ONE_CTA_GEMM": moe.PLAN_ONE_CTA_GEMM, "MOE_PLAN_DECODE_CHAIN": moe.PLAN_DECODE_CHAIN,
              "MOE_PLAN_DECODE_SEPARATE": moe.PLAN_DECODE_SEPARATE, "MOE_PLAN_FUSED_GATHER": moe.PLAN_FUSED_GATHER,
              "MOE_PLAN_DECODE_ONE_LAUNCH": moe.PLAN_DECODE_ONE_LAUNCH,
+             "MOE_PLAN_TEST_UNREACHABLE_WAIT": moe.PLAN_TEST_UNREACHABLE_WAIT,
+             "MOE_WAIT_LIMIT_MIN_NS": moe.WAIT_LIMIT_MIN_NS, "MOE_WAIT_LIMIT_MAX_NS": moe.WAIT_LIMIT_MAX_NS,
              "MOE_DEV_BAD_EXPERT": moe.DEV_BAD_EXPERT, "MOE_DEV_TIMEOUT": moe.DEV_TIMEOUT}
     for name, value in pairs.items():
         assert defines.get(name) == value, name

@@ -33,17 +33,18 @@ def _oracle_route(wl):
     return wl.topk_ids.cpu().numpy(), wl.topk_w.cpu().numpy()
 
 
-def _oracle_out(wl, tokens=None, w1=None, w2=None):
+def _oracle_out(wl, tokens=None, w1=None, w2=None, clamp_limit=None):
     """The oracle's output rows for the tokens, with the end-to-end floor (the
-    tensor-core accumulation model's agreement with them) attached."""
+    tensor-core accumulation model's agreement with them) attached;
+    clamp_limit [L] selects the SwiGLUStep(limit) epilogue."""
     ids, w = _oracle_route(wl)
     w1 = W.bf16_bits(wl.w1) if w1 is None else w1
     w2 = W.bf16_bits(wl.w2) if w2 is None else w2
     x = W.bf16_bits(wl.x)
     out, st = oracle.moe_tokens(x, ids, w, w1, w2, wl.E, tokens=tokens,
-                                local_offset=wl.local_offset, num_local=wl.num_local)
+                                local_offset=wl.local_offset, num_local=wl.num_local, clamp_limit=clamp_limit)
     frac, n = accum_model.floor(x, ids, w, w1, w2, wl.E, out, tokens=tokens, local_offset=wl.local_offset,
-                                num_local=wl.num_local)
+                                num_local=wl.num_local, clamp_limit=clamp_limit)
     return with_floor(out, frac, n), st
 
 
@@ -480,6 +481,41 @@ def test_plans_sharing_one_workspace_alternate():
             check_bf16_end_to_end(W.bf16_bits(p.out), want, f"shared workspace {wl.name} T={wl.T} round {rnd}")
 
 
+def test_bounded_wait_runs_out_reports_and_the_next_launch_is_right():
+    """A one-launch decode chain whose FC2 tiles wait for FC1 counts that can
+    never complete (test hook: the counts start at -1) with a 2 ms wait limit:
+    the launch returns, the status word carries MOE_DEV_TIMEOUT, and a normal
+    plan on the same buffers and workspace then gives the oracle's output with
+    a clean status word (the context stays usable)."""
+    import time
+    wl = W.make_moe(T=2, H=256, I=192, E=16, top_k=4, mode="prerouted", seed=71)
+    d = _dev(wl)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    need = moe.moe_workspace_size(wl.T, wl.H, wl.I, wl.E, wl.top_k, wl.num_local)
+    ws = torch.empty(need, dtype=torch.uint8, device=DEV)
+    out = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=DEV)
+    kw = dict(topk_ids=d["topk_ids"], topk_w=d["topk_w"], out=out, workspace=ws, status=status,
+              path=moe.PATH_DECODE, decode_one_launch=True)
+    hooked = moe.MoEPlan(d["x"], d["w1"], d["w2"], wl.E, wl.top_k, test_unreachable_wait=True, **kw)
+    hooked.set_wait_limit(2_000_000)
+    assert hooked.kernels_per_launch() == 1
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    hooked.launch()
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    assert int(status.item()) & moe.DEV_TIMEOUT, f"status {int(status.item())}"
+    assert dt < 2.0, f"the launch took {dt:.3f} s"
+    normal = moe.MoEPlan(d["x"], d["w1"], d["w2"], wl.E, wl.top_k, **kw)
+    want, _ = _oracle_out(wl)
+    for _ in range(2):
+        out.fill_(7.0)
+        normal.launch()
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        check_bf16_end_to_end(W.bf16_bits(out), want, "launch after a timed-out launch")
+
+
 @pytest.mark.parametrize("one", [False, True])
 def test_decode_chain_status_and_bad_ids(one):
     wl = W.make_moe(T=6, H=128, I=128, E=9, top_k=3, mode="prerouted", seed=12)
@@ -509,3 +545,57 @@ def test_decode_chain_expert_shard(off, L, one):
     assert plan.kernels_per_launch() == (2 if one else 3)  # route + the chain kernel(s)
     want, _ = _oracle_out(wl)
     check_bf16_end_to_end(W.bf16_bits(out), want, f"chain shard {off}+{L}")
+
+
+# ------------------------------------------------------- SwiGLUStep(limit) --
+
+def _limits(L, seed):
+    """Per-expert limits that bind on N(0,1) GEMM1 outputs (plus one +inf)."""
+    lim = np.random.default_rng(seed).uniform(0.4, 2.5, size=L).astype(np.float32)
+    lim[0] = np.inf
+    return lim
+
+
+@pytest.mark.parametrize("T,H,I,E,k", [(600, 256, 192, 12, 3), (40, 512, 256, 9, 4)])
+def test_swiglu_step_stage_parity(T, H, I, E, k):
+    """moe_fc1_swiglu with clamp limits on the oracle's gathered rows against
+    the oracle's SwiGLUStep h (strict rule); limits of +inf give moe_fc1_swiglu
+    bitwise."""
+    wl = W.make_moe(T=T, H=H, I=I, E=E, top_k=k, mode="logits", seed=T + 5)
+    ids, _ = _oracle_route(wl)
+    m_o, p2e_o, _, _ = oracle.sort(ids, E)
+    xp = W.bf16_bits(wl.x)[p2e_o // k]
+    lim = _limits(E, T)
+    rows = np.arange(len(p2e_o), dtype=np.int32)
+    want = oracle.fc1_swiglu_rows(xp, W.bf16_bits(wl.w1), m_o[1:], rows, clamp_limit=lim)
+    xp_d, w1_d, m_d = W.from_bf16_bits(xp).to(DEV), wl.w1.to(DEV), torch.from_numpy(m_o).to(DEV)
+    h = moe.moe_fc1_swiglu(xp_d, w1_d, m_d, clamp_limit=torch.from_numpy(lim).to(DEV))
+    torch.cuda.synchronize()
+    check_bf16_close(W.bf16_bits(h), want, f"SwiGLUStep h T={T} H={H} I={I}")
+    plain = moe.moe_fc1_swiglu(xp_d, w1_d, m_d)
+    inf = moe.moe_fc1_swiglu(xp_d, w1_d, m_d, clamp_limit=torch.full((E,), float("inf"), device=DEV))
+    torch.cuda.synchronize()
+    assert torch.equal(plain, inf)
+    assert not torch.equal(plain, h)  # the finite limits bind
+
+
+@pytest.mark.parametrize("form", ["pair", "one_cta", "decode_separate", "decode_chain", "one_launch"])
+def test_swiglu_step_layer_every_form(form):
+    """The whole layer with per-expert SwiGLUStep limits on every kernel form
+    against the oracle's SwiGLUStep layer."""
+    decode = form.startswith("decode") or form == "one_launch"
+    T = 3 if decode else 600
+    wl = W.make_moe(T=T, H=256, I=192, E=12, top_k=3, mode="logits", seed=90 + T)
+    d = _dev(wl)
+    lim = _limits(wl.E, 7)
+    plan = moe.MoEPlan(d["x"], d["w1"], d["w2"], wl.E, wl.top_k, logits=d["logits"],
+                       path=moe.PATH_DECODE if decode else moe.PATH_GROUPED, one_cta_gemm=form == "one_cta",
+                       decode_chain=True if form == "decode_chain" else (False if form == "decode_separate" else None),
+                       decode_one_launch=form == "one_launch", clamp_limit=torch.from_numpy(lim).to(DEV))
+    out = plan.launch()
+    torch.cuda.synchronize()
+    assert int(plan.status.item()) == 0
+    want, _ = _oracle_out(wl, clamp_limit=lim)
+    check_bf16_end_to_end(W.bf16_bits(out), want, f"SwiGLUStep layer ({form})")
+    plain, _ = _oracle_out(wl)
+    assert not np.array_equal(np.asarray(plain), np.asarray(want))  # the limits change the layer
