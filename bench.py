@@ -633,6 +633,104 @@ def run_grouped_gemm(args, world, rank, local):
     return 0
 
 
+def run_grouped_gemm_bwd(args, world, rank, local):
+    """One step = the backward of the ragged grouped GEMM on the grouped-GEMM
+    workload (sum_m=16384 rows over 64 Dirichlet(0.3)-sized groups, K=4096,
+    N=1536): dX = G W[g] (dgrad, bf16) and dW[g] = G^T X (wgrad, fp32), each
+    timed alone as back-to-back CUDA-graph replays, inputs resident in HBM."""
+    import mixture_experts_expert_router_gb300 as moe
+    from mixture_experts_expert_router_gb300 import workloads as W
+    moe.library()
+    dev = torch.device("cuda", local)
+    d = W.make_grouped_gemm(seed=args.seed + rank, device="cpu", weights_device=dev, with_grad=True)
+    X, G, Wt, offs = d["X"].to(dev), d["G"].to(dev), d["W"], d["offs"].to(dev)
+    sum_m, E, K, N = d["sum_m"], d["E"], d["K"], d["N"]
+    dX = torch.empty((sum_m, K), dtype=torch.bfloat16, device=dev)
+    dW = torch.empty((E, N, K), dtype=torch.float32, device=dev)
+    active = int((d["sizes"] > 0).sum())
+    F = 2.0 * sum_m * K * N
+    B_dgrad = active * N * K * 2.0 + sum_m * N * 2.0 + sum_m * K * 2.0       # W (non-empty), G, dX
+    B_wgrad = sum_m * N * 2.0 + sum_m * K * 2.0 + E * N * K * 4.0            # G, X, every dW[e] (fp32)
+    stream = torch.cuda.current_stream(dev)
+    calls = {"dgrad": lambda: moe.grouped_gemm_dgrad(G, Wt, offs, dX),
+             "wgrad": lambda: moe.grouped_gemm_wgrad(G, X, offs, out_dtype=torch.float32, dW=dW)}
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            for fn in calls.values():
+                fn()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    graphs = {}
+    for name, fn in calls.items():
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        graphs[name] = g
+    clocks = ClockSampler(str(local))
+    time.sleep(0.3)
+    for _ in range(args.warmup):
+        for g in graphs.values():
+            g.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.time()
+    ms = {}
+    for name, g in graphs.items():
+        ms[name] = max_over_ranks(world, timed_steps(g.replay, args.steps, stream)) / args.steps
+    t1 = time.time()
+    # end to end: G and X in from pinned host memory, dX and dW back, every step
+    G_h, X_h = d["G"].pin_memory(), d["X"].pin_memory()
+    dX_h = torch.empty(dX.shape, dtype=dX.dtype).pin_memory()
+    dW_h = torch.empty(dW.shape, dtype=dW.dtype).pin_memory()
+
+    def e2e():
+        G.copy_(G_h, non_blocking=True)
+        X.copy_(X_h, non_blocking=True)
+        calls["dgrad"]()
+        calls["wgrad"]()
+        dX_h.copy_(dX, non_blocking=True)
+        dW_h.copy_(dW, non_blocking=True)
+    for _ in range(args.warmup):
+        e2e()
+    torch.cuda.synchronize()
+    n_e2e = min(args.steps, 50)
+    ms_e2e = max_over_ranks(world, timed_steps(e2e, n_e2e, stream)) / n_e2e
+    clocks.stop()
+    if rank != 0:
+        return 0
+    peaks, src = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    step_ms = ms["dgrad"] + ms["wgrad"]
+    rows_all = sum_m * world
+
+    def roof(name, B):
+        gbs = B / (ms[name] / 1000.0) / 1e9
+        return {"kernel": f"grouped_gemm_{name}", "bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                "frac": gbs / hbm, "traffic": None, "bytes_per_launch": B, "flops_per_launch": F,
+                "tflops": F / (ms[name] / 1000.0) / 1e12, "ms": ms[name], "peak_kind": f"{src} HBM copy bandwidth"}
+    r_d, r_w = roof("dgrad", B_dgrad), roof("wgrad", B_wgrad)
+    line = {
+        "metric": METRIC, "value": rows_all / (step_ms / 1000.0), "unit": "rows/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded)",
+        "config": {"workload": "grouped_gemm_bwd", "sum_m": sum_m, "E": E, "K": K, "N": N,
+                   "empty_groups": int((d["sizes"] == 0).sum()), "dW": "fp32",
+                   "l2": "inputs larger than L2 (W is 805 MB, dW 1.6 GB)",
+                   "parallelism": "single GPU" if world == 1 else f"replicas x{world}"},
+        "roofline": r_w if r_w["ms"] >= r_d["ms"] else r_d,
+        "kernels": {"dgrad": r_d, "wgrad": r_w},
+        "timing": "each kernel as back-to-back CUDA-graph replays; step = dgrad + wgrad",
+        "e2e": {"value": rows_all / (ms_e2e / 1000.0), "unit": "rows/s",
+                "h2d_bytes_per_step": (G_h.numel() + X_h.numel()) * 2,
+                "d2h_bytes_per_step": dX_h.numel() * 2 + dW_h.numel() * 4},
+        "gpu_launches": 2 * args.steps, "clocks": clocks.summary(t0, t1),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -665,6 +763,8 @@ def main():
             return run_reference(args, world, rank)
         if args.config == "grouped_gemm":
             return run_grouped_gemm(args, world, rank, local)
+        if args.config == "grouped_gemm_bwd":
+            return run_grouped_gemm_bwd(args, world, rank, local)
         return run_ours(args, world, rank, local)
     finally:
         if world > 1:

@@ -241,6 +241,27 @@ MOE_API int moe_finalize(const float *y, const int32_t *exp_to_perm,
 MOE_API int grouped_gemm_fwd(const moe_bf16 *X, const moe_bf16 *W, const int32_t *offs,
                      int sum_m, int E, int N, int K, moe_bf16 *Y, void *stream);
 
+/* ---- ragged grouped GEMM backward ---------------------------------------------------------
+ * The dgrad and wgrad rows of Cake ragged BF16 grouped GEMM, operation table
+ * (and its Autograd section: x.grad from dgrad, w.grad from wgrad), groups as
+ * in grouped_gemm_fwd (offs [E] cumulative ends read on the device; groups may
+ * be empty or any size; no padding, no host synchronisation).  bf16 operands,
+ * fp32 accumulation in a fixed order, no atomics: replays are bitwise equal.
+ *
+ * grouped_gemm_dgrad: dX[offs[e-1]:offs[e]] = G[offs[e-1]:offs[e]] . W[e],
+ *   W used in place.  G [sum_m, N], W [E, N, K], dX [sum_m, K] bf16 (rows
+ *   outside [0, offs[E-1]) are not written).
+ * grouped_gemm_wgrad: dW[e] = G[offs[e-1]:offs[e]]^T . X[offs[e-1]:offs[e]]
+ *   for every e, exactly zero for an empty group.  G [sum_m, N], X [sum_m, K],
+ *   dW [E, N, K] fp32 (dw_fp32 != 0) or bf16 (one rounding of the fp32 sum).
+ * N % 64 == 0, K % 64 == 0, 1 <= E <= MOE_MAX_EXPERTS, offs[E-1] <= sum_m;
+ * pointers 16-byte aligned.  sum_m == 0: dgrad does nothing, wgrad zeroes dW. */
+MOE_API int grouped_gemm_dgrad(const moe_bf16 *G, const moe_bf16 *W, const int32_t *offs,
+                               int sum_m, int E, int N, int K, moe_bf16 *dX, void *stream);
+MOE_API int grouped_gemm_wgrad(const moe_bf16 *G, const moe_bf16 *X, const int32_t *offs,
+                               int sum_m, int E, int N, int K, void *dW, int dw_fp32,
+                               void *stream);
+
 /* ---- whole layer (one shot) --------------------------------------------------------------
  * Routing inputs: exactly one of
  *   logits [T, E] fp32                      (RoutingInputMode.FromLogits), or

@@ -25,7 +25,7 @@ __all__ = [
     "MoEError", "library", "library_path", "moe_status_string", "moe_route", "moe_sort", "moe_sort_no_alloc",
     "moe_sort_workspace_size", "moe_gather", "moe_fc1_swiglu", "moe_fc2", "moe_finalize",
     "moe_fc1_swiglu_swapab", "moe_fc2_swapab", "moe_fc1_swiglu_gathered",
-    "grouped_gemm_fwd", "moe_workspace_size", "moe_forward", "MoEPlan", "ABI_SYMBOLS",
+    "grouped_gemm_fwd", "grouped_gemm_dgrad", "grouped_gemm_wgrad", "moe_workspace_size", "moe_forward", "MoEPlan", "ABI_SYMBOLS",
     "PATH_AUTO", "PATH_GROUPED", "PATH_DECODE", "DEV_BAD_EXPERT", "DEV_TIMEOUT",
 ]
 
@@ -52,7 +52,7 @@ ABI_SYMBOLS = [
     "moe_plan_buffers_get", "moe_plan_stage_count", "moe_plan_stage_name", "moe_plan_stage_times",
     "moe_plan_stage_reset", "moe_plan_kernels_per_launch", "moe_plan_destroy", "moe_sort_no_alloc",
     "moe_fc1_swiglu_swapab", "moe_fc2_swapab", "moe_fc1_swiglu_gathered", "moe_plan_set_wait_limit",
-    "moe_fc1_swiglu_step",
+    "moe_fc1_swiglu_step", "grouped_gemm_dgrad", "grouped_gemm_wgrad",
 ]
 
 
@@ -114,6 +114,8 @@ def library():
             "moe_fc2_swapab": ([P, P, P, I, I, I, I, I, P, P], I),
             "moe_finalize": ([P, P, P, I, I, I, P, P], I),
             "grouped_gemm_fwd": ([P, P, P, I, I, I, I, P, P], I),
+            "grouped_gemm_dgrad": ([P, P, P, I, I, I, I, P, P], I),
+            "grouped_gemm_wgrad": ([P, P, P, I, I, I, I, P, I, P], I),
             "moe_workspace_size": ([I, I, I, I, I, I], Z),
             "moe_forward": ([P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, Z, P, P], I),
             "moe_forward_prepare": ([ctypes.POINTER(_Desc), ctypes.POINTER(P)], I),
@@ -365,6 +367,42 @@ def grouped_gemm_fwd(X: torch.Tensor, W: torch.Tensor, offs: torch.Tensor, Y=Non
     _check(library().grouped_gemm_fwd(_ptr(X), _ptr(W), _ptr(offs), sum_m, E, N, K, _ptr(Y),
                                       _stream(X.device)), "grouped_gemm_fwd")
     return Y
+
+
+def grouped_gemm_dgrad(G: torch.Tensor, W: torch.Tensor, offs: torch.Tensor, dX=None):
+    """Data gradient of the ragged grouped GEMM: dX[group e] = G[group e] @ W[e]
+    (W [E, N, K] used in place, bf16)."""
+    _need(G, torch.bfloat16, "G")
+    _need(W, torch.bfloat16, "W")
+    _need(offs, torch.int32, "offs")
+    sum_m, N = G.shape
+    E, N2, K = W.shape
+    if N2 != N or offs.numel() != E:
+        raise ValueError("shapes: G [sum_m, N], W [E, N, K], offs [E]")
+    dX = torch.empty((sum_m, K), dtype=torch.bfloat16, device=G.device) if dX is None else dX
+    _need(dX, torch.bfloat16, "dX", (sum_m, K), G.device)
+    _check(library().grouped_gemm_dgrad(_ptr(G), _ptr(W), _ptr(offs), sum_m, E, N, K, _ptr(dX),
+                                        _stream(G.device)), "grouped_gemm_dgrad")
+    return dX
+
+
+def grouped_gemm_wgrad(G: torch.Tensor, X: torch.Tensor, offs: torch.Tensor, out_dtype=torch.float32, dW=None):
+    """Weight gradient of the ragged grouped GEMM: dW[e] = G[group e].T @ X[group e]
+    ([E, N, K], fp32 or bf16; exactly zero for an empty group)."""
+    _need(G, torch.bfloat16, "G")
+    _need(X, torch.bfloat16, "X")
+    _need(offs, torch.int32, "offs")
+    sum_m, N = G.shape
+    sum_m2, K = X.shape
+    E = offs.numel()
+    if sum_m2 != sum_m or out_dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("shapes: G [sum_m, N], X [sum_m, K], offs [E]; out_dtype fp32 or bf16")
+    dW = torch.empty((E, N, K), dtype=out_dtype, device=G.device) if dW is None else dW
+    _need(dW, out_dtype, "dW", (E, N, K), G.device)
+    _check(library().grouped_gemm_wgrad(_ptr(G), _ptr(X), _ptr(offs), sum_m, E, N, K, _ptr(dW),
+                                        1 if out_dtype == torch.float32 else 0, _stream(G.device)),
+           "grouped_gemm_wgrad")
+    return dW
 
 
 # ------------------------------------------------------------ whole layer --

@@ -347,6 +347,40 @@ int grouped_gemm_fwd(const moe_bf16 *X, const moe_bf16 *W, const int32_t *offs, 
   return cuda_rc(launch_gemm(p, l));
 }
 
+int grouped_gemm_dgrad(const moe_bf16 *G, const moe_bf16 *W, const int32_t *offs, int sum_m, int E,
+                       int N, int K, moe_bf16 *dX, void *stream) {
+  if (sum_m < 0 || E < 1 || E > MOE_MAX_EXPERTS || N <= 0 || K <= 0 || N % 64 || K % 64)
+    return MOE_ERR_SHAPE;
+  if (sum_m == 0) return MOE_OK;
+  if (!G || !W || !offs || !dX) return MOE_ERR_NULL;
+  if (!aligned16(G) || !aligned16(W) || !aligned16(dX)) return MOE_ERR_ALIGN;
+  if (int rc = check_device()) return rc;
+  BwdPlan p;
+  if (int rc = bwd_prepare(p, false, false, G, W, offs, sum_m, E, N, K, dX, nullptr)) return rc;
+  Launch l;
+  l.stream = static_cast<cudaStream_t>(stream);
+  return cuda_rc(launch_bwd(p, l));
+}
+
+int grouped_gemm_wgrad(const moe_bf16 *G, const moe_bf16 *X, const int32_t *offs, int sum_m, int E,
+                       int N, int K, void *dW, int dw_fp32, void *stream) {
+  if (sum_m < 0 || E < 1 || E > MOE_MAX_EXPERTS || N <= 0 || K <= 0 || N % 64 || K % 64)
+    return MOE_ERR_SHAPE;
+  if (!dW) return MOE_ERR_NULL;
+  if (!aligned16(dW)) return MOE_ERR_ALIGN;
+  if (int rc = check_device()) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (sum_m == 0)  // every group is empty: dW is exactly zero
+    return cuda_rc(cudaMemsetAsync(dW, 0, (size_t)E * N * K * (dw_fp32 ? 4 : 2), s));
+  if (!G || !X || !offs) return MOE_ERR_NULL;
+  if (!aligned16(G) || !aligned16(X)) return MOE_ERR_ALIGN;
+  BwdPlan p;
+  if (int rc = bwd_prepare(p, true, dw_fp32 != 0, G, X, offs, sum_m, E, N, K, dW, nullptr)) return rc;
+  Launch l;
+  l.stream = s;
+  return cuda_rc(launch_bwd(p, l));
+}
+
 size_t moe_workspace_size(int T, int H, int I, int E, int top_k, int num_local) {
   if (check_layer_shape(T, H, I, E, top_k, 0, num_local) != MOE_OK) return 0;
   return ws_layout(T, H, I, top_k, num_local).total;

@@ -103,6 +103,25 @@ bool pair_gemm_supported(Epi epi, int n_out);
 cudaError_t pair_gemm_configure(Epi epi, size_t smem);
 cudaError_t launch_pair_gemm(const GemmPlan &p, const Launch &l);
 
+// Grouped GEMM backward (gemm_bwd.cu): dgrad dX = G . W[g] (W in place) and
+// wgrad dW[g] = G^T . X over each group's rows, one-CTA tcgen05 kernels with
+// MN-major operands.
+struct BwdPlan {
+  CUtensorMap map_a, map_b;
+  const int32_t *group_end = nullptr;
+  void *out = nullptr;
+  int32_t *status = nullptr;
+  unsigned long long wait_ns = kWaitLimitNs;
+  long sum_m = 0;
+  int E = 0, N = 0, K = 0, mode = 0, grid = 0;
+  size_t smem = 0;
+};
+// G [sum_m, N]; B = W [E, N, K] (dgrad) or X [sum_m, K] (wgrad); out dX
+// [sum_m, K] bf16, or dW [E, N, K] fp32 / bf16.  N % 64 == 0, K % 64 == 0.
+int bwd_prepare(BwdPlan &p, bool wgrad, bool out_f32, const uint16_t *G, const uint16_t *B,
+                const int32_t *offs, long sum_m, int E, int N, int K, void *out, int32_t *status);
+cudaError_t launch_bwd(const BwdPlan &p, const Launch &l);
+
 // S7: swap-AB weight-streaming GEMMs for few tokens per expert (decode.cu) ----
 struct SwapPlan {
   CUtensorMap map_w;            // weights [G * w_rows, K], box {64, 64 | 128}
