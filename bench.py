@@ -243,8 +243,8 @@ def make_workload(args, rank, weights_device):
     if args.shape:
         T, H, I, E, k = (int(v) for v in args.shape.split(","))
         wl = W.make_moe(T=T, H=H, I=I, E=E, top_k=k, mode="logits", seed=args.seed + rank, device="cpu",
-                        weights_device=weights_device)
-        wl.name = f"custom_T{T}_H{H}_I{I}_E{E}_k{k}"
+                        weights_device=weights_device, bias=f"zipf{args.zipf}" if args.zipf else None)
+        wl.name = f"custom_T{T}_H{H}_I{I}_E{E}_k{k}" + (f"_zipf{args.zipf}" if args.zipf else "")
         return wl
     return W.make_moe(args.config, seed=args.seed + rank, device="cpu", weights_device=weights_device)
 
@@ -741,6 +741,8 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--shape", default=None,
                     help="T,H,I,E,top_k of a custom logits-routed workload (profiling runs)")
+    ap.add_argument("--zipf", type=float, default=None,
+                    help="with --shape: per-expert logit bias ln p_e, p_e ~ rank^-s (imbalanced groups)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch the plan directly instead of a CUDA graph")
     ap.add_argument("--decode-chain", action="store_true", help="decode path: always the two-kernel chain")
