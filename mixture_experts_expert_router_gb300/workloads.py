@@ -15,6 +15,10 @@ Distributions (one independent stream per tensor, derived from ``seed``):
   grouped GEMM sizes: Dirichlet(alpha * 1_E) proportions of sum_m, floored,
            the remainder handed to the largest fractional parts.
   grouped GEMM upstream gradient G ~ N(0, 1)  bf16 [sum_m, N] (backward).
+  BGMV LoRA-MoE: x ~ N(0,1) [T, H]; per slice A ~ N(0, 1/H) [L, E, R, H] and
+           B ~ N(0, 1/R) [L, E, F, R]; each token a uniform LoRA index and a
+           uniform k-subset of the experts, weights a flat Dirichlet draw; pairs
+           laid out token-major (p = t*k + j) or sorted by expert (stable).
 
 Small tensors are drawn on the host with numpy's PCG64 generator (the same
 stream on every platform) and converted to bf16 by round-to-nearest-even.
@@ -169,6 +173,48 @@ def make_grouped_gemm(*, seed: int = 0, device="cpu", weights_device=None, sum_m
     if with_grad:
         out["G"] = _normal_bf16((cfg["sum_m"], cfg["N"]), 1.0, seed, 14).to(device)
     return out
+
+
+@dataclass
+class BgmvWorkload:
+    """BGMV LoRA-MoE inputs (prepare_bgmv_moe's tensors)."""
+    T: int
+    H: int
+    R: int
+    E: int
+    num_loras: int
+    top_k: int
+    x: torch.Tensor                 # [T, H] bf16
+    lora_a: list                    # per slice [L, E, R, H] bf16
+    lora_b: list                    # per slice [L, E, F_s, R] bf16
+    tok: torch.Tensor               # [P] int32 (sorted_token_ids)
+    eid: torch.Tensor               # [P] int32 (expert_ids)
+    lora: torch.Tensor              # [T] int32 (lora_indices)
+    w: torch.Tensor                 # [P] fp32 (topk_weights)
+    contiguous: bool                # pairs laid out p = t*k + j
+
+
+def make_bgmv(*, T: int, H: int, R: int, E: int, num_loras: int, top_k: int, feat_out=None, slices: int = 1,
+              contiguous: bool = True, seed: int = 0, device="cpu", weights_device=None) -> BgmvWorkload:
+    wdev = device if weights_device is None else weights_device
+    F = list(feat_out) if feat_out is not None else [H] * slices
+    x = _normal_bf16((T, H), 1.0, seed, 21).to(device)
+    A = [_normal_bf16((num_loras, E, R, H), 1.0 / np.sqrt(H), seed, 22 + 2 * s, wdev) for s in range(len(F))]
+    B = [_normal_bf16((num_loras, E, F[s], R), 1.0 / np.sqrt(R), seed, 23 + 2 * s, wdev) for s in range(len(F))]
+    r = _rng(seed, 24)
+    lora = r.integers(0, num_loras, size=T).astype(np.int32)
+    ex = np.argsort(r.random((T, E)), axis=1)[:, :top_k].astype(np.int32)
+    wt = r.dirichlet(np.ones(top_k), size=T).astype(np.float32)
+    tok = np.repeat(np.arange(T, dtype=np.int32), top_k)
+    eid, w = ex.ravel(), wt.ravel()
+    if not contiguous:  # expert-sorted dispatch order (stable)
+        order = np.argsort(eid, kind="stable")
+        tok, eid, w = tok[order], eid[order], w[order]
+    return BgmvWorkload(T=T, H=H, R=R, E=E, num_loras=num_loras, top_k=top_k, x=x, lora_a=A, lora_b=B,
+                        tok=torch.from_numpy(np.ascontiguousarray(tok)).to(device),
+                        eid=torch.from_numpy(np.ascontiguousarray(eid)).to(device),
+                        lora=torch.from_numpy(lora).to(device),
+                        w=torch.from_numpy(np.ascontiguousarray(w)).to(device), contiguous=contiguous)
 
 
 def bf16_bits(t: torch.Tensor) -> np.ndarray:

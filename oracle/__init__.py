@@ -74,6 +74,8 @@ def _declare(lib):
     lib.oracle_grouped_gemm_dgrad_rows.restype = None
     lib.oracle_grouped_gemm_wgrad_rows.argtypes = [P, P, P, i, i, i, P, P, i, P, P, i]
     lib.oracle_grouped_gemm_wgrad_rows.restype = None
+    lib.oracle_bgmv.argtypes = [P, i, i, P, P, i, P, i, i, i, P, P, P, P, i, P, P, i, i]
+    lib.oracle_bgmv.restype = i
     lib.oracle_float_to_bf16.argtypes = [ctypes.c_float]
     lib.oracle_float_to_bf16.restype = ctypes.c_uint16
     lib.oracle_bf16_to_float.argtypes = [ctypes.c_uint16]
@@ -251,6 +253,36 @@ def grouped_gemm_wgrad_rows(G, X, offs, sel_e, sel_n, K=None, nthreads=0, lib=No
     lib.oracle_grouped_gemm_wgrad_rows(_p(G), _p(X), _p(offs), offs.shape[0], N, K, _p(sel_e), _p(sel_n), n,
                                        _p(f32), _p(b16), nthreads)
     return f32, b16
+
+
+def bgmv(x, lora_a, lora_b, tok, eid, lora, w, nthreads=0, lib=None):
+    """BGMV LoRA-MoE shrink + expand (prepare_bgmv_moe).
+
+    x [T, H] u16; lora_a / lora_b lists (one entry per slice) of
+    [num_loras, E, R, H] / [num_loras, E, F_s, R] u16; tok, eid [P] int32 per
+    routed pair; lora [T] int32 per token; w [P] fp32.
+    Returns (shrink [S, P, R] u16, y [T, sum F_s] fp32, status)."""
+    lib = lib or load()
+    x = _c(x, np.uint16)
+    T, H = x.shape
+    A = [_c(a, np.uint16) for a in lora_a]
+    B = [_c(b, np.uint16) for b in lora_b]
+    S = len(A)
+    L, E, R, H2 = A[0].shape
+    assert H2 == H and all(a.shape == (L, E, R, H) for a in A)
+    F = [b.shape[2] for b in B]
+    assert all(b.shape == (L, E, f, R) for b, f in zip(B, F))
+    tok, eid, lora, w = _c(tok, np.int32), _c(eid, np.int32), _c(lora, np.int32), _c(w, np.float32)
+    P = tok.shape[0]
+    shrink = np.empty((S, P, R), np.uint16)
+    y = np.empty((T, sum(F)), np.float32)
+    a_ptrs = (ctypes.c_void_p * S)(*[a.ctypes.data for a in A])
+    b_ptrs = (ctypes.c_void_p * S)(*[b.ctypes.data for b in B])
+    f_arr = (ctypes.c_int * S)(*F)
+    st = lib.oracle_bgmv(_p(x), T, H, ctypes.cast(a_ptrs, ctypes.c_void_p), ctypes.cast(b_ptrs, ctypes.c_void_p),
+                         S, ctypes.cast(f_arr, ctypes.c_void_p), L, E, R, _p(tok), _p(eid), _p(lora), _p(w), P,
+                         _p(shrink), _p(y), sum(F), nthreads)
+    return shrink, y, st
 
 
 def bf16_to_f32(a: np.ndarray) -> np.ndarray:

@@ -25,6 +25,9 @@
  *   [P1] same page, opening paragraph and "Unified MoE API opt-in": the
  *        StepFun activation SwiGLUStep(limit) with a per-expert clamp limit
  *        (gemm1_clamp_limit).
+ *   [P5] "flashinfer.fused_moe.prepare_bgmv_moe": BGMV LoRA shrink + expand
+ *        over routed (token, expert) pairs, one owner per output that
+ *        accumulates routes in fixed input order, FP32 output accumulator.
  *   [P3] "Cake ragged BF16 grouped GEMM (experimental)", operation table:
  *        Y[offs[e-1]:offs[e]] = X[offs[e-1]:offs[e]] . W[e]^T, offs holding
  *        cumulative group end offsets, groups may be empty; dgrad
@@ -429,6 +432,101 @@ void oracle_grouped_gemm_wgrad_rows(const uint16_t *G, const uint16_t *X,
             if (dW_bf16) dW_bf16[(size_t)q * K + c] = float_to_bf16(acc);
         }
     }
+}
+
+/* ---- BGMV LoRA-MoE shrink + expand  [P5 prepare_bgmv_moe: description and
+ * Parameters] -------------------------------------------------------------
+ *
+ * Routed pairs p = 0..P-1 (any order): token t = tok[p], expert e = eid[p],
+ * LoRA l = lora[t], routing weight w[p].  For every slice s of the S slices
+ * (rank R; A_s [num_loras, E, R, H], B_s [num_loras, E, F_s, R], bf16):
+ *
+ *   shrink[s, p, r] = bf16( sum_h A_s[l, e, r, h] * x[t, h] )
+ *                     (fp32, sequential in h; the shrink workspace holds the
+ *                     weight dtype)
+ *   y[t, off_s + f] = sum over the pairs p of token t, in ascending p, of
+ *                     w[p] * ( sum_r B_s[l, e, f, r] * shrink[s, p, r] )
+ *                     (fp32, sequential; "each output has one owner that
+ *                     accumulates routes in fixed input order")
+ *
+ * where off_s = F_0 + .. + F_{s-1} and y has ld_y >= sum F_s floats per row.
+ * A token without pairs gets zeros.  A pair whose token, expert or LoRA index
+ * is out of range is dropped (its shrink rows are zero) and the call returns
+ * ORACLE_BAD_EXPERT ("out-of-range routing indices" are invalid inputs). */
+int oracle_bgmv(const uint16_t *x, int T, int H, const uint16_t *const *lora_a,
+                const uint16_t *const *lora_b, int S, const int *feat_out,
+                int num_loras, int E, int R, const int32_t *tok,
+                const int32_t *eid, const int32_t *lora, const float *w, int P,
+                uint16_t *shrink, float *y, int ld_y, int nthreads) {
+    int status = 0;
+    char *ok = (char *)malloc((size_t)(P > 0 ? P : 1));
+    for (int p = 0; p < P; ++p) {
+        int t = tok[p];
+        int good = t >= 0 && t < T && eid[p] >= 0 && eid[p] < E;
+        if (good) good = lora[t] >= 0 && lora[t] < num_loras;
+        ok[p] = (char)good;
+        if (!good) status |= ORACLE_BAD_EXPERT;
+    }
+    set_threads(nthreads);
+    /* shrink, pair by pair */
+    for (int sl = 0; sl < S; ++sl) {
+#pragma omp parallel for schedule(dynamic, 16)
+        for (int p = 0; p < P; ++p) {
+            uint16_t *out = shrink + ((size_t)sl * P + p) * R;
+            if (!ok[p]) {
+                for (int r = 0; r < R; ++r) out[r] = 0;
+                continue;
+            }
+            int t = tok[p];
+            const uint16_t *a = lora_a[sl] +
+                                (((size_t)lora[t] * E + eid[p]) * R) * (size_t)H;
+            for (int r = 0; r < R; ++r) {
+                float acc = 0.0f;
+                for (int h = 0; h < H; ++h)
+                    acc = acc + bf16_to_float(a[(size_t)r * H + h]) *
+                                    bf16_to_float(x[(size_t)t * H + h]);
+                out[r] = float_to_bf16(acc);
+            }
+        }
+    }
+    /* the pairs of each token in ascending p */
+    int *cnt = (int *)calloc((size_t)T + 1, sizeof(int));
+    int *list = (int *)malloc(sizeof(int) * (size_t)(P > 0 ? P : 1));
+    for (int p = 0; p < P; ++p)
+        if (ok[p]) cnt[tok[p] + 1]++;
+    for (int t = 0; t < T; ++t) cnt[t + 1] += cnt[t];
+    int *fill = (int *)malloc(sizeof(int) * (size_t)(T > 0 ? T : 1));
+    for (int t = 0; t < T; ++t) fill[t] = cnt[t];
+    for (int p = 0; p < P; ++p)
+        if (ok[p]) list[fill[tok[p]]++] = p;
+    /* expand: one owner per output row */
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int t = 0; t < T; ++t) {
+        int col = 0;
+        for (int sl = 0; sl < S; ++sl) {
+            int F = feat_out[sl];
+            for (int f = 0; f < F; ++f) {
+                float acc = 0.0f;
+                for (int q = cnt[t]; q < cnt[t + 1]; ++q) {
+                    int p = list[q];
+                    const uint16_t *b = lora_b[sl] +
+                                        (((size_t)lora[t] * E + eid[p]) * F + f) * (size_t)R;
+                    const uint16_t *sp = shrink + ((size_t)sl * P + p) * R;
+                    float v = 0.0f;
+                    for (int r = 0; r < R; ++r)
+                        v = v + bf16_to_float(b[r]) * bf16_to_float(sp[r]);
+                    acc = acc + w[p] * v;
+                }
+                y[(size_t)t * ld_y + col + f] = acc;
+            }
+            col += F;
+        }
+    }
+    free(fill);
+    free(list);
+    free(cnt);
+    free(ok);
+    return status;
 }
 
 int oracle_max_threads(void) {

@@ -47,6 +47,9 @@ MUTANTS = {
                                "            for (int n = 0; n < N - 1; ++n)\n                acc = acc + bf16_to_float(gr[n]) *")],
     "wgrad_takes_next_row": [("for (int p = start; p < end; ++p)",
                               "for (int p = start; p < end + (end < offs[E - 1]); ++p)")],
+    "bgmv_wrong_lora": [("(((size_t)lora[t] * E + eid[p]) * R) * (size_t)H;",
+                         "(((size_t)(num_loras - 1 - lora[t]) * E + eid[p]) * R) * (size_t)H;")],
+    "bgmv_drops_weight": [("acc = acc + w[p] * v;", "acc = acc + v;")],
     "finalize_skips_slot0": [("            for (int j = 0; j < k; ++j) {\n                int p = exp_to_perm[(size_t)t * k + j];",
                               "            for (int j = 1; j < k; ++j) {\n                int p = exp_to_perm[(size_t)t * k + j];")],
 }
@@ -67,6 +70,8 @@ PIN_CALLS = [
     ("dgrad_torch", lambda: pins.test_grouped_gemm_dgrad_vs_torch_per_group()),
     ("wgrad_torch", lambda: pins.test_grouped_gemm_wgrad_vs_torch_per_group_and_empty_groups_zero()),
     ("gg_adjoint", lambda: pins.test_grouped_gemm_adjoint_identity()),
+    ("bgmv_torch", lambda: pins.test_bgmv_vs_torch_per_pair(False)),
+    ("bgmv_invariants", lambda: pins.test_bgmv_rank_padding_linearity_and_zero_b()),
     ("step_per_expert", lambda: pins.test_swiglu_step_infinite_limit_is_plain_swiglu_and_limits_are_per_local_expert()),
 ]
 

@@ -519,6 +519,78 @@ def test_grouped_gemm_adjoint_identity():
     assert abs(by_dx - fwd) <= 2e-3 * scale, (by_dx, fwd)   # dX carries one bf16 rounding
 
 
+# ----------------------------------------------------- BGMV LoRA-MoE --------
+# flashinfer.fused_moe.prepare_bgmv_moe: shrink s = bf16(A[l,e] x[t]) per pair,
+# expand y[t] = sum over the token's pairs (ascending) of w * (B[l,e] s), fp32.
+
+def _bgmv_bits(wl):
+    return (W.bf16_bits(wl.x), [W.bf16_bits(a) for a in wl.lora_a], [W.bf16_bits(b) for b in wl.lora_b],
+            wl.tok.numpy(), wl.eid.numpy(), wl.lora.numpy(), wl.w.numpy())
+
+
+@pytest.mark.parametrize("contiguous", [True, False])
+def test_bgmv_vs_torch_per_pair(contiguous):
+    wl = W.make_bgmv(T=40, H=64, R=16, E=6, num_loras=3, top_k=2, feat_out=[64, 32], contiguous=contiguous,
+                     seed=5)
+    x, A, B, tok, eid, lora, w = _bgmv_bits(wl)
+    shrink, y, st = oracle.bgmv(x, A, B, tok, eid, lora, w)
+    assert st == 0
+    xf = torch.from_numpy(bf16_to_f64(x).astype(np.float32))
+    want_y = torch.zeros((wl.T, y.shape[1]), dtype=torch.float64)
+    col = 0
+    for s in range(2):
+        Af = torch.from_numpy(bf16_to_f64(A[s]).astype(np.float32))
+        Bf = torch.from_numpy(bf16_to_f64(B[s]).astype(np.float32))
+        la, ea = torch.from_numpy(lora[tok].astype(np.int64)), torch.from_numpy(eid.astype(np.int64))
+        sh = torch.bmm(Af[la, ea], xf[torch.from_numpy(tok.astype(np.int64))].unsqueeze(2)).squeeze(2)
+        check_bf16_close(shrink[s], torch_bf16_bits(sh.numpy()), f"shrink slice {s}")
+        sp = torch.from_numpy(bf16_to_f64(shrink[s]).astype(np.float32))          # the oracle's own s
+        v = torch.bmm(Bf[la, ea], sp.unsqueeze(2)).squeeze(2) * torch.from_numpy(w).unsqueeze(1)
+        F = Bf.shape[2]
+        want_y[:, col:col + F].index_add_(0, torch.from_numpy(tok.astype(np.int64)), v.double())
+        col += F
+    from tests.tolerances import check_f32_close
+    check_f32_close(y, want_y.numpy(), "bgmv y")
+
+
+def test_bgmv_rank_padding_linearity_and_zero_b():
+    wl = W.make_bgmv(T=30, H=64, R=8, E=4, num_loras=2, top_k=3, seed=6)
+    x, A, B, tok, eid, lora, w = _bgmv_bits(wl)
+    _, y, _ = oracle.bgmv(x, A, B, tok, eid, lora, w)
+    # zero-padding the rank from 8 to 16 adds exact zero terms: y is bitwise equal
+    A2 = np.zeros(A[0].shape[:2] + (16, 64), np.uint16)
+    A2[:, :, :8] = A[0]
+    B2 = np.zeros(B[0].shape[:3] + (16,), np.uint16)
+    B2[..., :8] = B[0]
+    _, y2, _ = oracle.bgmv(x, [A2], [B2], tok, eid, lora, w)
+    assert np.array_equal(y, y2)
+    # doubling every routing weight doubles y exactly (a power-of-two scale)
+    _, y3, _ = oracle.bgmv(x, A, B, tok, eid, lora, 2 * w)
+    assert np.array_equal(2 * y, y3)
+    # B = 0 gives y = 0
+    _, y4, _ = oracle.bgmv(x, A, [np.zeros_like(B[0])], tok, eid, lora, w)
+    assert not np.any(y4)
+
+
+def test_bgmv_out_of_range_pairs_are_dropped_and_flagged():
+    wl = W.make_bgmv(T=20, H=64, R=8, E=4, num_loras=2, top_k=2, seed=7)
+    x, A, B, tok, eid, lora, w = _bgmv_bits(wl)
+    _, y_ok, st = oracle.bgmv(x, A, B, tok, eid, lora, w)
+    assert st == 0
+    keep = np.ones(len(tok), bool)
+    keep[[3, 10]] = False
+    eid_bad = eid.copy()
+    eid_bad[3] = 9            # expert out of range
+    lora_bad = lora.copy()
+    lora_bad[tok[10]] = 5     # LoRA of token tok[10] out of range: all its pairs drop
+    keep[tok == tok[10]] = False
+    shrink, y_bad, st = oracle.bgmv(x, A, B, tok, eid_bad, lora_bad, w)
+    assert st == oracle.BAD_EXPERT
+    assert not np.any(shrink[0][~keep])
+    _, y_ref, _ = oracle.bgmv(x, A, B, tok[keep], eid[keep], lora, w[keep])
+    assert np.array_equal(y_bad, y_ref)
+
+
 def test_workload_generator_is_seeded():
     a = W.make_moe("tiny", seed=0)
     b = W.make_moe("tiny", seed=0)
