@@ -731,6 +731,99 @@ def run_grouped_gemm_bwd(args, world, rank, local):
     return 0
 
 
+BGMV_WORKLOAD = dict(T=2048, H=3072, R=32, E=64, num_loras=4, top_k=2)
+
+
+def run_bgmv(args, world, rank, local):
+    """One step = one BGMV LoRA-MoE shrink + expand (moe_bgmv) over T=2048
+    tokens, hidden 3072 (feat_out = hidden), rank 32, 64 experts, 4 LoRAs,
+    contiguous top-2 pairs; inputs resident in HBM, steps rotating over
+    copies of the LoRA banks whose used weights together exceed L2."""
+    import mixture_experts_expert_router_gb300 as moe
+    from mixture_experts_expert_router_gb300 import workloads as W
+    moe.library()
+    dev = torch.device("cuda", local)
+    c = BGMV_WORKLOAD
+    wl = W.make_bgmv(T=c["T"], H=c["H"], R=c["R"], E=c["E"], num_loras=c["num_loras"], top_k=c["top_k"],
+                     seed=args.seed + rank, device="cpu", weights_device=dev)
+    x, tok, eid, lora, w = (t.to(dev) for t in (wl.x, wl.tok, wl.eid, wl.lora, wl.w))
+    T, H, R, P = wl.T, wl.H, wl.R, wl.tok.numel()
+    used = len(set(zip(wl.lora.numpy()[wl.tok.numpy()].tolist(), wl.eid.numpy().tolist())))
+    w_bytes = used * (R * H + H * R) * 2.0            # A and B of every (LoRA, expert) pair used
+    B = w_bytes + T * H * 2.0 + T * H * 4.0 + P * (4 + 4 + 4) + T * 4 + 2 * P * R * 2.0
+    banks = 1 if 3 * w_bytes >= 3 * L2_NOMINAL else min(MAX_BANKS, int(np.ceil(3 * L2_NOMINAL / w_bytes)))
+    A = [wl.lora_a[0]] + [wl.lora_a[0].clone() for _ in range(banks - 1)]
+    Bw = [wl.lora_b[0]] + [wl.lora_b[0].clone() for _ in range(banks - 1)]
+    y = torch.empty((T, H), dtype=torch.float32, device=dev)
+    sh = torch.empty((1, P, R), dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    calls = [(lambda i=i: moe.bgmv(x, [A[i]], [Bw[i]], tok, eid, lora, w, contiguous_top_k=wl.top_k,
+                                   shrink_out=sh, y_accum=y, status=status)) for i in range(banks)]
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for fn in calls:
+            fn()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    graphs = []
+    for fn in calls:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        graphs.append(g)
+    k = [0]
+
+    def step():
+        graphs[k[0] % banks].replay()
+        k[0] += 1
+    clocks = ClockSampler(str(local))
+    time.sleep(0.3)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.time()
+    ms = max_over_ranks(world, timed_steps(step, args.steps, stream))
+    t1 = time.time()
+    x_h = wl.x.pin_memory()
+    y_h = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+
+    def e2e():
+        x.copy_(x_h, non_blocking=True)
+        step()
+        y_h.copy_(y, non_blocking=True)
+    for _ in range(args.warmup):
+        e2e()
+    torch.cuda.synchronize()
+    ms_e2e = max_over_ranks(world, timed_steps(e2e, args.steps, stream))
+    clocks.stop()
+    if rank != 0:
+        return 0
+    peaks, src = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    step_s = ms / 1000.0 / args.steps
+    gbs = B / step_s / 1e9
+    line = {
+        "metric": METRIC, "value": T * world / step_s, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded)",
+        "config": {"workload": "bgmv", **c, "feat_out": H, "slices": 1, "pairs": "contiguous top-k",
+                   "lora_pairs_used": used,
+                   "l2": f"steps rotate over {banks} copies of the LoRA banks" if banks > 1 else "weights exceed L2",
+                   "parallelism": "single GPU" if world == 1 else f"replicas x{world}"},
+        "roofline": {"kernel": "moe_bgmv (shrink + expand)", "bound": "hbm", "achieved": gbs, "peak": hbm,
+                     "unit": "GB/s", "frac": gbs / hbm, "traffic": None, "bytes_per_launch": B,
+                     "peak_kind": f"{src} HBM copy bandwidth"},
+        "e2e": {"value": T * world / (ms_e2e / 1000.0 / args.steps), "unit": "tokens/s",
+                "h2d_bytes_per_step": x_h.numel() * 2, "d2h_bytes_per_step": y_h.numel() * 4},
+        "gpu_launches": 2 * args.steps, "clocks": clocks.summary(t0, t1), "device_status": int(status.item()),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -767,6 +860,8 @@ def main():
             return run_grouped_gemm(args, world, rank, local)
         if args.config == "grouped_gemm_bwd":
             return run_grouped_gemm_bwd(args, world, rank, local)
+        if args.config == "bgmv":
+            return run_bgmv(args, world, rank, local)
         return run_ours(args, world, rank, local)
     finally:
         if world > 1:

@@ -262,6 +262,44 @@ MOE_API int grouped_gemm_wgrad(const moe_bf16 *G, const moe_bf16 *X, const int32
                                int sum_m, int E, int N, int K, void *dW, int dw_fp32,
                                void *stream);
 
+/* ---- BGMV LoRA-MoE shrink + expand ------------------------------------------------------------
+ * LoRA deltas of the routed (token, expert) pairs of an MoE layer
+ * (flashinfer.fused_moe.prepare_bgmv_moe, description and Parameters).  For
+ * routed pair p: t = sorted_token_ids[p], e = expert_ids[p], l = lora_indices[t].
+ * For every slice s (rank R; A_s = lora_a[s] [num_loras, E, R, H],
+ * B_s = lora_b[s] [num_loras, E, feat_out[s], R], bf16):
+ *   shrink_out[s, p, r] = bf16( A_s[l, e, r, :] . x[t, :] )      (fp32 sum)
+ *   y_accum[t, off_s + f] = sum over the pairs p of token t, in ascending p,
+ *                           of topk_weights[p] * (B_s[l, e, f, :] . shrink_out[s, p, :])
+ * in fp32 (off_s = feat_out[0] + .. + feat_out[s-1]).  Each output element is
+ * written by one owner that adds the token's pairs in that fixed order, so
+ * replays are bitwise identical; a token without pairs gets zeros.  The
+ * library's readings: y_accum is overwritten (not added to), and the shrink
+ * values are rounded to bf16 (the weight dtype of the page's shrink
+ * workspace) before the expand.
+ *   x [T, H] bf16 (H % 8 == 0); lora_a, lora_b, feat_out: HOST arrays of
+ *   num_slices (1..8) device pointers / sizes (feat_out[s] % 8 == 0);
+ *   rank in {8, 16, 32, 64}; sorted_token_ids, expert_ids, topk_weights
+ *   [num_pairs]; lora_indices [T]; shrink_out [num_slices, num_pairs, rank]
+ *   bf16; y_accum [T, ld_y] fp32, ld_y >= sum feat_out (it may be a column
+ *   slice of a wider row-major buffer).
+ *   contiguous_top_k = k > 0 (k <= MOE_MAX_TOP_K): the pairs are token-major,
+ *   pair p of token p / k (num_pairs == T * k), no index is built; 0: any
+ *   order (e.g. sorted by expert), through a route index in the workspace of
+ *   moe_bgmv_workspace_size(T, num_pairs, 0) bytes (zero bytes for k > 0).
+ *   A pair whose token, expert or LoRA index is out of range (or, with
+ *   contiguous_top_k, whose token is not p / k) contributes nothing and raises
+ *   MOE_DEV_BAD_EXPERT in *status (cleared first; optional).
+ * No allocation, no host synchronisation: capturable in a CUDA graph. */
+MOE_API size_t moe_bgmv_workspace_size(int T, int num_pairs, int contiguous_top_k);
+MOE_API int moe_bgmv(const moe_bf16 *x, int T, int H, const moe_bf16 *const *lora_a,
+                     const moe_bf16 *const *lora_b, int num_slices, const int *feat_out, int rank,
+                     int num_loras, int E, const int32_t *sorted_token_ids,
+                     const int32_t *expert_ids, const int32_t *lora_indices,
+                     const float *topk_weights, int num_pairs, int contiguous_top_k,
+                     moe_bf16 *shrink_out, float *y_accum, int ld_y, void *workspace,
+                     size_t workspace_bytes, int32_t *status, void *stream);
+
 /* ---- whole layer (one shot) --------------------------------------------------------------
  * Routing inputs: exactly one of
  *   logits [T, E] fp32                      (RoutingInputMode.FromLogits), or

@@ -25,7 +25,7 @@ __all__ = [
     "MoEError", "library", "library_path", "moe_status_string", "moe_route", "moe_sort", "moe_sort_no_alloc",
     "moe_sort_workspace_size", "moe_gather", "moe_fc1_swiglu", "moe_fc2", "moe_finalize",
     "moe_fc1_swiglu_swapab", "moe_fc2_swapab", "moe_fc1_swiglu_gathered",
-    "grouped_gemm_fwd", "grouped_gemm_dgrad", "grouped_gemm_wgrad", "moe_workspace_size", "moe_forward", "MoEPlan", "ABI_SYMBOLS",
+    "grouped_gemm_fwd", "grouped_gemm_dgrad", "grouped_gemm_wgrad", "bgmv", "moe_workspace_size", "moe_forward", "MoEPlan", "ABI_SYMBOLS",
     "PATH_AUTO", "PATH_GROUPED", "PATH_DECODE", "DEV_BAD_EXPERT", "DEV_TIMEOUT",
 ]
 
@@ -52,7 +52,7 @@ ABI_SYMBOLS = [
     "moe_plan_buffers_get", "moe_plan_stage_count", "moe_plan_stage_name", "moe_plan_stage_times",
     "moe_plan_stage_reset", "moe_plan_kernels_per_launch", "moe_plan_destroy", "moe_sort_no_alloc",
     "moe_fc1_swiglu_swapab", "moe_fc2_swapab", "moe_fc1_swiglu_gathered", "moe_plan_set_wait_limit",
-    "moe_fc1_swiglu_step", "grouped_gemm_dgrad", "grouped_gemm_wgrad",
+    "moe_fc1_swiglu_step", "grouped_gemm_dgrad", "grouped_gemm_wgrad", "moe_bgmv_workspace_size", "moe_bgmv",
 ]
 
 
@@ -115,6 +115,8 @@ def library():
             "moe_finalize": ([P, P, P, I, I, I, P, P], I),
             "grouped_gemm_fwd": ([P, P, P, I, I, I, I, P, P], I),
             "grouped_gemm_dgrad": ([P, P, P, I, I, I, I, P, P], I),
+            "moe_bgmv_workspace_size": ([I, I, I], Z),
+            "moe_bgmv": ([P, I, I, P, P, I, P, I, I, I, P, P, P, P, I, I, P, P, I, P, Z, P, P], I),
             "grouped_gemm_wgrad": ([P, P, P, I, I, I, I, P, I, P], I),
             "moe_workspace_size": ([I, I, I, I, I, I], Z),
             "moe_forward": ([P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, Z, P, P], I),
@@ -403,6 +405,54 @@ def grouped_gemm_wgrad(G: torch.Tensor, X: torch.Tensor, offs: torch.Tensor, out
                                         1 if out_dtype == torch.float32 else 0, _stream(G.device)),
            "grouped_gemm_wgrad")
     return dW
+
+
+def bgmv(x, lora_a, lora_b, sorted_token_ids, expert_ids, lora_indices, topk_weights, contiguous_top_k=0,
+         shrink_out=None, y_accum=None, workspace=None, status=None):
+    """BGMV LoRA-MoE shrink + expand (moe_bgmv): returns (y_accum [T, sum F]
+    fp32, shrink_out [S, P, R] bf16).  lora_a / lora_b are lists with one
+    tensor per slice ([L, E, R, H] / [L, E, F_s, R] bf16)."""
+    _need(x, torch.bfloat16, "x")
+    T, H = x.shape
+    S = len(lora_a)
+    if S < 1 or len(lora_b) != S:
+        raise ValueError("lora_a and lora_b need one tensor per slice")
+    L, E, R, H2 = lora_a[0].shape
+    if H2 != H:
+        raise ValueError("lora_a must be [num_loras, E, rank, H]")
+    F = []
+    for a_s, b_s in zip(lora_a, lora_b):
+        _need(a_s, torch.bfloat16, "lora_a", (L, E, R, H), x.device)
+        _need(b_s, torch.bfloat16, "lora_b", None, x.device)
+        if tuple(b_s.shape[:2]) != (L, E) or b_s.shape[3] != R:
+            raise ValueError("lora_b must be [num_loras, E, feat_out, rank]")
+        F.append(int(b_s.shape[2]))
+    P = sorted_token_ids.numel()
+    for t_, n_, dt in ((sorted_token_ids, "sorted_token_ids", torch.int32), (expert_ids, "expert_ids", torch.int32),
+                       (topk_weights, "topk_weights", torch.float32)):
+        _need(t_, dt, n_, (P,), x.device)
+    _need(lora_indices, torch.int32, "lora_indices", (T,), x.device)
+    dev = x.device
+    shrink_out = torch.empty((S, P, R), dtype=torch.bfloat16, device=dev) if shrink_out is None else shrink_out
+    _need(shrink_out, torch.bfloat16, "shrink_out", (S, P, R), dev)
+    if y_accum is None:
+        y_accum = torch.empty((T, sum(F)), dtype=torch.float32, device=dev)
+    if y_accum.dtype != torch.float32 or not y_accum.is_cuda or y_accum.shape[0] != T or y_accum.stride(1) != 1:
+        raise ValueError("y_accum must be a CUDA fp32 [T, >= sum(feat_out)] tensor with unit column stride")
+    need = int(library().moe_bgmv_workspace_size(T, P, contiguous_top_k))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+    a_ptrs = (ctypes.c_void_p * S)(*[a_s.data_ptr() for a_s in lora_a])
+    b_ptrs = (ctypes.c_void_p * S)(*[b_s.data_ptr() for b_s in lora_b])
+    f_arr = (ctypes.c_int * S)(*F)
+    _check(library().moe_bgmv(_ptr(x), T, H, ctypes.cast(a_ptrs, ctypes.c_void_p), ctypes.cast(b_ptrs, ctypes.c_void_p),
+                              S, ctypes.cast(f_arr, ctypes.c_void_p), R, L, E, _ptr(sorted_token_ids),
+                              _ptr(expert_ids), _ptr(lora_indices), _ptr(topk_weights), P, contiguous_top_k,
+                              _ptr(shrink_out), _ptr(y_accum), y_accum.stride(0), _ptr(workspace),
+                              workspace.numel(), _ptr(status), _stream(dev)), "moe_bgmv")
+    return y_accum, shrink_out
 
 
 # ------------------------------------------------------------ whole layer --

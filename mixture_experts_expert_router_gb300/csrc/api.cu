@@ -381,6 +381,77 @@ int grouped_gemm_wgrad(const moe_bf16 *G, const moe_bf16 *X, const int32_t *offs
   return cuda_rc(launch_bwd(p, l));
 }
 
+size_t moe_bgmv_workspace_size(int T, int num_pairs, int contiguous_top_k) {
+  (void)num_pairs;
+  if (T < 0 || contiguous_top_k < 0) return 0;
+  return bgmv_workspace_bytes(T, contiguous_top_k);
+}
+
+int moe_bgmv(const moe_bf16 *x, int T, int H, const moe_bf16 *const *lora_a,
+             const moe_bf16 *const *lora_b, int num_slices, const int *feat_out, int rank,
+             int num_loras, int E, const int32_t *sorted_token_ids, const int32_t *expert_ids,
+             const int32_t *lora_indices, const float *topk_weights, int num_pairs,
+             int contiguous_top_k, moe_bf16 *shrink_out, float *y_accum, int ld_y,
+             void *workspace, size_t workspace_bytes, int32_t *status, void *stream) {
+  if (T < 0 || H <= 0 || H % 8 || num_slices < 1 || num_slices > kBgmvMaxSlices || num_loras < 1 ||
+      E < 1 || num_pairs < 0 || contiguous_top_k < 0 || contiguous_top_k > MOE_MAX_TOP_K)
+    return MOE_ERR_SHAPE;
+  if (rank != 8 && rank != 16 && rank != 32 && rank != 64) return MOE_ERR_SHAPE;
+  if (contiguous_top_k > 0 && (long)T * contiguous_top_k != num_pairs) return MOE_ERR_SHAPE;
+  if (!lora_a || !lora_b || !feat_out) return MOE_ERR_NULL;
+  long cols = 0;
+  for (int s = 0; s < num_slices; ++s) {
+    if (feat_out[s] <= 0 || feat_out[s] % 8) return MOE_ERR_SHAPE;
+    cols += feat_out[s];
+  }
+  if (ld_y < cols) return MOE_ERR_SHAPE;
+  if (T == 0) return MOE_OK;
+  if (!x || !y_accum || (num_pairs > 0 && (!sorted_token_ids || !expert_ids || !lora_indices ||
+                                           !topk_weights || !shrink_out)))
+    return MOE_ERR_NULL;
+  for (int s = 0; s < num_slices; ++s) {
+    if (!lora_a[s] || !lora_b[s]) return MOE_ERR_NULL;
+    if (!aligned16(lora_a[s]) || !aligned16(lora_b[s])) return MOE_ERR_ALIGN;
+  }
+  if (!aligned16(x)) return MOE_ERR_ALIGN;
+  const size_t need = bgmv_workspace_bytes(T, contiguous_top_k);
+  if (need > 0 && (!workspace || workspace_bytes < need)) return MOE_ERR_WORKSPACE;
+  if (int rc = check_device()) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (status && cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
+  BgmvPlan p;
+  p.x = x;
+  int off = 0;
+  for (int i = 0; i < num_slices; ++i) {
+    p.a[i] = lora_a[i];
+    p.b[i] = lora_b[i];
+    p.f[i] = feat_out[i];
+    p.off[i] = off;
+    off += feat_out[i];
+  }
+  p.tok = sorted_token_ids;
+  p.eid = expert_ids;
+  p.lora = lora_indices;
+  p.w = topk_weights;
+  p.shrink = shrink_out;
+  p.y = y_accum;
+  p.ws = static_cast<int32_t *>(workspace);
+  p.status = status;
+  p.T = T;
+  p.H = H;
+  p.R = rank;
+  p.S = num_slices;
+  p.L = num_loras;
+  p.E = E;
+  p.P = num_pairs;
+  p.k = contiguous_top_k;
+  p.ld_y = ld_y;
+  Launch l;
+  l.stream = s;
+  l.pdl = true;
+  return cuda_rc(launch_bgmv(p, l));
+}
+
 size_t moe_workspace_size(int T, int H, int I, int E, int top_k, int num_local) {
   if (check_layer_shape(T, H, I, E, top_k, 0, num_local) != MOE_OK) return 0;
   return ws_layout(T, H, I, top_k, num_local).total;

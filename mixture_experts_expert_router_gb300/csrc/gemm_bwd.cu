@@ -29,8 +29,13 @@
 // CTA (224 threads, one per SM, persistent): warp 0 TMA producer, warp 1 TMEM
 // owner and MMA issuer (M = 128, N = 256, K = 16), warps 2..5 epilogue, warp 6
 // the masking warp (wgrad).  Two 256-column TMEM accumulators alternate so the
-// epilogue of one tile overlaps the main loop of the next.  Every wait is
-// bounded (the plan's wait limit); a timeout raises MOE_DEV_TIMEOUT.
+// epilogue of one tile overlaps the main loop of the next.  wgrad's output
+// (dW, [E, N, K], the larger part of its traffic) leaves the epilogue as
+// 128-byte-wide column chunks of the tile staged in 128-byte-swizzled shared
+// memory and written by TMA bulk stores through a 3-D [E, N, K] tensor map,
+// which clips a partial tile at N instead of writing into the next expert's
+// rows.  Every wait is bounded (the plan's wait limit); a timeout raises
+// MOE_DEV_TIMEOUT.
 #include <cuda_bf16.h>
 
 #include "launch.cuh"
@@ -51,7 +56,9 @@ constexpr int B_BYTES = BN * BK * 2;          // 32 KB: four 8 KB chunks
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int CHUNK = 64 * BK * 2;            // one 64 x 64 box: 8 KB
 constexpr int NBARS = 3 * STAGES + 5;         // full, ready, empty, tfull[2], tempty[2], drain
-constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+constexpr int STG_OFF = STAGES * STAGE_BYTES;  // wgrad: one 128-row x 128-byte staging chunk
+constexpr int STG_BYTES = BM * 128;
+constexpr int BAR_OFF = STG_OFF + STG_BYTES;
 constexpr int MISC_OFF = BAR_OFF + NBARS * 8; // tmem base, abort flag
 constexpr int TAB_OFF = MISC_OFF + 16;
 constexpr uint32_t TMEM_COLS = 2 * BN;
@@ -61,6 +68,7 @@ enum Mode : int { kDgrad = 0, kWgradF32 = 1, kWgradBf16 = 2 };
 struct BwdArgs {
   CUtensorMap map_a;   // dgrad: G [sum_m, N] box {64, 128}; wgrad: G [sum_m, N] box {64, 64}
   CUtensorMap map_b;   // dgrad: W [E*N, K] box {64, 64};   wgrad: X [sum_m, K] box {64, 64}
+  CUtensorMap map_o;   // wgrad: dW [E, N, K] store map, box {128 bytes of K, 128, 1}
   const int32_t *group_end;
   void *out;           // dgrad: dX [sum_m, K] bf16; wgrad: dW [E, N, K]
   int32_t *status;
@@ -86,6 +94,24 @@ __device__ __forceinline__ uint64_t smem_desc_mn_sw128(uint32_t saddr, uint32_t 
 // kind::f16 instruction descriptor bits marking A / B as MN-major.
 constexpr uint32_t kTransposeA = 1u << 15;
 constexpr uint32_t kTransposeB = 1u << 16;
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// True on every epilogue thread when `flag` is set on any of the 128 (the
+// epilogue leaves its loop together, so no named barrier waits for a thread
+// that has gone).
+__device__ __forceinline__ bool epi_bar_any(bool flag) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, 1, 128, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)flag)
+      : "memory");
+  return r != 0;
+}
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -330,7 +356,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_bwd_kernel(const __grid_c
       const Tile c = decode<MODE>(t, tile_start, G, a);
       const int acc = tc & 1;
       const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
-      if (!mbar_wait(tfull_bar(acc), aph, abort_flag, a.status, a.wait_ns)) break;
+      const bool got = mbar_wait(tfull_bar(acc), aph, abort_flag, a.status, a.wait_ns);
+      if (epi_bar_any(!got)) break;  // all four warps stop together
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
       const int col0 = c.n * BN;
@@ -354,33 +381,45 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_bwd_kernel(const __grid_c
           }
         }
       } else {
-        const int n_row = c.m * BM + r_in_tile;  // row of dW[g]
-        const bool row_ok = n_row < a.N;
+        // dW[g] rows c.m * BM .., columns col0 ..: 128-byte column chunks
+        // (32 fp32 or 64 bf16) staged swizzled, then one TMA store each
+        constexpr int CW = MODE == kWgradF32 ? 32 : 64;  // columns per chunk
         const bool empty = gend[c.g] <= gstart(c.g);
-        const long orow = (long)c.g * a.N + n_row;
+        const int etid = threadIdx.x - 64;
+        const uint32_t row_addr = smem_base + STG_OFF + r_in_tile * 128;
 #pragma unroll 1
-        for (int col = 0; col < BN; col += 32) {
-          uint32_t r[32];
-          if (!empty) {
-            tmem_ld_32x32b_x32(taddr + col, r);
+        for (int col = 0; col < BN && col0 + col < a.K; col += CW) {
+          uint32_t v[32];  // this row's 128 bytes of the chunk
+          if (empty) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = 0u;  // +0.0
+          } else if (MODE == kWgradF32) {
+            tmem_ld_32x32b_x32(taddr + col, v);
             tmem_ld_wait();
           } else {
+            uint32_t r0[32], r1[32];
+            tmem_ld_32x32b_x32(taddr + col, r0);
+            tmem_ld_32x32b_x32(taddr + col + 32, r1);
+            tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) r[j] = 0u;  // +0.0
+            for (int j = 0; j < 16; ++j) {
+              v[j] = pack2(__uint_as_float(r0[2 * j]), __uint_as_float(r0[2 * j + 1]));
+              v[16 + j] = pack2(__uint_as_float(r1[2 * j]), __uint_as_float(r1[2 * j + 1]));
+            }
           }
-          if (!row_ok || col0 + col >= a.K) continue;
-          if (MODE == kWgradF32) {
-            uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<float *>(a.out) + orow * a.K + col0 + col);
+          if (etid == 0) bulk_wait_read<0>();  // the previous store has read the staging chunk
+          epi_bar();
 #pragma unroll
-            for (int v = 0; v < 8; ++v) dst[v] = make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
-          } else {
-            uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(a.out) + orow * a.K + col0 + col);
-#pragma unroll
-            for (int v = 0; v < 4; ++v)
-              dst[v] = make_uint4(pack2(__uint_as_float(r[8 * v]), __uint_as_float(r[8 * v + 1])),
-                                  pack2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3])),
-                                  pack2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5])),
-                                  pack2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7])));
+          for (int q = 0; q < 8; ++q)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                             row_addr + (uint32_t)((q ^ (r_in_tile & 7)) * 16)),
+                         "r"(v[4 * q]), "r"(v[4 * q + 1]), "r"(v[4 * q + 2]), "r"(v[4 * q + 3])
+                         : "memory");
+          fence_proxy_async_smem();
+          epi_bar();
+          if (etid == 0) {
+            tma_store_3d(&a.map_o, smem_base + STG_OFF, col0 + col, c.m * BM, c.g);
+            bulk_commit();
           }
         }
       }
@@ -389,6 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_bwd_kernel(const __grid_c
     }
   }
 
+  if (kW && threadIdx.x == 64) bulk_wait_all();  // the last stores are done before the CTA exits
   __syncthreads();
   if (warp == 1) {
     __syncwarp();
@@ -425,11 +465,36 @@ int encode(CUtensorMap *map, const void *ptr, long rows, int cols, int box_rows)
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_TENSOR_MAP;
 }
 
+// dW [E, N, K] (fp32 or bf16) as a 3-D store map: box {128 bytes of K, 128 rows, 1 expert}.
+int encode_dw(CUtensorMap *map, void *ptr, int E, int N, int K, bool f32) {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return MOE_ERR_DEVICE;
+    fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  const int esz = f32 ? 4 : 2;
+  cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)N, (cuuint64_t)E};
+  cuuint64_t strides[2] = {(cuuint64_t)K * esz, (cuuint64_t)N * K * esz};
+  cuuint32_t box[3] = {(cuuint32_t)(128 / esz), (cuuint32_t)BM, 1u};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                        ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_TENSOR_MAP;
+}
+
 template <int MODE>
 cudaError_t launch_mode(const BwdPlan &p, const Launch &l) {
   BwdArgs a;
   a.map_a = p.map_a;
   a.map_b = p.map_b;
+  a.map_o = p.map_o;
   a.group_end = p.group_end;
   a.out = p.out;
   a.status = p.status;
@@ -461,6 +526,7 @@ int bwd_prepare(BwdPlan &p, bool wgrad, bool out_f32, const uint16_t *G, const u
   if (wgrad) {
     rc = encode(&p.map_a, G, sum_m, N, 64);            // G^T: boxes of 64 dW rows x 64 group rows
     if (rc == MOE_OK) rc = encode(&p.map_b, B, sum_m, K, 64);  // X
+    if (rc == MOE_OK) rc = encode_dw(&p.map_o, out, E, N, K, out_f32);
   } else {
     rc = encode(&p.map_a, G, sum_m, N, BM);             // G rows, K-major
     if (rc == MOE_OK) rc = encode(&p.map_b, B, (long)E * N, K, 64);  // W in place

@@ -107,7 +107,7 @@ cudaError_t launch_pair_gemm(const GemmPlan &p, const Launch &l);
 // wgrad dW[g] = G^T . X over each group's rows, one-CTA tcgen05 kernels with
 // MN-major operands.
 struct BwdPlan {
-  CUtensorMap map_a, map_b;
+  CUtensorMap map_a, map_b, map_o;
   const int32_t *group_end = nullptr;
   void *out = nullptr;
   int32_t *status = nullptr;
@@ -121,6 +121,23 @@ struct BwdPlan {
 int bwd_prepare(BwdPlan &p, bool wgrad, bool out_f32, const uint16_t *G, const uint16_t *B,
                 const int32_t *offs, long sum_m, int E, int N, int K, void *out, int32_t *status);
 cudaError_t launch_bwd(const BwdPlan &p, const Launch &l);
+
+// BGMV LoRA-MoE shrink + expand (bgmv.cu) ----------------------------------------
+constexpr int kBgmvMaxSlices = 8;
+struct BgmvPlan {
+  const uint16_t *x = nullptr;
+  const uint16_t *a[kBgmvMaxSlices] = {}, *b[kBgmvMaxSlices] = {};
+  int f[kBgmvMaxSlices] = {}, off[kBgmvMaxSlices] = {};
+  const int32_t *tok = nullptr, *eid = nullptr, *lora = nullptr;
+  const float *w = nullptr;
+  uint16_t *shrink = nullptr;
+  float *y = nullptr;
+  int32_t *ws = nullptr;      // general pair order: route index (bgmv_workspace_bytes)
+  int32_t *status = nullptr;
+  int T = 0, H = 0, R = 0, S = 0, L = 0, E = 0, P = 0, k = 0, ld_y = 0;
+};
+size_t bgmv_workspace_bytes(int T, int contiguous_k);
+cudaError_t launch_bgmv(const BgmvPlan &p, const Launch &l);
 
 // S7: swap-AB weight-streaming GEMMs for few tokens per expert (decode.cu) ----
 struct SwapPlan {

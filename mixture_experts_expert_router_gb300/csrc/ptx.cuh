@@ -352,6 +352,13 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t sr
                "r"(x), "r"(y), "r"(src)
                : "memory");
 }
+// The same for a 3-D tensor map (the box is clipped at every dimension's end).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t src, int32_t x, int32_t y, int32_t z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z), "r"(src)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until at most N of this thread's bulk groups still read shared memory.
 template <int N>
