@@ -15,6 +15,9 @@ Distributions (one independent stream per tensor, derived from ``seed``):
   grouped GEMM sizes: Dirichlet(alpha * 1_E) proportions of sum_m, floored,
            the remainder handed to the largest fractional parts.
   grouped GEMM upstream gradient G ~ N(0, 1)  bf16 [sum_m, N] (backward).
+  FP8 per-tensor family: W1q, W2q E4M3 codes of N(0, 1) draws (torch's
+           float8_e4m3fn cast), per-expert scales s1 = u / sqrt(H), s2 = u / sqrt(I)
+           with u ~ U(0.5, 1.5), static activation scales a1 = 4/448, a2 = 2/448.
   BGMV LoRA-MoE: x ~ N(0,1) [T, H]; per slice A ~ N(0, 1/H) [L, E, R, H] and
            B ~ N(0, 1/R) [L, E, F, R]; each token a uniform LoRA index and a
            uniform k-subset of the experts, weights a flat Dirichlet draw; pairs
@@ -215,6 +218,39 @@ def make_bgmv(*, T: int, H: int, R: int, E: int, num_loras: int, top_k: int, fea
                         eid=torch.from_numpy(np.ascontiguousarray(eid)).to(device),
                         lora=torch.from_numpy(lora).to(device),
                         w=torch.from_numpy(np.ascontiguousarray(w)).to(device), contiguous=contiguous)
+
+
+@dataclass
+class Fp8Weights:
+    """E4M3 expert banks (uint8 codes) with their scales."""
+    w1q: torch.Tensor   # [L, 2I, H] uint8 codes, rows [up | gate]
+    w2q: torch.Tensor   # [L, H, I] uint8 codes
+    s1: torch.Tensor    # [L] fp32
+    s2: torch.Tensor    # [L] fp32
+    a1: float           # x scale
+    a2: float           # h scale (requantisation)
+
+
+def _e4m3_codes(shape, seed: int, stream: int, device="cpu") -> torch.Tensor:
+    dev = torch.device(device)
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed * 1_000_003 + stream)
+    out = torch.empty(shape, dtype=torch.uint8, device=dev)
+    flat = out.view(-1)
+    slab = 1 << 28
+    for s in range(0, flat.numel(), slab):
+        n = min(slab, flat.numel() - s)
+        flat[s:s + n].copy_(torch.randn(n, generator=g, device=dev).to(torch.float8_e4m3fn).view(torch.uint8))
+    return out
+
+
+def make_fp8_weights(L: int, H: int, I: int, *, seed: int = 0, device="cpu") -> Fp8Weights:
+    r = _rng(seed, 31)
+    s1 = (r.uniform(0.5, 1.5, size=L) / np.sqrt(H)).astype(np.float32)
+    s2 = (r.uniform(0.5, 1.5, size=L) / np.sqrt(I)).astype(np.float32)
+    return Fp8Weights(w1q=_e4m3_codes((L, 2 * I, H), seed, 32, device), w2q=_e4m3_codes((L, H, I), seed, 33, device),
+                      s1=torch.from_numpy(s1).to(device), s2=torch.from_numpy(s2).to(device),
+                      a1=4.0 / 448.0, a2=2.0 / 448.0)
 
 
 def bf16_bits(t: torch.Tensor) -> np.ndarray:

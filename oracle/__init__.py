@@ -76,6 +76,19 @@ def _declare(lib):
     lib.oracle_grouped_gemm_wgrad_rows.restype = None
     lib.oracle_bgmv.argtypes = [P, i, i, P, P, i, P, i, i, i, P, P, P, P, i, P, P, i, i]
     lib.oracle_bgmv.restype = i
+    f = ctypes.c_float
+    lib.oracle_float_to_e4m3.argtypes = [f]
+    lib.oracle_float_to_e4m3.restype = ctypes.c_uint8
+    lib.oracle_e4m3_to_float.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_to_float.restype = f
+    lib.oracle_quantize_e4m3.argtypes = [P, ctypes.c_long, f, P]
+    lib.oracle_quantize_e4m3.restype = None
+    lib.oracle_moe_tokens_fp8.argtypes = [P, P, P, P, P, P, P, f, f, i, i, i, i, i, i, i, P, i, P, P, P, i, P]
+    lib.oracle_moe_tokens_fp8.restype = i
+    lib.oracle_fc1_fp8_rows.argtypes = [P, P, P, f, f, P, i, i, i, P, i, P, i, P]
+    lib.oracle_fc1_fp8_rows.restype = None
+    lib.oracle_fc2_fp8_rows.argtypes = [P, P, P, f, P, i, i, i, P, i, P, i]
+    lib.oracle_fc2_fp8_rows.restype = None
     lib.oracle_float_to_bf16.argtypes = [ctypes.c_float]
     lib.oracle_float_to_bf16.restype = ctypes.c_uint16
     lib.oracle_bf16_to_float.argtypes = [ctypes.c_uint16]
@@ -283,6 +296,80 @@ def bgmv(x, lora_a, lora_b, tok, eid, lora, w, nthreads=0, lib=None):
                          S, ctypes.cast(f_arr, ctypes.c_void_p), L, E, R, _p(tok), _p(eid), _p(lora), _p(w), P,
                          _p(shrink), _p(y), sum(F), nthreads)
     return shrink, y, st
+
+
+def e4m3_encode(v: float, lib=None) -> int:
+    return int((lib or load()).oracle_float_to_e4m3(float(v)))
+
+
+def e4m3_decode(code: int, lib=None) -> float:
+    return float((lib or load()).oracle_e4m3_to_float(int(code)))
+
+
+def quantize_e4m3(x_bits, a1, lib=None):
+    """E4M3 codes of x / a1 (x as bf16 bits), any shape."""
+    lib = lib or load()
+    x = _c(x_bits, np.uint16)
+    out = np.empty(x.shape, np.uint8)
+    lib.oracle_quantize_e4m3(_p(x), x.size, float(a1), _p(out))
+    return out
+
+
+def moe_tokens_fp8(x, ids, w, w1q, w2q, s1, s2, a1, a2, num_experts, tokens=None, local_offset=0,
+                   num_local=None, want_intermediates=False, nthreads=0, lib=None, clamp_limit=None):
+    """The layer with E4M3 weights (codes w1q [L,2I,H], w2q [L,H,I], per-expert
+    scales s1, s2 [L]) and per-tensor activation scales a1 (x) and a2 (h).
+    Returns out [n_tok, H] u16 (and hq [n_tok*k, I] u8, y [n_tok*k, H] f32), status."""
+    lib = lib or load()
+    x = _c(x, np.uint16)
+    ids = _c(ids, np.int32)
+    w = _c(w, np.float32)
+    w1q = _c(w1q, np.uint8)
+    w2q = _c(w2q, np.uint8)
+    T, H = x.shape
+    k = ids.shape[1]
+    L = w1q.shape[0] if num_local is None else num_local
+    I = w1q.shape[1] // 2
+    assert w1q.shape == (L, 2 * I, H) and w2q.shape == (L, H, I)
+    s1, s2 = _c(s1, np.float32), _c(s2, np.float32)
+    tokens = np.arange(T, dtype=np.int32) if tokens is None else _c(tokens, np.int32)
+    n = tokens.shape[0]
+    out = np.empty((n, H), np.uint16)
+    hq = y = None
+    if want_intermediates:
+        hq = np.zeros((n * k, I), np.uint8)
+        y = np.zeros((n * k, H), np.float32)
+    clamp = None if clamp_limit is None else _c(clamp_limit, np.float32)
+    st = lib.oracle_moe_tokens_fp8(_p(x), _p(ids), _p(w), _p(w1q), _p(w2q), _p(s1), _p(s2), float(a1), float(a2),
+                                   T, H, I, num_experts, k, local_offset, L, _p(tokens), n, _p(out), _p(hq), _p(y),
+                                   nthreads, _p(clamp))
+    if want_intermediates:
+        return out, hq, y, st
+    return out, st
+
+
+def fc1_fp8_rows(xq, w1q, s1, a1, a2, group_end, rows, nthreads=0, lib=None, clamp_limit=None):
+    lib = lib or load()
+    xq, w1q = _c(xq, np.uint8), _c(w1q, np.uint8)
+    ge, rows, s1 = _c(group_end, np.int32), _c(rows, np.int32), _c(s1, np.float32)
+    L, twoI, H = w1q.shape
+    I = twoI // 2
+    out = np.empty((rows.shape[0], I), np.uint8)
+    clamp = None if clamp_limit is None else _c(clamp_limit, np.float32)
+    lib.oracle_fc1_fp8_rows(_p(xq), _p(w1q), _p(s1), float(a1), float(a2), _p(ge), L, H, I, _p(rows), rows.shape[0],
+                            _p(out), nthreads, _p(clamp))
+    return out
+
+
+def fc2_fp8_rows(hq, w2q, s2, a2, group_end, rows, nthreads=0, lib=None):
+    lib = lib or load()
+    hq, w2q = _c(hq, np.uint8), _c(w2q, np.uint8)
+    ge, rows, s2 = _c(group_end, np.int32), _c(rows, np.int32), _c(s2, np.float32)
+    L, H, I = w2q.shape
+    out = np.empty((rows.shape[0], H), np.float32)
+    lib.oracle_fc2_fp8_rows(_p(hq), _p(w2q), _p(s2), float(a2), _p(ge), L, H, I, _p(rows), rows.shape[0], _p(out),
+                            nthreads)
+    return out
 
 
 def bf16_to_f32(a: np.ndarray) -> np.ndarray:

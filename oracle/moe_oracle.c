@@ -28,6 +28,7 @@
  *   [P5] "flashinfer.fused_moe.prepare_bgmv_moe": BGMV LoRA shrink + expand
  *        over routed (token, expert) pairs, one owner per output that
  *        accumulates routes in fixed input order, FP32 output accumulator.
+ *   [P1] same page, opening paragraph: the fp8 (per-tensor) weight family.
  *   [P3] "Cake ragged BF16 grouped GEMM (experimental)", operation table:
  *        Y[offs[e-1]:offs[e]] = X[offs[e-1]:offs[e]] . W[e]^T, offs holding
  *        cumulative group end offsets, groups may be empty; dgrad
@@ -90,6 +91,44 @@ static uint16_t float_to_bf16(float f) {
         hi += 1u;
     return (uint16_t)hi;
 }
+
+/* ---- FP8 E4M3 (the OCP 8-bit format "E4M3FN") ---------------------------
+ * Bits s eeee mmm, exponent bias 7.  e = 0: subnormal, (m / 8) * 2^-6;
+ * otherwise (1 + m / 8) * 2^(e - 7).  The largest finite magnitude is
+ * 1.75 * 2^8 = 448 (code 0x7E); 0x7F and 0xFF are NaN; there is no infinity. */
+static float e4m3_to_float(uint8_t b) {
+    int e = (b >> 3) & 15, m = b & 7;
+    float v = e == 0 ? ldexpf((float)m, -9) : ldexpf((float)(8 + m), e - 10);
+    return (b & 0x80) ? -v : v;
+}
+
+/* fp32 -> E4M3, round to nearest, ties to even code, magnitudes above 448
+ * saturating to 448 (finite inputs).  Subnormal range: q = round(|f| * 2^9)
+ * is the code itself (q = 8 is the smallest normal, code 0x08); normal range:
+ * |f| = mant * 2^e with mant in [1, 2), q = round(mant * 8) in [8, 16]. */
+static uint8_t float_to_e4m3(float f) {
+    uint8_t s = signbit(f) ? 0x80 : 0x00;
+    float a = fabsf(f);
+    if (a >= 448.0f) return (uint8_t)(s | 0x7E);
+    if (a < ldexpf(1.0f, -6)) {
+        float q = nearbyintf(ldexpf(a, 9)); /* default rounding: nearest, ties even */
+        return (uint8_t)(s | (uint8_t)q);
+    }
+    int k;
+    float fr = frexpf(a, &k);       /* a = fr * 2^k, fr in [0.5, 1) */
+    int e = k - 1;                  /* a = mant * 2^e, mant in [1, 2) */
+    float q = nearbyintf(ldexpf(fr, 4)); /* mant * 8 = fr * 16 */
+    if (q == 16.0f) {
+        q = 8.0f;
+        e += 1;
+    }
+    int code = ((e + 7) << 3) | ((int)q - 8);
+    if (code > 0x7E) code = 0x7E;
+    return (uint8_t)(s | (uint8_t)code);
+}
+
+uint8_t oracle_float_to_e4m3(float f) { return float_to_e4m3(f); }
+float oracle_e4m3_to_float(uint8_t b) { return e4m3_to_float(b); }
 
 uint16_t oracle_float_to_bf16(float f) { return float_to_bf16(f); }
 float oracle_bf16_to_float(uint16_t b) { return bf16_to_float(b); }
@@ -221,6 +260,20 @@ static void expert_ffn_row(const uint16_t *x_row, const uint16_t *w1e,
     }
 }
 
+/* ---- the combine of one token  [P4 Parameters, use_fused_finalize=False] --
+ * out[c] = bf16( sum over the local slots j, ascending, of w[j] * y[j][c] ),
+ * fp32 with one final rounding. */
+static void combine_row(const float *w, const float *y, const char *local, int k, int H,
+                        uint16_t *out) {
+    for (int c = 0; c < H; ++c) {
+        float acc = 0.0f;
+        for (int j = 0; j < k; ++j)
+            if (local[j])
+                acc = acc + w[j] * y[(size_t)j * H + c];
+        out[c] = float_to_bf16(acc);
+    }
+}
+
 /* ---- whole layer for a list of tokens  [P4 formula, EP rule, combine] -----
  *
  * x [T, H] bf16; ids, w [T, k]; w1 [L, 2I, H]; w2 [L, H, I] (local experts,
@@ -261,13 +314,7 @@ int oracle_moe_tokens(const uint16_t *x, const int32_t *ids, const float *w,
                 memcpy(y_out + ((size_t)i * k + j) * H, y + (size_t)j * H,
                        sizeof(float) * H);
         }
-        for (int c = 0; c < H; ++c) {
-            float acc = 0.0f;
-            for (int j = 0; j < k; ++j)
-                if (local[j])
-                    acc = acc + w[(size_t)t * k + j] * y[(size_t)j * H + c];
-            out[(size_t)i * H + c] = float_to_bf16(acc);
-        }
+        combine_row(w + (size_t)t * k, y, local, k, H, out + (size_t)i * H);
         free(local);
         free(y);
         free(h);
@@ -527,6 +574,139 @@ int oracle_bgmv(const uint16_t *x, int T, int H, const uint16_t *const *lora_a,
     free(cnt);
     free(ok);
     return status;
+}
+
+/* ---- FP8 per-tensor weight family  [P1 "flashinfer.experimental.
+ * cake_stepfun_moe", opening paragraph: the fp8 (per-tensor) weight family]
+ *
+ * Reading: W1q [L, 2I, H] and W2q [L, H, I] hold E4M3 codes with one fp32
+ * scale per local expert and weight tensor (s1[e], s2[e]); the activations
+ * entering each GEMM are quantised to E4M3 with one static fp32 scale per
+ * tensor (a1 for x, a2 for h, the requantisation between FC1 and FC2):
+ *   xq = e4m3(x / a1)
+ *   u, g = (sum_c xq * W1q) * (a1 * s1[e])        fp32, sequential in c
+ *   hq = e4m3(swiglu_step(g, u, limit) / a2)      (no bf16 rounding of h)
+ *   y  = (sum_n hq * W2q) * (a2 * s2[e])          fp32, sequential in n
+ *   out = bf16(sum_j w_j * y_j)                    as in the bf16 family
+ * Products of two E4M3 values are exact in fp32. */
+static void expert_ffn_row_fp8(const uint8_t *xq, const uint8_t *w1e, const uint8_t *w2e,
+                               int H, int I, float scale1, float a2, float scale2,
+                               float limit, uint8_t *hq, float *y) {
+    for (int n = 0; n < I; ++n) {
+        const uint8_t *up_row = w1e + (size_t)n * H;
+        const uint8_t *gate_row = w1e + (size_t)(I + n) * H;
+        float u = 0.0f, g = 0.0f;
+        for (int c = 0; c < H; ++c) {
+            float xv = e4m3_to_float(xq[c]);
+            u = u + xv * e4m3_to_float(up_row[c]);
+            g = g + xv * e4m3_to_float(gate_row[c]);
+        }
+        u = u * scale1;
+        g = g * scale1;
+        hq[n] = float_to_e4m3(swiglu_step(g, u, limit) / a2);
+    }
+    for (int c = 0; c < H; ++c) {
+        const uint8_t *w2_row = w2e + (size_t)c * I;
+        float acc = 0.0f;
+        for (int n = 0; n < I; ++n)
+            acc = acc + e4m3_to_float(hq[n]) * e4m3_to_float(w2_row[n]);
+        y[c] = acc * scale2;
+    }
+}
+
+/* x bf16 [n, H] -> xq E4M3 codes [n, H] with scale a1. */
+void oracle_quantize_e4m3(const uint16_t *x, long n, float a1, uint8_t *xq) {
+    for (long i = 0; i < n; ++i) xq[i] = float_to_e4m3(bf16_to_float(x[i]) / a1);
+}
+
+/* The layer with FP8 weights for the listed tokens (arguments as
+ * oracle_moe_tokens; w1q, w2q E4M3 codes; s1, s2 [L]; a1, a2 scalars).
+ * hq_out [n_tok*k, I] E4M3 codes and y_out [n_tok*k, H] fp32 optional. */
+int oracle_moe_tokens_fp8(const uint16_t *x, const int32_t *ids, const float *w,
+                          const uint8_t *w1q, const uint8_t *w2q, const float *s1,
+                          const float *s2, float a1, float a2, int T, int H, int I,
+                          int E, int k, int off, int L, const int32_t *tokens,
+                          int n_tok, uint16_t *out, uint8_t *hq_out, float *y_out,
+                          int nthreads, const float *clamp) {
+    (void)T;
+    int status = 0;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : status)
+    for (int i = 0; i < n_tok; ++i) {
+        int t = tokens[i];
+        uint8_t *xq = (uint8_t *)malloc((size_t)H);
+        uint8_t *hq = (uint8_t *)malloc((size_t)I);
+        float *y = (float *)malloc(sizeof(float) * (size_t)H * (size_t)k);
+        char *local = (char *)calloc((size_t)k, 1);
+        for (int c = 0; c < H; ++c) xq[c] = float_to_e4m3(bf16_to_float(x[(size_t)t * H + c]) / a1);
+        for (int j = 0; j < k; ++j) {
+            int e = ids[(size_t)t * k + j];
+            if (e < 0 || e >= E) { status |= ORACLE_BAD_EXPERT; continue; }
+            if (e < off || e >= off + L) continue;
+            local[j] = 1;
+            int le = e - off;
+            const uint8_t *w1e = w1q + (size_t)le * 2 * I * H;
+            const uint8_t *w2e = w2q + (size_t)le * H * I;
+            expert_ffn_row_fp8(xq, w1e, w2e, H, I, a1 * s1[le], a2, a2 * s2[le],
+                               limit_of(clamp, le), hq, y + (size_t)j * H);
+            if (hq_out) memcpy(hq_out + ((size_t)i * k + j) * I, hq, (size_t)I);
+            if (y_out)
+                memcpy(y_out + ((size_t)i * k + j) * H, y + (size_t)j * H, sizeof(float) * H);
+        }
+        combine_row(w + (size_t)t * k, y, local, k, H, out + (size_t)i * H);
+        free(local);
+        free(y);
+        free(hq);
+        free(xq);
+    }
+    return status;
+}
+
+/* FC1 + SwiGLU + requantisation on selected permuted rows of xq (E4M3). */
+void oracle_fc1_fp8_rows(const uint8_t *xq, const uint8_t *w1q, const float *s1, float a1,
+                         float a2, const int32_t *group_end, int L, int H, int I,
+                         const int32_t *rows, int n_rows, uint8_t *hq_rows, int nthreads,
+                         const float *clamp) {
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int q = 0; q < n_rows; ++q) {
+        int p = rows[q];
+        int g = group_of_row(group_end, L, p);
+        const uint8_t *xr = xq + (size_t)p * H;
+        const uint8_t *w1e = w1q + (size_t)g * 2 * I * H;
+        for (int n = 0; n < I; ++n) {
+            float u = 0.0f, gt = 0.0f;
+            for (int c = 0; c < H; ++c) {
+                float xv = e4m3_to_float(xr[c]);
+                u = u + xv * e4m3_to_float(w1e[(size_t)n * H + c]);
+                gt = gt + xv * e4m3_to_float(w1e[(size_t)(I + n) * H + c]);
+            }
+            float sc = a1 * s1[g];
+            hq_rows[(size_t)q * I + n] =
+                float_to_e4m3(swiglu_step(gt * sc, u * sc, limit_of(clamp, g)) / a2);
+        }
+    }
+}
+
+/* FC2 with the dequantisation on selected permuted rows of hq (E4M3) ->
+ * y_rows [n_rows, H] fp32. */
+void oracle_fc2_fp8_rows(const uint8_t *hq, const uint8_t *w2q, const float *s2, float a2,
+                         const int32_t *group_end, int L, int H, int I, const int32_t *rows,
+                         int n_rows, float *y_rows, int nthreads) {
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int q = 0; q < n_rows; ++q) {
+        int p = rows[q];
+        int g = group_of_row(group_end, L, p);
+        const uint8_t *hr = hq + (size_t)p * I;
+        const uint8_t *w2e = w2q + (size_t)g * H * I;
+        for (int c = 0; c < H; ++c) {
+            float acc = 0.0f;
+            for (int n = 0; n < I; ++n)
+                acc = acc + e4m3_to_float(hr[n]) * e4m3_to_float(w2e[(size_t)c * I + n]);
+            y_rows[(size_t)q * H + c] = acc * (a2 * s2[g]);
+        }
+    }
 }
 
 int oracle_max_threads(void) {

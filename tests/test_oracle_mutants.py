@@ -28,7 +28,7 @@ MUTANTS = {
     "round_half_up": [("if (lo > 0x8000u || (lo == 0x8000u && (hi & 1u)))", "if (lo >= 0x8000u)")],
     "w2_transposed": [("acc = acc + bf16_to_float(h[n]) * bf16_to_float(w2_row[n]);",
                        "acc = acc + bf16_to_float(h[n]) * bf16_to_float(w2e[(size_t)n * H + c]);")],
-    "combine_drops_weight": [("acc = acc + w[(size_t)t * k + j] * y[(size_t)j * H + c];",
+    "combine_drops_weight": [("acc = acc + w[j] * y[(size_t)j * H + c];",
                               "acc = acc + y[(size_t)j * H + c];")],
     "fc1_drops_last_term": [("        for (int c = 0; c < H; ++c) {\n            float xv = bf16_to_float(x_row[c]);",
                              "        for (int c = 0; c < H - 1; ++c) {\n            float xv = bf16_to_float(x_row[c]);")],
@@ -50,6 +50,11 @@ MUTANTS = {
     "bgmv_wrong_lora": [("(((size_t)lora[t] * E + eid[p]) * R) * (size_t)H;",
                          "(((size_t)(num_loras - 1 - lora[t]) * E + eid[p]) * R) * (size_t)H;")],
     "bgmv_drops_weight": [("acc = acc + w[p] * v;", "acc = acc + v;")],
+    "e4m3_no_saturation": [("    if (a >= 448.0f) return (uint8_t)(s | 0x7E);\n", "    if (a >= 480.0f) return (uint8_t)(s | 0x7F);\n")],
+    "e4m3_truncates": [("    float q = nearbyintf(ldexpf(fr, 4)); /* mant * 8 = fr * 16 */",
+                        "    float q = floorf(ldexpf(fr, 4));")],
+    "fp8_h_not_requantised_by_a2": [("        hq[n] = float_to_e4m3(swiglu_step(g, u, limit) / a2);",
+                                     "        hq[n] = float_to_e4m3(swiglu_step(g, u, limit));")],
     "finalize_skips_slot0": [("            for (int j = 0; j < k; ++j) {\n                int p = exp_to_perm[(size_t)t * k + j];",
                               "            for (int j = 1; j < k; ++j) {\n                int p = exp_to_perm[(size_t)t * k + j];")],
 }
@@ -72,6 +77,9 @@ PIN_CALLS = [
     ("gg_adjoint", lambda: pins.test_grouped_gemm_adjoint_identity()),
     ("bgmv_torch", lambda: pins.test_bgmv_vs_torch_per_pair(False)),
     ("bgmv_invariants", lambda: pins.test_bgmv_rank_padding_linearity_and_zero_b()),
+    ("e4m3_torch", lambda: pins.test_e4m3_codes_exhaustive_against_torch()),
+    ("e4m3_round", lambda: pins.test_e4m3_rounding_ties_and_saturation()),
+    ("fp8_fp64", lambda: pins.test_fp8_layer_fp64_tiny()),
     ("step_per_expert", lambda: pins.test_swiglu_step_infinite_limit_is_plain_swiglu_and_limits_are_per_local_expert()),
 ]
 

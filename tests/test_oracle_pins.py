@@ -591,6 +591,107 @@ def test_bgmv_out_of_range_pairs_are_dropped_and_flagged():
     assert np.array_equal(y_bad, y_ref)
 
 
+# ------------------------------------------------- FP8 per-tensor family --
+# flashinfer.experimental.cake_stepfun_moe, opening paragraph ("fp8
+# (per-tensor)").  E4M3 as the OCP 8-bit format defines it; reading of the
+# family: xq = e4m3(x / a1), u, g dequantised by a1 * s1[e], hq = e4m3(h / a2),
+# y dequantised by a2 * s2[e].
+
+def _torch_e4m3_decode(codes):
+    return torch.from_numpy(np.ascontiguousarray(codes, np.uint8)).view(torch.float8_e4m3fn).float().numpy()
+
+
+def _torch_e4m3_encode(vals):
+    return torch.from_numpy(np.ascontiguousarray(vals, np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def test_e4m3_codes_exhaustive_against_torch():
+    for c in range(256):
+        if c & 0x7F == 0x7F:
+            continue  # NaN codes
+        v = oracle.e4m3_decode(c)
+        assert v == float(_torch_e4m3_decode(np.array([c]))[0]), c
+        assert oracle.e4m3_encode(v) == c, c
+    assert oracle.e4m3_decode(0x7E) == 448.0 and oracle.e4m3_decode(0x01) == 2.0 ** -9
+
+
+def test_e4m3_rounding_ties_and_saturation():
+    rng = np.random.default_rng(3)
+    vals = np.concatenate([rng.standard_normal(20000) * s for s in (1e-3, 0.05, 1.0, 30.0)]).astype(np.float32)
+    vals = vals[np.abs(vals) < 440]
+    got = np.array([oracle.e4m3_encode(v) for v in vals], np.uint8)
+    assert np.array_equal(got, _torch_e4m3_encode(vals))  # a library rounding, nearest even
+    # exact midpoints between neighbouring codes go to the even code
+    for c in range(0, 0x7D):
+        lo, hi = oracle.e4m3_decode(c), oracle.e4m3_decode(c + 1)
+        mid = np.float32((lo + hi) / 2)
+        assert oracle.e4m3_encode(mid) == (c if c % 2 == 0 else c + 1), c
+        assert oracle.e4m3_encode(-mid) == 0x80 | (c if c % 2 == 0 else c + 1), c
+    # above the largest finite magnitude: saturate
+    for v in (448.0, 449.0, 470.0, 1e6):
+        assert oracle.e4m3_encode(v) == 0x7E and oracle.e4m3_encode(-v) == 0xFE
+
+
+def _fp8_case(seed=11, T=20, H=64, I=64, E=5, k=2):
+    wl = W.make_moe(T=T, H=H, I=I, E=E, top_k=k, mode="logits", seed=seed)
+    fw = W.make_fp8_weights(E, H, I, seed=seed)
+    x = W.bf16_bits(wl.x)
+    ids, w = oracle.route(wl.logits.numpy(), k)
+    return wl, fw, x, ids, w
+
+
+def test_fp8_layer_fp64_tiny():
+    """Dense fp64 evaluation from torch's E4M3 decoding of the same codes:
+    xq exact, hq within one code (fp32 sums may straddle a rounding boundary),
+    out within one bf16 ulp of the fp64 combine of the oracle's own y."""
+    wl, fw, x, ids, w = _fp8_case()
+    w1q, w2q, s1, s2 = fw.w1q.numpy(), fw.w2q.numpy(), fw.s1.numpy(), fw.s2.numpy()
+    out, hq, y, st = oracle.moe_tokens_fp8(x, ids, w, w1q, w2q, s1, s2, fw.a1, fw.a2, wl.E, want_intermediates=True)
+    assert st == 0
+    xq = oracle.quantize_e4m3(x, fw.a1)
+    v = bf16_to_f64(x).astype(np.float32) / np.float32(fw.a1)
+    inr = np.abs(v) < 448  # torch's cast gives NaN above 448 where this family saturates
+    assert np.array_equal(xq[inr], _torch_e4m3_encode(v[inr]))
+    assert np.all(xq[~inr] & 0x7F == 0x7E)
+    xq64 = _torch_e4m3_decode(xq).astype(np.float64)
+    I = wl.I
+    near = 0
+    for t in range(wl.T):
+        for j in range(wl.top_k):
+            e = ids[t, j]
+            w1 = _torch_e4m3_decode(w1q[e]).astype(np.float64)
+            sc = float(np.float32(fw.a1) * np.float32(s1[e]))
+            u, g = (w1[:I] @ xq64[t]) * sc, (w1[I:] @ xq64[t]) * sc
+            h64 = g / (1 + np.exp(-g)) * u / fw.a2
+            want = _torch_e4m3_encode(np.clip(h64, -448, 448))
+            d = np.abs(_torch_e4m3_decode(hq[t * wl.top_k + j]).astype(np.float64) - _torch_e4m3_decode(want))
+            step = np.maximum(np.abs(_torch_e4m3_decode(want)) * 2.0 ** -3, 2.0 ** -9)
+            assert np.all(d <= step + 1e-12)
+            near += int(np.sum(d == 0))
+            w2 = _torch_e4m3_decode(w2q[e]).astype(np.float64)
+            y64 = (w2 @ _torch_e4m3_decode(hq[t * wl.top_k + j]).astype(np.float64)) * float(np.float32(fw.a2) * np.float32(s2[e]))
+            assert np.all(np.abs(y[t * wl.top_k + j] - y64) <= 1e-5 * (np.abs(y64).max() + 1e-6))
+    assert near >= 0.99 * wl.T * wl.top_k * I
+    comb = np.zeros((wl.T, wl.H))
+    for t in range(wl.T):
+        for j in range(wl.top_k):
+            comb[t] += w[t, j] * y[t * wl.top_k + j]
+    assert np.all(ulp_distance(out, torch_bf16_bits(comb)) <= 1)
+
+
+def test_fp8_stages_compose_to_layer():
+    wl, fw, x, ids, w = _fp8_case(seed=12, T=30, H=128, I=64, E=6, k=2)
+    w1q, w2q, s1, s2 = fw.w1q.numpy(), fw.w2q.numpy(), fw.s1.numpy(), fw.s2.numpy()
+    m, p2e, e2p, _ = oracle.sort(ids, wl.E)
+    xq = oracle.quantize_e4m3(x, fw.a1)[p2e // 2]
+    rows = np.arange(len(p2e), dtype=np.int32)
+    hq = oracle.fc1_fp8_rows(xq, w1q, s1, fw.a1, fw.a2, m[1:], rows)
+    y = oracle.fc2_fp8_rows(hq, w2q, s2, fw.a2, m[1:], rows)
+    out = oracle.finalize(y, e2p, w)
+    ref, _ = oracle.moe_tokens_fp8(x, ids, w, w1q, w2q, s1, s2, fw.a1, fw.a2, wl.E)
+    assert np.array_equal(out, ref)
+
+
 def test_workload_generator_is_seeded():
     a = W.make_moe("tiny", seed=0)
     b = W.make_moe("tiny", seed=0)
