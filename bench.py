@@ -149,13 +149,13 @@ def layer_flops(M: int, H: int, I: int) -> float:
     return 2.0 * M * (H * 2 * I + I * H)
 
 
-def layer_bytes(wl, ids: np.ndarray) -> float:
+def layer_bytes(wl, ids: np.ndarray, wbytes_per_elem: float = 2.0) -> float:
     """Algorithmic bytes: weights of non-empty local experts, x read, out
     written, routing inputs read."""
     L = wl.num_local
     local = ids[(ids >= wl.local_offset) & (ids < wl.local_offset + L)] - wl.local_offset
     active = len(np.unique(local))
-    wbytes = active * (2 * wl.I * wl.H + wl.H * wl.I) * 2.0
+    wbytes = active * (2 * wl.I * wl.H + wl.H * wl.I) * wbytes_per_elem
     route = wl.T * wl.E * 4.0 if wl.mode == "logits" else wl.T * wl.top_k * 8.0
     return wbytes + wl.T * wl.H * 2.0 * 2 + route, active
 
@@ -168,7 +168,7 @@ def oracle_sample_rate(wl, ids, w, n_tok: int, seed: int, threads: int, host_w=N
     rng = np.random.default_rng(seed)
     tokens = np.sort(rng.choice(wl.T, size=min(n_tok, wl.T), replace=False)).astype(np.int32)
     x = W.bf16_bits(wl.x)
-    w1, w2 = host_w
+    w1, w2 = host_w[:2]
     t0 = time.perf_counter()
     if wl.mode == "logits":
         lg = wl.logits.cpu().numpy()[tokens]
@@ -178,8 +178,12 @@ def oracle_sample_rate(wl, ids, w, n_tok: int, seed: int, threads: int, host_w=N
         ids_full[tokens], w_full[tokens] = ids_s, w_s
     else:
         ids_full, w_full = ids, w
-    oracle.moe_tokens(x, ids_full, w_full, w1, w2, wl.E, tokens=tokens, local_offset=wl.local_offset,
-                      num_local=wl.num_local, nthreads=threads)
+    if len(host_w) > 2:  # E4M3 family: (w1q, w2q, s1, s2, a1, a2)
+        oracle.moe_tokens_fp8(x, ids_full, w_full, *host_w, wl.E, tokens=tokens, local_offset=wl.local_offset,
+                              num_local=wl.num_local, nthreads=threads)
+    else:
+        oracle.moe_tokens(x, ids_full, w_full, w1, w2, wl.E, tokens=tokens, local_offset=wl.local_offset,
+                          num_local=wl.num_local, nthreads=threads)
     dt = time.perf_counter() - t0
     return len(tokens) / dt, dt, len(tokens)
 
@@ -361,8 +365,17 @@ def run_ours(args, world, rank, local):
                 decode_one_launch=args.decode_one_launch)
     # one plan per copy of the expert banks; the steps rotate over them
     banks = weight_banks(wl)
-    w1s = [wl.w1] + [wl.w1.clone() for _ in range(banks - 1)]
-    w2s = [wl.w2] + [wl.w2.clone() for _ in range(banks - 1)]
+    fw = None
+    if args.e4m3:  # the fp8 per-tensor family: E4M3 codes with per-expert scales
+        fw = W.make_fp8_weights(wl.num_local, wl.H, wl.I, seed=args.seed + rank, device=dev)
+        opts["e4m3"] = dict(w1_scale=fw.s1, w2_scale=fw.s2, x_scale=fw.a1, h_scale=fw.a2)
+        base1, base2 = fw.w1q, fw.w2q
+        wl.w1, wl.w2 = None, None  # the bf16 banks are not used
+        torch.cuda.empty_cache()
+    else:
+        base1, base2 = wl.w1, wl.w2
+    w1s = [base1] + [base1.clone() for _ in range(banks - 1)]
+    w2s = [base2] + [base2.clone() for _ in range(banks - 1)]
     plans, plans_t = [], []
     for b in range(banks):
         p_b = moe.MoEPlan(x, w1s[b], w2s[b], wl.E, wl.top_k, logits=logits, topk_ids=tids, topk_w=tw,
@@ -390,7 +403,7 @@ def run_ours(args, world, rank, local):
     M = int(np.sum((ids_np >= wl.local_offset) & (ids_np < wl.local_offset + L)))
     F = layer_flops(M, wl.H, wl.I)
     F_fc1 = 2.0 * M * wl.H * 2 * wl.I
-    B, active = layer_bytes(wl, ids_np)
+    B, active = layer_bytes(wl, ids_np, 1.0 if fw is not None else 2.0)
 
     # one step = one replay of the prepared launch captured in a CUDA graph
     side = torch.cuda.Stream(dev)
@@ -499,9 +512,15 @@ def run_ours(args, world, rank, local):
     peaks, peak_src = load_peaks()
     fc1_s = stage_ms.get("fc1_swiglu", 0.0) / 1000.0 / max(1, n_timed)
     peak_b = float(peaks.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"]))
+    # E4M3 MMAs: the nominal fp8 / bf16 ratio (4.5 / 2.25 PFLOP/s) times the measured bf16 peaks
+    tmul = 2.0 if fw is not None else 1.0
+    if fw is not None:
+        peaks = dict(peaks, bf16_tflops=tmul * float(peaks["bf16_tflops"]),
+                     bf16_tflops_sustained=tmul * float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])))
     roofline_t = max(F / (float(peaks["bf16_tflops"]) * 1e12), B / (peak_b * 1e9))
     # FC1's algorithmic bytes: W1 of the active experts, its gathered input rows, h written
-    B_fc1 = active * 2.0 * wl.I * wl.H * 2 + M * wl.H * 2.0 + M * wl.I * 2.0
+    esz = 1.0 if fw is not None else 2.0
+    B_fc1 = active * 2.0 * wl.I * wl.H * esz + M * wl.H * esz + M * wl.I * esz
     decode_path = plan.buffers()["path"] == moe.PATH_DECODE
     traffic = None if decode_path else recorded_traffic(wl.name, "fc1_swiglu")
     # the decode chain in one launch: one kernel (plus the router with logits)
@@ -512,8 +531,10 @@ def run_ours(args, world, rank, local):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded)",
-        "config": config_dict(wl, world, banks),
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if fw is not None else "bf16",
+        "data": "synthetic (seeded)",
+        "config": dict(config_dict(wl, world, banks), **({"weights": "e4m3 per-tensor (fp8 family); tensor peak "
+                                                         "= 2 x the measured bf16 peak"} if fw is not None else {})),
         "tflops": F * world / step_s / 1e12,
         "hbm_gbs": B * world / step_s / 1e9,
         "roofline_step": {"time_ms": roofline_t * 1000.0, "frac": roofline_t / step_s,
@@ -533,7 +554,8 @@ def run_ours(args, world, rank, local):
     }
     if world == 1 and not args.no_cpu_baseline:
         threads = host_cores()
-        host_w = (W.bf16_bits(wl.w1), W.bf16_bits(wl.w2))
+        host_w = ((fw.w1q.cpu().numpy(), fw.w2q.cpu().numpy(), fw.s1.cpu().numpy(), fw.s2.cpu().numpy(), fw.a1, fw.a2)
+                  if fw is not None else (W.bf16_bits(wl.w1), W.bf16_bits(wl.w2)))
         ids2 = wl.topk_ids.numpy() if wl.topk_ids is not None else None
         w2 = wl.topk_w.numpy() if wl.topk_w is not None else None
         n_tok = calibrated_tokens(wl, ids2, w2, threads, host_w, args.cpu_budget)
@@ -837,6 +859,7 @@ def main():
     ap.add_argument("--zipf", type=float, default=None,
                     help="with --shape: per-expert logit bias ln p_e, p_e ~ rank^-s (imbalanced groups)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e4m3", action="store_true", help="the fp8 per-tensor weight family (E4M3 weights)")
     ap.add_argument("--no-graph", action="store_true", help="launch the plan directly instead of a CUDA graph")
     ap.add_argument("--decode-chain", action="store_true", help="decode path: always the two-kernel chain")
     ap.add_argument("--decode-one-launch", action="store_true",

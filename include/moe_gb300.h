@@ -195,6 +195,22 @@ MOE_API int moe_fc1_swiglu_step(const moe_bf16 *xp, const moe_bf16 *w1, const fl
                                 const int32_t *m_indptr, int max_rows, int H, int I,
                                 int num_local, moe_bf16 *h, void *stream);
 
+/* ---- S4 / S5 with E4M3 operands (the fp8 per-tensor family, MOE_WEIGHTS_E4M3) --------
+ * moe_fc1_swiglu_e4m3: hq[p] = e4m3( swiglu_step(g * sc, u * sc, limit[i]) / h_scale )
+ *   with u, g = xq[p] . W1q[i, up / gate rows]^T (fp32) and sc = x_scale * w1_scale[i];
+ *   xq [max_rows, H], w1q [L, 2I, H], hq [max_rows, I] E4M3 codes (uint8);
+ *   clamp_limit [L] or NULL (plain SwiGLU).
+ * moe_fc2_e4m3: y[p] = (hq[p] . W2q[i]^T) * (h_scale * w2_scale[i]), fp32;
+ *   w2q [L, H, I] E4M3 codes, y [max_rows, H] fp32.
+ * H % 128 == 0, I % 128 == 0; m_indptr [L+1] on the device. */
+MOE_API int moe_fc1_swiglu_e4m3(const uint8_t *xq, const uint8_t *w1q, const float *w1_scale,
+                                float x_scale, float h_scale, const float *clamp_limit,
+                                const int32_t *m_indptr, int max_rows, int H, int I,
+                                int num_local, uint8_t *hq, void *stream);
+MOE_API int moe_fc2_e4m3(const uint8_t *hq, const uint8_t *w2q, const float *w2_scale,
+                         float h_scale, const int32_t *m_indptr, int max_rows, int H, int I,
+                         int num_local, float *y, void *stream);
+
 /* ---- S5 FC2 ------------------------------------------------------------------------
  * y[p] = h[p] . W2[i]^T, fp32, unscaled and unrounded (cute_dsl_fused_moe_bf16,
  * Parameters, use_fused_finalize=False).
@@ -384,7 +400,28 @@ typedef struct moe_forward_desc {
     int flags;               /* MOE_PLAN_* */
     const float *clamp_limit; /* [L] fp32 SwiGLUStep limits per local expert
                                  (moe_fc1_swiglu_step), or NULL for SwiGLU */
+    int weight_format;        /* MOE_WEIGHTS_BF16 or MOE_WEIGHTS_E4M3         */
+    const float *w1_scale;    /* E4M3: [L] fp32 scale of each expert's W1      */
+    const float *w2_scale;    /* E4M3: [L] fp32 scale of each expert's W2      */
+    float x_scale;            /* E4M3: per-tensor scale of x (FC1 input)       */
+    float h_scale;            /* E4M3: per-tensor scale of h (FC2 input)       */
 } moe_forward_desc;
+
+/* Weight families of the prepared launch (flashinfer.experimental.
+ * cake_stepfun_moe, opening paragraph: bf16 and fp8 (per-tensor) among the
+ * families served).  MOE_WEIGHTS_E4M3, the library's reading of the fp8
+ * per-tensor family: w1 / w2 hold E4M3 codes (uint8, the same [L, 2I, H] /
+ * [L, H, I] layouts) with one fp32 scale per expert and tensor (w1_scale,
+ * w2_scale); x enters FC1 as e4m3(x / x_scale) and h enters FC2 as
+ * e4m3(h / h_scale) (the requantisation between the GEMMs; h is not rounded
+ * to bf16), codes rounded to nearest even and saturated at 448; FC1's
+ * accumulator is dequantised by x_scale * w1_scale[e] before the SwiGLU(Step),
+ * FC2's by h_scale * w2_scale[e]; the combine and out are as in the bf16
+ * family.  E4M3 plans run the grouped path with one-CTA tcgen05 kernels
+ * (kind::f8f6f4) for any T; H % 128 == 0, I % 128 == 0; MOE_PATH_DECODE is
+ * refused (MOE_ERR_SHAPE). */
+#define MOE_WEIGHTS_BF16 0
+#define MOE_WEIGHTS_E4M3 1
 
 typedef struct moe_plan moe_plan;
 

@@ -40,6 +40,7 @@ PLAN_DECODE_SEPARATE = 8
 PLAN_FUSED_GATHER = 16
 PLAN_DECODE_ONE_LAUNCH = 32
 PLAN_TEST_UNREACHABLE_WAIT = 64
+WEIGHTS_BF16, WEIGHTS_E4M3 = 0, 1
 WAIT_LIMIT_MIN_NS, WAIT_LIMIT_MAX_NS = 1000, 600_000_000_000
 DEV_BAD_EXPERT, DEV_TIMEOUT = 1, 2
 MAX_EXPERTS, MAX_TOP_K = 1024, 16
@@ -53,6 +54,7 @@ ABI_SYMBOLS = [
     "moe_plan_stage_reset", "moe_plan_kernels_per_launch", "moe_plan_destroy", "moe_sort_no_alloc",
     "moe_fc1_swiglu_swapab", "moe_fc2_swapab", "moe_fc1_swiglu_gathered", "moe_plan_set_wait_limit",
     "moe_fc1_swiglu_step", "grouped_gemm_dgrad", "grouped_gemm_wgrad", "moe_bgmv_workspace_size", "moe_bgmv",
+    "moe_fc1_swiglu_e4m3", "moe_fc2_e4m3",
 ]
 
 
@@ -70,7 +72,8 @@ class _Desc(ctypes.Structure):
         ("status", ctypes.c_void_p), ("T", ctypes.c_int), ("H", ctypes.c_int), ("I", ctypes.c_int),
         ("E", ctypes.c_int), ("top_k", ctypes.c_int), ("local_offset", ctypes.c_int),
         ("num_local", ctypes.c_int), ("path", ctypes.c_int), ("flags", ctypes.c_int),
-        ("clamp_limit", ctypes.c_void_p),
+        ("clamp_limit", ctypes.c_void_p), ("weight_format", ctypes.c_int), ("w1_scale", ctypes.c_void_p),
+        ("w2_scale", ctypes.c_void_p), ("x_scale", ctypes.c_float), ("h_scale", ctypes.c_float),
     ]
 
 
@@ -108,6 +111,8 @@ def library():
             "moe_gather": ([P, P, P, I, I, I, I, P, P], I),
             "moe_fc1_swiglu": ([P, P, P, I, I, I, I, P, P], I),
             "moe_fc1_swiglu_step": ([P, P, P, P, I, I, I, I, P, P], I),
+            "moe_fc1_swiglu_e4m3": ([P, P, P, ctypes.c_float, ctypes.c_float, P, P, I, I, I, I, P, P], I),
+            "moe_fc2_e4m3": ([P, P, P, ctypes.c_float, P, I, I, I, I, P, P], I),
             "moe_fc2": ([P, P, P, I, I, I, I, P, P], I),
             "moe_fc1_swiglu_swapab": ([P, P, P, I, I, I, I, I, P, P], I),
             "moe_fc1_swiglu_gathered": ([P, P, P, I, I, P, I, I, I, P, P], I),
@@ -272,6 +277,34 @@ def moe_fc1_swiglu(xp: torch.Tensor, w1: torch.Tensor, m_indptr: torch.Tensor, h
     _check(library().moe_fc1_swiglu(_ptr(xp), _ptr(w1), _ptr(m_indptr), rows, H, I, L, _ptr(h),
                                     _stream(xp.device)), "moe_fc1_swiglu")
     return h
+
+
+def moe_fc1_swiglu_e4m3(xq, w1q, w1_scale, x_scale: float, h_scale: float, m_indptr, hq=None, clamp_limit=None):
+    """FC1 + SwiGLU(Step) on E4M3 rows: hq = e4m3(swiglu(dequantised u, g) / h_scale)."""
+    _need(xq, torch.uint8, "xq")
+    _need(w1q, torch.uint8, "w1q")
+    rows, H = xq.shape
+    L, twoI, _ = w1q.shape
+    I = twoI // 2
+    _need(w1_scale, torch.float32, "w1_scale", (L,), xq.device)
+    hq = torch.empty((rows, I), dtype=torch.uint8, device=xq.device) if hq is None else hq
+    _check(library().moe_fc1_swiglu_e4m3(_ptr(xq), _ptr(w1q), _ptr(w1_scale), float(x_scale), float(h_scale),
+                                         _ptr(clamp_limit), _ptr(m_indptr), rows, H, I, L, _ptr(hq),
+                                         _stream(xq.device)), "moe_fc1_swiglu_e4m3")
+    return hq
+
+
+def moe_fc2_e4m3(hq, w2q, w2_scale, h_scale: float, m_indptr, y=None):
+    """FC2 on E4M3 rows: y = (hq . W2q^T) * h_scale * w2_scale[e], fp32."""
+    _need(hq, torch.uint8, "hq")
+    _need(w2q, torch.uint8, "w2q")
+    rows, I = hq.shape
+    L, H, _ = w2q.shape
+    _need(w2_scale, torch.float32, "w2_scale", (L,), hq.device)
+    y = torch.empty((rows, H), dtype=torch.float32, device=hq.device) if y is None else y
+    _check(library().moe_fc2_e4m3(_ptr(hq), _ptr(w2q), _ptr(w2_scale), float(h_scale), _ptr(m_indptr), rows, H, I,
+                                  L, _ptr(y), _stream(hq.device)), "moe_fc2_e4m3")
+    return y
 
 
 def moe_fc2(h: torch.Tensor, w2: torch.Tensor, m_indptr: torch.Tensor, y=None):
@@ -461,12 +494,12 @@ def moe_workspace_size(T: int, H: int, I: int, E: int, top_k: int, num_local: in
     return int(library().moe_workspace_size(T, H, I, E, top_k, E if num_local is None else num_local))
 
 
-def _layer_args(x, w1, w2, num_experts, top_k, logits, topk_ids, topk_w, local_offset, out):
+def _layer_args(x, w1, w2, num_experts, top_k, logits, topk_ids, topk_w, local_offset, out, wdtype=torch.bfloat16):
     _need(x, torch.bfloat16, "x")
     dev = x.device
     T, H = x.shape
-    _need(w1, torch.bfloat16, "w1", device=dev)
-    _need(w2, torch.bfloat16, "w2", device=dev)
+    _need(w1, wdtype, "w1", device=dev)
+    _need(w2, wdtype, "w2", device=dev)
     L, twoI, H1 = w1.shape
     I = twoI // 2
     if H1 != H or tuple(w2.shape) != (L, H, I):
@@ -509,7 +542,7 @@ class MoEPlan:
                  local_offset: int = 0, out=None, workspace=None, status=None, path: int = PATH_AUTO,
                  stage_timing: bool = False, one_cta_gemm: bool = False, decode_chain: bool | None = None,
                  fused_gather: bool = False, decode_one_launch: bool = False,
-                 test_unreachable_wait: bool = False, clamp_limit=None):
+                 test_unreachable_wait: bool = False, clamp_limit=None, e4m3=None):
         """decode_chain: None lets the library choose the decode form (the
         chain in one launch for few routes, else five kernels), True forces
         the chain as two kernels, False the five separate kernels.
@@ -518,18 +551,27 @@ class MoEPlan:
         test_unreachable_wait: test hook (MOE_PLAN_TEST_UNREACHABLE_WAIT) that
         makes the one-launch decode chain's FC2 waits run out.
         clamp_limit: [L] fp32 device tensor of per-expert SwiGLUStep limits
-        (None: plain SwiGLU)."""
+        (None: plain SwiGLU).
+        e4m3: the fp8 per-tensor weight family: w1 / w2 are uint8 E4M3 codes and
+        e4m3 = dict(w1_scale=[L] fp32, w2_scale=[L] fp32, x_scale=float,
+        h_scale=float)."""
         T, H, I, L, out = _layer_args(x, w1, w2, num_experts, top_k, logits, topk_ids, topk_w,
-                                      local_offset, out)
+                                      local_offset, out, torch.uint8 if e4m3 is not None else torch.bfloat16)
         dev = x.device
         need = moe_workspace_size(T, H, I, num_experts, top_k, L)
         if workspace is None:
             workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
         if status is None:
             status = torch.zeros(1, dtype=torch.int32, device=dev)
+        q = dict(weight_format=WEIGHTS_BF16)
+        if e4m3 is not None:
+            _need(e4m3["w1_scale"], torch.float32, "w1_scale", (L,), dev)
+            _need(e4m3["w2_scale"], torch.float32, "w2_scale", (L,), dev)
+            q = dict(weight_format=WEIGHTS_E4M3, w1_scale=_ptr(e4m3["w1_scale"]), w2_scale=_ptr(e4m3["w2_scale"]),
+                     x_scale=float(e4m3["x_scale"]), h_scale=float(e4m3["h_scale"]))
         if clamp_limit is not None:
             _need(clamp_limit, torch.float32, "clamp_limit", (L,), dev)
-        self._keep = (x, w1, w2, logits, topk_ids, topk_w, out, workspace, status, clamp_limit)
+        self._keep = (x, w1, w2, logits, topk_ids, topk_w, out, workspace, status, clamp_limit, e4m3)
         self.x, self.w1, self.w2, self.logits, self.topk_ids, self.topk_w = x, w1, w2, logits, topk_ids, topk_w
         self.out, self.workspace, self.status = out, workspace, status
         self.T, self.H, self.I, self.E, self.top_k, self.L = T, H, I, num_experts, top_k, L
@@ -544,7 +586,7 @@ class MoEPlan:
                   | (PLAN_FUSED_GATHER if fused_gather else 0)
                   | (PLAN_DECODE_ONE_LAUNCH if decode_one_launch else 0)
                   | (PLAN_TEST_UNREACHABLE_WAIT if test_unreachable_wait else 0),
-                  clamp_limit=_ptr(clamp_limit))
+                  clamp_limit=_ptr(clamp_limit), **q)
         handle = ctypes.c_void_p()
         _check(library().moe_forward_prepare(ctypes.byref(d), ctypes.byref(handle)), "moe_forward_prepare")
         self._h = handle

@@ -109,6 +109,7 @@ struct moe_plan {
   bool use_chain;
   bool unreachable_wait;  // test hook MOE_PLAN_TEST_UNREACHABLE_WAIT
   bool fused_gather;    // grouped path: FC1 gathers its rows itself
+  bool e4m3;            // E4M3 weight family (one-CTA kernels, quantising gather)
   bool timing;
   cudaEvent_t (*ev)[kNumStages + 1];
   long n_recorded;
@@ -132,7 +133,7 @@ const char *moe_status_string(int code) {
   }
 }
 
-int moe_abi_version(void) { return 101; }
+int moe_abi_version(void) { return 102; }
 
 int moe_route(const float *logits, int T, int E, int top_k, int32_t *topk_ids, float *topk_w,
               void *stream) {
@@ -239,6 +240,50 @@ int moe_fc1_swiglu_step(const moe_bf16 *xp, const moe_bf16 *w1, const float *cla
                             m_indptr + 1, max_rows, h, nullptr))
     return rc;
   p.clamp = clamp_limit;
+  Launch l;
+  l.stream = static_cast<cudaStream_t>(stream);
+  return cuda_rc(launch_gemm(p, l));
+}
+
+int moe_fc1_swiglu_e4m3(const uint8_t *xq, const uint8_t *w1q, const float *w1_scale, float x_scale,
+                        float h_scale, const float *clamp_limit, const int32_t *m_indptr, int max_rows,
+                        int H, int I, int num_local, uint8_t *hq, void *stream) {
+  if (max_rows < 0 || H <= 0 || I <= 0 || H % 128 || I % 128 || num_local < 1 ||
+      num_local > MOE_MAX_EXPERTS || !(x_scale > 0.f) || !(h_scale > 0.f))
+    return MOE_ERR_SHAPE;
+  if (max_rows == 0) return MOE_OK;
+  if (!xq || !w1q || !w1_scale || !m_indptr || !hq) return MOE_ERR_NULL;
+  if (!aligned16(xq) || !aligned16(w1q) || !aligned16(hq)) return MOE_ERR_ALIGN;
+  if (int rc = check_device()) return rc;
+  GemmPlan p;
+  if (int rc = gemm_prepare_e4m3(p, Epi::kSwiGLU, xq, max_rows, w1q, num_local, 2 * I, H, I, m_indptr + 1,
+                                 max_rows, hq, nullptr))
+    return rc;
+  p.clamp = clamp_limit;
+  p.wscale = w1_scale;
+  p.ascale = x_scale;
+  p.oscale = h_scale;
+  Launch l;
+  l.stream = static_cast<cudaStream_t>(stream);
+  return cuda_rc(launch_gemm(p, l));
+}
+
+int moe_fc2_e4m3(const uint8_t *hq, const uint8_t *w2q, const float *w2_scale, float h_scale,
+                 const int32_t *m_indptr, int max_rows, int H, int I, int num_local, float *y,
+                 void *stream) {
+  if (max_rows < 0 || H <= 0 || I <= 0 || H % 128 || I % 128 || num_local < 1 ||
+      num_local > MOE_MAX_EXPERTS || !(h_scale > 0.f))
+    return MOE_ERR_SHAPE;
+  if (max_rows == 0) return MOE_OK;
+  if (!hq || !w2q || !w2_scale || !m_indptr || !y) return MOE_ERR_NULL;
+  if (!aligned16(hq) || !aligned16(w2q) || !aligned16(y)) return MOE_ERR_ALIGN;
+  if (int rc = check_device()) return rc;
+  GemmPlan p;
+  if (int rc = gemm_prepare_e4m3(p, Epi::kF32, hq, max_rows, w2q, num_local, H, I, H, m_indptr + 1,
+                                 max_rows, y, nullptr))
+    return rc;
+  p.wscale = w2_scale;
+  p.ascale = h_scale;
   Launch l;
   l.stream = static_cast<cudaStream_t>(stream);
   return cuda_rc(launch_gemm(p, l));
@@ -471,6 +516,13 @@ int moe_forward_prepare(const moe_forward_desc *desc, moe_plan **plan_out) {
     if (routed_mode && (!d.topk_ids || !d.topk_w)) return MOE_ERR_MODE;
   }
   if (d.path < MOE_PATH_AUTO || d.path > MOE_PATH_DECODE) return MOE_ERR_SHAPE;
+  if (d.weight_format != MOE_WEIGHTS_BF16 && d.weight_format != MOE_WEIGHTS_E4M3) return MOE_ERR_SHAPE;
+  const bool e4m3 = d.weight_format == MOE_WEIGHTS_E4M3;
+  if (e4m3) {
+    if (d.H % 128 || d.I % 128 || d.path == MOE_PATH_DECODE) return MOE_ERR_SHAPE;
+    if (!(d.x_scale > 0.f) || !(d.h_scale > 0.f)) return MOE_ERR_SHAPE;
+    if (d.T > 0 && (!d.w1_scale || !d.w2_scale)) return MOE_ERR_NULL;
+  }
   if (d.T > 0) {
     if (!d.x || !d.w1 || !d.w2 || !d.out) return MOE_ERR_NULL;
     if (!aligned16(d.x) || !aligned16(d.w1) || !aligned16(d.w2) || !aligned16(d.out))
@@ -488,6 +540,8 @@ int moe_forward_prepare(const moe_forward_desc *desc, moe_plan **plan_out) {
   p->logits_mode = logits_mode;
   // Few tokens: each expert gets at most a few rows, the layer streams weights.
   p->path = d.path != MOE_PATH_AUTO ? d.path : (d.T <= kDecodeMaxTokens ? MOE_PATH_DECODE : MOE_PATH_GROUPED);
+  p->e4m3 = e4m3;
+  if (e4m3) p->path = MOE_PATH_GROUPED;
   p->R = (long)d.T * d.top_k;
   unsigned char *ws = static_cast<unsigned char *>(d.workspace);
   if (d.T > 0) {
@@ -543,6 +597,20 @@ int moe_forward_prepare(const moe_forward_desc *desc, moe_plan **plan_out) {
       if (rc == MOE_OK)
         rc = swap_prepare(p->fc2d, false, d.w2, d.num_local, d.H, d.I, p->h, p->R, d.H,
                           p->m_indptr + 1, d.T, p->y, d.status, true);
+    } else if (e4m3) {
+      uint8_t *xq = reinterpret_cast<uint8_t *>(p->xp), *hq = reinterpret_cast<uint8_t *>(p->h);
+      rc = gemm_prepare_e4m3(p->fc1, Epi::kSwiGLU, xq, p->R, static_cast<const uint8_t *>(static_cast<const void *>(d.w1)),
+                             d.num_local, 2 * d.I, d.H, d.I, p->m_indptr + 1, p->R, hq, d.status);
+      p->fc1.clamp = d.clamp_limit;
+      p->fc1.wscale = d.w1_scale;
+      p->fc1.ascale = d.x_scale;
+      p->fc1.oscale = d.h_scale;
+      if (rc == MOE_OK) {
+        rc = gemm_prepare_e4m3(p->fc2, Epi::kF32, hq, p->R, static_cast<const uint8_t *>(static_cast<const void *>(d.w2)),
+                               d.num_local, d.H, d.I, d.H, p->m_indptr + 1, p->R, p->y, d.status);
+        p->fc2.wscale = d.w2_scale;
+        p->fc2.ascale = d.h_scale;
+      }
     } else {
       const bool pair = (d.flags & MOE_PLAN_ONE_CTA_GEMM) == 0;
       // Either the gather kernel builds xp (one 128-row TMA box per k-block
@@ -635,9 +703,13 @@ int moe_plan_launch(moe_plan *p, void *stream) {
   const bool dec = p->path == MOE_PATH_DECODE;
   // grouped path: one warp per token (x read once); decode path: one warp
   // per route (a handful of tokens would leave most of the GPU idle)
-  if (!p->fused_gather &&
-      (dec ? launch_gather(d.x, p->p2e, p->m_indptr + d.num_local, d.H, d.top_k, p->R, p->xp, l)
-           : launch_gather_tokens(d.x, p->e2p, d.T, d.H, d.top_k, p->R, p->xp, l)) != cudaSuccess)
+  if (p->e4m3) {
+    if (launch_gather_tokens_q(d.x, p->e2p, d.T, d.H, d.top_k, d.x_scale, p->R,
+                               reinterpret_cast<uint8_t *>(p->xp), l) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  } else if (!p->fused_gather &&
+             (dec ? launch_gather(d.x, p->p2e, p->m_indptr + d.num_local, d.H, d.top_k, p->R, p->xp, l)
+                  : launch_gather_tokens(d.x, p->e2p, d.T, d.H, d.top_k, p->R, p->xp, l)) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (!mark(kFc1)) return MOE_ERR_CUDA;
   if ((dec ? launch_swap(p->fc1d, l) : launch_gemm(p->fc1, l)) != cudaSuccess) return MOE_ERR_CUDA;

@@ -13,6 +13,12 @@
 //             (GEMM1 with the SwiGLU fused, cute_dsl_fused_moe_bf16,
 //             Supported configuration);
 //   kF32    - Y stored as fp32, unrounded (GEMM2 of the deterministic path).
+// With Q = 1 the operands are E4M3 codes (the fp8 per-tensor weight family of
+// flashinfer.experimental.cake_stepfun_moe, opening paragraph): a k-block is
+// 128 codes (still one 128-byte swizzled row), the MMA is kind::f8f6f4 with
+// K = 32, the accumulator is dequantised by ascale * wscale[group], and the
+// SwiGLU epilogue writes E4M3 h = e4m3(h / oscale) (the requantisation
+// between FC1 and FC2).
 //
 // CTA organisation (192 threads, one CTA per SM, persistent):
 //   warp 0      TMA producer: one thread streams A and B k-blocks into a
@@ -54,6 +60,8 @@ struct GemmArgs {
   int32_t *status;
   unsigned long long wait_ns;  // bounded-wait limit of this launch
   const float *clamp;         // SwiGLU epilogue: [groups] SwiGLUStep limits, or null
+  const float *wscale;        // E4M3: [groups] weight scales
+  float ascale, oscale;       // E4M3: activation scale of A, requantisation scale of h
   long max_rows;
   int G;
   int K;
@@ -111,7 +119,7 @@ __device__ __forceinline__ TileCoord decode_tile(int t, const int *tile_start, i
   return c;
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, int Q>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmArgs args) {
   using C = Cfg<BN>;
   extern __shared__ unsigned char smem_raw[];
@@ -192,7 +200,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
 
   const uint32_t tmem_base = *tmem_holder;
   const int total = tile_start[G] * args.n_tiles;
-  const int num_kb = args.K / BK;
+  constexpr int KB = Q ? 128 : BK;  // elements per k-block (128 bytes either way)
+  const int num_kb = args.K / KB;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -220,12 +229,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
           const uint32_t a_dst = smem_base + s * C::STAGE_BYTES;
           const uint32_t b_dst = a_dst + C::A_BYTES;
           mbar_arrive_expect_tx(full_bar(s), C::STAGE_BYTES);
-          tma_load_2d(a_dst, &args.map_a, full_bar(s), kb * BK, row0, pol);
+          tma_load_2d(a_dst, &args.map_a, full_bar(s), kb * KB, row0, pol);
           if (EPI == (int)Epi::kSwiGLU) {
-            tma_load_2d(b_dst, &args.map_b, full_bar(s), kb * BK, brow0, pol);
-            tma_load_2d(b_dst + (BN / 2) * 128, &args.map_b, full_bar(s), kb * BK, brow1, pol);
+            tma_load_2d(b_dst, &args.map_b, full_bar(s), kb * KB, brow0, pol);
+            tma_load_2d(b_dst + (BN / 2) * 128, &args.map_b, full_bar(s), kb * KB, brow1, pol);
           } else {
-            tma_load_2d(b_dst, &args.map_b, full_bar(s), kb * BK, brow0, pol);
+            tma_load_2d(b_dst, &args.map_b, full_bar(s), kb * KB, brow0, pol);
           }
         }
       }
@@ -257,7 +266,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
           const uint64_t b_desc = smem_desc_k_sw128(a_addr + C::A_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)  // K = 16 per MMA: +32 bytes in the swizzled row
-            umma_bf16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, C::IDESC, (kb | k) != 0);
+            if (Q)  // K = 32 E4M3 codes per MMA: the same 32 bytes of the swizzled row
+              umma_e4m3(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc_e4m3_f32(BM, BN), (kb | k) != 0);
+            else
+              umma_bf16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, C::IDESC, (kb | k) != 0);
           umma_commit(empty_bar(s));
         }
         if (ok) umma_commit(tfull_bar(acc));
@@ -282,7 +294,55 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
       const bool row_ok = r_in_tile < valid;
       const long orow = (long)row0 + r_in_tile;
-      if (EPI == (int)Epi::kSwiGLU) {
+      if (Q && EPI == (int)Epi::kSwiGLU) {
+        // E4M3: u, g dequantised by ascale * wscale[g], SwiGLU(Step), h requantised
+        uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(args.out) +
+                                               orow * args.n_out + (long)c.n * (BN / 2));
+        const float lim = step_limit(args.clamp, c.g);
+        const float sc = __fmul_rn(args.ascale, __ldg(args.wscale + c.g));
+#pragma unroll 1
+        for (int col = 0; col < BN / 2; col += 32) {
+          uint32_t u[32], g[32];
+          tmem_ld_32x32b_x32(taddr + col, u);
+          tmem_ld_32x32b_x32(taddr + BN / 2 + col, g);
+          tmem_ld_wait();
+          uint32_t packed[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            float hv[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float uu = __fmul_rn(__uint_as_float(u[4 * i + q]), sc);
+              const float gg = __fmul_rn(__uint_as_float(g[4 * i + q]), sc);
+              hv[q] = __fdiv_rn(swiglu_step(gg, uu, lim), args.oscale);
+            }
+            packed[i] = e4m3x2(hv[0], hv[1]) | (e4m3x2(hv[2], hv[3]) << 16);
+          }
+          if (row_ok) {
+            dst[col / 16] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            dst[col / 16 + 1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+          }
+        }
+      } else if (Q && EPI == (int)Epi::kF32) {
+        // E4M3: y dequantised by ascale * wscale[g]
+        uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<float *>(args.out) +
+                                               orow * args.n_out + (long)c.n * BN);
+        const float sc = __fmul_rn(args.ascale, __ldg(args.wscale + c.g));
+#pragma unroll 1
+        for (int col = 0; col < BN; col += 32) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(taddr + col, r);
+          tmem_ld_wait();
+          if (row_ok) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              dst[col / 4 + v] = make_uint4(__float_as_uint(__fmul_rn(__uint_as_float(r[4 * v]), sc)),
+                                            __float_as_uint(__fmul_rn(__uint_as_float(r[4 * v + 1]), sc)),
+                                            __float_as_uint(__fmul_rn(__uint_as_float(r[4 * v + 2]), sc)),
+                                            __float_as_uint(__fmul_rn(__uint_as_float(r[4 * v + 3]), sc)));
+          }
+        }
+      } else if (EPI == (int)Epi::kSwiGLU) {
         uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(args.out) +
                                                orow * args.n_out + (long)c.n * (BN / 2));
         const float lim = step_limit(args.clamp, c.g);
@@ -396,15 +456,15 @@ int encode_2d(CUtensorMap *map, const void *ptr, long rows, int K, int box_rows)
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_TENSOR_MAP;
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, int Q = 0>
 cudaError_t configure_inst(const GemmPlan &p) {
-  return cudaFuncSetAttribute(grouped_gemm_kernel<BN, EPI>,
+  return cudaFuncSetAttribute(grouped_gemm_kernel<BN, EPI, Q>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, int Q = 0>
 cudaError_t launch_inst(const GemmPlan &p, const Launch &l) {
-  auto kern = grouped_gemm_kernel<BN, EPI>;
+  auto kern = grouped_gemm_kernel<BN, EPI, Q>;
   GemmArgs a;
   a.map_a = p.map_a;
   a.map_b = p.map_b;
@@ -413,6 +473,9 @@ cudaError_t launch_inst(const GemmPlan &p, const Launch &l) {
   a.status = p.status;
   a.wait_ns = p.wait_ns;
   a.clamp = p.clamp;
+  a.wscale = p.wscale;
+  a.ascale = p.ascale;
+  a.oscale = p.oscale;
   a.max_rows = p.max_rows;
   a.G = p.G;
   a.K = p.K;
@@ -503,6 +566,67 @@ static cudaError_t configure_gemm(const GemmPlan &p) {
   return configure_inst<64, (int)Epi::kBf16>(p);
 }
 
+// uint8 [rows, K] (E4M3 codes), box {128, box_rows}, 128-byte swizzle, zero fill.
+static int encode_2d_u8(CUtensorMap *map, const void *ptr, long rows, int K, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return MOE_ERR_DEVICE;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)(rows > 0 ? rows : 1)};
+  cuuint64_t strides[1] = {(cuuint64_t)K};
+  cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides,
+                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_TENSOR_MAP;
+}
+
+int gemm_prepare_e4m3(GemmPlan &p, Epi epi, const uint8_t *A, long a_rows, const uint8_t *B, int G,
+                      int b_rows, int K, int n_out, const int32_t *group_end, long max_rows,
+                      void *out, int32_t *status) {
+  if (K % 128 != 0 || epi == Epi::kBf16) return MOE_ERR_SHAPE;
+  p = GemmPlan();
+  p.q = 1;
+  p.epi = epi;
+  p.G = G;
+  p.K = K;
+  p.n_out = n_out;
+  p.b_rows = b_rows;
+  p.group_end = group_end;
+  p.max_rows = max_rows;
+  p.out = out;
+  p.status = status;
+  int box_b;
+  if (epi == Epi::kSwiGLU) {
+    if (n_out % 128 != 0) return MOE_ERR_SHAPE;  // 32 h codes per epilogue step, 128 per tile half
+    p.bn = 256;
+    p.n_tiles = n_out / 128;
+    box_b = 128;
+  } else {
+    p.bn = (n_out % 256 == 0) ? 256 : ((n_out % 128 == 0) ? 128 : 64);
+    p.n_tiles = n_out / p.bn;
+    box_b = p.bn;
+  }
+  int rc = encode_2d_u8(&p.map_a, A, a_rows, K, BM);
+  if (rc == MOE_OK) rc = encode_2d_u8(&p.map_b, B, (long)G * b_rows, K, box_b);
+  if (rc != MOE_OK) return rc;
+  const double b_group_bytes = (double)b_rows * K;
+  p.m_major = b_group_bytes <= 64.0 * 1024 * 1024 ? 1 : 0;
+  switch (p.bn) {
+    case 256: p.smem = Cfg<256>::smem_bytes(G); break;
+    case 128: p.smem = Cfg<128>::smem_bytes(G); break;
+    default: p.smem = Cfg<64>::smem_bytes(G); break;
+  }
+  const long sms = device_sm_count();
+  const long max_tiles = ((max_rows + BM - 1) / BM + G) * (long)p.n_tiles;
+  p.grid = (int)(max_tiles < sms ? (max_tiles > 0 ? max_tiles : 1) : sms);
+  cudaError_t e;
+  if (epi == Epi::kSwiGLU) e = configure_inst<256, (int)Epi::kSwiGLU, 1>(p);
+  else if (p.bn == 256) e = configure_inst<256, (int)Epi::kF32, 1>(p);
+  else if (p.bn == 128) e = configure_inst<128, (int)Epi::kF32, 1>(p);
+  else e = configure_inst<64, (int)Epi::kF32, 1>(p);
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 int gemm_prepare_gather(GemmPlan &p, const uint16_t *x, long x_rows, const int32_t *p2e, int k,
                         const uint16_t *W1, int G, int I, int H, const int32_t *group_end,
                         long max_rows, void *h, int32_t *status) {
@@ -520,6 +644,13 @@ int gemm_prepare_gather(GemmPlan &p, const uint16_t *x, long x_rows, const int32
 
 cudaError_t launch_gemm(const GemmPlan &p, const Launch &l) {
   if (p.pair) return launch_pair_gemm(p, l);
+  if (p.q) {
+    if (p.epi == Epi::kSwiGLU)
+      return p.bn == 256 ? launch_inst<256, (int)Epi::kSwiGLU, 1>(p, l) : launch_inst<128, (int)Epi::kSwiGLU, 1>(p, l);
+    if (p.bn == 256) return launch_inst<256, (int)Epi::kF32, 1>(p, l);
+    if (p.bn == 128) return launch_inst<128, (int)Epi::kF32, 1>(p, l);
+    return launch_inst<64, (int)Epi::kF32, 1>(p, l);
+  }
   if (p.epi == Epi::kSwiGLU) {
     if (p.bn == 256) return launch_inst<256, (int)Epi::kSwiGLU>(p, l);
     return launch_inst<128, (int)Epi::kSwiGLU>(p, l);

@@ -50,6 +50,9 @@ cudaError_t launch_gather_tokens(const uint16_t *x, const int32_t *e2p, int T, i
                                  long max_rows, uint16_t *xp, const Launch &l);
 cudaError_t launch_finalize(const float *y, const int32_t *e2p, const float *w, int T, int k,
                             int H, uint16_t *out, const Launch &l);
+// Token-major copy with E4M3 quantisation: xq[p] = e4m3(x[t] / scale) (H % 16 == 0).
+cudaError_t launch_gather_tokens_q(const uint16_t *x, const int32_t *e2p, int T, int H, int k,
+                                   float scale, long max_rows, uint8_t *xq, const Launch &l);
 
 // S4 / S5 / S8: persistent tcgen05 grouped GEMM --------------------------------
 enum class Epi : int { kBf16 = 0, kSwiGLU = 1, kF32 = 2 };
@@ -81,6 +84,11 @@ struct GemmPlan {
   int32_t *status = nullptr;
   unsigned long long wait_ns = kWaitLimitNs;
   const float *clamp = nullptr;  // SwiGLU epilogue: [G] SwiGLUStep limits (device), or null
+  // E4M3 operands (one-CTA kernel only): the accumulator is dequantised by
+  // ascale * wscale[g]; the SwiGLU epilogue writes E4M3 h = e4m3(h / oscale)
+  int q = 0;
+  const float *wscale = nullptr;
+  float ascale = 1.f, oscale = 1.f;
 };
 
 // Encodes the tensor maps and picks tile shapes; host only.  allow_pair lets
@@ -94,6 +102,12 @@ int gemm_prepare_gather(GemmPlan &p, const uint16_t *x, long x_rows, const int32
                         const uint16_t *W1, int G, int I, int H, const int32_t *group_end,
                         long max_rows, void *h, int32_t *status);
 cudaError_t launch_gemm(const GemmPlan &p, const Launch &l);
+// E4M3 operands A [a_rows, K], B [G * b_rows, K] (uint8 codes), one-CTA kernel,
+// SwiGLU (E4M3 h out) or fp32 epilogue; K % 128 == 0.  Set wscale / ascale /
+// oscale on the plan afterwards.
+int gemm_prepare_e4m3(GemmPlan &p, Epi epi, const uint8_t *A, long a_rows, const uint8_t *B, int G,
+                      int b_rows, int K, int n_out, const int32_t *group_end, long max_rows,
+                      void *out, int32_t *status);
 
 // CTA-pair form (gemm2sm.cu)
 size_t pair_gemm_smem(Epi epi, int G);

@@ -216,6 +216,33 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
          | ((M >> 4) << 24);  // M / 16
 }
 
+// Instruction descriptor: dense kind::f8f6f4 MMA, A and B E4M3 K-major, D fp32.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t M, uint32_t N) {
+  return (1u << 4)            // D format: f32
+                              // A, B format 0: E4M3
+         | ((N >> 3) << 17)   // N / 8
+         | ((M >> 4) << 24);  // M / 16
+}
+
+// D[tmem] (+)= A[smem] . B[smem]^T with E4M3 operands (K = 32 per instruction).
+__device__ __forceinline__ void umma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Two fp32 values to E4M3 codes (round to nearest even, magnitudes above 448
+// saturating to 448): lo in bits 0..7, hi in bits 8..15.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return (uint32_t)r;
+}
+
 // silu(g) = g / (1 + exp(-g)) in fp32: exp from the fast hardware exponential,
 // the quotient as g times a correctly rounded reciprocal.  The result is
 // rounded to bf16 right after (h), so its few-ulp fp32 error only decides

@@ -85,6 +85,48 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// The token-major copy for E4M3 activations: each element of x is divided by
+// the per-tensor scale (fp32, correctly rounded) and converted to E4M3
+// (nearest even, saturating at 448); a lane turns 16 bf16 values (32 bytes)
+// into 16 codes (one 16-byte store per route row).
+__global__ void __launch_bounds__(256)
+    gather_tokens_q_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ e2p, int T, int k,
+                           int vec16, float scale, long max_rows, uint4 *__restrict__ xq) {
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const long warp = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const long nwarps = ((long)gridDim.x * blockDim.x) >> 5;
+  pdl_launch_dependents();
+  for (long t = warp; t < T; t += nwarps) {
+    const int my_p = lane < k ? e2p[t * k + lane] : -1;
+    const uint4 *src = x + t * 2 * vec16;
+    for (int b = 0; b < vec16; b += 32) {  // warp-uniform bounds: every lane reaches each shuffle
+      const int i = b + lane;
+      const bool in = i < vec16;
+      uint4 q = make_uint4(0, 0, 0, 0);
+      if (in) {
+        const uint4 v0 = __ldg(src + 2 * i), v1 = __ldg(src + 2 * i + 1);
+        const uint32_t u[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        uint32_t c[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t a = u[2 * j], bb = u[2 * j + 1];
+          const uint32_t lo = e4m3x2(__fdiv_rn(__uint_as_float(a << 16), scale),
+                                     __fdiv_rn(__uint_as_float(a & 0xFFFF0000u), scale));
+          const uint32_t hi = e4m3x2(__fdiv_rn(__uint_as_float(bb << 16), scale),
+                                     __fdiv_rn(__uint_as_float(bb & 0xFFFF0000u), scale));
+          c[j] = lo | (hi << 16);
+        }
+        q = make_uint4(c[0], c[1], c[2], c[3]);
+      }
+      for (int s = 0; s < k; ++s) {
+        const int p = __shfl_sync(0xffffffffu, my_p, s);
+        if (p >= 0 && p < max_rows && in) __stcs(xq + (long)p * vec16 + i, q);
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t *>(&v);
@@ -144,6 +186,17 @@ cudaError_t launch_gather(const uint16_t *x, const int32_t *p2e, const int32_t *
   return launch_kernel(gather_kernel, dim3(blocks), dim3(256), 0, l,
                        reinterpret_cast<const uint4 *>(x), p2e, m_total, H / 8, k,
                        reinterpret_cast<uint4 *>(xp));
+}
+
+cudaError_t launch_gather_tokens_q(const uint16_t *x, const int32_t *e2p, int T, int H, int k,
+                                   float scale, long max_rows, uint8_t *xq, const Launch &l) {
+  if (T <= 0) return cudaSuccess;
+  const long want_blocks = ((long)T + 7) / 8;
+  const long cap = (long)device_sm_count() * 8;
+  const int blocks = (int)(want_blocks < cap ? want_blocks : cap);
+  return launch_kernel(gather_tokens_q_kernel, dim3(blocks), dim3(256), 0, l,
+                       reinterpret_cast<const uint4 *>(x), e2p, T, k, H / 16, scale, max_rows,
+                       reinterpret_cast<uint4 *>(xq));
 }
 
 cudaError_t launch_gather_tokens(const uint16_t *x, const int32_t *e2p, int T, int H, int k,

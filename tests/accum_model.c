@@ -168,6 +168,123 @@ int am_moe_tokens(const uint16_t *x, const int32_t *ids, const float *w, const u
   return bad;
 }
 
+/* ---- the fp8 per-tensor family (E4M3 operands) --------------------------
+ * xq = e4m3(x / a1); u, g = model dot of xq and W1q rows times a1 * s1[e];
+ * hq = e4m3(swiglu(limit) / a2); y = model dot of hq and W2q rows times
+ * a2 * s2[e]; the combine as above.  In mode 1 the blocks are 32 products
+ * (the K of one E4M3 MMA); products of two E4M3 values are exact. */
+static float am_e4m3_to_float(uint8_t b) {
+  const int e = (b >> 3) & 15, m = b & 7;
+  const float v = e == 0 ? ldexpf((float)m, -9) : ldexpf((float)(8 + m), e - 10);
+  return (b & 0x80) ? -v : v;
+}
+
+/* nearest E4M3 code by search over the 127 magnitudes, ties to the even code,
+ * above 448 saturating */
+static uint8_t am_float_to_e4m3(float f) {
+  const uint8_t s = signbit(f) ? 0x80 : 0;
+  const float a = fabsf(f);
+  if (a >= 448.0f) return s | 0x7E;
+  int best = 0;
+  float bd = a;
+  for (int c = 1; c <= 0x7E; ++c) {
+    const float d = fabsf(am_e4m3_to_float((uint8_t)c) - a);
+    if (d < bd || (d == bd && (c & 1) == 0)) {
+      bd = d;
+      best = c;
+    }
+  }
+  return (uint8_t)(s | best);
+}
+
+static double am_dot_q(const uint8_t *a, const uint8_t *b, int K, int mode) {
+  enum { QB = 32 };
+  float acc = 0.0f;
+  for (int k0 = 0; k0 < K; k0 += QB) {
+    const int n = K - k0 < QB ? K - k0 : QB;
+    double p[QB + 1];
+    for (int i = 0; i < n; ++i) p[i] = (double)am_e4m3_to_float(a[k0 + i]) * (double)am_e4m3_to_float(b[k0 + i]);
+    if (mode == 0) {
+      float s = 0.0f;
+      for (int i = 0; i < n; ++i) s = s + (float)p[i];
+      acc = acc + s;
+      continue;
+    }
+    p[n] = (double)acc;
+    double big = 0.0;
+    for (int i = 0; i <= n; ++i)
+      if (fabs(p[i]) > big) big = fabs(p[i]);
+    if (big == 0.0) continue;
+    const double up = ldexp(1.0, 23 + GUARD_BITS - ilogb(big));
+    double s = 0.0;
+    for (int i = 0; i <= n; ++i) s += trunc(p[i] * up);
+    acc = am_round_toward_zero(s / up);
+  }
+  return (double)acc;
+}
+
+int am_moe_tokens_e4m3(const uint16_t *x, const int32_t *ids, const float *w, const uint8_t *w1q,
+                       const uint8_t *w2q, const float *s1, const float *s2, float a1, float a2, int T,
+                       int H, int I, int E, int k, int off, int L, const int32_t *tokens, int n_tok,
+                       uint16_t *out, int mode, int nthreads, const float *clamp) {
+  (void)T;
+  int bad = 0;
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+  (void)nthreads;
+#endif
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+  for (int i = 0; i < n_tok; ++i) {
+    const int t = tokens[i];
+    uint8_t *xq = (uint8_t *)malloc((size_t)H);
+    uint8_t *hq = (uint8_t *)malloc((size_t)I);
+    float *ys = (float *)malloc(sizeof(float) * (size_t)k * H);
+    if (!xq || !hq || !ys) {
+      free(xq);
+      free(hq);
+      free(ys);
+      bad |= 2;
+      continue;
+    }
+    for (int c = 0; c < H; ++c) xq[c] = am_float_to_e4m3(am_bf16_to_float(x[(size_t)t * H + c]) / a1);
+    int local[16];
+    for (int j = 0; j < k; ++j) {
+      const int g = ids[(size_t)t * k + j];
+      local[j] = 0;
+      if (g < 0 || g >= E) {
+        bad |= 1;
+        continue;
+      }
+      if (g < off || g >= off + L) continue;
+      local[j] = 1;
+      const int e = g - off;
+      const uint8_t *W1 = w1q + (size_t)e * 2 * I * H;
+      const uint8_t *W2 = w2q + (size_t)e * H * I;
+      const float sc1 = a1 * s1[e], sc2 = a2 * s2[e];
+      const float lim = clamp ? clamp[e] : INFINITY;
+      for (int c = 0; c < I; ++c) {
+        float u = (float)am_dot_q(xq, W1 + (size_t)c * H, H, mode) * sc1;
+        float gt = (float)am_dot_q(xq, W1 + (size_t)(I + c) * H, H, mode) * sc1;
+        gt = gt > lim ? lim : gt;
+        u = u > lim ? lim : (u < -lim ? -lim : u);
+        hq[c] = am_float_to_e4m3((gt / (1.0f + expf(-gt))) * u / a2);
+      }
+      for (int c = 0; c < H; ++c) ys[(size_t)j * H + c] = (float)am_dot_q(hq, W2 + (size_t)c * I, I, mode) * sc2;
+    }
+    for (int c = 0; c < H; ++c) {
+      float acc = 0.0f;
+      for (int j = 0; j < k; ++j)
+        if (local[j]) acc = acc + w[(size_t)t * k + j] * ys[(size_t)j * H + c];
+      out[(size_t)i * H + c] = am_float_to_bf16(acc);
+    }
+    free(xq);
+    free(hq);
+    free(ys);
+  }
+  return bad;
+}
+
 int am_max_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();

@@ -57,6 +57,9 @@ def load():
         lib.am_dot.restype = ctypes.c_double
         lib.am_dots.argtypes = [P, P, i, i, i, i, P]
         lib.am_dots.restype = None
+        f = ctypes.c_float
+        lib.am_moe_tokens_e4m3.argtypes = [P, P, P, P, P, P, P, f, f, i, i, i, i, i, i, i, P, i, P, i, i, P]
+        lib.am_moe_tokens_e4m3.restype = i
         lib.am_moe_tokens.argtypes = [P, P, P, P, P, i, i, i, i, i, i, i, P, i, P, P, i, i, P]
         lib.am_moe_tokens.restype = i
         _lib = lib
@@ -129,5 +132,32 @@ def floor(x, ids, w, w1, w2, num_experts, want_bits, tokens=None, local_offset=0
     sub = tokens[:n]
     out = moe_tokens(x, ids, w, w1, w2, num_experts, TENSOR_CORE, tokens=sub, local_offset=local_offset,
                      num_local=num_local, clamp_limit=clamp_limit)
+    ref = np.asarray(want_bits)[:n]
+    return float(np.mean(ulp_distance(out, ref) <= 2)), int(out.size)
+
+
+def floor_e4m3(x, ids, w, w1q, w2q, s1, s2, a1, a2, num_experts, want_bits, tokens=None, local_offset=0,
+               num_local=None, max_macs=1.5e10, clamp_limit=None):
+    """The floor of the fp8 per-tensor family: the tensor-core model of the
+    E4M3 layer on (a subset of) the tokens against the oracle's rows."""
+    from tests.tolerances import ulp_distance
+    x = np.ascontiguousarray(x, np.uint16)
+    T, H = x.shape
+    ids = np.ascontiguousarray(ids, np.int32)
+    k = ids.shape[1]
+    w1q = np.ascontiguousarray(w1q, np.uint8)
+    w2q = np.ascontiguousarray(w2q, np.uint8)
+    L = w1q.shape[0] if num_local is None else num_local
+    I = w1q.shape[1] // 2
+    tokens = np.arange(T, dtype=np.int32) if tokens is None else np.asarray(tokens, np.int32)
+    n = int(min(len(tokens), max(1, max_macs // max(1.0, k * 3.0 * H * I))))
+    sub = np.ascontiguousarray(tokens[:n])
+    out = np.empty((n, H), np.uint16)
+    clamp = None if clamp_limit is None else np.ascontiguousarray(clamp_limit, np.float32)
+    rc = load().am_moe_tokens_e4m3(_p(x), _p(ids), _p(np.ascontiguousarray(w, np.float32)), _p(w1q), _p(w2q),
+                                   _p(np.ascontiguousarray(s1, np.float32)), _p(np.ascontiguousarray(s2, np.float32)),
+                                   float(a1), float(a2), T, H, I, num_experts, k, local_offset, L, _p(sub), n,
+                                   _p(out), TENSOR_CORE, 0, _p(clamp))
+    assert rc & 2 == 0
     ref = np.asarray(want_bits)[:n]
     return float(np.mean(ulp_distance(out, ref) <= 2)), int(out.size)

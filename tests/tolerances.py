@@ -107,10 +107,21 @@ def floor_margin(frac: float, n: int) -> float:
     return 1e-3 + 4.0 * float(np.sqrt(max(frac * (1.0 - frac), 1.0 / n) / n))
 
 
-def check_bf16_end_to_end(got_bits: np.ndarray, want_bits: np.ndarray, what: str = "output"):
-    """End-to-end rule: per-element max bound as in check_bf16_close, and the
-    2-ulp fraction at least the attached floor less floor_margin.  Returns the
-    fraction."""
+# The E4M3 family requantises h to 3 mantissa bits instead of bf16's 8, so one
+# rounding flip of h moves the outputs it feeds 2^5 = 32 times further than in
+# the bf16 family: w * h_scale * w2_scale * |W2| * 2^-3 |h|, about 1-1.5 % of
+# rms(out) per flip at the test shapes.  North_star states no bound for this
+# family; the max term below allows a few coinciding flips (4 % of rms) while a
+# wrong scale, a dropped term or a wrong expert still moves outputs by 10 % of
+# rms or more.  The 2-ulp fraction keeps its accumulation-model floor.
+RMS_FRAC_E4M3 = 4e-2
+
+
+def check_bf16_end_to_end(got_bits: np.ndarray, want_bits: np.ndarray, what: str = "output",
+                          rms_frac: float = RMS_FRAC):
+    """End-to-end rule: per-element max bound as in check_bf16_close (with
+    rms_frac, RMS_FRAC_E4M3 for the E4M3 family), and the 2-ulp fraction at
+    least the attached floor less floor_margin.  Returns the fraction."""
     floor = getattr(want_bits, "floor", None)
     assert floor is not None, f"{what}: end-to-end check without an accumulation-model floor"
     got = bf16_to_f64(got_bits)
@@ -120,10 +131,10 @@ def check_bf16_end_to_end(got_bits: np.ndarray, want_bits: np.ndarray, what: str
         return 1.0
     assert np.all(np.isfinite(got)), f"{what}: non-finite values"
     rms = float(np.sqrt(np.mean(want * want)))
-    excess = np.abs(got - want) - bf16_ulp_of(want_bits) - RMS_FRAC * rms
+    excess = np.abs(got - want) - bf16_ulp_of(want_bits) - rms_frac * rms
     worst = int(np.argmax(excess))
     assert excess.flat[worst] <= 0, (f"{what}: |diff| {abs(got.flat[worst] - want.flat[worst])} at "
-                                     f"{want.flat[worst]} exceeds 1e-2*rms ({RMS_FRAC * rms}) + 1 ulp")
+                                     f"{want.flat[worst]} exceeds {rms_frac}*rms ({rms_frac * rms}) + 1 ulp")
     frac = float(np.mean(ulp_distance(got_bits, want_bits) <= ULP_MAX))
     f_model, n_model = floor
     need = f_model - floor_margin(f_model, n_model)
