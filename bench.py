@@ -362,7 +362,7 @@ def run_ours(args, world, rank, local):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     opts = dict(decode_chain=True if args.decode_chain else (False if args.decode_separate else None),
                 one_cta_gemm=args.one_cta_gemm, fused_gather=args.fused_gather,
-                decode_one_launch=args.decode_one_launch)
+                decode_one_launch=args.decode_one_launch, no_tail_tiles=args.no_tail_tiles)
     # one plan per copy of the expert banks; the steps rotate over them
     banks = weight_banks(wl)
     fw = None
@@ -586,12 +586,12 @@ def run_grouped_gemm(args, world, rank, local):
     side.wait_stream(stream)
     with torch.cuda.stream(side):
         for _ in range(3):
-            moe.grouped_gemm_fwd(X, Wt, offs, Y)
+            moe.grouped_gemm_fwd(X, Wt, offs, Y, no_tail_tiles=args.no_tail_tiles)
     stream.wait_stream(side)
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
-        moe.grouped_gemm_fwd(X, Wt, offs, Y)
+        moe.grouped_gemm_fwd(X, Wt, offs, Y, no_tail_tiles=args.no_tail_tiles)
     clocks = ClockSampler(str(local))
     time.sleep(0.3)
     for _ in range(args.warmup):
@@ -614,13 +614,13 @@ def run_grouped_gemm(args, world, rank, local):
     Y_h = torch.empty(Y.shape, dtype=Y.dtype).pin_memory()
     for _ in range(args.warmup):
         X.copy_(X_h, non_blocking=True)
-        moe.grouped_gemm_fwd(X, Wt, offs, Y)
+        moe.grouped_gemm_fwd(X, Wt, offs, Y, no_tail_tiles=args.no_tail_tiles)
         Y_h.copy_(Y, non_blocking=True)
     torch.cuda.synchronize()
     e0.record(stream)
     for _ in range(args.steps):
         X.copy_(X_h, non_blocking=True)
-        moe.grouped_gemm_fwd(X, Wt, offs, Y)
+        moe.grouped_gemm_fwd(X, Wt, offs, Y, no_tail_tiles=args.no_tail_tiles)
         Y_h.copy_(Y, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -860,6 +860,8 @@ def main():
                     help="with --shape: per-expert logit bias ln p_e, p_e ~ rank^-s (imbalanced groups)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e4m3", action="store_true", help="the fp8 per-tensor weight family (E4M3 weights)")
+    ap.add_argument("--no-tail-tiles", action="store_true",
+                    help="CTA-pair GEMMs: remainders as main tiles instead of swap-AB tail tiles")
     ap.add_argument("--no-graph", action="store_true", help="launch the plan directly instead of a CUDA graph")
     ap.add_argument("--decode-chain", action="store_true", help="decode path: always the two-kernel chain")
     ap.add_argument("--decode-one-launch", action="store_true",

@@ -256,6 +256,10 @@ MOE_API int moe_finalize(const float *y, const int32_t *exp_to_perm,
  * N % 64 == 0, K % 64 == 0, 1 <= E <= MOE_MAX_EXPERTS, offs[E-1] <= sum_m. */
 MOE_API int grouped_gemm_fwd(const moe_bf16 *X, const moe_bf16 *W, const int32_t *offs,
                      int sum_m, int E, int N, int K, moe_bf16 *Y, void *stream);
+/* The same with plan flags; MOE_PLAN_NO_TAIL_TILES is the only one it reads. */
+MOE_API int grouped_gemm_fwd_flags(const moe_bf16 *X, const moe_bf16 *W, const int32_t *offs,
+                                   int sum_m, int E, int N, int K, moe_bf16 *Y, int flags,
+                                   void *stream);
 
 /* ---- ragged grouped GEMM backward ---------------------------------------------------------
  * The dgrad and wgrad rows of Cake ragged BF16 grouped GEMM, operation table
@@ -300,14 +304,21 @@ MOE_API int grouped_gemm_wgrad(const moe_bf16 *G, const moe_bf16 *X, const int32
  *   bf16; y_accum [T, ld_y] fp32, ld_y >= sum feat_out (it may be a column
  *   slice of a wider row-major buffer).
  *   contiguous_top_k = k > 0 (k <= MOE_MAX_TOP_K): the pairs are token-major,
- *   pair p of token p / k (num_pairs == T * k), no index is built; 0: any
- *   order (e.g. sorted by expert), through a route index in the workspace of
- *   moe_bgmv_workspace_size(T, num_pairs, 0) bytes (zero bytes for k > 0).
+ *   pair p of token p / k (num_pairs == T * k); 0: any order (e.g. sorted by
+ *   expert), through a per-token route index.
+ *   While num_loras * E <= 2048 the pairs are grouped by (LoRA, expert) with
+ *   the routes' stable counting sort, so each A and B block is read once per
+ *   group; the expand writes fp32 per-pair partials that one owner per token
+ *   adds in ascending pair order (the page's pair-grouped pipeline).  Larger
+ *   products run one CTA per pair (shrink) and one per token (expand).
+ *   workspace: moe_bgmv_workspace_size(T, num_pairs, contiguous_top_k,
+ *   num_loras, E, sum feat_out) bytes (route index, grouping, partials).
  *   A pair whose token, expert or LoRA index is out of range (or, with
  *   contiguous_top_k, whose token is not p / k) contributes nothing and raises
  *   MOE_DEV_BAD_EXPERT in *status (cleared first; optional).
  * No allocation, no host synchronisation: capturable in a CUDA graph. */
-MOE_API size_t moe_bgmv_workspace_size(int T, int num_pairs, int contiguous_top_k);
+MOE_API size_t moe_bgmv_workspace_size(int T, int num_pairs, int contiguous_top_k, int num_loras,
+                                       int E, int total_feat_out);
 MOE_API int moe_bgmv(const moe_bf16 *x, int T, int H, const moe_bf16 *const *lora_a,
                      const moe_bf16 *const *lora_b, int num_slices, const int *feat_out, int rank,
                      int num_loras, int E, const int32_t *sorted_token_ids,
@@ -374,6 +385,11 @@ MOE_API int moe_forward(const moe_bf16 *x, const float *logits, const int32_t *t
                                          per SM; if other work holds SMs for longer
                                          than the wait limit, the launch reports
                                          MOE_DEV_TIMEOUT in the status word. */
+#define MOE_PLAN_NO_TAIL_TILES 128 /* CTA-pair GEMMs: a group's last rows run as a
+                                     main tile (256 token rows, the rows past the
+                                     group computed and not stored) instead of a
+                                     swap-AB tail tile (weights on the MMA's M
+                                     side, the group's rows on N) */
 #define MOE_PLAN_TEST_UNREACHABLE_WAIT 64 /* test hook, not for production: the
                                              decode chain in one launch seeds its
                                              per-expert counts of finished FC1 tiles

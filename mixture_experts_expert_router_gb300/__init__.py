@@ -40,6 +40,7 @@ PLAN_DECODE_SEPARATE = 8
 PLAN_FUSED_GATHER = 16
 PLAN_DECODE_ONE_LAUNCH = 32
 PLAN_TEST_UNREACHABLE_WAIT = 64
+PLAN_NO_TAIL_TILES = 128
 WEIGHTS_BF16, WEIGHTS_E4M3 = 0, 1
 WAIT_LIMIT_MIN_NS, WAIT_LIMIT_MAX_NS = 1000, 600_000_000_000
 DEV_BAD_EXPERT, DEV_TIMEOUT = 1, 2
@@ -54,7 +55,7 @@ ABI_SYMBOLS = [
     "moe_plan_stage_reset", "moe_plan_kernels_per_launch", "moe_plan_destroy", "moe_sort_no_alloc",
     "moe_fc1_swiglu_swapab", "moe_fc2_swapab", "moe_fc1_swiglu_gathered", "moe_plan_set_wait_limit",
     "moe_fc1_swiglu_step", "grouped_gemm_dgrad", "grouped_gemm_wgrad", "moe_bgmv_workspace_size", "moe_bgmv",
-    "moe_fc1_swiglu_e4m3", "moe_fc2_e4m3",
+    "moe_fc1_swiglu_e4m3", "moe_fc2_e4m3", "grouped_gemm_fwd_flags",
 ]
 
 
@@ -119,8 +120,9 @@ def library():
             "moe_fc2_swapab": ([P, P, P, I, I, I, I, I, P, P], I),
             "moe_finalize": ([P, P, P, I, I, I, P, P], I),
             "grouped_gemm_fwd": ([P, P, P, I, I, I, I, P, P], I),
+            "grouped_gemm_fwd_flags": ([P, P, P, I, I, I, I, P, I, P], I),
             "grouped_gemm_dgrad": ([P, P, P, I, I, I, I, P, P], I),
-            "moe_bgmv_workspace_size": ([I, I, I], Z),
+            "moe_bgmv_workspace_size": ([I, I, I, I, I, I], Z),
             "moe_bgmv": ([P, I, I, P, P, I, P, I, I, I, P, P, P, P, I, I, P, P, I, P, Z, P, P], I),
             "grouped_gemm_wgrad": ([P, P, P, I, I, I, I, P, I, P], I),
             "moe_workspace_size": ([I, I, I, I, I, I], Z),
@@ -388,7 +390,7 @@ def moe_finalize(y: torch.Tensor, exp_to_perm: torch.Tensor, topk_w: torch.Tenso
     return out
 
 
-def grouped_gemm_fwd(X: torch.Tensor, W: torch.Tensor, offs: torch.Tensor, Y=None):
+def grouped_gemm_fwd(X: torch.Tensor, W: torch.Tensor, offs: torch.Tensor, Y=None, no_tail_tiles: bool = False):
     """Ragged grouped GEMM forward: Y[group e] = X[group e] @ W[e].T (bf16)."""
     _need(X, torch.bfloat16, "X")
     _need(W, torch.bfloat16, "W")
@@ -399,8 +401,9 @@ def grouped_gemm_fwd(X: torch.Tensor, W: torch.Tensor, offs: torch.Tensor, Y=Non
         raise ValueError("shapes: X [sum_m, K], W [E, N, K], offs [E]")
     Y = torch.empty((sum_m, N), dtype=torch.bfloat16, device=X.device) if Y is None else Y
     _need(Y, torch.bfloat16, "Y", (sum_m, N), X.device)
-    _check(library().grouped_gemm_fwd(_ptr(X), _ptr(W), _ptr(offs), sum_m, E, N, K, _ptr(Y),
-                                      _stream(X.device)), "grouped_gemm_fwd")
+    _check(library().grouped_gemm_fwd_flags(_ptr(X), _ptr(W), _ptr(offs), sum_m, E, N, K, _ptr(Y),
+                                            PLAN_NO_TAIL_TILES if no_tail_tiles else 0, _stream(X.device)),
+           "grouped_gemm_fwd")
     return Y
 
 
@@ -472,7 +475,7 @@ def bgmv(x, lora_a, lora_b, sorted_token_ids, expert_ids, lora_indices, topk_wei
         y_accum = torch.empty((T, sum(F)), dtype=torch.float32, device=dev)
     if y_accum.dtype != torch.float32 or not y_accum.is_cuda or y_accum.shape[0] != T or y_accum.stride(1) != 1:
         raise ValueError("y_accum must be a CUDA fp32 [T, >= sum(feat_out)] tensor with unit column stride")
-    need = int(library().moe_bgmv_workspace_size(T, P, contiguous_top_k))
+    need = int(library().moe_bgmv_workspace_size(T, P, contiguous_top_k, L, E, sum(F)))
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
     if status is None:
@@ -542,7 +545,7 @@ class MoEPlan:
                  local_offset: int = 0, out=None, workspace=None, status=None, path: int = PATH_AUTO,
                  stage_timing: bool = False, one_cta_gemm: bool = False, decode_chain: bool | None = None,
                  fused_gather: bool = False, decode_one_launch: bool = False,
-                 test_unreachable_wait: bool = False, clamp_limit=None, e4m3=None):
+                 test_unreachable_wait: bool = False, clamp_limit=None, e4m3=None, no_tail_tiles: bool = False):
         """decode_chain: None lets the library choose the decode form (the
         chain in one launch for few routes, else five kernels), True forces
         the chain as two kernels, False the five separate kernels.
@@ -585,7 +588,8 @@ class MoEPlan:
                   | (PLAN_DECODE_SEPARATE if decode_chain is False else 0)
                   | (PLAN_FUSED_GATHER if fused_gather else 0)
                   | (PLAN_DECODE_ONE_LAUNCH if decode_one_launch else 0)
-                  | (PLAN_TEST_UNREACHABLE_WAIT if test_unreachable_wait else 0),
+                  | (PLAN_TEST_UNREACHABLE_WAIT if test_unreachable_wait else 0)
+                  | (PLAN_NO_TAIL_TILES if no_tail_tiles else 0),
                   clamp_limit=_ptr(clamp_limit), **q)
         handle = ctypes.c_void_p()
         _check(library().moe_forward_prepare(ctypes.byref(d), ctypes.byref(handle)), "moe_forward_prepare")

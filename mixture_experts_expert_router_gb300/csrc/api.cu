@@ -133,7 +133,7 @@ const char *moe_status_string(int code) {
   }
 }
 
-int moe_abi_version(void) { return 102; }
+int moe_abi_version(void) { return 103; }
 
 int moe_route(const float *logits, int T, int E, int top_k, int32_t *topk_ids, float *topk_w,
               void *stream) {
@@ -376,8 +376,8 @@ int moe_finalize(const float *y, const int32_t *exp_to_perm, const float *topk_w
   return cuda_rc(launch_finalize(y, exp_to_perm, topk_w, T, top_k, H, out, l));
 }
 
-int grouped_gemm_fwd(const moe_bf16 *X, const moe_bf16 *W, const int32_t *offs, int sum_m, int E,
-                     int N, int K, moe_bf16 *Y, void *stream) {
+int grouped_gemm_fwd_flags(const moe_bf16 *X, const moe_bf16 *W, const int32_t *offs, int sum_m, int E,
+                           int N, int K, moe_bf16 *Y, int flags, void *stream) {
   if (sum_m < 0 || E < 1 || E > MOE_MAX_EXPERTS || N <= 0 || K <= 0 || N % 64 || K % 64)
     return MOE_ERR_SHAPE;
   if (sum_m == 0) return MOE_OK;
@@ -387,9 +387,15 @@ int grouped_gemm_fwd(const moe_bf16 *X, const moe_bf16 *W, const int32_t *offs, 
   GemmPlan p;
   if (int rc = gemm_prepare(p, Epi::kBf16, X, sum_m, W, E, N, K, N, offs, sum_m, Y, nullptr))
     return rc;
+  if (flags & MOE_PLAN_NO_TAIL_TILES) p.tail_max = 0;
   Launch l;
   l.stream = static_cast<cudaStream_t>(stream);
   return cuda_rc(launch_gemm(p, l));
+}
+
+int grouped_gemm_fwd(const moe_bf16 *X, const moe_bf16 *W, const int32_t *offs, int sum_m, int E, int N,
+                     int K, moe_bf16 *Y, void *stream) {
+  return grouped_gemm_fwd_flags(X, W, offs, sum_m, E, N, K, Y, 0, stream);
 }
 
 int grouped_gemm_dgrad(const moe_bf16 *G, const moe_bf16 *W, const int32_t *offs, int sum_m, int E,
@@ -426,10 +432,10 @@ int grouped_gemm_wgrad(const moe_bf16 *G, const moe_bf16 *X, const int32_t *offs
   return cuda_rc(launch_bwd(p, l));
 }
 
-size_t moe_bgmv_workspace_size(int T, int num_pairs, int contiguous_top_k) {
-  (void)num_pairs;
-  if (T < 0 || contiguous_top_k < 0) return 0;
-  return bgmv_workspace_bytes(T, contiguous_top_k);
+size_t moe_bgmv_workspace_size(int T, int num_pairs, int contiguous_top_k, int num_loras, int E,
+                               int total_feat_out) {
+  if (T < 0 || num_pairs < 0 || contiguous_top_k < 0 || num_loras < 1 || E < 1 || total_feat_out < 0) return 0;
+  return bgmv_workspace_bytes(T, num_pairs, contiguous_top_k, num_loras, E, total_feat_out);
 }
 
 int moe_bgmv(const moe_bf16 *x, int T, int H, const moe_bf16 *const *lora_a,
@@ -459,7 +465,7 @@ int moe_bgmv(const moe_bf16 *x, int T, int H, const moe_bf16 *const *lora_a,
     if (!aligned16(lora_a[s]) || !aligned16(lora_b[s])) return MOE_ERR_ALIGN;
   }
   if (!aligned16(x)) return MOE_ERR_ALIGN;
-  const size_t need = bgmv_workspace_bytes(T, contiguous_top_k);
+  const size_t need = bgmv_workspace_bytes(T, num_pairs, contiguous_top_k, num_loras, E, (int)cols);
   if (need > 0 && (!workspace || workspace_bytes < need)) return MOE_ERR_WORKSPACE;
   if (int rc = check_device()) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -627,6 +633,7 @@ int moe_forward_prepare(const moe_forward_desc *desc, moe_plan **plan_out) {
       if (rc == MOE_OK)
         rc = gemm_prepare(p->fc2, Epi::kF32, p->h, p->R, d.w2, d.num_local, d.H, d.I, d.H,
                           p->m_indptr + 1, p->R, p->y, d.status, pair);
+      if (d.flags & MOE_PLAN_NO_TAIL_TILES) p->fc1.tail_max = p->fc2.tail_max = 0;
     }
     if (rc != MOE_OK) {
       delete p;

@@ -17,6 +17,30 @@
 //           columns f and adding w_p * (B row f . shrink) in pair order, so
 //           every replay is bitwise identical and nothing uses atomics.
 //
+// Two pipelines compute exactly this.  The pair-grouped one (the default
+// while num_loras * E <= kBgmvMaxGroups) sorts the pairs by (LoRA, expert)
+// with the stable counting sort of the routes (sort.cu), so each A and B block
+// is read once per group instead of once per pair:
+//   key      key[p] = lora[t] * E + e (negative for an invalid pair, whose
+//            shrink rows are zeroed);
+//   gshrink  one CTA per (group, slice): tiles of 16 pairs times the group's
+//            A block, H staged through shared memory 256 columns at a time
+//            (cp.async, double-buffered) into m16n8k16 tensor-core MMAs with
+//            fp32 accumulators, the eight warps' k-step sums added in warp
+//            order;
+//   gexpand  one CTA per (group, 256 output columns of a slice): the columns'
+//            B rows staged once, tiles of 16 pairs' shrink values times them
+//            (m16n8k16 MMAs, K = R), writing the fp32 partial
+//            w_p * (B row . shrink_p) of every pair of the group;
+// Per group the contraction is 16 or so pairs by R <= 64, far below the 64- and
+// 128-row tiles of the single-thread-issued MMA, so the warp-level m16n8k16
+// shape serves it; both kernels stay bound by the A and B bytes.
+//   combine  one CTA per token adds its pairs' partials in ascending pair
+//            index (the owner rule), so the output does not depend on the
+//            grouping.
+// The per-route pipeline below (one CTA per pair for the shrink, one per
+// token for the expand) serves more (LoRA, expert) pairs than that.
+//
 // Pair layouts: "contiguous top-k" (pair p belongs to token p / k, the layout
 // the page's fast path serves) needs no index.  Any other order (for example
 // pairs sorted by expert) goes through a route index built by one kernel: up
@@ -36,6 +60,9 @@ constexpr int kShrinkThreads = 256;
 constexpr int kExpandThreads = 256;
 constexpr int kSlots = 16;
 
+struct BgmvArgs;
+__device__ __forceinline__ bool pair_ok(const BgmvArgs &a, int p);
+
 struct BgmvArgs {
   const uint16_t *x;
   const uint16_t *a[kBgmvMaxSlices];
@@ -49,6 +76,12 @@ struct BgmvArgs {
   int32_t *cnt;      // general layout: [T] pairs per token
   int32_t *idx;      // general layout: [T, kSlots] pair numbers
   int32_t *status;
+  // grouped pipeline
+  int32_t *keys;            // [P]
+  const int32_t *g_indptr;  // [G + 1] pair rows of each (LoRA, expert) group
+  const int32_t *g_pairs;   // [P] pair numbers in group order, ascending inside a group
+  float *partial;           // [P, ld_part] fp32 w_p * (B row . shrink_p)
+  int ld_part;              // sum of feat_out
   int T, H, R, S, L, E, P, k, ld_y;
 };
 
@@ -207,10 +240,332 @@ __global__ void __launch_bounds__(kExpandThreads) bgmv_expand_kernel(const __gri
   pdl_launch_dependents();
 }
 
+// ------------------------------------------------------------ grouped pipeline --
+constexpr int kGroupTile = 16;  // pairs per tile: the M of the m16n8k16 tensor-core MMA
+
+__global__ void __launch_bounds__(256) bgmv_key_kernel(const __grid_constant__ BgmvArgs a) {
+  pdl_wait();
+  const int p = blockIdx.x * blockDim.x + threadIdx.x;
+  if (p < a.P) {
+    const bool ok = pair_ok(a, p);
+    a.keys[p] = ok ? a.lora[a.tok[p]] * a.E + a.eid[p] : -1;  // the sort flags and drops -1
+    if (!ok)
+      for (int s = 0; s < a.S; ++s)
+        for (int r = 0; r < a.R; ++r) a.shrink[((long)s * a.P + p) * a.R + r] = 0;
+  }
+  pdl_launch_dependents();
+}
+
+// Shared-memory row pitch of the staged bf16 operands: a multiple of 16 bytes
+// whose word stride is 4 mod 32, so the eight rows and four column pairs of an
+// m16n8k16 fragment load fall in 32 distinct banks.
+constexpr int kKC = 256;        // x / A columns per shrink stage
+constexpr int kKP = kKC + 8;    // pitch (bf16) of a staged row
+
+template <int R>
+struct GShrinkSmem {
+  // ring depth: two CTAs per SM up to rank 32
+  static constexpr int NST = R <= 32 ? 4 : 3;
+  static constexpr int STAGE = (R + kGroupTile) * kKP;  // bf16: A rows, then the tile's x rows
+  static constexpr size_t RING_BYTES = (size_t)NST * STAGE * 2;
+  // the eight warps' sums [8][16][R] fp32 reuse the ring once a tile's k-loop is over
+  static_assert((size_t)8 * kGroupTile * R * 4 <= RING_BYTES, "the warp sums fit in the ring");
+  static constexpr size_t TOK_OFF = RING_BYTES;
+  static constexpr size_t BYTES = TOK_OFF + kGroupTile * 4;
+};
+
+__device__ __forceinline__ uint32_t lds32(const uint16_t *p) { return *reinterpret_cast<const uint32_t *>(p); }
+
+// One CTA per (group, slice): the group's pairs in tiles of 16 (the MMA's M),
+// its A block [R, H] on N, H on K.  Each stage copies kKC columns of A and of
+// the tile's x rows into shared memory (cp.async, a ring of NST stages with
+// NST - 1 in flight); warp w takes the k-steps w, w + 8, .. of every stage into
+// its own accumulators, and the eight warps' sums are added in warp order at
+// the end of the tile.
+template <int R>
+__global__ void __launch_bounds__(256) bgmv_gshrink_kernel(const __grid_constant__ BgmvArgs a) {
+  using SM = GShrinkSmem<R>;
+  extern __shared__ __align__(16) unsigned char gs_smem[];
+  uint16_t *stage = reinterpret_cast<uint16_t *>(gs_smem);
+  float *red = reinterpret_cast<float *>(gs_smem);  // [8 warps][16 pairs][R], over the ring
+  int *tp = reinterpret_cast<int *>(gs_smem + SM::TOK_OFF);       // token of each pair of the tile
+  pdl_wait();
+  const int g = blockIdx.x, s = blockIdx.y;
+  const int p0 = a.g_indptr[g], p1 = a.g_indptr[g + 1];
+  if (p1 > p0) {
+    const int l = g / a.E, e = g - l * a.E;
+    const uint16_t *A = a.a[s] + ((long)l * a.E + e) * R * a.H;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gq = lane >> 2, c2 = 2 * (lane & 3);
+    const int nch = (a.H + kKC - 1) / kKC;
+    const uint64_t pol_a = policy_evict_first();  // each A element is read by one tile of one CTA
+    const uint64_t pol_x = policy_evict_normal();
+    for (int q0 = p0; q0 < p1; q0 += kGroupTile) {
+      const int n = p1 - q0 < kGroupTile ? p1 - q0 : kGroupTile;
+      __syncthreads();  // the previous tile no longer reads tp, red or the stages
+      if (threadIdx.x < kGroupTile) tp[threadIdx.x] = (int)threadIdx.x < n ? a.tok[a.g_pairs[q0 + threadIdx.x]] : -1;
+      __syncthreads();
+      auto load = [&](int ch) {
+        uint16_t *st = stage + (ch % SM::NST) * SM::STAGE;
+        const int h0 = ch * kKC, hn = a.H - h0 < kKC ? a.H - h0 : kKC;  // hn % 8 == 0
+        for (int i = threadIdx.x; i < (R + kGroupTile) * (kKC / 8); i += 256) {
+          const int row = i / (kKC / 8), v = i - row * (kKC / 8);
+          uint16_t *dst = st + row * kKP + 8 * v;
+          const uint16_t *src = nullptr;
+          if (8 * v < hn) {
+            if (row < R) src = A + (long)row * a.H + h0 + 8 * v;
+            else if (tp[row - R] >= 0) src = a.x + (long)tp[row - R] * a.H + h0 + 8 * v;
+          }
+          if (src) cp_async_16(smem_u32(dst), src, row < R ? pol_a : pol_x);
+          else *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        cp_async_commit();
+      };
+      float d[R / 8][4];
+#pragma unroll
+      for (int nt = 0; nt < R / 8; ++nt) d[nt][0] = d[nt][1] = d[nt][2] = d[nt][3] = 0.f;
+      // one commit group per chunk (empty past the end), so that waiting for
+      // all but the NST - 1 newest groups means chunk ch has landed
+      for (int i = 0; i < SM::NST - 1; ++i) {
+        if (i < nch) load(i);
+        else cp_async_commit();
+      }
+      for (int ch = 0; ch < nch; ++ch) {
+        // chunk ch + NST - 1 into the stage that chunk ch - 1 used, freed by
+        // the barrier that ended ch - 1
+        if (ch + SM::NST - 1 < nch) load(ch + SM::NST - 1);
+        else cp_async_commit();
+        cp_async_wait_pending<SM::NST - 1>();
+        __syncthreads();  // stage ch has landed for every thread
+        const uint16_t *As = stage + (ch % SM::NST) * SM::STAGE, *xs = As + R * kKP;
+        const int hn = a.H - ch * kKC < kKC ? a.H - ch * kKC : kKC;
+        for (int ks = warp; ks < (hn + 15) / 16; ks += 8) {
+          const int c = ks * 16 + c2;
+          const uint32_t a0 = lds32(xs + gq * kKP + c), a1 = lds32(xs + (gq + 8) * kKP + c);
+          const uint32_t a2 = lds32(xs + gq * kKP + c + 8), a3 = lds32(xs + (gq + 8) * kKP + c + 8);
+#pragma unroll
+          for (int nt = 0; nt < R / 8; ++nt) {
+            const uint16_t *br = As + (nt * 8 + gq) * kKP + c;
+            mma_bf16_16816(d[nt], a0, a1, a2, a3, lds32(br), lds32(br + 8));
+          }
+        }
+        __syncthreads();  // stage ch may be overwritten (by chunk ch + NST)
+      }
+      cp_async_wait_all();  // the empty trailing groups
+#pragma unroll
+      for (int nt = 0; nt < R / 8; ++nt) {
+        float *r0 = red + (warp * kGroupTile + gq) * R + nt * 8 + c2;
+        r0[0] = d[nt][0];
+        r0[1] = d[nt][1];
+        r0[8 * R] = d[nt][2];
+        r0[8 * R + 1] = d[nt][3];
+      }
+      __syncthreads();
+      for (int o = threadIdx.x; o < n * R; o += 256) {
+        const int row = o / R, col = o - row * R;
+        float v = red[row * R + col];
+#pragma unroll
+        for (int w = 1; w < 8; ++w) v = __fadd_rn(v, red[(w * kGroupTile + row) * R + col]);
+        a.shrink[((long)s * a.P + a.g_pairs[q0 + row]) * R + col] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+      }
+    }
+  }
+  pdl_launch_dependents();
+}
+
+// One CTA per (group, 256 output columns of a slice): the group's pairs in
+// tiles of 16 (M), the columns' B rows [256, R] on N (staged once), R on K
+// (zero-padded to 16).  Each warp owns 32 columns (four n-tiles) and writes
+// w_p * (B row . shrink_p) of every pair of the tile.
+template <int R>
+__global__ void __launch_bounds__(256) bgmv_gexpand_kernel(const __grid_constant__ BgmvArgs a) {
+  constexpr int RK = R < 16 ? 16 : R, RP = RK + 8;  // K and the row pitch (bf16)
+  __shared__ __align__(16) uint16_t bs[256 * RP];
+  __shared__ __align__(16) uint16_t sh[kGroupTile * RP];
+  __shared__ float sw[kGroupTile];
+  __shared__ int sp[kGroupTile];
+  pdl_wait();
+  const int g = blockIdx.x;
+  const int p0 = a.g_indptr[g], p1 = a.g_indptr[g + 1];
+  if (p1 > p0) {
+    int s = 0, c = blockIdx.y;
+    while (s < a.S && c >= (a.f[s] + 255) / 256) c -= (a.f[s++] + 255) / 256;
+    const int F = a.f[s], f0 = c * 256, fn = F - f0 < 256 ? F - f0 : 256;  // fn % 8 == 0
+    const int l = g / a.E, e = g - l * a.E;
+    const uint16_t *B = a.b[s] + (((long)l * a.E + e) * F + f0) * R;
+    const uint64_t pol_b = policy_evict_first();
+    for (int i = threadIdx.x; i < 256 * (RK / 8); i += 256) {
+      const int row = i / (RK / 8), v = i - row * (RK / 8);
+      uint16_t *dst = bs + row * RP + 8 * v;
+      if (row < fn && 8 * v < R) cp_async_16(smem_u32(dst), B + (long)row * R + 8 * v, pol_b);
+      else *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    cp_async_commit();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gq = lane >> 2, c2 = 2 * (lane & 3);
+    const uint16_t *shr = a.shrink + (long)s * a.P * R;
+    float *part = a.partial + a.off[s] + f0;
+    for (int q0 = p0; q0 < p1; q0 += kGroupTile) {
+      const int n = p1 - q0 < kGroupTile ? p1 - q0 : kGroupTile;
+      __syncthreads();  // the previous tile no longer reads sh, sw, sp
+      for (int i = threadIdx.x; i < kGroupTile * RK; i += 256) {
+        const int pr = i / RK, rr = i - pr * RK;
+        sh[pr * RP + rr] = pr < n && rr < R ? shr[(long)a.g_pairs[q0 + pr] * R + rr] : (uint16_t)0;
+      }
+      if (threadIdx.x < kGroupTile) {
+        const int pr = threadIdx.x;
+        sp[pr] = pr < n ? a.g_pairs[q0 + pr] : 0;
+        sw[pr] = pr < n ? a.w[sp[pr]] : 0.f;
+      }
+      cp_async_wait_all();
+      __syncthreads();
+      uint32_t af[RK / 16][4];
+#pragma unroll
+      for (int ks = 0; ks < RK / 16; ++ks) {
+        const int cc = ks * 16 + c2;
+        af[ks][0] = lds32(sh + gq * RP + cc);
+        af[ks][1] = lds32(sh + (gq + 8) * RP + cc);
+        af[ks][2] = lds32(sh + gq * RP + cc + 8);
+        af[ks][3] = lds32(sh + (gq + 8) * RP + cc + 8);
+      }
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        const int n0 = warp * 32 + nt * 8;
+        if (n0 >= fn) break;
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < RK / 16; ++ks) {
+          const uint16_t *br = bs + (n0 + gq) * RP + ks * 16 + c2;
+          mma_bf16_16816(d, af[ks][0], af[ks][1], af[ks][2], af[ks][3], lds32(br), lds32(br + 8));
+        }
+        if (gq < n)
+          *reinterpret_cast<float2 *>(part + (long)sp[gq] * a.ld_part + n0 + c2) =
+              make_float2(__fmul_rn(sw[gq], d[0]), __fmul_rn(sw[gq], d[1]));
+        if (gq + 8 < n)
+          *reinterpret_cast<float2 *>(part + (long)sp[gq + 8] * a.ld_part + n0 + c2) =
+              make_float2(__fmul_rn(sw[gq + 8], d[2]), __fmul_rn(sw[gq + 8], d[3]));
+      }
+    }
+  }
+  pdl_launch_dependents();
+}
+
+// y[t] = sum of the partials of t's pairs in ascending pair index.  Token-major
+// pairs are checked one per lane of the first warp; the columns go four at a
+// time (the partial rows are 16-byte aligned: sum feat_out % 8 == 0).
+__global__ void __launch_bounds__(256) bgmv_combine_kernel(const __grid_constant__ BgmvArgs a) {
+  __shared__ int pairs[kSlots];
+  __shared__ int n_pairs;
+  pdl_wait();
+  const int t = blockIdx.x;
+  if (a.k > 0) {
+    if (threadIdx.x < 32) {  // k <= MOE_MAX_TOP_K == kSlots <= 32
+      const int lane = threadIdx.x, p = t * a.k + lane;
+      bool mine = false, mismatch = false;
+      if (lane < a.k && p < a.P) {
+        if (a.tok[p] != t) mismatch = true;
+        else mine = pair_ok(a, p);
+      }
+      const unsigned m = __ballot_sync(0xffffffffu, mine);
+      if (mine) pairs[__popc(m & ((1u << lane) - 1u))] = p;
+      if (__any_sync(0xffffffffu, mismatch) && lane == 0 && a.status)
+        atomicOr(reinterpret_cast<unsigned int *>(a.status), MOE_DEV_BAD_EXPERT);
+      if (lane == 0) n_pairs = __popc(m);
+    }
+  } else if (threadIdx.x == 0) {
+    int n = a.cnt[t];
+    if (n <= kSlots) {
+      for (int i = 0; i < n; ++i) pairs[i] = a.idx[(long)t * kSlots + i];
+      for (int i = 1; i < n; ++i) {
+        const int v = pairs[i];
+        int j = i - 1;
+        while (j >= 0 && pairs[j] > v) {
+          pairs[j + 1] = pairs[j];
+          --j;
+        }
+        pairs[j + 1] = v;
+      }
+    } else {
+      n = -1;  // more pairs than slots: walk all pairs in order
+    }
+    n_pairs = n;
+  }
+  __syncthreads();
+  const int n = n_pairs;
+  float *yrow = a.y + (long)t * a.ld_y;
+  const bool vec_y = ((reinterpret_cast<uintptr_t>(yrow)) & 15u) == 0;
+  for (int c = 4 * (int)threadIdx.x; c < a.ld_part; c += 4 * 256) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    auto add = [&](int p) {
+      const float4 v = __ldcs(reinterpret_cast<const float4 *>(a.partial + (long)p * a.ld_part + c));
+      acc.x = __fadd_rn(acc.x, v.x);
+      acc.y = __fadd_rn(acc.y, v.y);
+      acc.z = __fadd_rn(acc.z, v.z);
+      acc.w = __fadd_rn(acc.w, v.w);
+    };
+    if (n >= 0) {
+      for (int q = 0; q < n; ++q) add(pairs[q]);
+    } else {
+      for (int p = 0; p < a.P; ++p)
+        if (a.tok[p] == t && pair_ok(a, p)) add(p);
+    }
+    if (vec_y) {
+      *reinterpret_cast<float4 *>(yrow + c) = acc;
+    } else {
+      yrow[c] = acc.x;
+      yrow[c + 1] = acc.y;
+      yrow[c + 2] = acc.z;
+      yrow[c + 3] = acc.w;
+    }
+  }
+  pdl_launch_dependents();
+}
+
 }  // namespace
 
-size_t bgmv_workspace_bytes(int T, int contiguous_k) {
-  return contiguous_k > 0 ? 0 : (size_t)T * (kSlots + 1) * sizeof(int32_t);
+static size_t bgmv_align(size_t v) { return (v + 255) / 256 * 256; }
+
+template <int R>
+static cudaError_t launch_gshrink(int G, int S, const Launch &l, const BgmvArgs &a) {
+  constexpr size_t bytes = GShrinkSmem<R>::BYTES;
+  static const cudaError_t attr =
+      cudaFuncSetAttribute(bgmv_gshrink_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (attr != cudaSuccess) return attr;
+  return launch_kernel(bgmv_gshrink_kernel<R>, dim3(G, S), dim3(256), bytes, l, a);
+}
+
+// Workspace: [route index (general order)] [grouped pipeline: keys, group
+// offsets, pairs in group order, their inverse, the sort's table, partials].
+struct BgmvLayout {
+  size_t cnt, idx, keys, g_indptr, g_pairs, g_inv, sort_ws, partial, total;
+  bool grouped;
+};
+
+static BgmvLayout bgmv_layout(int T, int P, int k, int G, int total_f) {
+  BgmvLayout o{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += bgmv_align(bytes > 0 ? bytes : 1);
+    return at;
+  };
+  if (k == 0) {
+    o.cnt = take((size_t)T * 4);
+    o.idx = take((size_t)T * kSlots * 4);
+  }
+  o.grouped = G >= 1 && G <= kBgmvMaxGroups;
+  if (o.grouped) {
+    o.keys = take((size_t)P * 4);
+    o.g_indptr = take((size_t)(G + 1) * 4);
+    o.g_pairs = take((size_t)P * 4);
+    o.g_inv = take((size_t)P * 4);
+    o.sort_ws = take(sort_workspace_bytes(P, G));
+    o.partial = take((size_t)P * total_f * 4);
+  }
+  o.total = off;
+  return o;
+}
+
+size_t bgmv_workspace_bytes(int T, int P, int contiguous_k, int num_loras, int E, int total_f) {
+  return bgmv_layout(T, P, contiguous_k, num_loras * E, total_f).total;
 }
 
 cudaError_t launch_bgmv(const BgmvPlan &p, const Launch &l) {
@@ -228,9 +583,19 @@ cudaError_t launch_bgmv(const BgmvPlan &p, const Launch &l) {
   a.w = p.w;
   a.shrink = p.shrink;
   a.y = p.y;
-  a.cnt = p.ws;
-  a.idx = p.ws ? p.ws + p.T : nullptr;
+  const int G = p.L * p.E;
+  int total_f = 0;
+  for (int i = 0; i < p.S; ++i) total_f += p.f[i];
+  const BgmvLayout lay = bgmv_layout(p.T, p.P, p.k, G, total_f);
+  unsigned char *ws = reinterpret_cast<unsigned char *>(p.ws);
+  a.cnt = p.k == 0 ? reinterpret_cast<int32_t *>(ws + lay.cnt) : nullptr;
+  a.idx = p.k == 0 ? reinterpret_cast<int32_t *>(ws + lay.idx) : nullptr;
   a.status = p.status;
+  a.keys = lay.grouped ? reinterpret_cast<int32_t *>(ws + lay.keys) : nullptr;
+  a.g_indptr = lay.grouped ? reinterpret_cast<int32_t *>(ws + lay.g_indptr) : nullptr;
+  a.g_pairs = lay.grouped ? reinterpret_cast<int32_t *>(ws + lay.g_pairs) : nullptr;
+  a.partial = lay.grouped ? reinterpret_cast<float *>(ws + lay.partial) : nullptr;
+  a.ld_part = total_f;
   a.T = p.T;
   a.H = p.H;
   a.R = p.R;
@@ -244,13 +609,38 @@ cudaError_t launch_bgmv(const BgmvPlan &p, const Launch &l) {
   Launch first = l;  // the first kernel of the call waits for everything before it
   first.pdl = false;
   if (p.k == 0) {
-    e = cudaMemsetAsync(p.ws, 0, (size_t)p.T * sizeof(int32_t), l.stream);
+    e = cudaMemsetAsync(a.cnt, 0, (size_t)p.T * sizeof(int32_t), l.stream);
     if (e != cudaSuccess) return e;
     if (p.P > 0) {
       e = launch_kernel(bgmv_index_kernel, dim3((p.P + 255) / 256), dim3(256), 0, first, a);
       if (e != cudaSuccess) return e;
       first = l;
     }
+  }
+  if (lay.grouped && p.P > 0) {
+    e = launch_kernel(bgmv_key_kernel, dim3((p.P + 255) / 256), dim3(256), 0, first, a);
+    if (e != cudaSuccess) return e;
+    e = launch_sort(a.keys, p.P, G, 0, G, const_cast<int32_t *>(a.g_indptr), const_cast<int32_t *>(a.g_pairs),
+                    reinterpret_cast<int32_t *>(ws + lay.g_inv), reinterpret_cast<int32_t *>(ws + lay.sort_ws),
+                    p.status, l);
+    if (e != cudaSuccess) return e;
+    switch (p.R) {
+      case 8: e = launch_gshrink<8>(G, p.S, l, a); break;
+      case 16: e = launch_gshrink<16>(G, p.S, l, a); break;
+      case 32: e = launch_gshrink<32>(G, p.S, l, a); break;
+      default: e = launch_gshrink<64>(G, p.S, l, a); break;
+    }
+    if (e != cudaSuccess) return e;
+    int chunks = 0;
+    for (int i = 0; i < p.S; ++i) chunks += (p.f[i] + 255) / 256;
+    switch (p.R) {
+      case 8: e = launch_kernel(bgmv_gexpand_kernel<8>, dim3(G, chunks), dim3(256), 0, l, a); break;
+      case 16: e = launch_kernel(bgmv_gexpand_kernel<16>, dim3(G, chunks), dim3(256), 0, l, a); break;
+      case 32: e = launch_kernel(bgmv_gexpand_kernel<32>, dim3(G, chunks), dim3(256), 0, l, a); break;
+      default: e = launch_kernel(bgmv_gexpand_kernel<64>, dim3(G, chunks), dim3(256), 0, l, a); break;
+    }
+    if (e != cudaSuccess) return e;
+    return launch_kernel(bgmv_combine_kernel, dim3(p.T), dim3(256), 0, l, a);
   }
   if (p.P > 0) {
     e = launch_kernel(bgmv_shrink_kernel, dim3(p.P, p.S), dim3(kShrinkThreads), 0, first, a);

@@ -99,6 +99,7 @@ struct PairArgs {
   const float *clamp;         // SwiGLU epilogue: [groups] SwiGLUStep limits, or null
   long max_rows;
   int G, K, n_out, b_rows, n_tiles, m_major;
+  int tail_max;               // remainders of up to this many rows run as swap-AB tail tiles (0: none)
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -141,7 +142,7 @@ __device__ __forceinline__ int group_pairs(int cnt) { return cnt > 0 ? (cnt + 2 
 // evenly among the others was measured slower: their once-read weight
 // streams then evict the large groups' reused weight blocks from L2.)
 __device__ __forceinline__ PairTile decode_pair_tile(int t, const int *tile_start, const int *gend, int G,
-                                                     int n_tiles, int m_major) {
+                                                     int n_tiles, int m_major, int tail_max) {
   int lo = 0, hi = G;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -161,7 +162,7 @@ __device__ __forceinline__ PairTile decode_pair_tile(int t, const int *tile_star
   }
   c.gstart = lo == 0 ? 0 : gend[lo - 1];
   const int r = gend[lo] - c.gstart - c.mp * 2 * BM;  // rows from this tile's first row to the group's end
-  c.tail = (r > 0 && r <= kTailMax) ? r : 0;
+  c.tail = (r > 0 && r <= tail_max) ? r : 0;
   return c;
 }
 
@@ -309,7 +310,7 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : kThreads, 1)
         it += n_rounds;
         continue;
       }
-      const PairTile c = decode_pair_tile(t, tile_start, gend, G, args.n_tiles, args.m_major);
+      const PairTile c = decode_pair_tile(t, tile_start, gend, G, args.n_tiles, args.m_major, args.tail_max);
       const uint64_t pol = (c.tail && c.mp == 0) ? pol_first : pol_last;
       const PairOperands o = pair_operands<kSwiGLU>(c, rank, args.b_rows);
       const CUtensorMap *tok_map = c.tail ? &args.map_t[o.tmap] : &args.map_a;
@@ -346,7 +347,7 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : kThreads, 1)
       int it = 0;
       bool ok = true;
       for (int t = cluster; t < total && ok; t += nclusters) {
-        const PairTile c = decode_pair_tile(t, tile_start, gend, G, args.n_tiles, args.m_major);
+        const PairTile c = decode_pair_tile(t, tile_start, gend, G, args.n_tiles, args.m_major, args.tail_max);
         // L2: a group that is only this tail reads its weights once (stream them
         // through); everything else is read again by neighbouring tiles (keep it)
         const uint64_t pol = (c.tail && c.mp == 0) ? pol_first : pol_last;
@@ -381,7 +382,7 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : kThreads, 1)
       int it = 0, tc = 0;
       bool ok = true;
       for (int t = cluster; t < total && ok; t += nclusters, ++tc) {
-        const PairTile c = decode_pair_tile(t, tile_start, gend, G, args.n_tiles, args.m_major);
+        const PairTile c = decode_pair_tile(t, tile_start, gend, G, args.n_tiles, args.m_major, args.tail_max);
         const uint32_t idesc = c.tail ? idesc_bf16_f32(2 * BM, (uint32_t)tail_n(c.tail)) : IDESC_MAIN;
         const int acc = tc & 1;
         const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
@@ -420,7 +421,7 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : kThreads, 1)
     const uint32_t leader_tempty1 = mapa_shared(tempty_bar(1), 0);
     int tc = 0;
     for (int t = cluster; t < total; t += nclusters, ++tc) {
-      const PairTile c = decode_pair_tile(t, tile_start, gend, G, args.n_tiles, args.m_major);
+      const PairTile c = decode_pair_tile(t, tile_start, gend, G, args.n_tiles, args.m_major, args.tail_max);
       const int acc = tc & 1;
       const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
       const bool got = mbar_wait(tfull_bar(acc), aph, abort_flag, args.status, args.wait_ns);
@@ -593,7 +594,7 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : kThreads, 1)
     int it = 0;
     bool ok = true;
     for (int t = cluster; t < total && ok; t += nclusters) {
-      const PairTile c = decode_pair_tile(t, tile_start, gend, G, args.n_tiles, args.m_major);
+      const PairTile c = decode_pair_tile(t, tile_start, gend, G, args.n_tiles, args.m_major, args.tail_max);
       const PairOperands o = pair_operands<kSwiGLU>(c, rank, args.b_rows);
       const int r4 = o.tok_rows / 4;  // rows per lane: 2 .. 32
       int tok[32];
@@ -750,6 +751,7 @@ cudaError_t launch_pair_gemm(const GemmPlan &p, const Launch &l) {
   a.b_rows = p.b_rows;
   a.n_tiles = p.n_tiles;
   a.m_major = p.m_major;
+  a.tail_max = p.tail_max;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.grid);
   const bool gath = p.gather_k > 0 && p.epi == Epi::kSwiGLU;

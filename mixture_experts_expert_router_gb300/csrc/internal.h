@@ -89,6 +89,10 @@ struct GemmPlan {
   int q = 0;
   const float *wscale = nullptr;
   float ascale = 1.f, oscale = 1.f;
+  // CTA-pair kernel: a group's last rows up to this many run as swap-AB tail
+  // tiles (weights on the MMA's M side); 0 makes every remainder a main tile
+  // whose rows past the group are computed and not stored
+  int tail_max = 128;
 };
 
 // Encodes the tensor maps and picks tile shapes; host only.  allow_pair lets
@@ -138,6 +142,9 @@ cudaError_t launch_bwd(const BwdPlan &p, const Launch &l);
 
 // BGMV LoRA-MoE shrink + expand (bgmv.cu) ----------------------------------------
 constexpr int kBgmvMaxSlices = 8;
+// (LoRA, expert) groups up to which the pair-grouped pipeline runs (the sort's
+// shared-memory tables hold one entry per group).
+constexpr int kBgmvMaxGroups = 2048;
 struct BgmvPlan {
   const uint16_t *x = nullptr;
   const uint16_t *a[kBgmvMaxSlices] = {}, *b[kBgmvMaxSlices] = {};
@@ -150,7 +157,7 @@ struct BgmvPlan {
   int32_t *status = nullptr;
   int T = 0, H = 0, R = 0, S = 0, L = 0, E = 0, P = 0, k = 0, ld_y = 0;
 };
-size_t bgmv_workspace_bytes(int T, int contiguous_k);
+size_t bgmv_workspace_bytes(int T, int P, int contiguous_k, int num_loras, int E, int total_f);
 cudaError_t launch_bgmv(const BgmvPlan &p, const Launch &l);
 
 // S7: swap-AB weight-streaming GEMMs for few tokens per expert (decode.cu) ----

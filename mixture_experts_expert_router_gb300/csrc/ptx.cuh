@@ -442,5 +442,23 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint6
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+// all but the N most recent committed groups have landed
+template <int N>
+__device__ __forceinline__ void cp_async_wait_pending() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// D[16 x 8] += A[16 x 16] . B[16 x 8], bf16 operands, fp32 accumulators, one
+// warp (the m16n8k16 fragment layout: with g = lane / 4 and c = 2 * (lane % 4),
+// a0 = A[g][c..c+1], a1 = A[g+8][c..c+1], a2 = A[g][c+8..c+9], a3 = A[g+8][c+8..c+9];
+// b0 = B[c..c+1][g], b1 = B[c+8..c+9][g]; d0, d1 = D[g][c..c+1], d2, d3 = D[g+8][c..c+1]).
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
 
 }  // namespace moe

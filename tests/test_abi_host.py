@@ -44,7 +44,7 @@ def test_status_strings(lib):
         s = moe.moe_status_string(code)
         assert s and s != "unknown status code"
     assert moe.moe_status_string(-99) == "unknown status code"
-    assert lib.moe_abi_version() == 102
+    assert lib.moe_abi_version() == 103
 
 
 def test_argument_errors_before_device(lib):
@@ -106,6 +106,7 @@ def test_binding_constants_match_header():
              "MOE_PLAN_DECODE_SEPARATE": moe.PLAN_DECODE_SEPARATE, "MOE_PLAN_FUSED_GATHER": moe.PLAN_FUSED_GATHER,
              "MOE_PLAN_DECODE_ONE_LAUNCH": moe.PLAN_DECODE_ONE_LAUNCH,
              "MOE_PLAN_TEST_UNREACHABLE_WAIT": moe.PLAN_TEST_UNREACHABLE_WAIT,
+             "MOE_PLAN_NO_TAIL_TILES": moe.PLAN_NO_TAIL_TILES,
              "MOE_WEIGHTS_BF16": moe.WEIGHTS_BF16, "MOE_WEIGHTS_E4M3": moe.WEIGHTS_E4M3,
              "MOE_WAIT_LIMIT_MIN_NS": moe.WAIT_LIMIT_MIN_NS, "MOE_WAIT_LIMIT_MAX_NS": moe.WAIT_LIMIT_MAX_NS,
              "MOE_DEV_BAD_EXPERT": moe.DEV_BAD_EXPERT, "MOE_DEV_TIMEOUT": moe.DEV_TIMEOUT}

@@ -49,11 +49,11 @@ def _oracle_out(wl, tokens=None, w1=None, w2=None, clamp_limit=None):
 
 
 def _forward(wl, d, path=moe.PATH_AUTO, status=None, one_cta_gemm=False, decode_chain=False,
-             fused_gather=False, one_launch=False):
+             fused_gather=False, one_launch=False, no_tail_tiles=False):
     plan = moe.MoEPlan(d["x"], d["w1"], d["w2"], wl.E, wl.top_k, logits=d["logits"],
                        topk_ids=d["topk_ids"], topk_w=d["topk_w"], local_offset=wl.local_offset,
                        status=status, path=path, one_cta_gemm=one_cta_gemm, decode_chain=decode_chain,
-                       fused_gather=fused_gather, decode_one_launch=one_launch)
+                       fused_gather=fused_gather, decode_one_launch=one_launch, no_tail_tiles=no_tail_tiles)
     out = plan.launch()
     torch.cuda.synchronize()
     return out, plan
@@ -91,6 +91,18 @@ def test_odd_shapes(path, T, H, I, E, k, one_cta):
     out, _ = _forward(wl, _dev(wl), path, one_cta_gemm=one_cta)
     want, _ = _oracle_out(wl)
     check_bf16_end_to_end(W.bf16_bits(out), want, f"T={T} H={H} I={I} E={E} k={k}")
+
+
+@pytest.mark.parametrize("fused", [False, True])
+@pytest.mark.parametrize("T,H,I,E,k", [(700, 512, 256, 5, 2), (1500, 256, 256, 64, 6), (300, 256, 320, 16, 4)])
+def test_without_tail_tiles(T, H, I, E, k, fused):
+    """MOE_PLAN_NO_TAIL_TILES on the grouped path (gather kernel or fused
+    gather): the oracle's output under the end-to-end rule."""
+    wl = W.make_moe(T=T, H=H, I=I, E=E, top_k=k, mode="logits", seed=T + E + 3)
+    out, plan = _forward(wl, _dev(wl), moe.PATH_GROUPED, fused_gather=fused, no_tail_tiles=True)
+    assert int(plan.status.item()) == 0
+    want, _ = _oracle_out(wl)
+    check_bf16_end_to_end(W.bf16_bits(out), want, f"no tail tiles T={T} H={H} I={I} E={E} k={k}")
 
 
 @pytest.mark.parametrize("T,H,I,E,k", ODD_SHAPES + [(2000, 320, 384, 7, 2), (1500, 256, 256, 64, 6)])

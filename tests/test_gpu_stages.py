@@ -166,6 +166,21 @@ def test_grouped_gemm_parity(sizes, N, K):
     assert torch.all(sentinel[d["sum_m"]:] == -7.0)  # nothing written past the last group
 
 
+@pytest.mark.parametrize("sizes", [[0, 1, 129, 255, 256, 300, 0, 17], [1000, 3, 130, 64]])
+def test_grouped_gemm_without_tail_tiles_parity(sizes):
+    """MOE_PLAN_NO_TAIL_TILES: every remainder runs as a main tile whose rows
+    past the group are computed and not stored."""
+    d = W.make_grouped_gemm(seed=len(sizes) + 50, sizes=sizes, N=256, K=320)
+    X, Wt, offs = d["X"].to(DEV), d["W"].to(DEV), d["offs"].to(DEV)
+    sentinel = torch.full((d["sum_m"] + 3, 256), -7.0, dtype=torch.bfloat16, device=DEV)
+    Y = sentinel[:d["sum_m"]]
+    moe.grouped_gemm_fwd(X, Wt, offs, Y, no_tail_tiles=True)
+    torch.cuda.synchronize()
+    Yo = oracle.grouped_gemm_rows(W.bf16_bits(d["X"]), W.bf16_bits(d["W"]), d["offs"].numpy())
+    check_bf16_close(W.bf16_bits(Y), Yo, "Y (no tail tiles)")
+    assert torch.all(sentinel[d["sum_m"]:] == -7.0)
+
+
 def test_grouped_gemm_many_small_groups_parity():
     """800 groups of 0..40 rows (nearly all of them tail tiles, the group
     tables filling a large part of shared memory); K = 192 is an odd number of
