@@ -262,33 +262,36 @@ __global__ void __launch_bounds__(256) bgmv_key_kernel(const __grid_constant__ B
 constexpr int kKC = 256;        // x / A columns per shrink stage
 constexpr int kKP = kKC + 8;    // pitch (bf16) of a staged row
 
+constexpr int kShrinkPass = 2 * kGroupTile;  // pairs per shrink pass: two m16 tiles share each A chunk
+constexpr int kGsThreads = 512;               // 16 warps: 8 k-step lanes x 2 m-tiles
+
 template <int R>
 struct GShrinkSmem {
-  // ring depth: two CTAs per SM up to rank 32
-  static constexpr int NST = R <= 32 ? 4 : 3;
-  static constexpr int STAGE = (R + kGroupTile) * kKP;  // bf16: A rows, then the tile's x rows
+  static constexpr int NST = 3;  // ring depth (two CTAs per SM up to rank 32)
+  static constexpr int STAGE = (R + kShrinkPass) * kKP;  // bf16: A rows, then the pass's x rows
   static constexpr size_t RING_BYTES = (size_t)NST * STAGE * 2;
-  // the eight warps' sums [8][16][R] fp32 reuse the ring once a tile's k-loop is over
-  static_assert((size_t)8 * kGroupTile * R * 4 <= RING_BYTES, "the warp sums fit in the ring");
+  // the sixteen warps' sums [16][16][R] fp32 reuse the ring once a pass's k-loop is over
+  static_assert((size_t)16 * kGroupTile * R * 4 <= RING_BYTES, "the warp sums fit in the ring");
   static constexpr size_t TOK_OFF = RING_BYTES;
-  static constexpr size_t BYTES = TOK_OFF + kGroupTile * 4;
+  static constexpr size_t BYTES = TOK_OFF + kShrinkPass * 4;
 };
 
 __device__ __forceinline__ uint32_t lds32(const uint16_t *p) { return *reinterpret_cast<const uint32_t *>(p); }
 
-// One CTA per (group, slice): the group's pairs in tiles of 16 (the MMA's M),
-// its A block [R, H] on N, H on K.  Each stage copies kKC columns of A and of
-// the tile's x rows into shared memory (cp.async, a ring of NST stages with
-// NST - 1 in flight); warp w takes the k-steps w, w + 8, .. of every stage into
-// its own accumulators, and the eight warps' sums are added in warp order at
-// the end of the tile.
+// One CTA per (group, slice): the group's pairs in passes of up to 32 (two
+// 16-pair tiles, the M of the m16n8k16 MMA, sharing every A chunk), its A
+// block [R, H] on N, H on K.  Each stage copies kKC columns of A and of the
+// pass's x rows into shared memory (cp.async, one row per warp, a ring of NST
+// stages with NST - 1 in flight).  Warp w works on tile w % 2 and takes the
+// k-steps w / 2, w / 2 + 8 of every stage into its own accumulators; the eight
+// warps' sums of a tile are added in k-step-lane order at the end of the pass.
 template <int R>
-__global__ void __launch_bounds__(256) bgmv_gshrink_kernel(const __grid_constant__ BgmvArgs a) {
+__global__ void __launch_bounds__(kGsThreads) bgmv_gshrink_kernel(const __grid_constant__ BgmvArgs a) {
   using SM = GShrinkSmem<R>;
   extern __shared__ __align__(16) unsigned char gs_smem[];
   uint16_t *stage = reinterpret_cast<uint16_t *>(gs_smem);
-  float *red = reinterpret_cast<float *>(gs_smem);  // [8 warps][16 pairs][R], over the ring
-  int *tp = reinterpret_cast<int *>(gs_smem + SM::TOK_OFF);       // token of each pair of the tile
+  float *red = reinterpret_cast<float *>(gs_smem);  // [16 warps][16 pairs][R], over the ring
+  int *tp = reinterpret_cast<int *>(gs_smem + SM::TOK_OFF);  // token of each pair of the pass
   pdl_wait();
   const int g = blockIdx.x, s = blockIdx.y;
   const int p0 = a.g_indptr[g], p1 = a.g_indptr[g + 1];
@@ -296,30 +299,32 @@ __global__ void __launch_bounds__(256) bgmv_gshrink_kernel(const __grid_constant
     const int l = g / a.E, e = g - l * a.E;
     const uint16_t *A = a.a[s] + ((long)l * a.E + e) * R * a.H;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gq = lane >> 2, c2 = 2 * (lane & 3);
+    const int mt = warp & 1, kw = warp >> 1;  // this warp's tile and k-step lane
     const int nch = (a.H + kKC - 1) / kKC;
-    const uint64_t pol_a = policy_evict_first();  // each A element is read by one tile of one CTA
+    const uint64_t pol_a = policy_evict_first();  // each A element is read by one pass of one CTA
     const uint64_t pol_x = policy_evict_normal();
-    for (int q0 = p0; q0 < p1; q0 += kGroupTile) {
-      const int n = p1 - q0 < kGroupTile ? p1 - q0 : kGroupTile;
-      __syncthreads();  // the previous tile no longer reads tp, red or the stages
-      if (threadIdx.x < kGroupTile) tp[threadIdx.x] = (int)threadIdx.x < n ? a.tok[a.g_pairs[q0 + threadIdx.x]] : -1;
+    for (int q0 = p0; q0 < p1; q0 += kShrinkPass) {
+      const int n = p1 - q0 < kShrinkPass ? p1 - q0 : kShrinkPass;
+      __syncthreads();  // the previous pass no longer reads tp, red or the stages
+      if (threadIdx.x < kShrinkPass) tp[threadIdx.x] = (int)threadIdx.x < n ? a.tok[a.g_pairs[q0 + threadIdx.x]] : -1;
       __syncthreads();
-      auto load = [&](int ch) {
+      auto load = [&](int ch) {  // row r of the stage by warp r % 16, 16 bytes a lane
         uint16_t *st = stage + (ch % SM::NST) * SM::STAGE;
         const int h0 = ch * kKC, hn = a.H - h0 < kKC ? a.H - h0 : kKC;  // hn % 8 == 0
-        for (int i = threadIdx.x; i < (R + kGroupTile) * (kKC / 8); i += 256) {
-          const int row = i / (kKC / 8), v = i - row * (kKC / 8);
-          uint16_t *dst = st + row * kKP + 8 * v;
+        const bool in = 8 * lane < hn;
+        for (int row = warp; row < R + kShrinkPass; row += kGsThreads / 32) {
+          uint16_t *dst = st + row * kKP + 8 * lane;
           const uint16_t *src = nullptr;
-          if (8 * v < hn) {
-            if (row < R) src = A + (long)row * a.H + h0 + 8 * v;
-            else if (tp[row - R] >= 0) src = a.x + (long)tp[row - R] * a.H + h0 + 8 * v;
+          if (in) {
+            if (row < R) src = A + (long)row * a.H + h0 + 8 * lane;
+            else if (tp[row - R] >= 0) src = a.x + (long)tp[row - R] * a.H + h0 + 8 * lane;
           }
           if (src) cp_async_16(smem_u32(dst), src, row < R ? pol_a : pol_x);
           else *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
         }
         cp_async_commit();
       };
+      const bool active = mt * kGroupTile < n;  // this warp's tile has pairs
       float d[R / 8][4];
 #pragma unroll
       for (int nt = 0; nt < R / 8; ++nt) d[nt][0] = d[nt][1] = d[nt][2] = d[nt][3] = 0.f;
@@ -336,16 +341,19 @@ __global__ void __launch_bounds__(256) bgmv_gshrink_kernel(const __grid_constant
         else cp_async_commit();
         cp_async_wait_pending<SM::NST - 1>();
         __syncthreads();  // stage ch has landed for every thread
-        const uint16_t *As = stage + (ch % SM::NST) * SM::STAGE, *xs = As + R * kKP;
+        const uint16_t *As = stage + (ch % SM::NST) * SM::STAGE;
+        const uint16_t *xs = As + (R + mt * kGroupTile) * kKP;
         const int hn = a.H - ch * kKC < kKC ? a.H - ch * kKC : kKC;
-        for (int ks = warp; ks < (hn + 15) / 16; ks += 8) {
-          const int c = ks * 16 + c2;
-          const uint32_t a0 = lds32(xs + gq * kKP + c), a1 = lds32(xs + (gq + 8) * kKP + c);
-          const uint32_t a2 = lds32(xs + gq * kKP + c + 8), a3 = lds32(xs + (gq + 8) * kKP + c + 8);
+        if (active) {
+          for (int ks = kw; ks < (hn + 15) / 16; ks += 8) {
+            const int c = ks * 16 + c2;
+            const uint32_t a0 = lds32(xs + gq * kKP + c), a1 = lds32(xs + (gq + 8) * kKP + c);
+            const uint32_t a2 = lds32(xs + gq * kKP + c + 8), a3 = lds32(xs + (gq + 8) * kKP + c + 8);
 #pragma unroll
-          for (int nt = 0; nt < R / 8; ++nt) {
-            const uint16_t *br = As + (nt * 8 + gq) * kKP + c;
-            mma_bf16_16816(d[nt], a0, a1, a2, a3, lds32(br), lds32(br + 8));
+            for (int nt = 0; nt < R / 8; ++nt) {
+              const uint16_t *br = As + (nt * 8 + gq) * kKP + c;
+              mma_bf16_16816(d[nt], a0, a1, a2, a3, lds32(br), lds32(br + 8));
+            }
           }
         }
         __syncthreads();  // stage ch may be overwritten (by chunk ch + NST)
@@ -360,12 +368,12 @@ __global__ void __launch_bounds__(256) bgmv_gshrink_kernel(const __grid_constant
         r0[8 * R + 1] = d[nt][3];
       }
       __syncthreads();
-      for (int o = threadIdx.x; o < n * R; o += 256) {
-        const int row = o / R, col = o - row * R;
-        float v = red[row * R + col];
+      for (int o = threadIdx.x; o < n * R; o += kGsThreads) {
+        const int pr = o / R, col = o - pr * R, t = pr / kGroupTile, row = pr - t * kGroupTile;
+        float v = red[(t * kGroupTile + row) * R + col];  // k-step lane 0 (warp t)
 #pragma unroll
-        for (int w = 1; w < 8; ++w) v = __fadd_rn(v, red[(w * kGroupTile + row) * R + col]);
-        a.shrink[((long)s * a.P + a.g_pairs[q0 + row]) * R + col] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+        for (int k = 1; k < 8; ++k) v = __fadd_rn(v, red[((2 * k + t) * kGroupTile + row) * R + col]);
+        a.shrink[((long)s * a.P + a.g_pairs[q0 + pr]) * R + col] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
       }
     }
   }
@@ -529,7 +537,7 @@ static cudaError_t launch_gshrink(int G, int S, const Launch &l, const BgmvArgs 
   static const cudaError_t attr =
       cudaFuncSetAttribute(bgmv_gshrink_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (attr != cudaSuccess) return attr;
-  return launch_kernel(bgmv_gshrink_kernel<R>, dim3(G, S), dim3(256), bytes, l, a);
+  return launch_kernel(bgmv_gshrink_kernel<R>, dim3(G, S), dim3(kGsThreads), bytes, l, a);
 }
 
 // Workspace: [route index (general order)] [grouped pipeline: keys, group

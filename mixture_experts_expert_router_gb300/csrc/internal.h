@@ -30,9 +30,10 @@ cudaError_t launch_route(const float *logits, int T, int E, int k, int32_t *ids,
 
 // S2 ---------------------------------------------------------------------------
 // Routes per CTA of the multi-CTA sort, and the largest route count the
-// single-CTA sort handles.
+// single-CTA sort handles (one chunk: below it the multi-CTA path would run
+// three one-CTA kernels).
 constexpr int kSortChunk = 4096;
-constexpr int kSortSingleMax = 2048;
+constexpr int kSortSingleMax = kSortChunk;
 size_t sort_workspace_bytes(long routes, int L);
 cudaError_t launch_sort(const int32_t *ids, long routes, int E, int off, int L, int32_t *m_indptr,
                         int32_t *p2e, int32_t *e2p, int32_t *ws, int32_t *status,

@@ -63,6 +63,7 @@ def _check_sort(ids, E, off, L):
 
 @pytest.mark.parametrize("T,k,E,off,L", [
     (16, 2, 4, 0, 4), (1, 1, 1, 0, 1), (1024, 2, 8, 0, 8), (1025, 2, 8, 0, 8), (256, 8, 256, 0, 256),
+    (2048, 2, 16, 0, 16), (2049, 2, 16, 0, 16),  # 4096 routes: one CTA; 4098: two chunks
     (8192, 8, 256, 0, 256), (4096, 2, 8, 2, 3), (25000, 8, 1000, 100, 900), (3000, 6, 64, 63, 1),
     (64, 8, 128, 0, 128)])
 def test_sort_parity(T, k, E, off, L):
