@@ -352,10 +352,10 @@ MOE_API int moe_forward(const moe_bf16 *x, const float *logits, const int32_t *t
  * encodes the TMA tensor maps (host memory only).  moe_plan_launch then only
  * enqueues work: no allocation, no host synchronisation, capturable in a
  * CUDA graph, and valid for new VALUES written into the bound buffers.  Every
- * launch first clears the status word (if given) with cudaMemsetAsync on the
- * launch stream; for the decode chain in one launch it also zeroes, the same
- * way, the counters that the kernel keeps in the workspace, so plans may share
- * a workspace.  The workspace is every launch's scratch: launches of one plan
+ * launch first clears the status word (if given) on the launch stream, before
+ * any kernel of the launch can report into it: with cudaMemsetAsync, or, for
+ * the decode chain in one launch, with a one-CTA kernel that also zeroes the
+ * counters the chain keeps in the workspace, so plans may share a workspace.  The workspace is every launch's scratch: launches of one plan
  * (or of plans sharing a workspace) must run one after another (one stream,
  * or streams ordered by events).
  */

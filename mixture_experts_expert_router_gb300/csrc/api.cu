@@ -669,13 +669,23 @@ int moe_plan_launch(moe_plan *p, void *stream) {
   const moe_forward_desc &d = p->d;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // The status word is cleared on the stream before any kernel of the launch
-  // can OR a bit into it.
-  if (d.status && cudaMemsetAsync(d.status, 0, sizeof(int32_t), s) != cudaSuccess)
+  // can OR a bit into it: by a memset, or, for the decode chain in one launch,
+  // by the kernel that also zeroes the chain's counters (first of the launch).
+  const bool chain_clear = p->use_chain && p->chain.one_launch && d.T > 0;
+  if (d.status && !chain_clear && cudaMemsetAsync(d.status, 0, sizeof(int32_t), s) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (d.T == 0) return MOE_OK;
   Launch l;
   l.stream = s;
   l.pdl = !p->timing;
+  if (chain_clear) {
+    // The chain's counters live in the workspace, which other plans may
+    // share: every launch zeroes them first.  The clearing kernel follows the
+    // stream's earlier work in plain order; what comes next may start early.
+    Launch first = l;
+    first.pdl = false;
+    if (launch_chain_clear(p->chain, p->unreachable_wait, first) != cudaSuccess) return MOE_ERR_CUDA;
+  }
   cudaEvent_t *ev = p->timing ? p->ev[p->n_recorded % kTimingRing] : nullptr;
   auto mark = [&](int stage) -> bool {
     return !ev || cudaEventRecord(ev[stage], s) == cudaSuccess;
@@ -685,10 +695,6 @@ int moe_plan_launch(moe_plan *p, void *stream) {
     if (launch_route(d.logits, d.T, d.E, d.top_k, p->ids, p->w, l) != cudaSuccess) return MOE_ERR_CUDA;
   }
   if (p->use_chain) {  // sort, gather and finalize run inside the GEMM kernels
-    // The one-launch kernel's counters live in the workspace, which other
-    // plans may share: every launch zeroes them first.
-    if (p->chain.one_launch && chain_zero_counters(p->chain, s, p->unreachable_wait) != cudaSuccess)
-      return MOE_ERR_CUDA;
     if (!mark(kSort) || !mark(kGather) || !mark(kFc1)) return MOE_ERR_CUDA;
     if (p->chain.one_launch) {
       if (launch_chain(p->chain, 0, l) != cudaSuccess) return MOE_ERR_CUDA;

@@ -22,10 +22,12 @@
 // first CTA zeroes the combine counters.  One launch: every CTA runs its FC1
 // tiles first and then its FC2 tiles; an FC2 tile loads h once the count of
 // finished FC1 tiles of its expert is complete (a bounded wait on a counter
-// that FC1 epilogues raise after their h stores).  Every launch zeroes the
-// counters and clears the status word on its stream before the kernel starts
-// (chain_zero_counters), so no state carries over from another launch or from
-// another plan that shares the workspace.  With at most one CTA per SM and
+// that FC1 epilogues raise after their h stores).  Every launch first runs a
+// one-CTA kernel that zeroes the counters and clears the status word
+// (chain_clear_kernel); the chain follows it by programmatic dependent launch
+// and touches neither before its griddepcontrol.wait, so no state carries over
+// from another launch or from another plan that shares the workspace.  With
+// at most one CTA per SM and
 // no more CTAs than SMs, every CTA that others wait for has an SM, and FC1
 // tiles wait for nothing.
 //
@@ -390,6 +392,9 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
     int pend_s[HS], pend_kb[HS];
     int n_pend = 0;
     bool pdl_done = false;
+    // one launch: the clear kernel before this one zeroes the counters and the
+    // status word; no wait below may report into the status word before it
+    if (MODE == kModeBoth) pdl_wait();
     for (int wi = blockIdx.x; wi < total && ok; wi += gridDim.x) {
       const Item it = item(wi);
       const Tile c = it.c;
@@ -500,6 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
     const int q = warp == 1 ? 0 : 1;
     int iq = 0, tc = 0;
     bool ok = true;
+    if (MODE == kModeBoth) pdl_wait();  // as for the producers
     for (int wi = blockIdx.x; wi < total && ok; wi += gridDim.x, ++tc) {
       const int num_kb = (wi < total1 ? a.H : a.I) / BK;
       const int acc = tc & 1;
@@ -762,16 +768,27 @@ int chain_prepare(ChainPlan &p) {
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
-cudaError_t chain_zero_counters(const ChainPlan &p, cudaStream_t stream, bool unreachable) {
-  cudaError_t e;
-  // the plan lays out done1 right after comb, so one memset covers both
-  const char *lo = reinterpret_cast<const char *>(p.comb);
-  const char *hi = reinterpret_cast<const char *>(p.done1 + p.L + 1);
-  if (!unreachable && hi > lo && (size_t)(reinterpret_cast<const char *>(p.done1) - lo) < (1u << 20))
-    return cudaMemsetAsync(p.comb, 0, (size_t)(hi - lo), stream);
-  e = cudaMemsetAsync(p.done1, unreachable ? 0xFF : 0, ((size_t)p.L + 1) * sizeof(int32_t), stream);
-  if (e == cudaSuccess) e = cudaMemsetAsync(p.comb, 0, chain_comb_ints(p.T, p.H) * sizeof(int32_t), stream);
-  return e;
+namespace {
+
+// Zeroes the one-launch kernel's counters (comb, then done1: consecutive in
+// the workspace) and the status word, and lets the chain kernel start at once
+// (programmatic dependent launch): the chain touches neither before its
+// griddepcontrol.wait.  unreachable: done1 is filled with -1 instead.
+__global__ void __launch_bounds__(256) chain_clear_kernel(int32_t *lo, int n, const int32_t *done1, int32_t *status,
+                                                          int unreachable) {
+  pdl_launch_dependents();
+  for (int i = threadIdx.x; i < n; i += blockDim.x) lo[i] = unreachable && lo + i >= done1 ? -1 : 0;
+  if (threadIdx.x == 0 && status) *status = 0;
+}
+
+}  // namespace
+
+cudaError_t launch_chain_clear(const ChainPlan &p, bool unreachable, const Launch &l) {
+  // the plan lays out done1 right after comb (256-byte aligned), so one range
+  // from comb to the end of done1 covers both
+  const int n = (int)(p.done1 + p.L + 1 - p.comb);
+  return launch_kernel(chain_clear_kernel, dim3(1), dim3(256), 0, l, p.comb, n, (const int32_t *)p.done1,
+                       p.status, unreachable ? 1 : 0);
 }
 
 cudaError_t launch_chain(const ChainPlan &p, int part, const Launch &l) {

@@ -211,10 +211,12 @@ size_t chain_comb_ints(int T, int H);
 int chain_prepare(ChainPlan &p);
 // part 1: FC1 kernel, 2: FC2 kernel, 0: both phases in one kernel
 cudaError_t launch_chain(const ChainPlan &p, int part, const Launch &l);
-// One launch keeps counters in the workspace; every launch zeroes them on its
-// stream before the kernel (one memset: done1 follows comb in the workspace).
-// unreachable: the test hook MOE_PLAN_TEST_UNREACHABLE_WAIT, which fills the
-// per-expert FC1 counts with -1 instead, so that no FC2 wait can complete.
-cudaError_t chain_zero_counters(const ChainPlan &p, cudaStream_t stream, bool unreachable = false);
+// One launch keeps counters in the workspace; every launch first runs a
+// one-CTA kernel that zeroes them and the status word (done1 follows comb in
+// the workspace), and the chain kernel follows it by programmatic dependent
+// launch.  unreachable: the test hook MOE_PLAN_TEST_UNREACHABLE_WAIT, which
+// fills the per-expert FC1 counts with -1 instead, so that no FC2 wait can
+// complete.
+cudaError_t launch_chain_clear(const ChainPlan &p, bool unreachable, const Launch &l);
 
 }  // namespace moe
