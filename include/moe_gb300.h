@@ -306,11 +306,12 @@ MOE_API int grouped_gemm_wgrad(const moe_bf16 *G, const moe_bf16 *X, const int32
  *   contiguous_top_k = k > 0 (k <= MOE_MAX_TOP_K): the pairs are token-major,
  *   pair p of token p / k (num_pairs == T * k); 0: any order (e.g. sorted by
  *   expert), through a per-token route index.
- *   While num_loras * E <= 2048 the pairs are grouped by (LoRA, expert) with
- *   the routes' stable counting sort, so each A and B block is read once per
- *   group; the expand writes fp32 per-pair partials that one owner per token
- *   adds in ascending pair order (the page's pair-grouped pipeline).  Larger
- *   products run one CTA per pair (shrink) and one per token (expand).
+ *   The pairs are grouped by (LoRA, expert), so each A and B block is read
+ *   once per group (the page's pair-grouped pipeline): while groups x pairs
+ *   <= 2^22 by a scan (one CTA per group), else, up to MOE_MAX_EXPERTS
+ *   groups, by the routes' stable counting sort; the expand writes fp32
+ *   per-pair partials that one owner per token adds in ascending pair order.
+ *   Otherwise one CTA per pair (shrink) and one per token (expand).
  *   workspace: moe_bgmv_workspace_size(T, num_pairs, contiguous_top_k,
  *   num_loras, E, sum feat_out) bytes (route index, grouping, partials).
  *   A pair whose token, expert or LoRA index is out of range (or, with

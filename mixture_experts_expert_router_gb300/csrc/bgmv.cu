@@ -17,12 +17,14 @@
 //           columns f and adding w_p * (B row f . shrink) in pair order, so
 //           every replay is bitwise identical and nothing uses atomics.
 //
-// Two pipelines compute exactly this.  The pair-grouped one (the default
-// while num_loras * E <= kBgmvMaxGroups) sorts the pairs by (LoRA, expert)
-// with the stable counting sort of the routes (sort.cu), so each A and B block
-// is read once per group instead of once per pair:
-//   key      key[p] = lora[t] * E + e (negative for an invalid pair, whose
-//            shrink rows are zeroed);
+// Two pipelines compute exactly this.  The pair-grouped one groups the pairs
+// by (LoRA, expert), ascending pair index inside a group, so each A and B
+// block is read once per group instead of once per pair:
+//   group    while groups x pairs <= kScanGroupingMax: one CTA per group scans
+//            the pairs (bgmv_group_kernel); else, up to kBgmvSortMaxGroups
+//            groups, key[p] = lora[t] * E + e (negative for an invalid pair,
+//            whose shrink rows are zeroed) and the stable counting sort of the
+//            routes (sort.cu);
 //   gshrink  one CTA per (group, slice): tiles of 16 pairs times the group's
 //            A block, H staged through shared memory 256 columns at a time
 //            (cp.async, double-buffered) into m16n8k16 tensor-core MMAs with
@@ -39,7 +41,7 @@
 //            index (the owner rule), so the output does not depend on the
 //            grouping.
 // The per-route pipeline below (one CTA per pair for the shrink, one per
-// token for the expand) serves more (LoRA, expert) pairs than that.
+// token for the expand) serves whatever neither grouping takes.
 //
 // Pair layouts: "contiguous top-k" (pair p belongs to token p / k, the layout
 // the page's fast path serves) needs no index.  Any other order (for example
@@ -77,8 +79,10 @@ struct BgmvArgs {
   int32_t *idx;      // general layout: [T, kSlots] pair numbers
   int32_t *status;
   // grouped pipeline
-  int32_t *keys;            // [P]
-  const int32_t *g_indptr;  // [G + 1] pair rows of each (LoRA, expert) group
+  int32_t *keys;            // [P] (sorted grouping)
+  const int32_t *g_indptr;  // [G + 1] pair rows of each (LoRA, expert) group (sorted grouping)
+  int32_t *g_start, *g_cnt; // [G] each group's range of g_pairs (scanned grouping), else null
+  int32_t *g_total;         // pairs placed so far (scanned grouping; zeroed before it)
   const int32_t *g_pairs;   // [P] pair numbers in group order, ascending inside a group
   float *partial;           // [P, ld_part] fp32 w_p * (B row . shrink_p)
   int ld_part;              // sum of feat_out
@@ -243,15 +247,77 @@ __global__ void __launch_bounds__(kExpandThreads) bgmv_expand_kernel(const __gri
 // ------------------------------------------------------------ grouped pipeline --
 constexpr int kGroupTile = 16;  // pairs per tile: the M of the m16n8k16 tensor-core MMA
 
+// Scanned grouping (few groups times pairs): after bgmv_key_kernel, one CTA
+// per (LoRA, expert) group scans the keys, finds its pairs in ascending pair
+// index and writes them to a range of g_pairs claimed with one atomic add.
+// Where the range lands varies from run to run and does not matter: the
+// shrink, expand and combine read each group's pairs in their order, wherever
+// they sit.
+constexpr int kGroupThreads = 512;
+
+__global__ void __launch_bounds__(kGroupThreads) bgmv_group_kernel(const __grid_constant__ BgmvArgs a) {
+  __shared__ int wsum[kGroupThreads / 32];
+  __shared__ int base_s;
+  pdl_wait();
+  const int g = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int n = 0;
+#pragma unroll 4
+  for (int p = tid; p < a.P; p += kGroupThreads) n += __ldg(a.keys + p) == g;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
+  if (lane == 0) wsum[warp] = n;
+  __syncthreads();
+  if (tid == 0) {
+    int tot = 0;
+    for (int w = 0; w < kGroupThreads / 32; ++w) tot += wsum[w];
+    const int off = tot > 0 ? atomicAdd(a.g_total, tot) : 0;
+    a.g_start[g] = off;
+    a.g_cnt[g] = tot;
+    base_s = off;
+  }
+  __syncthreads();
+  int run = base_s;
+  for (int c = 0; c < a.P; c += kGroupThreads) {
+    const int p = c + tid;
+    const bool m = p < a.P && __ldg(a.keys + p) == g;
+    const unsigned b = __ballot_sync(0xffffffffu, m);
+    if (lane == 0) wsum[warp] = __popc(b);
+    __syncthreads();
+    int before = 0, tot = 0;
+    for (int w = 0; w < kGroupThreads / 32; ++w) {
+      const int x = wsum[w];
+      before += w < warp ? x : 0;
+      tot += x;
+    }
+    if (m) const_cast<int32_t *>(a.g_pairs)[run + before + __popc(b & ((1u << lane) - 1u))] = p;
+    run += tot;
+    __syncthreads();  // wsum is rewritten by the next round
+  }
+  pdl_launch_dependents();
+}
+
+// A group's range of g_pairs: from the scanned grouping, else the sort's offsets.
+__device__ __forceinline__ void group_range(const BgmvArgs &a, int g, int &p0, int &p1) {
+  if (a.g_start) {
+    p0 = a.g_start[g];
+    p1 = p0 + a.g_cnt[g];
+  } else {
+    p0 = a.g_indptr[g];
+    p1 = a.g_indptr[g + 1];
+  }
+}
+
 __global__ void __launch_bounds__(256) bgmv_key_kernel(const __grid_constant__ BgmvArgs a) {
   pdl_wait();
   const int p = blockIdx.x * blockDim.x + threadIdx.x;
   if (p < a.P) {
     const bool ok = pair_ok(a, p);
-    a.keys[p] = ok ? a.lora[a.tok[p]] * a.E + a.eid[p] : -1;  // the sort flags and drops -1
-    if (!ok)
+    a.keys[p] = ok ? a.lora[a.tok[p]] * a.E + a.eid[p] : -1;  // no group takes -1
+    if (!ok) {
       for (int s = 0; s < a.S; ++s)
         for (int r = 0; r < a.R; ++r) a.shrink[((long)s * a.P + p) * a.R + r] = 0;
+      if (a.status) atomicOr(reinterpret_cast<unsigned int *>(a.status), MOE_DEV_BAD_EXPERT);
+    }
   }
   pdl_launch_dependents();
 }
@@ -294,7 +360,8 @@ __global__ void __launch_bounds__(kGsThreads) bgmv_gshrink_kernel(const __grid_c
   int *tp = reinterpret_cast<int *>(gs_smem + SM::TOK_OFF);  // token of each pair of the pass
   pdl_wait();
   const int g = blockIdx.x, s = blockIdx.y;
-  const int p0 = a.g_indptr[g], p1 = a.g_indptr[g + 1];
+  int p0, p1;
+  group_range(a, g, p0, p1);
   if (p1 > p0) {
     const int l = g / a.E, e = g - l * a.E;
     const uint16_t *A = a.a[s] + ((long)l * a.E + e) * R * a.H;
@@ -393,7 +460,8 @@ __global__ void __launch_bounds__(256) bgmv_gexpand_kernel(const __grid_constant
   __shared__ int sp[kGroupTile];
   pdl_wait();
   const int g = blockIdx.x;
-  const int p0 = a.g_indptr[g], p1 = a.g_indptr[g + 1];
+  int p0, p1;
+  group_range(a, g, p0, p1);
   if (p1 > p0) {
     int s = 0, c = blockIdx.y;
     while (s < a.S && c >= (a.f[s] + 255) / 256) c -= (a.f[s++] + 255) / 256;
@@ -543,9 +611,15 @@ static cudaError_t launch_gshrink(int G, int S, const Launch &l, const BgmvArgs 
 // Workspace: [route index (general order)] [grouped pipeline: keys, group
 // offsets, pairs in group order, their inverse, the sort's table, partials].
 struct BgmvLayout {
-  size_t cnt, idx, keys, g_indptr, g_pairs, g_inv, sort_ws, partial, total;
+  size_t g_total, cnt, idx, keys, g_indptr, g_pairs, g_inv, sort_ws, g_start, g_cnt, partial, total;
   bool grouped;
 };
+
+// Group count times pairs up to which the grouping scans (one CTA per group
+// reading every pair); above it the pairs are keyed and sorted (S2's sort).
+constexpr long kScanGroupingMax = 1L << 22;
+
+static bool bgmv_scan_grouping(int G, int P) { return G >= 1 && (long)G * P <= kScanGroupingMax; }
 
 static BgmvLayout bgmv_layout(int T, int P, int k, int G, int total_f) {
   BgmvLayout o{};
@@ -555,17 +629,21 @@ static BgmvLayout bgmv_layout(int T, int P, int k, int G, int total_f) {
     off += bgmv_align(bytes > 0 ? bytes : 1);
     return at;
   };
+  // g_total right before cnt: one memset clears both
+  o.g_total = take(4);
   if (k == 0) {
     o.cnt = take((size_t)T * 4);
     o.idx = take((size_t)T * kSlots * 4);
   }
-  o.grouped = G >= 1 && G <= kBgmvMaxGroups;
+  o.grouped = bgmv_scan_grouping(G, P) || (G >= 1 && G <= kBgmvSortMaxGroups);
   if (o.grouped) {
     o.keys = take((size_t)P * 4);
     o.g_indptr = take((size_t)(G + 1) * 4);
     o.g_pairs = take((size_t)P * 4);
     o.g_inv = take((size_t)P * 4);
     o.sort_ws = take(sort_workspace_bytes(P, G));
+    o.g_start = take((size_t)G * 4);
+    o.g_cnt = take((size_t)G * 4);
     o.partial = take((size_t)P * total_f * 4);
   }
   o.total = off;
@@ -602,6 +680,10 @@ cudaError_t launch_bgmv(const BgmvPlan &p, const Launch &l) {
   a.keys = lay.grouped ? reinterpret_cast<int32_t *>(ws + lay.keys) : nullptr;
   a.g_indptr = lay.grouped ? reinterpret_cast<int32_t *>(ws + lay.g_indptr) : nullptr;
   a.g_pairs = lay.grouped ? reinterpret_cast<int32_t *>(ws + lay.g_pairs) : nullptr;
+  const bool scan = bgmv_scan_grouping(G, p.P);
+  a.g_start = scan ? reinterpret_cast<int32_t *>(ws + lay.g_start) : nullptr;
+  a.g_cnt = scan ? reinterpret_cast<int32_t *>(ws + lay.g_cnt) : nullptr;
+  a.g_total = reinterpret_cast<int32_t *>(ws + lay.g_total);
   a.partial = lay.grouped ? reinterpret_cast<float *>(ws + lay.partial) : nullptr;
   a.ld_part = total_f;
   a.T = p.T;
@@ -616,9 +698,13 @@ cudaError_t launch_bgmv(const BgmvPlan &p, const Launch &l) {
   cudaError_t e;
   Launch first = l;  // the first kernel of the call waits for everything before it
   first.pdl = false;
-  if (p.k == 0) {
-    e = cudaMemsetAsync(a.cnt, 0, (size_t)p.T * sizeof(int32_t), l.stream);
+  // the scanned grouping's pair counter and the route index's counts start at 0
+  if (p.k == 0 || scan) {
+    const size_t bytes = p.k == 0 ? lay.cnt + (size_t)p.T * sizeof(int32_t) - lay.g_total : sizeof(int32_t);
+    e = cudaMemsetAsync(a.g_total, 0, bytes, l.stream);
     if (e != cudaSuccess) return e;
+  }
+  if (p.k == 0) {
     if (p.P > 0) {
       e = launch_kernel(bgmv_index_kernel, dim3((p.P + 255) / 256), dim3(256), 0, first, a);
       if (e != cudaSuccess) return e;
@@ -628,9 +714,13 @@ cudaError_t launch_bgmv(const BgmvPlan &p, const Launch &l) {
   if (lay.grouped && p.P > 0) {
     e = launch_kernel(bgmv_key_kernel, dim3((p.P + 255) / 256), dim3(256), 0, first, a);
     if (e != cudaSuccess) return e;
-    e = launch_sort(a.keys, p.P, G, 0, G, const_cast<int32_t *>(a.g_indptr), const_cast<int32_t *>(a.g_pairs),
-                    reinterpret_cast<int32_t *>(ws + lay.g_inv), reinterpret_cast<int32_t *>(ws + lay.sort_ws),
-                    p.status, l);
+    if (scan) {
+      e = launch_kernel(bgmv_group_kernel, dim3(G), dim3(kGroupThreads), 0, l, a);
+    } else {
+      e = launch_sort(a.keys, p.P, G, 0, G, const_cast<int32_t *>(a.g_indptr), const_cast<int32_t *>(a.g_pairs),
+                      reinterpret_cast<int32_t *>(ws + lay.g_inv), reinterpret_cast<int32_t *>(ws + lay.sort_ws),
+                      p.status, l);
+    }
     if (e != cudaSuccess) return e;
     switch (p.R) {
       case 8: e = launch_gshrink<8>(G, p.S, l, a); break;

@@ -143,9 +143,9 @@ cudaError_t launch_bwd(const BwdPlan &p, const Launch &l);
 
 // BGMV LoRA-MoE shrink + expand (bgmv.cu) ----------------------------------------
 constexpr int kBgmvMaxSlices = 8;
-// (LoRA, expert) groups up to which the pair-grouped pipeline runs (the sort's
-// shared-memory tables hold one entry per group).
-constexpr int kBgmvMaxGroups = 2048;
+// (LoRA, expert) groups up to which the pair-grouped pipeline may group the
+// pairs with the route sort (its scans take at most MOE_MAX_EXPERTS groups).
+constexpr int kBgmvSortMaxGroups = MOE_MAX_EXPERTS;
 struct BgmvPlan {
   const uint16_t *x = nullptr;
   const uint16_t *a[kBgmvMaxSlices] = {}, *b[kBgmvMaxSlices] = {};

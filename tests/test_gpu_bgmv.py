@@ -1,9 +1,10 @@
 """Parity of the BGMV LoRA-MoE shrink + expand (moe_bgmv, called through the C
 ABI) against the CPU oracle (flashinfer.fused_moe.prepare_bgmv_moe: shrink
 bf16(A[l,e] . x[t]) per routed pair, expand summed per token in ascending pair
-order in fp32, one owner per output), on the pair-grouped pipeline and, past
-2048 (LoRA, expert) groups, the per-route one.  The shrink values use the strict bf16
-rule, y the fp32 rule; replays are bitwise identical."""
+order in fp32, one owner per output), on the pair-grouped pipeline (grouped by
+a scan while groups x pairs <= 2^22, else by keys and the route sort up to 1024
+(LoRA, expert) groups) and on the per-route one beyond.  The shrink values use
+the strict bf16 rule, y the fp32 rule; replays are bitwise identical."""
 import numpy as np
 import pytest
 import torch
@@ -38,7 +39,9 @@ def _oracle(wl, tok=None, eid=None, lora=None):
 SHAPES = [  # T, H, R, E, L, k, feat_out
     (37, 64, 8, 5, 2, 2, None), (200, 256, 16, 16, 3, 2, [256, 64]), (64, 3072, 32, 64, 4, 2, None),
     (50, 512, 64, 8, 1, 6, [128]), (300, 128, 32, 32, 5, 4, [96, 128, 32]),
-    (60, 64, 8, 1024, 3, 2, None),  # 3072 (LoRA, expert) groups: the per-route pipeline
+    (60, 64, 8, 1024, 3, 2, None),  # 3072 (LoRA, expert) groups x 120 pairs: scanned grouping
+    (2100, 128, 16, 256, 4, 2, None),  # 1024 groups x 4200 pairs: keyed and sorted grouping
+    (700, 64, 8, 1024, 3, 2, None),  # 3072 groups x 1400 pairs: the per-route pipeline
 ]
 
 
