@@ -605,18 +605,20 @@ int moe_forward_prepare(const moe_forward_desc *desc, moe_plan **plan_out) {
                           p->m_indptr + 1, d.T, p->y, d.status, true);
     } else if (e4m3) {
       uint8_t *xq = reinterpret_cast<uint8_t *>(p->xp), *hq = reinterpret_cast<uint8_t *>(p->h);
+      const bool pair = (d.flags & MOE_PLAN_ONE_CTA_GEMM) == 0;
       rc = gemm_prepare_e4m3(p->fc1, Epi::kSwiGLU, xq, p->R, static_cast<const uint8_t *>(static_cast<const void *>(d.w1)),
-                             d.num_local, 2 * d.I, d.H, d.I, p->m_indptr + 1, p->R, hq, d.status);
+                             d.num_local, 2 * d.I, d.H, d.I, p->m_indptr + 1, p->R, hq, d.status, pair);
       p->fc1.clamp = d.clamp_limit;
       p->fc1.wscale = d.w1_scale;
       p->fc1.ascale = d.x_scale;
       p->fc1.oscale = d.h_scale;
       if (rc == MOE_OK) {
         rc = gemm_prepare_e4m3(p->fc2, Epi::kF32, hq, p->R, static_cast<const uint8_t *>(static_cast<const void *>(d.w2)),
-                               d.num_local, d.H, d.I, d.H, p->m_indptr + 1, p->R, p->y, d.status);
+                               d.num_local, d.H, d.I, d.H, p->m_indptr + 1, p->R, p->y, d.status, pair);
         p->fc2.wscale = d.w2_scale;
         p->fc2.ascale = d.h_scale;
       }
+      if (d.flags & MOE_PLAN_NO_TAIL_TILES) p->fc1.tail_max = p->fc2.tail_max = 0;
     } else {
       const bool pair = (d.flags & MOE_PLAN_ONE_CTA_GEMM) == 0;
       // Either the gather kernel builds xp (one 128-row TMA box per k-block

@@ -582,7 +582,7 @@ static int encode_2d_u8(CUtensorMap *map, const void *ptr, long rows, int K, int
 
 int gemm_prepare_e4m3(GemmPlan &p, Epi epi, const uint8_t *A, long a_rows, const uint8_t *B, int G,
                       int b_rows, int K, int n_out, const int32_t *group_end, long max_rows,
-                      void *out, int32_t *status) {
+                      void *out, int32_t *status, bool allow_pair) {
   if (K % 128 != 0 || epi == Epi::kBf16) return MOE_ERR_SHAPE;
   p = GemmPlan();
   p.q = 1;
@@ -606,17 +606,28 @@ int gemm_prepare_e4m3(GemmPlan &p, Epi epi, const uint8_t *A, long a_rows, const
     p.n_tiles = n_out / p.bn;
     box_b = p.bn;
   }
+  const double b_group_bytes = (double)b_rows * K;
+  p.m_major = b_group_bytes <= 64.0 * 1024 * 1024 ? 1 : 0;
+  const long sms = device_sm_count();
+  if (allow_pair && pair_gemm_supported(epi, n_out)) {  // CTA pairs: 128 of the 256 B rows per CTA
+    p.pair = 1;
+    p.bn = 256;
+    p.n_tiles = epi == Epi::kSwiGLU ? n_out / 128 : n_out / 256;
+    if (int rc = pair_gemm_encode_u8(p, A, a_rows, B, (long)G * b_rows, K)) return rc;
+    p.smem = pair_gemm_smem(epi, G);
+    const long max_pairs = ((max_rows + 2 * BM - 1) / (2 * BM) + G) * (long)p.n_tiles;
+    const long clusters = sms / 2;
+    p.grid = 2 * (int)(max_pairs < clusters ? (max_pairs > 0 ? max_pairs : 1) : clusters);
+    return pair_gemm_configure(epi, p.smem, 1) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  }
   int rc = encode_2d_u8(&p.map_a, A, a_rows, K, BM);
   if (rc == MOE_OK) rc = encode_2d_u8(&p.map_b, B, (long)G * b_rows, K, box_b);
   if (rc != MOE_OK) return rc;
-  const double b_group_bytes = (double)b_rows * K;
-  p.m_major = b_group_bytes <= 64.0 * 1024 * 1024 ? 1 : 0;
   switch (p.bn) {
     case 256: p.smem = Cfg<256>::smem_bytes(G); break;
     case 128: p.smem = Cfg<128>::smem_bytes(G); break;
     default: p.smem = Cfg<64>::smem_bytes(G); break;
   }
-  const long sms = device_sm_count();
   const long max_tiles = ((max_rows + BM - 1) / BM + G) * (long)p.n_tiles;
   p.grid = (int)(max_tiles < sms ? (max_tiles > 0 ? max_tiles : 1) : sms);
   cudaError_t e;

@@ -27,6 +27,12 @@
 // rows followed by the matching 64 gate rows, and the gate half hands its
 // values to the up half through shared memory.
 //
+// E4M3 operands (the fp8 per-tensor family, Q = 1): a k-block is 128 codes,
+// the same 128 bytes per row as 64 bf16 values, so stages, boxes and
+// descriptor steps are unchanged; the MMAs are kind::f8f6f4 (K = 32); the
+// epilogues dequantise by ascale * wscale[group], and FC1 requantises h to
+// E4M3 codes e4m3(h / oscale), exactly as the one-CTA kernel does.
+//
 // Synchronisation across the pair:
 //   full[s]   leader only; both CTAs' TMA loads signal it (the leader arms the
 //             transaction bytes of both);
@@ -79,8 +85,6 @@ struct PairLayout {
   static constexpr int TAB_OFF = SG_OFF + 16 * 64 * 4;
 };
 constexpr uint32_t TMEM_COLS = 2 * BN;
-constexpr uint32_t IDESC_MAIN = idesc_bf16_f32(2 * BM, BN);
-constexpr int kTailMax = 128;
 
 struct PairArgs {
   CUtensorMap map_a;      // tokens [rows, K], box {64, 128}
@@ -97,6 +101,8 @@ struct PairArgs {
   int32_t *status;
   unsigned long long wait_ns;  // bounded-wait limit of this launch
   const float *clamp;         // SwiGLU epilogue: [groups] SwiGLUStep limits, or null
+  const float *wscale;        // E4M3: [groups] weight scales
+  float ascale, oscale;       // E4M3: activation scale of A, requantisation scale of h
   long max_rows;
   int G, K, n_out, b_rows, n_tiles, m_major;
   int tail_max;               // remainders of up to this many rows run as swap-AB tail tiles (0: none)
@@ -206,9 +212,11 @@ __device__ __forceinline__ PairOperands pair_operands(const PairTile &c, uint32_
   return o;
 }
 
-template <int EPI, bool GATH>
+template <int EPI, bool GATH, int Q>
 __global__ void __launch_bounds__(GATH ? kThreadsGather : kThreads, 1)
     pair_gemm_kernel(const __grid_constant__ PairArgs args) {
+  static_assert(!Q || (!GATH && EPI != (int)Epi::kBf16), "E4M3: FC1 and FC2 epilogues, token rows by TMA");
+  constexpr int KE = Q ? 128 : BK;  // elements per k-block (128 bytes of a row either way)
   using Lay = PairLayout<EPI>;
   constexpr int STAGES = Lay::STAGES;
   static_assert(kThreadsGather / 32 - kGatherWarp0 == STAGES, "one gather warp per ring slot");
@@ -292,7 +300,7 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : kThreads, 1)
 
   const uint32_t tmem_base = *tmem_holder;
   const int total = tile_start[G] * args.n_tiles;
-  const int num_kb = args.K / BK;
+  const int num_kb = args.K / KE;
   const int n_rounds = (num_kb + KH - 1) / KH;  // ring stages per tile
   const int cluster = blockIdx.x >> 1;
   const int nclusters = gridDim.x >> 1;
@@ -326,7 +334,7 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : kThreads, 1)
           const uint32_t leader_full = mapa_shared(full_bar(s), 0);
           if (rank == 0) mbar_arrive_expect_tx(full_bar(s), 2 * o.bytes * (uint32_t)nk);
           for (int h = 0; h < nk; ++h) {
-            const int kx = (kr * KH + h) * BK;
+            const int kx = (kr * KH + h) * KE;
             const uint32_t t_dst = smem_base + s * STAGE_BYTES + (c.tail ? A_STAGE + h * B_BYTES : h * A_BYTES);
             tma_load_2d_pair(t_dst, tok_map, leader_full, kx, o.tok_row, pol);
           }
@@ -364,7 +372,7 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : kThreads, 1)
           // gather mode: only the weight boxes are counted as transaction bytes
           if (GATH && rank == 0) mbar_arrive_expect_tx(full_bar(s), 2 * o.w_bytes * (uint32_t)nk);
           for (int h = 0; h < nk; ++h) {
-            const int kx = (kr * KH + h) * BK;
+            const int kx = (kr * KH + h) * KE;
             const uint32_t w_dst = smem_base + s * STAGE_BYTES + (c.tail ? h * A_BYTES : A_STAGE + h * B_BYTES);
             if (c.tail && kSwiGLU) {  // 64 up rows then the matching 64 gate rows
               tma_load_2d_pair(w_dst, &args.map_w64, leader_full, kx, o.w_row, pol);
@@ -383,7 +391,8 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : kThreads, 1)
       bool ok = true;
       for (int t = cluster; t < total && ok; t += nclusters, ++tc) {
         const PairTile c = decode_pair_tile(t, tile_start, gend, G, args.n_tiles, args.m_major, args.tail_max);
-        const uint32_t idesc = c.tail ? idesc_bf16_f32(2 * BM, (uint32_t)tail_n(c.tail)) : IDESC_MAIN;
+        const uint32_t n_mma = c.tail ? (uint32_t)tail_n(c.tail) : (uint32_t)BN;
+        const uint32_t idesc = Q ? idesc_e4m3_f32(2 * BM, n_mma) : idesc_bf16_f32(2 * BM, n_mma);
         const int acc = tc & 1;
         const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
         if (!mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag, args.status, args.wait_ns)) break;
@@ -403,8 +412,10 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : kThreads, 1)
             const uint64_t a_desc = smem_desc_k_sw128(st + h * A_BYTES);
             const uint64_t b_desc = smem_desc_k_sw128(st + A_STAGE + h * B_BYTES);
 #pragma unroll
-            for (int k = 0; k < BK / 16; ++k)
-              umma_bf16_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, (kr | h | k) != 0);
+            for (int k = 0; k < 4; ++k) {  // 32 bytes of each row per MMA: 16 bf16 or 32 E4M3 values
+              if (Q) umma_e4m3_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, (kr | h | k) != 0);
+              else umma_bf16_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, (kr | h | k) != 0);
+            }
           }
           umma_commit_pair(empty_bar(s), 0x3);
         }
@@ -433,7 +444,36 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : kThreads, 1)
         const int valid = gend[c.g] - row0;  // may be <= 0 for the second CTA's rows
         const bool row_ok = r_in_tile < valid;
         const long orow = (long)row0 + r_in_tile;
-        if (kSwiGLU) {
+        if (kSwiGLU && Q) {
+          // E4M3: u, g dequantised by ascale * wscale[g], SwiGLU(Step), h requantised
+          uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(args.out) + orow * args.n_out +
+                                                 (long)c.n * (BN / 2));
+          const float lim = step_limit(args.clamp, c.g);
+          const float sc = __fmul_rn(args.ascale, __ldg(args.wscale + c.g));
+#pragma unroll 1
+          for (int col = 0; col < BN / 2; col += 32) {
+            uint32_t u[32], g[32];
+            tmem_ld_32x32b_x32(taddr + col, u);
+            tmem_ld_32x32b_x32(taddr + BN / 2 + col, g);
+            tmem_ld_wait();
+            uint32_t packed[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              float hv[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const float uu = __fmul_rn(__uint_as_float(u[4 * i + q]), sc);
+                const float gg = __fmul_rn(__uint_as_float(g[4 * i + q]), sc);
+                hv[q] = __fdiv_rn(swiglu_step(gg, uu, lim), args.oscale);
+              }
+              packed[i] = e4m3x2(hv[0], hv[1]) | (e4m3x2(hv[2], hv[3]) << 16);
+            }
+            if (row_ok) {
+              dst[col / 16] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+              dst[col / 16 + 1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+            }
+          }
+        } else if (kSwiGLU) {
           uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(args.out) +
                                                  orow * args.n_out + (long)c.n * (BN / 2));
           const float lim = step_limit(args.clamp, c.g);
@@ -456,6 +496,8 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : kThreads, 1)
             }
           }
         } else if (EPI == (int)Epi::kF32) {
+          // E4M3: y dequantised by ascale * wscale[g]
+          const float sc = Q ? __fmul_rn(args.ascale, __ldg(args.wscale + c.g)) : 1.f;
           if (valid >= BM) {
             // full tile: 32-column chunks staged in swizzled shared memory and
             // written by TMA stores (whole 128-byte rows)
@@ -469,6 +511,10 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : kThreads, 1)
               uint32_t r[32];
               tmem_ld_32x32b_x32(taddr + col, r);
               tmem_ld_wait();
+              if (Q) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__fmul_rn(__uint_as_float(r[i]), sc));
+              }
               const uint32_t row_addr = smem_base + Lay::STG_OFF + r_in_tile * 128;
 #pragma unroll
               for (int v = 0; v < 8; ++v)
@@ -493,6 +539,10 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : kThreads, 1)
               uint32_t r[32];
               tmem_ld_32x32b_x32(taddr + col, r);
               tmem_ld_wait();
+              if (Q) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__fmul_rn(__uint_as_float(r[i]), sc));
+              }
               if (row_ok) {
 #pragma unroll
                 for (int v = 0; v < 8; ++v)
@@ -526,6 +576,7 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : kThreads, 1)
         const int n = tail_n(c.tail);
         const long tok0 = (long)c.gstart + c.mp * 2 * BM;
         const float lim = step_limit(args.clamp, c.g);
+        const float sc = Q ? __fmul_rn(args.ascale, __ldg(args.wscale + c.g)) : 1.f;  // E4M3 dequantisation
 #pragma unroll 1
         for (int c0 = 0; c0 < n; c0 += 16) {
           uint32_t r[16];
@@ -544,13 +595,25 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : kThreads, 1)
             }
             epi_bar();
             if (r_in_tile < 64) {
-              __nv_bfloat16 *h = reinterpret_cast<__nv_bfloat16 *>(args.out);
               const long col = (long)c.n * (BN / 2) + (int)rank * 64 + r_in_tile;
+              if (Q) {
+                uint8_t *h = reinterpret_cast<uint8_t *>(args.out);
 #pragma unroll
-              for (int j = 0; j < 16; ++j)
-                if (c0 + j < c.tail)
-                  h[(tok0 + c0 + j) * args.n_out + col] =
-                      __float2bfloat16_rn(swiglu_step(sg[j * 64 + r_in_tile], __uint_as_float(r[j]), lim));
+                for (int j = 0; j < 16; ++j)
+                  if (c0 + j < c.tail) {
+                    const float uu = __fmul_rn(__uint_as_float(r[j]), sc);
+                    const float gg = __fmul_rn(sg[j * 64 + r_in_tile], sc);
+                    h[(tok0 + c0 + j) * args.n_out + col] =
+                        (uint8_t)(e4m3x2(__fdiv_rn(swiglu_step(gg, uu, lim), args.oscale), 0.f) & 0xFFu);
+                  }
+              } else {
+                __nv_bfloat16 *h = reinterpret_cast<__nv_bfloat16 *>(args.out);
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                  if (c0 + j < c.tail)
+                    h[(tok0 + c0 + j) * args.n_out + col] =
+                        __float2bfloat16_rn(swiglu_step(sg[j * 64 + r_in_tile], __uint_as_float(r[j]), lim));
+              }
             }
             epi_bar();
           } else {
@@ -559,7 +622,8 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : kThreads, 1)
               float *y = reinterpret_cast<float *>(args.out);
 #pragma unroll
               for (int j = 0; j < 16; ++j)
-                if (c0 + j < c.tail) y[(tok0 + c0 + j) * args.n_out + col] = __uint_as_float(r[j]);
+                if (c0 + j < c.tail)
+                  y[(tok0 + c0 + j) * args.n_out + col] = Q ? __fmul_rn(__uint_as_float(r[j]), sc) : __uint_as_float(r[j]);
             } else {
               __nv_bfloat16 *y = reinterpret_cast<__nv_bfloat16 *>(args.out);
 #pragma unroll
@@ -676,6 +740,24 @@ int encode(CUtensorMap *map, const void *ptr, long rows, int K, int box_rows) {
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_TENSOR_MAP;
 }
 
+// uint8 [rows, K] (E4M3 codes): box {128, box_rows}, 128-byte swizzle.
+int encode_u8(CUtensorMap *map, const void *ptr, long rows, int K, int box_rows) {
+  void *p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return MOE_ERR_DEVICE;
+  EncodeTiledFn fn = reinterpret_cast<EncodeTiledFn>(p);
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)(rows > 0 ? rows : 1)};
+  cuuint64_t strides[1] = {(cuuint64_t)K};
+  cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_TENSOR_MAP;
+}
+
 // fp32 [rows, cols] row-major for TMA stores: box {32, 128}, 128-byte swizzle.
 int encode_f32_store(CUtensorMap *map, void *ptr, long rows, int cols) {
   EncodeTiledFn fn = nullptr;
@@ -717,15 +799,28 @@ int pair_gemm_encode_extra(GemmPlan &p, const uint16_t *A, long a_rows, const ui
   return rc;
 }
 
-cudaError_t pair_gemm_configure(Epi epi, size_t smem) {
+int pair_gemm_encode_u8(GemmPlan &p, const uint8_t *A, long a_rows, const uint8_t *B, long b_rows_total, int K) {
+  int rc = encode_u8(&p.map_a, A, a_rows, K, BM);
+  if (rc == MOE_OK) rc = encode_u8(&p.map_b, B, b_rows_total, K, BN / 2);
+  if (rc == MOE_OK) rc = encode_u8(&p.map_w64, B, b_rows_total, K, 64);
+  for (int i = 0; i < 4 && rc == MOE_OK; ++i) rc = encode_u8(&p.map_t[i], A, a_rows, K, 8 << i);
+  if (rc == MOE_OK && p.epi == Epi::kF32) rc = encode_f32_store(&p.map_y, p.out, p.max_rows, p.n_out);
+  return rc;
+}
+
+cudaError_t pair_gemm_configure(Epi epi, size_t smem, int q) {
   constexpr auto kAttr = cudaFuncAttributeMaxDynamicSharedMemorySize;
-  if (epi == Epi::kSwiGLU) {
-    const cudaError_t e = cudaFuncSetAttribute(pair_gemm_kernel<(int)Epi::kSwiGLU, false>, kAttr, (int)smem);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(pair_gemm_kernel<(int)Epi::kSwiGLU, true>, kAttr, (int)smem);
+  if (q) {
+    if (epi == Epi::kSwiGLU) return cudaFuncSetAttribute(pair_gemm_kernel<(int)Epi::kSwiGLU, false, 1>, kAttr, (int)smem);
+    return cudaFuncSetAttribute(pair_gemm_kernel<(int)Epi::kF32, false, 1>, kAttr, (int)smem);
   }
-  if (epi == Epi::kF32) return cudaFuncSetAttribute(pair_gemm_kernel<(int)Epi::kF32, false>, kAttr, (int)smem);
-  return cudaFuncSetAttribute(pair_gemm_kernel<(int)Epi::kBf16, false>, kAttr, (int)smem);
+  if (epi == Epi::kSwiGLU) {
+    const cudaError_t e = cudaFuncSetAttribute(pair_gemm_kernel<(int)Epi::kSwiGLU, false, 0>, kAttr, (int)smem);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(pair_gemm_kernel<(int)Epi::kSwiGLU, true, 0>, kAttr, (int)smem);
+  }
+  if (epi == Epi::kF32) return cudaFuncSetAttribute(pair_gemm_kernel<(int)Epi::kF32, false, 0>, kAttr, (int)smem);
+  return cudaFuncSetAttribute(pair_gemm_kernel<(int)Epi::kBf16, false, 0>, kAttr, (int)smem);
 }
 
 cudaError_t launch_pair_gemm(const GemmPlan &p, const Launch &l) {
@@ -744,6 +839,9 @@ cudaError_t launch_pair_gemm(const GemmPlan &p, const Launch &l) {
   a.status = p.status;
   a.wait_ns = p.wait_ns;
   a.clamp = p.clamp;
+  a.wscale = p.wscale;
+  a.ascale = p.ascale;
+  a.oscale = p.oscale;
   a.max_rows = p.max_rows;
   a.G = p.G;
   a.K = p.K;
@@ -767,10 +865,14 @@ cudaError_t launch_pair_gemm(const GemmPlan &p, const Launch &l) {
   attr[1].val.programmaticStreamSerializationAllowed = l.pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  if (gath) return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<(int)Epi::kSwiGLU, true>, a);
-  if (p.epi == Epi::kSwiGLU) return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<(int)Epi::kSwiGLU, false>, a);
-  if (p.epi == Epi::kF32) return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<(int)Epi::kF32, false>, a);
-  return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<(int)Epi::kBf16, false>, a);
+  if (p.q) {
+    if (p.epi == Epi::kSwiGLU) return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<(int)Epi::kSwiGLU, false, 1>, a);
+    return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<(int)Epi::kF32, false, 1>, a);
+  }
+  if (gath) return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<(int)Epi::kSwiGLU, true, 0>, a);
+  if (p.epi == Epi::kSwiGLU) return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<(int)Epi::kSwiGLU, false, 0>, a);
+  if (p.epi == Epi::kF32) return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<(int)Epi::kF32, false, 0>, a);
+  return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<(int)Epi::kBf16, false, 0>, a);
 }
 
 }  // namespace moe

@@ -107,19 +107,22 @@ int gemm_prepare_gather(GemmPlan &p, const uint16_t *x, long x_rows, const int32
                         const uint16_t *W1, int G, int I, int H, const int32_t *group_end,
                         long max_rows, void *h, int32_t *status);
 cudaError_t launch_gemm(const GemmPlan &p, const Launch &l);
-// E4M3 operands A [a_rows, K], B [G * b_rows, K] (uint8 codes), one-CTA kernel,
-// SwiGLU (E4M3 h out) or fp32 epilogue; K % 128 == 0.  Set wscale / ascale /
-// oscale on the plan afterwards.
+// E4M3 operands A [a_rows, K], B [G * b_rows, K] (uint8 codes), SwiGLU (E4M3
+// h out) or fp32 epilogue; K % 128 == 0.  The CTA-pair kernel where the shape
+// allows it and allow_pair is set, else the one-CTA kernel.  Set wscale /
+// ascale / oscale on the plan afterwards.
 int gemm_prepare_e4m3(GemmPlan &p, Epi epi, const uint8_t *A, long a_rows, const uint8_t *B, int G,
                       int b_rows, int K, int n_out, const int32_t *group_end, long max_rows,
-                      void *out, int32_t *status);
+                      void *out, int32_t *status, bool allow_pair = true);
 
 // CTA-pair form (gemm2sm.cu)
 size_t pair_gemm_smem(Epi epi, int G);
 int pair_gemm_encode_extra(GemmPlan &p, const uint16_t *A, long a_rows, const uint16_t *B,
                            long b_rows_total, int K);
+// E4M3: all of the pair kernel's tensor maps from uint8 operands.
+int pair_gemm_encode_u8(GemmPlan &p, const uint8_t *A, long a_rows, const uint8_t *B, long b_rows_total, int K);
 bool pair_gemm_supported(Epi epi, int n_out);
-cudaError_t pair_gemm_configure(Epi epi, size_t smem);
+cudaError_t pair_gemm_configure(Epi epi, size_t smem, int q = 0);
 cudaError_t launch_pair_gemm(const GemmPlan &p, const Launch &l);
 
 // Grouped GEMM backward (gemm_bwd.cu): dgrad dX = G . W[g] (W in place) and

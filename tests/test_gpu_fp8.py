@@ -59,11 +59,12 @@ def check_e4m3_close(got, want, what):
     assert frac >= 0.999, f"{what}: only {frac:.5f} of the codes equal"
 
 
-def _plan(wl, fw, clamp=None):
+def _plan(wl, fw, clamp=None, one_cta=False):
     d = dict(x=wl.x.to(DEV), logits=wl.logits.to(DEV))
     e4 = dict(w1_scale=fw.s1.to(DEV), w2_scale=fw.s2.to(DEV), x_scale=fw.a1, h_scale=fw.a2)
     return moe.MoEPlan(d["x"], fw.w1q.to(DEV), fw.w2q.to(DEV), wl.E, wl.top_k, logits=d["logits"], e4m3=e4,
-                       clamp_limit=None if clamp is None else torch.from_numpy(clamp).to(DEV))
+                       clamp_limit=None if clamp is None else torch.from_numpy(clamp).to(DEV),
+                       one_cta_gemm=one_cta)
 
 
 @pytest.mark.parametrize("si", range(len(SHAPES)))
@@ -99,16 +100,18 @@ def test_e4m3_gather_and_stages(si):
     check_bf16_close(W.bf16_bits(out), want, f"E4M3 FC2 + finalize shape {si}")
 
 
+@pytest.mark.parametrize("one_cta", [False, True])
 @pytest.mark.parametrize("clamped", [False, True])
 @pytest.mark.parametrize("si", range(len(SHAPES)))
-def test_e4m3_layer_end_to_end(si, clamped):
+def test_e4m3_layer_end_to_end(si, clamped, one_cta):
+    """CTA-pair GEMMs where the shape allows them (the default), and the one-CTA kernel."""
     T, H, I, E, k = SHAPES[si]
     wl, fw, ids, w = _case(T, H, I, E, k, 70 + si)
     clamp = None
     if clamped:
         clamp = np.random.default_rng(si).uniform(0.3, 2.0, size=E).astype(np.float32)
         clamp[0] = np.inf
-    plan = _plan(wl, fw, clamp)
+    plan = _plan(wl, fw, clamp, one_cta)
     out = plan.launch().clone()
     torch.cuda.synchronize()
     assert int(plan.status.item()) == 0
