@@ -17,8 +17,9 @@
 // flashinfer.experimental.cake_stepfun_moe, opening paragraph): a k-block is
 // 128 codes (still one 128-byte swizzled row), the MMA is kind::f8f6f4 with
 // K = 32, the accumulator is dequantised by ascale * wscale[group], and the
-// SwiGLU epilogue writes E4M3 h = e4m3(h / oscale) (the requantisation
-// between FC1 and FC2).
+// SwiGLU epilogue writes E4M3 h = e4m3(h * RN(1 / oscale)) (the
+// requantisation between FC1 and FC2; the product is within one fp32 ulp of
+// the quotient h / oscale).
 //
 // CTA organisation (192 threads, one CTA per SM, persistent):
 //   warp 0      TMA producer: one thread streams A and B k-blocks into a
@@ -300,6 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                                                orow * args.n_out + (long)c.n * (BN / 2));
         const float lim = step_limit(args.clamp, c.g);
         const float sc = __fmul_rn(args.ascale, __ldg(args.wscale + c.g));
+        const float inv = __frcp_rn(args.oscale);  // h / h_scale as h times RN(1 / h_scale)
 #pragma unroll 1
         for (int col = 0; col < BN / 2; col += 32) {
           uint32_t u[32], g[32];
@@ -314,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             for (int q = 0; q < 4; ++q) {
               const float uu = __fmul_rn(__uint_as_float(u[4 * i + q]), sc);
               const float gg = __fmul_rn(__uint_as_float(g[4 * i + q]), sc);
-              hv[q] = __fdiv_rn(swiglu_step(gg, uu, lim), args.oscale);
+              hv[q] = __fmul_rn(swiglu_step(gg, uu, lim), inv);
             }
             packed[i] = e4m3x2(hv[0], hv[1]) | (e4m3x2(hv[2], hv[3]) << 16);
           }
