@@ -66,11 +66,17 @@ constexpr int BK = 64;  // k-block: one 128-byte-wide TMA box, four K = 16 MMAs
 constexpr int KH = 2;
 // warps: 0 token producer, 1 TMEM owner + MMA issuer, 2..5 epilogue (TMEM
 // lane quarters warp % 4), 6 weight producer; in gather mode warps 7..9 copy
-// the token rows (one ring slot each) and warp 0 only drains the ring.
+// the token rows (one ring slot each) and warp 0 only drains the ring.  With
+// E4M3 operands warps 7..10 are a second epilogue group: they take the upper
+// half of a SwiGLU main tile's h columns (the requantising epilogue would
+// otherwise outlast the tile's E4M3 MMAs) and only release the accumulator
+// of the other tiles.
 constexpr int kThreads = 224;
 constexpr int kWeightWarp = 6;
 constexpr int kGatherWarp0 = 7;
 constexpr int kThreadsGather = 320;
+constexpr int kEpiWarp1 = 7;
+constexpr int kThreadsQ = 352;
 constexpr int A_BYTES = BM * BK * 2;        // one k-block of the M-side operand
 constexpr int B_BYTES = (BN / 2) * BK * 2;  // one k-block of this CTA's half of the N side
 constexpr int A_STAGE = KH * A_BYTES;
@@ -119,6 +125,20 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// The second epilogue group's own barrier (E4M3): ORs a flag across its four warps.
+__device__ __forceinline__ bool epi1_bar_any(bool flag) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, 3, 128, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)flag)
+      : "memory");
+  return r != 0;
+}
 
 // Barrier over the four epilogue warps of this CTA that ORs a flag across them.
 __device__ __forceinline__ bool epi_bar_any(bool flag) {
@@ -177,6 +197,42 @@ __device__ __forceinline__ PairTile decode_pair_tile(int t, const int *tile_star
   return c;
 }
 
+// E4M3 SwiGLU main tile, h columns [col_lo, col_hi) of this thread's token
+// row: u and g dequantised by ascale * wscale[g], SwiGLU(Step), h requantised
+// as h times RN(1 / h_scale).
+template <int BNT>
+__device__ __forceinline__ void epi_swiglu_e4m3(const PairArgs &args, uint32_t taddr, long orow, bool row_ok,
+                                                int g, int n_blk, int col_lo, int col_hi) {
+  uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(args.out) + orow * args.n_out +
+                                         (long)n_blk * (BNT / 2));
+  const float lim = step_limit(args.clamp, g);
+  const float sc = __fmul_rn(args.ascale, __ldg(args.wscale + g));
+  const float inv = __frcp_rn(args.oscale);  // h / h_scale as h times RN(1 / h_scale)
+#pragma unroll 1
+  for (int col = col_lo; col < col_hi; col += 32) {
+    uint32_t u[32], gv[32];
+    tmem_ld_32x32b_x32(taddr + col, u);
+    tmem_ld_32x32b_x32(taddr + BNT / 2 + col, gv);
+    tmem_ld_wait();
+    uint32_t packed[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float hv[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float uu = __fmul_rn(__uint_as_float(u[4 * i + q]), sc);
+        const float gg = __fmul_rn(__uint_as_float(gv[4 * i + q]), sc);
+        hv[q] = __fmul_rn(swiglu_step(gg, uu, lim), inv);
+      }
+      packed[i] = e4m3x2(hv[0], hv[1]) | (e4m3x2(hv[2], hv[3]) << 16);
+    }
+    if (row_ok) {
+      dst[col / 16] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+      dst[col / 16 + 1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+    }
+  }
+}
+
 // This CTA's operand boxes for a tile: the token box (rows tok_row ..
 // tok_row + tok_rows) and the weight box(es), and the bytes both bring per
 // k-block.
@@ -218,7 +274,7 @@ __device__ __forceinline__ PairOperands pair_operands(const PairTile &c, uint32_
 }
 
 template <int EPI, bool GATH, int Q>
-__global__ void __launch_bounds__(GATH ? kThreadsGather : kThreads, 1)
+__global__ void __launch_bounds__(GATH ? kThreadsGather : (Q ? kThreadsQ : kThreads), 1)
     pair_gemm_kernel(const __grid_constant__ PairArgs args) {
   static_assert(!Q || (!GATH && EPI != (int)Epi::kBf16), "E4M3: FC1 and FC2 epilogues, token rows by TMA");
   constexpr int KE = Q ? 128 : BK;  // elements per k-block (128 bytes of a row either way)
@@ -259,7 +315,7 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 8);  // 4 epilogue warps x 2 CTAs
+      mbar_init(tempty_bar(a), Q ? 16 : 8);  // 4 (E4M3: 8) epilogue warps x 2 CTAs
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -450,35 +506,8 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : kThreads, 1)
         const bool row_ok = r_in_tile < valid;
         const long orow = (long)row0 + r_in_tile;
         if (kSwiGLU && Q) {
-          // E4M3: u, g dequantised by ascale * wscale[g], SwiGLU(Step), h requantised
-          uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(args.out) + orow * args.n_out +
-                                                 (long)c.n * (BN / 2));
-          const float lim = step_limit(args.clamp, c.g);
-          const float sc = __fmul_rn(args.ascale, __ldg(args.wscale + c.g));
-          const float inv = __frcp_rn(args.oscale);  // h / h_scale as h times RN(1 / h_scale)
-#pragma unroll 1
-          for (int col = 0; col < BN / 2; col += 32) {
-            uint32_t u[32], g[32];
-            tmem_ld_32x32b_x32(taddr + col, u);
-            tmem_ld_32x32b_x32(taddr + BN / 2 + col, g);
-            tmem_ld_wait();
-            uint32_t packed[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              float hv[4];
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const float uu = __fmul_rn(__uint_as_float(u[4 * i + q]), sc);
-                const float gg = __fmul_rn(__uint_as_float(g[4 * i + q]), sc);
-                hv[q] = __fmul_rn(swiglu_step(gg, uu, lim), inv);
-              }
-              packed[i] = e4m3x2(hv[0], hv[1]) | (e4m3x2(hv[2], hv[3]) << 16);
-            }
-            if (row_ok) {
-              dst[col / 16] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-              dst[col / 16 + 1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-            }
-          }
+          // E4M3: the lower half of the h columns (the second group takes the upper half)
+          epi_swiglu_e4m3<BN>(args, taddr, orow, row_ok, c.g, c.n, 0, BN / 4);
         } else if (kSwiGLU) {
           uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(args.out) +
                                                  orow * args.n_out + (long)c.n * (BN / 2));
@@ -639,6 +668,30 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : kThreads, 1)
             }
           }
         }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acc ? leader_tempty1 : leader_tempty0);
+    }
+  } else if (Q && warp >= kEpiWarp1 && warp < kEpiWarp1 + 4) {
+    // ------------------------------------------------ second epilogue group (E4M3) --
+    const int quarter = warp & 3;
+    const int r_in_tile = quarter * 32 + lane;
+    const uint32_t leader_tempty0 = mapa_shared(tempty_bar(0), 0);
+    const uint32_t leader_tempty1 = mapa_shared(tempty_bar(1), 0);
+    int tc = 0;
+    for (int t = cluster; t < total; t += nclusters, ++tc) {
+      const PairTile c = decode_pair_tile(t, tile_start, gend, G, args.n_tiles, args.m_major, args.tail_max);
+      const int acc = tc & 1;
+      const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
+      const bool got = mbar_wait(tfull_bar(acc), aph, abort_flag, args.status, args.wait_ns);
+      if (epi1_bar_any(!got)) break;  // all four warps of the group stop together
+      tc_fence_after();
+      if (kSwiGLU && !c.tail) {
+        const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+        const int row0 = c.gstart + (2 * c.mp + (int)rank) * BM;
+        const int valid = gend[c.g] - row0;
+        epi_swiglu_e4m3<BN>(args, taddr, (long)row0 + r_in_tile, r_in_tile < valid, c.g, c.n, BN / 4, BN / 2);
       }
       tc_fence_before();
       __syncwarp();
@@ -859,7 +912,7 @@ cudaError_t launch_pair_gemm(const GemmPlan &p, const Launch &l) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.grid);
   const bool gath = p.gather_k > 0 && p.epi == Epi::kSwiGLU;
-  cfg.blockDim = dim3(gath ? kThreadsGather : kThreads);
+  cfg.blockDim = dim3(gath ? kThreadsGather : (p.q ? kThreadsQ : kThreads));
   cfg.dynamicSmemBytes = p.smem;
   cfg.stream = l.stream;
   cudaLaunchAttribute attr[2];
