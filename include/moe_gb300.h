@@ -196,8 +196,10 @@ MOE_API int moe_fc1_swiglu_step(const moe_bf16 *xp, const moe_bf16 *w1, const fl
                                 int num_local, moe_bf16 *h, void *stream);
 
 /* ---- S4 / S5 with E4M3 operands (the fp8 per-tensor family, MOE_WEIGHTS_E4M3) --------
- * moe_fc1_swiglu_e4m3: hq[p] = e4m3( swiglu_step(g * sc, u * sc, limit[i]) / h_scale )
- *   with u, g = xq[p] . W1q[i, up / gate rows]^T (fp32) and sc = x_scale * w1_scale[i];
+ * moe_fc1_swiglu_e4m3: hq[p] = e4m3( swiglu_step(g * sc, u * sc, limit[i]) * RN(1 / h_scale) )
+ *   with u, g = xq[p] . W1q[i, up / gate rows]^T (fp32) and sc = x_scale * w1_scale[i]
+ *   (the product with the correctly rounded reciprocal is within one fp32 ulp of the
+ *   quotient by h_scale);
  *   xq [max_rows, H], w1q [L, 2I, H], hq [max_rows, I] E4M3 codes (uint8);
  *   clamp_limit [L] or NULL (plain SwiGLU).
  * moe_fc2_e4m3: y[p] = (hq[p] . W2q[i]^T) * (h_scale * w2_scale[i]), fp32;
