@@ -32,9 +32,9 @@
 // epilogue of one tile overlaps the main loop of the next.  wgrad's output
 // (dW, [E, N, K], the larger part of its traffic) leaves the epilogue as
 // 128-byte-wide column chunks of the tile staged in 128-byte-swizzled shared
-// memory and written by TMA bulk stores through a 3-D [E, N, K] tensor map,
-// which clips a partial tile at N instead of writing into the next expert's
-// rows.  Every wait is bounded (the plan's wait limit); a timeout raises
+// memory (four chunks in rotation) and written by TMA bulk stores through a
+// 3-D [E, N, K] tensor map, which clips a partial tile at N instead of
+// writing into the next expert's rows.  Every wait is bounded (the plan's wait limit); a timeout raises
 // MOE_DEV_TIMEOUT.
 #include <cuda_bf16.h>
 
@@ -47,7 +47,6 @@ namespace {
 constexpr int BM = 128;   // rows of the output tile (dX rows / dW rows)
 constexpr int BN = 256;   // columns of the output tile
 constexpr int BK = 64;    // contraction per k-block
-constexpr int STAGES = 4;
 constexpr int kThreads = 224;
 constexpr int kEpiThreads = 128;
 constexpr int kMaskWarp = 6;
@@ -55,15 +54,25 @@ constexpr int A_BYTES = BM * BK * 2;          // 16 KB: two 8 KB chunks when MN-
 constexpr int B_BYTES = BN * BK * 2;          // 32 KB: four 8 KB chunks
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int CHUNK = 64 * BK * 2;            // one 64 x 64 box: 8 KB
-constexpr int NBARS = 3 * STAGES + 5;         // full, ready, empty, tfull[2], tempty[2], drain
-constexpr int STG_OFF = STAGES * STAGE_BYTES;  // wgrad: one 128-row x 128-byte staging chunk
-constexpr int STG_BYTES = BM * 128;
-constexpr int BAR_OFF = STG_OFF + STG_BYTES;
-constexpr int MISC_OFF = BAR_OFF + NBARS * 8; // tmem base, abort flag
-constexpr int TAB_OFF = MISC_OFF + 16;
+constexpr int STG_BYTES = BM * 128;           // one 128-row x 128-byte staging chunk
 constexpr uint32_t TMEM_COLS = 2 * BN;
 
 enum Mode : int { kDgrad = 0, kWgradF32 = 1, kWgradBf16 = 2 };
+
+// Shared memory per mode.  wgrad's contraction over one group is short (a few
+// k-blocks per tile) and its output is the bulk of its traffic, so it trades a
+// ring stage for four staging chunks: while one chunk of a tile is written
+// the TMA stores of the previous three are still reading theirs.
+template <int MODE>
+struct BwdLayout {
+  static constexpr int STAGES = MODE == kDgrad ? 4 : 3;
+  static constexpr int NSTG = MODE == kDgrad ? 0 : 4;
+  static constexpr int NBARS = 3 * STAGES + 5;   // full, ready, empty, tfull[2], tempty[2], drain
+  static constexpr int STG_OFF = STAGES * STAGE_BYTES;
+  static constexpr int BAR_OFF = STG_OFF + NSTG * STG_BYTES;
+  static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;  // tmem base, abort flag
+  static constexpr int TAB_OFF = MISC_OFF + 16;
+};
 
 struct BwdArgs {
   CUtensorMap map_a;   // dgrad: G [sum_m, N] box {64, 128}; wgrad: G [sum_m, N] box {64, 64}
@@ -151,6 +160,10 @@ __device__ __forceinline__ Tile decode(int t, const int *tile_start, int G, cons
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1) grouped_bwd_kernel(const __grid_constant__ BwdArgs a) {
   constexpr bool kW = MODE != kDgrad;
+  using Lay = BwdLayout<MODE>;
+  constexpr int STAGES = Lay::STAGES;
+  constexpr int BAR_OFF = Lay::BAR_OFF, MISC_OFF = Lay::MISC_OFF, TAB_OFF = Lay::TAB_OFF;
+  constexpr int NSTG = Lay::NSTG > 0 ? Lay::NSTG : 1;  // wgrad's staging chunks (dgrad has none)
   extern __shared__ unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -352,6 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_bwd_kernel(const __grid_c
     const int quarter = warp & 3;
     const int r_in_tile = quarter * 32 + lane;
     int tc = 0;
+    int n_stg = 0;  // wgrad: staging chunks used so far (the ring position)
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++tc) {
       const Tile c = decode<MODE>(t, tile_start, G, a);
       const int acc = tc & 1;
@@ -386,9 +400,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_bwd_kernel(const __grid_c
         constexpr int CW = MODE == kWgradF32 ? 32 : 64;  // columns per chunk
         const bool empty = gend[c.g] <= gstart(c.g);
         const int etid = threadIdx.x - 64;
-        const uint32_t row_addr = smem_base + STG_OFF + r_in_tile * 128;
 #pragma unroll 1
-        for (int col = 0; col < BN && col0 + col < a.K; col += CW) {
+        for (int col = 0; col < BN && col0 + col < a.K; col += CW, ++n_stg) {
+          const uint32_t stg = smem_base + Lay::STG_OFF + (uint32_t)((n_stg % NSTG) * STG_BYTES);
+          const uint32_t row_addr = stg + r_in_tile * 128;
           uint32_t v[32];  // this row's 128 bytes of the chunk
           if (empty) {
 #pragma unroll
@@ -407,7 +422,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_bwd_kernel(const __grid_c
               v[16 + j] = pack2(__uint_as_float(r1[2 * j]), __uint_as_float(r1[2 * j + 1]));
             }
           }
-          if (etid == 0) bulk_wait_read<0>();  // the previous store has read the staging chunk
+          // the store that used this staging chunk NSTG chunks ago has read it
+          if (etid == 0) bulk_wait_read<NSTG - 1>();
           epi_bar();
 #pragma unroll
           for (int q = 0; q < 8; ++q)
@@ -418,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_bwd_kernel(const __grid_c
           fence_proxy_async_smem();
           epi_bar();
           if (etid == 0) {
-            tma_store_3d(&a.map_o, smem_base + STG_OFF, col0 + col, c.m * BM, c.g);
+            tma_store_3d(&a.map_o, stg, col0 + col, c.m * BM, c.g);
             bulk_commit();
           }
         }
@@ -532,7 +548,8 @@ int bwd_prepare(BwdPlan &p, bool wgrad, bool out_f32, const uint16_t *G, const u
     if (rc == MOE_OK) rc = encode(&p.map_b, B, (long)E * N, K, 64);  // W in place
   }
   if (rc != MOE_OK) return rc;
-  p.smem = 1024 + TAB_OFF + (size_t)(2 * E + 2) * 4;
+  const int tab_off = wgrad ? BwdLayout<kWgradF32>::TAB_OFF : BwdLayout<kDgrad>::TAB_OFF;
+  p.smem = 1024 + tab_off + (size_t)(2 * E + 2) * 4;
   const long n_tiles = (K + BN - 1) / BN;
   const long tiles = wgrad ? (long)E * ((N + BM - 1) / BM) * n_tiles
                            : ((sum_m + BM - 1) / BM + E) * n_tiles;
