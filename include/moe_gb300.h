@@ -183,7 +183,7 @@ MOE_API int moe_fc1_swiglu_gathered(const moe_bf16 *x, const int32_t *perm_to_ex
  * moe_fc1_swiglu with SwiGLUStep(limit): GEMM1's outputs are clamped before
  * the activation, g' = min(g, limit[i]), u' = min(max(u, -limit[i]), limit[i]),
  * h[p] = bf16_rne(silu(g') * u') for permuted rows p of local expert i (the
- * StepFun activation "SwiGLUStep(limit) with a per-expert clamp limit",
+ * StepFun SwiGLUStep activation with one clamp limit per expert,
  * flashinfer.experimental.cake_stepfun_moe, opening paragraph; the per-expert
  * gemm1_clamp_limit of Unified MoE API opt-in).  This clamp is the library's
  * reading: the page names the activation and the per-expert limit only.

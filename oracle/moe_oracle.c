@@ -499,7 +499,8 @@ void oracle_grouped_gemm_wgrad_rows(const uint16_t *G, const uint16_t *X,
  * where off_s = F_0 + .. + F_{s-1} and y has ld_y >= sum F_s floats per row.
  * A token without pairs gets zeros.  A pair whose token, expert or LoRA index
  * is out of range is dropped (its shrink rows are zero) and the call returns
- * ORACLE_BAD_EXPERT ("out-of-range routing indices" are invalid inputs). */
+ * ORACLE_BAD_EXPERT (the page treats routing indices out of range as invalid
+ * inputs). */
 int oracle_bgmv(const uint16_t *x, int T, int H, const uint16_t *const *lora_a,
                 const uint16_t *const *lora_b, int S, const int *feat_out,
                 int num_loras, int E, int R, const int32_t *tok,

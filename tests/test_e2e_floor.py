@@ -1,7 +1,7 @@
 """Pins of the end-to-end acceptance floor (CPU only).
 
-the benchmark spec asks, end to end, for at least 99.9% of the outputs within 2 bf16
-ulp of the oracle.  The layer rounds h to bf16 between the two GEMMs, so any
+The acceptance rule asks, end to end, for at least 99.9% of the outputs within
+2 bf16 ulp of the oracle.  The layer rounds h to bf16 between the two GEMMs, so any
 fp32 difference that moves an h value across a rounding boundary shows up
 again in every output that h value feeds, and outputs near zero have tiny
 ulps.  These tests pin, on the CPU and without the GPU path:

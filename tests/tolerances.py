@@ -110,8 +110,8 @@ def floor_margin(frac: float, n: int) -> float:
 # The E4M3 family requantises h to 3 mantissa bits instead of bf16's 8, so one
 # rounding flip of h moves the outputs it feeds 2^5 = 32 times further than in
 # the bf16 family: w * h_scale * w2_scale * |W2| * 2^-3 |h|, about 1-1.5 % of
-# rms(out) per flip at the test shapes.  North_star states no bound for this
-# family; the max term below allows a few coinciding flips (4 % of rms) while a
+# rms(out) per flip at the test shapes.  The acceptance rule states no bound
+# for this family; the max term below allows a few coinciding flips (4 % of rms) while a
 # wrong scale, a dropped term or a wrong expert still moves outputs by 10 % of
 # rms or more.  The 2-ulp fraction keeps its accumulation-model floor.
 RMS_FRAC_E4M3 = 4e-2
