@@ -362,7 +362,8 @@ def run_ours(args, world, rank, local):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     opts = dict(decode_chain=True if args.decode_chain else (False if args.decode_separate else None),
                 one_cta_gemm=args.one_cta_gemm, fused_gather=args.fused_gather,
-                decode_one_launch=args.decode_one_launch, no_tail_tiles=args.no_tail_tiles)
+                decode_one_launch=args.decode_one_launch, no_tail_tiles=args.no_tail_tiles,
+                small_group_kernel={"auto": None, "on": True, "off": False}[args.small_group_kernel])
     # one plan per copy of the expert banks; the steps rotate over them
     banks = weight_banks(wl)
     fw = None
@@ -869,6 +870,8 @@ def main():
     ap.add_argument("--decode-separate", action="store_true",
                     help="decode path: always the five separate kernels (comparison)")
     ap.add_argument("--one-cta-gemm", action="store_true", help="grouped path: one-CTA GEMMs (comparison)")
+    ap.add_argument("--small-group-kernel", default="auto", choices=["auto", "on", "off"],
+                    help="grouped path: groups of at most 64 rows in their own kernel beside the CTA-pair GEMMs")
     ap.add_argument("--fused-gather", action="store_true",
                     help="grouped path: FC1 copies its token rows from x (no gather kernel)")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")

@@ -393,6 +393,18 @@ MOE_API int moe_forward(const moe_bf16 *x, const float *logits, const int32_t *t
                                      group computed and not stored) instead of a
                                      swap-AB tail tile (weights on the MMA's M
                                      side, the group's rows on N) */
+#define MOE_PLAN_NO_SMALL_GROUP_KERNEL 256 /* grouped path, CTA-pair GEMMs: the
+                                             pair kernel takes every group.
+                                             Without this flag, when the plan's
+                                             routes average at most 512 per local
+                                             expert, each GEMM runs as two kernels
+                                             at once: a one-CTA kernel on a few
+                                             SMs takes the groups of at most 64
+                                             rows (weights on the MMA's N side),
+                                             the pair kernel the others; both
+                                             claim tiles at run time. */
+#define MOE_PLAN_SMALL_GROUP_KERNEL 512 /* grouped path, CTA-pair GEMMs: the two
+                                          kernels whatever the average group */
 #define MOE_PLAN_TEST_UNREACHABLE_WAIT 64 /* test hook, not for production: the
                                              decode chain in one launch seeds its
                                              per-expert counts of finished FC1 tiles

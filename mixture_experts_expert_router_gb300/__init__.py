@@ -41,6 +41,8 @@ PLAN_FUSED_GATHER = 16
 PLAN_DECODE_ONE_LAUNCH = 32
 PLAN_TEST_UNREACHABLE_WAIT = 64
 PLAN_NO_TAIL_TILES = 128
+PLAN_NO_SMALL_GROUP_KERNEL = 256
+PLAN_SMALL_GROUP_KERNEL = 512
 WEIGHTS_BF16, WEIGHTS_E4M3 = 0, 1
 WAIT_LIMIT_MIN_NS, WAIT_LIMIT_MAX_NS = 1000, 600_000_000_000
 DEV_BAD_EXPERT, DEV_TIMEOUT = 1, 2
@@ -545,7 +547,8 @@ class MoEPlan:
                  local_offset: int = 0, out=None, workspace=None, status=None, path: int = PATH_AUTO,
                  stage_timing: bool = False, one_cta_gemm: bool = False, decode_chain: bool | None = None,
                  fused_gather: bool = False, decode_one_launch: bool = False,
-                 test_unreachable_wait: bool = False, clamp_limit=None, e4m3=None, no_tail_tiles: bool = False):
+                 test_unreachable_wait: bool = False, clamp_limit=None, e4m3=None, no_tail_tiles: bool = False,
+                 small_group_kernel: bool | None = None):
         """decode_chain: None lets the library choose the decode form (the
         chain in one launch for few routes, else five kernels), True forces
         the chain as two kernels, False the five separate kernels.
@@ -557,7 +560,10 @@ class MoEPlan:
         (None: plain SwiGLU).
         e4m3: the fp8 per-tensor weight family: w1 / w2 are uint8 E4M3 codes and
         e4m3 = dict(w1_scale=[L] fp32, w2_scale=[L] fp32, x_scale=float,
-        h_scale=float)."""
+        h_scale=float).
+        small_group_kernel: None lets the library decide whether the groups of
+        at most 64 rows run in their own kernel beside the CTA-pair GEMMs, True
+        forces it, False keeps every group in the pair kernel."""
         T, H, I, L, out = _layer_args(x, w1, w2, num_experts, top_k, logits, topk_ids, topk_w,
                                       local_offset, out, torch.uint8 if e4m3 is not None else torch.bfloat16)
         dev = x.device
@@ -589,7 +595,9 @@ class MoEPlan:
                   | (PLAN_FUSED_GATHER if fused_gather else 0)
                   | (PLAN_DECODE_ONE_LAUNCH if decode_one_launch else 0)
                   | (PLAN_TEST_UNREACHABLE_WAIT if test_unreachable_wait else 0)
-                  | (PLAN_NO_TAIL_TILES if no_tail_tiles else 0),
+                  | (PLAN_NO_TAIL_TILES if no_tail_tiles else 0)
+                  | (PLAN_SMALL_GROUP_KERNEL if small_group_kernel is True else 0)
+                  | (PLAN_NO_SMALL_GROUP_KERNEL if small_group_kernel is False else 0),
                   clamp_limit=_ptr(clamp_limit), **q)
         handle = ctypes.c_void_p()
         _check(library().moe_forward_prepare(ctypes.byref(d), ctypes.byref(handle)), "moe_forward_prepare")

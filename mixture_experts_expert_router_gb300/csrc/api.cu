@@ -46,8 +46,12 @@ int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct WsLayout {
-  size_t ids, w, m_indptr, p2e, e2p, sort_ws, xp, h, y, comb, done1, total;
+  size_t ids, w, m_indptr, p2e, e2p, sort_ws, xp, h, y, comb, done1, sched, total;
 };
+
+// Claim counters of the two grouped GEMMs when the small-group kernel runs
+// beside the CTA-pair kernel (four per GEMM), zeroed at the start of every launch.
+constexpr int kSchedInts = 8;
 
 WsLayout ws_layout(long T, int H, int I, int k, int L) {
   WsLayout o;
@@ -69,6 +73,7 @@ WsLayout ws_layout(long T, int H, int I, int k, int L) {
   o.y = take(R * (size_t)H * 4);
   o.comb = take(chain_comb_ints((int)T, H) * 4);
   o.done1 = take(((size_t)L + 1) * 4);
+  o.sched = take(kSchedInts * 4);
   o.total = off;
   return o;
 }
@@ -87,6 +92,14 @@ const char *kStageNames[kNumStages] = {"route", "sort", "gather", "fc1_swiglu", 
 constexpr int kTimingRing = 512;
 // Token count up to which MOE_PATH_AUTO picks the weight-streaming decode path.
 constexpr int kDecodeMaxTokens = 64;
+// Small-group kernel beside the CTA-pair GEMMs: the CTAs it takes, and the
+// routes per local expert up to which a plan uses it without a flag (above,
+// groups of at most 64 rows are rare).  With 24 CTAs streaming weights at
+// about 100 GB/s each, the small groups of the Zipf-routed 256-expert
+// workload end about when the pair kernel's tiles do; claims at run time
+// even out any other mix.
+constexpr int kSmallGroupCtas = 24;
+constexpr long kSmallGroupMeanRows = 512;
 
 }  // namespace
 }  // namespace moe
@@ -110,6 +123,7 @@ struct moe_plan {
   bool unreachable_wait;  // test hook MOE_PLAN_TEST_UNREACHABLE_WAIT
   bool fused_gather;    // grouped path: FC1 gathers its rows itself
   bool e4m3;            // E4M3 weight family (one-CTA kernels, quantising gather)
+  int32_t *sched;       // grouped path beside the small-group kernel: claim counters (else null)
   bool timing;
   cudaEvent_t (*ev)[kNumStages + 1];
   long n_recorded;
@@ -133,7 +147,7 @@ const char *moe_status_string(int code) {
   }
 }
 
-int moe_abi_version(void) { return 103; }
+int moe_abi_version(void) { return 104; }
 
 int moe_route(const float *logits, int T, int E, int top_k, int32_t *topk_ids, float *topk_w,
               void *stream) {
@@ -637,6 +651,16 @@ int moe_forward_prepare(const moe_forward_desc *desc, moe_plan **plan_out) {
                           p->m_indptr + 1, p->R, p->y, d.status, pair);
       if (d.flags & MOE_PLAN_NO_TAIL_TILES) p->fc1.tail_max = p->fc2.tail_max = 0;
     }
+    if (rc == MOE_OK && p->path == MOE_PATH_GROUPED && !p->fused_gather && p->fc1.pair &&
+        p->fc2.pair && (d.flags & MOE_PLAN_NO_SMALL_GROUP_KERNEL) == 0 &&
+        ((d.flags & MOE_PLAN_SMALL_GROUP_KERNEL) != 0 || p->R <= kSmallGroupMeanRows * d.num_local) &&
+        p->fc1.tail_max >= small_gemm_max_rows()) {
+      const int ctas = device_sm_count() >= 4 * kSmallGroupCtas ? kSmallGroupCtas : 2;
+      int32_t *sched = reinterpret_cast<int32_t *>(ws + lay.sched);
+      rc = gemm_attach_small(p->fc1, sched, ctas);
+      if (rc == MOE_OK) rc = gemm_attach_small(p->fc2, sched + 4, ctas);
+      if (rc == MOE_OK) p->sched = sched;
+    }
     if (rc != MOE_OK) {
       delete p;
       return rc;
@@ -677,6 +701,9 @@ int moe_plan_launch(moe_plan *p, void *stream) {
   if (d.status && !chain_clear && cudaMemsetAsync(d.status, 0, sizeof(int32_t), s) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (d.T == 0) return MOE_OK;
+  // The GEMMs' claim counters (the small-group kernel beside the pair kernel).
+  if (p->sched && cudaMemsetAsync(p->sched, 0, kSchedInts * sizeof(int32_t), s) != cudaSuccess)
+    return MOE_ERR_CUDA;
   Launch l;
   l.stream = s;
   l.pdl = !p->timing;
@@ -794,6 +821,7 @@ int moe_plan_kernels_per_launch(const moe_plan *p) {
   int n = p->logits_mode ? 1 : 0;                       // route
   n += p->R <= kSortSingleMax ? 1 : 3;                  // sort
   n += (p->fused_gather ? 0 : 1) + 1 + 1 + 1;           // gather, fc1, fc2, finalize
+  if (p->sched) n += 2;                                  // small-group kernels beside fc1, fc2
   return n;
 }
 

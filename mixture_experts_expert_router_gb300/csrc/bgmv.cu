@@ -603,7 +603,7 @@ template <int R>
 static cudaError_t launch_gshrink(int G, int S, const Launch &l, const BgmvArgs &a) {
   constexpr size_t bytes = GShrinkSmem<R>::BYTES;
   static const cudaError_t attr =
-      cudaFuncSetAttribute(bgmv_gshrink_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+      raise_smem_limit(bgmv_gshrink_kernel<R>, bytes);
   if (attr != cudaSuccess) return attr;
   return launch_kernel(bgmv_gshrink_kernel<R>, dim3(G, S), dim3(kGsThreads), bytes, l, a);
 }

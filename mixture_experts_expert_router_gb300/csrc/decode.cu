@@ -429,8 +429,7 @@ size_t inst_smem(int G) {
 
 template <int BNT, bool SW>
 cudaError_t inst_configure(size_t smem) {
-  return cudaFuncSetAttribute(swapab_kernel<BNT, SW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)smem);
+  return raise_smem_limit(swapab_kernel<BNT, SW>, smem);
 }
 
 template <int BNT, bool SW>

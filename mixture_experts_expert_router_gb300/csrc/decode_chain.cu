@@ -690,10 +690,9 @@ int encode(CUtensorMap *map, const void *ptr, long rows, int K, int box_rows) {
 
 template <int BNT>
 cudaError_t configure(size_t smem) {
-  constexpr auto kAttr = cudaFuncAttributeMaxDynamicSharedMemorySize;
-  cudaError_t e = cudaFuncSetAttribute(chain_kernel<BNT, kModeFc1>, kAttr, (int)smem);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(chain_kernel<BNT, kModeFc2>, kAttr, (int)smem);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(chain_kernel<BNT, kModeBoth>, kAttr, (int)smem);
+  cudaError_t e = raise_smem_limit(chain_kernel<BNT, kModeFc1>, smem);
+  if (e == cudaSuccess) e = raise_smem_limit(chain_kernel<BNT, kModeFc2>, smem);
+  if (e == cudaSuccess) e = raise_smem_limit(chain_kernel<BNT, kModeBoth>, smem);
   return e;
 }
 

@@ -460,8 +460,7 @@ int encode_2d(CUtensorMap *map, const void *ptr, long rows, int K, int box_rows)
 
 template <int BN, int EPI, int Q = 0>
 cudaError_t configure_inst(const GemmPlan &p) {
-  return cudaFuncSetAttribute(grouped_gemm_kernel<BN, EPI, Q>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+  return raise_smem_limit(grouped_gemm_kernel<BN, EPI, Q>, p.smem);
 }
 
 template <int BN, int EPI, int Q = 0>
@@ -655,7 +654,27 @@ int gemm_prepare_gather(GemmPlan &p, const uint16_t *x, long x_rows, const int32
   return pair_gemm_encode_extra(p, x, x_rows, W1, (long)G * 2 * I, H);
 }
 
+int gemm_attach_small(GemmPlan &p, int32_t *sched, int ctas) {
+  if (!p.pair || p.gather_k > 0 || p.epi == Epi::kBf16 || !sched || ctas < 2 || ctas % 2 ||
+      p.tail_max < small_gemm_max_rows())
+    return MOE_ERR_SHAPE;
+  p.sched = sched;
+  p.side_ctas = ctas;
+  p.small_max = small_gemm_max_rows();
+  return small_gemm_configure(p.epi, p.q, small_gemm_smem(p.G)) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 cudaError_t launch_gemm(const GemmPlan &p, const Launch &l) {
+  if (p.pair && p.side_ctas > 0) {
+    // The small-group kernel first: the pair kernel launches once all of its
+    // CTAs are running (they signal dependents at once), so both hold SMs
+    // together; the pair kernel starts on that kernel's flag, not on a
+    // dependent-launch wait.
+    if (cudaError_t e = launch_small_gemm(p, l)) return e;
+    Launch behind = l;
+    behind.pdl = true;
+    return launch_pair_gemm(p, behind);
+  }
   if (p.pair) return launch_pair_gemm(p, l);
   if (p.q) {
     if (p.epi == Epi::kSwiGLU)

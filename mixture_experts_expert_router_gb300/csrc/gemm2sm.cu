@@ -85,15 +85,20 @@ constexpr int STG_BYTES = BM * 32 * 4;                 // fp32 store staging: 12
 
 // Shared-memory layout per epilogue kind (the fp32 form adds one store-staging
 // buffer).
+// Tiles claimed at run time (beside the small-group kernel) reach every role
+// of both CTAs through a queue of this many slots in each CTA.
+constexpr int kPairQD = 8;
+
 template <int EPI>
 struct PairLayout {
   static constexpr int STAGES = 3;
-  static constexpr int NBARS = 2 * STAGES + 5;
+  static constexpr int NBARS = 2 * STAGES + 5 + 2 * kPairQD;  // ring, accumulators, drain, queue
   static constexpr int STG_OFF = STAGES * STAGE_BYTES;
   static constexpr int BAR_OFF = STG_OFF + (EPI == (int)Epi::kF32 ? STG_BYTES : 0);
   static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
-  static constexpr int SG_OFF = MISC_OFF + 16;  // tail gate hand-off [16][64] fp32
-  static constexpr int TAB_OFF = SG_OFF + 16 * 64 * 4;
+  static constexpr int TQ_OFF = MISC_OFF + 16;  // tile queue [kPairQD]
+  static constexpr int SG_OFF = TQ_OFF + kPairQD * 4;  // tail gate hand-off [16][64] fp32
+  static constexpr int TAB_OFF = SG_OFF + 16 * 64 * 4;  // tile_start [G+1], gend [G], small groups [G]
 };
 constexpr uint32_t TMEM_COLS = 2 * BN;
 
@@ -117,6 +122,11 @@ struct PairArgs {
   long max_rows;
   int G, K, n_out, b_rows, n_tiles, m_major;
   int tail_max;               // remainders of up to this many rows run as swap-AB tail tiles (0: none)
+  // Beside the small-group kernel (null: static round-robin over all groups):
+  // [0] main-tile claims, [1] small-tile claims (shared with it), [2] its
+  // start flag, [3] its CTAs done.  Groups of 1..small_max rows are its tiles.
+  int32_t *sched;
+  int small_max, side_ctas;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -297,9 +307,17 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : (Q ? kThreadsQ : kThre
   const uint32_t drain_bar = bar_base + 8u * (2 * STAGES + 4);
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + MISC_OFF);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + MISC_OFF + 4);
+  volatile int *n_small_s = reinterpret_cast<volatile int *>(smem + MISC_OFF + 8);
+  volatile int *tq = reinterpret_cast<volatile int *>(smem + Lay::TQ_OFF);
   float *sg = reinterpret_cast<float *>(smem + SG_OFF);
   int *tile_start = reinterpret_cast<int *>(smem + TAB_OFF);
   int *gend = tile_start + (args.G + 1);
+  int *small_g = gend + args.G;
+  // Run-time tile claims (beside the small-group kernel): the leader's weight
+  // producer claims each tile and publishes it to both CTAs' queues.
+  const bool dyn = !GATH && args.sched != nullptr;
+  auto qfull_bar = [&](int j) { return bar_base + 8u * (2 * STAGES + 5 + j); };
+  auto qempty_bar = [&](int j) { return bar_base + 8u * (2 * STAGES + 5 + kPairQD + j); };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -318,6 +336,13 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : (Q ? kThreadsQ : kThre
       mbar_init(tempty_bar(a), Q ? 16 : 8);  // 4 (E4M3: 8) epilogue warps x 2 CTAs
     }
     mbar_init(drain_bar, 1);
+    // queue readers: token producer and epilogue warps of both CTAs, the MMA
+    // thread, the peer's weight producer
+    const uint32_t readers = 2u * (1u + 4u + (Q ? 4u : 0u)) + 2u;
+    for (int j = 0; j < kPairQD; ++j) {
+      mbar_init(qfull_bar(j), 1);
+      mbar_init(qempty_bar(j), readers);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -329,20 +354,36 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : (Q ? kThreadsQ : kThre
     tmem_alloc_pair(smem_u32(tmem_holder), TMEM_COLS);
     tmem_relinquish_pair();
   }
-  pdl_wait();
+  if (dyn) {
+    // Launched behind the small-group kernel, which sets the flag once the
+    // gather and the sort have finished (waiting for the whole previous grid
+    // here would wait for that kernel to end).
+    if (threadIdx.x == 0 && counter_wait(args.sched + 2, 1, abort_flag, args.status, args.wait_ns))
+      fence_proxy_async_global();  // the rows the flag releases are read by TMA
+    __syncthreads();
+  } else {
+    pdl_wait();
+  }
   for (int g = threadIdx.x; g < G; g += (int)blockDim.x) {
     long e = args.group_end[g];
     e = e < 0 ? 0 : (e > args.max_rows ? args.max_rows : e);
     gend[g] = (int)e;
   }
   __syncthreads();
-  if (warp == 0) {  // tile_start = prefix of per-group tile counts (per n-block)
-    int carry = 0;
+  if (warp == 0) {
+    // tile_start = prefix of per-group tile counts (per n-block); with claims
+    // at run time the groups of 1..small_max rows are listed apart (small_g)
+    int carry = 0, scarry = 0;
     if (lane == 0) tile_start[0] = 0;
     for (int base = 0; base < G; base += 32) {
       const int g = base + lane;
       int mp = 0;
-      if (g < G) mp = group_pairs(gend[g] - (g == 0 ? 0 : gend[g - 1]));
+      bool small = false;
+      if (g < G) {
+        const int cnt = gend[g] - (g == 0 ? 0 : gend[g - 1]);
+        small = dyn && cnt > 0 && cnt <= args.small_max;
+        mp = small ? 0 : group_pairs(cnt);
+      }
       int inc = mp;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -351,7 +392,11 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : (Q ? kThreadsQ : kThre
       }
       if (g < G) tile_start[g + 1] = carry + inc;
       carry += __shfl_sync(0xffffffffu, inc, 31);
+      const uint32_t m = __ballot_sync(0xffffffffu, small);
+      if (small) small_g[scarry + __popc(m & ((1u << lane) - 1u))] = g;
+      scarry += __popc(m);
     }
+    if (lane == 0) *n_small_s = scarry;
   }
   tc_fence_before();
   __syncthreads();
@@ -360,11 +405,43 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : (Q ? kThreadsQ : kThre
   pdl_launch_dependents();
 
   const uint32_t tmem_base = *tmem_holder;
-  const int total = tile_start[G] * args.n_tiles;
+  const bool dead = *abort_flag != 0;  // the start flag never came: no tiles
+  const int total = dead ? 0 : tile_start[G] * args.n_tiles;  // tiles numbered 0 .. total - 1 first
+  const int total_small = dead ? 0 : *n_small_s * args.n_tiles;  // then small-group tiles
   const int num_kb = args.K / KE;
   const int n_rounds = (num_kb + KH - 1) / KH;  // ring stages per tile
   const int cluster = blockIdx.x >> 1;
   const int nclusters = gridDim.x >> 1;
+
+  // Tile number -> coordinates: the main numbering, then (claims at run time
+  // only) the small groups' tiles, each a tail-only group.
+  auto tile_of = [&](int t) -> PairTile {
+    if (t < total) return decode_pair_tile(t, tile_start, gend, G, args.n_tiles, args.m_major, args.tail_max);
+    PairTile c;
+    const int s = t - total;
+    const int j = s / args.n_tiles;
+    c.n = s - j * args.n_tiles;
+    c.g = small_g[j];
+    c.mp = 0;
+    c.gstart = c.g == 0 ? 0 : gend[c.g - 1];
+    c.tail = gend[c.g] - c.gstart;
+    return c;
+  };
+  // The i-th tile of this cluster for one reader thread (-1: no more).
+  // Static: round-robin over the clusters.  Run time: the queue entry, whose
+  // slot the reader then releases on the leader's qempty barrier.
+  auto seq_tile = [&](int i) -> int {
+    if (!dyn) {
+      const int t = cluster + i * nclusters;
+      return t < total ? t : -1;
+    }
+    const int j = i % kPairQD;
+    if (!mbar_wait<true>(qfull_bar(j), (uint32_t)(i / kPairQD) & 1u, abort_flag, args.status, args.wait_ns))
+      return -1;
+    const int t = tq[j];
+    mbar_arrive_cluster(mapa_shared(qempty_bar(j), 0));
+    return t;
+  };
 
   if (warp == 0) {
     // --------------------------------------------------------- token producer --
@@ -374,12 +451,16 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : (Q ? kThreadsQ : kThre
     const uint64_t pol_first = policy_evict_first(), pol_last = policy_evict_last();
     int it = 0;
     bool ok = true;
-    for (int t = cluster; t < total && ok; t += nclusters) {
+    for (int i = 0; ok; ++i) {
+      int t = -1;
+      if (lane == 0) t = seq_tile(i);
+      t = __shfl_sync(0xffffffffu, t, 0);
+      if (t < 0) break;
       if (GATH) {
         it += n_rounds;
         continue;
       }
-      const PairTile c = decode_pair_tile(t, tile_start, gend, G, args.n_tiles, args.m_major, args.tail_max);
+      const PairTile c = tile_of(t);
       const uint64_t pol = (c.tail && c.mp == 0) ? pol_first : pol_last;
       const PairOperands o = pair_operands<kSwiGLU>(c, rank, args.b_rows);
       const CUtensorMap *tok_map = c.tail ? &args.map_t[o.tmap] : &args.map_a;
@@ -415,8 +496,55 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : (Q ? kThreadsQ : kThre
       const uint64_t pol_first = policy_evict_first(), pol_last = policy_evict_last();
       int it = 0;
       bool ok = true;
-      for (int t = cluster; t < total && ok; t += nclusters) {
-        const PairTile c = decode_pair_tile(t, tile_start, gend, G, args.n_tiles, args.m_major, args.tail_max);
+      // Claims (leader, run time): main tiles while any are left, then
+      // small-group tiles.  The queue runs one tile ahead of this thread (the
+      // peer's producers find the next tile published when they reach it),
+      // and each claim is made one tile before it is published (the counter's
+      // round trip overlaps a tile's copies), after the publication before
+      // it (a release, which would otherwise wait for the round trip).
+      bool main_left = true, pend_main = true;
+      int pend = 0, cur = -1;
+      auto resolve = [&]() -> int {  // the pending claim as a tile number, -1 when none is left
+        if (pend_main && pend >= total) {
+          main_left = false;
+          pend_main = false;
+          pend = atomicAdd(args.sched + 1, 1);
+        }
+        return pend_main ? pend : (pend < total_small ? total + pend : -1);
+      };
+      auto publish = [&](int i, int t) -> int {  // queue slot of the cluster's i-th tile, in both CTAs
+        const int j = i % kPairQD;
+        if (t >= 0 && !mbar_wait<true>(qempty_bar(j), ((uint32_t)(i / kPairQD) & 1u) ^ 1u, abort_flag,
+                                       args.status, args.wait_ns))
+          t = -1;
+        tq[j] = t;
+        asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(mapa_shared(smem_u32((const void *)(tq + j)), 1)),
+                     "r"(t)
+                     : "memory");
+        mbar_arrive_cluster(mapa_shared(qfull_bar(j), 0));
+        mbar_arrive_cluster(mapa_shared(qfull_bar(j), 1));
+        if (t >= 0) {  // the claim for the tile after it
+          pend_main = main_left;
+          pend = atomicAdd(args.sched + (main_left ? 0 : 1), 1);
+        }
+        return t;
+      };
+      if (dyn && rank == 0) {
+        pend = atomicAdd(args.sched + 0, 1);
+        cur = publish(0, resolve());
+      }
+      for (int i = 0;; ++i) {
+        int t;
+        if (dyn && rank == 0) {
+          t = cur;
+          if (t < 0) break;
+          cur = publish(i + 1, ok ? resolve() : -1);  // -1 ends every role's loop
+        } else {
+          if (!ok) break;
+          t = seq_tile(i);
+        }
+        if (t < 0) break;
+        const PairTile c = tile_of(t);
         // L2: a group that is only this tail reads its weights once (stream them
         // through); everything else is read again by neighbouring tiles (keep it)
         const uint64_t pol = (c.tail && c.mp == 0) ? pol_first : pol_last;
@@ -448,10 +576,12 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : (Q ? kThreadsQ : kThre
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
       // ----------------------------------------------------- MMA issuer (leader) --
-      int it = 0, tc = 0;
+      int it = 0;
       bool ok = true;
-      for (int t = cluster; t < total && ok; t += nclusters, ++tc) {
-        const PairTile c = decode_pair_tile(t, tile_start, gend, G, args.n_tiles, args.m_major, args.tail_max);
+      for (int tc = 0; ok; ++tc) {
+        const int t = seq_tile(tc);
+        if (t < 0) break;
+        const PairTile c = tile_of(t);
         const uint32_t n_mma = c.tail ? (uint32_t)tail_n(c.tail) : (uint32_t)BN;
         const uint32_t idesc = Q ? idesc_e4m3_f32(2 * BM, n_mma) : idesc_bf16_f32(2 * BM, n_mma);
         const int acc = tc & 1;
@@ -491,13 +621,16 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : (Q ? kThreadsQ : kThre
     const int r_in_tile = quarter * 32 + lane;  // TMEM lane: token row (main) or weight row (tail)
     const uint32_t leader_tempty0 = mapa_shared(tempty_bar(0), 0);
     const uint32_t leader_tempty1 = mapa_shared(tempty_bar(1), 0);
-    int tc = 0;
-    for (int t = cluster; t < total; t += nclusters, ++tc) {
-      const PairTile c = decode_pair_tile(t, tile_start, gend, G, args.n_tiles, args.m_major, args.tail_max);
+    for (int tc = 0;; ++tc) {
+      int t = -1;
+      if (lane == 0) t = seq_tile(tc);
+      t = __shfl_sync(0xffffffffu, t, 0);
+      if (epi_bar_any(t < 0)) break;  // all four warps stop together
+      const PairTile c = tile_of(t);
       const int acc = tc & 1;
       const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
       const bool got = mbar_wait(tfull_bar(acc), aph, abort_flag, args.status, args.wait_ns);
-      if (epi_bar_any(!got)) break;  // all four warps stop together
+      if (epi_bar_any(!got)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
       if (!c.tail) {
@@ -679,13 +812,16 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : (Q ? kThreadsQ : kThre
     const int r_in_tile = quarter * 32 + lane;
     const uint32_t leader_tempty0 = mapa_shared(tempty_bar(0), 0);
     const uint32_t leader_tempty1 = mapa_shared(tempty_bar(1), 0);
-    int tc = 0;
-    for (int t = cluster; t < total; t += nclusters, ++tc) {
-      const PairTile c = decode_pair_tile(t, tile_start, gend, G, args.n_tiles, args.m_major, args.tail_max);
+    for (int tc = 0;; ++tc) {
+      int t = -1;
+      if (lane == 0) t = seq_tile(tc);
+      t = __shfl_sync(0xffffffffu, t, 0);
+      if (epi1_bar_any(t < 0)) break;  // all four warps of the group stop together
+      const PairTile c = tile_of(t);
       const int acc = tc & 1;
       const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
       const bool got = mbar_wait(tfull_bar(acc), aph, abort_flag, args.status, args.wait_ns);
-      if (epi1_bar_any(!got)) break;  // all four warps of the group stop together
+      if (epi1_bar_any(!got)) break;
       tc_fence_after();
       if (kSwiGLU && !c.tail) {
         const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
@@ -763,6 +899,11 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : (Q ? kThreadsQ : kThre
   }
 
   if (EPI == (int)Epi::kF32 && threadIdx.x == 64) bulk_wait_all();  // TMA stores complete
+  // Beside the small-group kernel: this grid ends only after that kernel's
+  // CTAs have written their rows, so whatever waits for this grid (the next
+  // kernel's dependent-launch wait) also sees those rows.
+  if (dyn && blockIdx.x == 0 && threadIdx.x == 0)
+    counter_wait(args.sched + 3, args.side_ctas, abort_flag, args.status, args.wait_ns);
   __syncthreads();
   cluster_sync();  // the peer no longer reads this CTA's shared memory or TMEM
   if (warp == 1) {
@@ -843,7 +984,7 @@ int encode_f32_store(CUtensorMap *map, void *ptr, long rows, int cols) {
 
 size_t pair_gemm_smem(Epi epi, int G) {
   const int tab = epi == Epi::kF32 ? PairLayout<(int)Epi::kF32>::TAB_OFF : PairLayout<(int)Epi::kBf16>::TAB_OFF;
-  return 1024 + tab + (size_t)(2 * G + 2) * 4;
+  return 1024 + tab + (size_t)(3 * G + 1) * 4;
 }
 
 bool pair_gemm_supported(Epi epi, int n_out) {
@@ -868,18 +1009,17 @@ int pair_gemm_encode_u8(GemmPlan &p, const uint8_t *A, long a_rows, const uint8_
 }
 
 cudaError_t pair_gemm_configure(Epi epi, size_t smem, int q) {
-  constexpr auto kAttr = cudaFuncAttributeMaxDynamicSharedMemorySize;
   if (q) {
-    if (epi == Epi::kSwiGLU) return cudaFuncSetAttribute(pair_gemm_kernel<(int)Epi::kSwiGLU, false, 1>, kAttr, (int)smem);
-    return cudaFuncSetAttribute(pair_gemm_kernel<(int)Epi::kF32, false, 1>, kAttr, (int)smem);
+    if (epi == Epi::kSwiGLU) return raise_smem_limit(pair_gemm_kernel<(int)Epi::kSwiGLU, false, 1>, smem);
+    return raise_smem_limit(pair_gemm_kernel<(int)Epi::kF32, false, 1>, smem);
   }
   if (epi == Epi::kSwiGLU) {
-    const cudaError_t e = cudaFuncSetAttribute(pair_gemm_kernel<(int)Epi::kSwiGLU, false, 0>, kAttr, (int)smem);
+    const cudaError_t e = raise_smem_limit(pair_gemm_kernel<(int)Epi::kSwiGLU, false, 0>, smem);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(pair_gemm_kernel<(int)Epi::kSwiGLU, true, 0>, kAttr, (int)smem);
+    return raise_smem_limit(pair_gemm_kernel<(int)Epi::kSwiGLU, true, 0>, smem);
   }
-  if (epi == Epi::kF32) return cudaFuncSetAttribute(pair_gemm_kernel<(int)Epi::kF32, false, 0>, kAttr, (int)smem);
-  return cudaFuncSetAttribute(pair_gemm_kernel<(int)Epi::kBf16, false, 0>, kAttr, (int)smem);
+  if (epi == Epi::kF32) return raise_smem_limit(pair_gemm_kernel<(int)Epi::kF32, false, 0>, smem);
+  return raise_smem_limit(pair_gemm_kernel<(int)Epi::kBf16, false, 0>, smem);
 }
 
 cudaError_t launch_pair_gemm(const GemmPlan &p, const Launch &l) {
@@ -909,6 +1049,9 @@ cudaError_t launch_pair_gemm(const GemmPlan &p, const Launch &l) {
   a.n_tiles = p.n_tiles;
   a.m_major = p.m_major;
   a.tail_max = p.tail_max;
+  a.sched = p.sched;
+  a.small_max = p.small_max;
+  a.side_ctas = p.side_ctas;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.grid);
   const bool gath = p.gather_k > 0 && p.epi == Epi::kSwiGLU;

@@ -557,9 +557,9 @@ int bwd_prepare(BwdPlan &p, bool wgrad, bool out_f32, const uint16_t *G, const u
   p.grid = (int)(tiles < sms ? (tiles > 0 ? tiles : 1) : sms);
   cudaError_t e = cudaSuccess;
   switch (p.mode) {
-    case kDgrad: e = cudaFuncSetAttribute(grouped_bwd_kernel<kDgrad>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem); break;
-    case kWgradF32: e = cudaFuncSetAttribute(grouped_bwd_kernel<kWgradF32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem); break;
-    default: e = cudaFuncSetAttribute(grouped_bwd_kernel<kWgradBf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem); break;
+    case kDgrad: e = raise_smem_limit(grouped_bwd_kernel<kDgrad>, p.smem); break;
+    case kWgradF32: e = raise_smem_limit(grouped_bwd_kernel<kWgradF32>, p.smem); break;
+    default: e = raise_smem_limit(grouped_bwd_kernel<kWgradBf16>, p.smem); break;
   }
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -94,6 +94,13 @@ struct GemmPlan {
   // tiles (weights on the MMA's M side); 0 makes every remainder a main tile
   // whose rows past the group are computed and not stored
   int tail_max = 128;
+  // CTA-pair kernel beside the small-group kernel (gemm_small.cu): side_ctas
+  // CTAs of that kernel take the tiles of the groups of 1..small_max rows,
+  // both kernels claim tiles through the four counters at sched (device,
+  // zero before each launch).  side_ctas = 0: the pair kernel alone.
+  int32_t *sched = nullptr;
+  int side_ctas = 0;
+  int small_max = 0;
 };
 
 // Encodes the tensor maps and picks tile shapes; host only.  allow_pair lets
@@ -124,6 +131,17 @@ int pair_gemm_encode_u8(GemmPlan &p, const uint8_t *A, long a_rows, const uint8_
 bool pair_gemm_supported(Epi epi, int n_out);
 cudaError_t pair_gemm_configure(Epi epi, size_t smem, int q = 0);
 cudaError_t launch_pair_gemm(const GemmPlan &p, const Launch &l);
+
+// Small-group kernel (gemm_small.cu), launched by launch_gemm ahead of the
+// CTA-pair kernel when a plan has side_ctas > 0.
+size_t small_gemm_smem(int G);
+int small_gemm_max_rows();
+cudaError_t small_gemm_configure(Epi epi, int q, size_t smem);
+cudaError_t launch_small_gemm(const GemmPlan &p, const Launch &l);
+// Gives a CTA-pair plan (SwiGLU or fp32 epilogue) the small-group kernel:
+// `ctas` CTAs (even), claim counters at sched (4 ints, zeroed before every
+// launch).  MOE_ERR_SHAPE if the plan cannot take it.
+int gemm_attach_small(GemmPlan &p, int32_t *sched, int ctas);
 
 // Grouped GEMM backward (gemm_bwd.cu): dgrad dX = G . W[g] (W in place) and
 // wgrad dW[g] = G^T . X over each group's rows, one-CTA tcgen05 kernels with

@@ -24,4 +24,17 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Raises a kernel's dynamic shared-memory limit to at least `bytes`.  The
+// limit belongs to the kernel, not to a plan: plans prepared one after another
+// with different group counts must not lower it under one another's launches.
+template <typename... KArgs>
+cudaError_t raise_smem_limit(void (*kernel)(KArgs...), size_t bytes) {
+  cudaFuncAttributes a;
+  cudaError_t e = cudaFuncGetAttributes(&a, reinterpret_cast<const void *>(kernel));
+  if (e != cudaSuccess) return e;
+  if ((size_t)a.maxDynamicSharedSizeBytes >= bytes) return cudaSuccess;
+  return cudaFuncSetAttribute(reinterpret_cast<const void *>(kernel), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)bytes);
+}
+
 }  // namespace moe

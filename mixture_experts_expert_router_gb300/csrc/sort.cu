@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <typename K>
 cudaError_t allow_smem(K kernel, size_t bytes) {
   if (bytes <= 48 * 1024) return cudaSuccess;
-  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  return raise_smem_limit(kernel, bytes);
 }
 
 }  // namespace

@@ -44,7 +44,7 @@ def test_status_strings(lib):
         s = moe.moe_status_string(code)
         assert s and s != "unknown status code"
     assert moe.moe_status_string(-99) == "unknown status code"
-    assert lib.moe_abi_version() == 103
+    assert lib.moe_abi_version() == 104
 
 
 def test_argument_errors_before_device(lib):
