@@ -266,9 +266,10 @@ def timed_steps(fn, steps, stream):
 
 
 def recorded_traffic(workload: str, kernel: str):
-    """DRAM bytes per launch (read + write) recorded from an ncu capture in
-    profiles/traffic.json, or None when none exists or the kernel's source
-    file changed since the capture (its sha256 prefix is stored beside it)."""
+    """DRAM bytes per stage launch (read + write, summed over the stage's
+    kernels) recorded from an ncu capture in profiles/traffic.json, or None
+    when none exists or a kernel source file changed since the capture (their
+    sha256 prefixes are stored beside it)."""
     import hashlib
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
@@ -276,9 +277,11 @@ def recorded_traffic(workload: str, kernel: str):
         for entry in rec.get("captures", []):
             if entry.get("workload") != workload or entry.get("kernel") != kernel:
                 continue
-            src = os.path.join(ROOT, entry["source"])
-            sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-            return int(entry["bytes"]) if entry.get("source_sha16") == sha else None
+            for src, want in zip(entry["sources"], entry["sources_sha16"]):
+                sha = hashlib.sha256(open(os.path.join(ROOT, src), "rb").read()).hexdigest()[:16]
+                if sha != want:
+                    return None
+            return int(entry["bytes"])
     except (OSError, ValueError, KeyError):
         pass
     return None
@@ -523,7 +526,10 @@ def run_ours(args, world, rank, local):
     esz = 1.0 if fw is not None else 2.0
     B_fc1 = active * 2.0 * wl.I * wl.H * esz + M * wl.H * esz + M * wl.I * esz
     decode_path = plan.buffers()["path"] == moe.PATH_DECODE
-    traffic = None if decode_path else recorded_traffic(wl.name, "fc1_swiglu")
+    # the captures are of the default bf16 plan's kernels; other kernel choices have none recorded
+    default_kernels = not (args.e4m3 or args.one_cta_gemm or args.no_tail_tiles or args.fused_gather
+                           or args.small_group_kernel != "auto")
+    traffic = recorded_traffic(wl.name, "fc1_swiglu") if (default_kernels and not decode_path) else None
     # the decode chain in one launch: one kernel (plus the router with logits)
     one_kernel = decode_path and kernels == (1 if logits is None else 2)
 
