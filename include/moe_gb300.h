@@ -358,9 +358,13 @@ MOE_API int moe_forward(const moe_bf16 *x, const float *logits, const int32_t *t
  * launch first clears the status word (if given) on the launch stream, before
  * any kernel of the launch can report into it: with cudaMemsetAsync, or, for
  * the decode chain in one launch, with a one-CTA kernel that also zeroes the
- * counters the chain keeps in the workspace, so plans may share a workspace.  The workspace is every launch's scratch: launches of one plan
- * (or of plans sharing a workspace) must run one after another (one stream,
- * or streams ordered by events).
+ * counters the chain keeps in the workspace.  A grouped-path launch that runs
+ * the small-group kernel beside the CTA-pair GEMMs (MOE_PLAN_SMALL_GROUP_KERNEL
+ * below) likewise zeroes the GEMMs' tile-claim counters in the workspace with
+ * one more cudaMemsetAsync first, so plans may share a workspace.  The
+ * workspace is every launch's scratch: launches of one plan (or of plans
+ * sharing a workspace) must run one after another (one stream, or streams
+ * ordered by events).
  */
 #define MOE_PATH_AUTO 0    /* decided from the shape                         */
 #define MOE_PATH_GROUPED 1 /* route/sort/gather + tcgen05 grouped GEMMs       */
@@ -398,11 +402,13 @@ MOE_API int moe_forward(const moe_bf16 *x, const float *logits, const int32_t *t
                                              Without this flag, when the plan's
                                              routes average at most 512 per local
                                              expert, each GEMM runs as two kernels
-                                             at once: a one-CTA kernel on a few
-                                             SMs takes the groups of at most 64
-                                             rows (weights on the MMA's N side),
-                                             the pair kernel the others; both
-                                             claim tiles at run time. */
+                                             at once: a one-CTA kernel on 24 SMs
+                                             streams the groups of at most 64
+                                             rows (weights on the MMA's M side,
+                                             the group's rows on N), the pair
+                                             kernel takes the others; both claim
+                                             tiles at run time.  The outputs are
+                                             bitwise the same either way. */
 #define MOE_PLAN_SMALL_GROUP_KERNEL 512 /* grouped path, CTA-pair GEMMs: the two
                                           kernels whatever the average group */
 #define MOE_PLAN_TEST_UNREACHABLE_WAIT 64 /* test hook, not for production: the
