@@ -589,16 +589,22 @@ def run_grouped_gemm(args, world, rank, local):
     F = 2.0 * d["sum_m"] * d["K"] * d["N"]
     B = active * d["N"] * d["K"] * 2.0 + d["sum_m"] * d["K"] * 2.0 + d["sum_m"] * d["N"] * 2.0
     stream = torch.cuda.current_stream(dev)
+    counters = torch.empty(moe.GROUPED_GEMM_COUNTERS, dtype=torch.int32, device=dev)
+    gopts = dict(no_tail_tiles=args.no_tail_tiles, counters=counters,
+                 small_group_kernel={"auto": None, "on": True, "off": False}[args.small_group_kernel])
+    # the CTA-pair kernel, and the small-group kernel beside it where the call runs it (on request)
+    with_small = bool(gopts["small_group_kernel"]) and not args.no_tail_tiles and d["N"] % 256 == 0
+    kernels_per_call = 2 if with_small else 1
     side = torch.cuda.Stream(dev)
     side.wait_stream(stream)
     with torch.cuda.stream(side):
         for _ in range(3):
-            moe.grouped_gemm_fwd(X, Wt, offs, Y, no_tail_tiles=args.no_tail_tiles)
+            moe.grouped_gemm_fwd(X, Wt, offs, Y, **gopts)
     stream.wait_stream(side)
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
-        moe.grouped_gemm_fwd(X, Wt, offs, Y, no_tail_tiles=args.no_tail_tiles)
+        moe.grouped_gemm_fwd(X, Wt, offs, Y, **gopts)
     clocks = ClockSampler(str(local))
     time.sleep(0.3)
     for _ in range(args.warmup):
@@ -621,13 +627,13 @@ def run_grouped_gemm(args, world, rank, local):
     Y_h = torch.empty(Y.shape, dtype=Y.dtype).pin_memory()
     for _ in range(args.warmup):
         X.copy_(X_h, non_blocking=True)
-        moe.grouped_gemm_fwd(X, Wt, offs, Y, no_tail_tiles=args.no_tail_tiles)
+        moe.grouped_gemm_fwd(X, Wt, offs, Y, **gopts)
         Y_h.copy_(Y, non_blocking=True)
     torch.cuda.synchronize()
     e0.record(stream)
     for _ in range(args.steps):
         X.copy_(X_h, non_blocking=True)
-        moe.grouped_gemm_fwd(X, Wt, offs, Y, no_tail_tiles=args.no_tail_tiles)
+        moe.grouped_gemm_fwd(X, Wt, offs, Y, **gopts)
         Y_h.copy_(Y, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -655,7 +661,7 @@ def run_grouped_gemm(args, world, rank, local):
                                          B / (float(peaks["hbm_gbs"]) * 1e9)) * 1000.0},
         "e2e": {"value": rows_all / (ms_e2e / 1000.0), "unit": "rows/s",
                 "h2d_bytes_per_step": X_h.numel() * 2, "d2h_bytes_per_step": Y_h.numel() * 2},
-        "gpu_launches": args.steps, "clocks": clocks.summary(t0, t1),
+        "gpu_launches": args.steps * kernels_per_call, "clocks": clocks.summary(t0, t1),
     }
     line["roofline_step"]["frac"] = line["roofline_step"]["time_ms"] / (ms / args.steps)
     print(json.dumps(line), flush=True)

@@ -262,6 +262,22 @@ MOE_API int grouped_gemm_fwd(const moe_bf16 *X, const moe_bf16 *W, const int32_t
 MOE_API int grouped_gemm_fwd_flags(const moe_bf16 *X, const moe_bf16 *W, const int32_t *offs,
                                    int sum_m, int E, int N, int K, moe_bf16 *Y, int flags,
                                    void *stream);
+/* The same with the small-group kernel beside the CTA-pair kernel: when
+ * counters is not NULL (and the shape takes the pair kernel, N % 256 == 0,
+ * with tail tiles), the groups of at most 64 rows are streamed by a one-CTA
+ * swap-AB kernel on 24 SMs while the pair kernel takes the others, both
+ * claiming tiles at run time through the counters (see
+ * MOE_PLAN_NO_SMALL_GROUP_KERNEL).  counters: device int32
+ * [MOE_GROUPED_GEMM_COUNTERS], 16-byte aligned, owned by the caller and
+ * cleared on the stream by every call; calls that overlap on the GPU need
+ * counters of their own.  Y is bitwise the same as without it.  NULL counters:
+ * grouped_gemm_fwd_flags.  It pays where the GEMM is tensor-bound (active
+ * groups averaging well over 280 rows) with some small groups; where weight
+ * streaming bounds the GEMM it only takes SMs from the pair kernel. */
+#define MOE_GROUPED_GEMM_COUNTERS 4
+MOE_API int grouped_gemm_fwd_ex(const moe_bf16 *X, const moe_bf16 *W, const int32_t *offs,
+                                int sum_m, int E, int N, int K, moe_bf16 *Y, int flags,
+                                int32_t *counters, void *stream);
 
 /* ---- ragged grouped GEMM backward ---------------------------------------------------------
  * The dgrad and wgrad rows of Cake ragged BF16 grouped GEMM, operation table

@@ -57,7 +57,7 @@ ABI_SYMBOLS = [
     "moe_plan_stage_reset", "moe_plan_kernels_per_launch", "moe_plan_destroy", "moe_sort_no_alloc",
     "moe_fc1_swiglu_swapab", "moe_fc2_swapab", "moe_fc1_swiglu_gathered", "moe_plan_set_wait_limit",
     "moe_fc1_swiglu_step", "grouped_gemm_dgrad", "grouped_gemm_wgrad", "moe_bgmv_workspace_size", "moe_bgmv",
-    "moe_fc1_swiglu_e4m3", "moe_fc2_e4m3", "grouped_gemm_fwd_flags",
+    "moe_fc1_swiglu_e4m3", "moe_fc2_e4m3", "grouped_gemm_fwd_flags", "grouped_gemm_fwd_ex",
 ]
 
 
@@ -123,6 +123,7 @@ def library():
             "moe_finalize": ([P, P, P, I, I, I, P, P], I),
             "grouped_gemm_fwd": ([P, P, P, I, I, I, I, P, P], I),
             "grouped_gemm_fwd_flags": ([P, P, P, I, I, I, I, P, I, P], I),
+            "grouped_gemm_fwd_ex": ([P, P, P, I, I, I, I, P, I, P, P], I),
             "grouped_gemm_dgrad": ([P, P, P, I, I, I, I, P, P], I),
             "moe_bgmv_workspace_size": ([I, I, I, I, I, I], Z),
             "moe_bgmv": ([P, I, I, P, P, I, P, I, I, I, P, P, P, P, I, I, P, P, I, P, Z, P, P], I),
@@ -392,8 +393,19 @@ def moe_finalize(y: torch.Tensor, exp_to_perm: torch.Tensor, topk_w: torch.Tenso
     return out
 
 
-def grouped_gemm_fwd(X: torch.Tensor, W: torch.Tensor, offs: torch.Tensor, Y=None, no_tail_tiles: bool = False):
-    """Ragged grouped GEMM forward: Y[group e] = X[group e] @ W[e].T (bf16)."""
+GROUPED_GEMM_COUNTERS = 4
+
+
+def grouped_gemm_fwd(X: torch.Tensor, W: torch.Tensor, offs: torch.Tensor, Y=None, no_tail_tiles: bool = False,
+                     small_group_kernel: bool | None = None, counters=None):
+    """Ragged grouped GEMM forward: Y[group e] = X[group e] @ W[e].T (bf16).
+
+    small_group_kernel=True runs the groups of at most 64 rows in the
+    small-group kernel beside the CTA-pair kernel (grouped_gemm_fwd_ex); it
+    pays where the GEMM is tensor-bound (active groups averaging well over
+    about 280 rows) with some small groups, and not where weight streaming
+    bounds it (off by default).  counters: the call's int32
+    [GROUPED_GEMM_COUNTERS] claim counters (allocated when None)."""
     _need(X, torch.bfloat16, "X")
     _need(W, torch.bfloat16, "W")
     _need(offs, torch.int32, "offs")
@@ -403,8 +415,16 @@ def grouped_gemm_fwd(X: torch.Tensor, W: torch.Tensor, offs: torch.Tensor, Y=Non
         raise ValueError("shapes: X [sum_m, K], W [E, N, K], offs [E]")
     Y = torch.empty((sum_m, N), dtype=torch.bfloat16, device=X.device) if Y is None else Y
     _need(Y, torch.bfloat16, "Y", (sum_m, N), X.device)
+    flags = PLAN_NO_TAIL_TILES if no_tail_tiles else 0
+    if small_group_kernel:
+        if counters is None:
+            counters = torch.empty(GROUPED_GEMM_COUNTERS, dtype=torch.int32, device=X.device)
+        _need(counters, torch.int32, "counters", (GROUPED_GEMM_COUNTERS,), X.device)
+        _check(library().grouped_gemm_fwd_ex(_ptr(X), _ptr(W), _ptr(offs), sum_m, E, N, K, _ptr(Y), flags,
+                                             _ptr(counters), _stream(X.device)), "grouped_gemm_fwd")
+        return Y
     _check(library().grouped_gemm_fwd_flags(_ptr(X), _ptr(W), _ptr(offs), sum_m, E, N, K, _ptr(Y),
-                                            PLAN_NO_TAIL_TILES if no_tail_tiles else 0, _stream(X.device)),
+                                            flags, _stream(X.device)),
            "grouped_gemm_fwd")
     return Y
 

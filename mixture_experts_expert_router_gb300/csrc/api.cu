@@ -390,13 +390,13 @@ int moe_finalize(const float *y, const int32_t *exp_to_perm, const float *topk_w
   return cuda_rc(launch_finalize(y, exp_to_perm, topk_w, T, top_k, H, out, l));
 }
 
-int grouped_gemm_fwd_flags(const moe_bf16 *X, const moe_bf16 *W, const int32_t *offs, int sum_m, int E,
-                           int N, int K, moe_bf16 *Y, int flags, void *stream) {
+int grouped_gemm_fwd_ex(const moe_bf16 *X, const moe_bf16 *W, const int32_t *offs, int sum_m, int E, int N,
+                        int K, moe_bf16 *Y, int flags, int32_t *counters, void *stream) {
   if (sum_m < 0 || E < 1 || E > MOE_MAX_EXPERTS || N <= 0 || K <= 0 || N % 64 || K % 64)
     return MOE_ERR_SHAPE;
   if (sum_m == 0) return MOE_OK;
   if (!X || !W || !offs || !Y) return MOE_ERR_NULL;
-  if (!aligned16(X) || !aligned16(W) || !aligned16(Y)) return MOE_ERR_ALIGN;
+  if (!aligned16(X) || !aligned16(W) || !aligned16(Y) || !aligned16(counters)) return MOE_ERR_ALIGN;
   if (int rc = check_device()) return rc;
   GemmPlan p;
   if (int rc = gemm_prepare(p, Epi::kBf16, X, sum_m, W, E, N, K, N, offs, sum_m, Y, nullptr))
@@ -404,7 +404,19 @@ int grouped_gemm_fwd_flags(const moe_bf16 *X, const moe_bf16 *W, const int32_t *
   if (flags & MOE_PLAN_NO_TAIL_TILES) p.tail_max = 0;
   Launch l;
   l.stream = static_cast<cudaStream_t>(stream);
+  // The small-group kernel beside the pair kernel, on the caller's counters.
+  if (counters && p.pair && p.tail_max >= small_gemm_max_rows()) {
+    const int ctas = device_sm_count() >= 4 * kSmallGroupCtas ? kSmallGroupCtas : 2;
+    if (int rc = gemm_attach_small(p, counters, ctas)) return rc;
+    if (cudaMemsetAsync(counters, 0, MOE_GROUPED_GEMM_COUNTERS * sizeof(int32_t), l.stream) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
   return cuda_rc(launch_gemm(p, l));
+}
+
+int grouped_gemm_fwd_flags(const moe_bf16 *X, const moe_bf16 *W, const int32_t *offs, int sum_m, int E,
+                           int N, int K, moe_bf16 *Y, int flags, void *stream) {
+  return grouped_gemm_fwd_ex(X, W, offs, sum_m, E, N, K, Y, flags, nullptr, stream);
 }
 
 int grouped_gemm_fwd(const moe_bf16 *X, const moe_bf16 *W, const int32_t *offs, int sum_m, int E, int N,

@@ -655,7 +655,7 @@ int gemm_prepare_gather(GemmPlan &p, const uint16_t *x, long x_rows, const int32
 }
 
 int gemm_attach_small(GemmPlan &p, int32_t *sched, int ctas) {
-  if (!p.pair || p.gather_k > 0 || p.epi == Epi::kBf16 || !sched || ctas < 2 || ctas % 2 ||
+  if (!p.pair || p.gather_k > 0 || (p.q && p.epi == Epi::kBf16) || !sched || ctas < 2 || ctas % 2 ||
       p.tail_max < small_gemm_max_rows())
     return MOE_ERR_SHAPE;
   p.sched = sched;

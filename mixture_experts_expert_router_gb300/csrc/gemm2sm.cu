@@ -86,18 +86,24 @@ constexpr int STG_BYTES = BM * 32 * 4;                 // fp32 store staging: 12
 // Shared-memory layout per epilogue kind (the fp32 form adds one store-staging
 // buffer).
 // Tiles claimed at run time (beside the small-group kernel) reach every role
-// of both CTAs through a queue of this many slots in each CTA.
+// of both CTAs through a queue of this many slots in each CTA.  A slot is 64
+// bits, the entry's sequence number (index + 1) above the tile number, so a
+// reader needs only the slot itself: it spins on its own CTA's copy, with no
+// acquire, and then counts itself done on the leader's empty barrier, with no
+// release (the leader refills a slot once all readers have counted).  Waits and
+// arrivals with cluster-scope acquire or release at every tile boundary cost
+// the kernel about 7 % at 17 us tiles.
 constexpr int kPairQD = 8;
 
 template <int EPI>
 struct PairLayout {
   static constexpr int STAGES = 3;
-  static constexpr int NBARS = 2 * STAGES + 5 + 2 * kPairQD;  // ring, accumulators, drain, queue
+  static constexpr int NBARS = 2 * STAGES + 5 + kPairQD;  // ring, accumulators, drain, queue slots free
   static constexpr int STG_OFF = STAGES * STAGE_BYTES;
   static constexpr int BAR_OFF = STG_OFF + (EPI == (int)Epi::kF32 ? STG_BYTES : 0);
   static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
-  static constexpr int TQ_OFF = MISC_OFF + 16;  // tile queue [kPairQD]
-  static constexpr int SG_OFF = TQ_OFF + kPairQD * 4;  // tail gate hand-off [16][64] fp32
+  static constexpr int TQ_OFF = MISC_OFF + 16;  // tile queue [kPairQD] x 64 bits
+  static constexpr int SG_OFF = TQ_OFF + kPairQD * 8;  // tail gate hand-off [16][64] fp32
   static constexpr int TAB_OFF = SG_OFF + 16 * 64 * 4;  // tile_start [G+1], gend [G], small groups [G]
 };
 constexpr uint32_t TMEM_COLS = 2 * BN;
@@ -162,6 +168,33 @@ __device__ __forceinline__ bool epi_bar_any(bool flag) {
       : "r"((uint32_t)flag)
       : "memory");
   return r != 0;
+}
+
+// Waits (bounded, like mbar_wait) until the 64-bit queue slot holds sequence
+// number seq and returns its tile number in *t; false on abort or timeout.
+__device__ __forceinline__ bool queue_wait(volatile unsigned long long *slot, uint32_t seq, volatile int *abort,
+                                           int32_t *status, unsigned long long limit_ns, int *t) {
+  unsigned long long v = *slot;
+  if ((uint32_t)(v >> 32) == seq) {
+    *t = (int)(uint32_t)v;
+    return true;
+  }
+  const unsigned long long t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    v = *slot;
+    if ((uint32_t)(v >> 32) == seq) {
+      *t = (int)(uint32_t)v;
+      return true;
+    }
+    if ((it & 63u) == 0u) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > limit_ns) {
+        *abort = 1;
+        if (status) atomicOr(reinterpret_cast<unsigned int *>(status), MOE_DEV_TIMEOUT);
+        return false;
+      }
+    }
+  }
 }
 
 // Tail tile N for r tail rows (1..128): the smallest of 16, 32, 64, 128.
@@ -308,7 +341,7 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : (Q ? kThreadsQ : kThre
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + MISC_OFF);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + MISC_OFF + 4);
   volatile int *n_small_s = reinterpret_cast<volatile int *>(smem + MISC_OFF + 8);
-  volatile int *tq = reinterpret_cast<volatile int *>(smem + Lay::TQ_OFF);
+  volatile unsigned long long *tq = reinterpret_cast<volatile unsigned long long *>(smem + Lay::TQ_OFF);
   float *sg = reinterpret_cast<float *>(smem + SG_OFF);
   int *tile_start = reinterpret_cast<int *>(smem + TAB_OFF);
   int *gend = tile_start + (args.G + 1);
@@ -316,8 +349,7 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : (Q ? kThreadsQ : kThre
   // Run-time tile claims (beside the small-group kernel): the leader's weight
   // producer claims each tile and publishes it to both CTAs' queues.
   const bool dyn = !GATH && args.sched != nullptr;
-  auto qfull_bar = [&](int j) { return bar_base + 8u * (2 * STAGES + 5 + j); };
-  auto qempty_bar = [&](int j) { return bar_base + 8u * (2 * STAGES + 5 + kPairQD + j); };
+  auto qempty_bar = [&](int j) { return bar_base + 8u * (2 * STAGES + 5 + j); };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -340,8 +372,8 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : (Q ? kThreadsQ : kThre
     // thread, the peer's weight producer
     const uint32_t readers = 2u * (1u + 4u + (Q ? 4u : 0u)) + 2u;
     for (int j = 0; j < kPairQD; ++j) {
-      mbar_init(qfull_bar(j), 1);
       mbar_init(qempty_bar(j), readers);
+      tq[j] = 0ull;  // sequence 0: nothing published
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -408,6 +440,10 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : (Q ? kThreadsQ : kThre
   const bool dead = *abort_flag != 0;  // the start flag never came: no tiles
   const int total = dead ? 0 : tile_start[G] * args.n_tiles;  // tiles numbered 0 .. total - 1 first
   const int total_small = dead ? 0 : *n_small_s * args.n_tiles;  // then small-group tiles
+  // Claims at run time only when there are small-group tiles to share: without
+  // them the small-group kernel leaves at once and this grid's late clusters
+  // start a few microseconds late, which costs less than the claims.
+  const bool claims = dyn && total_small > 0;
   const int num_kb = args.K / KE;
   const int n_rounds = (num_kb + KH - 1) / KH;  // ring stages per tile
   const int cluster = blockIdx.x >> 1;
@@ -431,15 +467,16 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : (Q ? kThreadsQ : kThre
   // Static: round-robin over the clusters.  Run time: the queue entry, whose
   // slot the reader then releases on the leader's qempty barrier.
   auto seq_tile = [&](int i) -> int {
-    if (!dyn) {
+    if (!claims) {
       const int t = cluster + i * nclusters;
       return t < total ? t : -1;
     }
     const int j = i % kPairQD;
-    if (!mbar_wait<true>(qfull_bar(j), (uint32_t)(i / kPairQD) & 1u, abort_flag, args.status, args.wait_ns))
-      return -1;
-    const int t = tq[j];
-    mbar_arrive_cluster(mapa_shared(qempty_bar(j), 0));
+    int t;
+    if (!queue_wait(tq + j, (uint32_t)(i + 1), abort_flag, args.status, args.wait_ns, &t)) return -1;
+    // t came from the slot (the wait ended on it), so the arrival cannot pass the read
+    if (rank == 0) mbar_arrive_relaxed(qempty_bar(j));
+    else mbar_arrive_relaxed_cluster(mapa_shared(qempty_bar(j), 0));
     return t;
   };
 
@@ -514,28 +551,27 @@ __global__ void __launch_bounds__(GATH ? kThreadsGather : (Q ? kThreadsQ : kThre
       };
       auto publish = [&](int i, int t) -> int {  // queue slot of the cluster's i-th tile, in both CTAs
         const int j = i % kPairQD;
-        if (t >= 0 && !mbar_wait<true>(qempty_bar(j), ((uint32_t)(i / kPairQD) & 1u) ^ 1u, abort_flag,
-                                       args.status, args.wait_ns))
+        if (t >= 0 && !mbar_wait<false, true>(qempty_bar(j), ((uint32_t)(i / kPairQD) & 1u) ^ 1u, abort_flag,
+                                              args.status, args.wait_ns))
           t = -1;
-        tq[j] = t;
-        asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(mapa_shared(smem_u32((const void *)(tq + j)), 1)),
-                     "r"(t)
+        const unsigned long long v = ((unsigned long long)(uint32_t)(i + 1) << 32) | (uint32_t)t;
+        tq[j] = v;
+        asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(mapa_shared(smem_u32((const void *)(tq + j)), 1)),
+                     "l"(v)
                      : "memory");
-        mbar_arrive_cluster(mapa_shared(qfull_bar(j), 0));
-        mbar_arrive_cluster(mapa_shared(qfull_bar(j), 1));
         if (t >= 0) {  // the claim for the tile after it
           pend_main = main_left;
           pend = atomicAdd(args.sched + (main_left ? 0 : 1), 1);
         }
         return t;
       };
-      if (dyn && rank == 0) {
+      if (claims && rank == 0) {
         pend = atomicAdd(args.sched + 0, 1);
         cur = publish(0, resolve());
       }
       for (int i = 0;; ++i) {
         int t;
-        if (dyn && rank == 0) {
+        if (claims && rank == 0) {
           t = cur;
           if (t < 0) break;
           cur = publish(i + 1, ok ? resolve() : -1);  // -1 ends every role's loop

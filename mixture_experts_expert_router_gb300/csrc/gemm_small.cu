@@ -1,4 +1,4 @@
-// S4 / S5 for the groups of at most 64 rows, beside the CTA-pair grouped GEMM.
+// S4 / S5 / S8 for the groups of at most 64 rows, beside the CTA-pair grouped GEMM.
 //
 // A group of r <= 64 rows reads its whole weight block once for very little
 // MMA work, so its speed is how fast an SM can stream weights.  Inside the
@@ -13,8 +13,9 @@
 // whatever the mix of group sizes.
 //
 // The MMAs are swap-AB, one CTA: the tile's 256 weight rows are two M = 128
-// operands (FC1: the 128 up rows and the matching 128 gate rows; FC2: two
-// halves of 128 output columns), the group's r token rows the N side
+// operands (FC1: the 128 up rows and the matching 128 gate rows; FC2 and the
+// grouped GEMM forward: two halves of 128 output columns), the group's r
+// token rows the N side
 // (N = 16, 32 or 64).  Each half has its own accumulator and its own issuing
 // thread: a thread issues a small-N MMA on a new weight tile only about every
 // 83 ns, so two threads stream about twice as many bytes.  With the weights
@@ -373,7 +374,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) small_group_gemm_kernel(cons
                   h[(row + j) * args.n_out + col] =
                       __float2bfloat16_rn(swiglu_step(__uint_as_float(b[j]), __uint_as_float(a[j]), lim));
             }
-          } else {  // y[token][n * 256 + wr] and [.. + 128 + wr]
+          } else if (EPI == (int)Epi::kF32) {  // y[token][n * 256 + wr] and [.. + 128 + wr]
             float *y = reinterpret_cast<float *>(args.out);
             const long col = (long)c.n * 2 * SM_BM + wr;
 #pragma unroll
@@ -382,6 +383,16 @@ __global__ void __launch_bounds__(kSmallThreads, 1) small_group_gemm_kernel(cons
                 float *yr = y + (row + j) * args.n_out + col;
                 yr[0] = Q ? __fmul_rn(__uint_as_float(a[j]), sc) : __uint_as_float(a[j]);
                 yr[SM_BM] = Q ? __fmul_rn(__uint_as_float(b[j]), sc) : __uint_as_float(b[j]);
+              }
+          } else {  // the grouped GEMM forward: Y rounded to bf16
+            __nv_bfloat16 *y = reinterpret_cast<__nv_bfloat16 *>(args.out);
+            const long col = (long)c.n * 2 * SM_BM + wr;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (c0 + j < c.r) {
+                __nv_bfloat16 *yr = y + (row + j) * args.n_out + col;
+                yr[0] = __float2bfloat16_rn(__uint_as_float(a[j]));
+                yr[SM_BM] = __float2bfloat16_rn(__uint_as_float(b[j]));
               }
           }
         }
@@ -417,7 +428,8 @@ cudaError_t small_gemm_configure(Epi epi, int q, size_t smem) {
     return raise_smem_limit(small_group_gemm_kernel<(int)Epi::kF32, 1>, smem);
   }
   if (epi == Epi::kSwiGLU) return raise_smem_limit(small_group_gemm_kernel<(int)Epi::kSwiGLU, 0>, smem);
-  return raise_smem_limit(small_group_gemm_kernel<(int)Epi::kF32, 0>, smem);
+  if (epi == Epi::kF32) return raise_smem_limit(small_group_gemm_kernel<(int)Epi::kF32, 0>, smem);
+  return raise_smem_limit(small_group_gemm_kernel<(int)Epi::kBf16, 0>, smem);
 }
 
 cudaError_t launch_small_gemm(const GemmPlan &p, const Launch &l) {
@@ -459,7 +471,8 @@ cudaError_t launch_small_gemm(const GemmPlan &p, const Launch &l) {
     return cudaLaunchKernelEx(&cfg, small_group_gemm_kernel<(int)Epi::kF32, 1>, a);
   }
   if (p.epi == Epi::kSwiGLU) return cudaLaunchKernelEx(&cfg, small_group_gemm_kernel<(int)Epi::kSwiGLU, 0>, a);
-  return cudaLaunchKernelEx(&cfg, small_group_gemm_kernel<(int)Epi::kF32, 0>, a);
+  if (p.epi == Epi::kF32) return cudaLaunchKernelEx(&cfg, small_group_gemm_kernel<(int)Epi::kF32, 0>, a);
+  return cudaLaunchKernelEx(&cfg, small_group_gemm_kernel<(int)Epi::kBf16, 0>, a);
 }
 
 }  // namespace moe

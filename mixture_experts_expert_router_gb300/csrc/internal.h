@@ -138,7 +138,7 @@ size_t small_gemm_smem(int G);
 int small_gemm_max_rows();
 cudaError_t small_gemm_configure(Epi epi, int q, size_t smem);
 cudaError_t launch_small_gemm(const GemmPlan &p, const Launch &l);
-// Gives a CTA-pair plan (SwiGLU or fp32 epilogue) the small-group kernel:
+// Gives a CTA-pair plan (any bf16 epilogue; SwiGLU or fp32 with E4M3) the small-group kernel:
 // `ctas` CTAs (even), claim counters at sched (4 ints, zeroed before every
 // launch).  MOE_ERR_SHAPE if the plan cannot take it.
 int gemm_attach_small(GemmPlan &p, int32_t *sched, int ctas);

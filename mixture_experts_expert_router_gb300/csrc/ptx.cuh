@@ -58,10 +58,18 @@ __device__ __forceinline__ void mbar_arrive_expect_tx_relaxed(uint32_t bar, uint
                : "memory");
 }
 
-template <bool kCluster = false>
+template <bool kCluster = false, bool kRelaxed = false>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
-  if (kCluster)  // acquire at cluster scope: the phase was completed by the peer CTA's threads
+  if (kRelaxed)  // no acquire: the waiter reads nothing the arrivals published
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.relaxed.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  else if (kCluster)  // acquire at cluster scope: the phase was completed by the peer CTA's threads
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
@@ -87,13 +95,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // `abort` may be null (the final drains, which must run to the end or the
 // time limit whatever the other roles did).  kCluster: acquire at cluster
 // scope, for phases completed by arrivals of the peer CTA's threads.
-template <bool kCluster = false>
+template <bool kCluster = false, bool kRelaxed = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
                                           int32_t *status, unsigned long long limit_ns) {
-  if (mbar_try_wait<kCluster>(bar, parity)) return true;
+  if (mbar_try_wait<kCluster, kRelaxed>(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait<kCluster>(bar, parity)) return true;
+    if (mbar_try_wait<kCluster, kRelaxed>(bar, parity)) return true;
     if ((it & 63u) == 0u) {
       if (abort != nullptr && *abort) return false;
       if (global_timer_ns() - t0 > limit_ns) {
@@ -309,6 +317,16 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
+}
+
+// Arrivals without release semantics (for a barrier that only counts that
+// something was done, publishing no data).  Release at cluster scope cost the
+// CTA-pair kernel several percent at every tile boundary.
+__device__ __forceinline__ void mbar_arrive_relaxed(uint32_t bar) {
+  asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_relaxed_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // 2-D tiled TMA load into this CTA's shared memory whose completion is

@@ -230,3 +230,49 @@ def test_e4m3_family_with_small_groups():
     from tests.tolerances import RMS_FRAC_E4M3
     check_bf16_end_to_end(W.bf16_bits(outs[True]), with_floor(want, frac, n), "E4M3 with small groups",
                           rms_frac=RMS_FRAC_E4M3)
+
+
+@pytest.mark.parametrize("sizes,N,K", [
+    ([1, 16, 17, 64, 65, 128, 300, 0, 33], 256, 320),
+    ([0, 0, 0, 7], 1536, 512),
+    (np.random.default_rng(7).integers(0, 90, 200).tolist(), 512, 192)])
+def test_grouped_gemm_fwd_with_small_groups(sizes, N, K):
+    """The ragged grouped GEMM forward with the small-group kernel (caller's
+    counters): bitwise the same as the pair kernel alone, and the oracle's Y;
+    rows past the last group untouched."""
+    d = W.make_grouped_gemm(seed=len(sizes) + 900, sizes=sizes, N=N, K=K)
+    X, Wt, offs = d["X"].to(DEV), d["W"].to(DEV), d["offs"].to(DEV)
+    counters = torch.full((moe.GROUPED_GEMM_COUNTERS,), 12345, dtype=torch.int32, device=DEV)
+    sentinel = torch.full((d["sum_m"] + 3, N), -7.0, dtype=torch.bfloat16, device=DEV)
+    Y = sentinel[:d["sum_m"]]
+    moe.grouped_gemm_fwd(X, Wt, offs, Y, small_group_kernel=True, counters=counters)
+    Y_off = moe.grouped_gemm_fwd(X, Wt, offs, small_group_kernel=False)
+    moe.grouped_gemm_fwd(X, Wt, offs, Y, small_group_kernel=True, counters=counters)  # counters reused
+    torch.cuda.synchronize()
+    assert torch.equal(Y, Y_off)
+    assert torch.all(sentinel[d["sum_m"]:] == -7.0)
+    Yo = oracle.grouped_gemm_rows(W.bf16_bits(d["X"]), W.bf16_bits(d["W"]), d["offs"].numpy())
+    check_bf16_close(W.bf16_bits(Y), Yo, "Y with the small-group kernel")
+
+
+def test_grouped_gemm_fwd_full_size_with_small_groups():
+    """The grouped-GEMM workload (sum_m = 16384, E = 64, K = 4096, N = 1536;
+    22 groups of at most 64 rows): bitwise the same with and without the
+    small-group kernel, and sampled rows of every group against the oracle."""
+    d = W.make_grouped_gemm(seed=0, device="cpu", weights_device=DEV)
+    X, Wt, offs = d["X"].to(DEV), d["W"], d["offs"].to(DEV)
+    sizes = d["sizes"]
+    assert ((sizes > 0) & (sizes <= 64)).sum() > 10
+    Y_on = moe.grouped_gemm_fwd(X, Wt, offs, small_group_kernel=True)
+    Y_off = moe.grouped_gemm_fwd(X, Wt, offs, small_group_kernel=False)
+    torch.cuda.synchronize()
+    assert torch.equal(Y_on, Y_off)
+    ends = d["offs"].numpy()
+    rows = set()
+    for e in range(len(ends)):
+        s0 = 0 if e == 0 else int(ends[e - 1])
+        if ends[e] > s0:
+            rows.update([s0, int(ends[e]) - 1, (s0 + int(ends[e])) // 2])
+    rows = np.array(sorted(rows), dtype=np.int32)
+    Yo = oracle.grouped_gemm_rows(W.bf16_bits(d["X"]), W.bf16_bits(Wt.cpu()), ends, rows)
+    check_bf16_close(W.bf16_bits(Y_on)[rows], Yo, "grouped GEMM workload with the small-group kernel")
