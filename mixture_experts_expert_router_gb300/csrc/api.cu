@@ -721,11 +721,10 @@ int moe_plan_launch(moe_plan *p, void *stream) {
   l.pdl = !p->timing;
   if (chain_clear) {
     // The chain's counters live in the workspace, which other plans may
-    // share: every launch zeroes them first.  The clearing kernel follows the
-    // stream's earlier work in plain order; what comes next may start early.
-    Launch first = l;
-    first.pdl = false;
-    if (launch_chain_clear(p->chain, p->unreachable_wait, first) != cudaSuccess) return MOE_ERR_CUDA;
+    // share: every launch zeroes them first.  The clearing kernel may start
+    // under the stream's previous kernel (a previous launch's chain) and waits
+    // for it before it clears; the chain behind it may start early too.
+    if (launch_chain_clear(p->chain, p->unreachable_wait, l) != cudaSuccess) return MOE_ERR_CUDA;
   }
   cudaEvent_t *ev = p->timing ? p->ev[p->n_recorded % kTimingRing] : nullptr;
   auto mark = [&](int stage) -> bool {

@@ -775,7 +775,11 @@ namespace {
 // griddepcontrol.wait.  unreachable: done1 is filled with -1 instead.
 __global__ void __launch_bounds__(256) chain_clear_kernel(int32_t *lo, int n, const int32_t *done1, int32_t *status,
                                                           int unreachable) {
+  // The chain behind this kernel may launch at once (its prologue then runs
+  // while the previous launch's chain ends); this kernel clears only once the
+  // kernel before it in the stream has finished with the counters.
   pdl_launch_dependents();
+  pdl_wait();
   for (int i = threadIdx.x; i < n; i += blockDim.x) lo[i] = unreachable && lo + i >= done1 ? -1 : 0;
   if (threadIdx.x == 0 && status) *status = 0;
 }
