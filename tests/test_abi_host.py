@@ -56,6 +56,10 @@ def test_argument_errors_before_device(lib):
     assert lib.moe_sort(None, 4, 2, 8, 6, 4, None, None, None, None, 0, None, None) == -2  # shard past E
     assert lib.grouped_gemm_fwd(None, None, None, 16, 4, 100, 64, None, None) == -2      # N % 64
     assert lib.grouped_gemm_fwd(None, None, None, 0, 4, 128, 64, None, None) == 0        # empty
+    # the claim counters of the small-group kernel: 16-byte aligned, checked before the device
+    assert lib.grouped_gemm_fwd_ex(None, None, None, 16, 4, 100, 64, None, 0, None, None) == -2  # N % 64
+    assert lib.grouped_gemm_fwd_ex(None, None, None, 0, 4, 256, 64, None, 0, None, None) == 0   # empty
+    assert lib.grouped_gemm_fwd_ex(256, 256, 256, 16, 4, 256, 64, 256, 0, 8, None) == -3     # counters
     assert lib.moe_fc1_swiglu(None, None, None, 8, 96, 64, 2, None, None) == -2          # H % 64
     assert lib.moe_finalize(None, None, None, 4, 2, 12, None, None) == -2                # H % 8
 
@@ -107,6 +111,9 @@ def test_binding_constants_match_header():
              "MOE_PLAN_DECODE_ONE_LAUNCH": moe.PLAN_DECODE_ONE_LAUNCH,
              "MOE_PLAN_TEST_UNREACHABLE_WAIT": moe.PLAN_TEST_UNREACHABLE_WAIT,
              "MOE_PLAN_NO_TAIL_TILES": moe.PLAN_NO_TAIL_TILES,
+             "MOE_PLAN_NO_SMALL_GROUP_KERNEL": moe.PLAN_NO_SMALL_GROUP_KERNEL,
+             "MOE_PLAN_SMALL_GROUP_KERNEL": moe.PLAN_SMALL_GROUP_KERNEL,
+             "MOE_GROUPED_GEMM_COUNTERS": moe.GROUPED_GEMM_COUNTERS,
              "MOE_WEIGHTS_BF16": moe.WEIGHTS_BF16, "MOE_WEIGHTS_E4M3": moe.WEIGHTS_E4M3,
              "MOE_WAIT_LIMIT_MIN_NS": moe.WAIT_LIMIT_MIN_NS, "MOE_WAIT_LIMIT_MAX_NS": moe.WAIT_LIMIT_MAX_NS,
              "MOE_DEV_BAD_EXPERT": moe.DEV_BAD_EXPERT, "MOE_DEV_TIMEOUT": moe.DEV_TIMEOUT}
