@@ -49,11 +49,12 @@ def _oracle_out(wl, tokens=None, w1=None, w2=None, clamp_limit=None):
 
 
 def _forward(wl, d, path=moe.PATH_AUTO, status=None, one_cta_gemm=False, decode_chain=False,
-             fused_gather=False, one_launch=False, no_tail_tiles=False):
+             fused_gather=False, one_launch=False, no_tail_tiles=False, small_group_kernel=None):
     plan = moe.MoEPlan(d["x"], d["w1"], d["w2"], wl.E, wl.top_k, logits=d["logits"],
                        topk_ids=d["topk_ids"], topk_w=d["topk_w"], local_offset=wl.local_offset,
                        status=status, path=path, one_cta_gemm=one_cta_gemm, decode_chain=decode_chain,
-                       fused_gather=fused_gather, decode_one_launch=one_launch, no_tail_tiles=no_tail_tiles)
+                       fused_gather=fused_gather, decode_one_launch=one_launch, no_tail_tiles=no_tail_tiles,
+                       small_group_kernel=small_group_kernel)
     out = plan.launch()
     torch.cuda.synchronize()
     return out, plan
@@ -300,12 +301,16 @@ def _sample_tokens(ids, T, n, seed):
     return np.array(sorted(chosen), dtype=np.int32)
 
 
-@pytest.mark.parametrize("form", ["pair", "one_cta", "fused_gather"])
+@pytest.mark.parametrize("form", ["pair", "pair_alone", "one_cta", "fused_gather"])
 @pytest.mark.parametrize("name", ["prefill_few_large", "prefill_many_fine"])
 def test_prefill_configs_sampled(name, form):
+    """pair: the plan's default (at the many-fine-experts workload the
+    small-group kernel beside the CTA-pair GEMMs); pair_alone: the CTA-pair
+    GEMMs without it."""
     wl = W.make_moe(name, weights_device=DEV)
     d = _dev(wl)
-    out, _ = _forward(wl, d, one_cta_gemm=form == "one_cta", fused_gather=form == "fused_gather")
+    out, _ = _forward(wl, d, one_cta_gemm=form == "one_cta", fused_gather=form == "fused_gather",
+                      small_group_kernel=False if form == "pair_alone" else None)
     ids, _ = _oracle_route(wl)
     tokens = _sample_tokens(ids, wl.T, 1024, 0)
     want, _ = _oracle_out(wl, tokens=tokens, w1=W.bf16_bits(wl.w1), w2=W.bf16_bits(wl.w2))
