@@ -116,3 +116,27 @@ def test_bench_accounting_matches_published_targets():
     wl = Shape(1, 2048, 768, 128, 8, "prerouted")
     B, active = bench.layer_bytes(wl, np.array([3, 9, 17, 40, 41, 77, 100, 127], np.int32))
     assert active == 8 and abs(B / 1e6 - 75.5) < 0.05
+
+
+def test_recorded_traffic_follows_every_source(tmp_path, monkeypatch):
+    """profiles/traffic.json: a stage's bytes are attached only while every
+    kernel source it lists still has the recorded hash."""
+    import hashlib
+    import json
+
+    import bench
+    (tmp_path / "profiles").mkdir()
+    a, b = tmp_path / "a.cu", tmp_path / "b.cu"
+    a.write_text("kernel a")
+    b.write_text("kernel b")
+    sha = lambda p: hashlib.sha256(p.read_bytes()).hexdigest()[:16]
+    rec = {"captures": [{"workload": "w", "kernel": "fc1_swiglu", "bytes": 123, "sources": ["a.cu", "b.cu"],
+                         "sources_sha16": [sha(a), sha(b)]}]}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.recorded_traffic("w", "fc1_swiglu") == 123
+    assert bench.recorded_traffic("w", "fc2") is None
+    assert bench.recorded_traffic("other", "fc1_swiglu") is None
+    b.write_text("kernel b, changed")
+    assert bench.recorded_traffic("w", "fc1_swiglu") is None
+
