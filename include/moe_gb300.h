@@ -515,8 +515,9 @@ MOE_API const char *moe_plan_stage_name(const moe_plan *plan, int stage);
 MOE_API int moe_plan_stage_times(moe_plan *plan, float *ms, int max_stages,
                          int *n_launches);
 MOE_API int moe_plan_stage_reset(moe_plan *plan);
-/* Number of kernels one moe_plan_launch enqueues (depends on the path and
- * on the shape only). */
+/* Number of kernels one moe_plan_launch enqueues (depends on the path, the
+ * shape and the plan flags only; memsets are not counted).  On the grouped
+ * path with the small-group kernel, each GEMM counts two kernels. */
 MOE_API int moe_plan_kernels_per_launch(const moe_plan *plan);
 MOE_API int moe_plan_destroy(moe_plan *plan);
 
